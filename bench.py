@@ -1,0 +1,493 @@
+"""Benchmark of the DiLoCo outer merge on GB300.
+
+A step is one merge round over the workload (every round of the workload's
+round list, the in-flight ones committed together on separate streams) with
+its inputs resident in HBM. The default workload is the 1.08B-parameter
+DiffuRefill-1B tensor list: K = 5 fp32 worker checkpoints, plain mean in
+arrival order, plain replacement, EMA beta 0.9 (34.43 GB of algorithmic
+traffic per round, far larger than the 129 MB L2, so no flush is needed).
+
+Prints one JSON line: whole-job algorithmic HBM GB/s (value), ms per round,
+the roofline of the fused merge kernel against the measured HBM copy
+bandwidth, SM clocks sampled during the timed region, an end-to-end figure
+through the public API with inputs in pinned host memory, and the CPU oracle
+timed on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload diffurefill1b|diffurefill1b_bf16|stand|pythia14m|sweep:T,N,K]
+Under torchrun (N > 1) each rank merges its own replica on its own GPU; no data
+crosses GPUs (the merge has no exchange step on one box), and the reported
+value is every rank's bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params"
+KERNEL_SRC = os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", "merge_kernels.cu")
+PROFILES = os.path.join(ROOT, "profiles")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- byte model ----------------------------------------------------------------
+
+def round_bytes(wl, frag: int, k_incl: int) -> int:
+    """Algorithmic HBM bytes of one round: each included worker element read
+    once, theta read (token-weighted mode or norms) and written once, momentum
+    read+written (Nesterov), EMA read+written."""
+    b_in = 2 if wl.ckpt_dtype == "bf16" else 4
+    per = k_incl * b_in + 4
+    if wl.mode == "delta" or wl.norms:
+        per += 4
+    if wl.mode == "delta":
+        per += 8
+    if wl.ema_beta is not None:
+        per += 8
+    return per * wl.fragment_numel(frag)
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary of this workload's
+    merge kernel, or None if absent or taken on a different kernel source."""
+    path = os.path.join(PROFILES, f"merge_fused_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not sha or not val or sha.group(1) != kernel_sha():
+        return None
+    return int(val.group(1))
+
+
+# ---- clocks ----------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- distributed plumbing ------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int) -> None:
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(per_rank_bytes: int, steps: int, elapsed_s: float, ws: int, device=None) -> dict:
+    """Whole-job figure: every rank's bytes over the slowest rank's time."""
+    t = max_over_ranks(elapsed_s, ws, device)
+    return {"seconds": t, "gbs": per_rank_bytes * steps * ws / t / 1e9,
+            "ms_per_step": t / steps * 1e3}
+
+
+# ---- CPU oracle timing ---------------------------------------------------------------
+
+def oracle_sample_rate(wl, max_seconds: float, seed: int = 0, max_elems: int | None = None,
+                       pool_elems: int = 1 << 24):
+    """Times the CPU oracle over the workload's first round, tensor by tensor in
+    list order, until max_seconds of oracle time (or max_elems elements) are
+    spent. Inputs follow the same recipe but are drawn once into a pool of
+    pool_elems values per array and reused slice by slice (the oracle is
+    elementwise, so its time does not depend on which values it sees).
+    Returns (GB/s, seconds, elements, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from checkpoint_averaging_gb300 import workloads as W
+
+    rnd, frag = wl.rounds[0]
+    draw = W.draw_round(wl, 0, seed)
+    k_incl = len(draw.included)
+    tensors = [t for t, s in enumerate(wl.specs) if frag == -1 or s.fragment == frag]
+    gen = torch.Generator().manual_seed(W.subseed(seed, wl.name, "cpu-sample"))
+    P = pool_elems
+    theta = (torch.randn(P, generator=gen) * wl.global_std).numpy()
+    xs = []
+    for _ in range(k_incl):
+        x = torch.from_numpy(theta) + torch.randn(P, generator=gen) * wl.noise_std
+        if wl.ckpt_dtype == "bf16":
+            xs.append(x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+        else:
+            xs.append(x.numpy().astype(np.float32))
+    m = np.zeros(P, np.float32) if wl.mode == "delta" else None
+    e = theta.copy() if wl.ema_beta is not None else None
+    mode = oracle.DELTA_NESTEROV if wl.mode == "delta" else oracle.MEAN_REPLACE
+    tokens = [draw.tokens[k] for k in draw.included] if wl.mode == "delta" else None
+    beta = wl.ema_beta if wl.ema_beta is not None else 0.9
+    b_per = round_bytes(wl, frag, k_incl) / max(1, wl.fragment_numel(frag))
+    spent, elems, used = 0.0, 0, 0
+    for t in tensors:
+        n = wl.specs[t].numel
+        if max_elems is not None:
+            n = min(n, max_elems - elems)
+        for s0 in range(0, n, P):
+            c = min(P, n - s0)
+            t0 = time.perf_counter()
+            oracle.merge_tensor([x[:c] for x in xs], theta[:c], mode=mode, tokens=tokens,
+                                lr=wl.lr, mu=wl.mu, m=None if m is None else m[:c],
+                                e=None if e is None else e[:c], beta=beta)
+            spent += time.perf_counter() - t0
+            elems += c
+        used += 1
+        if spent >= max_seconds or (max_elems is not None and elems >= max_elems):
+            break
+    desc = (f"first {used} of the round's {len(tensors)} tensors ({elems:,} of "
+            f"{wl.fragment_numel(frag):,} elements), same recipe, single-threaded C oracle")
+    return elems * b_per / spent / 1e9, spent, elems, desc
+
+
+# ---- the two arms ----------------------------------------------------------------------
+
+def run_reference(args, wl, ws, rank) -> int:
+    if rank != 0:
+        return 0
+    # each step times a bounded sample so that warmup + steps end within minutes
+    rates, secs = [], []
+    for i in range(args.warmup + args.steps):
+        gbs, s, n, desc = oracle_sample_rate(wl, max_seconds=args.ref_seconds_per_step,
+                                             pool_elems=1 << 22)
+        if i >= args.warmup:
+            rates.append(gbs)
+            secs.append(s)
+    gbs = statistics.median(rates)
+    bytes_full = sum(round_bytes(wl, f, wl.K - wl.n_masked) for _, f in wl.rounds)
+    ms_full = bytes_full / (gbs * 1e9) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_full, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "n_params": wl.n_params, "K": wl.K,
+                   "sample_per_step": desc,
+                   "ms_per_step_note": "extrapolated from the sample's rate to the full round"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl, ws, rank, local) -> int:
+    import torch
+
+    import __graft_entry__
+    from checkpoint_averaging_gb300 import binding as B
+    from checkpoint_averaging_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the merge runs only on the GPU")
+    if rank == 0:
+        __graft_entry__.build()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier(ws)
+        __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    seed = args.seed + rank
+
+    # inputs resident in HBM: the global, the state, K workers per round
+    g = W.make_global(wl, seed, dev)
+    theta = W.empty_arena(g.numels, torch.float32, dev)
+    theta.flat.copy_(g.flat)
+    m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
+    e = None
+    if wl.ema_beta is not None:
+        e = W.empty_arena(g.numels, torch.float32, dev)
+        e.flat.copy_(g.flat)
+    draws = [W.draw_round(wl, i, seed) for i in range(len(wl.rounds))]
+    workers = [[W.make_worker(wl, g, rnd, k, seed, dev) for k in range(wl.K)]
+               for rnd, _ in wl.rounds]
+    del g
+    mg = B.Merger(theta.views, momentum=None if m is None else m.views,
+                  ema=None if e is None else e.views, fragment_of=wl.fragment_of,
+                  n_fragments=wl.n_fragments, quorum=wl.quorum)
+    n_streams = max(1, wl.in_flight)
+    streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
+    norm_out = [(torch.zeros(len(mg.fragment_tensors(f)) or 1, dtype=torch.float64, device=dev),
+                 torch.zeros(1, dtype=torch.float64, device=dev)) for _, f in wl.rounds]
+    mode = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
+    round_no = [0]
+    ev_pairs = []
+
+    def step(timed: bool) -> None:
+        main = streams[0]
+        for s in streams[1:]:
+            s.wait_stream(main)
+        for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
+            s = streams[i % n_streams]
+            rd = mg.begin(round_no[0], frag)
+            round_no[0] += 1
+            for k in d.included:
+                rd.accumulate(w[k].views, d.tokens[k])
+            rd.finalize(mode, wl.lr, wl.mu)
+            if wl.ema_beta is not None:
+                rd.ema_update(wl.ema_beta)
+            if wl.norms:
+                rd.drift_norm(*norm_out[i])
+            if timed:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+            rd.commit(s)
+            if timed:
+                b.record(s)
+                ev_pairs.append((a, b))
+        for s in streams[1:]:
+            main.wait_stream(s)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    launches0 = mg.launch_count
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(streams[0])
+        for _ in range(args.steps):
+            step(True)
+        t1.record(streams[0])
+        torch.cuda.synchronize(dev)
+    elapsed = t0.elapsed_time(t1) / 1e3
+    barrier(ws)
+    launches = mg.launch_count - launches0
+    k_incl = [len(d.included) for d in draws]
+    step_bytes = sum(round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl))
+    agg = aggregate(step_bytes, args.steps, elapsed, ws, dev)
+
+    # roofline of the dominant launch: the merge pass of the biggest round
+    per_round = [round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl)]
+    big = max(range(len(per_round)), key=per_round.__getitem__)
+    durs = [a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
+            if i % len(wl.rounds) == big]
+    kern_s = statistics.mean(durs)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured"
+    if not peak:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    achieved = per_round[big] / kern_s / 1e9
+    traffic = stored_traffic(wl.name)
+
+    # end to end through the public API: worker inputs start in pinned host
+    # memory and are copied in every step; the new global and EMA are read back.
+    e2e = None
+    if args.e2e_steps > 0 and ws == 1:
+        e2e = run_e2e(args, wl, mg, workers, draws, theta, e, streams[0], mode, round_no)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        gbs, secs, n, desc = oracle_sample_rate(wl, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f"; {secs:.1f} s of oracle time"}
+
+    ck = clocks.summary()
+    mg.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(agg["ms_per_step"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if wl.ckpt_dtype == "f32" else "bf16->f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "n_params": wl.n_params, "K": wl.K,
+                       "included": k_incl, "mode": wl.mode, "ema": wl.ema_beta is not None,
+                       "norms": wl.norms, "rounds_per_step": len(wl.rounds),
+                       "streams": n_streams, "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (no flush needed)",
+                       "parallelism": f"replicas{ws}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": peak_src, "traffic": traffic,
+                         "kernel": "merge_fused", "kernel_ms": round(kern_s * 1e3, 4),
+                         "algorithmic_bytes_per_launch": per_round[big]},
+            "clocks": ck,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> dict:
+    import torch
+
+    dev = theta.flat.device
+    pinned = [[None] * wl.K for _ in wl.rounds]
+    h2d = 0
+    for i, d in enumerate(draws):
+        for k in d.included:
+            h = torch.empty_like(workers[i][k].flat, device="cpu").pin_memory()
+            h.copy_(workers[i][k].flat)
+            pinned[i][k] = h
+            h2d += h.numel() * h.element_size()
+    out_theta = torch.empty_like(theta.flat, device="cpu").pin_memory()
+    out_e = torch.empty_like(e.flat, device="cpu").pin_memory() if e is not None else None
+    d2h = out_theta.numel() * 4 + (out_e.numel() * 4 if out_e is not None else 0)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
+                for k in d.included:
+                    w[k].flat.copy_(pinned[i][k], non_blocking=True)
+                rd = mg.begin(round_no[0], frag)
+                round_no[0] += 1
+                for k in d.included:
+                    rd.accumulate(w[k].views, d.tokens[k])
+                rd.finalize(mode, wl.lr, wl.mu)
+                if wl.ema_beta is not None:
+                    rd.ema_update(wl.ema_beta)
+                rd.commit(stream)
+            out_theta.copy_(theta.flat, non_blocking=True)
+            if out_e is not None:
+                out_e.copy_(e.flat, non_blocking=True)
+        stream.synchronize()
+
+    step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        step()
+    el = time.perf_counter() - t0
+    step_bytes = sum(round_bytes(wl, f, len(d.included)) for (_, f), d in zip(wl.rounds, draws))
+    return {"value": round(step_bytes * args.e2e_steps / el / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(el / args.e2e_steps * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps,
+            "note": "algorithmic merge bytes per wall second; the step copies the included "
+                    "workers host->device and the new global and EMA device->host"}
+
+
+def parse(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="diffurefill1b")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-seconds-per-step", type=float, default=1.5)
+    return p.parse_args(argv)
+
+
+def main(argv=None) -> int:
+    args = parse(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    from checkpoint_averaging_gb300 import workloads as W
+    wl = W.workload(args.workload)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, wl, ws, rank)
+    return run_ours(args, wl, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,373 @@
+"""ctypes binding of libcam (C ABI in include/cam.h): argument marshalling only.
+
+The functions here carry the C ABI's names without the ``cam_`` prefix and
+turn error codes into exceptions. ``Merger`` / ``Round`` are a thin layer
+for torch users: they check that tensors live on the right CUDA device with
+the right dtype and layout, pass ``data_ptr()`` values and the current CUDA
+stream, and keep borrowed checkpoint tensors alive on the commit stream.
+Every step of a merge runs in libcam's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libcam.so")
+
+KMAX = 8
+MAX_OPEN_ROUNDS = 8
+
+F32, BF16 = 0, 1
+MEAN_REPLACE, DELTA_NESTEROV = 0, 1
+INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM = 1, 2
+
+OK, E_ARG, E_STATE, E_STALE, E_BUSY, E_QUORUM, E_KMAX, E_CUDA, E_NOMEM = \
+    0, -1, -2, -3, -4, -5, -6, -7, -8
+
+
+class CamError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class ArgError(CamError, ValueError):
+    pass
+
+
+class StateError(CamError):
+    pass
+
+
+class StaleRoundError(CamError):
+    pass
+
+
+class BusyError(CamError):
+    pass
+
+
+class QuorumError(CamError):
+    pass
+
+
+class KmaxError(CamError):
+    pass
+
+
+class CudaError(CamError):
+    pass
+
+
+_ERRORS = {E_ARG: ArgError, E_STATE: StateError, E_STALE: StaleRoundError,
+           E_BUSY: BusyError, E_QUORUM: QuorumError, E_KMAX: KmaxError,
+           E_CUDA: CudaError, E_NOMEM: CamError}
+
+
+class CtxDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_tensors", ctypes.c_int32),
+        ("numel", ctypes.POINTER(ctypes.c_int64)),
+        ("fragment_of", ctypes.POINTER(ctypes.c_int32)),
+        ("n_fragments", ctypes.c_int32),
+        ("quorum", ctypes.c_int32),
+        ("master", ctypes.POINTER(ctypes.c_void_p)),
+        ("momentum", ctypes.POINTER(ctypes.c_void_p)),
+        ("ema", ctypes.POINTER(ctypes.c_void_p)),
+        ("device", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
+           "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
+           "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
+           "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_last_error", "cam_version")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcam.so; raise if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libcam.so is missing at {LIB_PATH}: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, vpp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    L.cam_ctx_create.argtypes = [ctypes.POINTER(CtxDesc), vpp]
+    L.cam_ctx_destroy.argtypes = [vp]
+    L.cam_ctx_destroy.restype = None
+    L.cam_merge_begin.argtypes = [vp, i64, i32, vpp]
+    L.cam_merge_accumulate.argtypes = [vp, vpp, ctypes.c_int, i64]
+    L.cam_merge_finalize.argtypes = [vp, ctypes.c_int, ctypes.c_float, ctypes.c_float]
+    L.cam_ema_update.argtypes = [vp, ctypes.c_float]
+    L.cam_drift_norm.argtypes = [vp, vp, vp]
+    L.cam_merge_commit.argtypes = [vp, vp]
+    L.cam_merge_abort.argtypes = [vp]
+    L.cam_fragment_info.argtypes = [vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                    ctypes.POINTER(i32)]
+    L.cam_ctx_get_last_round.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_ctx_set_last_round.argtypes = [vp, i64]
+    L.cam_ctx_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_last_error.argtypes = []
+    L.cam_last_error.restype = ctypes.c_char_p
+    L.cam_version.argtypes = []
+    L.cam_version.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        fn = getattr(L, name)
+        if name not in ("cam_ctx_destroy", "cam_last_error", "cam_version"):
+            fn.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return lib().cam_last_error().decode()
+
+
+def version() -> str:
+    return lib().cam_version().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        raise _ERRORS.get(rc, CamError)(rc, last_error())
+
+
+def _ptrs(values: Sequence[int] | None):
+    if values is None:
+        return None
+    return (ctypes.c_void_p * max(1, len(values)))(*[int(v) for v in values])
+
+
+# ---- the C ABI, one function per entry point -----------------------------------
+
+def ctx_create(numel: Sequence[int], master: Sequence[int], *, fragment_of=None,
+               n_fragments: int = 1, quorum: int = 1, momentum=None, ema=None,
+               device: int = 0, flags: int = 0, stream: int = 0) -> int:
+    n = len(numel)
+    numel_a = (ctypes.c_int64 * max(1, n))(*[int(v) for v in numel])
+    frag_a = None if fragment_of is None else (ctypes.c_int32 * max(1, n))(*fragment_of)
+    keep = [numel_a, frag_a, _ptrs(master), _ptrs(momentum), _ptrs(ema)]
+    d = CtxDesc(n, numel_a,
+                None if frag_a is None else ctypes.cast(frag_a, ctypes.POINTER(ctypes.c_int32)),
+                n_fragments, quorum,
+                ctypes.cast(keep[2], ctypes.POINTER(ctypes.c_void_p)),
+                None if keep[3] is None else ctypes.cast(keep[3], ctypes.POINTER(ctypes.c_void_p)),
+                None if keep[4] is None else ctypes.cast(keep[4], ctypes.POINTER(ctypes.c_void_p)),
+                device, flags, stream or None)
+    out = ctypes.c_void_p()
+    _check(lib().cam_ctx_create(ctypes.byref(d), ctypes.byref(out)))
+    return out.value
+
+
+def ctx_destroy(ctx: int) -> None:
+    lib().cam_ctx_destroy(ctx)
+
+
+def merge_begin(ctx: int, round: int, fragment: int = -1) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().cam_merge_begin(ctx, round, fragment, ctypes.byref(out)))
+    return out.value
+
+
+def merge_accumulate(rd: int, ckpt: Sequence[int], dtype: int, tokens: int = 0) -> None:
+    arr = _ptrs(ckpt)
+    _check(lib().cam_merge_accumulate(rd, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)),
+                                      dtype, tokens))
+
+
+def merge_finalize(rd: int, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
+    _check(lib().cam_merge_finalize(rd, mode, lr, mu))
+
+
+def ema_update(rd: int, beta: float) -> None:
+    _check(lib().cam_ema_update(rd, beta))
+
+
+def drift_norm(rd: int, per_tensor: int | None, per_fragment: int | None) -> None:
+    _check(lib().cam_drift_norm(rd, per_tensor or None, per_fragment or None))
+
+
+def merge_commit(rd: int, stream: int = 0) -> None:
+    _check(lib().cam_merge_commit(rd, stream or None))
+
+
+def merge_abort(rd: int) -> None:
+    _check(lib().cam_merge_abort(rd))
+
+
+def fragment_info(ctx: int, fragment: int) -> tuple[list[int], int]:
+    nt, ne = ctypes.c_int32(), ctypes.c_int64()
+    _check(lib().cam_fragment_info(ctx, fragment, ctypes.byref(nt), ctypes.byref(ne), None))
+    ids = (ctypes.c_int32 * max(1, nt.value))()
+    _check(lib().cam_fragment_info(ctx, fragment, None, None, ids))
+    return list(ids[:nt.value]), ne.value
+
+
+def ctx_get_last_round(ctx: int) -> int:
+    out = ctypes.c_int64()
+    _check(lib().cam_ctx_get_last_round(ctx, ctypes.byref(out)))
+    return out.value
+
+
+def ctx_set_last_round(ctx: int, round: int) -> None:
+    _check(lib().cam_ctx_set_last_round(ctx, round))
+
+
+def ctx_launch_count(ctx: int) -> int:
+    out = ctypes.c_int64()
+    _check(lib().cam_ctx_launch_count(ctx, ctypes.byref(out)))
+    return out.value
+
+
+# ---- torch-facing layer ----------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+class Merger:
+    """The merger's state on one GPU: fp32 master weights (theta), optional
+    outer momentum and EMA buffers, the fragment map and the quorum. The
+    tensors are borrowed for the Merger's life and updated in place."""
+
+    def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
+                 n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
+                 zero_momentum=False, stream=None):
+        torch = _torch()
+        self.master = list(master)
+        self.momentum = None if momentum is None else list(momentum)
+        self.ema = None if ema is None else list(ema)
+        if not self.master:
+            raise ValueError("empty parameter list")
+        dev = self.master[0].device
+        if dev.type != "cuda":
+            raise ValueError("master tensors must be CUDA tensors")
+        self.device = dev
+        for group in (self.master, self.momentum, self.ema):
+            if group is None:
+                continue
+            if len(group) != len(self.master):
+                raise ValueError("momentum/ema lists must match the master list")
+            for t, ref in zip(group, self.master):
+                if (t.device != dev or t.dtype != torch.float32 or not t.is_contiguous()
+                        or t.numel() != ref.numel()):
+                    raise ValueError("state tensors must be contiguous fp32 on one device")
+        self.numel = [t.numel() for t in self.master]
+        self.fragment_of = list(fragment_of) if fragment_of is not None else [0] * len(self.master)
+        self.n_fragments = n_fragments
+        flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
+                (INIT_ZERO_MOMENTUM if zero_momentum else 0)
+        with torch.cuda.device(dev):
+            self.ctx = ctx_create(
+                self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,
+                n_fragments=n_fragments, quorum=quorum,
+                momentum=None if self.momentum is None else [t.data_ptr() for t in self.momentum],
+                ema=None if self.ema is None else [t.data_ptr() for t in self.ema],
+                device=dev.index if dev.index is not None else torch.cuda.current_device(),
+                flags=flags, stream=_stream_handle(stream))
+        self._frag_cache = {}
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            ctx_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def fragment_tensors(self, fragment: int) -> list[int]:
+        if fragment not in self._frag_cache:
+            self._frag_cache[fragment] = fragment_info(self.ctx, fragment)[0]
+        return self._frag_cache[fragment]
+
+    @property
+    def launch_count(self) -> int:
+        return ctx_launch_count(self.ctx)
+
+    @property
+    def last_round(self) -> int:
+        return ctx_get_last_round(self.ctx)
+
+    @last_round.setter
+    def last_round(self, r: int) -> None:
+        ctx_set_last_round(self.ctx, r)
+
+    def begin(self, round: int, fragment: int = -1) -> "Round":
+        return Round(self, merge_begin(self.ctx, round, fragment), fragment)
+
+
+class Round:
+    def __init__(self, merger: Merger, handle: int, fragment: int):
+        self.merger, self.handle, self.fragment = merger, handle, fragment
+        self.tensors = merger.fragment_tensors(fragment)
+        self._borrowed = []
+
+    def accumulate(self, ckpt, tokens: int = 0) -> None:
+        """ckpt: the worker's tensors of this fragment, in fragment order
+        (or the whole tensor list, from which the fragment's are taken)."""
+        torch = _torch()
+        ckpt = list(ckpt)
+        if len(ckpt) == len(self.merger.master) and len(ckpt) != len(self.tensors):
+            ckpt = [ckpt[g] for g in self.tensors]
+        if len(ckpt) != len(self.tensors):
+            raise ValueError(f"expected {len(self.tensors)} tensors, got {len(ckpt)}")
+        dt = ckpt[0].dtype if ckpt else torch.float32
+        if dt not in (torch.float32, torch.bfloat16):
+            raise ValueError("checkpoints must be fp32 or bf16")
+        for t, g in zip(ckpt, self.tensors):
+            if (t.device != self.merger.device or t.dtype != dt or not t.is_contiguous()
+                    or t.numel() != self.merger.numel[g]):
+                raise ValueError(f"checkpoint tensor for tensor {g} has wrong device/dtype/shape")
+        merge_accumulate(self.handle, [t.data_ptr() for t in ckpt],
+                         BF16 if dt == torch.bfloat16 else F32, int(tokens))
+        self._borrowed.extend(ckpt)
+
+    def finalize(self, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
+        merge_finalize(self.handle, mode, lr, mu)
+
+    def ema_update(self, beta: float) -> None:
+        ema_update(self.handle, beta)
+
+    def drift_norm(self, per_tensor=None, per_fragment=None) -> None:
+        torch = _torch()
+        for t, n in ((per_tensor, len(self.tensors)), (per_fragment, 1)):
+            if t is not None and (t.device != self.merger.device or t.dtype != torch.float64
+                                  or not t.is_contiguous() or t.numel() < n):
+                raise ValueError("norm outputs must be contiguous fp64 device tensors")
+        drift_norm(self.handle, None if per_tensor is None else per_tensor.data_ptr(),
+                   None if per_fragment is None else per_fragment.data_ptr())
+        self._borrowed.extend(t for t in (per_tensor, per_fragment) if t is not None)
+
+    def commit(self, stream=None) -> None:
+        torch = _torch()
+        s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
+        merge_commit(self.handle, int(s.cuda_stream))
+        self.handle = None
+        for t in self._borrowed:  # freed memory is not reused before the merge ran
+            t.record_stream(s)
+        self._borrowed = []
+
+    def abort(self) -> None:
+        merge_abort(self.handle)
+        self.handle = None

@@ -1,0 +1,83 @@
+// cam_internal.h -- structures shared by the host runtime and the CUDA kernels
+// of libcam. Not part of the C ABI (include/cam.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "cam.h"
+
+namespace cam {
+
+// Threads per block of the fused merge pass, and elements one thread handles
+// per step of its chunk loop (one 32-byte fp32 vector / one 16-byte bf16 one).
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+// Chunks are multiples of one block-step so that every chunk start keeps the
+// tensor's vector alignment.
+constexpr int kChunkQuantum = kThreads * kVec;  // 2048 elements
+constexpr int kMaxChunkElems = 8 * kChunkQuantum;
+// Worker pointers carried in one launch's parameter block. Kernel parameters
+// may take up to 32,764 bytes; this keeps MergeArgs under that.
+constexpr int kXCap = 3520;
+
+// One chunk of the fragment's element space: elements [start, start+len) of
+// the fragment's local tensor `local`. Chunks never straddle tensors.
+struct ChunkDesc {
+    int64_t start;
+    int32_t local;
+    int32_t len;
+};
+static_assert(sizeof(ChunkDesc) == 16, "ChunkDesc is one 16-byte load");
+
+// A fragment tensor's caller-owned state buffers.
+struct TensorSlot {
+    float* theta;
+    float* m;
+    float* e;
+    int64_t numel;
+};
+
+// Parameter block of one launch of the fused merge pass. The launch covers
+// the fragment's local tensors [local0, local0 + n_local) and their chunks.
+struct MergeArgs {
+    const ChunkDesc* chunks;  // first chunk of this launch (device)
+    const TensorSlot* slots;  // the fragment's tensors, by local index (device)
+    double* partials;         // drift partial per chunk of this launch (device) or null
+    int32_t n_chunks;
+    int32_t local0;
+    int32_t n_local;
+    int32_t K;
+    float Kf;                 // (float)K
+    float w[CAM_KMAX];        // (float)tokens_k
+    float W;                  // (float)sum tokens
+    float lr, mu, beta;
+    uint32_t vec[(kXCap + 31) / 32];  // bit l: tensor local0+l takes the vector path
+    // x[l*K + k]: worker k's copy of tensor local0+l. The CAM_KMAX spare slots
+    // keep every x[l*K + k] with l < n_local, k < CAM_KMAX inside the block.
+    const void* x[kXCap + CAM_KMAX];
+};
+static_assert(sizeof(MergeArgs) <= 32000, "kernel parameter block too large");
+
+// Parameter block of the deterministic norm finish.
+struct NormArgs {
+    const double* partials;     // [n_chunks of the fragment]
+    const int32_t* first_chunk; // [n_tensors + 1]: tensor t owns chunks [first[t], first[t+1])
+    int32_t n_tensors;
+    double* tsq;                // scratch [n_tensors]: squared norms
+    double* per_tensor;         // output or null
+    double* per_fragment;       // output or null
+};
+
+enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
+
+// Launches one fused merge pass with `grid` blocks.
+cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm,
+                         int grid, cudaStream_t s);
+// Resident blocks per SM of that variant (0 on error).
+int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm);
+cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s);
+cudaError_t launch_fill(float* dst, int64_t n, float v, cudaStream_t s);
+cudaError_t launch_copy(float* dst, const float* src, int64_t n, cudaStream_t s);
+
+}  // namespace cam

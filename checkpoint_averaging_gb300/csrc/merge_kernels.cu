@@ -1,0 +1,316 @@
+// merge_kernels.cu -- the device side of the DiLoCo outer merge for sm_103a.
+//
+// merge_fused: one pass over a fragment's ragged tensor list that, per
+// element, widens the K workers' values to fp32, folds them in arrival order
+// (plain mean, or token-weighted mean of the deltas), applies the outer step
+// (plain replacement, or outer Nesterov), updates the EMA of the globals and
+// accumulates the squared drift. Every state element (theta, m, e) is read at
+// most once and written once, every worker element is read once.
+//   Plain mean in a running fp32 sum as checkpoints arrive: "DiffuRefill-1B"
+//   model card, "How it is trained", Merging. Plain replacement and the EMA of
+//   globals (beta 0.9): "DiffuRefill-1B: Pretraining a Masked Diffusion
+//   Language Model on Free, Preemptible Notebook GPUs", section 3, Table 2.
+//   Token-weighted delta mean and outer Nesterov (lr 0.7, momentum 0.9):
+//   "Pythia-14M on four rented GPUs and a bucket", "Getting updates through
+//   the bucket".
+//
+// The pass is HBM-bound (a handful of flops per 20-40 bytes), so the design is
+// about bytes in flight: 32-byte fp32 / 16-byte bf16 vector loads per thread,
+// read-once worker data loaded through the non-coherent path without L1
+// allocation and marked evict-first in L2, and a persistent grid striding over
+// fixed-size chunks of the fragment. Arithmetic uses explicit round-to-nearest
+// intrinsics, so no multiply-add is contracted and every result is the fixed
+// sequence of binary32 operations the C ABI documents.
+//
+// norm_finish: sums the per-chunk drift partials per tensor and per fragment
+// in a fixed order, so norms are bitwise reproducible.
+#include <cuda_runtime.h>
+
+#include "cam_internal.h"
+
+namespace cam {
+namespace {
+
+constexpr int kMean = CAM_MODE_MEAN_REPLACE;
+constexpr int kDelta = CAM_MODE_DELTA_NESTEROV;
+
+// ---- memory access -----------------------------------------------------------
+
+// Worker data: read once, never written by this pass. XVec<T> holds one
+// thread's 8 consecutive elements of one worker as loaded (fp32 values, or
+// bf16 pairs packed in 32-bit words) and widens on access; bf16 is the high
+// half of a binary32, so widening is exact.
+template <typename XT>
+struct XVec;
+
+template <>
+struct XVec<float> {
+    float v[8];
+    __device__ __forceinline__ void load(const float* p) {
+        asm volatile(
+            "ld.global.nc.L1::no_allocate.L2::evict_first.v8.f32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+              "=f"(v[6]), "=f"(v[7])
+            : "l"(p));
+    }
+    __device__ __forceinline__ float get(int j) const { return v[j]; }
+};
+
+template <>
+struct XVec<uint16_t> {
+    uint32_t u[4];
+    __device__ __forceinline__ void load(const uint16_t* p) {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
+                     : "l"(p));
+    }
+    __device__ __forceinline__ float get(int j) const {
+        const uint32_t w = u[j >> 1];
+        return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+};
+
+__device__ __forceinline__ float load_x1(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float load_x1(const uint16_t* p) {
+    unsigned short b;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(b) : "l"(p));
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// State (theta, m, e): read once and written back by the same thread.
+__device__ __forceinline__ void load_s8(const float* p, float (&v)[8]) {
+    asm volatile(
+        "ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+          "=f"(v[6]), "=f"(v[7])
+        : "l"(p));
+}
+
+__device__ __forceinline__ void store_s8(float* p, const float (&v)[8]) {
+    asm volatile(
+        "st.global.L1::no_allocate.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+        "f"(v[7])
+        : "memory");
+}
+
+// ---- per-element arithmetic ----------------------------------------------------
+
+// One element of one round. xk[k] (k < K) are the workers' values in arrival
+// order; th, m, e are updated in place; acc collects the squared drift.
+template <int MODE, bool EMA, bool NORM>
+__device__ __forceinline__ void merge_elem(const MergeArgs& a, const float (&xk)[CAM_KMAX],
+                                           float& th, float& m, float& e, float& acc) {
+    if (MODE == kMean) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k)
+            if (k < a.K) s = __fadd_rn(s, xk[k]);
+        const float mean = __fdiv_rn(s, a.Kf);
+        if (NORM) {
+            const float d = __fsub_rn(mean, th);
+            acc = __fmaf_rn(d, d, acc);
+        }
+        th = mean;  // plain replacement
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k)
+            if (k < a.K) s = __fadd_rn(s, __fmul_rn(a.w[k], __fsub_rn(xk[k], th)));
+        const float delta = __fdiv_rn(s, a.W);
+        if (NORM) acc = __fmaf_rn(delta, delta, acc);
+        const float g = -delta;  // pseudo-gradient theta - (theta + delta)
+        const float m_new = __fadd_rn(__fmul_rn(a.mu, m), g);
+        const float step = __fadd_rn(g, __fmul_rn(a.mu, m_new));
+        th = __fsub_rn(th, __fmul_rn(a.lr, step));
+        m = m_new;
+    }
+    if (EMA) {
+        const float omb = __fsub_rn(1.0f, a.beta);
+        e = __fadd_rn(__fmul_rn(a.beta, e), __fmul_rn(omb, th));
+    }
+}
+
+template <typename XT, int MODE, bool EMA, bool NORM>
+__device__ __forceinline__ void merge_vec8(const MergeArgs& a, const void* const* xs,
+                                           const TensorSlot& ts, int64_t i, float& acc) {
+    XVec<XT> x[CAM_KMAX];
+#pragma unroll
+    for (int k = 0; k < CAM_KMAX; ++k)
+        if (k < a.K) x[k].load(static_cast<const XT*>(xs[k]) + i);
+    float th[8], m[8], e[8];
+    if (MODE == kDelta || NORM) load_s8(ts.theta + i, th);
+    if (MODE == kDelta) load_s8(ts.m + i, m);
+    if (EMA) load_s8(ts.e + i, e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float xk[CAM_KMAX];
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
+        merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
+    }
+    store_s8(ts.theta + i, th);
+    if (MODE == kDelta) store_s8(ts.m + i, m);
+    if (EMA) store_s8(ts.e + i, e);
+}
+
+template <typename XT, int MODE, bool EMA, bool NORM>
+__device__ __forceinline__ void merge_one(const MergeArgs& a, const void* const* xs,
+                                          const TensorSlot& ts, int64_t i, float& acc) {
+    float xk[CAM_KMAX];
+#pragma unroll
+    for (int k = 0; k < CAM_KMAX; ++k)
+        xk[k] = (k < a.K) ? load_x1(static_cast<const XT*>(xs[k]) + i) : 0.0f;
+    float th = ts.theta[i];
+    float m = (MODE == kDelta) ? ts.m[i] : 0.0f;
+    float e = EMA ? ts.e[i] : 0.0f;
+    merge_elem<MODE, EMA, NORM>(a, xk, th, m, e, acc);
+    ts.theta[i] = th;
+    if (MODE == kDelta) ts.m[i] = m;
+    if (EMA) ts.e[i] = e;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ---- the fused pass ------------------------------------------------------------
+
+template <typename XT, int MODE, bool EMA, bool NORM>
+__global__ void __launch_bounds__(kThreads, 2)
+    merge_fused(const __grid_constant__ MergeArgs a) {
+    __shared__ double warp_part[kThreads / 32];
+    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+        const ChunkDesc ch = a.chunks[c];
+        const int l = ch.local - a.local0;
+        const TensorSlot ts = a.slots[ch.local];
+        const void* const* xs = a.x + static_cast<int64_t>(l) * a.K;
+        const bool vec = (a.vec[l >> 5] >> (l & 31)) & 1u;
+        float acc = 0.0f;
+        if (vec) {
+            const int nv = ch.len >> 3;
+            for (int v = threadIdx.x; v < nv; v += kThreads)
+                merge_vec8<XT, MODE, EMA, NORM>(a, xs, ts, ch.start + 8 * int64_t(v), acc);
+            const int tail = ch.len & 7;
+            if (static_cast<int>(threadIdx.x) < tail)
+                merge_one<XT, MODE, EMA, NORM>(a, xs, ts,
+                                               ch.start + 8 * int64_t(nv) + threadIdx.x, acc);
+        } else {
+            for (int j = threadIdx.x; j < ch.len; j += kThreads)
+                merge_one<XT, MODE, EMA, NORM>(a, xs, ts, ch.start + j, acc);
+        }
+        if (NORM) {
+            // fp32 within a thread (at most a few dozen squares), fp64 above.
+            const double d = warp_sum(static_cast<double>(acc));
+            if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = d;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                double s = 0.0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) s += warp_part[w];
+                a.partials[c] = s;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int n_warps = blockDim.x >> 5;
+    for (int t = warp; t < a.n_tensors; t += n_warps) {
+        double s = 0.0;
+        for (int c = a.first_chunk[t] + lane; c < a.first_chunk[t + 1]; c += 32)
+            s += a.partials[c];
+        s = warp_sum(s);
+        if (lane == 0) a.tsq[t] = s;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        double s = 0.0;
+        for (int t = lane; t < a.n_tensors; t += 32) s += a.tsq[t];
+        s = warp_sum(s);
+        if (lane == 0 && a.per_fragment) *a.per_fragment = sqrt(s);
+    }
+    if (a.per_tensor)
+        for (int t = threadIdx.x; t < a.n_tensors; t += blockDim.x)
+            a.per_tensor[t] = sqrt(a.tsq[t]);
+}
+
+__global__ void fill_kernel(float* dst, int64_t n, float v) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        dst[i] = v;
+}
+
+__global__ void copy_kernel(float* dst, const float* src, int64_t n) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        dst[i] = src[i];
+}
+
+// ---- variant dispatch ------------------------------------------------------------
+
+using MergeFn = void (*)(MergeArgs);
+
+template <typename XT, int MODE>
+MergeFn pick3(bool ema, bool norm) {
+    if (ema) return norm ? merge_fused<XT, MODE, true, true> : merge_fused<XT, MODE, true, false>;
+    return norm ? merge_fused<XT, MODE, false, true> : merge_fused<XT, MODE, false, false>;
+}
+
+MergeFn pick(int dtype, int mode, bool ema, bool norm) {
+    if (dtype == kDtBF16)
+        return mode == kDelta ? pick3<uint16_t, kDelta>(ema, norm)
+                              : pick3<uint16_t, kMean>(ema, norm);
+    return mode == kDelta ? pick3<float, kDelta>(ema, norm) : pick3<float, kMean>(ema, norm);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm,
+                         int grid, cudaStream_t s) {
+    MergeFn fn = pick(dtype, mode, ema, norm);
+    void* args[] = {const_cast<MergeArgs*>(&a)};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads),
+                            args, 0, s);
+}
+
+int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, reinterpret_cast<const void*>(pick(dtype, mode, ema, norm)), kThreads, 0) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s) {
+    norm_finish<<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill(float* dst, int64_t n, float v, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    fill_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(dst, n, v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(float* dst, const float* src, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    copy_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(dst, src, n);
+    return cudaGetLastError();
+}
+
+}  // namespace cam

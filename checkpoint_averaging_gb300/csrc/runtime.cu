@@ -1,0 +1,534 @@
+// runtime.cu -- host side of libcam: contexts, fragment plans, the round state
+// machine, argument validation and kernel launches (C ABI in include/cam.h).
+//
+// A context owns, per fragment (and once for "all tensors"), a plan: the
+// fragment's tensors in order, its element space cut into chunks that never
+// straddle a tensor, and small device tables (chunk list, state pointers,
+// per-chunk drift partials). Chunk sizes are chosen per fragment from the
+// device's SM count so that even a small fragment spreads over every SM.
+//
+// Rounds follow the merger described on the pages: a round collects the
+// round's checkpoints as they arrive, closes once a quorum has arrived
+// ("Pythia-14M on four rented GPUs and a bucket", "Getting updates through the
+// bucket": quorum_size=3; "DiffuRefill-1B" technical report, section 3,
+// Table 2, "Merger": wait for N fresh checkpoints of the current round tag),
+// and round numbers only grow (same report, section 3, "Failure handling"
+// (iii): a rollback is republished under a new round number). Accumulate only
+// records the borrowed pointers; the commit runs the whole round as one fused
+// pass, which visits every element's workers in the same arrival order as an
+// eager fold would, so the result is the same bits.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "cam_internal.h"
+
+#define CAM_API extern "C" __attribute__((visibility("default")))
+
+using cam::ChunkDesc;
+using cam::MergeArgs;
+using cam::NormArgs;
+using cam::TensorSlot;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(CAM_E_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// Makes `dev` current for the scope of one call and restores the caller's.
+struct DeviceScope {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceScope(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+    }
+    ~DeviceScope() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct Plan {
+    std::vector<int32_t> tensors;      // global tensor ids, fragment order
+    std::vector<int32_t> first_chunk;  // [T_f + 1]
+    std::vector<ChunkDesc> chunks;     // host copy of the chunk list
+    int64_t n_elems = 0;
+    int32_t chunk_elems = 0;
+    ChunkDesc* d_chunks = nullptr;
+    TensorSlot* d_slots = nullptr;
+    int32_t* d_first = nullptr;
+    double* d_partials = nullptr;
+    double* d_tsq = nullptr;
+    int32_t n_chunks() const { return static_cast<int32_t>(chunks.size()); }
+    int32_t n_tensors() const { return static_cast<int32_t>(tensors.size()); }
+};
+
+struct cam_round;
+
+struct cam_ctx {
+    int device = 0;
+    int sm_count = 0;
+    int32_t n_tensors = 0;
+    int32_t n_fragments = 1;
+    int32_t quorum = 1;
+    std::vector<int64_t> numel;
+    std::vector<int32_t> fragment_of;
+    std::vector<float*> theta, m, e;
+    bool has_m = false, has_e = false;
+    std::vector<Plan> plans;  // [n_fragments] then "all"
+    void* dev_block = nullptr;
+    int64_t last_round = -1;
+    int64_t launches = 0;
+    std::vector<cam_round*> open;
+    int bps[2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm]
+    std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
+
+    Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
+    const Plan& plan_of(int32_t fragment) const {
+        return plans[fragment < 0 ? n_fragments : fragment];
+    }
+};
+
+struct cam_round {
+    cam_ctx* ctx = nullptr;
+    int64_t round = 0;
+    int32_t fragment = -1;
+    int K = 0;
+    int dtype = -1;
+    std::vector<const void*> x;  // x[k * T_f + l]
+    int64_t tokens[CAM_KMAX] = {};
+    bool finalized = false;
+    int mode = CAM_MODE_MEAN_REPLACE;
+    float lr = 1.0f, mu = 0.0f;
+    bool ema = false;
+    float beta = 0.0f;
+    bool norms = false;
+    double* out_tensor = nullptr;
+    double* out_fragment = nullptr;
+};
+
+namespace {
+
+// Elements per chunk for a fragment of n elements: aim at >= 8 chunks per SM,
+// within [one block-step, kMaxChunkElems], always a whole number of block-steps.
+int32_t choose_chunk(int64_t n, int sm_count) {
+    const int64_t q = cam::kChunkQuantum;
+    const int64_t target = std::max<int64_t>(1, int64_t(sm_count) * 8);
+    int64_t c = (n + target - 1) / target;
+    c = ((c + q - 1) / q) * q;
+    return static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(c, q), cam::kMaxChunkElems));
+}
+
+void build_plan(Plan& p, const cam_ctx& c, int32_t fragment) {
+    p.tensors.clear();
+    for (int32_t t = 0; t < c.n_tensors; ++t)
+        if (fragment < 0 || c.fragment_of[t] == fragment) p.tensors.push_back(t);
+    p.n_elems = 0;
+    for (int32_t g : p.tensors) p.n_elems += c.numel[g];
+    p.chunk_elems = choose_chunk(p.n_elems, c.sm_count);
+    p.chunks.clear();
+    p.first_chunk.assign(1, 0);
+    for (int32_t l = 0; l < p.n_tensors(); ++l) {
+        const int64_t n = c.numel[p.tensors[l]];
+        for (int64_t s = 0; s < n; s += p.chunk_elems)
+            p.chunks.push_back(ChunkDesc{s, l, static_cast<int32_t>(std::min<int64_t>(p.chunk_elems, n - s))});
+        p.first_chunk.push_back(static_cast<int32_t>(p.chunks.size()));
+    }
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int validate_desc(const cam_ctx_desc* d) {
+    if (!d) return fail(CAM_E_ARG, "cam_ctx_create: desc is NULL");
+    if (d->n_tensors < 1) return fail(CAM_E_ARG, "cam_ctx_create: n_tensors must be >= 1");
+    if (!d->numel || !d->master) return fail(CAM_E_ARG, "cam_ctx_create: numel and master are required");
+    if (d->n_fragments < 1) return fail(CAM_E_ARG, "cam_ctx_create: n_fragments must be >= 1");
+    if (d->quorum < 1 || d->quorum > CAM_KMAX)
+        return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
+    if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
+    if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM))
+        return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
+    if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
+        return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
+    if ((d->flags & CAM_INIT_ZERO_MOMENTUM) && !d->momentum)
+        return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_ZERO_MOMENTUM without momentum buffers");
+    for (int32_t t = 0; t < d->n_tensors; ++t) {
+        const int64_t n = d->numel[t];
+        if (n < 0) return fail(CAM_E_ARG, "cam_ctx_create: numel[%d] < 0", t);
+        if (n > (int64_t(1) << 40)) return fail(CAM_E_ARG, "cam_ctx_create: numel[%d] too large", t);
+        if (d->fragment_of && (d->fragment_of[t] < 0 || d->fragment_of[t] >= d->n_fragments))
+            return fail(CAM_E_ARG, "cam_ctx_create: fragment_of[%d]=%d out of [0, %d)", t,
+                        d->fragment_of[t], d->n_fragments);
+        if (n > 0 && !d->master[t]) return fail(CAM_E_ARG, "cam_ctx_create: master[%d] is NULL", t);
+        if (n > 0 && d->momentum && !d->momentum[t])
+            return fail(CAM_E_ARG, "cam_ctx_create: momentum[%d] is NULL", t);
+        if (n > 0 && d->ema && !d->ema[t])
+            return fail(CAM_E_ARG, "cam_ctx_create: ema[%d] is NULL", t);
+    }
+    return CAM_OK;
+}
+
+}  // namespace
+
+CAM_API const char* cam_last_error(void) { return g_err.c_str(); }
+
+CAM_API const char* cam_version(void) { return "0.1.0"; }
+
+CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
+    if (!out) return fail(CAM_E_ARG, "cam_ctx_create: out is NULL");
+    *out = nullptr;
+    int rc = validate_desc(d);
+    if (rc != CAM_OK) return rc;
+
+    int n_dev = 0;
+    cudaError_t ce = cudaGetDeviceCount(&n_dev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_create: no usable CUDA device");
+    if (d->device >= n_dev)
+        return fail(CAM_E_CUDA, "cam_ctx_create: device %d not present (%d devices)", d->device, n_dev);
+    DeviceScope scope(d->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_ctx_create: cudaSetDevice");
+
+    std::unique_ptr<cam_ctx> c(new (std::nothrow) cam_ctx);
+    if (!c) return fail(CAM_E_NOMEM, "cam_ctx_create: out of host memory");
+    c->args.reset(new (std::nothrow) MergeArgs);
+    if (!c->args) return fail(CAM_E_NOMEM, "cam_ctx_create: out of host memory");
+    c->device = d->device;
+    ce = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, d->device);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_create: SM count");
+    c->n_tensors = d->n_tensors;
+    c->n_fragments = d->n_fragments;
+    c->quorum = d->quorum;
+    c->numel.assign(d->numel, d->numel + d->n_tensors);
+    c->fragment_of.assign(d->n_tensors, 0);
+    if (d->fragment_of) c->fragment_of.assign(d->fragment_of, d->fragment_of + d->n_tensors);
+    c->theta.assign(d->master, d->master + d->n_tensors);
+    c->has_m = d->momentum != nullptr;
+    c->has_e = d->ema != nullptr;
+    c->m.assign(d->n_tensors, nullptr);
+    c->e.assign(d->n_tensors, nullptr);
+    if (c->has_m) c->m.assign(d->momentum, d->momentum + d->n_tensors);
+    if (c->has_e) c->e.assign(d->ema, d->ema + d->n_tensors);
+
+    // Plans and one device block holding every plan's tables.
+    c->plans.resize(c->n_fragments + 1);
+    size_t bytes = 0;
+    for (int32_t f = 0; f <= c->n_fragments; ++f) {
+        Plan& p = c->plans[f];
+        build_plan(p, *c, f < c->n_fragments ? f : -1);
+        bytes += round_up(sizeof(ChunkDesc) * p.chunks.size(), 256);
+        bytes += round_up(sizeof(TensorSlot) * p.tensors.size(), 256);
+        bytes += round_up(sizeof(int32_t) * p.first_chunk.size(), 256);
+        bytes += round_up(sizeof(double) * p.chunks.size(), 256);
+        bytes += round_up(sizeof(double) * p.tensors.size(), 256);
+    }
+    ce = cudaMalloc(&c->dev_block, std::max<size_t>(bytes, 256));
+    if (ce != cudaSuccess) {
+        c->dev_block = nullptr;
+        return fail(CAM_E_NOMEM, "cam_ctx_create: cudaMalloc(%zu): %s", bytes, cudaGetErrorString(ce));
+    }
+    std::vector<unsigned char> host(std::max<size_t>(bytes, 256), 0);
+    size_t off = 0;
+    auto carve = [&](size_t n) {
+        const size_t o = off;
+        off += round_up(n, 256);
+        return o;
+    };
+    for (Plan& p : c->plans) {
+        std::vector<TensorSlot> slots;
+        for (int32_t g : p.tensors) slots.push_back(TensorSlot{c->theta[g], c->m[g], c->e[g], c->numel[g]});
+        size_t o;
+        o = carve(sizeof(ChunkDesc) * p.chunks.size());
+        if (!p.chunks.empty()) std::memcpy(&host[o], p.chunks.data(), sizeof(ChunkDesc) * p.chunks.size());
+        p.d_chunks = reinterpret_cast<ChunkDesc*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(TensorSlot) * slots.size());
+        if (!slots.empty()) std::memcpy(&host[o], slots.data(), sizeof(TensorSlot) * slots.size());
+        p.d_slots = reinterpret_cast<TensorSlot*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(int32_t) * p.first_chunk.size());
+        std::memcpy(&host[o], p.first_chunk.data(), sizeof(int32_t) * p.first_chunk.size());
+        p.d_first = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(double) * p.chunks.size());
+        p.d_partials = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(double) * p.tensors.size());
+        p.d_tsq = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
+    }
+    ce = cudaMemcpy(c->dev_block, host.data(), bytes, cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) {
+        cudaFree(c->dev_block);
+        return cuda_fail(ce, "cam_ctx_create: table upload");
+    }
+    for (int dt = 0; dt < 2; ++dt)
+        for (int md = 0; md < 2; ++md)
+            for (int em = 0; em < 2; ++em)
+                for (int nm = 0; nm < 2; ++nm)
+                    c->bps[dt][md][em][nm] = std::max(1, cam::merge_blocks_per_sm(dt, md, em, nm));
+
+    cudaStream_t s = static_cast<cudaStream_t>(d->stream);
+    for (int32_t t = 0; t < c->n_tensors && ce == cudaSuccess; ++t) {
+        if (c->numel[t] == 0) continue;
+        if (d->flags & CAM_INIT_ZERO_MOMENTUM) {
+            ce = cam::launch_fill(c->m[t], c->numel[t], 0.0f, s);
+            ++c->launches;
+        }
+        if (ce == cudaSuccess && (d->flags & CAM_INIT_EMA_FROM_MASTER)) {
+            ce = cam::launch_copy(c->e[t], c->theta[t], c->numel[t], s);
+            ++c->launches;
+        }
+    }
+    if (ce != cudaSuccess) {
+        cudaFree(c->dev_block);
+        return cuda_fail(ce, "cam_ctx_create: init kernels");
+    }
+    *out = c.release();
+    return CAM_OK;
+}
+
+CAM_API void cam_ctx_destroy(cam_ctx* c) {
+    if (!c) return;
+    for (cam_round* r : c->open) delete r;
+    c->open.clear();
+    if (c->dev_block) {
+        DeviceScope scope(c->device);
+        cudaFree(c->dev_block);
+    }
+    delete c;
+}
+
+CAM_API int cam_merge_begin(cam_ctx* c, int64_t round, int32_t fragment, cam_round** out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_merge_begin: NULL argument");
+    *out = nullptr;
+    if (fragment < -1 || fragment >= c->n_fragments)
+        return fail(CAM_E_ARG, "cam_merge_begin: fragment %d out of [-1, %d)", fragment, c->n_fragments);
+    if (round <= c->last_round)
+        return fail(CAM_E_STALE, "cam_merge_begin: round %lld is not newer than %lld",
+                    static_cast<long long>(round), static_cast<long long>(c->last_round));
+    for (const cam_round* r : c->open)
+        if (r->fragment == -1 || fragment == -1 || r->fragment == fragment)
+            return fail(CAM_E_BUSY, "cam_merge_begin: fragment %d overlaps open round %lld (fragment %d)",
+                        fragment, static_cast<long long>(r->round), r->fragment);
+    if (static_cast<int>(c->open.size()) >= CAM_MAX_OPEN_ROUNDS)
+        return fail(CAM_E_BUSY, "cam_merge_begin: %d rounds already open", CAM_MAX_OPEN_ROUNDS);
+    cam_round* r = new (std::nothrow) cam_round;
+    if (!r) return fail(CAM_E_NOMEM, "cam_merge_begin: out of host memory");
+    r->ctx = c;
+    r->round = round;
+    r->fragment = fragment;
+    try {
+        r->x.reserve(size_t(CAM_KMAX) * c->plan_of(fragment).tensors.size());
+        c->open.push_back(r);
+    } catch (...) {
+        delete r;
+        return fail(CAM_E_NOMEM, "cam_merge_begin: out of host memory");
+    }
+    c->last_round = round;
+    *out = r;
+    return CAM_OK;
+}
+
+CAM_API int cam_merge_accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype,
+                                 int64_t tokens) {
+    if (!r) return fail(CAM_E_ARG, "cam_merge_accumulate: round is NULL");
+    if (r->finalized) return fail(CAM_E_STATE, "cam_merge_accumulate: round already finalized");
+    if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "cam_merge_accumulate: more than %d workers", CAM_KMAX);
+    if (dtype != CAM_F32 && dtype != CAM_BF16)
+        return fail(CAM_E_ARG, "cam_merge_accumulate: unknown dtype %d", static_cast<int>(dtype));
+    if (r->K > 0 && dtype != r->dtype)
+        return fail(CAM_E_ARG, "cam_merge_accumulate: dtype %d differs from the round's %d",
+                    static_cast<int>(dtype), r->dtype);
+    if (tokens < 0 || tokens > (int64_t(1) << 56))
+        return fail(CAM_E_ARG, "cam_merge_accumulate: tokens %lld out of range",
+                    static_cast<long long>(tokens));
+    const Plan& p = r->ctx->plan_of(r->fragment);
+    if (!ckpt && p.n_tensors() > 0) return fail(CAM_E_ARG, "cam_merge_accumulate: ckpt is NULL");
+    for (int32_t l = 0; l < p.n_tensors(); ++l)
+        if (!ckpt[l] && r->ctx->numel[p.tensors[l]] > 0)
+            return fail(CAM_E_ARG, "cam_merge_accumulate: ckpt[%d] is NULL", l);
+    for (int32_t l = 0; l < p.n_tensors(); ++l) r->x.push_back(ckpt[l]);
+    r->tokens[r->K] = tokens;
+    r->dtype = dtype;
+    ++r->K;
+    return CAM_OK;
+}
+
+CAM_API int cam_merge_finalize(cam_round* r, cam_mode mode, float lr, float mu) {
+    if (!r) return fail(CAM_E_ARG, "cam_merge_finalize: round is NULL");
+    if (r->finalized) return fail(CAM_E_STATE, "cam_merge_finalize: finalized twice");
+    if (mode != CAM_MODE_MEAN_REPLACE && mode != CAM_MODE_DELTA_NESTEROV)
+        return fail(CAM_E_ARG, "cam_merge_finalize: unknown mode %d", static_cast<int>(mode));
+    if (!std::isfinite(lr) || !std::isfinite(mu))
+        return fail(CAM_E_ARG, "cam_merge_finalize: lr and mu must be finite");
+    if (mode == CAM_MODE_DELTA_NESTEROV && !r->ctx->has_m)
+        return fail(CAM_E_ARG, "cam_merge_finalize: Nesterov needs momentum buffers");
+    r->finalized = true;
+    r->mode = mode;
+    r->lr = lr;
+    r->mu = mu;
+    return CAM_OK;
+}
+
+CAM_API int cam_ema_update(cam_round* r, float beta) {
+    if (!r) return fail(CAM_E_ARG, "cam_ema_update: round is NULL");
+    if (r->ema) return fail(CAM_E_STATE, "cam_ema_update: asked twice");
+    if (!std::isfinite(beta)) return fail(CAM_E_ARG, "cam_ema_update: beta must be finite");
+    if (!r->ctx->has_e) return fail(CAM_E_ARG, "cam_ema_update: context has no EMA buffers");
+    r->ema = true;
+    r->beta = beta;
+    return CAM_OK;
+}
+
+CAM_API int cam_drift_norm(cam_round* r, double* per_tensor, double* per_fragment) {
+    if (!r) return fail(CAM_E_ARG, "cam_drift_norm: round is NULL");
+    if (r->norms) return fail(CAM_E_STATE, "cam_drift_norm: asked twice");
+    if (!per_tensor && !per_fragment) return fail(CAM_E_ARG, "cam_drift_norm: both outputs NULL");
+    r->norms = true;
+    r->out_tensor = per_tensor;
+    r->out_fragment = per_fragment;
+    return CAM_OK;
+}
+
+namespace {
+
+void close_round(cam_round* r) {
+    auto& open = r->ctx->open;
+    open.erase(std::remove(open.begin(), open.end(), r), open.end());
+    delete r;
+}
+
+}  // namespace
+
+CAM_API int cam_merge_abort(cam_round* r) {
+    if (!r) return fail(CAM_E_ARG, "cam_merge_abort: round is NULL");
+    close_round(r);
+    return CAM_OK;
+}
+
+CAM_API int cam_merge_commit(cam_round* r, void* stream) {
+    if (!r) return fail(CAM_E_ARG, "cam_merge_commit: round is NULL");
+    cam_ctx* c = r->ctx;
+    if (!r->finalized) return fail(CAM_E_STATE, "cam_merge_commit: round not finalized");
+    if (r->K < c->quorum)
+        return fail(CAM_E_QUORUM, "cam_merge_commit: %d participants < quorum %d", r->K, c->quorum);
+    if (r->K < 1) return fail(CAM_E_QUORUM, "cam_merge_commit: no participants");
+    int64_t W = 0;
+    for (int k = 0; k < r->K; ++k) W += r->tokens[k];
+    if (r->mode == CAM_MODE_DELTA_NESTEROV && W <= 0)
+        return fail(CAM_E_ARG, "cam_merge_commit: total token count must be > 0");
+
+    const Plan& p = c->plan_of(r->fragment);
+    const int K = r->K;
+    const int T = p.n_tensors();
+    const bool delta = r->mode == CAM_MODE_DELTA_NESTEROV;
+    const uintptr_t xa = r->dtype == CAM_F32 ? 32 : 16;
+    MergeArgs& a = *c->args;
+    a.slots = p.d_slots;
+    a.K = K;
+    a.Kf = static_cast<float>(K);
+    for (int k = 0; k < CAM_KMAX; ++k) a.w[k] = k < K ? static_cast<float>(r->tokens[k]) : 0.0f;
+    a.W = static_cast<float>(W);
+    a.lr = r->lr;
+    a.mu = r->mu;
+    a.beta = r->beta;
+    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    DeviceScope scope(c->device);
+    if (scope.err != cudaSuccess) {
+        close_round(r);
+        return cuda_fail(scope.err, "cam_merge_commit: cudaSetDevice");
+    }
+    cudaError_t ce = cudaSuccess;
+    const int per_launch = cam::kXCap / K;
+    for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += per_launch) {
+        const int n = std::min(per_launch, T - l0);
+        const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
+        if (c1 == c0) continue;
+        std::memset(a.vec, 0, sizeof a.vec);
+        for (int l = 0; l < n; ++l) {
+            const int32_t g = p.tensors[l0 + l];
+            bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
+                     (!r->ema || aligned(c->e[g], 32));
+            for (int k = 0; k < K; ++k) {
+                const void* xp = r->x[size_t(k) * T + l0 + l];
+                a.x[size_t(l) * K + k] = xp;
+                v = v && aligned(xp, xa);
+            }
+            if (v) a.vec[l >> 5] |= 1u << (l & 31);
+        }
+        a.chunks = p.d_chunks + c0;
+        a.partials = r->norms ? p.d_partials + c0 : nullptr;
+        a.n_chunks = c1 - c0;
+        a.local0 = l0;
+        a.n_local = n;
+        const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
+        ce = cam::launch_merge(a, r->dtype, r->mode, r->ema, r->norms, grid, s);
+        ++c->launches;
+    }
+    if (ce == cudaSuccess && r->norms) {
+        NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment};
+        ce = cam::launch_norm_finish(na, s);
+        ++c->launches;
+    }
+    close_round(r);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_commit: launch");
+    return CAM_OK;
+}
+
+CAM_API int cam_fragment_info(const cam_ctx* c, int32_t fragment, int32_t* n_tensors,
+                              int64_t* n_elems, int32_t* tensor_ids) {
+    if (!c) return fail(CAM_E_ARG, "cam_fragment_info: ctx is NULL");
+    if (fragment < -1 || fragment >= c->n_fragments)
+        return fail(CAM_E_ARG, "cam_fragment_info: fragment %d out of [-1, %d)", fragment, c->n_fragments);
+    const Plan& p = c->plan_of(fragment);
+    if (n_tensors) *n_tensors = p.n_tensors();
+    if (n_elems) *n_elems = p.n_elems;
+    if (tensor_ids && !p.tensors.empty())
+        std::memcpy(tensor_ids, p.tensors.data(), sizeof(int32_t) * p.tensors.size());
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_launch_count(const cam_ctx* c, int64_t* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_launch_count: NULL argument");
+    *out = c->launches;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_get_last_round(const cam_ctx* c, int64_t* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_get_last_round: NULL argument");
+    *out = c->last_round;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_set_last_round(cam_ctx* c, int64_t round) {
+    if (!c) return fail(CAM_E_ARG, "cam_ctx_set_last_round: ctx is NULL");
+    if (!c->open.empty()) return fail(CAM_E_STATE, "cam_ctx_set_last_round: a round is open");
+    if (round < c->last_round)
+        return fail(CAM_E_STALE, "cam_ctx_set_last_round: %lld would lower %lld",
+                    static_cast<long long>(round), static_cast<long long>(c->last_round));
+    c->last_round = round;
+    return CAM_OK;
+}

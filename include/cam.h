@@ -1,0 +1,208 @@
+/*
+ * cam.h -- C ABI of libcam, the GB300 DiLoCo outer-merge library.
+ *
+ * One merge round takes the round's worker checkpoints and moves the global
+ * model (fp32 master weights theta) one outer step:
+ *
+ *   - plain replacement: theta' = mean of the workers, folded into a running
+ *     fp32 sum in arrival order ("DiffuRefill-1B" model card, "How it is
+ *     trained", Merging; "DiffuRefill-1B: Pretraining a Masked Diffusion
+ *     Language Model on Free, Preemptible Notebook GPUs", section 3, Table 2,
+ *     "Outer step": outer learning rate 1, no momentum);
+ *   - outer Nesterov on the token-weighted mean of the deltas
+ *     ("Pythia-14M on four rented GPUs and a bucket", "Getting updates through
+ *     the bucket": learning rate 0.7, momentum 0.9);
+ *
+ * then optionally updates the EMA of the globals (same report, Table 2, "Side
+ * averages", beta 0.9) and reports L2 drift norms. A round may be restricted to
+ * one of F parameter fragments and closes only with a quorum of participants
+ * (Pythia page, same section: fragments=4, quorum_size=3; two rounds may be in
+ * flight at once).
+ *
+ * Element arithmetic (fixed, so results are reproducible bit for bit): every
+ * operation is one IEEE binary32 operation rounded to nearest-even, no fused
+ * multiply-add, correctly rounded division. With x_k the k-th accumulated
+ * worker's value widened to fp32 (bf16 widening is exact), in accumulate-call
+ * order k = 1..K:
+ *   MEAN_REPLACE:    s = sum_k x_k;  theta' = s / K
+ *   DELTA_NESTEROV:  s = sum_k w_k * (x_k - theta);  Delta = s / W,
+ *                    w_k = (float)tokens_k, W = (float)(sum_k tokens_k);
+ *                    g = -Delta;  m' = mu*m + g;  theta' = theta - lr*(g + mu*m')
+ *   EMA:             e' = beta*e + (1 - beta)*theta'
+ *   drift norm:      per tensor sqrt(sum_i delta_i^2), delta = Delta (DELTA mode)
+ *                    or theta' - theta (MEAN mode), squares summed in fp64 in a
+ *                    fixed order; per fragment sqrt(sum over its tensors).
+ *
+ * Conventions:
+ *   - Every call returns CAM_OK (0) or a negative cam_status. On any error the
+ *     library state is unchanged unless the call's comment says otherwise, and
+ *     cam_last_error() returns a message for the calling thread.
+ *   - "device pointer" means memory on the context's CUDA device; "host
+ *     pointer" means ordinary CPU memory read during the call only.
+ *   - All device work is stream-ordered on the stream passed to
+ *     cam_merge_commit; nothing in this library synchronises the device.
+ *   - Not thread-safe per context: calls on one context must not overlap.
+ */
+#ifndef CAM_H
+#define CAM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CAM_KMAX 8            /* most workers one round may accumulate */
+#define CAM_MAX_OPEN_ROUNDS 8 /* rounds begun and not yet committed, per context */
+
+typedef enum {
+    CAM_OK = 0,
+    CAM_E_ARG = -1,    /* null/invalid argument, size or dtype mismatch, non-finite scalar */
+    CAM_E_STATE = -2,  /* call out of order (e.g. commit before finalize) */
+    CAM_E_STALE = -3,  /* round number not newer than every round already begun */
+    CAM_E_BUSY = -4,   /* the fragment overlaps a round that is open */
+    CAM_E_QUORUM = -5, /* fewer accumulated workers than the quorum */
+    CAM_E_KMAX = -6,   /* more than CAM_KMAX accumulate calls */
+    CAM_E_CUDA = -7,   /* a CUDA call failed (no device, launch error, ...) */
+    CAM_E_NOMEM = -8   /* host or device allocation failed */
+} cam_status;
+
+typedef enum { CAM_F32 = 0, CAM_BF16 = 1 } cam_dtype;
+
+typedef enum {
+    CAM_MODE_MEAN_REPLACE = 0,   /* plain mean, plain replacement */
+    CAM_MODE_DELTA_NESTEROV = 1  /* token-weighted delta mean, outer Nesterov */
+} cam_mode;
+
+/* cam_ctx_desc.flags */
+#define CAM_INIT_EMA_FROM_MASTER 1u /* at create: e <- theta (EMA starts at the first global) */
+#define CAM_INIT_ZERO_MOMENTUM 2u   /* at create: m <- 0 */
+
+typedef struct cam_ctx cam_ctx;     /* opaque */
+typedef struct cam_round cam_round; /* opaque */
+
+/*
+ * The merger's parameter list. Tensor t has numel[t] fp32 elements at
+ * master[t] (theta), momentum[t] (m) and ema[t] (e); each is a contiguous
+ * device buffer owned by the caller for the life of the context. momentum may
+ * be NULL (Nesterov rounds are then rejected) and so may ema (ema_update is
+ * then rejected). fragment_of[t] in [0, n_fragments) assigns tensors to
+ * fragments (NULL: every tensor in fragment 0). A fragment's tensors are
+ * always taken in increasing t: that is the "fragment order" of every
+ * per-tensor array below. numel[t] may be 0. Buffers need no particular
+ * alignment; 32-byte aligned buffers take the vectorised path.
+ */
+typedef struct {
+    int32_t n_tensors;
+    const int64_t* numel;       /* host, [n_tensors] */
+    const int32_t* fragment_of; /* host, [n_tensors] or NULL */
+    int32_t n_fragments;        /* >= 1 */
+    int32_t quorum;             /* >= 1: accumulate calls needed to commit */
+    float* const* master;       /* host array of n_tensors device pointers */
+    float* const* momentum;     /* host array of n_tensors device pointers, or NULL */
+    float* const* ema;          /* host array of n_tensors device pointers, or NULL */
+    int32_t device;             /* CUDA device ordinal holding the buffers */
+    uint32_t flags;             /* CAM_INIT_* */
+    void* stream;               /* cudaStream_t for the CAM_INIT_* work; NULL = default */
+} cam_ctx_desc;
+
+/*
+ * Creates a context: validates the description, plans the chunking of every
+ * fragment for the device, allocates the library's small device tables and
+ * runs the CAM_INIT_* work on desc->stream. Copies every host array it reads.
+ * Errors: CAM_E_ARG (invalid description, checked before any CUDA call),
+ * CAM_E_CUDA (no usable device), CAM_E_NOMEM.
+ */
+int cam_ctx_create(const cam_ctx_desc* desc, cam_ctx** out);
+
+/* Frees the context and every round still open on it. The caller makes sure
+ * no committed work of the context is still running on the device. NULL is a
+ * no-op. */
+void cam_ctx_destroy(cam_ctx* ctx);
+
+/*
+ * Opens round `round` on `fragment` (or -1: every tensor). Round numbers must
+ * strictly increase over the context's life, so a republished global always
+ * carries a new number ("DiffuRefill-1B" technical report, section 3,
+ * "Failure handling" (iii)). Errors: CAM_E_ARG (fragment out of range),
+ * CAM_E_STALE (round not above every round begun so far), CAM_E_BUSY (an open
+ * round covers an overlapping fragment), CAM_E_NOMEM.
+ */
+int cam_merge_begin(cam_ctx* ctx, int64_t round, int32_t fragment, cam_round** out);
+
+/*
+ * Adds one worker to the round, in arrival order. ckpt is a host array of
+ * T_f device pointers, the worker's copy of each tensor of the fragment in
+ * fragment order (each numel[t] contiguous elements of `dtype`). tokens is
+ * the worker's token count (>= 0; used as its weight in DELTA_NESTEROV mode,
+ * ignored in MEAN_REPLACE). The buffers are BORROWED: they must stay valid
+ * and unmodified until the committed work has run on the commit stream.
+ * Every accumulate of one round must use the same dtype.
+ * Errors: CAM_E_ARG, CAM_E_STATE (already finalized), CAM_E_KMAX.
+ */
+int cam_merge_accumulate(cam_round* rd, const void* const* ckpt, cam_dtype dtype,
+                         int64_t tokens);
+
+/*
+ * Chooses the outer step. MEAN_REPLACE ignores lr, mu and the token counts.
+ * DELTA_NESTEROV needs momentum buffers. lr and mu must be finite.
+ * Errors: CAM_E_ARG, CAM_E_STATE (finalized twice).
+ */
+int cam_merge_finalize(cam_round* rd, cam_mode mode, float lr, float mu);
+
+/*
+ * Asks for the EMA update e' = beta*e + (1-beta)*theta' on the round's
+ * tensors, fused into the same pass. beta must be finite. Needs EMA buffers.
+ * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
+ */
+int cam_ema_update(cam_round* rd, float beta);
+
+/*
+ * Asks for drift norms, written on the commit stream: per_tensor[T_f] (device
+ * pointer, fragment order) and per_fragment[1] (device pointer); either may be
+ * NULL but not both. Local drift is the workers' movement away from the last
+ * global ("DiffuRefill-1B" technical report, section 5.1). Errors: CAM_E_ARG,
+ * CAM_E_STATE (asked twice).
+ */
+int cam_drift_norm(cam_round* rd, double* per_tensor, double* per_fragment);
+
+/*
+ * Closes the round: checks it (finalized, quorum met, weights valid), then
+ * launches the fused merge pass (and the norm pass if asked) on `stream`
+ * (a cudaStream_t; NULL = legacy default stream) and frees the round handle.
+ * Returns before the device work finishes. On CAM_E_STATE / CAM_E_QUORUM /
+ * CAM_E_ARG nothing is launched and the round stays open. On CAM_E_CUDA the
+ * round is freed and the fragment's buffers are undefined.
+ */
+int cam_merge_commit(cam_round* rd, void* stream);
+
+/* Drops an open round without touching any buffer. The round number stays
+ * used. */
+int cam_merge_abort(cam_round* rd);
+
+/* Number of tensors and elements of `fragment` (-1: all), and its tensor
+ * indices in fragment order when `tensor_ids` (host, [T_f]) is not NULL. */
+int cam_fragment_info(const cam_ctx* ctx, int32_t fragment, int32_t* n_tensors,
+                      int64_t* n_elems, int32_t* tensor_ids);
+
+/* Highest round number begun so far (-1 before the first), and restoring it
+ * when a merger restarts from saved state. set fails with CAM_E_STATE while a
+ * round is open and with CAM_E_STALE when it would lower the number. */
+int cam_ctx_get_last_round(const cam_ctx* ctx, int64_t* out);
+int cam_ctx_set_last_round(cam_ctx* ctx, int64_t round);
+
+/* Kernels this context has launched so far (merge passes, norm passes and
+ * the CAM_INIT_* work), for accounting what a timed region ran. */
+int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
+
+/* Message describing the calling thread's last error ("" if none). */
+const char* cam_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* cam_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAM_H */

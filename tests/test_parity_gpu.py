@@ -1,0 +1,431 @@
+"""GPU parity: libcam's fused merge pass against the CPU oracle, through the C ABI.
+
+Workloads are the five synthetic configurations (Pythia-14M fragments with a
+quorum and Nesterov; the 63M stand with plain mean + EMA over 10 rounds; the
+1.08B list in fp32 with plain mean + EMA; the 1.08B list with bf16 workers,
+fragments, quorum, Nesterov, norms and two rounds in flight; ragged sweeps up
+to 4e9 parameters) plus edge cases: ragged and empty tensors, misaligned
+views, K = 1 and K = KMAX, many tensors per round, the round state machine.
+Tolerance per fp32 element: |gpu - oracle| <= 1e-7 + 2e-6 |oracle|; drift
+norms within 1e-5 relative.
+"""
+import gc
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from checkpoint_averaging_gb300 import binding as B
+from checkpoint_averaging_gb300 import workloads as W
+
+from merge_harness import (assert_close, bitwise_equal, compare_full, gather_state,
+                           gpu_round, make_gpu_state, oracle_round, oracle_state_from,
+                           run_full, sample_indices, sampled_round_check, to_np,
+                           full_tensor_norm, NORM_RTOL)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _cuda_cleanup():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    yield
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+# ---- the five workloads ----------------------------------------------------------
+
+def test_pythia14m_fragments_quorum_nesterov_full():
+    run_full(W.workload("pythia14m"))
+
+
+def test_stand_mean_ema_ten_rounds_full():
+    run_full(W.workload("stand"))
+
+
+def test_small_workloads_bitwise_equal_to_oracle():
+    # The fixed op sequence makes GPU and oracle agree bit for bit, not only
+    # within tolerance.
+    run_full(W.workload("pythia14m"), seed=3, bitwise=True)
+    wl = W.workload("stand")
+    run_full(W.Workload(wl.name, wl.specs, 1, K=5, n_masked=0, quorum=5, ckpt_dtype="f32",
+                        mode="mean", ema_beta=0.9, rounds=((0, -1), (1, -1)), noise_std=2e-3,
+                        workers_track_global=True), seed=4, bitwise=True)
+
+
+def _sampled_workload(wl, seed=0, per_tensor=4096, norm_tensors=()):
+    g = W.make_global(wl, seed, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    rng = np.random.default_rng(seed)
+    for idx, (rnd, frag) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, seed)
+        workers = [W.make_worker(wl, g, rnd, k, seed, DEV) for k in range(wl.K)]
+        tensors = [t for t in range(len(wl.specs)) if frag == -1 or wl.specs[t].fragment == frag]
+        idxs = [sample_indices(wl.specs[t].numel, per_tensor, rng) for t in tensors]
+        before = gather_state(st, tensors, idxs)
+        full_before = {t: to_np(st.theta.views[t]).copy() for t in norm_tensors if t in tensors}
+        gn = gpu_round(st, wl, rnd, frag, workers, draw)
+        torch.cuda.synchronize()
+        sampled_round_check(wl, st, frag, workers, draw, idxs, before, f"{wl.name} round {rnd}")
+        if gn is not None:
+            pt = gn[0].cpu().numpy()[:len(tensors)]
+            pf = gn[1].item()
+            assert (pt >= 0).all()
+            assert abs(math.sqrt(float(np.sum(pt.astype(np.float64) ** 2))) - pf) <= 1e-9 * pf
+            for t, th0 in full_before.items():
+                want = full_tensor_norm(wl, workers, draw, th0, t)
+                got = pt[tensors.index(t)]
+                assert abs(got - want) <= NORM_RTOL * want, f"norm of tensor {t}: {got} vs {want}"
+        del workers
+    st.merger.close()
+
+
+def test_diffurefill1b_f32_mean_ema_sampled():
+    _sampled_workload(W.workload("diffurefill1b"))
+
+
+def test_diffurefill1b_bf16_fragments_nesterov_norms_sampled():
+    # last fragment includes the final norm; tensor 0 is the 151M embedding
+    _sampled_workload(W.workload("diffurefill1b_bf16"), norm_tensors=(0, 8, 9, 10, 18))
+
+
+def test_diffurefill1b_bf16_two_rounds_in_flight_equal_sequential():
+    """Rounds 0 and 1 (fragments 0 and 1) committed on two streams before any
+    synchronisation give the same bits as committing them one after another,
+    and match the oracle on sampled elements."""
+    wl = W.workload("diffurefill1b_bf16")
+    g = W.make_global(wl, 0, DEV)
+    draws = [W.draw_round(wl, i, 0) for i in range(2)]
+    workers = [[W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)]
+               for rnd, _ in wl.rounds]
+    rng = np.random.default_rng(5)
+    frag_tensors = [[t for t in range(len(wl.specs)) if wl.specs[t].fragment == f]
+                    for _, f in wl.rounds]
+    idxs = [[sample_indices(wl.specs[t].numel, 2048, rng) for t in ts] for ts in frag_tensors]
+
+    par = make_gpu_state(wl, g, DEV)
+    befores = [gather_state(par, ts, ix) for ts, ix in zip(frag_tensors, idxs)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    s1.wait_stream(cur)
+    s2.wait_stream(cur)
+    norms_par = []
+    for (rnd, frag), w, d, s in zip(wl.rounds, workers, draws, (s1, s2)):
+        with torch.cuda.stream(s):
+            norms_par.append(gpu_round(par, wl, rnd, frag, w, d, stream=s))
+    cur.wait_stream(s1)
+    cur.wait_stream(s2)
+    torch.cuda.synchronize()
+    for (rnd, frag), w, d, ix, bf in zip(wl.rounds, workers, draws, idxs, befores):
+        sampled_round_check(wl, par, frag, w, d, ix, bf, f"in flight round {rnd}")
+
+    seq = make_gpu_state(wl, g, DEV)
+    norms_seq = [gpu_round(seq, wl, rnd, frag, w, d)
+                 for (rnd, frag), w, d in zip(wl.rounds, workers, draws)]
+    torch.cuda.synchronize()
+    assert torch.equal(par.theta.flat.view(torch.int32), seq.theta.flat.view(torch.int32))
+    assert torch.equal(par.m.flat.view(torch.int32), seq.m.flat.view(torch.int32))
+    for a, b in zip(norms_par, norms_seq):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    par.merger.close()
+    seq.merger.close()
+
+
+@pytest.mark.parametrize("K", [2, 4, 8])
+def test_sweep_16m_full(K):
+    run_full(W.sweep_workload(64, 16_000_000, K))
+
+
+@pytest.mark.parametrize("t,n,K", [(128, 256_000_000, 4), (256, 1_000_000_000, 4),
+                                   (512, 4_000_000_000, 8)])
+def test_sweep_large_sampled(t, n, K):
+    _sampled_workload(W.sweep_workload(t, n, K), per_tensor=1024)
+
+
+# ---- edge cases ------------------------------------------------------------------
+
+RAGGED = [1, 2, 7, 8, 9, 15, 0, 2047, 2048, 2049, 16383, 16384, 16385, 100_003, 3]
+
+
+def _custom(sizes, *, K, mode="delta", dtype="f32", ema=True, frags=None, n_fragments=1,
+            rounds=((0, -1),), n_masked=0, quorum=None, tokens=(100_000, 150_000), norms=True):
+    frags = frags or [0] * len(sizes)
+    specs = tuple(W.TensorSpec(f"t{i}", (n,), f) for i, (n, f) in enumerate(zip(sizes, frags)))
+    return W.Workload("custom", specs, n_fragments, K=K, n_masked=n_masked,
+                      quorum=quorum or (K - n_masked), ckpt_dtype=dtype, mode=mode,
+                      lr=0.7 if mode == "delta" else 1.0, mu=0.9 if mode == "delta" else 0.0,
+                      ema_beta=0.9 if ema else None, rounds=rounds,
+                      tokens=tokens if mode == "delta" else None, norms=norms)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["mean", "delta"])
+def test_ragged_and_empty_tensors(dtype, mode):
+    run_full(_custom(RAGGED, K=3, mode=mode, dtype=dtype), seed=7)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_k1_replacement_returns_input_bitwise(dtype):
+    wl = _custom([4099, 65536], K=1, mode="mean", dtype=dtype, ema=False, norms=False)
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    w = [W.make_worker(wl, g, 0, 0, 0, DEV)]
+    gpu_round(st, wl, 0, -1, w, W.RoundDraw(0, -1, [0], [0]))
+    torch.cuda.synchronize()
+    for t in range(2):
+        assert torch.equal(st.theta.views[t].view(torch.int32),
+                           w[0].views[t].float().view(torch.int32))
+    st.merger.close()
+
+
+def test_kmax_workers_and_one_more_rejected():
+    wl = _custom([5000, 33], K=8)
+    run_full(wl, seed=8)
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    w = W.make_worker(wl, g, 0, 0, 0, DEV)
+    rd = st.merger.begin(0)
+    for _ in range(8):
+        rd.accumulate(w.views, 1)
+    with pytest.raises(B.KmaxError):
+        rd.accumulate(w.views, 1)
+    rd.abort()
+    st.merger.close()
+
+
+def test_many_tensors_split_over_launches():
+    # 1000 tensors with K = 8 exceed one launch's pointer block (3520 pointers)
+    sizes = [(i * 37) % 300 + 1 for i in range(1000)]
+    run_full(_custom(sizes, K=8, mode="delta", dtype="bf16"), seed=9)
+
+
+def test_empty_fragment_and_zero_size_tensors():
+    sizes = [0, 0, 5000, 0]
+    frags = [0, 0, 1, 2]   # fragment 0 has only empty tensors, fragment 3 has none
+    wl = _custom(sizes, K=2, frags=frags, n_fragments=4,
+                 rounds=((0, 0), (1, 3), (2, 1), (3, 2)))
+    run_full(wl, seed=10)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_misaligned_views_take_the_scalar_path(dtype):
+    """Tensors viewed at odd element offsets (not 16/32-byte aligned)."""
+    sizes = [1001, 4096, 77]
+    wl = _custom(sizes, K=3, dtype=dtype)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    g = W.make_global(wl, 0, DEV)
+
+    def shifted(src_views, dtype_):
+        views = []
+        for v in src_views:
+            buf = torch.empty(v.numel() + 1, dtype=dtype_, device=DEV)
+            buf[1:].copy_(v)
+            views.append(buf[1:])
+        return views
+
+    theta = shifted(g.views, torch.float32)
+    m = shifted([torch.zeros_like(v) for v in g.views], torch.float32)
+    e = shifted(g.views, torch.float32)
+    mg = B.Merger(theta, momentum=m, ema=e, quorum=3)
+    ost = oracle_state_from(g, wl)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(3)]
+    xw = [shifted(w.views, dt) for w in workers]
+    rd = mg.begin(0)
+    for k in draw.included:
+        rd.accumulate(xw[k], draw.tokens[k])
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.ema_update(0.9)
+    rd.commit()
+    oracle_round(ost, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    for t in range(3):
+        assert_close(to_np(theta[t]), ost.theta[t], f"theta[{t}]")
+        assert_close(to_np(m[t]), ost.m[t], f"m[{t}]")
+        assert_close(to_np(e[t]), ost.e[t], f"e[{t}]")
+    mg.close()
+
+
+def test_large_token_counts_round_like_the_oracle():
+    # counts above 2**24 are not exact in fp32: both sides round them the same way
+    wl = _custom([3000, 129], K=3, tokens=(2**24 + 1, 2**26 + 7))
+    run_full(wl, seed=11, bitwise=True)
+
+
+def test_lr1_mu0_delta_is_token_weighted_mean():
+    wl = _custom([4096, 999], K=4, ema=False)
+    wl = W.Workload(wl.name, wl.specs, 1, K=4, n_masked=0, quorum=4, ckpt_dtype="f32",
+                    mode="delta", lr=1.0, mu=0.0, tokens=(100_000, 150_000))
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(4)]
+    gpu_round(st, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    Wt = sum(draw.tokens[k] for k in draw.included)
+    u = 2.0 ** -24
+    for t in range(2):
+        th0 = g.views[t].double()
+        want = sum(draw.tokens[k] * workers[k].views[t].double() for k in draw.included) / Wt
+        dmag = torch.stack([(workers[k].views[t].double() - th0).abs()
+                            for k in draw.included]).max(0).values
+        got = st.theta.views[t].double()
+        # fp32 error bound of theta - 1*(-Delta) with Delta a 4-term weighted sum
+        assert ((got - want).abs() <= 4 * u * (th0.abs() + 8 * dmag) + 1e-12).all()
+    st.merger.close()
+
+
+def test_determinism_repeat_is_bitwise_identical():
+    wl = W.workload("pythia14m")
+    runs = []
+    for _ in range(2):
+        g = W.make_global(wl, 0, DEV)
+        st = make_gpu_state(wl, g, DEV)
+        norms = []
+        for idx, (rnd, frag) in enumerate(wl.rounds):
+            draw = W.draw_round(wl, idx, 0)
+            workers = [W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)]
+            pt, pf = gpu_round(st, wl, rnd, frag, workers, draw)
+            norms.append((pt.clone(), pf.clone()))
+        torch.cuda.synchronize()
+        runs.append((st.theta.flat.clone(), st.m.flat.clone(), norms))
+        st.merger.close()
+    (a_th, a_m, a_n), (b_th, b_m, b_n) = runs
+    assert torch.equal(a_th.view(torch.int32), b_th.view(torch.int32))
+    assert torch.equal(a_m.view(torch.int32), b_m.view(torch.int32))
+    for (x1, y1), (x2, y2) in zip(a_n, b_n):
+        assert torch.equal(x1, x2) and torch.equal(y1, y2)
+
+
+def test_masked_worker_is_never_read():
+    wl = _custom([3000, 17], K=4, n_masked=1, quorum=3)
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    masked = [k for k in range(4) if k not in draw.included][0]
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(4)]
+    workers[masked].flat.fill_(float("nan"))
+    gpu_round(st, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    assert torch.isfinite(st.theta.flat).all() and torch.isfinite(st.e.flat).all()
+    st.merger.close()
+
+
+# ---- the round state machine -----------------------------------------------------
+
+def _tiny_merger(n_fragments=2, quorum=2):
+    th = [torch.zeros(100, device=DEV), torch.zeros(50, device=DEV)]
+    m = [torch.zeros_like(t) for t in th]
+    e = [torch.zeros_like(t) for t in th]
+    return B.Merger(th, momentum=m, ema=e, fragment_of=[0, n_fragments - 1],
+                    n_fragments=n_fragments, quorum=quorum), th
+
+
+def test_quorum_stale_busy_and_order_errors():
+    mg, th = _tiny_merger()
+    x = [torch.ones(100, device=DEV)]
+    rd = mg.begin(5, 0)
+    with pytest.raises(B.BusyError):
+        mg.begin(6, 0)            # same fragment open
+    with pytest.raises(B.BusyError):
+        mg.begin(6, -1)           # "all" overlaps
+    rd2 = mg.begin(7, 1)          # disjoint fragment: fine (two rounds in flight)
+    with pytest.raises(B.StaleRoundError):
+        B.merge_begin(mg.ctx, 6, 1)   # not newer than round 7
+    rd.accumulate(x, 10)
+    with pytest.raises(B.StateError):
+        rd.commit()               # not finalized
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    with pytest.raises(B.StateError):
+        rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    with pytest.raises(B.StateError):
+        rd.accumulate(x, 10)      # after finalize
+    with pytest.raises(B.QuorumError):
+        rd.commit()               # 1 < quorum 2; round stays open
+    assert torch.count_nonzero(th[0]) == 0
+    rd2.abort()
+    rd.abort()
+    rd = mg.begin(8, 0)
+    rd.accumulate(x, 10)
+    rd.accumulate(x, 30)
+    rd.finalize(B.DELTA_NESTEROV, 1.0, 0.0)
+    rd.commit()
+    torch.cuda.synchronize()
+    assert torch.allclose(th[0], torch.ones(100, device=DEV))
+    assert mg.last_round == 8
+    with pytest.raises(B.StaleRoundError):
+        mg.last_round = 3
+    mg.last_round = 20
+    with pytest.raises(B.StaleRoundError):
+        mg.begin(20, 0)
+    mg.close()
+
+
+def test_argument_errors():
+    mg, th = _tiny_merger()
+    rd = mg.begin(0, 0)
+    with pytest.raises(ValueError):
+        rd.accumulate([torch.ones(99, device=DEV)], 1)            # wrong size
+    rd.accumulate([torch.ones(100, device=DEV)], 1)
+    with pytest.raises(ValueError):
+        rd.accumulate([torch.ones(100, device=DEV, dtype=torch.bfloat16)], 1)
+    with pytest.raises(B.ArgError):                               # mixed dtype at the ABI
+        B.merge_accumulate(rd.handle, [torch.ones(100, device=DEV, dtype=torch.bfloat16).data_ptr()], B.BF16, 1)
+    with pytest.raises(B.ArgError):
+        B.merge_accumulate(rd.handle, [0], B.F32, 1)              # null pointer
+    with pytest.raises(B.ArgError):
+        rd.accumulate([torch.ones(100, device=DEV)], -5)          # negative tokens
+    with pytest.raises(B.ArgError):
+        rd.finalize(B.DELTA_NESTEROV, float("nan"), 0.9)
+    with pytest.raises(B.ArgError):
+        rd.ema_update(float("inf"))
+    rd.accumulate([torch.ones(100, device=DEV)], 0)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.abort()
+    rd = mg.begin(1, 0)
+    rd.accumulate([torch.ones(100, device=DEV)], 0)
+    rd.accumulate([torch.ones(100, device=DEV)], 0)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    with pytest.raises(B.ArgError):
+        rd.commit()                                               # zero total weight
+    rd.abort()
+    with pytest.raises(B.ArgError):
+        mg.begin(2, 5)                                            # no such fragment
+    mg.close()
+
+
+def test_resume_after_restart_is_bitwise_identical():
+    """A merger killed between rounds and restarted from its saved theta, m, e
+    and round counter continues exactly as an uninterrupted one."""
+    wl = W.workload("pythia14m")
+    g = W.make_global(wl, 0, DEV)
+    draws = [W.draw_round(wl, i, 0) for i in range(3)]
+    workers = [[W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)] for rnd, _ in wl.rounds]
+    a = make_gpu_state(wl, g, DEV)
+    for (rnd, frag), w, d in zip(wl.rounds, workers, draws):
+        gpu_round(a, wl, rnd, frag, w, d)
+    b = make_gpu_state(wl, g, DEV)
+    gpu_round(b, wl, 0, 0, workers[0], draws[0])
+    torch.cuda.synchronize()
+    saved = (b.theta.flat.cpu(), b.m.flat.cpu(), b.merger.last_round)
+    b.merger.close()
+    c = make_gpu_state(wl, g, DEV)          # "restarted process"
+    c.theta.flat.copy_(saved[0])
+    c.m.flat.copy_(saved[1])
+    c.merger.last_round = saved[2]
+    with pytest.raises(B.StaleRoundError):
+        c.merger.begin(0, 0)                # the old round number is refused
+    for (rnd, frag), w, d in list(zip(wl.rounds, workers, draws))[1:]:
+        gpu_round(c, wl, rnd, frag, w, d)
+    torch.cuda.synchronize()
+    assert torch.equal(a.theta.flat.view(torch.int32), c.theta.flat.view(torch.int32))
+    assert torch.equal(a.m.flat.view(torch.int32), c.m.flat.view(torch.int32))
+    a.merger.close()
+    c.merger.close()
