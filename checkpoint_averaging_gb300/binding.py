@@ -87,7 +87,11 @@ _lib = None
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
-           "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_last_error", "cam_version")
+           "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_merge_round_noalloc",
+           "cam_last_error", "cam_version")
+
+NOALLOC_MAX_TENSORS = 4096
+NOALLOC_MAX_CHUNKS = 131072
 
 
 def lib() -> ctypes.CDLL:
@@ -117,6 +121,10 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_get_last_round.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_ctx_set_last_round.argtypes = [vp, i64]
     L.cam_ctx_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_merge_round_noalloc.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, i32, vpp,
+                                          ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int,
+                                          ctypes.c_float, ctypes.c_float, i32, ctypes.c_float,
+                                          vp, vp, vp]
     L.cam_last_error.argtypes = []
     L.cam_last_error.restype = ctypes.c_char_p
     L.cam_version.argtypes = []
@@ -227,6 +235,34 @@ def ctx_launch_count(ctx: int) -> int:
     out = ctypes.c_int64()
     _check(lib().cam_ctx_launch_count(ctx, ctypes.byref(out)))
     return out.value
+
+
+def merge_round_noalloc(numel: Sequence[int], master: Sequence[int], ckpt: Sequence[Sequence[int]],
+                        dtype: int, mode: int, *, tokens: Sequence[int] | None = None,
+                        lr: float = 1.0, mu: float = 0.0, momentum: Sequence[int] | None = None,
+                        ema: Sequence[int] | None = None, beta: float = 0.9,
+                        per_tensor: int | None = None, per_round: int | None = None,
+                        stream: int = 0) -> None:
+    """One whole round through cam_merge_round_noalloc, the entry point that
+    allocates nothing (for callers that may not allocate device memory).
+    ckpt[k][t] is worker k's device pointer for tensor t, in arrival order.
+    The EMA is updated when `ema` is given."""
+    n = len(numel)
+    K = len(ckpt)
+    numel_a = (ctypes.c_int64 * max(1, n))(*[int(v) for v in numel])
+    flat = [int(p) for w in ckpt for p in w]
+    if len(flat) != K * n:
+        raise ValueError("ckpt must hold one pointer per tensor per worker")
+    tok = None if tokens is None else (ctypes.c_int64 * max(1, K))(*[int(t) for t in tokens])
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+
+    def arr(v):
+        return None if v is None else ctypes.cast(_ptrs(v), vpp)
+
+    keep = [arr(master), arr(momentum), arr(ema), arr(flat)]
+    _check(lib().cam_merge_round_noalloc(
+        n, numel_a, keep[0], keep[1], keep[2], K, keep[3], dtype, tok, mode, lr, mu,
+        int(ema is not None), beta, per_tensor or None, per_round or None, stream or None))
 
 
 # ---- torch-facing layer ----------------------------------------------------------

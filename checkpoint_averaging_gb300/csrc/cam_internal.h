@@ -71,6 +71,10 @@ struct NormArgs {
 
 enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 
+// Records a message for the calling thread (returned by cam_last_error) and
+// returns `code`.
+int record_error(int code, const char* fmt, ...);
+
 // Launches one fused merge pass with `grid` blocks.
 cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm,
                          int grid, cudaStream_t s);

@@ -27,160 +27,12 @@
 #include <cuda_runtime.h>
 
 #include "cam_internal.h"
+#include "merge_device.cuh"
 
 namespace cam {
 namespace {
 
-constexpr int kMean = CAM_MODE_MEAN_REPLACE;
-constexpr int kDelta = CAM_MODE_DELTA_NESTEROV;
-
-// ---- memory access -----------------------------------------------------------
-
-// Worker data: read once, never written by this pass. XVec<T> holds one
-// thread's 8 consecutive elements of one worker as loaded (fp32 values, or
-// bf16 pairs packed in 32-bit words) and widens on access; bf16 is the high
-// half of a binary32, so widening is exact.
-template <typename XT>
-struct XVec;
-
-template <>
-struct XVec<float> {
-    float v[8];
-    __device__ __forceinline__ void load(const float* p) {
-        asm volatile(
-            "ld.global.nc.L1::no_allocate.L2::evict_first.v8.f32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-            : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
-              "=f"(v[6]), "=f"(v[7])
-            : "l"(p));
-    }
-    __device__ __forceinline__ float get(int j) const { return v[j]; }
-};
-
-template <>
-struct XVec<uint16_t> {
-    uint32_t u[4];
-    __device__ __forceinline__ void load(const uint16_t* p) {
-        asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
-                     : "l"(p));
-    }
-    __device__ __forceinline__ float get(int j) const {
-        const uint32_t w = u[j >> 1];
-        return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
-    }
-};
-
-__device__ __forceinline__ float load_x1(const float* p) {
-    float v;
-    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float load_x1(const uint16_t* p) {
-    unsigned short b;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(b) : "l"(p));
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-// State (theta, m, e): read once and written back by the same thread.
-__device__ __forceinline__ void load_s8(const float* p, float (&v)[8]) {
-    asm volatile(
-        "ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
-          "=f"(v[6]), "=f"(v[7])
-        : "l"(p));
-}
-
-__device__ __forceinline__ void store_s8(float* p, const float (&v)[8]) {
-    asm volatile(
-        "st.global.L1::no_allocate.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
-        "f"(v[7])
-        : "memory");
-}
-
-// ---- per-element arithmetic ----------------------------------------------------
-
-// One element of one round. xk[k] (k < K) are the workers' values in arrival
-// order; th, m, e are updated in place; acc collects the squared drift.
-template <int MODE, bool EMA, bool NORM>
-__device__ __forceinline__ void merge_elem(const MergeArgs& a, const float (&xk)[CAM_KMAX],
-                                           float& th, float& m, float& e, float& acc) {
-    if (MODE == kMean) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k)
-            if (k < a.K) s = __fadd_rn(s, xk[k]);
-        const float mean = __fdiv_rn(s, a.Kf);
-        if (NORM) {
-            const float d = __fsub_rn(mean, th);
-            acc = __fmaf_rn(d, d, acc);
-        }
-        th = mean;  // plain replacement
-    } else {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k)
-            if (k < a.K) s = __fadd_rn(s, __fmul_rn(a.w[k], __fsub_rn(xk[k], th)));
-        const float delta = __fdiv_rn(s, a.W);
-        if (NORM) acc = __fmaf_rn(delta, delta, acc);
-        const float g = -delta;  // pseudo-gradient theta - (theta + delta)
-        const float m_new = __fadd_rn(__fmul_rn(a.mu, m), g);
-        const float step = __fadd_rn(g, __fmul_rn(a.mu, m_new));
-        th = __fsub_rn(th, __fmul_rn(a.lr, step));
-        m = m_new;
-    }
-    if (EMA) {
-        const float omb = __fsub_rn(1.0f, a.beta);
-        e = __fadd_rn(__fmul_rn(a.beta, e), __fmul_rn(omb, th));
-    }
-}
-
-template <typename XT, int MODE, bool EMA, bool NORM>
-__device__ __forceinline__ void merge_vec8(const MergeArgs& a, const void* const* xs,
-                                           const TensorSlot& ts, int64_t i, float& acc) {
-    XVec<XT> x[CAM_KMAX];
-#pragma unroll
-    for (int k = 0; k < CAM_KMAX; ++k)
-        if (k < a.K) x[k].load(static_cast<const XT*>(xs[k]) + i);
-    float th[8], m[8], e[8];
-    if (MODE == kDelta || NORM) load_s8(ts.theta + i, th);
-    if (MODE == kDelta) load_s8(ts.m + i, m);
-    if (EMA) load_s8(ts.e + i, e);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float xk[CAM_KMAX];
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
-        merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
-    }
-    store_s8(ts.theta + i, th);
-    if (MODE == kDelta) store_s8(ts.m + i, m);
-    if (EMA) store_s8(ts.e + i, e);
-}
-
-template <typename XT, int MODE, bool EMA, bool NORM>
-__device__ __forceinline__ void merge_one(const MergeArgs& a, const void* const* xs,
-                                          const TensorSlot& ts, int64_t i, float& acc) {
-    float xk[CAM_KMAX];
-#pragma unroll
-    for (int k = 0; k < CAM_KMAX; ++k)
-        xk[k] = (k < a.K) ? load_x1(static_cast<const XT*>(xs[k]) + i) : 0.0f;
-    float th = ts.theta[i];
-    float m = (MODE == kDelta) ? ts.m[i] : 0.0f;
-    float e = EMA ? ts.e[i] : 0.0f;
-    merge_elem<MODE, EMA, NORM>(a, xk, th, m, e, acc);
-    ts.theta[i] = th;
-    if (MODE == kDelta) ts.m[i] = m;
-    if (EMA) ts.e[i] = e;
-}
-
-__device__ __forceinline__ double warp_sum(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
+using namespace cam::dev;
 
 // ---- the fused pass ------------------------------------------------------------
 

@@ -74,6 +74,16 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+int cam::record_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
 struct Plan {
     std::vector<int32_t> tensors;      // global tensor ids, fragment order
     std::vector<int32_t> first_chunk;  // [T_f + 1]

@@ -195,6 +195,56 @@ int cam_ctx_set_last_round(cam_ctx* ctx, int64_t round);
  * the CAM_INIT_* work), for accounting what a timed region ran. */
 int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
 
+/*
+ * cam_merge_round_noalloc -- a whole round (accumulate, finalize, optional
+ * EMA update and drift norms, commit) in one call that allocates no memory.
+ * The pages have no counterpart to this call: it exists for callers that may
+ * not allocate device memory. One example is code embedded in a host
+ * framework whose memory pool has reserved the device's memory up front, so a
+ * cudaMalloc outside it fails or fragments the pool. Another is a merge issued
+ * on a path where cudaMalloc/cudaFree would synchronise the device and stall
+ * other streams. cam_ctx_create allocates its tables; this call needs no
+ * context.
+ *
+ * Arguments, all plain pointers: n_tensors in [0, CAM_NOALLOC_MAX_TENSORS];
+ * numel (host, [n_tensors]); master / momentum / ema (host arrays of device
+ * pointers to fp32 buffers, as in cam_ctx_desc; momentum is needed for
+ * DELTA_NESTEROV, ema when ema_update != 0); n_workers in [1, CAM_KMAX];
+ * ckpt (host, [n_workers * n_tensors] device pointers, worker-major in arrival
+ * order: ckpt[k * n_tensors + t]); dtype of every checkpoint; tokens (host,
+ * [n_workers], read in DELTA_NESTEROV mode only); mode, lr, mu, beta as for
+ * the context calls; per_tensor ([n_tensors]) and per_round ([1]) are device
+ * pointers for the drift norms, either or both NULL. The element arithmetic
+ * is the one documented at the top of this header, so the results equal those
+ * of a context round on the same inputs. Buffers must live on the current
+ * CUDA device; the work is queued on `stream` and the call returns before it
+ * runs.
+ *
+ * Memory: the drift partials live in one fixed array in the library's device
+ * memory: (CAM_NOALLOC_MAX_CHUNKS + CAM_NOALLOC_MAX_TENSORS) doubles, about
+ * 1.1 MB, held on every GPU that loads the library until the process exits.
+ * A round is cut into chunks of at most 16,384 elements, so one call covers
+ * at most CAM_NOALLOC_MAX_CHUNKS chunks (about 2.1e9 elements). Larger rounds,
+ * and more than CAM_NOALLOC_MAX_TENSORS tensors, are rejected with CAM_E_ARG
+ * before anything runs. The array keeps the previous call's contents; every
+ * entry a call reads is written by that call first, so nothing needs
+ * clearing. All calls share the one array: calls whose device work overlaps
+ * (different streams without ordering, or several host threads) race on it
+ * whenever one of them asks for norms. Calls on one stream are ordered and safe.
+ *
+ * The first call on each device looks up the array's device address and the
+ * device's properties, with that device current; make that first call before
+ * any stream capture. Errors: CAM_E_ARG (checked before any CUDA call),
+ * CAM_E_CUDA.
+ */
+#define CAM_NOALLOC_MAX_TENSORS 4096
+#define CAM_NOALLOC_MAX_CHUNKS 131072
+int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, float* const* master,
+                            float* const* momentum, float* const* ema, int32_t n_workers,
+                            const void* const* ckpt, cam_dtype dtype, const int64_t* tokens,
+                            cam_mode mode, float lr, float mu, int32_t ema_update, float beta,
+                            double* per_tensor, double* per_round, void* stream);
+
 /* Message describing the calling thread's last error ("" if none). */
 const char* cam_last_error(void);
 
