@@ -308,9 +308,16 @@ def run_ours(args, wl, ws, rank, local) -> int:
     mode = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
     round_no = [0]
     ev_pairs = []
+    prepared = [{k: mg.checkpoint(w[k].views, frag) for k in d.included}
+                for (_, frag), w, d in zip(wl.rounds, workers, draws)]
+
+    group_pairs = []
 
     def step(timed: bool) -> None:
         main = streams[0]
+        if timed and n_streams > 1:
+            ga = torch.cuda.Event(enable_timing=True)
+            ga.record(main)
         for s in streams[1:]:
             s.wait_stream(main)
         for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
@@ -318,7 +325,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
             rd = mg.begin(round_no[0], frag)
             round_no[0] += 1
             for k in d.included:
-                rd.accumulate(w[k].views, d.tokens[k])
+                rd.accumulate(prepared[i][k], d.tokens[k])
             rd.finalize(mode, wl.lr, wl.mu)
             if wl.ema_beta is not None:
                 rd.ema_update(wl.ema_beta)
@@ -333,6 +340,10 @@ def run_ours(args, wl, ws, rank, local) -> int:
                 ev_pairs.append((a, b))
         for s in streams[1:]:
             main.wait_stream(s)
+        if timed and n_streams > 1:
+            gb = torch.cuda.Event(enable_timing=True)
+            gb.record(main)
+            group_pairs.append((ga, gb))
 
     for _ in range(args.warmup):
         step(False)
@@ -355,18 +366,26 @@ def run_ours(args, wl, ws, rank, local) -> int:
     step_bytes = sum(round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl))
     agg = aggregate(step_bytes, args.steps, elapsed, ws, dev)
 
-    # roofline of the dominant launch: the merge pass of the biggest round
+    # roofline of the dominant launch: the merge pass of the biggest round.
+    # Rounds committed together on several streams share HBM, so their
+    # launches are timed as one group from the fork to the join.
     per_round = [round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl)]
     big = max(range(len(per_round)), key=per_round.__getitem__)
-    durs = [a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
-            if i % len(wl.rounds) == big]
-    kern_s = statistics.mean(durs)
+    if n_streams > 1:
+        kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for a, b in group_pairs)
+        launch_bytes = step_bytes
+        kernel_desc = f"merge_fused x{len(wl.rounds)} concurrent on {n_streams} streams"
+    else:
+        kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
+                                 if i % len(wl.rounds) == big)
+        launch_bytes = per_round[big]
+        kernel_desc = "merge_fused"
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured"
     if not peak:
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
-    achieved = per_round[big] / kern_s / 1e9
+    achieved = launch_bytes / kern_s / 1e9
     traffic = stored_traffic(wl.name)
 
     # end to end through the public API: worker inputs start in pinned host
@@ -400,8 +419,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_src, "traffic": traffic,
-                         "kernel": "merge_fused", "kernel_ms": round(kern_s * 1e3, 4),
-                         "algorithmic_bytes_per_launch": per_round[big]},
+                         "kernel": kernel_desc, "kernel_ms": round(kern_s * 1e3, 4),
+                         "algorithmic_bytes_per_launch": launch_bytes},
             "clocks": ck,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -415,37 +434,60 @@ def run_ours(args, wl, ws, rank, local) -> int:
 
 
 def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> dict:
+    """The round through the public API with the inputs in pinned host memory
+    and the result read back to pinned host memory, every step.
+
+    stream (default): the fused pass reads the included workers straight from
+      host memory (cam_merge_accumulate_host) and writes the new global and
+      EMA into host buffers in the same pass (cam_merge_publish).
+    copy: the workers are copied host->device with the copy engine, merged,
+      and the new global and EMA copied device->host afterwards."""
     import torch
+
+    from checkpoint_averaging_gb300 import workloads as W
 
     dev = theta.flat.device
     pinned = [[None] * wl.K for _ in wl.rounds]
     h2d = 0
     for i, d in enumerate(draws):
         for k in d.included:
-            h = torch.empty_like(workers[i][k].flat, device="cpu").pin_memory()
+            h = torch.empty(workers[i][k].flat.numel(), dtype=workers[i][k].flat.dtype,
+                            pin_memory=True)
             h.copy_(workers[i][k].flat)
-            pinned[i][k] = h
+            pinned[i][k] = W.Arena(h, workers[i][k].offsets, workers[i][k].numels)
             h2d += h.numel() * h.element_size()
-    out_theta = torch.empty_like(theta.flat, device="cpu").pin_memory()
-    out_e = torch.empty_like(e.flat, device="cpu").pin_memory() if e is not None else None
-    d2h = out_theta.numel() * 4 + (out_e.numel() * 4 if out_e is not None else 0)
+    out_theta = W.Arena(torch.empty(theta.flat.numel(), pin_memory=True), theta.offsets,
+                        theta.numels)
+    out_e = None
+    if e is not None:
+        out_e = W.Arena(torch.empty(e.flat.numel(), pin_memory=True), e.offsets, e.numels)
+    d2h = out_theta.flat.numel() * 4 + (out_e.flat.numel() * 4 if out_e is not None else 0)
+
+    src = [{k: mg.checkpoint((pinned[i][k] if args.e2e_mode == "stream" else w[k]).views, frag)
+            for k in d.included} for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws))]
 
     def step():
         with torch.cuda.stream(stream):
             for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
-                for k in d.included:
-                    w[k].flat.copy_(pinned[i][k], non_blocking=True)
+                if args.e2e_mode == "copy":
+                    for k in d.included:
+                        w[k].flat.copy_(pinned[i][k].flat, non_blocking=True)
                 rd = mg.begin(round_no[0], frag)
                 round_no[0] += 1
                 for k in d.included:
-                    rd.accumulate(w[k].views, d.tokens[k])
+                    rd.accumulate(src[i][k], d.tokens[k])
                 rd.finalize(mode, wl.lr, wl.mu)
                 if wl.ema_beta is not None:
                     rd.ema_update(wl.ema_beta)
+                if args.e2e_mode == "stream":
+                    ids = mg.fragment_tensors(frag)
+                    rd.publish([out_theta.views[t] for t in ids],
+                               None if out_e is None else [out_e.views[t] for t in ids])
                 rd.commit(stream)
-            out_theta.copy_(theta.flat, non_blocking=True)
-            if out_e is not None:
-                out_e.copy_(e.flat, non_blocking=True)
+            if args.e2e_mode == "copy":
+                out_theta.flat.copy_(theta.flat, non_blocking=True)
+                if out_e is not None:
+                    out_e.flat.copy_(e.flat, non_blocking=True)
         stream.synchronize()
 
     step()
@@ -458,8 +500,8 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
     return {"value": round(step_bytes * args.e2e_steps / el / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(el / args.e2e_steps * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": args.e2e_steps,
-            "note": "algorithmic merge bytes per wall second; the step copies the included "
+            "steps": args.e2e_steps, "mode": args.e2e_mode,
+            "note": "algorithmic merge bytes per wall second; each step moves the included "
                     "workers host->device and the new global and EMA device->host"}
 
 
@@ -472,6 +514,7 @@ def parse(argv=None):
     p.add_argument("--workload", default="diffurefill1b")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-mode", choices=("stream", "copy"), default="stream")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-seconds-per-step", type=float, default=1.5)

@@ -85,6 +85,7 @@ class CtxDesc(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
+           "cam_merge_accumulate_host", "cam_merge_publish",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_merge_round_noalloc",
@@ -111,6 +112,8 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_destroy.restype = None
     L.cam_merge_begin.argtypes = [vp, i64, i32, vpp]
     L.cam_merge_accumulate.argtypes = [vp, vpp, ctypes.c_int, i64]
+    L.cam_merge_accumulate_host.argtypes = [vp, vpp, ctypes.c_int, i64]
+    L.cam_merge_publish.argtypes = [vp, vpp, vpp]
     L.cam_merge_finalize.argtypes = [vp, ctypes.c_int, ctypes.c_float, ctypes.c_float]
     L.cam_ema_update.argtypes = [vp, ctypes.c_float]
     L.cam_drift_norm.argtypes = [vp, vp, vp]
@@ -193,6 +196,12 @@ def merge_accumulate(rd: int, ckpt: Sequence[int], dtype: int, tokens: int = 0) 
                                       dtype, tokens))
 
 
+def merge_accumulate_host(rd: int, ckpt: Sequence[int], dtype: int, tokens: int = 0) -> None:
+    arr = _ptrs(ckpt)
+    _check(lib().cam_merge_accumulate_host(
+        rd, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), dtype, tokens))
+
+
 def merge_finalize(rd: int, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
     _check(lib().cam_merge_finalize(rd, mode, lr, mu))
 
@@ -203,6 +212,13 @@ def ema_update(rd: int, beta: float) -> None:
 
 def drift_norm(rd: int, per_tensor: int | None, per_fragment: int | None) -> None:
     _check(lib().cam_drift_norm(rd, per_tensor or None, per_fragment or None))
+
+
+def merge_publish(rd: int, theta_out: Sequence[int], ema_out: Sequence[int] | None = None) -> None:
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    th = ctypes.cast(_ptrs(theta_out), vpp)
+    em = None if ema_out is None else ctypes.cast(_ptrs(ema_out), vpp)
+    _check(lib().cam_merge_publish(rd, th, em))
 
 
 def merge_commit(rd: int, stream: int = 0) -> None:
@@ -332,6 +348,16 @@ class Merger:
         except Exception:
             pass
 
+    def _hold_until_done(self, host_tensors, stream) -> None:
+        """Keeps host checkpoints referenced until the work that reads them
+        has run (torch cannot record a stream on a CPU tensor)."""
+        torch = _torch()
+        self._inflight = [(ev, ts) for ev, ts in getattr(self, "_inflight", []) if not ev.query()]
+        if host_tensors:
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            self._inflight.append((ev, host_tensors))
+
     def fragment_tensors(self, fragment: int) -> list[int]:
         if fragment not in self._frag_cache:
             self._frag_cache[fragment] = fragment_info(self.ctx, fragment)[0]
@@ -352,6 +378,51 @@ class Merger:
     def begin(self, round: int, fragment: int = -1) -> "Round":
         return Round(self, merge_begin(self.ctx, round, fragment), fragment)
 
+    def checkpoint(self, ckpt, fragment: int = -1) -> "Checkpoint":
+        """Validates a worker's tensors once for rounds on `fragment`."""
+        return Checkpoint(self, ckpt, fragment)
+
+
+class Checkpoint:
+    """One worker's tensors for one fragment of a Merger, validated once.
+
+    The pointer array handed to the C ABI is built here, so accumulating a
+    prepared checkpoint is a single library call. CUDA tensors must live on
+    the Merger's device; CPU tensors (pinned, or pageable where the GPU reads
+    host page tables) are streamed from host memory by the merge pass."""
+
+    def __init__(self, merger: "Merger", ckpt, fragment: int = -1):
+        torch = _torch()
+        ids = merger.fragment_tensors(fragment)
+        ckpt = list(ckpt)
+        if len(ckpt) == len(merger.master) and len(ckpt) != len(ids):
+            ckpt = [ckpt[g] for g in ids]
+        if len(ckpt) != len(ids):
+            raise ValueError(f"expected {len(ids)} tensors, got {len(ckpt)}")
+        dt = ckpt[0].dtype if ckpt else torch.float32
+        if dt not in (torch.float32, torch.bfloat16):
+            raise ValueError("checkpoints must be fp32 or bf16")
+        host = False
+        for t, g in zip(ckpt, ids):
+            on_host = t.device.type == "cpu"
+            host = host or on_host
+            if ((not on_host and t.device != merger.device) or t.dtype != dt
+                    or not t.is_contiguous() or t.numel() != merger.numel[g]):
+                raise ValueError(f"checkpoint tensor for tensor {g} has wrong device/dtype/shape")
+        self.merger, self.fragment, self.host = merger, fragment, host
+        self.dtype_code = BF16 if dt == torch.bfloat16 else F32
+        self._arr = _ptrs([t.data_ptr() for t in ckpt])
+        self.ptr_array = ctypes.cast(self._arr, ctypes.POINTER(ctypes.c_void_p))
+        # one tensor per underlying storage is enough to keep memory alive and
+        # to record the commit stream on the caching allocator's block
+        seen, keep = set(), []
+        for t in ckpt:
+            key = t.untyped_storage().data_ptr()
+            if key not in seen:
+                seen.add(key)
+                keep.append(t)
+        self.keep = keep
+
 
 class Round:
     def __init__(self, merger: Merger, handle: int, fragment: int):
@@ -360,24 +431,16 @@ class Round:
         self._borrowed = []
 
     def accumulate(self, ckpt, tokens: int = 0) -> None:
-        """ckpt: the worker's tensors of this fragment, in fragment order
-        (or the whole tensor list, from which the fragment's are taken)."""
-        torch = _torch()
-        ckpt = list(ckpt)
-        if len(ckpt) == len(self.merger.master) and len(ckpt) != len(self.tensors):
-            ckpt = [ckpt[g] for g in self.tensors]
-        if len(ckpt) != len(self.tensors):
-            raise ValueError(f"expected {len(self.tensors)} tensors, got {len(ckpt)}")
-        dt = ckpt[0].dtype if ckpt else torch.float32
-        if dt not in (torch.float32, torch.bfloat16):
-            raise ValueError("checkpoints must be fp32 or bf16")
-        for t, g in zip(ckpt, self.tensors):
-            if (t.device != self.merger.device or t.dtype != dt or not t.is_contiguous()
-                    or t.numel() != self.merger.numel[g]):
-                raise ValueError(f"checkpoint tensor for tensor {g} has wrong device/dtype/shape")
-        merge_accumulate(self.handle, [t.data_ptr() for t in ckpt],
-                         BF16 if dt == torch.bfloat16 else F32, int(tokens))
-        self._borrowed.extend(ckpt)
+        """Adds one worker, in arrival order. ckpt is a Checkpoint made for
+        this round's fragment, or its tensors: the fragment's tensors in
+        fragment order, or the whole tensor list (the fragment's are taken)."""
+        if not isinstance(ckpt, Checkpoint):
+            ckpt = Checkpoint(self.merger, ckpt, self.fragment)
+        elif ckpt.merger is not self.merger or ckpt.fragment != self.fragment:
+            raise ValueError("checkpoint was prepared for another merger or fragment")
+        fn = lib().cam_merge_accumulate_host if ckpt.host else lib().cam_merge_accumulate
+        _check(fn(self.handle, ckpt.ptr_array, ckpt.dtype_code, int(tokens)))
+        self._borrowed.extend(ckpt.keep)
 
     def finalize(self, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
         merge_finalize(self.handle, mode, lr, mu)
@@ -395,14 +458,39 @@ class Round:
                    None if per_fragment is None else per_fragment.data_ptr())
         self._borrowed.extend(t for t in (per_tensor, per_fragment) if t is not None)
 
+    def publish(self, theta_out, ema_out=None) -> None:
+        """Also write the new theta (and EMA) into these fp32 tensors, fragment
+        order, in the same pass: CUDA tensors or (pinned) CPU tensors."""
+        torch = _torch()
+        for group in (theta_out, ema_out):
+            if group is None:
+                continue
+            if len(group) != len(self.tensors):
+                raise ValueError(f"expected {len(self.tensors)} output tensors")
+            for t, g in zip(group, self.tensors):
+                if (t.dtype != torch.float32 or not t.is_contiguous()
+                        or t.numel() != self.merger.numel[g]
+                        or (t.device.type != "cpu" and t.device != self.merger.device)):
+                    raise ValueError(f"publish buffer for tensor {g} has wrong device/dtype/shape")
+        merge_publish(self.handle, [t.data_ptr() for t in theta_out],
+                      None if ema_out is None else [t.data_ptr() for t in ema_out])
+        self._borrowed.extend(theta_out)
+        if ema_out is not None:
+            self._borrowed.extend(ema_out)
+
     def commit(self, stream=None) -> None:
         torch = _torch()
         s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
         merge_commit(self.handle, int(s.cuda_stream))
         self.handle = None
+        host = []
         for t in self._borrowed:  # freed memory is not reused before the merge ran
-            t.record_stream(s)
+            if t.device.type == "cuda":
+                t.record_stream(s)
+            else:
+                host.append(t)
         self._borrowed = []
+        self.merger._hold_until_done(host, s)
 
     def abort(self) -> None:
         merge_abort(self.handle)

@@ -48,14 +48,16 @@ struct MergeArgs {
     int32_t local0;
     int32_t n_local;
     int32_t K;
+    int32_t stride;           // pointers per tensor in x: K, or K + 2 when publishing
     float Kf;                 // (float)K
     float w[CAM_KMAX];        // (float)tokens_k
     float W;                  // (float)sum tokens
     float lr, mu, beta;
     uint32_t vec[(kXCap + 31) / 32];  // bit l: tensor local0+l takes the vector path
-    // x[l*K + k]: worker k's copy of tensor local0+l. The CAM_KMAX spare slots
-    // keep every x[l*K + k] with l < n_local, k < CAM_KMAX inside the block.
-    const void* x[kXCap + CAM_KMAX];
+    // x[l*stride + k]: worker k's copy of tensor local0+l; when publishing,
+    // x[l*stride + K] and x[l*stride + K + 1] take the new theta and EMA. The
+    // spare slots keep every x[l*stride + k] with k < CAM_KMAX + 2 inside.
+    const void* x[kXCap + CAM_KMAX + 2];
 };
 static_assert(sizeof(MergeArgs) <= 32000, "kernel parameter block too large");
 
@@ -76,10 +78,10 @@ enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 int record_error(int code, const char* fmt, ...);
 
 // Launches one fused merge pass with `grid` blocks.
-cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm,
+cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
                          int grid, cudaStream_t s);
 // Resident blocks per SM of that variant (0 on error).
-int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm);
+int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm, bool pub);
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_fill(float* dst, int64_t n, float v, cudaStream_t s);
 cudaError_t launch_copy(float* dst, const float* src, int64_t n, cudaStream_t s);

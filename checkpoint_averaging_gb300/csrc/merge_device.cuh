@@ -122,7 +122,9 @@ __device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMA
     }
 }
 
-template <typename XT, int MODE, bool EMA, bool NORM, class A>
+// xs[0..K) are the workers' copies of the tensor; with PUB, xs[K] receives a
+// copy of the new theta and xs[K+1] (when not null) a copy of the new EMA.
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, class A>
 __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
                                            const TensorSlot& ts, int64_t i, float& acc) {
     XVec<XT> x[CAM_KMAX];
@@ -143,9 +145,13 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
     store_s8(ts.theta + i, th);
     if (MODE == kDelta) store_s8(ts.m + i, m);
     if (EMA) store_s8(ts.e + i, e);
+    if (PUB) {
+        store_s8(static_cast<float*>(const_cast<void*>(xs[a.K])) + i, th);
+        if (EMA && xs[a.K + 1]) store_s8(static_cast<float*>(const_cast<void*>(xs[a.K + 1])) + i, e);
+    }
 }
 
-template <typename XT, int MODE, bool EMA, bool NORM, class A>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, class A>
 __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
                                           const TensorSlot& ts, int64_t i, float& acc) {
     float xk[CAM_KMAX];
@@ -159,6 +165,10 @@ __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
     ts.theta[i] = th;
     if (MODE == kDelta) ts.m[i] = m;
     if (EMA) ts.e[i] = e;
+    if (PUB) {
+        static_cast<float*>(const_cast<void*>(xs[a.K]))[i] = th;
+        if (EMA && xs[a.K + 1]) static_cast<float*>(const_cast<void*>(xs[a.K + 1]))[i] = e;
+    }
 }
 
 __device__ __forceinline__ double warp_sum(double v) {

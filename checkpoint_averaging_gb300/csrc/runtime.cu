@@ -111,12 +111,13 @@ struct cam_ctx {
     std::vector<int32_t> fragment_of;
     std::vector<float*> theta, m, e;
     bool has_m = false, has_e = false;
+    bool pageable_access = false;  // the GPU reads pageable host memory directly
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
     int64_t last_round = -1;
     int64_t launches = 0;
     std::vector<cam_round*> open;
-    int bps[2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm]
+    int bps[2][2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm][publish]
     std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
 
     Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
@@ -141,6 +142,9 @@ struct cam_round {
     bool norms = false;
     double* out_tensor = nullptr;
     double* out_fragment = nullptr;
+    bool publish = false;
+    bool publish_ema = false;
+    std::vector<void*> pub_theta, pub_ema;  // [T_f] device-visible addresses
 };
 
 namespace {
@@ -231,6 +235,10 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->device = d->device;
     ce = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, d->device);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_create: SM count");
+    int pageable = 0;
+    ce = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, d->device);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_create: pageable memory access");
+    c->pageable_access = pageable != 0;
     c->n_tensors = d->n_tensors;
     c->n_fragments = d->n_fragments;
     c->quorum = d->quorum;
@@ -296,7 +304,9 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         for (int md = 0; md < 2; ++md)
             for (int em = 0; em < 2; ++em)
                 for (int nm = 0; nm < 2; ++nm)
-                    c->bps[dt][md][em][nm] = std::max(1, cam::merge_blocks_per_sm(dt, md, em, nm));
+                    for (int pb = 0; pb < 2; ++pb)
+                        c->bps[dt][md][em][nm][pb] =
+                            std::max(1, cam::merge_blocks_per_sm(dt, md, em, nm, pb));
 
     cudaStream_t s = static_cast<cudaStream_t>(d->stream);
     for (int32_t t = 0; t < c->n_tensors && ce == cudaSuccess; ++t) {
@@ -360,29 +370,79 @@ CAM_API int cam_merge_begin(cam_ctx* c, int64_t round, int32_t fragment, cam_rou
     return CAM_OK;
 }
 
-CAM_API int cam_merge_accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype,
-                                 int64_t tokens) {
-    if (!r) return fail(CAM_E_ARG, "cam_merge_accumulate: round is NULL");
-    if (r->finalized) return fail(CAM_E_STATE, "cam_merge_accumulate: round already finalized");
-    if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "cam_merge_accumulate: more than %d workers", CAM_KMAX);
+namespace {
+
+// Device address under which the GPU reaches host buffer p, or nullptr when
+// it cannot: page-locked memory mapped for the device (cudaHostAlloc,
+// cudaHostRegister, pinned torch tensors), managed memory, or ordinary pageable
+// memory on systems whose GPU reads host page tables (Grace: NVLink-C2C with
+// address translation). Device memory of the context's device is accepted too.
+const void* device_view_of_host(const cam_ctx* c, const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // the failed query must not linger as the last error
+        return nullptr;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeHost:
+            return at.devicePointer;
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeDevice:
+            return at.device == c->device ? p : nullptr;
+        default:  // unregistered pageable memory
+            return c->pageable_access ? p : nullptr;
+    }
+}
+
+int accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t tokens,
+               bool host, const char* fn) {
+    if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
+    if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
+    if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
     if (dtype != CAM_F32 && dtype != CAM_BF16)
-        return fail(CAM_E_ARG, "cam_merge_accumulate: unknown dtype %d", static_cast<int>(dtype));
+        return fail(CAM_E_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
     if (r->K > 0 && dtype != r->dtype)
-        return fail(CAM_E_ARG, "cam_merge_accumulate: dtype %d differs from the round's %d",
+        return fail(CAM_E_ARG, "%s: dtype %d differs from the round's %d", fn,
                     static_cast<int>(dtype), r->dtype);
     if (tokens < 0 || tokens > (int64_t(1) << 56))
-        return fail(CAM_E_ARG, "cam_merge_accumulate: tokens %lld out of range",
-                    static_cast<long long>(tokens));
-    const Plan& p = r->ctx->plan_of(r->fragment);
-    if (!ckpt && p.n_tensors() > 0) return fail(CAM_E_ARG, "cam_merge_accumulate: ckpt is NULL");
+        return fail(CAM_E_ARG, "%s: tokens %lld out of range", fn, static_cast<long long>(tokens));
+    const cam_ctx* c = r->ctx;
+    const Plan& p = c->plan_of(r->fragment);
+    if (!ckpt && p.n_tensors() > 0) return fail(CAM_E_ARG, "%s: ckpt is NULL", fn);
     for (int32_t l = 0; l < p.n_tensors(); ++l)
-        if (!ckpt[l] && r->ctx->numel[p.tensors[l]] > 0)
-            return fail(CAM_E_ARG, "cam_merge_accumulate: ckpt[%d] is NULL", l);
-    for (int32_t l = 0; l < p.n_tensors(); ++l) r->x.push_back(ckpt[l]);
+        if (!ckpt[l] && c->numel[p.tensors[l]] > 0)
+            return fail(CAM_E_ARG, "%s: ckpt[%d] is NULL", fn, l);
+    const size_t base = r->x.size();
+    for (int32_t l = 0; l < p.n_tensors(); ++l) {
+        const void* q = ckpt[l];
+        if (host && c->numel[p.tensors[l]] > 0) {
+            q = device_view_of_host(c, ckpt[l]);
+            if (!q) {
+                r->x.resize(base);
+                return fail(CAM_E_ARG,
+                            "%s: ckpt[%d] is host memory the GPU cannot read (pin it or "
+                            "register it with the CUDA driver)", fn, l);
+            }
+        }
+        r->x.push_back(q);
+    }
     r->tokens[r->K] = tokens;
     r->dtype = dtype;
     ++r->K;
     return CAM_OK;
+}
+
+}  // namespace
+
+CAM_API int cam_merge_accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype,
+                                 int64_t tokens) {
+    return accumulate(r, ckpt, dtype, tokens, false, "cam_merge_accumulate");
+}
+
+CAM_API int cam_merge_accumulate_host(cam_round* r, const void* const* ckpt, cam_dtype dtype,
+                                      int64_t tokens) {
+    return accumulate(r, ckpt, dtype, tokens, true, "cam_merge_accumulate_host");
 }
 
 CAM_API int cam_merge_finalize(cam_round* r, cam_mode mode, float lr, float mu) {
@@ -421,6 +481,34 @@ CAM_API int cam_drift_norm(cam_round* r, double* per_tensor, double* per_fragmen
     return CAM_OK;
 }
 
+CAM_API int cam_merge_publish(cam_round* r, float* const* theta_out, float* const* ema_out) {
+    const char* fn = "cam_merge_publish";
+    if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
+    if (r->publish) return fail(CAM_E_STATE, "%s: asked twice", fn);
+    const cam_ctx* c = r->ctx;
+    const Plan& p = c->plan_of(r->fragment);
+    if (!theta_out && p.n_tensors() > 0) return fail(CAM_E_ARG, "%s: theta_out is NULL", fn);
+    std::vector<void*> th(p.n_tensors(), nullptr), em;
+    if (ema_out) em.assign(p.n_tensors(), nullptr);
+    for (int32_t l = 0; l < p.n_tensors(); ++l) {
+        if (c->numel[p.tensors[l]] == 0) continue;
+        for (int which = 0; which < (ema_out ? 2 : 1); ++which) {
+            float* q = which == 0 ? theta_out[l] : ema_out[l];
+            if (!q) return fail(CAM_E_ARG, "%s: %s[%d] is NULL", fn, which ? "ema_out" : "theta_out", l);
+            const void* d = device_view_of_host(c, q);
+            if (!d)
+                return fail(CAM_E_ARG, "%s: %s[%d] is memory the GPU cannot write", fn,
+                            which ? "ema_out" : "theta_out", l);
+            (which == 0 ? th : em)[l] = const_cast<void*>(d);
+        }
+    }
+    r->publish = true;
+    r->publish_ema = ema_out != nullptr;
+    r->pub_theta.swap(th);
+    r->pub_ema.swap(em);
+    return CAM_OK;
+}
+
 namespace {
 
 void close_round(cam_round* r) {
@@ -444,6 +532,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     if (r->K < c->quorum)
         return fail(CAM_E_QUORUM, "cam_merge_commit: %d participants < quorum %d", r->K, c->quorum);
     if (r->K < 1) return fail(CAM_E_QUORUM, "cam_merge_commit: no participants");
+    if (r->publish_ema && !r->ema)
+        return fail(CAM_E_STATE, "cam_merge_commit: an EMA copy was asked for without an EMA update");
     int64_t W = 0;
     for (int k = 0; k < r->K; ++k) W += r->tokens[k];
     if (r->mode == CAM_MODE_DELTA_NESTEROV && W <= 0)
@@ -463,7 +553,9 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.lr = r->lr;
     a.mu = r->mu;
     a.beta = r->beta;
-    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms];
+    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms][r->publish];
+    const int stride = K + (r->publish ? 2 : 0);
+    a.stride = stride;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     DeviceScope scope(c->device);
@@ -472,7 +564,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         return cuda_fail(scope.err, "cam_merge_commit: cudaSetDevice");
     }
     cudaError_t ce = cudaSuccess;
-    const int per_launch = cam::kXCap / K;
+    const int per_launch = cam::kXCap / stride;
     for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += per_launch) {
         const int n = std::min(per_launch, T - l0);
         const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
@@ -484,8 +576,15 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                      (!r->ema || aligned(c->e[g], 32));
             for (int k = 0; k < K; ++k) {
                 const void* xp = r->x[size_t(k) * T + l0 + l];
-                a.x[size_t(l) * K + k] = xp;
+                a.x[size_t(l) * stride + k] = xp;
                 v = v && aligned(xp, xa);
+            }
+            if (r->publish) {
+                void* pt = r->pub_theta[l0 + l];
+                void* pe = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
+                a.x[size_t(l) * stride + K] = pt;
+                a.x[size_t(l) * stride + K + 1] = pe;
+                v = v && aligned(pt, 32) && aligned(pe, 32);
             }
             if (v) a.vec[l >> 5] |= 1u << (l & 31);
         }
@@ -495,7 +594,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         a.local0 = l0;
         a.n_local = n;
         const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
-        ce = cam::launch_merge(a, r->dtype, r->mode, r->ema, r->norms, grid, s);
+        ce = cam::launch_merge(a, r->dtype, r->mode, r->ema, r->norms, r->publish, grid, s);
         ++c->launches;
     }
     if (ce == cudaSuccess && r->norms) {

@@ -144,6 +144,23 @@ int cam_merge_accumulate(cam_round* rd, const void* const* ckpt, cam_dtype dtype
                          int64_t tokens);
 
 /*
+ * Like cam_merge_accumulate, but ckpt holds HOST pointers: the worker's
+ * tensors stay in CPU memory and the fused pass streams them to the GPU itself
+ * (over NVLink-C2C on Grace systems), so no staging copy or device buffer is
+ * needed. This is the merger of the DiffuRefill-1B pages folding each
+ * downloaded checkpoint as it arrives ("DiffuRefill-1B" model card, "How it
+ * is trained", Merging), with the checkpoint in host RAM. Each buffer must be
+ * readable by the device: page-locked memory mapped for it (cudaHostAlloc,
+ * cudaHostRegister, pinned torch tensors), managed memory, or pageable memory
+ * on systems where cudaDevAttrPageableMemoryAccess is 1. Anything else is
+ * rejected with CAM_E_ARG before any work and the round is unchanged. Host
+ * and device checkpoints may be mixed within a round. Borrowed like device
+ * checkpoints. Errors: as cam_merge_accumulate.
+ */
+int cam_merge_accumulate_host(cam_round* rd, const void* const* ckpt, cam_dtype dtype,
+                              int64_t tokens);
+
+/*
  * Chooses the outer step. MEAN_REPLACE ignores lr, mu and the token counts.
  * DELTA_NESTEROV needs momentum buffers. lr and mu must be finite.
  * Errors: CAM_E_ARG, CAM_E_STATE (finalized twice).
@@ -165,6 +182,21 @@ int cam_ema_update(cam_round* rd, float beta);
  * CAM_E_STATE (asked twice).
  */
 int cam_drift_norm(cam_round* rd, double* per_tensor, double* per_fragment);
+
+/*
+ * Asks the fused pass to also write the new global theta' (and, when ema_out
+ * is not NULL, the new EMA e') into theta_out[T_f] / ema_out[T_f], fragment
+ * order, in the same pass that computes them. These are typically pinned host
+ * buffers from which the merger publishes the new global and its EMA
+ * ("DiffuRefill-1B" technical report, section 3, Table 2, "Merger" and "Side
+ * averages"; the model card's Files: global_b.pt, global_ema.pt), so no
+ * separate device-to-host copy follows the round. Each buffer holds numel[t]
+ * floats and must be writable by the GPU (device memory of the context's
+ * device, or host memory as for cam_merge_accumulate_host). ema_out needs an
+ * EMA update in the same round (checked at commit, CAM_E_STATE). Errors:
+ * CAM_E_ARG, CAM_E_STATE (asked twice).
+ */
+int cam_merge_publish(cam_round* rd, float* const* theta_out, float* const* ema_out);
 
 /*
  * Closes the round: checks it (finalized, quorum met, weights valid), then

@@ -429,3 +429,83 @@ def test_resume_after_restart_is_bitwise_identical():
     assert torch.equal(a.m.flat.view(torch.int32), c.m.flat.view(torch.int32))
     a.merger.close()
     c.merger.close()
+
+
+# ---- host-resident checkpoints and published copies ------------------------------------
+
+def _host_copy(arena, pinned=True):
+    h = torch.empty(arena.flat.numel(), dtype=arena.flat.dtype, pin_memory=pinned)
+    h.copy_(arena.flat)
+    return W.Arena(h, arena.offsets, arena.numels)
+
+
+@pytest.mark.parametrize("where", ["pinned", "pageable", "mixed"])
+def test_host_resident_checkpoints_match_oracle(where):
+    """Workers left in host memory are streamed by the fused pass itself."""
+    wl = _custom(RAGGED, K=3, mode="delta", dtype="bf16", rounds=((0, -1), (1, -1)))
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    ost = oracle_state_from(g, wl)
+    for idx, (rnd, frag) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, 0)
+        workers = [W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)]
+        if where == "mixed":
+            used = [_host_copy(w) if k % 2 == 0 else w for k, w in enumerate(workers)]
+        else:
+            used = [_host_copy(w, pinned=where == "pinned") for w in workers]
+        try:
+            gn = gpu_round(st, wl, rnd, frag, used, draw)
+        except B.ArgError as ex:
+            assert where == "pageable" and "cannot read" in str(ex)
+            pytest.skip("this GPU does not read pageable host memory")
+        on = oracle_round(ost, wl, rnd, frag, workers, draw)
+        compare_full(st, ost, f"host workers ({where}) round {rnd}", bitwise=True)
+        from merge_harness import compare_norms
+        compare_norms(gn, on, f"host workers ({where}) round {rnd}")
+    st.merger.close()
+
+
+@pytest.mark.parametrize("dest", ["pinned", "device"])
+def test_publish_writes_copies_of_theta_and_ema(dest):
+    wl = _custom(RAGGED, K=3, mode="delta", dtype="f32")
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(3)]
+    if dest == "pinned":
+        pth = W.Arena(torch.full((st.theta.flat.numel(),), float("nan")).pin_memory(),
+                      st.theta.offsets, st.theta.numels)
+        pe = W.Arena(torch.full((st.e.flat.numel(),), float("nan")).pin_memory(),
+                     st.e.offsets, st.e.numels)
+    else:
+        pth = W.empty_arena(st.theta.numels, torch.float32, DEV)
+        pe = W.empty_arena(st.e.numels, torch.float32, DEV)
+    rd = st.merger.begin(0)
+    for k in draw.included:
+        rd.accumulate(workers[k].views, draw.tokens[k])
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.ema_update(0.9)
+    rd.publish(pth.views, pe.views)
+    rd.commit()
+    torch.cuda.synchronize()
+    for t, n in enumerate(RAGGED):
+        assert torch.equal(pth.views[t].cpu().view(torch.int32), st.theta.views[t].cpu().view(torch.int32))
+        assert torch.equal(pe.views[t].cpu().view(torch.int32), st.e.views[t].cpu().view(torch.int32))
+    st.merger.close()
+
+
+def test_publish_ema_needs_an_ema_update():
+    mg, th = _tiny_merger(n_fragments=1, quorum=1)
+    x = [torch.ones(100, device=DEV), torch.ones(50, device=DEV)]
+    out = [torch.empty(100, device=DEV), torch.empty(50, device=DEV)]
+    rd = mg.begin(0)
+    rd.accumulate(x, 1)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.publish(out, [torch.empty(100, device=DEV), torch.empty(50, device=DEV)])
+    with pytest.raises(B.StateError):
+        rd.commit()
+    rd.ema_update(0.9)
+    rd.commit()
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], th[0]) and torch.equal(out[1], th[1])
+    mg.close()
