@@ -53,11 +53,12 @@ def lib():
         L.ora_weighted_delta.argtypes = [i64, i32, vpp, i32, vp, vp, vp]
         L.ora_outer_nesterov.argtypes = [i64, vp, f32, f32, vp, vp]
         L.ora_ema.argtypes = [i64, vp, f32, vp]
+        L.ora_swa.argtypes = [i64, vp, i64, vp]
         L.ora_merge_tensor.argtypes = [i64, i32, vpp, i32, vp, i32, f32, f32,
                                        i32, f32, vp, vp, vp,
                                        ctypes.POINTER(ctypes.c_double)]
         for fn in (L.ora_widen_bf16, L.ora_plain_mean, L.ora_weighted_delta,
-                   L.ora_outer_nesterov, L.ora_ema, L.ora_merge_tensor):
+                   L.ora_outer_nesterov, L.ora_ema, L.ora_swa, L.ora_merge_tensor):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -142,6 +143,20 @@ def ema(theta_new: np.ndarray, beta: float, e: np.ndarray) -> None:
     _check(lib().ora_ema(theta_new.size, _ptr(theta_new), beta, _ptr(e)), "ema")
 
 
+def swa(theta_new: np.ndarray, count: int, mu: np.ndarray) -> None:
+    """In place on mu: fold one more global into the uniform running average;
+    count (>= 1) is the number of globals in the average after this one."""
+    theta_new = _contig(theta_new, np.float32)
+    assert mu.flags.c_contiguous and mu.dtype == np.float32
+    _check(lib().ora_swa(theta_new.size, _ptr(theta_new), int(count), _ptr(mu)), "swa")
+
+
+def plain_average(snapshots: Sequence[np.ndarray]) -> np.ndarray:
+    """Average of stored snapshots (the last-n snapshot averages of the
+    technical report's Table 5): their plain mean in the given order."""
+    return plain_mean(snapshots)
+
+
 def merge_tensor(xs: Sequence[np.ndarray], theta: np.ndarray, *, mode: int,
                  tokens: Sequence[int] | None = None, lr: float = 1.0,
                  mu: float = 0.0, m: np.ndarray | None = None,
@@ -188,6 +203,8 @@ class OracleState:
     e: list | None = None
     fragment_of: list = field(default_factory=list)
     last_round: int = -1
+    swa: list | None = None            # running uniform average of the globals
+    swa_count: list | None = None      # globals folded into it, per tensor
 
 
 def fragment_tensors(fragment_of: Sequence[int], fragment: int) -> list[int]:
@@ -199,7 +216,8 @@ def fragment_tensors(fragment_of: Sequence[int], fragment: int) -> list[int]:
 def merge_round(state: OracleState, *, round: int, fragment: int,
                 ckpts: Sequence[Sequence[np.ndarray]], included: Sequence[int],
                 tokens: Sequence[int] | None, mode: int, lr: float = 1.0,
-                mu: float = 0.0, quorum: int = 1, ema_beta: float | None = None):
+                mu: float = 0.0, quorum: int = 1, ema_beta: float | None = None,
+                swa_update: bool = False):
     """Apply one merge round in place on `state`.
 
     ckpts[k][t] is worker k's copy of tensor t (full tensor list; only the
@@ -215,6 +233,8 @@ def merge_round(state: OracleState, *, round: int, fragment: int,
         raise OracleError("momentum buffers required")
     if ema_beta is not None and state.e is None:
         raise OracleError("EMA buffers required")
+    if swa_update and state.swa is None:
+        raise OracleError("SWA buffers required")
     tlist = fragment_tensors(state.fragment_of, fragment)
     w = None if tokens is None else [int(tokens[k]) for k in included]
     sumsqs = []
@@ -224,6 +244,9 @@ def merge_round(state: OracleState, *, round: int, fragment: int,
                          m=None if state.m is None else state.m[t],
                          e=None if ema_beta is None else state.e[t],
                          beta=0.9 if ema_beta is None else ema_beta)
+        if swa_update:
+            state.swa_count[t] += 1
+            swa(state.theta[t], state.swa_count[t], state.swa[t])
         sumsqs.append(s)
     total = 0.0
     for s in sumsqs:

@@ -20,6 +20,10 @@
  *         updates through the bucket": the merge takes a token-weighted mean
  *         of the deltas and applies an outer Nesterov optimizer (learning rate
  *         0.7, momentum 0.9).
+ *   [TR 4] same report, section 4 (Data and schedule): the released weights
+ *         are the uniform average of the 130 merged globals of the final
+ *         stretch; section 5.4 / Table 5: uniform average and averages of
+ *         the last 3 and 5 snapshots.
  *   [TR 5.1] same report, section 5.1 (Distributed optimisation): "local
  *         drift", the movement of the workers away from the last global.
  *
@@ -35,6 +39,9 @@
  *   - plain mean ignores token counts;
  *   - EMA input is the new global theta' (after the outer step), no bias
  *     correction;
+ *   - uniform average of the globals (SWA): kept as a running mean,
+ *     mu_n = mu_{n-1} + (theta_n - mu_{n-1}) / n, n counting the globals
+ *     folded since the average was last reset (mu_1 = theta_1 exactly);
  *   - drift: per tensor the L2 norm of the mean worker displacement
  *     (Delta in the token-weighted mode, mean - theta_old in the plain mode),
  *     squares summed in fp64 in index order.
@@ -112,6 +119,13 @@ static float ema_step(float e, float theta_new, float beta) {
     return beta * e + one_minus_beta * theta_new;
 }
 
+/* ---- step: uniform running average of the globals [TR 4], [TR Tab.5] ---- */
+
+static float swa_step(float mu, float theta_new, float n) {
+    float d = theta_new - mu;
+    return mu + d / n;
+}
+
 /* ---- exported single-step entry points (used to pin each step) ----------- */
 
 int ora_widen_bf16(int64_t n, const uint16_t* in, float* out) {
@@ -167,6 +181,16 @@ int ora_outer_nesterov(int64_t n, const float* delta, float lr, float mu,
 int ora_ema(int64_t n, const float* theta_new, float beta, float* e) {
     if (n < 0 || !theta_new || !e) return ORA_EARG;
     for (int64_t i = 0; i < n; ++i) e[i] = ema_step(e[i], theta_new[i], beta);
+    return ORA_OK;
+}
+
+/* Folds one more global into the running average: swa <- swa + (theta_new -
+ * swa) / count, where count >= 1 is the number of globals in the average
+ * after this one. */
+int ora_swa(int64_t n, const float* theta_new, int64_t count, float* swa) {
+    if (n < 0 || count < 1 || !theta_new || !swa) return ORA_EARG;
+    float nf = (float)count;
+    for (int64_t i = 0; i < n; ++i) swa[i] = swa_step(swa[i], theta_new[i], nf);
     return ORA_OK;
 }
 

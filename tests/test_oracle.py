@@ -405,3 +405,73 @@ def test_fragment_minus_one_is_all_tensors():
     assert oracle.fragment_tensors([0, 1, 2, 1], -1) == [0, 1, 2, 3]
     assert oracle.fragment_tensors([0, 1, 2, 1], 1) == [1, 3]
     assert oracle.fragment_tensors([0, 1, 2, 1], 4) == []
+
+
+# ---- uniform average of the globals (SWA) and snapshot averages -------------------
+
+def test_swa_first_global_is_copied_exactly():
+    theta = rng(20).normal(0, 0.02, 1001).astype(np.float32)
+    mu = np.zeros(1001, np.float32)
+    oracle.swa(theta, 1, mu)
+    assert bitwise_equal_np(mu, theta)
+
+
+def bitwise_equal_np(a, b):
+    return (np.asarray(a, np.float32).view(np.uint32) == np.asarray(b, np.float32).view(np.uint32)).all()
+
+
+def test_swa_of_a_constant_stays_exact():
+    mu = np.zeros(64, np.float32)
+    c = rng(21).normal(0, 0.02, 64).astype(np.float32)
+    for n in range(1, 131):
+        oracle.swa(c, n, mu)
+        assert bitwise_equal_np(mu, c)
+
+
+def test_swa_is_the_uniform_average_of_130_globals():
+    # the released weights: the uniform average of the 130 globals of the
+    # final stretch (technical report, section 4 and Table 5)
+    r = rng(22)
+    n_el, n = 48, 130
+    thetas = [r.normal(0, 0.02, n_el).astype(np.float32) for _ in range(n)]
+    mu = np.zeros(n_el, np.float32)
+    for j, t in enumerate(thetas, 1):
+        oracle.swa(t, j, mu)
+    for i in range(n_el):
+        exact = sum(ex(t[i]) for t in thetas) / n
+        mag = max(abs(ex(t[i])) for t in thetas)
+        assert abs(ex(mu[i]) - exact) <= 4 * n * U * mag
+
+
+def test_swa_rejects_a_zero_count():
+    with pytest.raises(oracle.OracleError):
+        oracle.swa(np.zeros(4, np.float32), 0, np.zeros(4, np.float32))
+
+
+def test_snapshot_average_is_their_plain_mean():
+    # "average of the last 3 / 5 snapshots" (technical report, Table 5)
+    r = rng(23)
+    snaps = [r.normal(0, 0.02, 8).astype(np.float32) for _ in range(5)]
+    for w in (3, 5):
+        got = oracle.plain_average(snaps[-w:])
+        for i in range(8):
+            exact = sum(ex(s[i]) for s in snaps[-w:]) / w
+            assert abs(ex(got[i]) - exact) <= (w + 1) * U * sum(abs(ex(s[i])) for s in snaps[-w:])
+
+
+def test_round_level_swa_tracks_the_rounds_globals():
+    st, ck = _round_state(seed=24)
+    st.swa = [np.zeros_like(t) for t in st.theta]
+    st.swa_count = [0] * len(st.theta)
+    seen = {t: [] for t in range(6)}
+    for rnd in range(3):
+        oracle.merge_round(st, round=rnd, fragment=-1, ckpts=ck, included=[0, 1, 2],
+                           tokens=[1, 2, 3, 4], mode=oracle.DELTA_NESTEROV, lr=0.7, mu=0.9,
+                           quorum=3, swa_update=True)
+        for t in range(6):
+            seen[t].append(st.theta[t].copy())
+    for t in range(6):
+        assert st.swa_count[t] == 3
+        exact = [sum(ex(s[i]) for s in seen[t]) / 3 for i in range(st.theta[t].size)]
+        for i, x in enumerate(exact):
+            assert abs(ex(st.swa[t][i]) - x) <= 12 * U * max(abs(ex(s[i])) for s in seen[t])
