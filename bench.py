@@ -37,7 +37,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params"
-KERNEL_SRC = os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", "merge_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", f)
+               for f in ("merge_kernels.cu", "merge_device.cuh", "cam_internal.h")]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -56,6 +57,8 @@ def round_bytes(wl, frag: int, k_incl: int) -> int:
         per += 8
     if wl.ema_beta is not None:
         per += 8
+    if wl.swa:
+        per += 8
     return per * wl.fragment_numel(frag)
 
 
@@ -68,8 +71,12 @@ def measured_peaks() -> dict:
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the sources the fused merge kernel is compiled from."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def stored_traffic(workload: str):
@@ -294,13 +301,15 @@ def run_ours(args, wl, ws, rank, local) -> int:
     if wl.ema_beta is not None:
         e = W.empty_arena(g.numels, torch.float32, dev)
         e.flat.copy_(g.flat)
+    swa = W.empty_arena(g.numels, torch.float32, dev) if wl.swa else None
     draws = [W.draw_round(wl, i, seed) for i in range(len(wl.rounds))]
     workers = [[W.make_worker(wl, g, rnd, k, seed, dev) for k in range(wl.K)]
                for rnd, _ in wl.rounds]
     del g
     mg = B.Merger(theta.views, momentum=None if m is None else m.views,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
-                  n_fragments=wl.n_fragments, quorum=wl.quorum)
+                  n_fragments=wl.n_fragments, quorum=wl.quorum,
+                  swa=None if swa is None else swa.views)
     n_streams = max(1, wl.in_flight)
     streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
     norm_out = [(torch.zeros(len(mg.fragment_tensors(f)) or 1, dtype=torch.float64, device=dev),
@@ -329,6 +338,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
             rd.finalize(mode, wl.lr, wl.mu)
             if wl.ema_beta is not None:
                 rd.ema_update(wl.ema_beta)
+            if wl.swa:
+                rd.swa_update()
             if wl.norms:
                 rd.drift_norm(*norm_out[i])
             if timed:
@@ -412,6 +423,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
             "data": "synthetic",
             "config": {"workload": wl.name, "n_params": wl.n_params, "K": wl.K,
                        "included": k_incl, "mode": wl.mode, "ema": wl.ema_beta is not None,
+                       "swa": wl.swa,
                        "norms": wl.norms, "rounds_per_step": len(wl.rounds),
                        "streams": n_streams, "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
@@ -479,6 +491,8 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
                 rd.finalize(mode, wl.lr, wl.mu)
                 if wl.ema_beta is not None:
                     rd.ema_update(wl.ema_beta)
+                if wl.swa:
+                    rd.swa_update()
                 if args.e2e_mode == "stream":
                     ids = mg.fragment_tensors(frag)
                     rd.publish([out_theta.views[t] for t in ids],

@@ -21,7 +21,7 @@ MAX_OPEN_ROUNDS = 8
 
 F32, BF16 = 0, 1
 MEAN_REPLACE, DELTA_NESTEROV = 0, 1
-INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM = 1, 2
+INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
 
 OK, E_ARG, E_STATE, E_STALE, E_BUSY, E_QUORUM, E_KMAX, E_CUDA, E_NOMEM = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
@@ -79,13 +79,15 @@ class CtxDesc(ctypes.Structure):
         ("device", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
         ("stream", ctypes.c_void_p),
+        ("swa", ctypes.POINTER(ctypes.c_void_p)),
     ]
 
 
 _lib = None
 
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
-           "cam_merge_accumulate_host", "cam_merge_publish",
+           "cam_merge_accumulate_host", "cam_merge_publish", "cam_swa_update", "cam_swa_reset",
+           "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_merge_round_noalloc",
@@ -114,6 +116,10 @@ def lib() -> ctypes.CDLL:
     L.cam_merge_accumulate.argtypes = [vp, vpp, ctypes.c_int, i64]
     L.cam_merge_accumulate_host.argtypes = [vp, vpp, ctypes.c_int, i64]
     L.cam_merge_publish.argtypes = [vp, vpp, vpp]
+    L.cam_swa_update.argtypes = [vp]
+    L.cam_swa_reset.argtypes = [vp, i32, vp]
+    L.cam_swa_counts.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_swa_set_counts.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_merge_finalize.argtypes = [vp, ctypes.c_int, ctypes.c_float, ctypes.c_float]
     L.cam_ema_update.argtypes = [vp, ctypes.c_float]
     L.cam_drift_norm.argtypes = [vp, vp, vp]
@@ -163,18 +169,19 @@ def _ptrs(values: Sequence[int] | None):
 
 def ctx_create(numel: Sequence[int], master: Sequence[int], *, fragment_of=None,
                n_fragments: int = 1, quorum: int = 1, momentum=None, ema=None,
-               device: int = 0, flags: int = 0, stream: int = 0) -> int:
+               device: int = 0, flags: int = 0, stream: int = 0, swa=None) -> int:
     n = len(numel)
     numel_a = (ctypes.c_int64 * max(1, n))(*[int(v) for v in numel])
     frag_a = None if fragment_of is None else (ctypes.c_int32 * max(1, n))(*fragment_of)
-    keep = [numel_a, frag_a, _ptrs(master), _ptrs(momentum), _ptrs(ema)]
+    keep = [numel_a, frag_a, _ptrs(master), _ptrs(momentum), _ptrs(ema), _ptrs(swa)]
     d = CtxDesc(n, numel_a,
                 None if frag_a is None else ctypes.cast(frag_a, ctypes.POINTER(ctypes.c_int32)),
                 n_fragments, quorum,
                 ctypes.cast(keep[2], ctypes.POINTER(ctypes.c_void_p)),
                 None if keep[3] is None else ctypes.cast(keep[3], ctypes.POINTER(ctypes.c_void_p)),
                 None if keep[4] is None else ctypes.cast(keep[4], ctypes.POINTER(ctypes.c_void_p)),
-                device, flags, stream or None)
+                device, flags, stream or None,
+                None if keep[5] is None else ctypes.cast(keep[5], ctypes.POINTER(ctypes.c_void_p)))
     out = ctypes.c_void_p()
     _check(lib().cam_ctx_create(ctypes.byref(d), ctypes.byref(out)))
     return out.value
@@ -208,6 +215,25 @@ def merge_finalize(rd: int, mode: int, lr: float = 1.0, mu: float = 0.0) -> None
 
 def ema_update(rd: int, beta: float) -> None:
     _check(lib().cam_ema_update(rd, beta))
+
+
+def swa_update(rd: int) -> None:
+    _check(lib().cam_swa_update(rd))
+
+
+def swa_reset(ctx: int, fragment: int = -1, stream: int = 0) -> None:
+    _check(lib().cam_swa_reset(ctx, fragment, stream or None))
+
+
+def swa_counts(ctx: int, n_tensors: int) -> list[int]:
+    out = (ctypes.c_int64 * max(1, n_tensors))()
+    _check(lib().cam_swa_counts(ctx, out))
+    return list(out[:n_tensors])
+
+
+def swa_set_counts(ctx: int, counts: Sequence[int]) -> None:
+    arr = (ctypes.c_int64 * max(1, len(counts)))(*[int(c) for c in counts])
+    _check(lib().cam_swa_set_counts(ctx, arr))
 
 
 def drift_norm(rd: int, per_tensor: int | None, per_fragment: int | None) -> None:
@@ -281,6 +307,32 @@ def merge_round_noalloc(numel: Sequence[int], master: Sequence[int], ckpt: Seque
         int(ema is not None), beta, per_tensor or None, per_round or None, stream or None))
 
 
+def average_snapshots(out, snapshots, stream=None) -> None:
+    """out[t] = plain mean of snapshots[j][t] over j, for stored globals (the
+    averages of the last n snapshots of the DiffuRefill-1B technical report,
+    Table 5). One merge pass in plain-mean mode with the snapshots as the
+    workers and `out` as the global; at most KMAX snapshots; fp32 or bf16."""
+    torch = _torch()
+    out = list(out)
+    snaps = [list(sn) for sn in snapshots]
+    if not 1 <= len(snaps) <= KMAX:
+        raise ValueError(f"1..{KMAX} snapshots")
+    dt = snaps[0][0].dtype if out else torch.float32
+    for sn in snaps:
+        if len(sn) != len(out):
+            raise ValueError("every snapshot needs one tensor per output tensor")
+        for a, b in zip(sn, out):
+            if a.numel() != b.numel() or a.dtype != dt or not a.is_contiguous():
+                raise ValueError("snapshot tensors must match the outputs")
+    for b in out:
+        if b.dtype != torch.float32 or not b.is_contiguous() or b.device.type != "cuda":
+            raise ValueError("outputs must be contiguous fp32 CUDA tensors")
+    merge_round_noalloc([b.numel() for b in out], [b.data_ptr() for b in out],
+                        [[a.data_ptr() for a in sn] for sn in snaps],
+                        BF16 if dt == torch.bfloat16 else F32, MEAN_REPLACE,
+                        stream=_stream_handle(stream))
+
+
 # ---- torch-facing layer ----------------------------------------------------------
 
 def _torch():
@@ -302,18 +354,19 @@ class Merger:
 
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
-                 zero_momentum=False, stream=None):
+                 zero_momentum=False, stream=None, swa=None, zero_swa=False):
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
         self.ema = None if ema is None else list(ema)
+        self.swa = None if swa is None else list(swa)
         if not self.master:
             raise ValueError("empty parameter list")
         dev = self.master[0].device
         if dev.type != "cuda":
             raise ValueError("master tensors must be CUDA tensors")
         self.device = dev
-        for group in (self.master, self.momentum, self.ema):
+        for group in (self.master, self.momentum, self.ema, self.swa):
             if group is None:
                 continue
             if len(group) != len(self.master):
@@ -326,7 +379,7 @@ class Merger:
         self.fragment_of = list(fragment_of) if fragment_of is not None else [0] * len(self.master)
         self.n_fragments = n_fragments
         flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
-                (INIT_ZERO_MOMENTUM if zero_momentum else 0)
+                (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,
@@ -334,7 +387,8 @@ class Merger:
                 momentum=None if self.momentum is None else [t.data_ptr() for t in self.momentum],
                 ema=None if self.ema is None else [t.data_ptr() for t in self.ema],
                 device=dev.index if dev.index is not None else torch.cuda.current_device(),
-                flags=flags, stream=_stream_handle(stream))
+                flags=flags, stream=_stream_handle(stream),
+                swa=None if self.swa is None else [t.data_ptr() for t in self.swa])
         self._frag_cache = {}
 
     def close(self):
@@ -362,6 +416,19 @@ class Merger:
         if fragment not in self._frag_cache:
             self._frag_cache[fragment] = fragment_info(self.ctx, fragment)[0]
         return self._frag_cache[fragment]
+
+    @property
+    def swa_counts(self) -> list[int]:
+        """Globals folded into each tensor's running average."""
+        return swa_counts(self.ctx, len(self.master))
+
+    @swa_counts.setter
+    def swa_counts(self, counts) -> None:
+        swa_set_counts(self.ctx, counts)
+
+    def swa_reset(self, fragment: int = -1, stream=None) -> None:
+        """Zeroes the running averages of `fragment` (-1: all) and their counts."""
+        swa_reset(self.ctx, fragment, _stream_handle(stream))
 
     @property
     def launch_count(self) -> int:
@@ -447,6 +514,9 @@ class Round:
 
     def ema_update(self, beta: float) -> None:
         ema_update(self.handle, beta)
+
+    def swa_update(self) -> None:
+        swa_update(self.handle)
 
     def drift_norm(self, per_tensor=None, per_fragment=None) -> None:
         torch = _torch()

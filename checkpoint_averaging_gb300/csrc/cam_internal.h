@@ -35,6 +35,7 @@ struct TensorSlot {
     float* theta;
     float* m;
     float* e;
+    float* swa;  // uniform running average of the globals, or null
     int64_t numel;
 };
 
@@ -53,6 +54,7 @@ struct MergeArgs {
     float w[CAM_KMAX];        // (float)tokens_k
     float W;                  // (float)sum tokens
     float lr, mu, beta;
+    float swa_n;              // globals in the running average after this round
     uint32_t vec[(kXCap + 31) / 32];  // bit l: tensor local0+l takes the vector path
     // x[l*stride + k]: worker k's copy of tensor local0+l; when publishing,
     // x[l*stride + K] and x[l*stride + K + 1] take the new theta and EMA. The
@@ -78,10 +80,14 @@ enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 int record_error(int code, const char* fmt, ...);
 
 // Launches one fused merge pass with `grid` blocks.
-cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
-                         int grid, cudaStream_t s);
+// Variant selection of the fused pass.
+struct MergeVariant {
+    int dtype, mode;
+    bool ema, norm, pub, swa;
+};
+cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cudaStream_t s);
 // Resident blocks per SM of that variant (0 on error).
-int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm, bool pub);
+int merge_blocks_per_sm(const MergeVariant& v);
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_fill(float* dst, int64_t n, float v, cudaStream_t s);
 cudaError_t launch_copy(float* dst, const float* src, int64_t n, cudaStream_t s);

@@ -122,9 +122,18 @@ __device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMA
     }
 }
 
+// Folds the new global into the uniform running average: mu + (theta' - mu)/n,
+// n = the number of globals in the average after this one.
+template <class A>
+__device__ __forceinline__ float swa_fold(const A& a, float mu, float th) {
+    return __fadd_rn(mu, __fdiv_rn(__fsub_rn(th, mu), a.swa_n));
+}
+
 // xs[0..K) are the workers' copies of the tensor; with PUB, xs[K] receives a
 // copy of the new theta and xs[K+1] (when not null) a copy of the new EMA.
-template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, class A>
+// With SWA the uniform running average ts.swa is updated from the new theta.
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, bool SWA = false,
+          class A>
 __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
                                            const TensorSlot& ts, int64_t i, float& acc) {
     XVec<XT> x[CAM_KMAX];
@@ -135,14 +144,18 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
     if (MODE == kDelta || NORM) load_s8(ts.theta + i, th);
     if (MODE == kDelta) load_s8(ts.m + i, m);
     if (EMA) load_s8(ts.e + i, e);
+    float sw[8];
+    if constexpr (SWA) load_s8(ts.swa + i, sw);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         float xk[CAM_KMAX];
 #pragma unroll
         for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
         merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
+        if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
     }
     store_s8(ts.theta + i, th);
+    if constexpr (SWA) store_s8(ts.swa + i, sw);
     if (MODE == kDelta) store_s8(ts.m + i, m);
     if (EMA) store_s8(ts.e + i, e);
     if (PUB) {
@@ -151,7 +164,8 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
     }
 }
 
-template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, class A>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, bool SWA = false,
+          class A>
 __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
                                           const TensorSlot& ts, int64_t i, float& acc) {
     float xk[CAM_KMAX];
@@ -165,6 +179,7 @@ __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
     ts.theta[i] = th;
     if (MODE == kDelta) ts.m[i] = m;
     if (EMA) ts.e[i] = e;
+    if constexpr (SWA) ts.swa[i] = swa_fold(a, ts.swa[i], th);
     if (PUB) {
         static_cast<float*>(const_cast<void*>(xs[a.K]))[i] = th;
         if (EMA && xs[a.K + 1]) static_cast<float*>(const_cast<void*>(xs[a.K + 1]))[i] = e;

@@ -36,7 +36,7 @@ using namespace cam::dev;
 
 // ---- the fused pass ------------------------------------------------------------
 
-template <typename XT, int MODE, bool EMA, bool NORM, bool PUB>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB, bool SWA>
 __global__ void __launch_bounds__(kThreads, 2)
     merge_fused(const __grid_constant__ MergeArgs a) {
     __shared__ double warp_part[kThreads / 32];
@@ -50,14 +50,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (vec) {
             const int nv = ch.len >> 3;
             for (int v = threadIdx.x; v < nv; v += kThreads)
-                merge_vec8<XT, MODE, EMA, NORM, PUB>(a, xs, ts, ch.start + 8 * int64_t(v), acc);
+                merge_vec8<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts, ch.start + 8 * int64_t(v), acc);
             const int tail = ch.len & 7;
             if (static_cast<int>(threadIdx.x) < tail)
-                merge_one<XT, MODE, EMA, NORM, PUB>(a, xs, ts,
+                merge_one<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts,
                                                     ch.start + 8 * int64_t(nv) + threadIdx.x, acc);
         } else {
             for (int j = threadIdx.x; j < ch.len; j += kThreads)
-                merge_one<XT, MODE, EMA, NORM, PUB>(a, xs, ts, ch.start + j, acc);
+                merge_one<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts, ch.start + j, acc);
         }
         if (NORM) {
             // fp32 within a thread (at most a few dozen squares), fp64 above.
@@ -114,38 +114,42 @@ __global__ void copy_kernel(float* dst, const float* src, int64_t n) {
 
 using MergeFn = void (*)(MergeArgs);
 
-template <typename XT, int MODE, bool PUB>
-MergeFn pick3(bool ema, bool norm) {
-    if (ema) return norm ? merge_fused<XT, MODE, true, true, PUB> : merge_fused<XT, MODE, true, false, PUB>;
-    return norm ? merge_fused<XT, MODE, false, true, PUB> : merge_fused<XT, MODE, false, false, PUB>;
+template <typename XT, int MODE, bool PUB, bool SWA>
+MergeFn pick_en(bool ema, bool norm) {
+    if (ema)
+        return norm ? merge_fused<XT, MODE, true, true, PUB, SWA>
+                    : merge_fused<XT, MODE, true, false, PUB, SWA>;
+    return norm ? merge_fused<XT, MODE, false, true, PUB, SWA>
+                : merge_fused<XT, MODE, false, false, PUB, SWA>;
 }
 
-template <bool PUB>
-MergeFn pick_pub(int dtype, int mode, bool ema, bool norm) {
-    if (dtype == kDtBF16)
-        return mode == kDelta ? pick3<uint16_t, kDelta, PUB>(ema, norm)
-                              : pick3<uint16_t, kMean, PUB>(ema, norm);
-    return mode == kDelta ? pick3<float, kDelta, PUB>(ema, norm) : pick3<float, kMean, PUB>(ema, norm);
+template <bool PUB, bool SWA>
+MergeFn pick_dm(const MergeVariant& v) {
+    if (v.dtype == kDtBF16)
+        return v.mode == kDelta ? pick_en<uint16_t, kDelta, PUB, SWA>(v.ema, v.norm)
+                                : pick_en<uint16_t, kMean, PUB, SWA>(v.ema, v.norm);
+    return v.mode == kDelta ? pick_en<float, kDelta, PUB, SWA>(v.ema, v.norm)
+                            : pick_en<float, kMean, PUB, SWA>(v.ema, v.norm);
 }
 
-MergeFn pick(int dtype, int mode, bool ema, bool norm, bool pub) {
-    return pub ? pick_pub<true>(dtype, mode, ema, norm) : pick_pub<false>(dtype, mode, ema, norm);
+MergeFn pick(const MergeVariant& v) {
+    if (v.pub) return v.swa ? pick_dm<true, true>(v) : pick_dm<true, false>(v);
+    return v.swa ? pick_dm<false, true>(v) : pick_dm<false, false>(v);
 }
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
-                         int grid, cudaStream_t s) {
-    MergeFn fn = pick(dtype, mode, ema, norm, pub);
+cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cudaStream_t s) {
+    MergeFn fn = pick(v);
     void* args[] = {const_cast<MergeArgs*>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads),
                             args, 0, s);
 }
 
-int merge_blocks_per_sm(int dtype, int mode, bool ema, bool norm, bool pub) {
+int merge_blocks_per_sm(const MergeVariant& v) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, reinterpret_cast<const void*>(pick(dtype, mode, ema, norm, pub)), kThreads, 0) !=
+            &n, reinterpret_cast<const void*>(pick(v)), kThreads, 0) !=
         cudaSuccess)
         return 0;
     return n;

@@ -312,7 +312,7 @@ CAM_API int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, flo
             float* th = master[t];
             float* m = delta ? momentum[t] : nullptr;
             float* e = do_ema ? ema[t] : nullptr;
-            a.slots[l] = cam::TensorSlot{th, m, e, numel[t]};
+            a.slots[l] = cam::TensorSlot{th, m, e, nullptr, numel[t]};
             bool v = cam::aligned(th, 32) && (!delta || cam::aligned(m, 32)) &&
                      (!do_ema || cam::aligned(e, 32));
             for (int k = 0; k < n_workers; ++k) {

@@ -109,15 +109,16 @@ struct cam_ctx {
     int32_t quorum = 1;
     std::vector<int64_t> numel;
     std::vector<int32_t> fragment_of;
-    std::vector<float*> theta, m, e;
-    bool has_m = false, has_e = false;
+    std::vector<float*> theta, m, e, swa;
+    bool has_m = false, has_e = false, has_swa = false;
+    std::vector<int64_t> swa_count;  // globals folded into each tensor's running average
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
     int64_t last_round = -1;
     int64_t launches = 0;
     std::vector<cam_round*> open;
-    int bps[2][2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm][publish]
+    int bps[2][2][2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm][publish][swa]
     std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
 
     Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
@@ -142,6 +143,7 @@ struct cam_round {
     bool norms = false;
     double* out_tensor = nullptr;
     double* out_fragment = nullptr;
+    bool swa = false;
     bool publish = false;
     bool publish_ema = false;
     std::vector<void*> pub_theta, pub_ema;  // [T_f] device-visible addresses
@@ -186,12 +188,14 @@ int validate_desc(const cam_ctx_desc* d) {
     if (d->quorum < 1 || d->quorum > CAM_KMAX)
         return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
-    if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM))
+    if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
     if ((d->flags & CAM_INIT_ZERO_MOMENTUM) && !d->momentum)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_ZERO_MOMENTUM without momentum buffers");
+    if ((d->flags & CAM_INIT_ZERO_SWA) && !d->swa)
+        return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_ZERO_SWA without average buffers");
     for (int32_t t = 0; t < d->n_tensors; ++t) {
         const int64_t n = d->numel[t];
         if (n < 0) return fail(CAM_E_ARG, "cam_ctx_create: numel[%d] < 0", t);
@@ -204,6 +208,8 @@ int validate_desc(const cam_ctx_desc* d) {
             return fail(CAM_E_ARG, "cam_ctx_create: momentum[%d] is NULL", t);
         if (n > 0 && d->ema && !d->ema[t])
             return fail(CAM_E_ARG, "cam_ctx_create: ema[%d] is NULL", t);
+        if (n > 0 && d->swa && !d->swa[t])
+            return fail(CAM_E_ARG, "cam_ctx_create: swa[%d] is NULL", t);
     }
     return CAM_OK;
 }
@@ -248,10 +254,14 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->theta.assign(d->master, d->master + d->n_tensors);
     c->has_m = d->momentum != nullptr;
     c->has_e = d->ema != nullptr;
+    c->has_swa = d->swa != nullptr;
     c->m.assign(d->n_tensors, nullptr);
     c->e.assign(d->n_tensors, nullptr);
+    c->swa.assign(d->n_tensors, nullptr);
     if (c->has_m) c->m.assign(d->momentum, d->momentum + d->n_tensors);
     if (c->has_e) c->e.assign(d->ema, d->ema + d->n_tensors);
+    if (c->has_swa) c->swa.assign(d->swa, d->swa + d->n_tensors);
+    c->swa_count.assign(d->n_tensors, 0);
 
     // Plans and one device block holding every plan's tables.
     c->plans.resize(c->n_fragments + 1);
@@ -279,7 +289,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     };
     for (Plan& p : c->plans) {
         std::vector<TensorSlot> slots;
-        for (int32_t g : p.tensors) slots.push_back(TensorSlot{c->theta[g], c->m[g], c->e[g], c->numel[g]});
+        for (int32_t g : p.tensors)
+            slots.push_back(TensorSlot{c->theta[g], c->m[g], c->e[g], c->swa[g], c->numel[g]});
         size_t o;
         o = carve(sizeof(ChunkDesc) * p.chunks.size());
         if (!p.chunks.empty()) std::memcpy(&host[o], p.chunks.data(), sizeof(ChunkDesc) * p.chunks.size());
@@ -305,8 +316,10 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
             for (int em = 0; em < 2; ++em)
                 for (int nm = 0; nm < 2; ++nm)
                     for (int pb = 0; pb < 2; ++pb)
-                        c->bps[dt][md][em][nm][pb] =
-                            std::max(1, cam::merge_blocks_per_sm(dt, md, em, nm, pb));
+                        for (int sw = 0; sw < 2; ++sw)
+                            c->bps[dt][md][em][nm][pb][sw] = std::max(
+                                1, cam::merge_blocks_per_sm(cam::MergeVariant{
+                                       dt, md, em != 0, nm != 0, pb != 0, sw != 0}));
 
     cudaStream_t s = static_cast<cudaStream_t>(d->stream);
     for (int32_t t = 0; t < c->n_tensors && ce == cudaSuccess; ++t) {
@@ -317,6 +330,10 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         }
         if (ce == cudaSuccess && (d->flags & CAM_INIT_EMA_FROM_MASTER)) {
             ce = cam::launch_copy(c->e[t], c->theta[t], c->numel[t], s);
+            ++c->launches;
+        }
+        if (ce == cudaSuccess && (d->flags & CAM_INIT_ZERO_SWA)) {
+            ce = cam::launch_fill(c->swa[t], c->numel[t], 0.0f, s);
             ++c->launches;
         }
     }
@@ -471,6 +488,14 @@ CAM_API int cam_ema_update(cam_round* r, float beta) {
     return CAM_OK;
 }
 
+CAM_API int cam_swa_update(cam_round* r) {
+    if (!r) return fail(CAM_E_ARG, "cam_swa_update: round is NULL");
+    if (r->swa) return fail(CAM_E_STATE, "cam_swa_update: asked twice");
+    if (!r->ctx->has_swa) return fail(CAM_E_ARG, "cam_swa_update: context has no average buffers");
+    r->swa = true;
+    return CAM_OK;
+}
+
 CAM_API int cam_drift_norm(cam_round* r, double* per_tensor, double* per_fragment) {
     if (!r) return fail(CAM_E_ARG, "cam_drift_norm: round is NULL");
     if (r->norms) return fail(CAM_E_STATE, "cam_drift_norm: asked twice");
@@ -542,6 +567,18 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     const Plan& p = c->plan_of(r->fragment);
     const int K = r->K;
     const int T = p.n_tensors();
+    int64_t swa_prev = -1;
+    if (r->swa) {
+        for (int32_t g : p.tensors) {
+            if (c->numel[g] == 0) continue;
+            if (swa_prev >= 0 && c->swa_count[g] != swa_prev)
+                return fail(CAM_E_STATE,
+                            "cam_merge_commit: the fragment's running averages hold different "
+                            "numbers of globals (reset them together)");
+            swa_prev = c->swa_count[g];
+        }
+        if (swa_prev < 0) swa_prev = 0;
+    }
     const bool delta = r->mode == CAM_MODE_DELTA_NESTEROV;
     const uintptr_t xa = r->dtype == CAM_F32 ? 32 : 16;
     MergeArgs& a = *c->args;
@@ -553,7 +590,9 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.lr = r->lr;
     a.mu = r->mu;
     a.beta = r->beta;
-    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms][r->publish];
+    a.swa_n = static_cast<float>(swa_prev + 1);
+    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms][r->publish][r->swa];
+    const cam::MergeVariant variant{r->dtype, r->mode, r->ema, r->norms, r->publish, r->swa};
     const int stride = K + (r->publish ? 2 : 0);
     a.stride = stride;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -573,7 +612,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         for (int l = 0; l < n; ++l) {
             const int32_t g = p.tensors[l0 + l];
             bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
-                     (!r->ema || aligned(c->e[g], 32));
+                     (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32));
             for (int k = 0; k < K; ++k) {
                 const void* xp = r->x[size_t(k) * T + l0 + l];
                 a.x[size_t(l) * stride + k] = xp;
@@ -594,7 +633,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         a.local0 = l0;
         a.n_local = n;
         const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
-        ce = cam::launch_merge(a, r->dtype, r->mode, r->ema, r->norms, r->publish, grid, s);
+        ce = cam::launch_merge(a, variant, grid, s);
         ++c->launches;
     }
     if (ce == cudaSuccess && r->norms) {
@@ -602,8 +641,48 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }
+    if (ce == cudaSuccess && r->swa)
+        for (int32_t g : p.tensors) c->swa_count[g] = swa_prev + 1;
     close_round(r);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_commit: launch");
+    return CAM_OK;
+}
+
+CAM_API int cam_swa_reset(cam_ctx* c, int32_t fragment, void* stream) {
+    if (!c) return fail(CAM_E_ARG, "cam_swa_reset: ctx is NULL");
+    if (!c->has_swa) return fail(CAM_E_ARG, "cam_swa_reset: context has no average buffers");
+    if (fragment < -1 || fragment >= c->n_fragments)
+        return fail(CAM_E_ARG, "cam_swa_reset: fragment %d out of [-1, %d)", fragment, c->n_fragments);
+    for (const cam_round* r : c->open)
+        if (r->fragment == -1 || fragment == -1 || r->fragment == fragment)
+            return fail(CAM_E_BUSY, "cam_swa_reset: fragment %d overlaps open round %lld", fragment,
+                        static_cast<long long>(r->round));
+    DeviceScope scope(c->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_swa_reset: cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Plan& p = c->plan_of(fragment);
+    for (int32_t g : p.tensors) {
+        if (c->numel[g] == 0) continue;
+        cudaError_t ce = cam::launch_fill(c->swa[g], c->numel[g], 0.0f, s);
+        ++c->launches;
+        if (ce != cudaSuccess) return cuda_fail(ce, "cam_swa_reset: launch");
+    }
+    for (int32_t g : p.tensors) c->swa_count[g] = 0;
+    return CAM_OK;
+}
+
+CAM_API int cam_swa_counts(const cam_ctx* c, int64_t* counts) {
+    if (!c || !counts) return fail(CAM_E_ARG, "cam_swa_counts: NULL argument");
+    std::memcpy(counts, c->swa_count.data(), sizeof(int64_t) * c->swa_count.size());
+    return CAM_OK;
+}
+
+CAM_API int cam_swa_set_counts(cam_ctx* c, const int64_t* counts) {
+    if (!c || !counts) return fail(CAM_E_ARG, "cam_swa_set_counts: NULL argument");
+    if (!c->open.empty()) return fail(CAM_E_STATE, "cam_swa_set_counts: a round is open");
+    for (int32_t t = 0; t < c->n_tensors; ++t)
+        if (counts[t] < 0) return fail(CAM_E_ARG, "cam_swa_set_counts: counts[%d] < 0", t);
+    c->swa_count.assign(counts, counts + c->n_tensors);
     return CAM_OK;
 }
 

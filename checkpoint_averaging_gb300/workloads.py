@@ -186,6 +186,7 @@ class Workload:
     tokens: tuple | None = None  # inclusive integer range
     norms: bool = False
     workers_track_global: bool = False  # workers start from the current global
+    swa: bool = False                   # also fold each global into the uniform average
 
     @property
     def n_params(self) -> int:
@@ -219,6 +220,14 @@ def _wl_1b() -> Workload:
                     ema_beta=0.9, rounds=((0, -1),), noise_std=1e-3)
 
 
+def _wl_1b_swa() -> Workload:
+    """The 1.08B round of the final stretch: plain mean + EMA + the uniform
+    average of the globals, all in one pass."""
+    return Workload("diffurefill1b_k5_f32_mean_ema_swa", tuple(diffurefill1b_specs(1)), 1,
+                    K=5, n_masked=0, quorum=5, ckpt_dtype="f32", mode="mean",
+                    ema_beta=0.9, rounds=((0, -1),), noise_std=1e-3, swa=True)
+
+
 def _wl_1b_bf16() -> Workload:
     return Workload("diffurefill1b_bf16_f4_q3_delta_nesterov_norms",
                     tuple(diffurefill1b_specs(4)), 4, K=5, n_masked=2, quorum=3,
@@ -246,6 +255,7 @@ def workload(name: str) -> Workload:
         "stand": _wl_stand,
         "diffurefill1b": _wl_1b,
         "diffurefill1b_bf16": _wl_1b_bf16,
+        "diffurefill1b_swa": _wl_1b_swa,
     }
     if name in table:
         return table[name]()

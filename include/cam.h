@@ -77,6 +77,7 @@ typedef enum {
 /* cam_ctx_desc.flags */
 #define CAM_INIT_EMA_FROM_MASTER 1u /* at create: e <- theta (EMA starts at the first global) */
 #define CAM_INIT_ZERO_MOMENTUM 2u   /* at create: m <- 0 */
+#define CAM_INIT_ZERO_SWA 4u        /* at create: running averages <- 0, no globals folded */
 
 typedef struct cam_ctx cam_ctx;     /* opaque */
 typedef struct cam_round cam_round; /* opaque */
@@ -104,6 +105,8 @@ typedef struct {
     int32_t device;             /* CUDA device ordinal holding the buffers */
     uint32_t flags;             /* CAM_INIT_* */
     void* stream;               /* cudaStream_t for the CAM_INIT_* work; NULL = default */
+    float* const* swa;          /* host array of n_tensors device pointers, or NULL:
+                                   uniform running averages of the globals */
 } cam_ctx_desc;
 
 /*
@@ -173,6 +176,18 @@ int cam_merge_finalize(cam_round* rd, cam_mode mode, float lr, float mu);
  * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
  */
 int cam_ema_update(cam_round* rd, float beta);
+
+/*
+ * Asks the same pass to fold the new global into each tensor's uniform
+ * running average: swa' = swa + (theta' - swa) / n, n = the globals in the
+ * average after this round (the first fold after a reset copies theta'
+ * exactly). The DiffuRefill-1B run released the uniform average of the 130
+ * globals of its final stretch ("DiffuRefill-1B" technical report, section 4
+ * and Table 5). Needs average buffers; all tensors of the round's fragment
+ * must hold the same number of globals (CAM_E_STATE at commit otherwise).
+ * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
+ */
+int cam_swa_update(cam_round* rd);
 
 /*
  * Asks for drift norms, written on the commit stream: per_tensor[T_f] (device
@@ -279,6 +294,17 @@ int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, float* cons
 
 /* Message describing the calling thread's last error ("" if none). */
 const char* cam_last_error(void);
+
+/* Starts the running averages of `fragment` (-1: all) afresh: zeroes them on
+ * `stream` and sets their counts to 0. Errors: CAM_E_ARG, CAM_E_BUSY (an open
+ * round overlaps the fragment), CAM_E_CUDA. */
+int cam_swa_reset(cam_ctx* ctx, int32_t fragment, void* stream);
+
+/* The number of globals in each tensor's running average (counts, host,
+ * [n_tensors]), and restoring it when a merger restarts from saved state
+ * (CAM_E_STATE while a round is open). */
+int cam_swa_counts(const cam_ctx* ctx, int64_t* counts);
+int cam_swa_set_counts(cam_ctx* ctx, const int64_t* counts);
 
 /* Library version, e.g. "0.1.0". */
 const char* cam_version(void);

@@ -62,6 +62,7 @@ class GpuState:
     m: W.Arena | None
     e: W.Arena | None
     merger: B.Merger
+    swa: W.Arena | None = None
 
 
 def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None) -> GpuState:
@@ -72,10 +73,12 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None) -> GpuState:
     if wl.ema_beta is not None:
         e = W.empty_arena(g.numels, torch.float32, dev)
         e.flat.copy_(g.flat)  # EMA starts at the first global
+    swa = W.empty_arena(g.numels, torch.float32, dev) if wl.swa else None
     mg = B.Merger(theta.views, momentum=None if m is None else m.views,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
-                  n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum)
-    return GpuState(theta, m, e, mg)
+                  n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
+                  swa=None if swa is None else swa.views)
+    return GpuState(theta, m, e, mg, swa)
 
 
 def gpu_round(st: GpuState, wl: W.Workload, rnd: int, frag: int, workers, draw,
@@ -88,6 +91,8 @@ def gpu_round(st: GpuState, wl: W.Workload, rnd: int, frag: int, workers, draw,
     rd.finalize(B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE, wl.lr, wl.mu)
     if wl.ema_beta is not None:
         rd.ema_update(wl.ema_beta)
+    if wl.swa:
+        rd.swa_update()
     out = None
     if wl.norms if norms is None else norms:
         dev = st.theta.flat.device
@@ -105,7 +110,9 @@ def oracle_state_from(g: W.Arena, wl: W.Workload) -> oracle.OracleState:
         theta=th,
         m=[np.zeros(n, np.float32) for n in g.numels] if wl.mode == "delta" else None,
         e=[t.copy() for t in th] if wl.ema_beta is not None else None,
-        fragment_of=wl.fragment_of)
+        fragment_of=wl.fragment_of,
+        swa=[np.zeros(n, np.float32) for n in g.numels] if wl.swa else None,
+        swa_count=[0] * len(g.numels) if wl.swa else None)
 
 
 def oracle_round(ost: oracle.OracleState, wl: W.Workload, rnd: int, frag: int, workers,
@@ -116,7 +123,7 @@ def oracle_round(ost: oracle.OracleState, wl: W.Workload, rnd: int, frag: int, w
         tokens=draw.tokens if wl.mode == "delta" else None,
         mode=oracle.DELTA_NESTEROV if wl.mode == "delta" else oracle.MEAN_REPLACE,
         lr=wl.lr, mu=wl.mu, quorum=wl.quorum if quorum is None else quorum,
-        ema_beta=wl.ema_beta)
+        ema_beta=wl.ema_beta, swa_update=wl.swa)
 
 
 def compare_full(st: GpuState, ost: oracle.OracleState, what: str, bitwise=False) -> None:
@@ -127,6 +134,8 @@ def compare_full(st: GpuState, ost: oracle.OracleState, what: str, bitwise=False
             pairs.append(("m", st.m, ost.m))
         if st.e is not None:
             pairs.append(("e", st.e, ost.e))
+        if st.swa is not None:
+            pairs.append(("swa", st.swa, ost.swa))
         for name, arena, ref in pairs:
             got = to_np(arena.views[t])
             assert_close(got, ref[t], f"{what}: {name}[{t}]")

@@ -509,3 +509,92 @@ def test_publish_ema_needs_an_ema_update():
     torch.cuda.synchronize()
     assert torch.equal(out[0], th[0]) and torch.equal(out[1], th[1])
     mg.close()
+
+
+# ---- uniform average of the globals (SWA) and snapshot averages --------------------
+
+def _swa_workload(rounds, mode="delta", dtype="bf16"):
+    wl = _custom(RAGGED, K=3, mode=mode, dtype=dtype, frags=[i % 2 for i in range(len(RAGGED))],
+                 n_fragments=2, rounds=rounds)
+    return W.Workload(wl.name, wl.specs, wl.n_fragments, K=wl.K, n_masked=0, quorum=3,
+                      ckpt_dtype=dtype, mode=mode, lr=wl.lr, mu=wl.mu, ema_beta=0.9,
+                      rounds=rounds, tokens=wl.tokens, norms=True, swa=True)
+
+
+@pytest.mark.parametrize("mode,dtype", [("delta", "bf16"), ("mean", "f32")])
+def test_swa_over_fragment_rounds_matches_oracle(mode, dtype):
+    wl = _swa_workload(((0, 0), (1, 1), (2, 0), (3, 1), (4, -1)), mode, dtype)
+    st, ost = run_full(wl, seed=12, bitwise=True)
+    assert ost.swa_count == [3] * len(RAGGED)
+
+
+def test_swa_counts_must_agree_within_a_round():
+    wl = _swa_workload(((0, 0),))
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(3)]
+    gpu_round(st, wl, 0, 0, workers, draw)          # fragment 0 now holds one global
+    rd = st.merger.begin(1, -1)
+    for k in draw.included:
+        rd.accumulate(workers[k].views, draw.tokens[k])
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.swa_update()
+    with pytest.raises(B.StateError, match="different"):
+        rd.commit()
+    rd.abort()
+    counts = st.merger.swa_counts
+    assert [counts[t] for t in range(len(RAGGED)) if t % 2 == 0 and RAGGED[t]] == \
+        [1] * sum(1 for t in range(0, len(RAGGED), 2) if RAGGED[t])
+    st.merger.swa_reset(0)
+    assert all(c == 0 for c in st.merger.swa_counts)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(st.swa.flat) == 0
+    st.merger.swa_counts = [5] * len(RAGGED)       # resume from saved counts
+    assert st.merger.swa_counts == [5] * len(RAGGED)
+    rd = st.merger.begin(2, 1)
+    with pytest.raises(B.BusyError):
+        st.merger.swa_reset(-1)
+    with pytest.raises(B.StateError):
+        st.merger.swa_counts = [0] * len(RAGGED)
+    rd.abort()
+    st.merger.close()
+
+
+def test_swa_on_the_1b_list_two_rounds_sampled():
+    wl = W.workload("diffurefill1b_swa")
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    rng = np.random.default_rng(3)
+    draw = W.draw_round(wl, 0, 0)
+    idxs = [sample_indices(s.numel, 1024, rng) for s in wl.specs]
+    tensors = list(range(len(wl.specs)))
+    for rnd in (0, 1):
+        workers = [W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)]
+        before = gather_state(st, tensors, idxs)
+        swa_before = [to_np(st.swa.views[t][torch.from_numpy(i).to(DEV)]) for t, i in zip(tensors, idxs)]
+        gpu_round(st, wl, rnd, -1, workers, draw)
+        torch.cuda.synchronize()
+        sampled_round_check(wl, st, -1, workers, draw, idxs, before, f"swa round {rnd}")
+        th_after = [to_np(st.theta.views[t][torch.from_numpy(i).to(DEV)]) for t, i in zip(tensors, idxs)]
+        for t, i in zip(tensors, idxs):
+            want = swa_before[t].copy()
+            oracle.swa(th_after[t], rnd + 1, want)
+            assert_close(to_np(st.swa.views[t][torch.from_numpy(i).to(DEV)]), want, f"swa[{t}]")
+        del workers
+    st.merger.close()
+
+
+@pytest.mark.parametrize("window,dtype", [(3, "f32"), (5, "f32"), (5, "bf16")])
+def test_average_of_the_last_snapshots_matches_oracle(window, dtype):
+    specs = tuple(W.TensorSpec(f"t{i}", (n,), 0) for i, n in enumerate(RAGGED))
+    wl = W.Workload("snap", specs, 1, K=window, n_masked=0, quorum=window, ckpt_dtype=dtype,
+                    mode="mean")
+    g = W.make_global(wl, 1, DEV)
+    snaps = [W.make_worker(wl, g, 0, j, 1, DEV) for j in range(window)]
+    out = W.empty_arena(g.numels, torch.float32, DEV)
+    B.average_snapshots(out.views, [s.views for s in snaps])
+    torch.cuda.synchronize()
+    for t in range(len(RAGGED)):
+        want = oracle.plain_average([to_np(s.views[t]) for s in snaps])
+        assert bitwise_equal(to_np(out.views[t]), want)
