@@ -54,11 +54,14 @@ def lib():
         L.ora_outer_nesterov.argtypes = [i64, vp, f32, f32, vp, vp]
         L.ora_ema.argtypes = [i64, vp, f32, vp]
         L.ora_swa.argtypes = [i64, vp, i64, vp]
+        L.ora_worker_drift.argtypes = [i64, i32, vpp, i32, vp, vp]
+        L.ora_adopt_keep_drift.argtypes = [i64, vp, vp, vp, i32]
         L.ora_merge_tensor.argtypes = [i64, i32, vpp, i32, vp, i32, f32, f32,
                                        i32, f32, vp, vp, vp,
                                        ctypes.POINTER(ctypes.c_double)]
         for fn in (L.ora_widen_bf16, L.ora_plain_mean, L.ora_weighted_delta,
-                   L.ora_outer_nesterov, L.ora_ema, L.ora_swa, L.ora_merge_tensor):
+                   L.ora_outer_nesterov, L.ora_ema, L.ora_swa, L.ora_merge_tensor,
+                   L.ora_worker_drift, L.ora_adopt_keep_drift):
             fn.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -149,6 +152,28 @@ def swa(theta_new: np.ndarray, count: int, mu: np.ndarray) -> None:
     theta_new = _contig(theta_new, np.float32)
     assert mu.flags.c_contiguous and mu.dtype == np.float32
     _check(lib().ora_swa(theta_new.size, _ptr(theta_new), int(count), _ptr(mu)), "swa")
+
+
+def worker_drift(xs: Sequence[np.ndarray], theta: np.ndarray) -> list[float]:
+    """Per worker, the fp64 sum of (x_k - theta)^2 over the tensor (theta is
+    the global before the round)."""
+    xs = [np.ascontiguousarray(x) for x in xs]
+    dt = _dtype_code(xs[0])
+    theta = _contig(theta, np.float32)
+    pp, keep = _ptr_array(xs)
+    out = np.zeros(len(xs), np.float64)
+    _check(lib().ora_worker_drift(theta.size, len(xs), pp, dt, _ptr(theta), _ptr(out)),
+           "worker_drift")
+    return [float(v) for v in out]
+
+
+def adopt_keep_drift(theta_w: np.ndarray, g: np.ndarray, pushed: np.ndarray) -> None:
+    """In place on theta_w: theta_w + (g - pushed)."""
+    assert theta_w.dtype == np.float32 and theta_w.flags.c_contiguous
+    g = _contig(g, np.float32)
+    pushed = np.ascontiguousarray(pushed)
+    _check(lib().ora_adopt_keep_drift(theta_w.size, _ptr(theta_w), _ptr(g), _ptr(pushed),
+                                      _dtype_code(pushed)), "adopt_keep_drift")
 
 
 def plain_average(snapshots: Sequence[np.ndarray]) -> np.ndarray:

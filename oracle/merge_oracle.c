@@ -25,7 +25,10 @@
  *         stretch; section 5.4 / Table 5: uniform average and averages of
  *         the last 3 and 5 snapshots.
  *   [TR 5.1] same report, section 5.1 (Distributed optimisation): "local
- *         drift", the movement of the workers away from the last global.
+ *         drift", the movement of the workers away from the last global, and
+ *         the rejected alternative to plain replacement, adopting the global
+ *         as theta <- theta + (g - theta_pushed), which keeps each worker's
+ *         progress since its last push.
  *
  * Readings where the pages leave a step open (each is listed with its reason
  * in the design notes of the repository):
@@ -44,7 +47,10 @@
  *     folded since the average was last reset (mu_1 = theta_1 exactly);
  *   - drift: per tensor the L2 norm of the mean worker displacement
  *     (Delta in the token-weighted mode, mean - theta_old in the plain mode),
- *     squares summed in fp64 in index order.
+ *     squares summed in fp64 in index order; per worker, the L2 norm of that
+ *     worker's displacement x_k - theta_old;
+ *   - keeping local drift on adoption: theta_w + (g - theta_pushed), the
+ *     difference taken first, as the report writes it.
  *
  * Arithmetic: every operation below is one IEEE binary32 operation rounded to
  * nearest-even (the build passes -ffp-contract=off so no multiply-add is
@@ -191,6 +197,35 @@ int ora_swa(int64_t n, const float* theta_new, int64_t count, float* swa) {
     if (n < 0 || count < 1 || !theta_new || !swa) return ORA_EARG;
     float nf = (float)count;
     for (int64_t i = 0; i < n; ++i) swa[i] = swa_step(swa[i], theta_new[i], nf);
+    return ORA_OK;
+}
+
+/* Sum over elements of (x_k - theta)^2 for every worker k, each difference one
+ * fp32 subtraction, the squares summed in fp64 in index order [TR 5.1]. */
+int ora_worker_drift(int64_t n, int K, const void* const* x, int dtype,
+                     const float* theta, double* sumsq) {
+    if (n < 0 || K < 1 || K > ORA_KMAX || !x || !theta || !sumsq) return ORA_EARG;
+    for (int k = 0; k < K; ++k) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < n; ++i) {
+            float d = load_elem(x[k], dtype, i) - theta[i];
+            acc += (double)d * (double)d;
+        }
+        sumsq[k] = acc;
+    }
+    return ORA_OK;
+}
+
+/* Adopting the new global g while keeping the progress made since the push:
+ * theta_w <- theta_w + (g - theta_pushed) [TR 5.1]. theta_pushed has dtype
+ * `dtype` (the checkpoint as pushed); theta_w and g are fp32. */
+int ora_adopt_keep_drift(int64_t n, float* theta_w, const float* g, const void* pushed,
+                         int dtype) {
+    if (n < 0 || !theta_w || !g || !pushed) return ORA_EARG;
+    for (int64_t i = 0; i < n; ++i) {
+        float d = g[i] - load_elem(pushed, dtype, i);
+        theta_w[i] = theta_w[i] + d;
+    }
     return ORA_OK;
 }
 

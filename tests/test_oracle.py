@@ -475,3 +475,58 @@ def test_round_level_swa_tracks_the_rounds_globals():
         exact = [sum(ex(s[i]) for s in seen[t]) / 3 for i in range(st.theta[t].size)]
         for i, x in enumerate(exact):
             assert abs(ex(st.swa[t][i]) - x) <= 12 * U * max(abs(ex(s[i])) for s in seen[t])
+
+
+# ---- per-worker drift and keep-drift adoption (technical report, section 5.1) -----
+
+def test_worker_drift_matches_fsum_and_exact_case():
+    r = rng(30)
+    theta = r.normal(0, 0.02, 777).astype(np.float32)
+    xs = [(theta + r.normal(0, s, 777)).astype(np.float32) for s in (1e-3, 2e-3, 5e-4)]
+    got = oracle.worker_drift(xs, theta)
+    for x, v in zip(xs, got):
+        d = (x - theta).astype(np.float32)
+        assert v == pytest.approx(math.fsum(float(a) ** 2 for a in d), rel=1e-12)
+    assert got[1] > got[0] > got[2]          # ordered like the noise scales
+    t0 = np.zeros(2, np.float32)
+    assert oracle.worker_drift([np.array([3.0, 4.0], np.float32),
+                                np.array([0.0, 1.0], np.float32)], t0) == [25.0, 1.0]
+
+
+def test_worker_drift_bf16_uses_widened_values():
+    theta = np.zeros(2, np.float32)
+    x = np.array([0x3F80, 0xC000], np.uint16)  # 1.0, -2.0
+    assert oracle.worker_drift([x], theta) == [5.0]
+
+
+def test_keep_drift_adoption_exact_and_bounded():
+    # theta_w + (g - pushed): exact on representable inputs; a worker that did
+    # not move since its push lands on the global.
+    tw = np.array([1.0, 2.0, -3.0, 0.5], np.float32)
+    g = np.array([4.0, -2.0, 0.0, 0.25], np.float32)
+    p = np.array([0.5, 2.0, -1.0, 0.5], np.float32)
+    out = tw.copy()
+    oracle.adopt_keep_drift(out, g, p)
+    assert list(out) == [4.5, -2.0, -2.0, 0.25]
+    r = rng(31)
+    pushed = r.normal(0, 0.02, 500).astype(np.float32)
+    glob = (pushed + r.normal(0, 1e-3, 500)).astype(np.float32)
+    same = pushed.copy()
+    oracle.adopt_keep_drift(same, glob, pushed)   # no progress since the push
+    for i in range(500):                           # lands on the global (two roundings)
+        assert abs(ex(same[i]) - ex(glob[i])) <= 2 * U * (abs(ex(pushed[i])) + abs(ex(glob[i])))
+    tw = (pushed + r.normal(0, 1e-3, 500)).astype(np.float32)
+    out = tw.copy()
+    oracle.adopt_keep_drift(out, glob, pushed)
+    for i in range(500):
+        exact = ex(tw[i]) + ex(glob[i]) - ex(pushed[i])
+        bound = 2 * U * (abs(exact) + abs(ex(glob[i]) - ex(pushed[i])))
+        assert abs(ex(out[i]) - exact) <= bound
+
+
+def test_keep_drift_adoption_bf16_pushed():
+    tw = np.array([1.0, 1.0], np.float32)
+    g = np.array([2.0, 0.0], np.float32)
+    pushed = np.array([0x3F80, 0xBF80], np.uint16)   # 1.0, -1.0
+    oracle.adopt_keep_drift(tw, g, pushed)
+    assert list(tw) == [2.0, 2.0]
