@@ -314,6 +314,9 @@ def run_ours(args, wl, ws, rank, local) -> int:
     streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
     norm_out = [(torch.zeros(len(mg.fragment_tensors(f)) or 1, dtype=torch.float64, device=dev),
                  torch.zeros(1, dtype=torch.float64, device=dev)) for _, f in wl.rounds]
+    wnorm_out = [(torch.zeros(wl.K * max(1, len(mg.fragment_tensors(f))), dtype=torch.float64,
+                              device=dev), torch.zeros(wl.K, dtype=torch.float64, device=dev))
+                 for _, f in wl.rounds]
     mode = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
     round_no = [0]
     ev_pairs = []
@@ -342,6 +345,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
                 rd.swa_update()
             if wl.norms:
                 rd.drift_norm(*norm_out[i])
+            if wl.worker_norms:
+                rd.worker_drift_norm(*wnorm_out[i])
             if timed:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(s)
@@ -423,7 +428,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
             "data": "synthetic",
             "config": {"workload": wl.name, "n_params": wl.n_params, "K": wl.K,
                        "included": k_incl, "mode": wl.mode, "ema": wl.ema_beta is not None,
-                       "swa": wl.swa,
+                       "swa": wl.swa, "worker_norms": wl.worker_norms,
                        "norms": wl.norms, "rounds_per_step": len(wl.rounds),
                        "streams": n_streams, "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
@@ -519,6 +524,57 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
                     "workers host->device and the new global and EMA device->host"}
 
 
+def run_adopt(args, wl, ws, rank, local) -> int:
+    """Times keep-drift adoption, theta_w += g - theta_pushed, over the workload's
+    tensor list (technical report, section 5.1): 16 B/element with fp32 pushed
+    copies (theta_w read and written, g and the pushed copy read), 14 with bf16."""
+    import torch
+
+    import __graft_entry__
+    from checkpoint_averaging_gb300 import binding as B
+    from checkpoint_averaging_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = W.make_global(wl, args.seed, dev)
+    pushed = W.make_worker(wl, g, 0, 0, args.seed, dev)
+    local_w = W.make_worker(W.Workload(wl.name, wl.specs, 1, K=1, n_masked=0, quorum=1,
+                                       ckpt_dtype="f32", mode="mean"), g, 1, 1, args.seed, dev)
+    b_in = 2 if wl.ckpt_dtype == "bf16" else 4
+    step_bytes = (12 + b_in) * wl.n_params
+    s = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        B.adopt_keep_drift(local_w.views, g.views, pushed.views, s)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        evs = []
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            B.adopt_keep_drift(local_w.views, g.views, pushed.views, s)
+            b.record(s)
+            evs.append((a, b))
+        torch.cuda.synchronize(dev)
+    t = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+    gbs = step_bytes / t / 1e9
+    print(json.dumps({
+        "metric": "keep-drift adoption HBM GB/s", "value": round(gbs, 2), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "op": "adopt_keep_drift", "n_params": wl.n_params,
+                   "pushed_dtype": wl.ckpt_dtype, "bytes_per_step": step_bytes},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "kernel": "adopt_keep_drift"},
+        "clocks": clocks.summary(), "gpu_launches": args.steps}), flush=True)
+    return 0
+
+
 def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -526,6 +582,7 @@ def parse(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="diffurefill1b")
+    p.add_argument("--op", choices=("merge", "adopt"), default="merge")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy"), default="stream")
@@ -543,6 +600,8 @@ def main(argv=None) -> int:
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, wl, ws, rank)
+    if args.op == "adopt":
+        return run_adopt(args, wl, ws, rank, local)
     return run_ours(args, wl, ws, rank, local)
 
 

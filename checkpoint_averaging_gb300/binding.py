@@ -87,6 +87,7 @@ _lib = None
 
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
            "cam_merge_accumulate_host", "cam_merge_publish", "cam_swa_update", "cam_swa_reset",
+           "cam_worker_drift_norm", "cam_adopt_keep_drift",
            "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
@@ -117,6 +118,8 @@ def lib() -> ctypes.CDLL:
     L.cam_merge_accumulate_host.argtypes = [vp, vpp, ctypes.c_int, i64]
     L.cam_merge_publish.argtypes = [vp, vpp, vpp]
     L.cam_swa_update.argtypes = [vp]
+    L.cam_worker_drift_norm.argtypes = [vp, vp, vp]
+    L.cam_adopt_keep_drift.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, ctypes.c_int, vp]
     L.cam_swa_reset.argtypes = [vp, i32, vp]
     L.cam_swa_counts.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_swa_set_counts.argtypes = [vp, ctypes.POINTER(i64)]
@@ -217,6 +220,10 @@ def ema_update(rd: int, beta: float) -> None:
     _check(lib().cam_ema_update(rd, beta))
 
 
+def worker_drift_norm(rd: int, per_worker_tensor: int | None, per_worker: int | None) -> None:
+    _check(lib().cam_worker_drift_norm(rd, per_worker_tensor or None, per_worker or None))
+
+
 def swa_update(rd: int) -> None:
     _check(lib().cam_swa_update(rd))
 
@@ -305,6 +312,32 @@ def merge_round_noalloc(numel: Sequence[int], master: Sequence[int], ckpt: Seque
     _check(lib().cam_merge_round_noalloc(
         n, numel_a, keep[0], keep[1], keep[2], K, keep[3], dtype, tok, mode, lr, mu,
         int(ema is not None), beta, per_tensor or None, per_round or None, stream or None))
+
+
+def adopt_keep_drift(theta_w, global_, pushed, stream=None) -> None:
+    """theta_w[t] += global_[t] - pushed[t] for a worker's tensor list: adopt the
+    new global while keeping the progress made since the push (the alternative
+    to plain replacement in the DiffuRefill-1B report, section 5.1).
+    theta_w and global_ are fp32 CUDA tensors, pushed fp32 or bf16."""
+    torch = _torch()
+    theta_w, global_, pushed = list(theta_w), list(global_), list(pushed)
+    if not (len(theta_w) == len(global_) == len(pushed)):
+        raise ValueError("the three tensor lists must have the same length")
+    dt = pushed[0].dtype if pushed else torch.float32
+    for a, b, c in zip(theta_w, global_, pushed):
+        if (a.numel() != b.numel() or a.numel() != c.numel() or a.dtype != torch.float32
+                or b.dtype != torch.float32 or c.dtype != dt or a.device.type != "cuda"
+                or b.device != a.device or c.device != a.device
+                or not (a.is_contiguous() and b.is_contiguous() and c.is_contiguous())):
+            raise ValueError("adopt_keep_drift: mismatched tensors")
+    n = len(theta_w)
+    numel = (ctypes.c_int64 * max(1, n))(*[t.numel() for t in theta_w])
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    arrs = [ctypes.cast(_ptrs([t.data_ptr() for t in group]), vpp)
+            for group in (theta_w, global_, pushed)]
+    _check(lib().cam_adopt_keep_drift(n, numel, arrs[0], arrs[1], arrs[2],
+                                      BF16 if dt == torch.bfloat16 else F32,
+                                      _stream_handle(stream)))
 
 
 def average_snapshots(out, snapshots, stream=None) -> None:
@@ -517,6 +550,20 @@ class Round:
 
     def swa_update(self) -> None:
         swa_update(self.handle)
+
+    def worker_drift_norm(self, per_worker_tensor=None, per_worker=None) -> None:
+        """Each worker's drift from the round's starting global: per_worker_tensor
+        [K * T_f] (worker-major) and per_worker [K], fp64 CUDA tensors sized for
+        the K workers accumulated by commit time."""
+        torch = _torch()
+        for t in (per_worker_tensor, per_worker):
+            if t is not None and (t.device != self.merger.device or t.dtype != torch.float64
+                                  or not t.is_contiguous()):
+                raise ValueError("worker norm outputs must be contiguous fp64 device tensors")
+        worker_drift_norm(self.handle,
+                          None if per_worker_tensor is None else per_worker_tensor.data_ptr(),
+                          None if per_worker is None else per_worker.data_ptr())
+        self._borrowed.extend(t for t in (per_worker_tensor, per_worker) if t is not None)
 
     def drift_norm(self, per_tensor=None, per_fragment=None) -> None:
         torch = _torch()

@@ -45,6 +45,7 @@ struct MergeArgs {
     const ChunkDesc* chunks;  // first chunk of this launch (device)
     const TensorSlot* slots;  // the fragment's tensors, by local index (device)
     double* partials;         // drift partial per chunk of this launch (device) or null
+    double* worker_partials;  // [chunk * CAM_KMAX + k]: worker k's drift partials, or null
     int32_t n_chunks;
     int32_t local0;
     int32_t n_local;
@@ -71,6 +72,12 @@ struct NormArgs {
     double* tsq;                // scratch [n_tensors]: squared norms
     double* per_tensor;         // output or null
     double* per_fragment;       // output or null
+    // per-worker drift (K > 0 when asked for)
+    int32_t K;
+    const double* worker_partials;  // [n_chunks * CAM_KMAX]
+    double* worker_tsq;             // scratch [n_tensors * CAM_KMAX]
+    double* per_worker_tensor;      // output [K * n_tensors] or null
+    double* per_worker;             // output [K] or null
 };
 
 enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
@@ -80,11 +87,17 @@ enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 int record_error(int code, const char* fmt, ...);
 
 // Launches one fused merge pass with `grid` blocks.
-// Variant selection of the fused pass.
+// Variant selection of the fused pass. norm_level: 0 none, 1 round drift,
+// 2 round drift and per-worker drift.
 struct MergeVariant {
     int dtype, mode;
-    bool ema, norm, pub, swa;
+    bool ema;
+    int norm_level;
+    bool pub, swa;
 };
+using MergeFn = void (*)(MergeArgs);
+MergeFn pick_merge_f32(const MergeVariant& v);
+MergeFn pick_merge_bf16(const MergeVariant& v);
 cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cudaStream_t s);
 // Resident blocks per SM of that variant (0 on error).
 int merge_blocks_per_sm(const MergeVariant& v);

@@ -129,19 +129,34 @@ __device__ __forceinline__ float swa_fold(const A& a, float mu, float th) {
     return __fadd_rn(mu, __fdiv_rn(__fsub_rn(th, mu), a.swa_n));
 }
 
+// Per-worker drift: accw[k] += (x_k - theta_old)^2 for k < K, before the
+// outer step changes theta.
+template <class A>
+__device__ __forceinline__ void worker_drift(const A& a, const float (&xk)[CAM_KMAX], float th,
+                                             float* accw) {
+#pragma unroll
+    for (int k = 0; k < CAM_KMAX; ++k)
+        if (k < a.K) {
+            const float d = __fsub_rn(xk[k], th);
+            accw[k] = __fmaf_rn(d, d, accw[k]);
+        }
+}
+
 // xs[0..K) are the workers' copies of the tensor; with PUB, xs[K] receives a
 // copy of the new theta and xs[K+1] (when not null) a copy of the new EMA.
 // With SWA the uniform running average ts.swa is updated from the new theta.
+// With WD, accw[0..K) collect each worker's squared drift.
 template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, bool SWA = false,
-          class A>
+          bool WD = false, class A>
 __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
-                                           const TensorSlot& ts, int64_t i, float& acc) {
+                                           const TensorSlot& ts, int64_t i, float& acc,
+                                           float* accw = nullptr) {
     XVec<XT> x[CAM_KMAX];
 #pragma unroll
     for (int k = 0; k < CAM_KMAX; ++k)
         if (k < a.K) x[k].load(static_cast<const XT*>(xs[k]) + i);
     float th[8], m[8], e[8];
-    if (MODE == kDelta || NORM) load_s8(ts.theta + i, th);
+    if (MODE == kDelta || NORM || WD) load_s8(ts.theta + i, th);
     if (MODE == kDelta) load_s8(ts.m + i, m);
     if (EMA) load_s8(ts.e + i, e);
     float sw[8];
@@ -151,6 +166,7 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
         float xk[CAM_KMAX];
 #pragma unroll
         for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
+        if constexpr (WD) worker_drift(a, xk, th[j], accw);
         merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
         if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
     }
@@ -165,9 +181,10 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
 }
 
 template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, bool SWA = false,
-          class A>
+          bool WD = false, class A>
 __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
-                                          const TensorSlot& ts, int64_t i, float& acc) {
+                                          const TensorSlot& ts, int64_t i, float& acc,
+                                          float* accw = nullptr) {
     float xk[CAM_KMAX];
 #pragma unroll
     for (int k = 0; k < CAM_KMAX; ++k)
@@ -175,6 +192,7 @@ __device__ __forceinline__ void merge_one(const A& a, const void* const* xs,
     float th = ts.theta[i];
     float m = (MODE == kDelta) ? ts.m[i] : 0.0f;
     float e = EMA ? ts.e[i] : 0.0f;
+    if constexpr (WD) worker_drift(a, xk, th, accw);
     merge_elem<MODE, EMA, NORM>(a, xk, th, m, e, acc);
     ts.theta[i] = th;
     if (MODE == kDelta) ts.m[i] = m;

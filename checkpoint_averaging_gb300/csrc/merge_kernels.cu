@@ -23,7 +23,8 @@
 // sequence of binary32 operations the C ABI documents.
 //
 // norm_finish: sums the per-chunk drift partials per tensor and per fragment
-// in a fixed order, so norms are bitwise reproducible.
+// (and per worker, when asked) in a fixed order, so norms are bitwise
+// reproducible. The fused pass itself is in merge_fused.cuh.
 #include <cuda_runtime.h>
 
 #include "cam_internal.h"
@@ -33,47 +34,6 @@ namespace cam {
 namespace {
 
 using namespace cam::dev;
-
-// ---- the fused pass ------------------------------------------------------------
-
-template <typename XT, int MODE, bool EMA, bool NORM, bool PUB, bool SWA>
-__global__ void __launch_bounds__(kThreads, 2)
-    merge_fused(const __grid_constant__ MergeArgs a) {
-    __shared__ double warp_part[kThreads / 32];
-    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
-        const ChunkDesc ch = a.chunks[c];
-        const int l = ch.local - a.local0;
-        const TensorSlot ts = a.slots[ch.local];
-        const void* const* xs = a.x + static_cast<int64_t>(l) * a.stride;
-        const bool vec = (a.vec[l >> 5] >> (l & 31)) & 1u;
-        float acc = 0.0f;
-        if (vec) {
-            const int nv = ch.len >> 3;
-            for (int v = threadIdx.x; v < nv; v += kThreads)
-                merge_vec8<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts, ch.start + 8 * int64_t(v), acc);
-            const int tail = ch.len & 7;
-            if (static_cast<int>(threadIdx.x) < tail)
-                merge_one<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts,
-                                                    ch.start + 8 * int64_t(nv) + threadIdx.x, acc);
-        } else {
-            for (int j = threadIdx.x; j < ch.len; j += kThreads)
-                merge_one<XT, MODE, EMA, NORM, PUB, SWA>(a, xs, ts, ch.start + j, acc);
-        }
-        if (NORM) {
-            // fp32 within a thread (at most a few dozen squares), fp64 above.
-            const double d = warp_sum(static_cast<double>(acc));
-            if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = d;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                double s = 0.0;
-#pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) s += warp_part[w];
-                a.partials[c] = s;
-            }
-            __syncthreads();
-        }
-    }
-}
 
 __global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
     const int lane = threadIdx.x & 31;
@@ -86,6 +46,15 @@ __global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
         s = warp_sum(s);
         if (lane == 0) a.tsq[t] = s;
     }
+    // per worker and tensor: one warp per (tensor, worker) pair
+    for (int p = warp; p < a.n_tensors * a.K; p += n_warps) {
+        const int t = p / a.K, k = p % a.K;
+        double s = 0.0;
+        for (int c = a.first_chunk[t] + lane; c < a.first_chunk[t + 1]; c += 32)
+            s += a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + k];
+        s = warp_sum(s);
+        if (lane == 0) a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k] = s;
+    }
     __syncthreads();
     if (warp == 0) {
         double s = 0.0;
@@ -93,9 +62,22 @@ __global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
         s = warp_sum(s);
         if (lane == 0 && a.per_fragment) *a.per_fragment = sqrt(s);
     }
+    if (warp >= 1 && warp <= a.K) {  // warp 1 + k totals worker k
+        const int k = warp - 1;
+        double s = 0.0;
+        for (int t = lane; t < a.n_tensors; t += 32)
+            s += a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k];
+        s = warp_sum(s);
+        if (lane == 0 && a.per_worker) a.per_worker[k] = sqrt(s);
+    }
     if (a.per_tensor)
         for (int t = threadIdx.x; t < a.n_tensors; t += blockDim.x)
             a.per_tensor[t] = sqrt(a.tsq[t]);
+    if (a.per_worker_tensor)
+        for (int p = threadIdx.x; p < a.n_tensors * a.K; p += blockDim.x) {
+            const int k = p / a.n_tensors, t = p % a.n_tensors;
+            a.per_worker_tensor[p] = sqrt(a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k]);
+        }
 }
 
 __global__ void fill_kernel(float* dst, int64_t n, float v) {
@@ -110,31 +92,8 @@ __global__ void copy_kernel(float* dst, const float* src, int64_t n) {
         dst[i] = src[i];
 }
 
-// ---- variant dispatch ------------------------------------------------------------
-
-using MergeFn = void (*)(MergeArgs);
-
-template <typename XT, int MODE, bool PUB, bool SWA>
-MergeFn pick_en(bool ema, bool norm) {
-    if (ema)
-        return norm ? merge_fused<XT, MODE, true, true, PUB, SWA>
-                    : merge_fused<XT, MODE, true, false, PUB, SWA>;
-    return norm ? merge_fused<XT, MODE, false, true, PUB, SWA>
-                : merge_fused<XT, MODE, false, false, PUB, SWA>;
-}
-
-template <bool PUB, bool SWA>
-MergeFn pick_dm(const MergeVariant& v) {
-    if (v.dtype == kDtBF16)
-        return v.mode == kDelta ? pick_en<uint16_t, kDelta, PUB, SWA>(v.ema, v.norm)
-                                : pick_en<uint16_t, kMean, PUB, SWA>(v.ema, v.norm);
-    return v.mode == kDelta ? pick_en<float, kDelta, PUB, SWA>(v.ema, v.norm)
-                            : pick_en<float, kMean, PUB, SWA>(v.ema, v.norm);
-}
-
 MergeFn pick(const MergeVariant& v) {
-    if (v.pub) return v.swa ? pick_dm<true, true>(v) : pick_dm<true, false>(v);
-    return v.swa ? pick_dm<false, true>(v) : pick_dm<false, false>(v);
+    return v.dtype == kDtBF16 ? pick_merge_bf16(v) : pick_merge_f32(v);
 }
 
 }  // namespace

@@ -95,6 +95,8 @@ struct Plan {
     int32_t* d_first = nullptr;
     double* d_partials = nullptr;
     double* d_tsq = nullptr;
+    double* d_worker_partials = nullptr;  // [n_chunks * CAM_KMAX]
+    double* d_worker_tsq = nullptr;       // [n_tensors * CAM_KMAX]
     int32_t n_chunks() const { return static_cast<int32_t>(chunks.size()); }
     int32_t n_tensors() const { return static_cast<int32_t>(tensors.size()); }
 };
@@ -118,7 +120,8 @@ struct cam_ctx {
     int64_t last_round = -1;
     int64_t launches = 0;
     std::vector<cam_round*> open;
-    int bps[2][2][2][2][2][2] = {};  // resident blocks per SM: [dtype][mode][ema][norm][publish][swa]
+    // resident blocks per SM: [dtype][mode][ema][norm level][publish][swa]
+    int bps[2][2][2][3][2][2] = {};
     std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
 
     Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
@@ -143,6 +146,9 @@ struct cam_round {
     bool norms = false;
     double* out_tensor = nullptr;
     double* out_fragment = nullptr;
+    bool worker_norms = false;
+    double* out_worker_tensor = nullptr;
+    double* out_worker = nullptr;
     bool swa = false;
     bool publish = false;
     bool publish_ema = false;
@@ -274,6 +280,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         bytes += round_up(sizeof(int32_t) * p.first_chunk.size(), 256);
         bytes += round_up(sizeof(double) * p.chunks.size(), 256);
         bytes += round_up(sizeof(double) * p.tensors.size(), 256);
+        bytes += round_up(sizeof(double) * CAM_KMAX * p.chunks.size(), 256);
+        bytes += round_up(sizeof(double) * CAM_KMAX * p.tensors.size(), 256);
     }
     ce = cudaMalloc(&c->dev_block, std::max<size_t>(bytes, 256));
     if (ce != cudaSuccess) {
@@ -305,6 +313,10 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         p.d_partials = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
         o = carve(sizeof(double) * p.tensors.size());
         p.d_tsq = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(double) * CAM_KMAX * p.chunks.size());
+        p.d_worker_partials = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(double) * CAM_KMAX * p.tensors.size());
+        p.d_worker_tsq = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
     }
     ce = cudaMemcpy(c->dev_block, host.data(), bytes, cudaMemcpyHostToDevice);
     if (ce != cudaSuccess) {
@@ -314,12 +326,12 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     for (int dt = 0; dt < 2; ++dt)
         for (int md = 0; md < 2; ++md)
             for (int em = 0; em < 2; ++em)
-                for (int nm = 0; nm < 2; ++nm)
+                for (int nl = 0; nl < 3; ++nl)
                     for (int pb = 0; pb < 2; ++pb)
                         for (int sw = 0; sw < 2; ++sw)
-                            c->bps[dt][md][em][nm][pb][sw] = std::max(
+                            c->bps[dt][md][em][nl][pb][sw] = std::max(
                                 1, cam::merge_blocks_per_sm(cam::MergeVariant{
-                                       dt, md, em != 0, nm != 0, pb != 0, sw != 0}));
+                                       dt, md, em != 0, nl, pb != 0, sw != 0}));
 
     cudaStream_t s = static_cast<cudaStream_t>(d->stream);
     for (int32_t t = 0; t < c->n_tensors && ce == cudaSuccess; ++t) {
@@ -488,6 +500,17 @@ CAM_API int cam_ema_update(cam_round* r, float beta) {
     return CAM_OK;
 }
 
+CAM_API int cam_worker_drift_norm(cam_round* r, double* per_worker_tensor, double* per_worker) {
+    if (!r) return fail(CAM_E_ARG, "cam_worker_drift_norm: round is NULL");
+    if (r->worker_norms) return fail(CAM_E_STATE, "cam_worker_drift_norm: asked twice");
+    if (!per_worker_tensor && !per_worker)
+        return fail(CAM_E_ARG, "cam_worker_drift_norm: both outputs NULL");
+    r->worker_norms = true;
+    r->out_worker_tensor = per_worker_tensor;
+    r->out_worker = per_worker;
+    return CAM_OK;
+}
+
 CAM_API int cam_swa_update(cam_round* r) {
     if (!r) return fail(CAM_E_ARG, "cam_swa_update: round is NULL");
     if (r->swa) return fail(CAM_E_STATE, "cam_swa_update: asked twice");
@@ -591,8 +614,9 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.mu = r->mu;
     a.beta = r->beta;
     a.swa_n = static_cast<float>(swa_prev + 1);
-    const int bps = c->bps[r->dtype][r->mode][r->ema][r->norms][r->publish][r->swa];
-    const cam::MergeVariant variant{r->dtype, r->mode, r->ema, r->norms, r->publish, r->swa};
+    const int norm_level = r->worker_norms ? 2 : (r->norms ? 1 : 0);
+    const int bps = c->bps[r->dtype][r->mode][r->ema][norm_level][r->publish][r->swa];
+    const cam::MergeVariant variant{r->dtype, r->mode, r->ema, norm_level, r->publish, r->swa};
     const int stride = K + (r->publish ? 2 : 0);
     a.stride = stride;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -628,7 +652,9 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             if (v) a.vec[l >> 5] |= 1u << (l & 31);
         }
         a.chunks = p.d_chunks + c0;
-        a.partials = r->norms ? p.d_partials + c0 : nullptr;
+        a.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
+        a.worker_partials =
+            norm_level >= 2 ? p.d_worker_partials + static_cast<int64_t>(c0) * CAM_KMAX : nullptr;
         a.n_chunks = c1 - c0;
         a.local0 = l0;
         a.n_local = n;
@@ -636,8 +662,10 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ce = cam::launch_merge(a, variant, grid, s);
         ++c->launches;
     }
-    if (ce == cudaSuccess && r->norms) {
-        NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment};
+    if (ce == cudaSuccess && norm_level >= 1) {
+        NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
+                    norm_level >= 2 ? K : 0, p.d_worker_partials, p.d_worker_tsq,
+                    r->out_worker_tensor, r->out_worker};
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }

@@ -187,6 +187,7 @@ class Workload:
     norms: bool = False
     workers_track_global: bool = False  # workers start from the current global
     swa: bool = False                   # also fold each global into the uniform average
+    worker_norms: bool = False          # also report each worker's own drift
 
     @property
     def n_params(self) -> int:
@@ -228,6 +229,15 @@ def _wl_1b_swa() -> Workload:
                     ema_beta=0.9, rounds=((0, -1),), noise_std=1e-3, swa=True)
 
 
+def _wl_1b_bf16_wnorms() -> Workload:
+    """The bf16 fragment rounds with each worker's own drift reported too."""
+    w = _wl_1b_bf16()
+    return Workload(w.name + "_wnorms", w.specs, w.n_fragments, K=w.K, n_masked=w.n_masked,
+                    quorum=w.quorum, ckpt_dtype=w.ckpt_dtype, mode=w.mode, lr=w.lr, mu=w.mu,
+                    rounds=w.rounds, in_flight=w.in_flight, noise_std=w.noise_std,
+                    tokens=w.tokens, norms=True, worker_norms=True)
+
+
 def _wl_1b_bf16() -> Workload:
     return Workload("diffurefill1b_bf16_f4_q3_delta_nesterov_norms",
                     tuple(diffurefill1b_specs(4)), 4, K=5, n_masked=2, quorum=3,
@@ -256,6 +266,7 @@ def workload(name: str) -> Workload:
         "diffurefill1b": _wl_1b,
         "diffurefill1b_bf16": _wl_1b_bf16,
         "diffurefill1b_swa": _wl_1b_swa,
+        "diffurefill1b_bf16_wnorms": _wl_1b_bf16_wnorms,
     }
     if name in table:
         return table[name]()

@@ -178,6 +178,21 @@ int cam_merge_finalize(cam_round* rd, cam_mode mode, float lr, float mu);
 int cam_ema_update(cam_round* rd, float beta);
 
 /*
+ * Asks for each worker's own drift, written on the commit stream: worker k
+ * (arrival order) moved sqrt(sum_i (x_k - theta)^2) away from the global it
+ * started from, theta being the global before this round. per_worker_tensor
+ * (device, [K * T_f], worker-major: [k * T_f + t]) holds it per tensor and
+ * per_worker (device, [K]) over the fragment; either may be NULL but not
+ * both. K is the number of workers accumulated when the round commits.
+ * This is the per-worker form of the local drift the DiffuRefill-1B report
+ * tracks ("DiffuRefill-1B" technical report, section 5.1); a worker far from
+ * the others shows up here. Computed in the same pass, squares summed in fp32
+ * within a thread and fp64 above, in a fixed order. Errors: CAM_E_ARG,
+ * CAM_E_STATE (asked twice).
+ */
+int cam_worker_drift_norm(cam_round* rd, double* per_worker_tensor, double* per_worker);
+
+/*
  * Asks the same pass to fold the new global into each tensor's uniform
  * running average: swa' = swa + (theta' - swa) / n, n = the globals in the
  * average after this round (the first fold after a reset copies theta'
@@ -291,6 +306,23 @@ int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, float* cons
                             const void* const* ckpt, cam_dtype dtype, const int64_t* tokens,
                             cam_mode mode, float lr, float mu, int32_t ema_update, float beta,
                             double* per_tensor, double* per_round, void* stream);
+
+/*
+ * A worker adopting the new global while keeping the progress it made since
+ * its last push: theta_w <- theta_w + (g - theta_pushed), per element a
+ * binary32 subtraction then addition. The DiffuRefill-1B run tried this and
+ * found it worse than plain replacement in 60 of 63 probes ("DiffuRefill-1B"
+ * technical report, section 5.1), so plain replacement (copying g) remains
+ * the default; this call exists to run and measure the alternative.
+ * theta_w[t] (fp32, updated in place), global[t] (fp32) and pushed[t] (the
+ * checkpoint as pushed, fp32 or bf16) are device pointers to numel[t]
+ * elements, all arrays host arrays of n_tensors entries. No context and no
+ * allocation; queued on `stream`. Errors: CAM_E_ARG (checked before any CUDA
+ * call), CAM_E_CUDA.
+ */
+int cam_adopt_keep_drift(int32_t n_tensors, const int64_t* numel, float* const* theta_w,
+                         const float* const* global, const void* const* pushed,
+                         cam_dtype pushed_dtype, void* stream);
 
 /* Message describing the calling thread's last error ("" if none). */
 const char* cam_last_error(void);

@@ -598,3 +598,124 @@ def test_average_of_the_last_snapshots_matches_oracle(window, dtype):
     for t in range(len(RAGGED)):
         want = oracle.plain_average([to_np(s.views[t]) for s in snaps])
         assert bitwise_equal(to_np(out.views[t]), want)
+
+
+# ---- per-worker drift (technical report, section 5.1) ------------------------------
+
+def _worker_norm_check(wl, seed, with_round_norms, swa=False):
+    g = W.make_global(wl, seed, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    for idx, (rnd, frag) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, seed)
+        workers = [W.make_worker(wl, g, rnd, k, seed, DEV) for k in range(wl.K)]
+        tensors = [t for t in range(len(wl.specs)) if frag == -1 or wl.specs[t].fragment == frag]
+        th_before = {t: to_np(st.theta.views[t]).copy() for t in tensors}
+        K = len(draw.included)
+        pwt = torch.full((K * len(tensors),), -1.0, dtype=torch.float64, device=DEV)
+        pw = torch.full((K,), -1.0, dtype=torch.float64, device=DEV)
+        rd = st.merger.begin(rnd, frag)
+        for k in draw.included:
+            rd.accumulate(workers[k].views, draw.tokens[k])
+        rd.finalize(B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE, wl.lr, wl.mu)
+        if wl.ema_beta is not None:
+            rd.ema_update(wl.ema_beta)
+        if swa:
+            rd.swa_update()
+        if with_round_norms:
+            rd.drift_norm(torch.zeros(len(tensors), dtype=torch.float64, device=DEV), None)
+        rd.worker_drift_norm(pwt, pw)
+        rd.commit()
+        torch.cuda.synchronize()
+        got = pwt.cpu().numpy().reshape(K, len(tensors))
+        tot = np.zeros(K)
+        for j, t in enumerate(tensors):
+            want = oracle.worker_drift([to_np(workers[k].views[t]) for k in draw.included],
+                                       th_before[t])
+            tot += np.asarray(want)
+            for k in range(K):
+                w = math.sqrt(want[k])
+                assert abs(got[k, j] - w) <= NORM_RTOL * w + 1e-300, (t, k, got[k, j], w)
+        for k in range(K):
+            w = math.sqrt(tot[k])
+            assert abs(pw[k].item() - w) <= NORM_RTOL * w + 1e-300
+        del workers
+    st.merger.close()
+
+
+@pytest.mark.parametrize("mode,dtype,round_norms", [("delta", "bf16", True), ("mean", "f32", False),
+                                                    ("delta", "f32", False), ("mean", "bf16", True)])
+def test_worker_drift_matches_oracle(mode, dtype, round_norms):
+    wl = _custom(RAGGED, K=4, mode=mode, dtype=dtype, n_masked=1, quorum=3,
+                 rounds=((0, -1), (1, -1)))
+    _worker_norm_check(wl, 13, round_norms)
+
+
+def test_worker_drift_with_ema_and_swa_fp32():
+    wl = _swa_workload(((0, -1), (1, -1)), "delta", "f32")
+    _worker_norm_check(wl, 14, True, swa=True)
+
+
+def test_worker_drift_on_the_1b_bf16_fragment_whole_tensors():
+    wl = W.workload("diffurefill1b_bf16")
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    rnd, frag = wl.rounds[0]
+    workers = [W.make_worker(wl, g, rnd, k, 0, DEV) for k in range(wl.K)]
+    tensors = [t for t in range(len(wl.specs)) if wl.specs[t].fragment == frag]
+    K = len(draw.included)
+    pwt = torch.zeros(K * len(tensors), dtype=torch.float64, device=DEV)
+    pw = torch.zeros(K, dtype=torch.float64, device=DEV)
+    th0 = {t: to_np(st.theta.views[t]).copy() for t in tensors}
+    rd = st.merger.begin(rnd, frag)
+    for k in draw.included:
+        rd.accumulate(workers[k].views, draw.tokens[k])
+    rd.finalize(B.DELTA_NESTEROV, wl.lr, wl.mu)
+    rd.worker_drift_norm(pwt, pw)
+    rd.commit()
+    torch.cuda.synchronize()
+    got = pwt.cpu().numpy().reshape(K, len(tensors))
+    for j, t in enumerate(tensors):   # fragment 0: the 151M-element embedding
+        want = oracle.worker_drift([to_np(workers[k].views[t]) for k in draw.included], th0[t])
+        for k in range(K):
+            assert abs(got[k, j] - math.sqrt(want[k])) <= NORM_RTOL * math.sqrt(want[k])
+    st.merger.close()
+
+
+# ---- keep-drift adoption (technical report, section 5.1) ----------------------------
+
+@pytest.mark.parametrize("dtype,misaligned", [("f32", False), ("bf16", False), ("f32", True)])
+def test_keep_drift_adoption_matches_oracle(dtype, misaligned):
+    wl = _custom(RAGGED + [300_001], K=3, mode="mean", dtype=dtype)
+    g = W.make_global(wl, 21, DEV)
+    pushed = W.make_worker(wl, g, 0, 0, 21, DEV)       # the checkpoint as pushed
+    local = W.make_worker(wl, g, 1, 1, 21, DEV)        # the worker kept training
+    newg = W.make_worker(wl, g, 2, 2, 21, DEV)          # the merged global
+    th = [v.float().clone() for v in local.views]
+    gl = [v.float().clone() for v in newg.views]
+    if misaligned:  # odd element offsets: the scalar path
+        def shift(ts):
+            out = []
+            for t in ts:
+                buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+                buf[1:].copy_(t)
+                out.append(buf[1:])
+            return out
+        th, gl = shift(th), shift(gl)
+    want = [to_np(t).copy() for t in th]
+    for w, gg, p in zip(want, gl, pushed.views):
+        oracle.adopt_keep_drift(w, to_np(gg), to_np(p))
+    B.adopt_keep_drift(th, gl, pushed.views)
+    torch.cuda.synchronize()
+    for t, w in enumerate(want):
+        assert bitwise_equal(to_np(th[t]), w), f"tensor {t}"
+
+
+def test_keep_drift_adoption_of_an_unmoved_worker_lands_near_the_global():
+    n = 1 << 20
+    p = torch.randn(n, device=DEV) * 0.02
+    g = p + torch.randn(n, device=DEV) * 1e-3
+    th = p.clone()
+    B.adopt_keep_drift([th], [g], [p])
+    torch.cuda.synchronize()
+    assert ((th - g).abs() <= 2 * 2 ** -24 * (p.abs() + g.abs()) + 1e-30).all()
