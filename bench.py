@@ -38,7 +38,8 @@ if ROOT not in sys.path:
 
 METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params"
 KERNEL_SRCS = [os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", f)
-               for f in ("merge_kernels.cu", "merge_device.cuh", "cam_internal.h")]
+               for f in ("merge_fused.cuh", "merge_fused_f32.cu", "merge_fused_bf16.cu",
+                         "merge_device.cuh", "cam_internal.h")]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
 

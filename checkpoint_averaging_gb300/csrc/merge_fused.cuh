@@ -31,9 +31,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr bool NORM = NL >= 1;
     constexpr bool WD = NL >= 2;
     constexpr int kWarps = kThreads / 32;
-    __shared__ double warp_part[kWarps];
-    __shared__ double worker_part[WD ? kWarps * CAM_KMAX : 1];
-    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    // Two slots, alternating by chunk, so one barrier per chunk suffices: a
+    // slot is written again only after the next chunk's barrier, which thread
+    // 0 reaches only once it has read the slot.
+    __shared__ double warp_part[2][kWarps];
+    __shared__ double worker_part[2][WD ? kWarps * CAM_KMAX : 1];
+    int parity = 0;
+    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
         const ChunkDesc ch = a.chunks[c];
         const int l = ch.local - a.local0;
         const TensorSlot ts = a.slots[ch.local];
@@ -59,20 +63,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (NORM) {
             const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
             const double d = warp_sum(static_cast<double>(acc));
-            if (lane == 0) warp_part[warp] = d;
+            if (lane == 0) warp_part[parity][warp] = d;
             if constexpr (WD) {
 #pragma unroll
                 for (int k = 0; k < CAM_KMAX; ++k)
                     if (k < a.K) {  // K is the same for the whole block
                         const double dk = warp_sum(static_cast<double>(accw[k]));
-                        if (lane == 0) worker_part[warp * CAM_KMAX + k] = dk;
+                        if (lane == 0) worker_part[parity][warp * CAM_KMAX + k] = dk;
                     }
             }
             __syncthreads();
             if (threadIdx.x == 0) {
                 double s = 0.0;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) s += warp_part[w];
+                for (int w = 0; w < kWarps; ++w) s += warp_part[parity][w];
                 a.partials[c] = s;
             }
             if constexpr (WD) {
@@ -80,11 +84,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int k = threadIdx.x;
                     double s = 0.0;
 #pragma unroll
-                    for (int w = 0; w < kWarps; ++w) s += worker_part[w * CAM_KMAX + k];
+                    for (int w = 0; w < kWarps; ++w) s += worker_part[parity][w * CAM_KMAX + k];
                     a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + k] = s;
                 }
             }
-            __syncthreads();
         }
     }
 }
