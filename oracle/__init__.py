@@ -176,6 +176,39 @@ def adopt_keep_drift(theta_w: np.ndarray, g: np.ndarray, pushed: np.ndarray) -> 
                                       _dtype_code(pushed)), "adopt_keep_drift")
 
 
+ORTHO_SCALE_FIXED = 0       # update = lr * polar(Delta)
+ORTHO_SCALE_MATCH_NORM = 1  # update = lr * |Delta|_F / sqrt(r) * polar(Delta)
+
+
+def polar(delta: np.ndarray) -> np.ndarray:
+    """The polar factor U V^T of a 2-D array (thin SVD in fp64): the
+    semi-orthogonal matrix nearest to it ("DiffuRefill-1B" technical report,
+    section 5.3: outer orthogonalisation replaces the averaged update by its
+    polar factor)."""
+    u, _, vt = np.linalg.svd(np.asarray(delta, np.float64), full_matrices=False)
+    return u @ vt
+
+
+def orthogonal_update(xs: Sequence[np.ndarray], theta: np.ndarray, rows: int, *,
+                      lr: float, scale_mode: int = ORTHO_SCALE_FIXED):
+    """One orthogonalised plain-mean round on one 2-D tensor (row-major, `rows`
+    rows). The averaged update Delta = mean_k(x_k) - theta is formed in fp32
+    exactly as in a plain-mean round, then replaced by its polar factor:
+    theta' = theta + s * polar(Delta), s = lr (fixed) or lr * |Delta|_F /
+    sqrt(min(m, n)) (the update keeps Delta's Frobenius norm, the RMS-matched
+    form of the same report's section 5.3). Returns (theta' in fp64, Delta)."""
+    mean = plain_mean(xs)
+    delta = (mean - np.asarray(theta, np.float32)).astype(np.float32)  # one fp32 op
+    m = int(rows)
+    d2 = delta.reshape(m, -1)
+    o = polar(d2)
+    s = float(lr)
+    if scale_mode == ORTHO_SCALE_MATCH_NORM:
+        s = s * math.sqrt(float(np.sum(d2.astype(np.float64) ** 2))) / math.sqrt(min(d2.shape))
+    out = np.asarray(theta, np.float64).reshape(d2.shape) + s * o
+    return out.reshape(np.shape(theta)), delta
+
+
 def plain_average(snapshots: Sequence[np.ndarray]) -> np.ndarray:
     """Average of stored snapshots (the last-n snapshot averages of the
     technical report's Table 5): their plain mean in the given order."""

@@ -530,3 +530,56 @@ def test_keep_drift_adoption_bf16_pushed():
     pushed = np.array([0x3F80, 0xBF80], np.uint16)   # 1.0, -1.0
     oracle.adopt_keep_drift(tw, g, pushed)
     assert list(tw) == [2.0, 2.0]
+
+
+# ---- outer orthogonalisation (technical report, section 5.3) ---------------------
+
+def _orthonormal(rng_, m, r):
+    q, _ = np.linalg.qr(rng_.normal(size=(m, r)))
+    return q
+
+
+@pytest.mark.parametrize("m,n", [(40, 12), (12, 40), (25, 25)])
+def test_polar_of_a_known_svd_is_q_p_transposed(m, n):
+    r_ = rng(40 + m)
+    k = min(m, n)
+    q, p = _orthonormal(r_, m, k), _orthonormal(r_, n, k)
+    s = r_.uniform(0.1, 5.0, k)
+    got = oracle.polar(q @ np.diag(s) @ p.T)
+    assert np.allclose(got, q @ p.T, atol=1e-12)
+
+
+@pytest.mark.parametrize("m,n", [(30, 10), (10, 30)])
+def test_polar_agrees_with_the_inverse_square_root_route(m, n):
+    d = rng(41).normal(size=(m, n))
+    w, v = np.linalg.eigh(d.T @ d if m >= n else d @ d.T)
+    inv_sqrt = v @ np.diag(w ** -0.5) @ v.T
+    want = d @ inv_sqrt if m >= n else inv_sqrt @ d
+    assert np.allclose(oracle.polar(d), want, atol=1e-10)
+
+
+def test_polar_is_scale_invariant_and_semi_orthogonal():
+    d = rng(42).normal(size=(20, 7))
+    o = oracle.polar(d)
+    assert np.allclose(oracle.polar(3.7 * d), o, atol=1e-12)
+    assert np.allclose(o.T @ o, np.eye(7), atol=1e-12)
+    assert np.allclose(oracle.polar(o), o, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [oracle.ORTHO_SCALE_FIXED, oracle.ORTHO_SCALE_MATCH_NORM])
+def test_orthogonal_update_magnitude(mode):
+    r_ = rng(43)
+    m, n = 16, 6
+    theta = r_.normal(0, 0.02, m * n).astype(np.float32)
+    xs = [(theta + r_.normal(0, 1e-3, m * n)).astype(np.float32) for _ in range(3)]
+    new, delta = oracle.orthogonal_update(xs, theta, m, lr=0.5, scale_mode=mode)
+    step = new - theta.astype(np.float64)
+    fro = math.sqrt(float(np.sum(step ** 2)))
+    if mode == oracle.ORTHO_SCALE_FIXED:
+        assert fro == pytest.approx(0.5 * math.sqrt(n), rel=1e-10)
+    else:
+        assert fro == pytest.approx(0.5 * math.sqrt(float(np.sum(delta.astype(np.float64) ** 2))),
+                                    rel=1e-10)
+    # the step points along the update: <step, Delta> = s * nuclear norm > 0
+    assert float(np.sum(step * delta.astype(np.float64))) > 0
+    assert np.array_equal(delta, (oracle.plain_mean(xs) - theta).astype(np.float32))
