@@ -576,6 +576,86 @@ def run_adopt(args, wl, ws, rank, local) -> int:
     return 0
 
 
+def run_ortho(args, wl, ws, rank, local) -> int:
+    """Times an orthogonalised plain-mean round (technical report, section 5.3)
+    over the workload's tensor list: every matrix's averaged update replaced by
+    its polar factor with `--ortho-iterations` Newton-Schulz steps on the tensor
+    cores. The figure is GEMM TFLOP/s: each step of an m x n matrix costs
+    4 max(m,n) min(m,n)^2 flops (Gram matrix, then its product with X)."""
+    import torch
+
+    import __graft_entry__
+    from checkpoint_averaging_gb300 import binding as B
+    from checkpoint_averaging_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = W.make_global(wl, args.seed, dev)
+    th = W.empty_arena(g.numels, torch.float32, dev)
+    th.flat.copy_(g.flat)
+    e = W.empty_arena(g.numels, torch.float32, dev)
+    e.flat.copy_(g.flat)
+    rows = [sp.shape[0] if len(sp.shape) == 2 else 0 for sp in wl.specs]
+    workers = [W.make_worker(wl, g, 0, k, args.seed, dev) for k in range(wl.K)]
+    mg = B.Merger(th.views, ema=e.views, quorum=wl.K, rows=rows)
+    ck = [mg.checkpoint(w.views) for w in workers]
+    prec = B.ORTHO_FP32 if args.ortho_precision == "fp32" else B.ORTHO_TF32
+    its = args.ortho_iterations
+    flops = sum(4 * max(sp.shape) * min(sp.shape) ** 2 * its
+                for sp in wl.specs if len(sp.shape) == 2)
+    s = torch.cuda.current_stream(dev)
+    rnd = [0]
+
+    def step():
+        rd = mg.begin(rnd[0])
+        rnd[0] += 1
+        for c in ck:
+            rd.accumulate(c, 0)
+        rd.finalize(B.MEAN_REPLACE)
+        rd.ema_update(0.9)
+        rd.orthogonalize(0.01, B.ORTHO_SCALE_MATCH_NORM, prec, its)
+        rd.commit(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    l0 = mg.launch_count
+    with ClockSampler(local) as clocks:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(args.steps):
+            step()
+        b.record(s)
+        torch.cuda.synchronize(dev)
+    t = a.elapsed_time(b) / 1e3 / args.steps
+    own_launches = mg.launch_count - l0
+    n_mat = sum(1 for sp in wl.specs if len(sp.shape) == 2)
+    peaks = measured_peaks()
+    bf16 = peaks.get("bf16_tflops_sustained") or 1700.0
+    peak = bf16 * (1.1 / 2.25) if prec == B.ORTHO_TF32 else None
+    tflops = flops / t / 1e12
+    mg.close()
+    print(json.dumps({
+        "metric": "orthogonalised merge round GEMM TFLOP/s", "value": round(tflops, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": args.ortho_precision, "data": "synthetic",
+        "config": {"workload": wl.name, "op": "orthogonalize", "iterations": its,
+                   "n_params": wl.n_params, "K": wl.K, "flops_per_step": flops,
+                   "matrices": n_mat},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
+                     "peak": None if peak is None else round(peak, 1), "unit": "TFLOP/s",
+                     "frac": None if peak is None else round(tflops / peak, 4),
+                     "peak_source": "measured bf16 sustained x nominal tf32/bf16 (1.1/2.25)",
+                     "traffic": None, "kernel": "cuBLASLt GEMMs + ortho kernels"},
+        "clocks": clocks.summary(), "gpu_launches": own_launches,
+        "library_gemms": 2 * its * n_mat * args.steps}), flush=True)
+    return 0
+
+
 def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -583,7 +663,9 @@ def parse(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="diffurefill1b")
-    p.add_argument("--op", choices=("merge", "adopt"), default="merge")
+    p.add_argument("--op", choices=("merge", "adopt", "ortho"), default="merge")
+    p.add_argument("--ortho-iterations", type=int, default=30)
+    p.add_argument("--ortho-precision", choices=("tf32", "fp32"), default="tf32")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy"), default="stream")
@@ -603,6 +685,8 @@ def main(argv=None) -> int:
         return run_reference(args, wl, ws, rank)
     if args.op == "adopt":
         return run_adopt(args, wl, ws, rank, local)
+    if args.op == "ortho":
+        return run_ortho(args, wl, ws, rank, local)
     return run_ours(args, wl, ws, rank, local)
 
 

@@ -22,6 +22,8 @@ MAX_OPEN_ROUNDS = 8
 F32, BF16 = 0, 1
 MEAN_REPLACE, DELTA_NESTEROV = 0, 1
 INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
+ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
+ORTHO_TF32, ORTHO_FP32 = 0, 1
 
 OK, E_ARG, E_STATE, E_STALE, E_BUSY, E_QUORUM, E_KMAX, E_CUDA, E_NOMEM = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
@@ -80,6 +82,7 @@ class CtxDesc(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("stream", ctypes.c_void_p),
         ("swa", ctypes.POINTER(ctypes.c_void_p)),
+        ("rows", ctypes.POINTER(ctypes.c_int64)),
     ]
 
 
@@ -87,7 +90,7 @@ _lib = None
 
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
            "cam_merge_accumulate_host", "cam_merge_publish", "cam_swa_update", "cam_swa_reset",
-           "cam_worker_drift_norm", "cam_adopt_keep_drift",
+           "cam_worker_drift_norm", "cam_adopt_keep_drift", "cam_merge_orthogonalize",
            "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
@@ -119,6 +122,7 @@ def lib() -> ctypes.CDLL:
     L.cam_merge_publish.argtypes = [vp, vpp, vpp]
     L.cam_swa_update.argtypes = [vp]
     L.cam_worker_drift_norm.argtypes = [vp, vp, vp]
+    L.cam_merge_orthogonalize.argtypes = [vp, ctypes.c_float, i32, i32, i32]
     L.cam_adopt_keep_drift.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, ctypes.c_int, vp]
     L.cam_swa_reset.argtypes = [vp, i32, vp]
     L.cam_swa_counts.argtypes = [vp, ctypes.POINTER(i64)]
@@ -172,11 +176,12 @@ def _ptrs(values: Sequence[int] | None):
 
 def ctx_create(numel: Sequence[int], master: Sequence[int], *, fragment_of=None,
                n_fragments: int = 1, quorum: int = 1, momentum=None, ema=None,
-               device: int = 0, flags: int = 0, stream: int = 0, swa=None) -> int:
+               device: int = 0, flags: int = 0, stream: int = 0, swa=None, rows=None) -> int:
     n = len(numel)
     numel_a = (ctypes.c_int64 * max(1, n))(*[int(v) for v in numel])
     frag_a = None if fragment_of is None else (ctypes.c_int32 * max(1, n))(*fragment_of)
-    keep = [numel_a, frag_a, _ptrs(master), _ptrs(momentum), _ptrs(ema), _ptrs(swa)]
+    rows_a = None if rows is None else (ctypes.c_int64 * max(1, n))(*[int(v) for v in rows])
+    keep = [numel_a, frag_a, _ptrs(master), _ptrs(momentum), _ptrs(ema), _ptrs(swa), rows_a]
     d = CtxDesc(n, numel_a,
                 None if frag_a is None else ctypes.cast(frag_a, ctypes.POINTER(ctypes.c_int32)),
                 n_fragments, quorum,
@@ -184,7 +189,8 @@ def ctx_create(numel: Sequence[int], master: Sequence[int], *, fragment_of=None,
                 None if keep[3] is None else ctypes.cast(keep[3], ctypes.POINTER(ctypes.c_void_p)),
                 None if keep[4] is None else ctypes.cast(keep[4], ctypes.POINTER(ctypes.c_void_p)),
                 device, flags, stream or None,
-                None if keep[5] is None else ctypes.cast(keep[5], ctypes.POINTER(ctypes.c_void_p)))
+                None if keep[5] is None else ctypes.cast(keep[5], ctypes.POINTER(ctypes.c_void_p)),
+                None if rows_a is None else ctypes.cast(rows_a, ctypes.POINTER(ctypes.c_int64)))
     out = ctypes.c_void_p()
     _check(lib().cam_ctx_create(ctypes.byref(d), ctypes.byref(out)))
     return out.value
@@ -222,6 +228,11 @@ def ema_update(rd: int, beta: float) -> None:
 
 def worker_drift_norm(rd: int, per_worker_tensor: int | None, per_worker: int | None) -> None:
     _check(lib().cam_worker_drift_norm(rd, per_worker_tensor or None, per_worker or None))
+
+
+def merge_orthogonalize(rd: int, lr: float, scale_mode: int = ORTHO_SCALE_FIXED,
+                        precision: int = ORTHO_TF32, iterations: int = 30) -> None:
+    _check(lib().cam_merge_orthogonalize(rd, lr, scale_mode, precision, iterations))
 
 
 def swa_update(rd: int) -> None:
@@ -387,7 +398,9 @@ class Merger:
 
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
-                 zero_momentum=False, stream=None, swa=None, zero_swa=False):
+                 zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None):
+        """rows: optional per-tensor matrix rows (default: the tensors' first
+        dimension), used by orthogonalised rounds."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -421,7 +434,9 @@ class Merger:
                 ema=None if self.ema is None else [t.data_ptr() for t in self.ema],
                 device=dev.index if dev.index is not None else torch.cuda.current_device(),
                 flags=flags, stream=_stream_handle(stream),
-                swa=None if self.swa is None else [t.data_ptr() for t in self.swa])
+                swa=None if self.swa is None else [t.data_ptr() for t in self.swa],
+                rows=list(rows) if rows is not None else
+                [t.shape[0] if t.dim() >= 2 else 0 for t in self.master])
         self._frag_cache = {}
 
     def close(self):
@@ -550,6 +565,11 @@ class Round:
 
     def swa_update(self) -> None:
         swa_update(self.handle)
+
+    def orthogonalize(self, lr: float, scale_mode: int = ORTHO_SCALE_FIXED,
+                      precision: int = ORTHO_TF32, iterations: int = 30) -> None:
+        """Replace the averaged update of every matrix by its polar factor."""
+        merge_orthogonalize(self.handle, lr, scale_mode, precision, iterations)
 
     def worker_drift_norm(self, per_worker_tensor=None, per_worker=None) -> None:
         """Each worker's drift from the round's starting global: per_worker_tensor

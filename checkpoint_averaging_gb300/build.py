@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build", "cam")
 LIB = os.path.join(PKG, "libcam.so")
 
 SOURCES = ["merge_fused_f32.cu", "merge_fused_bf16.cu", "merge_kernels.cu", "runtime.cu",
-           "noalloc.cu", "adopt.cu"]
+           "noalloc.cu", "adopt.cu", "ortho.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if errors:
         raise RuntimeError("libcam build failed:\n" + "\n".join(errors))
     tmp = LIB + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"libcam link failed:\n$ {' '.join(link)}\n{r.stdout}")

@@ -82,6 +82,27 @@ struct NormArgs {
 
 enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 
+// Outer orthogonalisation (ortho.cu): a per-context workspace, made at the
+// first orthogonalised commit, and the per-matrix pipeline.
+struct OrthoWork;
+struct OrthoMatrix {
+    float* theta;
+    float* e;                    // EMA buffer or null
+    int64_t rows, cols;          // row-major
+    const void* x[CAM_KMAX];     // the included workers' copies, arrival order
+};
+struct OrthoParams {
+    int K, dtype;
+    float lr;
+    int scale_mode, precision, iterations;
+    bool ema;
+    float beta;
+};
+int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r);
+void ortho_destroy(OrthoWork* w);
+int ortho_matrix(OrthoWork* w, const OrthoMatrix& t, const OrthoParams& p, cudaStream_t s,
+                 int sm_count, int64_t* launches);
+
 // Records a message for the calling thread (returned by cam_last_error) and
 // returns `code`.
 int record_error(int code, const char* fmt, ...);

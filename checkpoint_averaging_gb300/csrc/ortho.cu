@@ -1,0 +1,385 @@
+// ortho.cu -- outer orthogonalisation of a plain-mean round: the averaged
+// update of every matrix-shaped tensor is replaced by its polar factor
+// ("DiffuRefill-1B: Pretraining a Masked Diffusion Language Model on Free,
+// Preemptible Notebook GPUs", section 5.3).
+//
+// Per matrix tensor (row-major m x n):
+//   1. Delta = mean_k(x_k) - theta with the plain-mean arithmetic of the fused
+//      pass, into a workspace, with |Delta|_F^2 summed in a fixed order;
+//   2. X0 = Delta / |Delta|_F, so every singular value lies in (0, 1];
+//   3. `iterations` Newton-Schulz steps X <- 1.5 X - 0.5 X (X^T X) (with the
+//      smaller Gram matrix), which drive every singular value to 1 and so
+//      converge to the polar factor U V^T;
+//   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), then the
+//      EMA of the globals.
+// The two GEMMs of a step are plain dense contractions and run on the tensor
+// cores through cuBLASLt (TF32 inputs with fp32 accumulation, or full fp32),
+// loaded with dlopen the first time a context orthogonalises, so the rest of
+// the library never depends on it. The element-wise steps are this file's
+// kernels.
+#include <cublasLt.h>
+#include <cuda_runtime.h>
+#include <dlfcn.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "cam_internal.h"
+#include "merge_device.cuh"
+
+namespace cam {
+namespace {
+
+// ---- cuBLASLt, resolved at run time ------------------------------------------------
+
+struct LtApi {
+    bool ok = false;
+    decltype(&cublasLtCreate) create = nullptr;
+    decltype(&cublasLtDestroy) destroy = nullptr;
+    decltype(&cublasLtMatmulDescCreate) desc_create = nullptr;
+    decltype(&cublasLtMatmulDescDestroy) desc_destroy = nullptr;
+    decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
+    decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
+    decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
+    decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
+    decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
+    decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
+    decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
+    decltype(&cublasLtMatmul) matmul = nullptr;
+};
+
+LtApi g_lt;
+std::mutex g_lt_mutex;
+
+template <typename F>
+bool resolve(void* h, const char* name, F& out) {
+    out = reinterpret_cast<F>(dlsym(h, name));
+    return out != nullptr;
+}
+
+const LtApi* lt_api() {
+    std::lock_guard<std::mutex> lock(g_lt_mutex);
+    if (g_lt.ok) return &g_lt;
+    void* h = dlopen("libcublasLt.so.13", RTLD_NOW | RTLD_GLOBAL);
+    if (!h) h = dlopen("/usr/local/cuda/lib64/libcublasLt.so.13", RTLD_NOW | RTLD_GLOBAL);
+    if (!h) return nullptr;
+    LtApi a;
+    bool ok = resolve(h, "cublasLtCreate", a.create) && resolve(h, "cublasLtDestroy", a.destroy) &&
+              resolve(h, "cublasLtMatmulDescCreate", a.desc_create) &&
+              resolve(h, "cublasLtMatmulDescDestroy", a.desc_destroy) &&
+              resolve(h, "cublasLtMatmulDescSetAttribute", a.desc_set) &&
+              resolve(h, "cublasLtMatrixLayoutCreate", a.layout_create) &&
+              resolve(h, "cublasLtMatrixLayoutDestroy", a.layout_destroy) &&
+              resolve(h, "cublasLtMatmulPreferenceCreate", a.pref_create) &&
+              resolve(h, "cublasLtMatmulPreferenceDestroy", a.pref_destroy) &&
+              resolve(h, "cublasLtMatmulPreferenceSetAttribute", a.pref_set) &&
+              resolve(h, "cublasLtMatmulAlgoGetHeuristic", a.heuristic) &&
+              resolve(h, "cublasLtMatmul", a.matmul);
+    if (!ok) return nullptr;
+    a.ok = true;
+    g_lt = a;
+    return &g_lt;
+}
+
+constexpr size_t kLtWorkspace = size_t(32) << 20;
+
+// One cached GEMM configuration (column-major D = alpha op(A) op(B) + beta C).
+struct GemmPlan {
+    int64_t M, N, Kd, lda, ldb, ldc;
+    bool ta, tb;
+    int precision;
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulAlgo_t algo;
+};
+
+}  // namespace
+
+// Per-context workspace of the orthogonalisation, made at the first
+// orthogonalised commit: two fp32 matrix buffers sized for the context's
+// largest matrix, the Gram matrix, reduction partials and a cuBLASLt handle.
+struct OrthoWork {
+    const LtApi* lt = nullptr;
+    cublasLtHandle_t handle = nullptr;
+    float* X = nullptr;
+    float* Y = nullptr;
+    float* G = nullptr;
+    double* partials = nullptr;  // [kOrthoBlocksMax]
+    double* scalars = nullptr;   // [0] = |Delta|_F^2
+    float* inv_norm = nullptr;   // [0] = 1 / |Delta|_F (0 when Delta = 0)
+    void* lt_ws = nullptr;
+    void* block = nullptr;       // one cudaMalloc holding all of the above
+    std::vector<GemmPlan> plans; // cuBLASLt configurations by GEMM shape
+};
+
+}  // namespace cam
+
+namespace cam {
+namespace {
+
+constexpr int kOrthoThreads = 256;
+constexpr int kOrthoBlocksMax = 4096;
+
+struct DeltaArgs {
+    const void* x[CAM_KMAX];
+    int32_t K;
+    float Kf;
+    const float* theta;
+    float* X;
+    int64_t n;
+    double* partials;  // one per block
+};
+
+// Delta = (sum_k x_k, arrival order) / K - theta, the plain-mean arithmetic of
+// the fused pass, and each block's sum of Delta^2 (fp32 over at most 32
+// elements per thread, then fp64, reduced in a fixed order).
+template <typename XT>
+__global__ void __launch_bounds__(kOrthoThreads) ortho_delta(const DeltaArgs a) {
+    __shared__ double part[kOrthoThreads / 32];
+    double dacc = 0.0;
+    float acc = 0.0f;
+    int cnt = 0;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < a.n; i += stride) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k)
+            if (k < a.K) s = __fadd_rn(s, dev::load_x1(static_cast<const XT*>(a.x[k]) + i));
+        const float d = __fsub_rn(__fdiv_rn(s, a.Kf), a.theta[i]);
+        a.X[i] = d;
+        acc = __fmaf_rn(d, d, acc);
+        if (++cnt == 32) {
+            dacc += static_cast<double>(acc);
+            acc = 0.0f;
+            cnt = 0;
+        }
+    }
+    dacc = dev::warp_sum(dacc + static_cast<double>(acc));
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = dacc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int w = 0; w < kOrthoThreads / 32; ++w) s += part[w];
+        a.partials[blockIdx.x] = s;
+    }
+}
+
+// |Delta|_F^2 in a fixed order, and 1/|Delta|_F (0 for a zero update, which
+// then stays zero through the iteration and leaves theta unchanged).
+__global__ void ortho_norm(const double* partials, int nb, double* scalars, float* inv_norm) {
+    double s = 0.0;
+    for (int b = threadIdx.x; b < nb; b += 32) s += partials[b];
+    s = dev::warp_sum(s);
+    if (threadIdx.x == 0) {
+        scalars[0] = s;
+        inv_norm[0] = s > 0.0 ? static_cast<float>(1.0 / sqrt(s)) : 0.0f;
+    }
+}
+
+__global__ void ortho_scale(float* X, int64_t n, const float* inv_norm) {
+    const float f = *inv_norm;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        X[i] = __fmul_rn(X[i], f);
+}
+
+struct ApplyArgs {
+    float* theta;
+    float* e;         // EMA buffer, or null
+    const float* O;   // the polar factor (converged iterate)
+    int64_t n;
+    const double* scalars;
+    float lr;
+    int32_t scale_mode;
+    int64_t r;        // min(m, n)
+    float beta;
+};
+
+// theta' = theta + s O, then e' = beta e + (1 - beta) theta'.
+__global__ void ortho_apply(const ApplyArgs a) {
+    float s = a.lr;
+    if (a.scale_mode == CAM_ORTHO_SCALE_MATCH_NORM)
+        s = static_cast<float>(static_cast<double>(a.lr) * sqrt(a.scalars[0]) /
+                               sqrt(static_cast<double>(a.r)));
+    const float omb = __fsub_rn(1.0f, a.beta);
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < a.n;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const float th = __fadd_rn(a.theta[i], __fmul_rn(s, a.O[i]));
+        a.theta[i] = th;
+        if (a.e) a.e[i] = __fadd_rn(__fmul_rn(a.beta, a.e[i]), __fmul_rn(omb, th));
+    }
+}
+
+}  // namespace
+}  // namespace cam
+
+namespace cam {
+namespace {
+
+int lt_fail(const char* what, int st) {
+    return record_error(CAM_E_CUDA, "orthogonalisation: %s failed (cuBLASLt status %d)", what, st);
+}
+
+// Finds or builds the plan for this GEMM shape.
+int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
+              int64_t M, int64_t N, int64_t Kd, int64_t lda, int64_t ldb, int64_t ldc,
+              const GemmPlan** out) {
+    std::vector<GemmPlan>& cache = w->plans;
+    for (const GemmPlan& p : cache)
+        if (p.M == M && p.N == N && p.Kd == Kd && p.lda == lda && p.ldb == ldb && p.ldc == ldc &&
+            p.ta == ta && p.tb == tb && p.precision == precision) {
+            *out = &p;
+            return CAM_OK;
+        }
+    const LtApi& L = *w->lt;
+    GemmPlan p{M, N, Kd, lda, ldb, ldc, ta, tb, precision};
+    const cublasComputeType_t ct =
+        precision == CAM_ORTHO_FP32 ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_FAST_TF32;
+    int st = L.desc_create(&p.op, ct, CUDA_R_32F);
+    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matmul descriptor", st);
+    const cublasOperation_t oa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, ob = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
+    L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &oa, sizeof oa);
+    L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &ob, sizeof ob);
+    st = L.layout_create(&p.la, CUDA_R_32F, ta ? Kd : M, ta ? M : Kd, lda);
+    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lb, CUDA_R_32F, tb ? N : Kd, tb ? Kd : N, ldb);
+    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lc, CUDA_R_32F, M, N, ldc);
+    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matrix layout", st);
+    cublasLtMatmulPreference_t pref = nullptr;
+    st = L.pref_create(&pref);
+    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("preference", st);
+    const uint64_t ws = kLtWorkspace;
+    L.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws, sizeof ws);
+    cublasLtMatmulHeuristicResult_t res;
+    int found = 0;
+    st = L.heuristic(w->handle, p.op, p.la, p.lb, p.lc, p.lc, pref, 1, &res, &found);
+    L.pref_destroy(pref);
+    if (st != CUBLAS_STATUS_SUCCESS || found < 1) return lt_fail("algorithm heuristic", st);
+    p.algo = res.algo;
+    cache.push_back(p);
+    *out = &cache.back();
+    return CAM_OK;
+}
+
+int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
+         int64_t N, int64_t Kd, float alpha, const float* A, int64_t lda, const float* B,
+         int64_t ldb, float beta, const float* C, float* D, int64_t ldc, cudaStream_t s) {
+    const GemmPlan* p = nullptr;
+    int rc = gemm_plan(w, precision, ta, tb, M, N, Kd, lda, ldb, ldc, &p);
+    if (rc != CAM_OK) return rc;
+    const int st = w->lt->matmul(w->handle, p->op, &alpha, A, p->la, B, p->lb, &beta, C, p->lc, D,
+                                 p->lc, &p->algo, w->lt_ws, kLtWorkspace, s);
+    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matmul", st);
+    return CAM_OK;
+}
+
+}  // namespace
+}  // namespace cam
+
+namespace cam {
+
+int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r) {
+    *out = nullptr;
+    const LtApi* lt = lt_api();
+    if (!lt)
+        return record_error(CAM_E_CUDA,
+                            "orthogonalisation needs cuBLASLt (libcublasLt.so.13), which could not "
+                            "be loaded");
+    OrthoWork* w = new (std::nothrow) OrthoWork;
+    if (!w) return record_error(CAM_E_NOMEM, "orthogonalisation: out of host memory");
+    w->lt = lt;
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    const size_t bx = up(sizeof(float) * size_t(std::max<int64_t>(max_elems, 1)));
+    const size_t bg = up(sizeof(float) * size_t(std::max<int64_t>(max_r * max_r, 1)));
+    const size_t bp = up(sizeof(double) * kOrthoBlocksMax);
+    const size_t total = 2 * bx + bg + bp + 256 + 256 + kLtWorkspace;
+    if (cudaMalloc(&w->block, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete w;
+        return record_error(CAM_E_NOMEM, "orthogonalisation: cudaMalloc(%zu) failed", total);
+    }
+    char* b = static_cast<char*>(w->block);
+    w->X = reinterpret_cast<float*>(b);
+    w->Y = reinterpret_cast<float*>(b + bx);
+    w->G = reinterpret_cast<float*>(b + 2 * bx);
+    w->partials = reinterpret_cast<double*>(b + 2 * bx + bg);
+    w->scalars = reinterpret_cast<double*>(b + 2 * bx + bg + bp);
+    w->inv_norm = reinterpret_cast<float*>(b + 2 * bx + bg + bp + 256);
+    w->lt_ws = b + 2 * bx + bg + bp + 512;
+    const int st = lt->create(&w->handle);
+    if (st != CUBLAS_STATUS_SUCCESS) {
+        cudaFree(w->block);
+        delete w;
+        return lt_fail("handle", st);
+    }
+    *out = w;
+    return CAM_OK;
+}
+
+void ortho_destroy(OrthoWork* w) {
+    if (!w) return;
+    for (GemmPlan& p : w->plans) {
+        w->lt->layout_destroy(p.la);
+        w->lt->layout_destroy(p.lb);
+        w->lt->layout_destroy(p.lc);
+        w->lt->desc_destroy(p.op);
+    }
+    if (w->handle) w->lt->destroy(w->handle);
+    cudaFree(w->block);
+    delete w;
+}
+
+int ortho_matrix(OrthoWork* w, const OrthoMatrix& t, const OrthoParams& p, cudaStream_t s,
+                 int sm_count, int64_t* launches) {
+    const int64_t m = t.rows, n = t.cols, numel = m * n;
+    const int grid = static_cast<int>(std::min<int64_t>(
+        kOrthoBlocksMax, std::max<int64_t>(1, std::min<int64_t>(int64_t(sm_count) * 4,
+                                                                (numel + kOrthoThreads - 1) / kOrthoThreads))));
+    DeltaArgs da;
+    for (int k = 0; k < CAM_KMAX; ++k) da.x[k] = k < p.K ? t.x[k] : nullptr;
+    da.K = p.K;
+    da.Kf = static_cast<float>(p.K);
+    da.theta = t.theta;
+    da.X = w->X;
+    da.n = numel;
+    da.partials = w->partials;
+    if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<grid, kOrthoThreads, 0, s>>>(da);
+    else ortho_delta<float><<<grid, kOrthoThreads, 0, s>>>(da);
+    ortho_norm<<<1, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
+    ortho_scale<<<grid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
+    *launches += 3;
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess)
+        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
+    // Row-major X (m x n) is the column-major n x m matrix A = X^T (ld n).
+    float* cur = w->X;
+    float* nxt = w->Y;
+    const int64_t r = std::min(m, n);
+    for (int it = 0; it < p.iterations; ++it) {
+        int rc;
+        if (m >= n) {  // G = X^T X = A A^T (n x n); X' = 1.5 X - 0.5 X G, i.e. A' = 1.5 A - 0.5 G A
+            rc = gemm(w, p.precision, false, true, n, n, m, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G, n, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, p.precision, false, false, n, m, n, -0.5f, w->G, n, cur, n, 1.5f, cur, nxt,
+                          n, s);
+        } else {       // G = X X^T = A^T A (m x m); A' = 1.5 A - 0.5 A G
+            rc = gemm(w, p.precision, true, false, m, m, n, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G, m, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, p.precision, false, false, n, m, m, -0.5f, cur, n, w->G, m, 1.5f, cur, nxt,
+                          n, s);
+        }
+        if (rc != CAM_OK) return rc;
+        std::swap(cur, nxt);
+    }
+    ApplyArgs aa{t.theta, p.ema ? t.e : nullptr, cur, numel, w->scalars, p.lr, p.scale_mode, r, p.beta};
+    ortho_apply<<<grid, kOrthoThreads, 0, s>>>(aa);
+    *launches += 1;
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess)
+        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
+    return CAM_OK;
+}
+
+}  // namespace cam

@@ -114,6 +114,12 @@ struct cam_ctx {
     std::vector<float*> theta, m, e, swa;
     bool has_m = false, has_e = false, has_swa = false;
     std::vector<int64_t> swa_count;  // globals folded into each tensor's running average
+    std::vector<int64_t> rows;       // matrix rows of each tensor (0: not a matrix)
+    cam::OrthoWork* ortho = nullptr; // made at the first orthogonalised commit
+    int64_t ortho_max_elems = 0, ortho_max_r = 0;
+    bool is_matrix(int32_t g) const {
+        return rows[g] >= 2 && numel[g] % rows[g] == 0 && numel[g] / rows[g] >= 2;
+    }
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
@@ -152,6 +158,9 @@ struct cam_round {
     bool swa = false;
     bool publish = false;
     bool publish_ema = false;
+    bool ortho = false;
+    float ortho_lr = 0.0f;
+    int ortho_scale = 0, ortho_precision = 0, ortho_iterations = 0;
     std::vector<void*> pub_theta, pub_ema;  // [T_f] device-visible addresses
 };
 
@@ -216,6 +225,7 @@ int validate_desc(const cam_ctx_desc* d) {
             return fail(CAM_E_ARG, "cam_ctx_create: ema[%d] is NULL", t);
         if (n > 0 && d->swa && !d->swa[t])
             return fail(CAM_E_ARG, "cam_ctx_create: swa[%d] is NULL", t);
+        if (d->rows && d->rows[t] < 0) return fail(CAM_E_ARG, "cam_ctx_create: rows[%d] < 0", t);
     }
     return CAM_OK;
 }
@@ -268,6 +278,13 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     if (c->has_e) c->e.assign(d->ema, d->ema + d->n_tensors);
     if (c->has_swa) c->swa.assign(d->swa, d->swa + d->n_tensors);
     c->swa_count.assign(d->n_tensors, 0);
+    c->rows.assign(d->n_tensors, 0);
+    if (d->rows) c->rows.assign(d->rows, d->rows + d->n_tensors);
+    for (int32_t t = 0; t < c->n_tensors; ++t)
+        if (c->is_matrix(t)) {
+            c->ortho_max_elems = std::max(c->ortho_max_elems, c->numel[t]);
+            c->ortho_max_r = std::max(c->ortho_max_r, std::min(c->rows[t], c->numel[t] / c->rows[t]));
+        }
 
     // Plans and one device block holding every plan's tables.
     c->plans.resize(c->n_fragments + 1);
@@ -361,9 +378,10 @@ CAM_API void cam_ctx_destroy(cam_ctx* c) {
     if (!c) return;
     for (cam_round* r : c->open) delete r;
     c->open.clear();
-    if (c->dev_block) {
+    if (c->dev_block || c->ortho) {
         DeviceScope scope(c->device);
-        cudaFree(c->dev_block);
+        if (c->dev_block) cudaFree(c->dev_block);
+        cam::ortho_destroy(c->ortho);
     }
     delete c;
 }
@@ -511,6 +529,26 @@ CAM_API int cam_worker_drift_norm(cam_round* r, double* per_worker_tensor, doubl
     return CAM_OK;
 }
 
+CAM_API int cam_merge_orthogonalize(cam_round* r, float lr, int32_t scale_mode, int32_t precision,
+                                    int32_t iterations) {
+    const char* fn = "cam_merge_orthogonalize";
+    if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
+    if (r->ortho) return fail(CAM_E_STATE, "%s: asked twice", fn);
+    if (!std::isfinite(lr)) return fail(CAM_E_ARG, "%s: lr must be finite", fn);
+    if (scale_mode != CAM_ORTHO_SCALE_FIXED && scale_mode != CAM_ORTHO_SCALE_MATCH_NORM)
+        return fail(CAM_E_ARG, "%s: unknown scale mode %d", fn, scale_mode);
+    if (precision != CAM_ORTHO_TF32 && precision != CAM_ORTHO_FP32)
+        return fail(CAM_E_ARG, "%s: unknown precision %d", fn, precision);
+    if (iterations < 1 || iterations > 1000)
+        return fail(CAM_E_ARG, "%s: iterations %d outside [1, 1000]", fn, iterations);
+    r->ortho = true;
+    r->ortho_lr = lr;
+    r->ortho_scale = scale_mode;
+    r->ortho_precision = precision;
+    r->ortho_iterations = iterations;
+    return CAM_OK;
+}
+
 CAM_API int cam_swa_update(cam_round* r) {
     if (!r) return fail(CAM_E_ARG, "cam_swa_update: round is NULL");
     if (r->swa) return fail(CAM_E_STATE, "cam_swa_update: asked twice");
@@ -587,6 +625,14 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     if (r->mode == CAM_MODE_DELTA_NESTEROV && W <= 0)
         return fail(CAM_E_ARG, "cam_merge_commit: total token count must be > 0");
 
+    if (r->ortho) {
+        if (r->mode != CAM_MODE_MEAN_REPLACE)
+            return fail(CAM_E_STATE, "cam_merge_commit: orthogonalisation applies to plain-mean rounds");
+        if (r->norms || r->worker_norms || r->publish || r->swa)
+            return fail(CAM_E_STATE,
+                        "cam_merge_commit: an orthogonalised round takes only an EMA update");
+    }
+
     const Plan& p = c->plan_of(r->fragment);
     const int K = r->K;
     const int T = p.n_tensors();
@@ -626,41 +672,85 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         close_round(r);
         return cuda_fail(scope.err, "cam_merge_commit: cudaSetDevice");
     }
+    if (r->ortho && !c->ortho) {  // workspace of the orthogonalisation, made once per context
+        const int rc = cam::ortho_create(&c->ortho, c->ortho_max_elems, c->ortho_max_r);
+        if (rc != CAM_OK) {
+            close_round(r);
+            return rc;
+        }
+    }
     cudaError_t ce = cudaSuccess;
     const int per_launch = cam::kXCap / stride;
-    for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += per_launch) {
-        const int n = std::min(per_launch, T - l0);
-        const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
-        if (c1 == c0) continue;
-        std::memset(a.vec, 0, sizeof a.vec);
-        for (int l = 0; l < n; ++l) {
-            const int32_t g = p.tensors[l0 + l];
-            bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
-                     (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32));
-            for (int k = 0; k < K; ++k) {
-                const void* xp = r->x[size_t(k) * T + l0 + l];
-                a.x[size_t(l) * stride + k] = xp;
-                v = v && aligned(xp, xa);
+    // Fused pass over the fragment's local tensors [lb, le).
+    auto launch_range = [&](int lb, int le) {
+        for (int l0 = lb; l0 < le && ce == cudaSuccess; l0 += per_launch) {
+            const int n = std::min(per_launch, le - l0);
+            const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
+            if (c1 == c0) continue;
+            std::memset(a.vec, 0, sizeof a.vec);
+            for (int l = 0; l < n; ++l) {
+                const int32_t g = p.tensors[l0 + l];
+                bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
+                         (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32));
+                for (int k = 0; k < K; ++k) {
+                    const void* xp = r->x[size_t(k) * T + l0 + l];
+                    a.x[size_t(l) * stride + k] = xp;
+                    v = v && aligned(xp, xa);
+                }
+                if (r->publish) {
+                    void* pt = r->pub_theta[l0 + l];
+                    void* pe = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
+                    a.x[size_t(l) * stride + K] = pt;
+                    a.x[size_t(l) * stride + K + 1] = pe;
+                    v = v && aligned(pt, 32) && aligned(pe, 32);
+                }
+                if (v) a.vec[l >> 5] |= 1u << (l & 31);
             }
-            if (r->publish) {
-                void* pt = r->pub_theta[l0 + l];
-                void* pe = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
-                a.x[size_t(l) * stride + K] = pt;
-                a.x[size_t(l) * stride + K + 1] = pe;
-                v = v && aligned(pt, 32) && aligned(pe, 32);
-            }
-            if (v) a.vec[l >> 5] |= 1u << (l & 31);
+            a.chunks = p.d_chunks + c0;
+            a.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
+            a.worker_partials =
+                norm_level >= 2 ? p.d_worker_partials + static_cast<int64_t>(c0) * CAM_KMAX : nullptr;
+            a.n_chunks = c1 - c0;
+            a.local0 = l0;
+            a.n_local = n;
+            const int grid =
+                static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
+            ce = cam::launch_merge(a, variant, grid, s);
+            ++c->launches;
         }
-        a.chunks = p.d_chunks + c0;
-        a.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
-        a.worker_partials =
-            norm_level >= 2 ? p.d_worker_partials + static_cast<int64_t>(c0) * CAM_KMAX : nullptr;
-        a.n_chunks = c1 - c0;
-        a.local0 = l0;
-        a.n_local = n;
-        const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
-        ce = cam::launch_merge(a, variant, grid, s);
-        ++c->launches;
+    };
+    if (!r->ortho) {
+        launch_range(0, T);
+    } else {
+        // the vectors and other non-matrix tensors take the fused pass ...
+        int run = -1;
+        for (int l = 0; l <= T; ++l) {
+            const bool mat = l < T && c->is_matrix(p.tensors[l]);
+            if (l < T && !mat) {
+                if (run < 0) run = l;
+            } else if (run >= 0) {
+                launch_range(run, l);
+                run = -1;
+            }
+        }
+        // ... and each matrix has its averaged update replaced by its polar factor
+        const cam::OrthoParams op{K, r->dtype, r->ortho_lr, r->ortho_scale, r->ortho_precision,
+                                  r->ortho_iterations, r->ema, r->beta};
+        for (int l = 0; l < T && ce == cudaSuccess; ++l) {
+            const int32_t g = p.tensors[l];
+            if (!c->is_matrix(g)) continue;
+            cam::OrthoMatrix om;
+            om.theta = c->theta[g];
+            om.e = c->e[g];
+            om.rows = c->rows[g];
+            om.cols = c->numel[g] / c->rows[g];
+            for (int k = 0; k < CAM_KMAX; ++k) om.x[k] = k < K ? r->x[size_t(k) * T + l] : nullptr;
+            const int rc = cam::ortho_matrix(c->ortho, om, op, s, c->sm_count, &c->launches);
+            if (rc != CAM_OK) {
+                close_round(r);
+                return rc;
+            }
+        }
     }
     if (ce == cudaSuccess && norm_level >= 1) {
         NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,

@@ -79,6 +79,12 @@ typedef enum {
 #define CAM_INIT_ZERO_MOMENTUM 2u   /* at create: m <- 0 */
 #define CAM_INIT_ZERO_SWA 4u        /* at create: running averages <- 0, no globals folded */
 
+/* cam_merge_orthogonalize */
+#define CAM_ORTHO_SCALE_FIXED 0      /* theta' = theta + lr * polar(Delta) */
+#define CAM_ORTHO_SCALE_MATCH_NORM 1 /* ... + lr * |Delta|_F / sqrt(min(m, n)) * polar(Delta) */
+#define CAM_ORTHO_TF32 0             /* GEMMs on the tensor cores, TF32 inputs, fp32 accumulation */
+#define CAM_ORTHO_FP32 1             /* GEMMs in full fp32 */
+
 typedef struct cam_ctx cam_ctx;     /* opaque */
 typedef struct cam_round cam_round; /* opaque */
 
@@ -107,6 +113,10 @@ typedef struct {
     void* stream;               /* cudaStream_t for the CAM_INIT_* work; NULL = default */
     float* const* swa;          /* host array of n_tensors device pointers, or NULL:
                                    uniform running averages of the globals */
+    const int64_t* rows;        /* host, [n_tensors] or NULL: tensor t is a row-major
+                                   rows[t] x (numel[t] / rows[t]) matrix when both are >= 2
+                                   and divide evenly; it matters only to orthogonalised
+                                   rounds (cam_merge_orthogonalize) */
 } cam_ctx_desc;
 
 /*
@@ -176,6 +186,28 @@ int cam_merge_finalize(cam_round* rd, cam_mode mode, float lr, float mu);
  * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
  */
 int cam_ema_update(cam_round* rd, float beta);
+
+/*
+ * Outer orthogonalisation ("DiffuRefill-1B" technical report, section 5.3:
+ * replacing the averaged update by its polar factor helped a 4-worker stand
+ * run). For every matrix-shaped tensor of the round (cam_ctx_desc.rows), the
+ * plain-mean update Delta = mean_k(x_k) - theta (the same fp32 arithmetic as
+ * a plain-mean round) is replaced by its polar factor U V^T, and
+ * theta' = theta + s * U V^T with s = lr (CAM_ORTHO_SCALE_FIXED) or
+ * s = lr * |Delta|_F / sqrt(min(m, n)) (CAM_ORTHO_SCALE_MATCH_NORM: the
+ * update keeps Delta's Frobenius norm). Other tensors are merged by plain
+ * replacement. The polar factor is reached by `iterations` Newton-Schulz
+ * steps from Delta / |Delta|_F (X <- 1.5 X - 0.5 X X^T X, on the tensor
+ * cores via cuBLASLt in `precision`); singular values of Delta below about
+ * 1.5^-(iterations - 8) of the largest have not converged by then. Only
+ * plain-mean rounds, and only with an EMA update (no drift norms, publish or
+ * running average: CAM_E_STATE at commit). The first orthogonalised commit
+ * of a context allocates its workspace (two fp32 copies of the largest
+ * matrix, its Gram matrix and 32 MiB for cuBLASLt) and loads cuBLASLt
+ * (CAM_E_CUDA if it cannot). Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
+ */
+int cam_merge_orthogonalize(cam_round* rd, float lr, int32_t scale_mode, int32_t precision,
+                            int32_t iterations);
 
 /*
  * Asks for each worker's own drift, written on the commit stream: worker k

@@ -719,3 +719,138 @@ def test_keep_drift_adoption_of_an_unmoved_worker_lands_near_the_global():
     B.adopt_keep_drift([th], [g], [p])
     torch.cuda.synchronize()
     assert ((th - g).abs() <= 2 * 2 ** -24 * (p.abs() + g.abs()) + 1e-30).all()
+
+
+# ---- outer orthogonalisation (technical report, section 5.3) -----------------------
+
+ORTHO_SHAPES = [(96, 40), (40, 96), (64, 64), (333, 0), (50, 7), (1, 0)]
+# Error of the applied step relative to its largest element, by GEMM precision.
+# TF32 rounds GEMM inputs to 11 significant bits (u = 2^-11 = 4.9e-4); the
+# Newton-Schulz fixed point absorbs each step's rounding, and the measured
+# error stays at 1.4-1.8 u (2048x2048 to 96x40 after 40 steps): the bound is
+# 8 u. With fp32 GEMMs the measured error is 0.6-2e-6; the bound is 1e-5.
+ORTHO_TOL = {B.ORTHO_FP32: 1e-5, B.ORTHO_TF32: 8 * 2.0 ** -11}
+
+
+def _ortho_round(shapes, dtype, precision, mode, lr, iterations=40, seed=31, K=3):
+    sizes = [r * c if c else r for r, c in shapes]
+    rows = [r if c else 0 for r, c in shapes]
+    wl = _custom(sizes, K=K, mode="mean", dtype=dtype)
+    g = W.make_global(wl, seed, DEV)
+    th = W.empty_arena(g.numels, torch.float32, DEV)
+    th.flat.copy_(g.flat)
+    e = W.empty_arena(g.numels, torch.float32, DEV)
+    e.flat.copy_(g.flat)
+    mg = B.Merger(th.views, ema=e.views, quorum=K, rows=rows)
+    workers = [W.make_worker(wl, g, 0, k, seed, DEV) for k in range(K)]
+    rd = mg.begin(0)
+    for k in range(K):
+        rd.accumulate(workers[k].views, 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.ema_update(0.9)
+    rd.orthogonalize(lr, mode, precision, iterations)
+    rd.commit()
+    torch.cuda.synchronize()
+    out = []
+    for t, (r, c) in enumerate(shapes):
+        xs = [to_np(w.views[t]) for w in workers]
+        th0 = to_np(g.views[t]).copy()
+        got = to_np(th.views[t])
+        if c:
+            want, delta = oracle.orthogonal_update(xs, th0, r, lr=lr, scale_mode=mode)
+            out.append(("matrix", t, r, c, th0, got, want, delta, to_np(e.views[t])))
+        else:
+            want = th0.copy()
+            oracle.merge_tensor(xs, want, mode=oracle.MEAN_REPLACE)
+            out.append(("vector", t, r, c, th0, got, want, None, to_np(e.views[t])))
+    mg.close()
+    return out
+
+
+@pytest.mark.parametrize("precision", [B.ORTHO_FP32, B.ORTHO_TF32])
+@pytest.mark.parametrize("mode", [B.ORTHO_SCALE_FIXED, B.ORTHO_SCALE_MATCH_NORM])
+def test_orthogonalised_round_matches_the_polar_factor(precision, mode):
+    lr = 0.01 if mode == B.ORTHO_SCALE_FIXED else 0.7
+    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(ORTHO_SHAPES, "f32", precision,
+                                                                 mode, lr):
+        if kind == "vector":   # non-matrix tensors take plain replacement, bit for bit
+            assert bitwise_equal(got, want.astype(np.float32)), t
+            continue
+        step_want = want - th0.astype(np.float64)
+        scale = np.abs(step_want).max()
+        err = np.abs(got.astype(np.float64) - want).max()
+        print(f"ortho precision={precision} mode={mode} {r}x{c}: max err / max step = {err / scale:.3e}")
+        # the fp32 rounding of theta' itself adds at most one ulp of |theta'|
+        assert err <= ORTHO_TOL[precision] * scale + 2 * np.spacing(np.float32(np.abs(want).max()))
+        # the applied step is semi-orthogonal up to the same tolerance
+        o = (got.astype(np.float64) - th0).reshape(r, c)
+        o *= np.sqrt(min(r, c)) / np.linalg.norm(o)   # singular values ~1 if semi-orthogonal
+        gram = o.T @ o if r >= c else o @ o.T
+        assert np.abs(gram - np.eye(min(r, c))).max() <= 30 * ORTHO_TOL[precision]
+        # EMA of the new global, from the GPU's theta'
+        e_want = 0.9 * th0.astype(np.float64) + np.float64(np.float32(1) - np.float32(0.9)) * got
+        assert np.abs(e.astype(np.float64) - e_want).max() <= 4 * np.spacing(np.float32(np.abs(e_want).max()))
+
+
+def test_orthogonalised_round_bf16_workers():
+    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(ORTHO_SHAPES[:3], "bf16",
+                                                                 B.ORTHO_FP32, B.ORTHO_SCALE_FIXED,
+                                                                 0.01, seed=32):
+        scale = np.abs(want - th0).max()
+        assert np.abs(got - want).max() <= ORTHO_TOL[B.ORTHO_FP32] * scale + 1e-9
+
+
+def test_orthogonalised_round_on_1b_block_shapes_tf32():
+    shapes = [(2048, 2048), (5632, 2048), (2048, 5632), (2048, 0)]
+    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(shapes, "f32", B.ORTHO_TF32,
+                                                                 B.ORTHO_SCALE_MATCH_NORM, 0.7,
+                                                                 iterations=40, seed=33):
+        if kind == "vector":
+            continue
+        scale = np.abs(want - th0).max()
+        err = np.abs(got.astype(np.float64) - want).max()
+        print(f"1b block {r}x{c}: max err / max step = {err / scale:.3e}")
+        assert err <= ORTHO_TOL[B.ORTHO_TF32] * scale + 2 * np.spacing(np.float32(np.abs(want).max()))
+
+
+def test_orthogonalisation_of_a_zero_update_leaves_theta():
+    th = [torch.randn(64 * 32, device=DEV) * 0.02]
+    orig = th[0].clone()
+    mg = B.Merger(th, quorum=2, rows=[64])
+    rd = mg.begin(0)
+    rd.accumulate([orig.clone()], 0)
+    rd.accumulate([orig.clone()], 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.orthogonalize(1.0)
+    rd.commit()
+    torch.cuda.synchronize()
+    assert torch.equal(th[0], orig)
+    mg.close()
+
+
+def test_orthogonalisation_takes_only_plain_mean_with_ema():
+    th = [torch.zeros(16 * 8, device=DEV)]
+    m = [torch.zeros_like(th[0])]
+    mg = B.Merger(th, momentum=m, quorum=1, rows=[16])
+    x = [torch.ones(16 * 8, device=DEV)]
+    rd = mg.begin(0)
+    rd.accumulate(x, 5)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.orthogonalize(1.0)
+    with pytest.raises(B.StateError, match="plain-mean"):
+        rd.commit()
+    rd.abort()
+    rd = mg.begin(1)
+    rd.accumulate(x, 5)
+    rd.finalize(B.MEAN_REPLACE)
+    for bad in ((7, 0, 10), (0, 9, 10), (0, 0, 0)):   # scale mode, precision, iterations
+        with pytest.raises(B.ArgError):
+            B.merge_orthogonalize(rd.handle, 1.0, *bad)
+    rd.orthogonalize(1.0)
+    with pytest.raises(B.StateError, match="twice"):
+        rd.orthogonalize(1.0)
+    rd.drift_norm(torch.zeros(1, dtype=torch.float64, device=DEV), None)
+    with pytest.raises(B.StateError, match="only an EMA"):
+        rd.commit()
+    rd.abort()
+    mg.close()
