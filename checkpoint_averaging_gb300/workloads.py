@@ -271,8 +271,13 @@ def workload(name: str) -> Workload:
     if name in table:
         return table[name]()
     if name.startswith("sweep:"):
-        t, n, k = (int(v) for v in name.split(":")[1].split(","))
-        return sweep_workload(t, n, k)
+        parts = name.split(":")[1].split(",")
+        t, n, k = (int(v) for v in parts[:3])
+        wl = sweep_workload(t, n, k)
+        if len(parts) > 3 and parts[3] == "norms":  # Nesterov + EMA + drift norms
+            import dataclasses
+            wl = dataclasses.replace(wl, name=wl.name + "_norms", norms=True)
+        return wl
     raise KeyError(name)
 
 
