@@ -633,6 +633,16 @@ def run_ortho(args, wl, ws, rank, local) -> int:
     t = a.elapsed_time(b) / 1e3 / args.steps
     own_launches = mg.launch_count - l0
     n_mat = sum(1 for sp in wl.specs if len(sp.shape) == 2)
+    # GEMM calls: equal shapes are batched, as many per call as the workspace
+    # holds (the library sizes it like this: 2^29 / 2^28 floats at most)
+    mats = [sp.shape for sp in wl.specs if len(sp.shape) == 2]
+    cap_e = max(max(a * b for a, b in mats), min(sum(a * b for a, b in mats), 1 << 29))
+    cap_g = max(max(min(a, b) ** 2 for a, b in mats), min(sum(min(a, b) ** 2 for a, b in mats), 1 << 28))
+    batches = 0
+    for shape in dict.fromkeys(mats):
+        cnt = mats.count(shape)
+        per = max(1, min(256, cap_e // (shape[0] * shape[1]), cap_g // min(shape) ** 2))
+        batches += -(-cnt // per)
     peaks = measured_peaks()
     bf16 = peaks.get("bf16_tflops_sustained") or 1700.0
     peak = bf16 * (1.1 / 2.25) if prec == B.ORTHO_TF32 else None
@@ -652,7 +662,7 @@ def run_ortho(args, wl, ws, rank, local) -> int:
                      "peak_source": "measured bf16 sustained x nominal tf32/bf16 (1.1/2.25)",
                      "traffic": None, "kernel": "cuBLASLt GEMMs + ortho kernels"},
         "clocks": clocks.summary(), "gpu_launches": own_launches,
-        "library_gemms": 2 * its * n_mat * args.steps}), flush=True)
+        "library_gemms": 2 * its * batches * args.steps}), flush=True)
     return 0
 
 

@@ -98,10 +98,14 @@ struct OrthoParams {
     bool ema;
     float beta;
 };
-int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r);
+// cap_elems / cap_gram: floats in each iterate buffer and in the Gram buffer
+// (at least one matrix's worth; batches of equal-shape matrices share them).
+int ortho_create(OrthoWork** out, int64_t cap_elems, int64_t cap_gram);
 void ortho_destroy(OrthoWork* w);
-int ortho_matrix(OrthoWork* w, const OrthoMatrix& t, const OrthoParams& p, cudaStream_t s,
-                 int sm_count, int64_t* launches);
+// Orthogonalises `count` matrices of one shape, batching them into strided
+// GEMMs as far as the workspace allows.
+int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoParams& p,
+                cudaStream_t s, int sm_count, int64_t* launches);
 
 // Records a message for the calling thread (returned by cam_last_error) and
 // returns `code`.

@@ -44,6 +44,7 @@ struct LtApi {
     decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
     decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
     decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
+    decltype(&cublasLtMatrixLayoutSetAttribute) layout_set = nullptr;
     decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
     decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
     decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
@@ -73,6 +74,7 @@ const LtApi* lt_api() {
               resolve(h, "cublasLtMatmulDescSetAttribute", a.desc_set) &&
               resolve(h, "cublasLtMatrixLayoutCreate", a.layout_create) &&
               resolve(h, "cublasLtMatrixLayoutDestroy", a.layout_destroy) &&
+              resolve(h, "cublasLtMatrixLayoutSetAttribute", a.layout_set) &&
               resolve(h, "cublasLtMatmulPreferenceCreate", a.pref_create) &&
               resolve(h, "cublasLtMatmulPreferenceDestroy", a.pref_destroy) &&
               resolve(h, "cublasLtMatmulPreferenceSetAttribute", a.pref_set) &&
@@ -85,12 +87,16 @@ const LtApi* lt_api() {
 }
 
 constexpr size_t kLtWorkspace = size_t(32) << 20;
+constexpr int kOrthoBatchMax = 256;  // matrices orthogonalised together
+constexpr int kOrthoBlocksMax = 4096;
 
 // One cached GEMM configuration (column-major D = alpha op(A) op(B) + beta C).
 struct GemmPlan {
     int64_t M, N, Kd, lda, ldb, ldc;
     bool ta, tb;
     int precision;
+    int32_t batch;                   // matrices per call (strided batch)
+    int64_t sa, sb, sc;              // element strides between them
     cublasLtMatmulDesc_t op = nullptr;
     cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
     cublasLtMatmulAlgo_t algo;
@@ -107,11 +113,13 @@ struct OrthoWork {
     float* X = nullptr;
     float* Y = nullptr;
     float* G = nullptr;
-    double* partials = nullptr;  // [kOrthoBlocksMax]
-    double* scalars = nullptr;   // [0] = |Delta|_F^2
-    float* inv_norm = nullptr;   // [0] = 1 / |Delta|_F (0 when Delta = 0)
+    double* partials = nullptr;  // [kOrthoBatchMax * kOrthoBlocksMax]
+    double* scalars = nullptr;   // [j] = |Delta_j|_F^2
+    float* inv_norm = nullptr;   // [j] = 1 / |Delta_j|_F (0 when Delta_j = 0)
     void* lt_ws = nullptr;
     void* block = nullptr;       // one cudaMalloc holding all of the above
+    int64_t cap_elems = 0;       // floats in X and in Y
+    int64_t cap_gram = 0;        // floats in G
     std::vector<GemmPlan> plans; // cuBLASLt configurations by GEMM shape
 };
 
@@ -121,7 +129,6 @@ namespace cam {
 namespace {
 
 constexpr int kOrthoThreads = 256;
-constexpr int kOrthoBlocksMax = 4096;
 
 struct DeltaArgs {
     const void* x[CAM_KMAX];
@@ -226,16 +233,17 @@ int lt_fail(const char* what, int st) {
 // Finds or builds the plan for this GEMM shape.
 int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
               int64_t M, int64_t N, int64_t Kd, int64_t lda, int64_t ldb, int64_t ldc,
-              const GemmPlan** out) {
+              int32_t batch, int64_t sa, int64_t sb, int64_t sc, const GemmPlan** out) {
     std::vector<GemmPlan>& cache = w->plans;
     for (const GemmPlan& p : cache)
         if (p.M == M && p.N == N && p.Kd == Kd && p.lda == lda && p.ldb == ldb && p.ldc == ldc &&
-            p.ta == ta && p.tb == tb && p.precision == precision) {
+            p.ta == ta && p.tb == tb && p.precision == precision && p.batch == batch &&
+            p.sa == sa && p.sb == sb && p.sc == sc) {
             *out = &p;
             return CAM_OK;
         }
     const LtApi& L = *w->lt;
-    GemmPlan p{M, N, Kd, lda, ldb, ldc, ta, tb, precision};
+    GemmPlan p{M, N, Kd, lda, ldb, ldc, ta, tb, precision, batch, sa, sb, sc};
     const cublasComputeType_t ct =
         precision == CAM_ORTHO_FP32 ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_FAST_TF32;
     int st = L.desc_create(&p.op, ct, CUDA_R_32F);
@@ -247,6 +255,17 @@ int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
     if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lb, CUDA_R_32F, tb ? N : Kd, tb ? Kd : N, ldb);
     if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lc, CUDA_R_32F, M, N, ldc);
     if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matrix layout", st);
+    if (batch > 1) {
+        const cublasLtMatrixLayout_t lays[3] = {p.la, p.lb, p.lc};
+        const int64_t strides[3] = {sa, sb, sc};
+        for (int i = 0; i < 3 && st == CUBLAS_STATUS_SUCCESS; ++i) {
+            st = L.layout_set(lays[i], CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &batch, sizeof batch);
+            if (st == CUBLAS_STATUS_SUCCESS)
+                st = L.layout_set(lays[i], CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &strides[i],
+                                  sizeof strides[i]);
+        }
+        if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("batched layout", st);
+    }
     cublasLtMatmulPreference_t pref = nullptr;
     st = L.pref_create(&pref);
     if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("preference", st);
@@ -263,11 +282,14 @@ int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
     return CAM_OK;
 }
 
+// D = alpha op(A) op(B) + beta C for `batch` matrices at element strides
+// sa, sb, sc (column-major; C and D share a layout).
 int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
          int64_t N, int64_t Kd, float alpha, const float* A, int64_t lda, const float* B,
-         int64_t ldb, float beta, const float* C, float* D, int64_t ldc, cudaStream_t s) {
+         int64_t ldb, float beta, const float* C, float* D, int64_t ldc, int32_t batch,
+         int64_t sa, int64_t sb, int64_t sc, cudaStream_t s) {
     const GemmPlan* p = nullptr;
-    int rc = gemm_plan(w, precision, ta, tb, M, N, Kd, lda, ldb, ldc, &p);
+    int rc = gemm_plan(w, precision, ta, tb, M, N, Kd, lda, ldb, ldc, batch, sa, sb, sc, &p);
     if (rc != CAM_OK) return rc;
     const int st = w->lt->matmul(w->handle, p->op, &alpha, A, p->la, B, p->lb, &beta, C, p->lc, D,
                                  p->lc, &p->algo, w->lt_ws, kLtWorkspace, s);
@@ -280,7 +302,7 @@ int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
 
 namespace cam {
 
-int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r) {
+int ortho_create(OrthoWork** out, int64_t cap_elems, int64_t cap_gram) {
     *out = nullptr;
     const LtApi* lt = lt_api();
     if (!lt)
@@ -290,11 +312,15 @@ int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r) {
     OrthoWork* w = new (std::nothrow) OrthoWork;
     if (!w) return record_error(CAM_E_NOMEM, "orthogonalisation: out of host memory");
     w->lt = lt;
+    w->cap_elems = std::max<int64_t>(cap_elems, 1);
+    w->cap_gram = std::max<int64_t>(cap_gram, 1);
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
-    const size_t bx = up(sizeof(float) * size_t(std::max<int64_t>(max_elems, 1)));
-    const size_t bg = up(sizeof(float) * size_t(std::max<int64_t>(max_r * max_r, 1)));
-    const size_t bp = up(sizeof(double) * kOrthoBlocksMax);
-    const size_t total = 2 * bx + bg + bp + 256 + 256 + kLtWorkspace;
+    const size_t bx = up(sizeof(float) * size_t(w->cap_elems));
+    const size_t bg = up(sizeof(float) * size_t(w->cap_gram));
+    const size_t bp = up(sizeof(double) * size_t(kOrthoBatchMax) * kOrthoBlocksMax);
+    const size_t bs = up(sizeof(double) * kOrthoBatchMax);
+    const size_t bi = up(sizeof(float) * kOrthoBatchMax);
+    const size_t total = 2 * bx + bg + bp + bs + bi + kLtWorkspace;
     if (cudaMalloc(&w->block, total) != cudaSuccess) {
         cudaGetLastError();
         delete w;
@@ -306,8 +332,8 @@ int ortho_create(OrthoWork** out, int64_t max_elems, int64_t max_r) {
     w->G = reinterpret_cast<float*>(b + 2 * bx);
     w->partials = reinterpret_cast<double*>(b + 2 * bx + bg);
     w->scalars = reinterpret_cast<double*>(b + 2 * bx + bg + bp);
-    w->inv_norm = reinterpret_cast<float*>(b + 2 * bx + bg + bp + 256);
-    w->lt_ws = b + 2 * bx + bg + bp + 512;
+    w->inv_norm = reinterpret_cast<float*>(b + 2 * bx + bg + bp + bs);
+    w->lt_ws = b + 2 * bx + bg + bp + bs + bi;
     const int st = lt->create(&w->handle);
     if (st != CUBLAS_STATUS_SUCCESS) {
         cudaFree(w->block);
@@ -331,54 +357,71 @@ void ortho_destroy(OrthoWork* w) {
     delete w;
 }
 
-int ortho_matrix(OrthoWork* w, const OrthoMatrix& t, const OrthoParams& p, cudaStream_t s,
-                 int sm_count, int64_t* launches) {
-    const int64_t m = t.rows, n = t.cols, numel = m * n;
+int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoParams& p,
+                cudaStream_t s, int sm_count, int64_t* launches) {
+    if (count <= 0) return CAM_OK;
+    const int64_t m = mats[0].rows, n = mats[0].cols, numel = m * n;
+    const int64_t r = std::min(m, n), gram = r * r;
     const int grid = static_cast<int>(std::min<int64_t>(
         kOrthoBlocksMax, std::max<int64_t>(1, std::min<int64_t>(int64_t(sm_count) * 4,
                                                                 (numel + kOrthoThreads - 1) / kOrthoThreads))));
-    DeltaArgs da;
-    for (int k = 0; k < CAM_KMAX; ++k) da.x[k] = k < p.K ? t.x[k] : nullptr;
-    da.K = p.K;
-    da.Kf = static_cast<float>(p.K);
-    da.theta = t.theta;
-    da.X = w->X;
-    da.n = numel;
-    da.partials = w->partials;
-    if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<grid, kOrthoThreads, 0, s>>>(da);
-    else ortho_delta<float><<<grid, kOrthoThreads, 0, s>>>(da);
-    ortho_norm<<<1, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
-    ortho_scale<<<grid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
-    *launches += 3;
-    cudaError_t ce = cudaGetLastError();
-    if (ce != cudaSuccess)
-        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
-    // Row-major X (m x n) is the column-major n x m matrix A = X^T (ld n).
-    float* cur = w->X;
-    float* nxt = w->Y;
-    const int64_t r = std::min(m, n);
-    for (int it = 0; it < p.iterations; ++it) {
-        int rc;
-        if (m >= n) {  // G = X^T X = A A^T (n x n); X' = 1.5 X - 0.5 X G, i.e. A' = 1.5 A - 0.5 G A
-            rc = gemm(w, p.precision, false, true, n, n, m, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G, n, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, p.precision, false, false, n, m, n, -0.5f, w->G, n, cur, n, 1.5f, cur, nxt,
-                          n, s);
-        } else {       // G = X X^T = A^T A (m x m); A' = 1.5 A - 0.5 A G
-            rc = gemm(w, p.precision, true, false, m, m, n, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G, m, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, p.precision, false, false, n, m, m, -0.5f, cur, n, w->G, m, 1.5f, cur, nxt,
-                          n, s);
+    int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_elems / numel, w->cap_gram / gram));
+    per = std::max<int64_t>(per, 1);
+    for (int first = 0; first < count; first += static_cast<int>(per)) {
+        const int B = static_cast<int>(std::min<int64_t>(per, count - first));
+        // Delta of each matrix into its slot, its norm, and the normalised start.
+        for (int j = 0; j < B; ++j) {
+            const OrthoMatrix& t = mats[first + j];
+            DeltaArgs da;
+            for (int k = 0; k < CAM_KMAX; ++k) da.x[k] = k < p.K ? t.x[k] : nullptr;
+            da.K = p.K;
+            da.Kf = static_cast<float>(p.K);
+            da.theta = t.theta;
+            da.X = w->X + int64_t(j) * numel;
+            da.n = numel;
+            da.partials = w->partials + int64_t(j) * kOrthoBlocksMax;
+            if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<grid, kOrthoThreads, 0, s>>>(da);
+            else ortho_delta<float><<<grid, kOrthoThreads, 0, s>>>(da);
+            ortho_norm<<<1, 32, 0, s>>>(da.partials, grid, w->scalars + j, w->inv_norm + j);
+            ortho_scale<<<grid, kOrthoThreads, 0, s>>>(da.X, numel, w->inv_norm + j);
+            *launches += 3;
         }
-        if (rc != CAM_OK) return rc;
-        std::swap(cur, nxt);
+        cudaError_t ce = cudaGetLastError();
+        if (ce != cudaSuccess)
+            return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
+        // Newton-Schulz on all B matrices at once. Row-major X (m x n) is the
+        // column-major n x m matrix A = X^T (ld n).
+        float* cur = w->X;
+        float* nxt = w->Y;
+        for (int it = 0; it < p.iterations; ++it) {
+            int rc;
+            if (m >= n) {  // G = X^T X = A A^T (n x n); A' = 1.5 A - 0.5 G A
+                rc = gemm(w, p.precision, false, true, n, n, m, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G,
+                          n, B, numel, numel, gram, s);
+                if (rc == CAM_OK)
+                    rc = gemm(w, p.precision, false, false, n, m, n, -0.5f, w->G, n, cur, n, 1.5f, cur,
+                              nxt, n, B, gram, numel, numel, s);
+            } else {       // G = X X^T = A^T A (m x m); A' = 1.5 A - 0.5 A G
+                rc = gemm(w, p.precision, true, false, m, m, n, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G,
+                          m, B, numel, numel, gram, s);
+                if (rc == CAM_OK)
+                    rc = gemm(w, p.precision, false, false, n, m, m, -0.5f, cur, n, w->G, m, 1.5f, cur,
+                              nxt, n, B, numel, gram, numel, s);
+            }
+            if (rc != CAM_OK) return rc;
+            std::swap(cur, nxt);
+        }
+        for (int j = 0; j < B; ++j) {
+            const OrthoMatrix& t = mats[first + j];
+            ApplyArgs aa{t.theta, p.ema ? t.e : nullptr, cur + int64_t(j) * numel, numel,
+                         w->scalars + j, p.lr, p.scale_mode, r, p.beta};
+            ortho_apply<<<grid, kOrthoThreads, 0, s>>>(aa);
+            *launches += 1;
+        }
+        ce = cudaGetLastError();
+        if (ce != cudaSuccess)
+            return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
     }
-    ApplyArgs aa{t.theta, p.ema ? t.e : nullptr, cur, numel, w->scalars, p.lr, p.scale_mode, r, p.beta};
-    ortho_apply<<<grid, kOrthoThreads, 0, s>>>(aa);
-    *launches += 1;
-    ce = cudaGetLastError();
-    if (ce != cudaSuccess)
-        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
     return CAM_OK;
 }
 

@@ -116,7 +116,7 @@ struct cam_ctx {
     std::vector<int64_t> swa_count;  // globals folded into each tensor's running average
     std::vector<int64_t> rows;       // matrix rows of each tensor (0: not a matrix)
     cam::OrthoWork* ortho = nullptr; // made at the first orthogonalised commit
-    int64_t ortho_max_elems = 0, ortho_max_r = 0;
+    int64_t ortho_cap_elems = 0, ortho_cap_gram = 0;  // workspace sizing (floats)
     bool is_matrix(int32_t g) const {
         return rows[g] >= 2 && numel[g] % rows[g] == 0 && numel[g] / rows[g] >= 2;
     }
@@ -280,11 +280,20 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->swa_count.assign(d->n_tensors, 0);
     c->rows.assign(d->n_tensors, 0);
     if (d->rows) c->rows.assign(d->rows, d->rows + d->n_tensors);
-    for (int32_t t = 0; t < c->n_tensors; ++t)
-        if (c->is_matrix(t)) {
-            c->ortho_max_elems = std::max(c->ortho_max_elems, c->numel[t]);
-            c->ortho_max_r = std::max(c->ortho_max_r, std::min(c->rows[t], c->numel[t] / c->rows[t]));
-        }
+    {   // iterate buffers hold a batch of equal-shape matrices: at least the
+        // largest one, at most all of them, capped at 2 GiB (1 GiB for Gram)
+        int64_t big = 0, big_gram = 0, all = 0, all_gram = 0;
+        for (int32_t t = 0; t < c->n_tensors; ++t)
+            if (c->is_matrix(t)) {
+                const int64_t r = std::min(c->rows[t], c->numel[t] / c->rows[t]);
+                big = std::max(big, c->numel[t]);
+                big_gram = std::max(big_gram, r * r);
+                all += c->numel[t];
+                all_gram += r * r;
+            }
+        c->ortho_cap_elems = std::max(big, std::min(all, int64_t(1) << 29));
+        c->ortho_cap_gram = std::max(big_gram, std::min(all_gram, int64_t(1) << 28));
+    }
 
     // Plans and one device block holding every plan's tables.
     c->plans.resize(c->n_fragments + 1);
@@ -673,7 +682,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         return cuda_fail(scope.err, "cam_merge_commit: cudaSetDevice");
     }
     if (r->ortho && !c->ortho) {  // workspace of the orthogonalisation, made once per context
-        const int rc = cam::ortho_create(&c->ortho, c->ortho_max_elems, c->ortho_max_r);
+        const int rc = cam::ortho_create(&c->ortho, c->ortho_cap_elems, c->ortho_cap_gram);
         if (rc != CAM_OK) {
             close_round(r);
             return rc;
@@ -733,19 +742,32 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                 run = -1;
             }
         }
-        // ... and each matrix has its averaged update replaced by its polar factor
+        // ... and each matrix has its averaged update replaced by its polar
+        // factor, equal shapes batched together (first-appearance order)
         const cam::OrthoParams op{K, r->dtype, r->ortho_lr, r->ortho_scale, r->ortho_precision,
                                   r->ortho_iterations, r->ema, r->beta};
+        std::vector<char> done(T, 0);
+        std::vector<cam::OrthoMatrix> group;
         for (int l = 0; l < T && ce == cudaSuccess; ++l) {
-            const int32_t g = p.tensors[l];
-            if (!c->is_matrix(g)) continue;
-            cam::OrthoMatrix om;
-            om.theta = c->theta[g];
-            om.e = c->e[g];
-            om.rows = c->rows[g];
-            om.cols = c->numel[g] / c->rows[g];
-            for (int k = 0; k < CAM_KMAX; ++k) om.x[k] = k < K ? r->x[size_t(k) * T + l] : nullptr;
-            const int rc = cam::ortho_matrix(c->ortho, om, op, s, c->sm_count, &c->launches);
+            const int32_t g0 = p.tensors[l];
+            if (done[l] || !c->is_matrix(g0)) continue;
+            group.clear();
+            for (int q = l; q < T; ++q) {
+                const int32_t g = p.tensors[q];
+                if (done[q] || !c->is_matrix(g) || c->rows[g] != c->rows[g0] ||
+                    c->numel[g] != c->numel[g0])
+                    continue;
+                done[q] = 1;
+                cam::OrthoMatrix om;
+                om.theta = c->theta[g];
+                om.e = c->e[g];
+                om.rows = c->rows[g];
+                om.cols = c->numel[g] / c->rows[g];
+                for (int k = 0; k < CAM_KMAX; ++k) om.x[k] = k < K ? r->x[size_t(k) * T + q] : nullptr;
+                group.push_back(om);
+            }
+            const int rc = cam::ortho_group(c->ortho, group.data(), static_cast<int>(group.size()), op,
+                                            s, c->sm_count, &c->launches);
             if (rc != CAM_OK) {
                 close_round(r);
                 return rc;

@@ -854,3 +854,18 @@ def test_orthogonalisation_takes_only_plain_mean_with_ema():
         rd.commit()
     rd.abort()
     mg.close()
+
+
+def test_orthogonalisation_batches_equal_shapes_each_with_its_own_norm():
+    # interleaved shapes: the three 48x20 and two 20x48 matrices are each
+    # orthogonalised in one strided batch, every matrix with its own |Delta|
+    shapes = [(48, 20), (20, 48), (7, 0), (48, 20), (20, 48), (48, 20), (33, 3)]
+    for precision in (B.ORTHO_FP32, B.ORTHO_TF32):
+        for kind, t, r, c, th0, got, want, delta, e in _ortho_round(
+                shapes, "f32", precision, B.ORTHO_SCALE_MATCH_NORM, 0.5, seed=34):
+            if kind == "vector":
+                assert bitwise_equal(got, want.astype(np.float32))
+                continue
+            scale = np.abs(want - th0).max()
+            assert np.abs(got.astype(np.float64) - want).max() <= ORTHO_TOL[precision] * scale + 1e-9, \
+                (precision, t)
