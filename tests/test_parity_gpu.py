@@ -869,3 +869,39 @@ def test_orthogonalisation_batches_equal_shapes_each_with_its_own_norm():
             scale = np.abs(want - th0).max()
             assert np.abs(got.astype(np.float64) - want).max() <= ORTHO_TOL[precision] * scale + 1e-9, \
                 (precision, t)
+
+
+def test_orthogonalised_fragment_round_with_pinned_host_workers():
+    """Only the round's fragment changes; its workers stream from host memory."""
+    shapes = [(40, 24), (24, 40), (100, 0), (40, 24)]
+    frags = [0, 1, 1, 0]
+    sizes = [r * c if c else r for r, c in shapes]
+    rows = [r if c else 0 for r, c in shapes]
+    wl = _custom(sizes, K=3, mode="mean", dtype="bf16", frags=frags, n_fragments=2)
+    g = W.make_global(wl, 35, DEV)
+    th = W.empty_arena(g.numels, torch.float32, DEV)
+    th.flat.copy_(g.flat)
+    mg = B.Merger(th.views, fragment_of=frags, n_fragments=2, quorum=3, rows=rows)
+    workers = [W.make_worker(wl, g, 0, k, 35, DEV) for k in range(3)]
+    host = [_host_copy(w) for w in workers]
+    rd = mg.begin(0, 1)
+    for h in host:
+        rd.accumulate(h.views, 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.orthogonalize(0.02, B.ORTHO_SCALE_FIXED, B.ORTHO_FP32, 40)
+    rd.commit()
+    torch.cuda.synchronize()
+    for t, (r, c) in enumerate(shapes):
+        got, th0 = to_np(th.views[t]), to_np(g.views[t])
+        if frags[t] != 1:
+            assert bitwise_equal(got, th0), t           # other fragment untouched
+            continue
+        xs = [to_np(w.views[t]) for w in workers]
+        if c:
+            want, _ = oracle.orthogonal_update(xs, th0, r, lr=0.02)
+            assert np.abs(got - want).max() <= ORTHO_TOL[B.ORTHO_FP32] * np.abs(want - th0).max() + 1e-9
+        else:
+            want = th0.copy()
+            oracle.merge_tensor(xs, want, mode=oracle.MEAN_REPLACE)
+            assert bitwise_equal(got, want)
+    mg.close()
