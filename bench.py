@@ -184,14 +184,40 @@ def aggregate(per_rank_bytes: int, steps: int, elapsed_s: float, ws: int, device
 
 # ---- CPU oracle timing ---------------------------------------------------------------
 
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_split(fn, n: int, threads: int, pool) -> None:
+    """Calls fn(lo, hi) on `threads` contiguous element ranges of [0, n) at once.
+    The oracle is elementwise, so each range's results equal those of one call
+    over the whole span; its ctypes calls release the GIL, so the ranges run on
+    separate cores."""
+    if threads <= 1 or pool is None:
+        fn(0, n)
+        return
+    step = (n + threads - 1) // threads
+    futs = [pool.submit(fn, lo, min(n, lo + step)) for lo in range(0, n, step)]
+    for f in futs:
+        f.result()
+
+
 def oracle_sample_rate(wl, max_seconds: float, seed: int = 0, max_elems: int | None = None,
-                       pool_elems: int = 1 << 24):
+                       pool_elems: int = 1 << 24, threads: int = 1):
     """Times the CPU oracle over the workload's first round, tensor by tensor in
-    list order, until max_seconds of oracle time (or max_elems elements) are
+    list order, until max_seconds of wall time (or max_elems elements) are
     spent. Inputs follow the same recipe but are drawn once into a pool of
     pool_elems values per array and reused slice by slice (the oracle is
-    elementwise, so its time does not depend on which values it sees).
+    elementwise, so its time does not depend on which values it sees). With
+    threads > 1 every slice is split into that many element ranges, each run
+    by the unchanged oracle on its own host thread.
     Returns (GB/s, seconds, elements, description)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import numpy as np
     import torch
 
@@ -218,25 +244,54 @@ def oracle_sample_rate(wl, max_seconds: float, seed: int = 0, max_elems: int | N
     tokens = [draw.tokens[k] for k in draw.included] if wl.mode == "delta" else None
     beta = wl.ema_beta if wl.ema_beta is not None else 0.9
     b_per = round_bytes(wl, frag, k_incl) / max(1, wl.fragment_numel(frag))
+    def one(lo: int, hi: int) -> None:
+        oracle.merge_tensor([x[lo:hi] for x in xs], theta[lo:hi], mode=mode, tokens=tokens,
+                            lr=wl.lr, mu=wl.mu, m=None if m is None else m[lo:hi],
+                            e=None if e is None else e[lo:hi], beta=beta)
+
+    pool = ThreadPoolExecutor(max_workers=threads) if threads > 1 else None
     spent, elems, used = 0.0, 0, 0
-    for t in tensors:
-        n = wl.specs[t].numel
-        if max_elems is not None:
-            n = min(n, max_elems - elems)
-        for s0 in range(0, n, P):
-            c = min(P, n - s0)
-            t0 = time.perf_counter()
-            oracle.merge_tensor([x[:c] for x in xs], theta[:c], mode=mode, tokens=tokens,
-                                lr=wl.lr, mu=wl.mu, m=None if m is None else m[:c],
-                                e=None if e is None else e[:c], beta=beta)
-            spent += time.perf_counter() - t0
-            elems += c
-        used += 1
-        if spent >= max_seconds or (max_elems is not None and elems >= max_elems):
-            break
+    try:
+        for t in tensors:
+            n = wl.specs[t].numel
+            if max_elems is not None:
+                n = min(n, max_elems - elems)
+            for s0 in range(0, n, P):
+                c = min(P, n - s0)
+                t0 = time.perf_counter()
+                run_split(one, c, threads, pool)
+                spent += time.perf_counter() - t0
+                elems += c
+            used += 1
+            if spent >= max_seconds or (max_elems is not None and elems >= max_elems):
+                break
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    how = "single-threaded C oracle" if threads <= 1 else \
+        f"C oracle on {threads} host threads, each slice split into {threads} element ranges"
     desc = (f"first {used} of the round's {len(tensors)} tensors ({elems:,} of "
-            f"{wl.fragment_numel(frag):,} elements), same recipe, single-threaded C oracle")
+            f"{wl.fragment_numel(frag):,} elements), same recipe, {how}")
     return elems * b_per / spent / 1e9, spent, elems, desc
+
+
+def cpu_threads(args) -> int:
+    return args.cpu_threads if args.cpu_threads > 0 else host_threads()
+
+
+def cpu_baseline(wl, args) -> dict:
+    """The oracle on the host: once split over every core (the reported value)
+    and once on one thread, each for about args.cpu_seconds of wall time."""
+    nt = cpu_threads(args)
+    g1, s1, n1, d1 = oracle_sample_rate(wl, args.cpu_seconds)
+    out = {"value": round(g1, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": d1 + f"; {s1:.1f} s"}
+    if nt > 1:
+        gn, sn, nn, dn = oracle_sample_rate(wl, args.cpu_seconds, threads=nt)
+        out = {"value": round(gn, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
+               "sample": dn + f"; {sn:.1f} s",
+               "single_thread": {"value": round(g1, 4), "sample": d1 + f"; {s1:.1f} s"}}
+    return out
 
 
 # ---- the two arms ----------------------------------------------------------------------
@@ -245,10 +300,11 @@ def run_reference(args, wl, ws, rank) -> int:
     if rank != 0:
         return 0
     # each step times a bounded sample so that warmup + steps end within minutes
+    nt = cpu_threads(args)
     rates, secs = [], []
     for i in range(args.warmup + args.steps):
         gbs, s, n, desc = oracle_sample_rate(wl, max_seconds=args.ref_seconds_per_step,
-                                             pool_elems=1 << 22)
+                                             pool_elems=1 << 22, threads=nt)
         if i >= args.warmup:
             rates.append(gbs)
             secs.append(s)
@@ -263,7 +319,7 @@ def run_reference(args, wl, ws, rank) -> int:
         "config": {"workload": wl.name, "n_params": wl.n_params, "K": wl.K,
                    "sample_per_step": desc,
                    "ms_per_step_note": "extrapolated from the sample's rate to the full round"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -413,9 +469,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        gbs, secs, n, desc = oracle_sample_rate(wl, args.cpu_seconds)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f"; {secs:.1f} s of oracle time"}
+        cpu = cpu_baseline(wl, args)
 
     ck = clocks.summary()
     mg.close()
@@ -679,7 +733,9 @@ def parse(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy"), default="stream")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=8.0)
+    p.add_argument("--cpu-threads", type=int, default=0,
+                   help="host threads for the CPU oracle legs (0: every core this process may use)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-seconds-per-step", type=float, default=1.5)
     return p.parse_args(argv)
