@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params"
 KERNEL_SRCS = [os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", f)
                for f in ("merge_fused.cuh", "merge_fused_f32.cu", "merge_fused_bf16.cu",
+                         "merge_staged.cuh", "merge_staged_f32.cu", "merge_staged_bf16.cu",
                          "merge_device.cuh", "cam_internal.h")]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
@@ -80,10 +81,10 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str):
+def stored_traffic(workload: str, kernel: str = "merge_staged"):
     """dram bytes per launch from the committed ncu summary of this workload's
     merge kernel, or None if absent or taken on a different kernel source."""
-    path = os.path.join(PROFILES, f"merge_fused_{workload}.md")
+    path = os.path.join(PROFILES, f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -366,7 +367,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
     mg = B.Merger(theta.views, momentum=None if m is None else m.views,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum,
-                  swa=None if swa is None else swa.views)
+                  swa=None if swa is None else swa.views, staging=not args.no_staging)
     n_streams = max(1, wl.in_flight)
     streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
     norm_out = [(torch.zeros(len(mg.fragment_tensors(f)) or 1, dtype=torch.float64, device=dev),
@@ -421,7 +422,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize(dev)
-    launches0 = mg.launch_count
+    launches0, staged0 = mg.launch_count, mg.staged_count
     barrier(ws)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
@@ -435,6 +436,9 @@ def run_ours(args, wl, ws, rank, local) -> int:
     elapsed = t0.elapsed_time(t1) / 1e3
     barrier(ws)
     launches = mg.launch_count - launches0
+    # which form of the merge pass the library chose for these rounds
+    staged_launches = mg.staged_count - staged0
+    kernel = "merge_staged" if staged_launches > 0 else "merge_fused"
     k_incl = [len(d.included) for d in draws]
     step_bytes = sum(round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl))
     agg = aggregate(step_bytes, args.steps, elapsed, ws, dev)
@@ -447,19 +451,19 @@ def run_ours(args, wl, ws, rank, local) -> int:
     if n_streams > 1:
         kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for a, b in group_pairs)
         launch_bytes = step_bytes
-        kernel_desc = f"merge_fused x{len(wl.rounds)} concurrent on {n_streams} streams"
+        kernel_desc = f"{kernel} x{len(wl.rounds)} concurrent on {n_streams} streams"
     else:
         kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
                                  if i % len(wl.rounds) == big)
         launch_bytes = per_round[big]
-        kernel_desc = "merge_fused"
+        kernel_desc = kernel
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured"
     if not peak:
         peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     achieved = launch_bytes / kern_s / 1e9
-    traffic = stored_traffic(wl.name)
+    traffic = stored_traffic(wl.name, kernel)
 
     # end to end through the public API: worker inputs start in pinned host
     # memory and are copied in every step; the new global and EMA are read back.
@@ -737,6 +741,8 @@ def parse(argv=None):
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="host threads for the CPU oracle legs (0: every core this process may use)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-staging", action="store_true",
+                   help="merge passes in the register form instead of the staged (bulk-copy) form")
     p.add_argument("--ref-seconds-per-step", type=float, default=1.5)
     return p.parse_args(argv)
 

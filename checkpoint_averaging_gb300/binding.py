@@ -22,6 +22,8 @@ MAX_OPEN_ROUNDS = 8
 F32, BF16 = 0, 1
 MEAN_REPLACE, DELTA_NESTEROV = 0, 1
 INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
+NO_STAGING = 8
+STATUS_WAIT_TIMEOUT = 1
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
 ORTHO_TF32, ORTHO_FP32 = 0, 1
 
@@ -94,7 +96,8 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
-           "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_merge_round_noalloc",
+           "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
+           "cam_ctx_staged_count", "cam_merge_round_noalloc",
            "cam_last_error", "cam_version")
 
 NOALLOC_MAX_TENSORS = 4096
@@ -137,6 +140,8 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_get_last_round.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_ctx_set_last_round.argtypes = [vp, i64]
     L.cam_ctx_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_ctx_status.argtypes = [vp, ctypes.POINTER(i32)]
+    L.cam_ctx_staged_count.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_merge_round_noalloc.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, i32, vpp,
                                           ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, i32, ctypes.c_float,
@@ -297,6 +302,18 @@ def ctx_launch_count(ctx: int) -> int:
     return out.value
 
 
+def ctx_staged_count(ctx: int) -> int:
+    out = ctypes.c_int64()
+    _check(lib().cam_ctx_staged_count(ctx, ctypes.byref(out)))
+    return out.value
+
+
+def ctx_status(ctx: int) -> int:
+    out = ctypes.c_int32()
+    _check(lib().cam_ctx_status(ctx, ctypes.byref(out)))
+    return out.value
+
+
 def merge_round_noalloc(numel: Sequence[int], master: Sequence[int], ckpt: Sequence[Sequence[int]],
                         dtype: int, mode: int, *, tokens: Sequence[int] | None = None,
                         lr: float = 1.0, mu: float = 0.0, momentum: Sequence[int] | None = None,
@@ -398,9 +415,12 @@ class Merger:
 
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
-                 zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None):
+                 zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
+                 staging=True):
         """rows: optional per-tensor matrix rows (default: the tensors' first
-        dimension), used by orthogonalised rounds."""
+        dimension), used by orthogonalised rounds. staging=False keeps every
+        merge pass on the register form (the staged form gives the same
+        results)."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -425,7 +445,8 @@ class Merger:
         self.fragment_of = list(fragment_of) if fragment_of is not None else [0] * len(self.master)
         self.n_fragments = n_fragments
         flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
-                (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0)
+                (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
+                (0 if staging else NO_STAGING)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,
@@ -481,6 +502,16 @@ class Merger:
     @property
     def launch_count(self) -> int:
         return ctx_launch_count(self.ctx)
+
+    @property
+    def staged_count(self) -> int:
+        """Merge passes launched in the staged (bulk-copy) form so far."""
+        return ctx_staged_count(self.ctx)
+
+    def status(self) -> int:
+        """Waits for the device, then returns its status word (0: no merge
+        pass gave up waiting on a barrier)."""
+        return ctx_status(self.ctx)
 
     @property
     def last_round(self) -> int:

@@ -21,6 +21,22 @@ constexpr int kMaxChunkElems = 8 * kChunkQuantum;
 // may take up to 32,764 bytes; this keeps MergeArgs under that.
 constexpr int kXCap = 3520;
 
+// The staged form of the fused pass (merge_staged.cuh): one block per SM of
+// 16 consumer warps, one producer warp that streams tiles of kStTile elements
+// of every input array into a ring of shared-memory stages with bulk copies,
+// and one warp that reduces the drift partials.
+constexpr int kStConsumerWarps = 16;
+constexpr int kStConsumers = kStConsumerWarps * 32;
+constexpr int kStThreads = kStConsumers + 64;
+constexpr int kStTile = kStConsumers * 4;      // 2048 elements: 4 per consumer
+constexpr int kStMaxStages = 16;
+constexpr int kStRedSlots = 2;                 // drift hand-over buffers (double buffering)
+constexpr int kStSmemBytes = 224 * 1024;       // dynamic shared memory: ring + hand-over
+static_assert(kChunkQuantum % kStTile == 0, "tiles must not straddle chunks");
+
+// Bits of the context's device status word (cam_ctx_status).
+constexpr int32_t kStatusWaitTimeout = 1;  // a staged pass gave up waiting on a barrier
+
 // One chunk of the fragment's element space: elements [start, start+len) of
 // the fragment's local tensor `local`. Chunks never straddle tensors.
 struct ChunkDesc {
@@ -56,6 +72,9 @@ struct MergeArgs {
     float W;                  // (float)sum tokens
     float lr, mu, beta;
     float swa_n;              // globals in the running average after this round
+    int32_t* status;          // device status word (kStatus* bits), staged pass only
+    int32_t st_stages;        // staged pass: stages in the shared-memory ring
+    int32_t st_stage_bytes;   // staged pass: bytes of one stage
     uint32_t vec[(kXCap + 31) / 32];  // bit l: tensor local0+l takes the vector path
     // x[l*stride + k]: worker k's copy of tensor local0+l; when publishing,
     // x[l*stride + K] and x[l*stride + K + 1] take the new theta and EMA. The
@@ -124,6 +143,19 @@ using MergeFn = void (*)(MergeArgs);
 MergeFn pick_merge_f32(const MergeVariant& v);
 MergeFn pick_merge_bf16(const MergeVariant& v);
 cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cudaStream_t s);
+// The staged pass: one block of kStThreads per SM, a ring of st_stages stages.
+MergeFn pick_staged_f32(const MergeVariant& v);
+MergeFn pick_staged_bf16(const MergeVariant& v);
+// State arrays a variant streams besides the workers (theta, m, e, swa).
+int staged_state_arrays(const MergeVariant& v);
+// Bytes of one stage for K workers of that variant.
+int64_t staged_stage_bytes(const MergeVariant& v, int K);
+// Bytes of the drift hand-over buffers after the ring (0 without norms).
+int64_t staged_red_bytes(const MergeVariant& v, int K);
+// Lets every staged variant use kStSmemBytes of dynamic shared memory.
+cudaError_t staged_prepare();
+cudaError_t launch_merge_staged(const MergeArgs& a, const MergeVariant& v, int grid,
+                                cudaStream_t s);
 // Resident blocks per SM of that variant (0 on error).
 int merge_blocks_per_sm(const MergeVariant& v);
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s);

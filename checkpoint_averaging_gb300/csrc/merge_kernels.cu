@@ -105,6 +105,58 @@ cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cu
                             args, 0, s);
 }
 
+int staged_state_arrays(const MergeVariant& v) {
+    const bool delta = v.mode == CAM_MODE_DELTA_NESTEROV;
+    return int(delta || v.norm_level >= 1) + int(delta) + int(v.ema) + int(v.swa);
+}
+
+int64_t staged_stage_bytes(const MergeVariant& v, int K) {
+    const int64_t xb = v.dtype == kDtBF16 ? 2 : 4;
+    return int64_t(kStTile) * (K * xb + 4 * staged_state_arrays(v));
+}
+
+int64_t staged_red_bytes(const MergeVariant& v, int K) {
+    if (v.norm_level < 1) return 0;
+    const int quantities = 1 + (v.norm_level >= 2 ? K : 0);
+    return int64_t(kStRedSlots) * quantities * kStConsumers * 4;
+}
+
+namespace {
+
+MergeFn pick_staged(const MergeVariant& v) {
+    return v.dtype == kDtBF16 ? pick_staged_bf16(v) : pick_staged_f32(v);
+}
+
+}  // namespace
+
+cudaError_t staged_prepare() {
+    for (int dt = 0; dt < 2; ++dt)
+        for (int md = 0; md < 2; ++md)
+            for (int em = 0; em < 2; ++em)
+                for (int nl = 0; nl < 3; ++nl)
+                    for (int pb = 0; pb < 2; ++pb)
+                        for (int sw = 0; sw < 2; ++sw) {
+                            const MergeVariant v{dt, md, em != 0, nl, pb != 0, sw != 0};
+                            const cudaError_t ce = cudaFuncSetAttribute(
+                                reinterpret_cast<const void*>(pick_staged(v)),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmemBytes);
+                            if (ce != cudaSuccess) return ce;
+                        }
+    return cudaSuccess;
+}
+
+cudaError_t launch_merge_staged(const MergeArgs& a, const MergeVariant& v, int grid,
+                                cudaStream_t s) {
+    const size_t smem = size_t(a.st_stages) * size_t(a.st_stage_bytes) +
+                        size_t(staged_red_bytes(v, a.K));
+    if (a.st_stages < 2 || a.st_stages > kStMaxStages || smem > size_t(kStSmemBytes) ||
+        a.st_stage_bytes != staged_stage_bytes(v, a.K) || a.status == nullptr)
+        return cudaErrorInvalidValue;
+    void* args[] = {const_cast<MergeArgs*>(&a)};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(pick_staged(v)), dim3(grid),
+                            dim3(kStThreads), args, smem, s);
+}
+
 int merge_blocks_per_sm(const MergeVariant& v) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(

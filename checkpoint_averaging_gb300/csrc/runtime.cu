@@ -121,10 +121,13 @@ struct cam_ctx {
         return rows[g] >= 2 && numel[g] % rows[g] == 0 && numel[g] / rows[g] >= 2;
     }
     bool pageable_access = false;  // the GPU reads pageable host memory directly
+    bool staged = true;            // the staged form of the merge pass may be used
+    int32_t* d_status = nullptr;   // device status word (CAM_STATUS_* bits), in dev_block
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
     int64_t last_round = -1;
     int64_t launches = 0;
+    int64_t staged_launches = 0;  // merge passes in the staged form
     std::vector<cam_round*> open;
     // resident blocks per SM: [dtype][mode][ema][norm level][publish][swa]
     int bps[2][2][2][3][2][2] = {};
@@ -143,6 +146,7 @@ struct cam_round {
     int K = 0;
     int dtype = -1;
     std::vector<const void*> x;  // x[k * T_f + l]
+    bool host_workers = false;   // some worker came through cam_merge_accumulate_host
     int64_t tokens[CAM_KMAX] = {};
     bool finalized = false;
     int mode = CAM_MODE_MEAN_REPLACE;
@@ -203,7 +207,8 @@ int validate_desc(const cam_ctx_desc* d) {
     if (d->quorum < 1 || d->quorum > CAM_KMAX)
         return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
-    if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA))
+    if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
+                     CAM_NO_STAGING))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -295,9 +300,10 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         c->ortho_cap_gram = std::max(big_gram, std::min(all_gram, int64_t(1) << 28));
     }
 
-    // Plans and one device block holding every plan's tables.
+    // Plans and one device block holding every plan's tables, after the
+    // status word.
     c->plans.resize(c->n_fragments + 1);
-    size_t bytes = 0;
+    size_t bytes = 256;
     for (int32_t f = 0; f <= c->n_fragments; ++f) {
         Plan& p = c->plans[f];
         build_plan(p, *c, f < c->n_fragments ? f : -1);
@@ -315,7 +321,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         return fail(CAM_E_NOMEM, "cam_ctx_create: cudaMalloc(%zu): %s", bytes, cudaGetErrorString(ce));
     }
     std::vector<unsigned char> host(std::max<size_t>(bytes, 256), 0);
-    size_t off = 0;
+    c->d_status = static_cast<int32_t*>(c->dev_block);
+    size_t off = 256;
     auto carve = [&](size_t n) {
         const size_t o = off;
         off += round_up(n, 256);
@@ -358,6 +365,15 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
                             c->bps[dt][md][em][nl][pb][sw] = std::max(
                                 1, cam::merge_blocks_per_sm(cam::MergeVariant{
                                        dt, md, em != 0, nl, pb != 0, sw != 0}));
+
+    c->staged = !(d->flags & CAM_NO_STAGING);
+    if (c->staged) {
+        ce = cam::staged_prepare();
+        if (ce != cudaSuccess) {
+            cudaFree(c->dev_block);
+            return cuda_fail(ce, "cam_ctx_create: staged pass set-up");
+        }
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(d->stream);
     for (int32_t t = 0; t < c->n_tensors && ce == cudaSuccess; ++t) {
@@ -485,6 +501,7 @@ int accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t t
     }
     r->tokens[r->K] = tokens;
     r->dtype = dtype;
+    r->host_workers = r->host_workers || host;
     ++r->K;
     return CAM_OK;
 }
@@ -690,12 +707,27 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     }
     cudaError_t ce = cudaSuccess;
     const int per_launch = cam::kXCap / stride;
+    // The staged form: a ring of as many stages as fit (at least 2, at most
+    // kStMaxStages), for launches whose workers are device memory.
+    const int64_t st_bytes = cam::staged_stage_bytes(variant, K);
+    const int st_stages = static_cast<int>(std::min<int64_t>(
+        cam::kStMaxStages, (cam::kStSmemBytes - cam::staged_red_bytes(variant, K)) / st_bytes));
+    // Measured on GB300 (1.08B lists, 4B sweep): the staged form is ahead
+    // when a round writes at most two state arrays (theta plus m or e) and
+    // behind when it writes three (theta, m, e or theta, e, swa), where the
+    // register form is kept.
+    const int state_writes = 1 + int(delta) + int(r->ema) + int(r->swa);
+    const bool staged_ok = c->staged && !r->host_workers && st_stages >= 2 && state_writes <= 2;
+    a.status = c->d_status;
+    a.st_stages = st_stages;
+    a.st_stage_bytes = static_cast<int32_t>(st_bytes);
     // Fused pass over the fragment's local tensors [lb, le).
     auto launch_range = [&](int lb, int le) {
         for (int l0 = lb; l0 < le && ce == cudaSuccess; l0 += per_launch) {
             const int n = std::min(per_launch, le - l0);
             const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
             if (c1 == c0) continue;
+            bool all_vec = true;
             std::memset(a.vec, 0, sizeof a.vec);
             for (int l = 0; l < n; ++l) {
                 const int32_t g = p.tensors[l0 + l];
@@ -714,6 +746,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                     v = v && aligned(pt, 32) && aligned(pe, 32);
                 }
                 if (v) a.vec[l >> 5] |= 1u << (l & 31);
+                all_vec = all_vec && v;
             }
             a.chunks = p.d_chunks + c0;
             a.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
@@ -722,9 +755,15 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             a.n_chunks = c1 - c0;
             a.local0 = l0;
             a.n_local = n;
-            const int grid =
-                static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
-            ce = cam::launch_merge(a, variant, grid, s);
+            if (staged_ok && all_vec) {  // one block per SM
+                const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, c->sm_count));
+                ce = cam::launch_merge_staged(a, variant, grid, s);
+                ++c->staged_launches;
+            } else {
+                const int grid =
+                    static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * bps));
+                ce = cam::launch_merge(a, variant, grid, s);
+            }
             ++c->launches;
         }
     };
@@ -842,6 +881,24 @@ CAM_API int cam_fragment_info(const cam_ctx* c, int32_t fragment, int32_t* n_ten
 CAM_API int cam_ctx_launch_count(const cam_ctx* c, int64_t* out) {
     if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_launch_count: NULL argument");
     *out = c->launches;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_status(cam_ctx* c, int32_t* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_status: NULL argument");
+    DeviceScope scope(c->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_ctx_status: cudaSetDevice");
+    cudaError_t ce = cudaDeviceSynchronize();
+    int32_t v = 0;
+    if (ce == cudaSuccess) ce = cudaMemcpy(&v, c->d_status, sizeof v, cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_status");
+    *out = v;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_staged_count(const cam_ctx* c, int64_t* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_staged_count: NULL argument");
+    *out = c->staged_launches;
     return CAM_OK;
 }
 

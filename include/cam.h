@@ -78,6 +78,10 @@ typedef enum {
 #define CAM_INIT_EMA_FROM_MASTER 1u /* at create: e <- theta (EMA starts at the first global) */
 #define CAM_INIT_ZERO_MOMENTUM 2u   /* at create: m <- 0 */
 #define CAM_INIT_ZERO_SWA 4u        /* at create: running averages <- 0, no globals folded */
+#define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
+
+/* Bits of the device status word (cam_ctx_status) */
+#define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
 
 /* cam_merge_orthogonalize */
 #define CAM_ORTHO_SCALE_FIXED 0      /* theta' = theta + lr * polar(Delta) */
@@ -288,6 +292,40 @@ int cam_ctx_set_last_round(cam_ctx* ctx, int64_t round);
 /* Kernels this context has launched so far (merge passes, norm passes and
  * the CAM_INIT_* work), for accounting what a timed region ran. */
 int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
+
+/*
+ * The merge pass has two forms with the same results, element for element.
+ *
+ * - The register form loads each thread's elements into registers.
+ * - The staged form streams tiles of every input array into a ring of
+ *   shared-memory stages with the TMA engine's bulk copies. It keeps more
+ *   bytes in flight per SM.
+ *
+ * A commit uses the staged form for every launch that meets all of these:
+ *
+ * - its workers came through cam_merge_accumulate;
+ * - its buffers are all vector-aligned;
+ * - the round writes at most two state arrays: theta plus m or e.
+ *
+ * Rounds that write three state arrays (Nesterov with an EMA update, or an
+ * EMA update with a running-average update) measure faster in the register
+ * form, so they keep it. Rounds with workers from cam_merge_accumulate_host
+ * always use the register form, and so does a context created with
+ * CAM_NO_STAGING.
+ *
+ * Every wait of the staged form on one of its barriers gives up after a few
+ * seconds. It then sets CAM_STATUS_WAIT_TIMEOUT in the context's device status
+ * word, and the results of that commit are undefined.
+ *
+ * cam_ctx_status waits for all work on the context's device, then writes the
+ * word (0: nothing went wrong) to *out. The word stays set once set.
+ * Errors: CAM_E_ARG, CAM_E_CUDA.
+ */
+int cam_ctx_status(cam_ctx* ctx, int32_t* out);
+
+/* Merge passes this context has launched in the staged form (a subset of
+ * cam_ctx_launch_count), so a caller can tell which form a round took. */
+int cam_ctx_staged_count(const cam_ctx* ctx, int64_t* out);
 
 /*
  * cam_merge_round_noalloc -- a whole round (accumulate, finalize, optional

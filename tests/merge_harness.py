@@ -65,7 +65,7 @@ class GpuState:
     swa: W.Arena | None = None
 
 
-def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None) -> GpuState:
+def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True) -> GpuState:
     theta = W.empty_arena(g.numels, torch.float32, dev)
     theta.flat.copy_(g.flat)
     m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
@@ -77,7 +77,7 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None) -> GpuState:
     mg = B.Merger(theta.views, momentum=None if m is None else m.views,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
-                  swa=None if swa is None else swa.views)
+                  swa=None if swa is None else swa.views, staging=staging)
     return GpuState(theta, m, e, mg, swa)
 
 
@@ -174,6 +174,7 @@ def run_full(wl: W.Workload, seed: int = 0, dev="cuda", bitwise=False):
         if gn is not None:
             compare_norms(gn, on, f"{wl.name} round {rnd}")
         del workers
+    assert st.merger.status() == 0, "a merge pass gave up waiting on a barrier"
     st.merger.close()
     return st, ost
 

@@ -9,6 +9,7 @@ views, K = 1 and K = KMAX, many tensors per round, the round state machine.
 Tolerance per fp32 element: |gpu - oracle| <= 1e-7 + 2e-6 |oracle|; drift
 norms within 1e-5 relative.
 """
+import dataclasses
 import gc
 import math
 
@@ -905,3 +906,138 @@ def test_orthogonalised_fragment_round_with_pinned_host_workers():
             oracle.merge_tensor(xs, want, mode=oracle.MEAN_REPLACE)
             assert bitwise_equal(got, want)
     mg.close()
+
+
+# ---- the staged and register forms of the merge pass ------------------------------
+
+STAGED_SIZES = [1, 7, 8, 9, 2047, 2048, 2049, 6000, 16385, 100_003, 0, 3, 1 << 20, 4100]
+
+
+def _ab_round(st, wl, rnd, workers, draw, *, worker_norms, publish):
+    rd = st.merger.begin(rnd, -1)
+    for k in draw.included:
+        rd.accumulate(workers[k].views, draw.tokens[k])
+    rd.finalize(B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE, wl.lr, wl.mu)
+    if wl.ema_beta is not None:
+        rd.ema_update(wl.ema_beta)
+    if wl.swa:
+        rd.swa_update()
+    T = len(rd.tensors)
+    out = {}
+    if wl.norms:
+        out["pt"] = torch.full((T,), -1.0, dtype=torch.float64, device=DEV)
+        out["pf"] = torch.full((1,), -1.0, dtype=torch.float64, device=DEV)
+        rd.drift_norm(out["pt"], out["pf"])
+    if worker_norms:
+        out["pwt"] = torch.full((len(draw.included) * T,), -1.0, dtype=torch.float64, device=DEV)
+        out["pw"] = torch.full((len(draw.included),), -1.0, dtype=torch.float64, device=DEV)
+        rd.worker_drift_norm(out["pwt"], out["pw"])
+    if publish:
+        out["th_pub"] = [torch.full_like(v, float("nan")) for v in st.theta.views]
+        out["e_pub"] = ([torch.full_like(v, float("nan")) for v in st.e.views]
+                        if st.e is not None else None)
+        rd.publish(out["th_pub"], out["e_pub"])
+    rd.commit()
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode,ema,norms,swa,K,worker_norms,publish", [
+    ("mean", True, False, False, 5, False, False),   # the 1.08B round's variant
+    ("mean", False, True, False, 1, False, False),
+    ("delta", False, True, False, 3, False, False),  # the bf16 in-flight rounds' variant
+    ("delta", False, True, False, 8, True, True),    # K = CAM_KMAX, worker norms, publish
+    ("mean", False, False, True, 2, False, True),    # running average, publish
+    ("mean", True, True, False, 3, True, True),
+    # three state arrays written: both sides take the register form
+    ("delta", True, True, True, 8, True, False),
+    ("mean", True, False, True, 2, False, True),
+])
+def test_staged_and_register_forms_agree_bitwise(dtype, mode, ema, norms, swa, K,
+                                                 worker_norms, publish):
+    """Same seeded rounds through both forms of the pass: theta, m, e, the running
+    average and the published copies agree bit for bit; drift norms (whose fp32
+    per-thread grouping differs between the forms) agree within the norm
+    tolerance; the oracle checks the staged form's values."""
+    wl = dataclasses.replace(_custom(STAGED_SIZES, K=K, mode=mode, dtype=dtype, ema=ema,
+                                     norms=norms, rounds=((0, -1), (1, -1))), swa=swa)
+    g = W.make_global(wl, 3, DEV)
+    states = [make_gpu_state(wl, g, DEV, staging=sg) for sg in (True, False)]
+    ost = oracle_state_from(g, wl)
+    for idx, (rnd, frag) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, 3)
+        workers = [W.make_worker(wl, g, rnd, k, 3, DEV) for k in range(wl.K)]
+        outs = [_ab_round(st, wl, rnd, workers, draw, worker_norms=worker_norms, publish=publish)
+                for st in states]
+        oracle_round(ost, wl, rnd, frag, workers, draw)
+        torch.cuda.synchronize()
+        a, b = states
+        for name in ("theta", "m", "e", "swa"):
+            x, y = getattr(a, name), getattr(b, name)
+            if x is not None:
+                assert torch.equal(x.flat.view(torch.int32), y.flat.view(torch.int32)), \
+                    f"round {rnd}: {name} differs between the staged and register forms"
+        compare_full(a, ost, f"staged round {rnd}")
+        if publish:
+            for t, v in enumerate(a.theta.views):
+                assert torch.equal(outs[0]["th_pub"][t].view(torch.int32), v.view(torch.int32))
+                if a.e is not None:
+                    assert torch.equal(outs[0]["e_pub"][t].view(torch.int32),
+                                       a.e.views[t].view(torch.int32))
+        for key in ("pt", "pf", "pwt", "pw"):
+            if key in outs[0]:
+                x, y = outs[0][key].cpu().numpy(), outs[1][key].cpu().numpy()
+                assert (x >= 0).all(), f"{key}: norm not written"
+                assert np.all(np.abs(x - y) <= NORM_RTOL * np.abs(y) + 1e-300), f"{key}: {x} vs {y}"
+    for st in states:
+        assert st.merger.status() == 0
+        st.merger.close()
+
+
+def test_staged_form_is_used_and_reproducible():
+    """Two identical staged runs agree bit for bit, norms included, and a round
+    of device workers launches exactly one merge pass plus the norm finish."""
+    wl = _custom([1 << 20, 3, 2049, 5_000_000], K=4, mode="delta", dtype="bf16", ema=True)
+    g = W.make_global(wl, 0, DEV)
+    res = []
+    for _ in range(2):
+        st = make_gpu_state(wl, g, DEV)
+        draw = W.draw_round(wl, 0, 0)
+        workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
+        n0 = st.merger.launch_count
+        pt, pf = gpu_round(st, wl, 0, -1, workers, draw)
+        assert st.merger.launch_count - n0 == 2
+        torch.cuda.synchronize()
+        res.append((st.theta.flat.clone(), st.m.flat.clone(), st.e.flat.clone(), pt.clone(), pf.clone()))
+        assert st.merger.status() == 0
+        st.merger.close()
+    for x, y in zip(*res):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("mode,ema,swa,host,staging,want_staged", [
+    ("mean", True, False, False, True, True),     # theta, e written
+    ("delta", False, False, False, True, True),   # theta, m written
+    ("delta", True, False, False, True, False),   # theta, m, e: register form
+    ("mean", True, True, False, True, False),     # theta, e, swa: register form
+    ("mean", True, False, True, True, False),     # host-resident workers
+    ("mean", True, False, False, False, False),   # CAM_NO_STAGING
+])
+def test_form_of_the_merge_pass(mode, ema, swa, host, staging, want_staged):
+    wl = dataclasses.replace(_custom([70_000, 2049], K=2, mode=mode, ema=ema, norms=False),
+                             swa=swa)
+    g = W.make_global(wl, 0, DEV)
+    st = make_gpu_state(wl, g, DEV, staging=staging)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
+    if host:
+        workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
+    n0 = st.merger.staged_count
+    gpu_round(st, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    assert (st.merger.staged_count - n0 > 0) == want_staged
+    ost = oracle_state_from(g, wl)
+    oracle_round(ost, wl, 0, -1, workers, draw)
+    compare_full(st, ost, f"form test {mode} ema={ema} swa={swa} host={host}")
+    assert st.merger.status() == 0
+    st.merger.close()
