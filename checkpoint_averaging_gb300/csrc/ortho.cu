@@ -130,33 +130,70 @@ namespace {
 
 constexpr int kOrthoThreads = 256;
 
+// Per-group launches: blockIdx.y picks the matrix (slot j of the batch), and
+// every matrix keeps the block count its size alone determines, so its
+// partials do not depend on the rest of the batch.
 struct DeltaArgs {
-    const void* x[CAM_KMAX];
+    const void* x[kOrthoBatchMax][CAM_KMAX];  // [j][k]: worker k's copy of matrix j
+    const float* theta[kOrthoBatchMax];
+    uint32_t vec[kOrthoBatchMax / 32];        // bit j: matrix j's buffers take 32-byte vectors
     int32_t K;
     float Kf;
-    const float* theta;
-    float* X;
-    int64_t n;
-    double* partials;  // one per block
+    float* X;          // slot j at X + j * n
+    int64_t n;         // elements per matrix
+    double* partials;  // [j * kOrthoBlocksMax + block]
 };
 
 // Delta = (sum_k x_k, arrival order) / K - theta, the plain-mean arithmetic of
 // the fused pass, and each block's sum of Delta^2 (fp32 over at most 32
 // elements per thread, then fp64, reduced in a fixed order).
 template <typename XT>
-__global__ void __launch_bounds__(kOrthoThreads) ortho_delta(const DeltaArgs a) {
+__global__ void __launch_bounds__(kOrthoThreads) ortho_delta(const __grid_constant__ DeltaArgs a) {
     __shared__ double part[kOrthoThreads / 32];
+    const int j = blockIdx.y;
+    const void* const* xs = a.x[j];
+    const float* theta = a.theta[j];
+    float* X = a.X + int64_t(j) * a.n;
     double dacc = 0.0;
     float acc = 0.0f;
     int cnt = 0;
+    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < a.n; i += stride) {
+    int64_t done = 0;
+    if ((a.vec[j >> 5] >> (j & 31)) & 1u) {  // 8 elements per step
+        const int64_t nv = a.n >> 3;
+        for (int64_t v = tid; v < nv; v += stride) {
+            dev::XVec<XT> x[CAM_KMAX];
+#pragma unroll
+            for (int k = 0; k < CAM_KMAX; ++k)
+                if (k < a.K) x[k].load(static_cast<const XT*>(xs[k]) + 8 * v);
+            float d[8];
+            dev::load_s8(theta + 8 * v, d);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float s = 0.0f;
+#pragma unroll
+                for (int k = 0; k < CAM_KMAX; ++k)
+                    if (k < a.K) s = __fadd_rn(s, x[k].get(e));
+                d[e] = __fsub_rn(__fdiv_rn(s, a.Kf), d[e]);
+                acc = __fmaf_rn(d[e], d[e], acc);
+            }
+            dev::store_s8(X + 8 * v, d);
+            if ((cnt += 8) == 32) {
+                dacc += static_cast<double>(acc);
+                acc = 0.0f;
+                cnt = 0;
+            }
+        }
+        done = 8 * nv;
+    }
+    for (int64_t i = done + tid; i < a.n; i += stride) {
         float s = 0.0f;
 #pragma unroll
         for (int k = 0; k < CAM_KMAX; ++k)
-            if (k < a.K) s = __fadd_rn(s, dev::load_x1(static_cast<const XT*>(a.x[k]) + i));
-        const float d = __fsub_rn(__fdiv_rn(s, a.Kf), a.theta[i]);
-        a.X[i] = d;
+            if (k < a.K) s = __fadd_rn(s, dev::load_x1(static_cast<const XT*>(xs[k]) + i));
+        const float d = __fsub_rn(__fdiv_rn(s, a.Kf), theta[i]);
+        X[i] = d;
         acc = __fmaf_rn(d, d, acc);
         if (++cnt == 32) {
             dacc += static_cast<double>(acc);
@@ -170,53 +207,96 @@ __global__ void __launch_bounds__(kOrthoThreads) ortho_delta(const DeltaArgs a) 
     if (threadIdx.x == 0) {
         double s = 0.0;
         for (int w = 0; w < kOrthoThreads / 32; ++w) s += part[w];
-        a.partials[blockIdx.x] = s;
+        a.partials[int64_t(j) * kOrthoBlocksMax + blockIdx.x] = s;
     }
 }
 
-// |Delta|_F^2 in a fixed order, and 1/|Delta|_F (0 for a zero update, which
-// then stays zero through the iteration and leaves theta unchanged).
+// |Delta_j|_F^2 in a fixed order, and 1/|Delta_j|_F (0 for a zero update,
+// which then stays zero through the iteration and leaves theta unchanged).
+// One 32-thread block per matrix.
 __global__ void ortho_norm(const double* partials, int nb, double* scalars, float* inv_norm) {
+    const int j = blockIdx.x;
     double s = 0.0;
-    for (int b = threadIdx.x; b < nb; b += 32) s += partials[b];
+    for (int b = threadIdx.x; b < nb; b += 32) s += partials[int64_t(j) * kOrthoBlocksMax + b];
     s = dev::warp_sum(s);
     if (threadIdx.x == 0) {
-        scalars[0] = s;
-        inv_norm[0] = s > 0.0 ? static_cast<float>(1.0 / sqrt(s)) : 0.0f;
+        scalars[j] = s;
+        inv_norm[j] = s > 0.0 ? static_cast<float>(1.0 / sqrt(s)) : 0.0f;
     }
 }
 
+// X_j <- X_j / |Delta_j|_F. Slot j is 32-byte aligned when n is a multiple of 8.
 __global__ void ortho_scale(float* X, int64_t n, const float* inv_norm) {
-    const float f = *inv_norm;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
-         i += int64_t(gridDim.x) * blockDim.x)
-        X[i] = __fmul_rn(X[i], f);
+    const int j = blockIdx.y;
+    const float f = inv_norm[j];
+    float* Xj = X + int64_t(j) * n;
+    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t done = 0;
+    if ((n & 7) == 0) {
+        for (int64_t v = tid; v < (n >> 3); v += stride) {
+            float x[8];
+            dev::load_s8(Xj + 8 * v, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], f);
+            dev::store_s8(Xj + 8 * v, x);
+        }
+        done = n;
+    }
+    for (int64_t i = done + tid; i < n; i += stride) Xj[i] = __fmul_rn(Xj[i], f);
 }
 
 struct ApplyArgs {
-    float* theta;
-    float* e;         // EMA buffer, or null
-    const float* O;   // the polar factor (converged iterate)
+    float* theta[kOrthoBatchMax];
+    float* e[kOrthoBatchMax];  // EMA buffers, or null
+    uint32_t vec[kOrthoBatchMax / 32];  // bit j: matrix j's buffers take 32-byte vectors
+    const float* O;            // the polar factors (converged iterates), slot j at O + j * n
     int64_t n;
-    const double* scalars;
+    const double* scalars;     // [j] = |Delta_j|_F^2
     float lr;
     int32_t scale_mode;
-    int64_t r;        // min(m, n)
+    int64_t r;                 // min(m, n)
     float beta;
 };
 
 // theta' = theta + s O, then e' = beta e + (1 - beta) theta'.
-__global__ void ortho_apply(const ApplyArgs a) {
+__global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
+    const int j = blockIdx.y;
+    float* theta = a.theta[j];
+    float* e = a.e[j];
+    const float* O = a.O + int64_t(j) * a.n;
     float s = a.lr;
     if (a.scale_mode == CAM_ORTHO_SCALE_MATCH_NORM)
-        s = static_cast<float>(static_cast<double>(a.lr) * sqrt(a.scalars[0]) /
+        s = static_cast<float>(static_cast<double>(a.lr) * sqrt(a.scalars[j]) /
                                sqrt(static_cast<double>(a.r)));
     const float omb = __fsub_rn(1.0f, a.beta);
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < a.n;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const float th = __fadd_rn(a.theta[i], __fmul_rn(s, a.O[i]));
-        a.theta[i] = th;
-        if (a.e) a.e[i] = __fadd_rn(__fmul_rn(a.beta, a.e[i]), __fmul_rn(omb, th));
+    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t done = 0;
+    if ((a.vec[j >> 5] >> (j & 31)) & 1u) {  // 8 elements per step
+        const int64_t nv = a.n >> 3;
+        for (int64_t v = tid; v < nv; v += stride) {
+            float th[8], o[8];
+            dev::load_s8(theta + 8 * v, th);
+            dev::load_s8(O + 8 * v, o);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) th[q] = __fadd_rn(th[q], __fmul_rn(s, o[q]));
+            dev::store_s8(theta + 8 * v, th);
+            if (e) {
+                float ev[8];
+                dev::load_s8(e + 8 * v, ev);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    ev[q] = __fadd_rn(__fmul_rn(a.beta, ev[q]), __fmul_rn(omb, th[q]));
+                dev::store_s8(e + 8 * v, ev);
+            }
+        }
+        done = 8 * nv;
+    }
+    for (int64_t i = done + tid; i < a.n; i += stride) {
+        const float th = __fadd_rn(theta[i], __fmul_rn(s, O[i]));
+        theta[i] = th;
+        if (e) e[i] = __fadd_rn(__fmul_rn(a.beta, e[i]), __fmul_rn(omb, th));
     }
 }
 
@@ -362,30 +442,51 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
     if (count <= 0) return CAM_OK;
     const int64_t m = mats[0].rows, n = mats[0].cols, numel = m * n;
     const int64_t r = std::min(m, n), gram = r * r;
-    const int grid = static_cast<int>(std::min<int64_t>(
-        kOrthoBlocksMax, std::max<int64_t>(1, std::min<int64_t>(int64_t(sm_count) * 4,
-                                                                (numel + kOrthoThreads - 1) / kOrthoThreads))));
     int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_elems / numel, w->cap_gram / gram));
     per = std::max<int64_t>(per, 1);
     for (int first = 0; first < count; first += static_cast<int>(per)) {
         const int B = static_cast<int>(std::min<int64_t>(per, count - first));
-        // Delta of each matrix into its slot, its norm, and the normalised start.
+        // Blocks per matrix: about 8 per SM over the whole batch, and no more
+        // than the matrix has 8-element steps for (small matrices in a big
+        // batch would otherwise leave most threads idle).
+        const int64_t steps = (numel + 8 * kOrthoThreads - 1) / (8 * kOrthoThreads);
+        const int64_t want = (int64_t(sm_count) * 8 + B - 1) / B;
+        const int grid = static_cast<int>(
+            std::min<int64_t>(kOrthoBlocksMax, std::max<int64_t>(1, std::min(want, steps))));
+        // Delta of each matrix into its slot, its norm, and the normalised
+        // start: one launch of each kernel for the whole batch.
+        // a slot of the workspace is 32-byte aligned when numel is a multiple of 8
+        const uintptr_t xa = p.dtype == kDtBF16 ? 16 : 32;
+        auto al = [](const void* q, uintptr_t b) { return reinterpret_cast<uintptr_t>(q) % b == 0; };
+        DeltaArgs da;
+        ApplyArgs aa;
+        std::fill(da.vec, da.vec + kOrthoBatchMax / 32, 0u);
+        std::fill(aa.vec, aa.vec + kOrthoBatchMax / 32, 0u);
         for (int j = 0; j < B; ++j) {
             const OrthoMatrix& t = mats[first + j];
-            DeltaArgs da;
-            for (int k = 0; k < CAM_KMAX; ++k) da.x[k] = k < p.K ? t.x[k] : nullptr;
-            da.K = p.K;
-            da.Kf = static_cast<float>(p.K);
-            da.theta = t.theta;
-            da.X = w->X + int64_t(j) * numel;
-            da.n = numel;
-            da.partials = w->partials + int64_t(j) * kOrthoBlocksMax;
-            if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<grid, kOrthoThreads, 0, s>>>(da);
-            else ortho_delta<float><<<grid, kOrthoThreads, 0, s>>>(da);
-            ortho_norm<<<1, 32, 0, s>>>(da.partials, grid, w->scalars + j, w->inv_norm + j);
-            ortho_scale<<<grid, kOrthoThreads, 0, s>>>(da.X, numel, w->inv_norm + j);
-            *launches += 3;
+            bool v = numel % 8 == 0 && al(t.theta, 32);
+            for (int k = 0; k < CAM_KMAX; ++k) {
+                da.x[j][k] = k < p.K ? t.x[k] : nullptr;
+                if (k < p.K) v = v && al(t.x[k], xa);
+            }
+            da.theta[j] = t.theta;
+            if (v) da.vec[j >> 5] |= 1u << (j & 31);
+            aa.theta[j] = t.theta;
+            aa.e[j] = p.ema ? t.e : nullptr;
+            if (numel % 8 == 0 && al(t.theta, 32) && (!p.ema || al(t.e, 32)))
+                aa.vec[j >> 5] |= 1u << (j & 31);
         }
+        da.K = p.K;
+        da.Kf = static_cast<float>(p.K);
+        da.X = w->X;
+        da.n = numel;
+        da.partials = w->partials;
+        const dim3 bgrid(grid, B);
+        if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(da);
+        else ortho_delta<float><<<bgrid, kOrthoThreads, 0, s>>>(da);
+        ortho_norm<<<B, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
+        ortho_scale<<<bgrid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
+        *launches += 3;
         cudaError_t ce = cudaGetLastError();
         if (ce != cudaSuccess)
             return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
@@ -411,13 +512,15 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
             if (rc != CAM_OK) return rc;
             std::swap(cur, nxt);
         }
-        for (int j = 0; j < B; ++j) {
-            const OrthoMatrix& t = mats[first + j];
-            ApplyArgs aa{t.theta, p.ema ? t.e : nullptr, cur + int64_t(j) * numel, numel,
-                         w->scalars + j, p.lr, p.scale_mode, r, p.beta};
-            ortho_apply<<<grid, kOrthoThreads, 0, s>>>(aa);
-            *launches += 1;
-        }
+        aa.O = cur;
+        aa.n = numel;
+        aa.scalars = w->scalars;
+        aa.lr = p.lr;
+        aa.scale_mode = p.scale_mode;
+        aa.r = r;
+        aa.beta = p.beta;
+        ortho_apply<<<bgrid, kOrthoThreads, 0, s>>>(aa);
+        *launches += 1;
         ce = cudaGetLastError();
         if (ce != cudaSuccess)
             return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
