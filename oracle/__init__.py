@@ -18,8 +18,8 @@ Sources (page title, section):
     the bucket": fragments=4, quorum_size=3, token-weighted mean of the deltas,
     outer Nesterov (lr 0.7, momentum 0.9), two rounds in flight.
 
-All arrays are numpy; floating point is fp32 as the pages fix it ("running fp32
-sum"), drift sums are fp64.
+All arrays are numpy; floating point is fp32 as the pages fix it (the running
+sum is kept in fp32), drift sums are fp64.
 """
 from __future__ import annotations
 

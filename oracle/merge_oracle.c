@@ -24,8 +24,8 @@
  *         are the uniform average of the 130 merged globals of the final
  *         stretch; section 5.4 / Table 5: uniform average and averages of
  *         the last 3 and 5 snapshots.
- *   [TR 5.1] same report, section 5.1 (Distributed optimisation): "local
- *         drift", the movement of the workers away from the last global, and
+ *   [TR 5.1] same report, section 5.1 (Distributed optimisation): local
+ *         drift, the movement of the workers away from the last global, and
  *         the rejected alternative to plain replacement, adopting the global
  *         as theta <- theta + (g - theta_pushed), which keeps each worker's
  *         progress since its last push.
