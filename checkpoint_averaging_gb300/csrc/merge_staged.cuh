@@ -406,58 +406,100 @@ __global__ void __launch_bounds__(kStThreads, 1)
         return;
     }
 
-    // ---- consumers: four elements per thread per tile, tiles in the order
-    // the producer filled the stages, until the end marker ----
+    // ---- consumers: four elements per thread per tile ----
     const int g = threadIdx.x;
     float acc = 0.0f;
     float accw[CAM_KMAX];
 #pragma unroll
     for (int k = 0; k < CAM_KMAX; ++k) accw[k] = 0.0f;
-    for (int it = 0, ci = 0;; ++it) {
-        const int s = it % P, n = it / P;
-        if (*abort_v) return;
+    // Hands chunk number ci's per-thread sums to the reducer warp; false when
+    // the wait for a free slot gave up.
+    auto hand_over = [&](int ci) -> bool {
+        const int slot = ci % kStRedSlots, use = ci / kStRedSlots;
+        if (use > 0 && !mbar_wait(smem_u32(&red_empty[slot]), (use - 1) & 1)) {
+            *abort_v = 1;
+            atomicOr(a.status, kStatusWaitTimeout);
+            return false;
+        }
+        float* rb = red + slot * nq * kStConsumers;
+        rb[g] = acc;
+        acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k) {
+            if (WD && k < a.K) rb[(1 + k) * kStConsumers + g] = accw[k];
+            accw[k] = 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&red_full[slot]));
+        return true;
+    };
+    // Waits for stage s's use n; false (with the abort flag set) on a timeout.
+    auto wait_full = [&](int s, int n) -> bool {
+        if (*abort_v) return false;
         if (!mbar_wait(smem_u32(&full[s]), n & 1)) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
-            return;
+            return false;
         }
-        const int len = meta[s].len;
-        if (len == 0) {  // end marker: release it and stop
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-            return;
+        return true;
+    };
+
+    if constexpr (WD) {
+        // With per-worker drift the arithmetic per element is heavy enough for
+        // the pass to be issue-bound. Here the consumers walk the block's
+        // chunks themselves and keep each chunk's pointers in registers, which
+        // measured faster than reading the per-tile descriptor; they only
+        // release the producer's end marker at the end.
+        int it = 0, ci = 0;
+        for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++ci) {
+            const ChunkDesc ch = a.chunks[c];
+            const TensorSlot ts = a.slots[ch.local];
+            const void* const* xs = a.x + static_cast<int64_t>(ch.local - a.local0) * a.stride;
+            for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
+                const int s = it % P;
+                if (!wait_full(s, it / P)) return;
+                const int len = min(kStTile, ch.len - t0);
+                const int len8 = len & ~7;
+                const int64_t i0 = ch.start + t0;
+                if (4 * g < len8)
+                    staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(
+                        a, xs, ts, ring0 + s * stage_bytes, L, i0 + 4 * g, 4 * g, acc, accw);
+                if (g < len - len8)  // the ragged end, straight from global memory
+                    merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc, accw);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            }
+            if (!hand_over(ci)) return;
         }
-        const TensorSlot ts = meta[s].ts;
-        const int64_t i0 = meta[s].i0;
-        const int last = meta[s].last;
-        const void* const* xs = a.x + static_cast<int64_t>(meta[s].l) * a.stride;
-        const int len8 = len & ~7;
-        if (4 * g < len8)
-            staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, ring0 + s * stage_bytes, L,
-                                                           i0 + 4 * g, 4 * g, acc, accw);
-        if (g < len - len8)  // the ragged end, straight from global memory
-            merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc, accw);
+        const int s = it % P;  // the end marker
+        if (!wait_full(s, it / P)) return;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-        if (NORM && last) {
-            // hand this chunk's per-thread sums to the reducer warp
-            const int slot = ci % kStRedSlots, use = ci / kStRedSlots;
-            ++ci;
-            if (use > 0 && !mbar_wait(smem_u32(&red_empty[slot]), (use - 1) & 1)) {
-                *abort_v = 1;
-                atomicOr(a.status, kStatusWaitTimeout);
+    } else {
+        // Otherwise they take the tiles in the order the producer filled the
+        // stages, reading each tile's descriptor, until the end marker.
+        for (int it = 0, ci = 0;; ++it) {
+            const int s = it % P;
+            if (!wait_full(s, it / P)) return;
+            const int len = meta[s].len;
+            if (len == 0) {  // end marker: release it and stop
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
                 return;
             }
-            float* rb = red + slot * nq * kStConsumers;
-            rb[g] = acc;
-            acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < CAM_KMAX; ++k) {
-                if (WD && k < a.K) rb[(1 + k) * kStConsumers + g] = accw[k];
-                accw[k] = 0.0f;
-            }
+            const TensorSlot ts = meta[s].ts;
+            const int64_t i0 = meta[s].i0;
+            const int last = meta[s].last;
+            const void* const* xs = a.x + static_cast<int64_t>(meta[s].l) * a.stride;
+            const int len8 = len & ~7;
+            if (4 * g < len8)
+                staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, ring0 + s * stage_bytes, L,
+                                                               i0 + 4 * g, 4 * g, acc, accw);
+            if (g < len - len8)  // the ragged end, straight from global memory
+                merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc, accw);
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&red_full[slot]));
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+            if (NORM && last && !hand_over(ci++)) return;
         }
     }
 }
