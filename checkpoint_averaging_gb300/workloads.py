@@ -261,11 +261,14 @@ SWEEP_K = (2, 4, 8)
 
 def workload(name: str) -> Workload:
     """A workload by name; a "+swa" suffix also folds each global into the
-    uniform running average."""
+    uniform running average, a "-ema" suffix drops the EMA update."""
+    import dataclasses
     if name.endswith("+swa"):
-        import dataclasses
         wl = workload(name[:-len("+swa")])
         return dataclasses.replace(wl, name=wl.name + "_swa", swa=True)
+    if name.endswith("-ema"):
+        wl = workload(name[:-len("-ema")])
+        return dataclasses.replace(wl, name=wl.name + "_noema", ema_beta=None)
     table = {
         "pythia14m": _wl_pythia,
         "stand": _wl_stand,
@@ -280,7 +283,6 @@ def workload(name: str) -> Workload:
         parts = name.split(":")[1].split(",")
         t, n, k = (int(v) for v in parts[:3])
         wl = sweep_workload(t, n, k)
-        import dataclasses
         if len(parts) > 3 and parts[3] == "norms":  # Nesterov + EMA + drift norms
             wl = dataclasses.replace(wl, name=wl.name + "_norms", norms=True)
         elif len(parts) > 3 and parts[3] == "wnorms":  # ... plus each worker's drift

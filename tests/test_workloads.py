@@ -98,3 +98,12 @@ def test_bf16_workers_are_rounded_fp32_workers():
     w = W.make_worker(small, g, 0, 0, 0, "cpu")
     assert w.flat.dtype == torch.bfloat16
     assert wl.ckpt_dtype == "bf16"
+
+
+def test_workload_name_modifiers():
+    base = W.workload("stand")
+    swa = W.workload("stand+swa")
+    assert swa.swa and not base.swa and swa.specs == base.specs
+    wn = W.workload("sweep:64,16000000,3,wnorms-ema")
+    assert wn.ema_beta is None and wn.norms and wn.worker_norms
+    assert W.workload("sweep:64,16000000,3").ema_beta == 0.9
