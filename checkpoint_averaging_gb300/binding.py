@@ -26,6 +26,7 @@ NO_STAGING = 8
 STATUS_WAIT_TIMEOUT = 1
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
 ORTHO_TF32, ORTHO_FP32 = 0, 1
+ORTHO_SHORT_SIDE = 4  # OR into the precision: iterate in the short side's space
 
 OK, E_ARG, E_STATE, E_STALE, E_BUSY, E_QUORUM, E_KMAX, E_CUDA, E_NOMEM = \
     0, -1, -2, -3, -4, -5, -6, -7, -8

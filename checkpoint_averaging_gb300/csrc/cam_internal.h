@@ -116,6 +116,7 @@ struct OrthoParams {
     int scale_mode, precision, iterations;
     bool ema;
     float beta;
+    bool short_side;  // iterate in the short side's space (CAM_ORTHO_SHORT_SIDE)
 };
 // cap_elems / cap_gram: floats in each iterate buffer and in the Gram buffer
 // (at least one matrix's worth; batches of equal-shape matrices share them).

@@ -246,6 +246,15 @@ __global__ void ortho_scale(float* X, int64_t n, const float* inv_norm) {
     for (int64_t i = done + tid; i < n; i += stride) Xj[i] = __fmul_rn(Xj[i], f);
 }
 
+// P_j <- I (r x r) for every slot j; total = slots x r x r.
+__global__ void ortho_identity(float* P, int64_t r, int64_t total) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t q = i % (r * r);
+        P[i] = (q / r == q % r) ? 1.0f : 0.0f;
+    }
+}
+
 struct ApplyArgs {
     float* theta[kOrthoBatchMax];
     float* e[kOrthoBatchMax];  // EMA buffers, or null
@@ -377,6 +386,78 @@ int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
     return CAM_OK;
 }
 
+// The short-side form of the iteration (CAM_ORTHO_SHORT_SIDE) for B
+// matrices of m x n with max(m, n) >= 4 r, r = min(m, n). With the iterate
+// written X_k = X_0 P_k (tall) or P_k X_0 (wide), a Newton-Schulz step becomes
+// P <- 1.5 P - 0.5 P (P^T G P) (tall) or 1.5 P - 0.5 (P G P^T) P (wide) on
+// r x r matrices, G the Gram matrix of X_0 on its short side; the polar
+// factor is then one product with X_0. The normalised starts are in w->X,
+// the factors end in w->Y. Workspace: P in w->G, and G, T, M and P's second
+// buffer in w->Y (4 B r^2 <= B m n floats), which the final product then
+// overwrites. G and the r x r steps run in fp32; the final product in
+// p.precision.
+int short_side_iteration(OrthoWork* w, const OrthoParams& p, int64_t m, int64_t n, int B,
+                         cudaStream_t s, int64_t* launches) {
+    const int64_t r = std::min(m, n), numel = m * n, gram = r * r;
+    const bool tall = m >= n;
+    const float* A = w->X;  // each X_0 as the column-major n x m matrix X_0^T (ld n)
+    float* G = w->Y;
+    float* T = G + int64_t(B) * gram;
+    float* M = T + int64_t(B) * gram;
+    float* Pa = w->G;
+    float* Pb = M + int64_t(B) * gram;
+    const int fp = CAM_ORTHO_FP32;
+    int rc = tall ? gemm(w, fp, false, true, n, n, m, 1.0f, A, n, A, n, 0.0f, G, G, n, B, numel,
+                         numel, gram, s)   // G = X_0^T X_0 = A A^T
+                  : gemm(w, fp, true, false, m, m, n, 1.0f, A, n, A, n, 0.0f, G, G, m, B, numel,
+                         numel, gram, s);  // G = X_0 X_0^T = A^T A
+    if (rc != CAM_OK) return rc;
+    const int64_t total = int64_t(B) * gram;
+    const int blocks =
+        static_cast<int>(std::min<int64_t>(4096, (total + kOrthoThreads - 1) / kOrthoThreads));
+    ortho_identity<<<blocks, kOrthoThreads, 0, s>>>(Pa, r, total);
+    ++*launches;
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess)
+        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
+    float* P = Pa;
+    float* Pn = Pb;
+    for (int it = 0; it < p.iterations && rc == CAM_OK; ++it) {
+        if (tall) {  // T = P^T G; M = T P; P' = 1.5 P - 0.5 P M
+            rc = gemm(w, fp, true, false, r, r, r, 1.0f, P, r, G, r, 0.0f, T, T, r, B, gram, gram,
+                      gram, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, fp, false, false, r, r, r, 1.0f, T, r, P, r, 0.0f, M, M, r, B, gram,
+                          gram, gram, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, fp, false, false, r, r, r, -0.5f, P, r, M, r, 1.5f, P, Pn, r, B, gram,
+                          gram, gram, s);
+        } else {     // T = P G; M = T P^T; P' = 1.5 P - 0.5 M P
+            rc = gemm(w, fp, false, false, r, r, r, 1.0f, P, r, G, r, 0.0f, T, T, r, B, gram, gram,
+                      gram, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, fp, false, true, r, r, r, 1.0f, T, r, P, r, 0.0f, M, M, r, B, gram,
+                          gram, gram, s);
+            if (rc == CAM_OK)
+                rc = gemm(w, fp, false, false, r, r, r, -0.5f, M, r, P, r, 1.5f, P, Pn, r, B, gram,
+                          gram, gram, s);
+        }
+        std::swap(P, Pn);
+    }
+    if (rc != CAM_OK) return rc;
+    if (P != Pa) {  // the final product writes over w->Y, where P_b lives
+        ce = cudaMemcpyAsync(Pa, P, sizeof(float) * total, cudaMemcpyDeviceToDevice, s);
+        if (ce != cudaSuccess)
+            return record_error(CAM_E_CUDA, "orthogonalisation: copy: %s", cudaGetErrorString(ce));
+        P = Pa;
+    }
+    // tall: X = X_0 P, column-major P^T A; wide: X = P X_0, column-major A P^T
+    return tall ? gemm(w, p.precision, true, false, n, m, n, 1.0f, P, n, A, n, 0.0f, w->Y, w->Y, n,
+                       B, gram, numel, numel, s)
+                : gemm(w, p.precision, false, true, n, m, m, 1.0f, A, n, P, m, 0.0f, w->Y, w->Y, n,
+                       B, numel, gram, numel, s);
+}
+
 }  // namespace
 }  // namespace cam
 
@@ -494,7 +575,13 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
         // column-major n x m matrix A = X^T (ld n).
         float* cur = w->X;
         float* nxt = w->Y;
-        for (int it = 0; it < p.iterations; ++it) {
+        const bool short_side = p.short_side && std::max(m, n) >= 4 * r;
+        if (short_side) {
+            const int rc = short_side_iteration(w, p, m, n, B, s, launches);
+            if (rc != CAM_OK) return rc;
+            cur = w->Y;
+        }
+        for (int it = 0; !short_side && it < p.iterations; ++it) {
             int rc;
             if (m >= n) {  // G = X^T X = A A^T (n x n); A' = 1.5 A - 0.5 G A
                 rc = gemm(w, p.precision, false, true, n, n, m, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G,

@@ -563,7 +563,8 @@ CAM_API int cam_merge_orthogonalize(cam_round* r, float lr, int32_t scale_mode, 
     if (!std::isfinite(lr)) return fail(CAM_E_ARG, "%s: lr must be finite", fn);
     if (scale_mode != CAM_ORTHO_SCALE_FIXED && scale_mode != CAM_ORTHO_SCALE_MATCH_NORM)
         return fail(CAM_E_ARG, "%s: unknown scale mode %d", fn, scale_mode);
-    if (precision != CAM_ORTHO_TF32 && precision != CAM_ORTHO_FP32)
+    const int32_t base = precision & ~int32_t(CAM_ORTHO_SHORT_SIDE);
+    if (base != CAM_ORTHO_TF32 && base != CAM_ORTHO_FP32)
         return fail(CAM_E_ARG, "%s: unknown precision %d", fn, precision);
     if (iterations < 1 || iterations > 1000)
         return fail(CAM_E_ARG, "%s: iterations %d outside [1, 1000]", fn, iterations);
@@ -783,8 +784,15 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         }
         // ... and each matrix has its averaged update replaced by its polar
         // factor, equal shapes batched together (first-appearance order)
-        const cam::OrthoParams op{K, r->dtype, r->ortho_lr, r->ortho_scale, r->ortho_precision,
-                                  r->ortho_iterations, r->ema, r->beta};
+        const cam::OrthoParams op{K,
+                                  r->dtype,
+                                  r->ortho_lr,
+                                  r->ortho_scale,
+                                  r->ortho_precision & ~int32_t(CAM_ORTHO_SHORT_SIDE),
+                                  r->ortho_iterations,
+                                  r->ema,
+                                  r->beta,
+                                  (r->ortho_precision & CAM_ORTHO_SHORT_SIDE) != 0};
         std::vector<char> done(T, 0);
         std::vector<cam::OrthoMatrix> group;
         for (int l = 0; l < T && ce == cudaSuccess; ++l) {

@@ -1041,3 +1041,41 @@ def test_form_of_the_merge_pass(mode, ema, swa, host, staging, want_staged):
     compare_full(st, ost, f"form test {mode} ema={ema} swa={swa} host={host}")
     assert st.merger.status() == 0
     st.merger.close()
+
+
+# tall and wide enough (long side >= 4 x short side) for the short-side form,
+# plus shapes below that ratio, which keep the plain iteration in the same round
+SHORT_SIDE_SHAPES = [(512, 64), (1000, 100), (48, 400), (96, 40), (64, 64), (333, 0)]
+
+
+@pytest.mark.parametrize("precision", [B.ORTHO_FP32, B.ORTHO_TF32])
+@pytest.mark.parametrize("mode", [B.ORTHO_SCALE_FIXED, B.ORTHO_SCALE_MATCH_NORM])
+def test_short_side_iteration_matches_the_polar_factor(precision, mode):
+    lr = 0.01 if mode == B.ORTHO_SCALE_FIXED else 0.7
+    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(
+            SHORT_SIDE_SHAPES, "f32", precision | B.ORTHO_SHORT_SIDE, mode, lr, seed=35):
+        if kind == "vector":
+            assert bitwise_equal(got, want.astype(np.float32)), t
+            continue
+        scale = np.abs(want - th0.astype(np.float64)).max()
+        err = np.abs(got.astype(np.float64) - want).max()
+        print(f"short side precision={precision} mode={mode} {r}x{c}: "
+              f"max err / max step = {err / scale:.3e}")
+        assert err <= ORTHO_TOL[precision] * scale + 2 * np.spacing(np.float32(np.abs(want).max()))
+        o = (got.astype(np.float64) - th0).reshape(r, c)
+        o *= np.sqrt(min(r, c)) / np.linalg.norm(o)
+        gram = o.T @ o if r >= c else o @ o.T
+        assert np.abs(gram - np.eye(min(r, c))).max() <= 30 * ORTHO_TOL[precision]
+
+
+def test_short_side_flag_is_validated():
+    th = [torch.zeros(64, device=DEV)]
+    e = [torch.zeros(64, device=DEV)]
+    mg = B.Merger(th, ema=e, quorum=1, rows=[8])
+    rd = mg.begin(0)
+    for bad in (2, 3, 6, 7, 8):
+        with pytest.raises(B.ArgError):
+            rd.orthogonalize(0.1, B.ORTHO_SCALE_FIXED, bad, 10)
+    rd.orthogonalize(0.1, B.ORTHO_SCALE_FIXED, B.ORTHO_FP32 | B.ORTHO_SHORT_SIDE, 10)
+    rd.abort()
+    mg.close()
