@@ -201,10 +201,12 @@ def test_kmax_workers_and_one_more_rejected():
     st.merger.close()
 
 
-def test_many_tensors_split_over_launches():
-    # 1000 tensors with K = 8 exceed one launch's pointer block (3520 pointers)
+@pytest.mark.parametrize("mode,ema", [("delta", True), ("delta", False), ("mean", True)])
+def test_many_tensors_split_over_launches(mode, ema):
+    # 1000 tensors with K = 8 exceed one launch's pointer block (3520 pointers);
+    # the last two cases write two state arrays and take the staged form
     sizes = [(i * 37) % 300 + 1 for i in range(1000)]
-    run_full(_custom(sizes, K=8, mode="delta", dtype="bf16"), seed=9)
+    run_full(_custom(sizes, K=8, mode=mode, dtype="bf16", ema=ema), seed=9)
 
 
 def test_empty_fragment_and_zero_size_tensors():
