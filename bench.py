@@ -517,32 +517,46 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
       host memory (cam_merge_accumulate_host) and writes the new global and
       EMA into host buffers in the same pass (cam_merge_publish).
     copy: the workers are copied host->device with the copy engine, merged,
-      and the new global and EMA copied device->host afterwards."""
+      and the new global and EMA copied device->host afterwards.
+    fold: as stream, but each worker is folded into the running sum as it
+      arrives (cam_merge_fold), so commit only finishes from the sum.
+
+    In stream and fold mode, post_arrival_ms is the time from the last
+    worker's arrival (its accumulate or fold call) to the new global in host
+    memory: what remains of a round once its quorum is in."""
     import torch
 
     from checkpoint_averaging_gb300 import workloads as W
 
     dev = theta.flat.device
     pinned = [[None] * wl.K for _ in wl.rounds]
-    h2d = 0
-    for i, d in enumerate(draws):
+    h2d = d2h = 0
+    x_size = 2 if wl.ckpt_dtype == "bf16" else 4
+    for i, ((_, frag), d) in enumerate(zip(wl.rounds, draws)):
         for k in d.included:
             h = torch.empty(workers[i][k].flat.numel(), dtype=workers[i][k].flat.dtype,
                             pin_memory=True)
             h.copy_(workers[i][k].flat)
             pinned[i][k] = W.Arena(h, workers[i][k].offsets, workers[i][k].numels)
-            h2d += h.numel() * h.element_size()
+            # stream/fold read only the round's fragment; copy moves whole arenas
+            h2d += (h.numel() * h.element_size() if args.e2e_mode == "copy"
+                    else wl.fragment_numel(frag) * x_size)
+        if args.e2e_mode != "copy":  # the published global (and EMA) of the fragment
+            d2h += wl.fragment_numel(frag) * 4 * (2 if e is not None else 1)
     out_theta = W.Arena(torch.empty(theta.flat.numel(), pin_memory=True), theta.offsets,
                         theta.numels)
     out_e = None
     if e is not None:
         out_e = W.Arena(torch.empty(e.flat.numel(), pin_memory=True), e.offsets, e.numels)
-    d2h = out_theta.flat.numel() * 4 + (out_e.flat.numel() * 4 if out_e is not None else 0)
+    if args.e2e_mode == "copy":
+        d2h = out_theta.flat.numel() * 4 + (out_e.flat.numel() * 4 if out_e is not None else 0)
 
-    src = [{k: mg.checkpoint((pinned[i][k] if args.e2e_mode == "stream" else w[k]).views, frag)
+    host_src = args.e2e_mode in ("stream", "fold")
+    src = [{k: mg.checkpoint((pinned[i][k] if host_src else w[k]).views, frag)
             for k in d.included} for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws))]
+    lat_pairs = []
 
-    def step():
+    def step(timed=False):
         with torch.cuda.stream(stream):
             for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
                 if args.e2e_mode == "copy":
@@ -550,18 +564,30 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
                         w[k].flat.copy_(pinned[i][k].flat, non_blocking=True)
                 rd = mg.begin(round_no[0], frag)
                 round_no[0] += 1
-                for k in d.included:
-                    rd.accumulate(src[i][k], d.tokens[k])
+                ev_a = ev_b = None
+                if timed and host_src:
+                    ev_a = torch.cuda.Event(enable_timing=True)
+                    ev_b = torch.cuda.Event(enable_timing=True)
+                for j, k in enumerate(d.included):
+                    if ev_a is not None and j == len(d.included) - 1:
+                        ev_a.record(stream)  # the last worker arrives
+                    if args.e2e_mode == "fold":
+                        rd.fold(src[i][k], d.tokens[k], mode, stream=stream)
+                    else:
+                        rd.accumulate(src[i][k], d.tokens[k])
                 rd.finalize(mode, wl.lr, wl.mu)
                 if wl.ema_beta is not None:
                     rd.ema_update(wl.ema_beta)
                 if wl.swa:
                     rd.swa_update()
-                if args.e2e_mode == "stream":
+                if host_src:
                     ids = mg.fragment_tensors(frag)
                     rd.publish([out_theta.views[t] for t in ids],
                                None if out_e is None else [out_e.views[t] for t in ids])
                 rd.commit(stream)
+                if ev_b is not None:
+                    ev_b.record(stream)
+                    lat_pairs.append((ev_a, ev_b))
             if args.e2e_mode == "copy":
                 out_theta.flat.copy_(theta.flat, non_blocking=True)
                 if out_e is not None:
@@ -572,11 +598,14 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
-        step()
+        step(timed=True)
     el = time.perf_counter() - t0
     step_bytes = sum(round_bytes(wl, f, len(d.included)) for (_, f), d in zip(wl.rounds, draws))
+    post = (round(statistics.mean(a.elapsed_time(b) for a, b in lat_pairs), 3)
+            if lat_pairs else None)
     return {"value": round(step_bytes * args.e2e_steps / el / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(el / args.e2e_steps * 1e3, 3),
+            "post_arrival_ms": post,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps, "mode": args.e2e_mode,
             "note": "algorithmic merge bytes per wall second; each step moves the included "
@@ -749,7 +778,7 @@ def parse(argv=None):
                    help="iterate in the short side's space for matrices of aspect ratio >= 4")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
-    p.add_argument("--e2e-mode", choices=("stream", "copy"), default="stream")
+    p.add_argument("--e2e-mode", choices=("stream", "copy", "fold"), default="stream")
     p.add_argument("--cpu-seconds", type=float, default=8.0)
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="host threads for the CPU oracle legs (0: every core this process may use)")

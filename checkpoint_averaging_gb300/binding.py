@@ -92,14 +92,13 @@ class CtxDesc(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
-           "cam_merge_accumulate_host", "cam_merge_publish", "cam_swa_update", "cam_swa_reset",
-           "cam_worker_drift_norm", "cam_adopt_keep_drift", "cam_merge_orthogonalize",
-           "cam_swa_counts", "cam_swa_set_counts",
+           "cam_merge_accumulate_host", "cam_merge_fold", "cam_merge_publish",
+           "cam_swa_update", "cam_swa_reset", "cam_worker_drift_norm", "cam_adopt_keep_drift",
+           "cam_merge_orthogonalize", "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
-           "cam_ctx_staged_count", "cam_merge_round_noalloc",
-           "cam_last_error", "cam_version")
+           "cam_ctx_staged_count", "cam_merge_round_noalloc", "cam_last_error", "cam_version")
 
 NOALLOC_MAX_TENSORS = 4096
 NOALLOC_MAX_CHUNKS = 131072
@@ -123,6 +122,7 @@ def lib() -> ctypes.CDLL:
     L.cam_merge_begin.argtypes = [vp, i64, i32, vpp]
     L.cam_merge_accumulate.argtypes = [vp, vpp, ctypes.c_int, i64]
     L.cam_merge_accumulate_host.argtypes = [vp, vpp, ctypes.c_int, i64]
+    L.cam_merge_fold.argtypes = [vp, vpp, ctypes.c_int, i64, ctypes.c_int, vp]
     L.cam_merge_publish.argtypes = [vp, vpp, vpp]
     L.cam_swa_update.argtypes = [vp]
     L.cam_worker_drift_norm.argtypes = [vp, vp, vp]
@@ -588,6 +588,26 @@ class Round:
         fn = lib().cam_merge_accumulate_host if ckpt.host else lib().cam_merge_accumulate
         _check(fn(self.handle, ckpt.ptr_array, ckpt.dtype_code, int(tokens)))
         self._borrowed.extend(ckpt.keep)
+
+    def fold(self, ckpt, tokens: int = 0, mode: int = MEAN_REPLACE, stream=None) -> None:
+        """Folds one arriving worker into the round's running sum at once, on
+        `stream` (default: the current stream). The worker's tensors are held
+        only until that fold has run; `mode` must match the later finalize."""
+        torch = _torch()
+        if not isinstance(ckpt, Checkpoint):
+            ckpt = Checkpoint(self.merger, ckpt, self.fragment)
+        elif ckpt.merger is not self.merger or ckpt.fragment != self.fragment:
+            raise ValueError("checkpoint was prepared for another merger or fragment")
+        s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
+        _check(lib().cam_merge_fold(self.handle, ckpt.ptr_array, ckpt.dtype_code, int(tokens),
+                                    int(mode), int(s.cuda_stream)))
+        host = []
+        for t in ckpt.keep:
+            if t.device.type == "cuda":
+                t.record_stream(s)
+            else:
+                host.append(t)
+        self.merger._hold_until_done(host, s)
 
     def finalize(self, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
         merge_finalize(self.handle, mode, lr, mu)

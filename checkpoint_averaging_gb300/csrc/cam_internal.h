@@ -101,6 +101,52 @@ struct NormArgs {
 
 enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 
+// Eagerly folded rounds (cam_merge_fold, eager.cu). One launch covers up to
+// kEagerTensors of the fragment's local tensors [local0, local0 + n_local).
+constexpr int kEagerTensors = 1024;
+
+// Folds one arriving worker into the round's fp32 running sum.
+struct FoldArgs {
+    const ChunkDesc* chunks;   // first chunk of this launch (device)
+    const TensorSlot* slots;   // the fragment's tensors, by local index (device)
+    double* worker_partials;   // [chunk * CAM_KMAX + k]: this worker's drift partials, or null
+    int32_t n_chunks;
+    int32_t local0;
+    int32_t n_local;
+    int32_t k;                 // the worker's arrival index
+    int32_t first;             // 1: the sum starts at +0 (first arrival)
+    float w;                   // (float)tokens, token-weighted delta mode
+    uint32_t vec[kEagerTensors / 32];  // bit l: tensor local0+l takes the vector path
+    const void* x[kEagerTensors];      // the worker's copy of tensor local0+l
+    float* sum[kEagerTensors];         // the running sum of tensor local0+l
+};
+static_assert(sizeof(FoldArgs) <= 32000, "kernel parameter block too large");
+
+// The final pass of an eagerly folded round: finalize from the running sum,
+// outer step, EMA, running average, drift partials and published copies.
+struct FinalArgs {
+    const ChunkDesc* chunks;
+    const TensorSlot* slots;
+    double* partials;          // drift partial per chunk of this launch, or null
+    int32_t n_chunks;
+    int32_t local0;
+    int32_t n_local;
+    int32_t K;
+    float Kf;                  // (float)K
+    float W;                   // (float)sum tokens
+    float lr, mu, beta;
+    float swa_n;               // globals in the running average after this round
+    uint32_t vec[kEagerTensors / 32];
+    const float* sum[kEagerTensors];
+    void* pub[2 * kEagerTensors];  // [2l]: copy of the new theta, [2l+1]: of the EMA (or null)
+};
+static_assert(sizeof(FinalArgs) <= 32000, "kernel parameter block too large");
+
+cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drift, int grid,
+                        cudaStream_t s);
+cudaError_t launch_final(const FinalArgs& a, int mode, bool ema, bool norm, bool pub, bool swa,
+                         int grid, cudaStream_t s);
+
 // Outer orthogonalisation (ortho.cu): a per-context workspace, made at the
 // first orthogonalised commit, and the per-matrix pipeline.
 struct OrthoWork;

@@ -1,0 +1,208 @@
+// eager.cu -- rounds whose checkpoints are folded as they arrive
+// (cam_merge_fold, declared in include/cam.h).
+//
+// "DiffuRefill-1B" model card, "How it is trained", Merging: the merger keeps
+// a running fp32 sum and adds each downloaded checkpoint to it on arrival, so
+// only the last arrival's fold remains once the quorum is in. Here:
+//
+//   fold_worker   s <- s + x_k (plain mean) or s + w_k (x_k - theta)
+//                 (token-weighted delta mean), s starting at +0 with the
+//                 first arrival; optionally worker k's squared drift
+//                 (x_k - theta)^2 per chunk. Reads the worker (device or
+//                 host memory) and s, writes s: the worker is no longer needed
+//                 once this launch has run.
+//   final_pass    at commit, from s: finalize, outer step, EMA, running
+//                 average, drift partials and published copies, through the
+//                 same merge_finish as the fused pass.
+//
+// Per element the operations are those of the fused pass in the same order,
+// so an eagerly folded round ends with the same bits as a round whose
+// workers are all read at commit. Both kernels are HBM-bound streaming passes
+// in the register form: persistent grid, 8 elements per thread per step,
+// 256-bit loads and stores where aligned.
+#include <cuda_runtime.h>
+
+#include "cam_internal.h"
+#include "merge_device.cuh"
+
+namespace cam {
+namespace {
+
+using namespace cam::dev;
+
+template <typename XT, int MODE, bool WD>
+__global__ void __launch_bounds__(kThreads, 2) fold_worker(const __grid_constant__ FoldArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    __shared__ double part[2][kWarps];
+    int parity = 0;
+    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
+        const ChunkDesc ch = a.chunks[c];
+        const int l = ch.local - a.local0;
+        const XT* x = static_cast<const XT*>(a.x[l]) + ch.start;
+        float* s = a.sum[l] + ch.start;
+        const float* th = a.slots[ch.local].theta + ch.start;
+        float accw = 0.0f;
+        int done = 0;
+        if ((a.vec[l >> 5] >> (l & 31)) & 1u) {
+            const int nv = ch.len >> 3;
+            for (int v = threadIdx.x; v < nv; v += kThreads) {
+                XVec<XT> xv;
+                xv.load(x + 8 * v);
+                float sv[8], t[8];
+                if (a.first) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sv[j] = 0.0f;
+                } else {
+                    load_s8(s + 8 * v, sv);
+                }
+                if (MODE == kDelta || WD) load_s8(th + 8 * v, t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float xj = xv.get(j);
+                    if constexpr (WD) {
+                        const float d = __fsub_rn(xj, t[j]);
+                        accw = __fmaf_rn(d, d, accw);
+                    }
+                    sv[j] = fold_term<MODE>(sv[j], xj, a.w, (MODE == kDelta) ? t[j] : 0.0f);
+                }
+                store_s8(s + 8 * v, sv);
+            }
+            done = 8 * nv;
+        }
+        for (int j = done + threadIdx.x; j < ch.len; j += kThreads) {
+            const float xj = load_x1(x + j);
+            const float t = (MODE == kDelta || WD) ? th[j] : 0.0f;
+            if constexpr (WD) {
+                const float d = __fsub_rn(xj, t);
+                accw = __fmaf_rn(d, d, accw);
+            }
+            s[j] = fold_term<MODE>(a.first ? 0.0f : s[j], xj, a.w, t);
+        }
+        if constexpr (WD) {
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            const double d = warp_sum(static_cast<double>(accw));
+            if (lane == 0) part[parity][warp] = d;
+            __syncthreads();  // the slot is rewritten only two chunks later
+            if (threadIdx.x == 0) {
+                double sum = 0.0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) sum += part[parity][w];
+                a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + a.k] = sum;
+            }
+        }
+    }
+}
+
+template <int MODE, bool EMA, bool NORM, bool PUB, bool SWA>
+__global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant__ FinalArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    __shared__ double part[2][kWarps];
+    int parity = 0;
+    for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
+        const ChunkDesc ch = a.chunks[c];
+        const int l = ch.local - a.local0;
+        const TensorSlot ts = a.slots[ch.local];
+        const float* sum = a.sum[l] + ch.start;
+        float* th_p = ts.theta + ch.start;
+        float* m_p = ts.m + ch.start;
+        float* e_p = ts.e + ch.start;
+        float* sw_p = ts.swa + ch.start;
+        float* pt = PUB ? static_cast<float*>(a.pub[2 * l]) + ch.start : nullptr;
+        float* pe = (PUB && EMA && a.pub[2 * l + 1]) ? static_cast<float*>(a.pub[2 * l + 1]) + ch.start
+                                                     : nullptr;
+        float acc = 0.0f;
+        int done = 0;
+        if ((a.vec[l >> 5] >> (l & 31)) & 1u) {
+            const int nv = ch.len >> 3;
+            for (int v = threadIdx.x; v < nv; v += kThreads) {
+                float sv[8], th[8], m[8], e[8], sw[8];
+                load_s8(sum + 8 * v, sv);
+                if (MODE == kDelta || NORM) load_s8(th_p + 8 * v, th);
+                if (MODE == kDelta) load_s8(m_p + 8 * v, m);
+                if (EMA) load_s8(e_p + 8 * v, e);
+                if constexpr (SWA) load_s8(sw_p + 8 * v, sw);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    merge_finish<MODE, EMA, NORM>(a, sv[j], th[j], m[j], e[j], acc);
+                    if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
+                }
+                store_s8(th_p + 8 * v, th);
+                if (MODE == kDelta) store_s8(m_p + 8 * v, m);
+                if (EMA) store_s8(e_p + 8 * v, e);
+                if constexpr (SWA) store_s8(sw_p + 8 * v, sw);
+                if (PUB) {
+                    store_s8(pt + 8 * v, th);
+                    if (pe) store_s8(pe + 8 * v, e);
+                }
+            }
+            done = 8 * nv;
+        }
+        for (int j = done + threadIdx.x; j < ch.len; j += kThreads) {
+            float th = (MODE == kDelta || NORM) ? th_p[j] : 0.0f;
+            float m = (MODE == kDelta) ? m_p[j] : 0.0f;
+            float e = EMA ? e_p[j] : 0.0f;
+            merge_finish<MODE, EMA, NORM>(a, sum[j], th, m, e, acc);
+            th_p[j] = th;
+            if (MODE == kDelta) m_p[j] = m;
+            if (EMA) e_p[j] = e;
+            if constexpr (SWA) sw_p[j] = swa_fold(a, sw_p[j], th);
+            if (PUB) {
+                pt[j] = th;
+                if (pe) pe[j] = e;
+            }
+        }
+        if constexpr (NORM) {
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            const double d = warp_sum(static_cast<double>(acc));
+            if (lane == 0) part[parity][warp] = d;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                double s = 0.0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) s += part[parity][w];
+                a.partials[c] = s;
+            }
+        }
+    }
+}
+
+using FoldFn = void (*)(FoldArgs);
+using FinalFn = void (*)(FinalArgs);
+
+template <typename XT>
+FoldFn pick_fold(int mode, bool wd) {
+    if (mode == kDelta) return wd ? fold_worker<XT, kDelta, true> : fold_worker<XT, kDelta, false>;
+    return wd ? fold_worker<XT, kMean, true> : fold_worker<XT, kMean, false>;
+}
+
+template <int MODE, bool EMA, bool NORM>
+FinalFn pick_final_ps(bool pub, bool swa) {
+    if (pub) return swa ? final_pass<MODE, EMA, NORM, true, true> : final_pass<MODE, EMA, NORM, true, false>;
+    return swa ? final_pass<MODE, EMA, NORM, false, true> : final_pass<MODE, EMA, NORM, false, false>;
+}
+
+template <int MODE>
+FinalFn pick_final_mode(bool ema, bool norm, bool pub, bool swa) {
+    if (ema) return norm ? pick_final_ps<MODE, true, true>(pub, swa) : pick_final_ps<MODE, true, false>(pub, swa);
+    return norm ? pick_final_ps<MODE, false, true>(pub, swa) : pick_final_ps<MODE, false, false>(pub, swa);
+}
+
+}  // namespace
+
+cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drift, int grid,
+                        cudaStream_t s) {
+    const FoldFn fn = dtype == kDtBF16 ? pick_fold<uint16_t>(mode, worker_drift)
+                                       : pick_fold<float>(mode, worker_drift);
+    void* args[] = {const_cast<FoldArgs*>(&a)};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), args, 0, s);
+}
+
+cudaError_t launch_final(const FinalArgs& a, int mode, bool ema, bool norm, bool pub, bool swa,
+                         int grid, cudaStream_t s) {
+    const FinalFn fn = mode == kDelta ? pick_final_mode<kDelta>(ema, norm, pub, swa)
+                                      : pick_final_mode<kMean>(ema, norm, pub, swa);
+    void* args[] = {const_cast<FinalArgs*>(&a)};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), args, 0, s);
+}
+
+}  // namespace cam

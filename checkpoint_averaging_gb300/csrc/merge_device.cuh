@@ -87,16 +87,15 @@ __device__ __forceinline__ void store_s8(float* p, const float (&v)[8]) {
 
 // ---- per-element arithmetic ----------------------------------------------------
 
-// One element of one round. xk[k] (k < K) are the workers' values in arrival
-// order; th, m, e are updated in place; acc collects the squared drift.
+// What follows the fold for one element: s is the arrival-order sum (the
+// plain sum of the workers, or the token-weighted sum of their deltas);
+// finalize, outer step and EMA update th, m, e in place, and acc collects the
+// squared drift. Shared by the fused pass and the final pass of eagerly folded
+// rounds, so both produce the same bits.
 template <int MODE, bool EMA, bool NORM, class A>
-__device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMAX],
-                                           float& th, float& m, float& e, float& acc) {
+__device__ __forceinline__ void merge_finish(const A& a, float s, float& th, float& m, float& e,
+                                             float& acc) {
     if (MODE == kMean) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k)
-            if (k < a.K) s = __fadd_rn(s, xk[k]);
         const float mean = __fdiv_rn(s, a.Kf);
         if (NORM) {
             const float d = __fsub_rn(mean, th);
@@ -104,10 +103,6 @@ __device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMA
         }
         th = mean;  // plain replacement
     } else {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k)
-            if (k < a.K) s = __fadd_rn(s, __fmul_rn(a.w[k], __fsub_rn(xk[k], th)));
         const float delta = __fdiv_rn(s, a.W);
         if (NORM) acc = __fmaf_rn(delta, delta, acc);
         const float g = -delta;  // pseudo-gradient theta - (theta + delta)
@@ -120,6 +115,25 @@ __device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMA
         const float omb = __fsub_rn(1.0f, a.beta);
         e = __fadd_rn(__fmul_rn(a.beta, e), __fmul_rn(omb, th));
     }
+}
+
+// One worker's term of the arrival-order fold: s + x (plain mean) or
+// s + w * (x - theta) (token-weighted delta mean), one rounding per operation.
+template <int MODE>
+__device__ __forceinline__ float fold_term(float s, float x, float w, float th) {
+    return MODE == kMean ? __fadd_rn(s, x) : __fadd_rn(s, __fmul_rn(w, __fsub_rn(x, th)));
+}
+
+// One element of one round. xk[k] (k < K) are the workers' values in arrival
+// order; th, m, e are updated in place; acc collects the squared drift.
+template <int MODE, bool EMA, bool NORM, class A>
+__device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMAX],
+                                           float& th, float& m, float& e, float& acc) {
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < CAM_KMAX; ++k)
+        if (k < a.K) s = fold_term<MODE>(s, xk[k], MODE == kMean ? 1.0f : a.w[k], th);
+    merge_finish<MODE, EMA, NORM>(a, s, th, m, e, acc);
 }
 
 // Folds the new global into the uniform running average: mu + (theta' - mu)/n,

@@ -122,6 +122,12 @@ struct cam_ctx {
     }
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     bool staged = true;            // the staged form of the merge pass may be used
+    // Running sums of eagerly folded rounds (cam_merge_fold): one fp32 buffer
+    // over every tensor, made at the first fold. Open rounds cover disjoint
+    // tensors, so they share it.
+    float* d_sum = nullptr;
+    std::vector<int64_t> sum_off;     // each tensor's offset in d_sum (8-element aligned)
+    std::vector<cudaEvent_t> sum_ev;  // per plan: the last fold or final pass on its tensors
     int32_t* d_status = nullptr;   // device status word (CAM_STATUS_* bits), in dev_block
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
@@ -147,6 +153,8 @@ struct cam_round {
     int dtype = -1;
     std::vector<const void*> x;  // x[k * T_f + l]
     bool host_workers = false;   // some worker came through cam_merge_accumulate_host
+    bool eager = false;          // workers are folded as they arrive (cam_merge_fold)
+    int eager_mode = 0;          // the mode those folds used
     int64_t tokens[CAM_KMAX] = {};
     bool finalized = false;
     int mode = CAM_MODE_MEAN_REPLACE;
@@ -403,10 +411,12 @@ CAM_API void cam_ctx_destroy(cam_ctx* c) {
     if (!c) return;
     for (cam_round* r : c->open) delete r;
     c->open.clear();
-    if (c->dev_block || c->ortho) {
+    if (c->dev_block || c->ortho || c->d_sum) {
         DeviceScope scope(c->device);
         if (c->dev_block) cudaFree(c->dev_block);
         cam::ortho_destroy(c->ortho);
+        if (c->d_sum) cudaFree(c->d_sum);
+        for (cudaEvent_t ev : c->sum_ev) cudaEventDestroy(ev);
     }
     delete c;
 }
@@ -471,6 +481,7 @@ int accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t t
                bool host, const char* fn) {
     if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
     if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
+    if (r->eager) return fail(CAM_E_STATE, "%s: the round folds its workers eagerly", fn);
     if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
     if (dtype != CAM_F32 && dtype != CAM_BF16)
         return fail(CAM_E_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
@@ -518,6 +529,147 @@ CAM_API int cam_merge_accumulate_host(cam_round* r, const void* const* ckpt, cam
     return accumulate(r, ckpt, dtype, tokens, true, "cam_merge_accumulate_host");
 }
 
+namespace {
+
+// Makes the context's running-sum buffer and its per-plan events.
+int ensure_sum(cam_ctx* c, const char* fn) {
+    if (c->d_sum) return CAM_OK;
+    std::vector<int64_t> off(c->n_tensors);
+    int64_t total = 0;
+    for (int32_t t = 0; t < c->n_tensors; ++t) {
+        off[t] = total;
+        total += (c->numel[t] + 7) / 8 * 8;
+    }
+    float* buf = nullptr;
+    cudaError_t ce = cudaMalloc(&buf, sizeof(float) * size_t(std::max<int64_t>(total, 8)));
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CAM_E_NOMEM, "%s: cudaMalloc of the running sums (%lld floats): %s", fn,
+                    static_cast<long long>(total), cudaGetErrorString(ce));
+    }
+    std::vector<cudaEvent_t> ev(c->n_fragments + 1, nullptr);
+    for (cudaEvent_t& e : ev) {
+        ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+        if (ce != cudaSuccess) {
+            for (cudaEvent_t x : ev)
+                if (x) cudaEventDestroy(x);
+            cudaFree(buf);
+            return cuda_fail(ce, "cam_merge_fold: event");
+        }
+    }
+    c->d_sum = buf;
+    c->sum_off.swap(off);
+    c->sum_ev.swap(ev);
+    return CAM_OK;
+}
+
+// Orders stream s after the last fold or final pass that touched any of the
+// round's tensors (its own plan, the whole-list plan, or every fragment's
+// plan for a whole-list round).
+cudaError_t sum_order(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+    cudaError_t ce = cudaSuccess;
+    for (int32_t f = 0; f <= c->n_fragments && ce == cudaSuccess; ++f)
+        if (fragment < 0 || f == fragment || f == c->n_fragments)
+            ce = cudaStreamWaitEvent(s, c->sum_ev[f], 0);
+    return ce;
+}
+
+cudaError_t sum_mark(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+    return cudaEventRecord(c->sum_ev[fragment < 0 ? c->n_fragments : fragment], s);
+}
+
+// Bit l of vec[]: tensor l0 + l of the plan takes the vector path in a
+// launch covering [l0, l0 + n), given its pointers' alignment.
+template <class F>
+void set_vec(uint32_t* vec, int n, F&& ok) {
+    std::fill(vec, vec + cam::kEagerTensors / 32, 0u);
+    for (int l = 0; l < n; ++l)
+        if (ok(l)) vec[l >> 5] |= 1u << (l & 31);
+}
+
+}  // namespace
+
+CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t tokens,
+                           cam_mode mode, void* stream) {
+    const char* fn = "cam_merge_fold";
+    if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
+    if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
+    if (!r->eager && r->K > 0)
+        return fail(CAM_E_STATE, "%s: the round already holds accumulated workers", fn);
+    if (r->ortho) return fail(CAM_E_STATE, "%s: an orthogonalised round needs its workers at commit", fn);
+    if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
+    if (dtype != CAM_F32 && dtype != CAM_BF16)
+        return fail(CAM_E_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
+    if (r->K > 0 && dtype != r->dtype)
+        return fail(CAM_E_ARG, "%s: dtype %d differs from the round's %d", fn,
+                    static_cast<int>(dtype), r->dtype);
+    if (mode != CAM_MODE_MEAN_REPLACE && mode != CAM_MODE_DELTA_NESTEROV)
+        return fail(CAM_E_ARG, "%s: unknown mode %d", fn, static_cast<int>(mode));
+    if (r->eager && mode != r->eager_mode)
+        return fail(CAM_E_ARG, "%s: mode %d differs from the earlier folds' %d", fn,
+                    static_cast<int>(mode), r->eager_mode);
+    if (tokens < 0 || tokens > (int64_t(1) << 56))
+        return fail(CAM_E_ARG, "%s: tokens %lld out of range", fn, static_cast<long long>(tokens));
+    cam_ctx* c = r->ctx;
+    const Plan& p = c->plan_of(r->fragment);
+    const int T = p.n_tensors();
+    if (!ckpt && T > 0) return fail(CAM_E_ARG, "%s: ckpt is NULL", fn);
+    std::vector<const void*> xs(T, nullptr);
+    for (int32_t l = 0; l < T; ++l) {
+        if (c->numel[p.tensors[l]] == 0) continue;
+        if (!ckpt[l]) return fail(CAM_E_ARG, "%s: ckpt[%d] is NULL", fn, l);
+        xs[l] = device_view_of_host(c, ckpt[l]);
+        if (!xs[l])
+            return fail(CAM_E_ARG, "%s: ckpt[%d] is memory the GPU cannot read", fn, l);
+    }
+    DeviceScope scope(c->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_merge_fold: cudaSetDevice");
+    int rc = ensure_sum(c, fn);
+    if (rc != CAM_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t ce = sum_order(c, r->fragment, s);
+    const int k = r->K;
+    const uintptr_t xa = dtype == CAM_F32 ? 32 : 16;
+    const bool wd = r->worker_norms;
+    cam::FoldArgs a;
+    a.slots = p.d_slots;
+    a.k = k;
+    a.first = k == 0;
+    a.w = static_cast<float>(tokens);
+    int64_t launched = 0;
+    for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += cam::kEagerTensors) {
+        const int n = std::min(cam::kEagerTensors, T - l0);
+        const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
+        if (c1 == c0) continue;
+        for (int l = 0; l < n; ++l) {
+            const int32_t g = p.tensors[l0 + l];
+            a.x[l] = xs[l0 + l];
+            a.sum[l] = c->d_sum + c->sum_off[g];
+        }
+        set_vec(a.vec, n, [&](int l) {
+            const int32_t g = p.tensors[l0 + l];
+            return aligned(a.x[l], xa) && aligned(c->theta[g], 32);
+        });
+        a.chunks = p.d_chunks + c0;
+        a.worker_partials = wd ? p.d_worker_partials + static_cast<int64_t>(c0) * CAM_KMAX : nullptr;
+        a.n_chunks = c1 - c0;
+        a.local0 = l0;
+        a.n_local = n;
+        const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * 2));
+        ce = cam::launch_fold(a, dtype, mode, wd, grid, s);
+        ++launched;
+    }
+    if (ce == cudaSuccess) ce = sum_mark(c, r->fragment, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_fold: launch");
+    c->launches += launched;
+    r->eager = true;
+    r->eager_mode = mode;
+    r->tokens[k] = tokens;
+    r->dtype = dtype;
+    ++r->K;
+    return CAM_OK;
+}
+
 CAM_API int cam_merge_finalize(cam_round* r, cam_mode mode, float lr, float mu) {
     if (!r) return fail(CAM_E_ARG, "cam_merge_finalize: round is NULL");
     if (r->finalized) return fail(CAM_E_STATE, "cam_merge_finalize: finalized twice");
@@ -527,6 +679,9 @@ CAM_API int cam_merge_finalize(cam_round* r, cam_mode mode, float lr, float mu) 
         return fail(CAM_E_ARG, "cam_merge_finalize: lr and mu must be finite");
     if (mode == CAM_MODE_DELTA_NESTEROV && !r->ctx->has_m)
         return fail(CAM_E_ARG, "cam_merge_finalize: Nesterov needs momentum buffers");
+    if (r->eager && mode != r->eager_mode)
+        return fail(CAM_E_STATE, "cam_merge_finalize: mode %d differs from the folds' mode %d",
+                    static_cast<int>(mode), r->eager_mode);
     r->finalized = true;
     r->mode = mode;
     r->lr = lr;
@@ -547,6 +702,9 @@ CAM_API int cam_ema_update(cam_round* r, float beta) {
 CAM_API int cam_worker_drift_norm(cam_round* r, double* per_worker_tensor, double* per_worker) {
     if (!r) return fail(CAM_E_ARG, "cam_worker_drift_norm: round is NULL");
     if (r->worker_norms) return fail(CAM_E_STATE, "cam_worker_drift_norm: asked twice");
+    if (r->eager)
+        return fail(CAM_E_STATE,
+                    "cam_worker_drift_norm: ask before the first fold (each fold computes its own)");
     if (!per_worker_tensor && !per_worker)
         return fail(CAM_E_ARG, "cam_worker_drift_norm: both outputs NULL");
     r->worker_norms = true;
@@ -560,6 +718,7 @@ CAM_API int cam_merge_orthogonalize(cam_round* r, float lr, int32_t scale_mode, 
     const char* fn = "cam_merge_orthogonalize";
     if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
     if (r->ortho) return fail(CAM_E_STATE, "%s: asked twice", fn);
+    if (r->eager) return fail(CAM_E_STATE, "%s: needs the workers at commit, not folded", fn);
     if (!std::isfinite(lr)) return fail(CAM_E_ARG, "%s: lr must be finite", fn);
     if (scale_mode != CAM_ORTHO_SCALE_FIXED && scale_mode != CAM_ORTHO_SCALE_MATCH_NORM)
         return fail(CAM_E_ARG, "%s: unknown scale mode %d", fn, scale_mode);
@@ -768,7 +927,47 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             ++c->launches;
         }
     };
-    if (!r->ortho) {
+    // Final pass of an eagerly folded round: from the running sums.
+    auto launch_final = [&]() {
+        ce = sum_order(c, r->fragment, s);
+        cam::FinalArgs fa;
+        fa.slots = p.d_slots;
+        fa.K = K;
+        fa.Kf = a.Kf;
+        fa.W = a.W;
+        fa.lr = a.lr;
+        fa.mu = a.mu;
+        fa.beta = a.beta;
+        fa.swa_n = a.swa_n;
+        for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += cam::kEagerTensors) {
+            const int n = std::min(cam::kEagerTensors, T - l0);
+            const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
+            if (c1 == c0) continue;
+            for (int l = 0; l < n; ++l) {
+                const int32_t g = p.tensors[l0 + l];
+                fa.sum[l] = c->d_sum + c->sum_off[g];
+                fa.pub[2 * l] = r->publish ? r->pub_theta[l0 + l] : nullptr;
+                fa.pub[2 * l + 1] = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
+            }
+            set_vec(fa.vec, n, [&](int l) {
+                const int32_t g = p.tensors[l0 + l];
+                return aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
+                       (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32)) &&
+                       aligned(fa.pub[2 * l], 32) && aligned(fa.pub[2 * l + 1], 32);
+            });
+            fa.chunks = p.d_chunks + c0;
+            fa.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
+            fa.n_chunks = c1 - c0;
+            fa.local0 = l0;
+            fa.n_local = n;
+            const int grid = static_cast<int>(std::min<int64_t>(fa.n_chunks, int64_t(c->sm_count) * 2));
+            ce = cam::launch_final(fa, r->mode, r->ema, norm_level >= 1, r->publish, r->swa, grid, s);
+            ++c->launches;
+        }
+    };
+    if (r->eager) {
+        launch_final();
+    } else if (!r->ortho) {
         launch_range(0, T);
     } else {
         // the vectors and other non-matrix tensors take the fused pass ...
@@ -828,6 +1027,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }
+    if (ce == cudaSuccess && r->eager) ce = sum_mark(c, r->fragment, s);  // the sums were read
     if (ce == cudaSuccess && r->swa)
         for (int32_t g : p.tensors) c->swa_count[g] = swa_prev + 1;
     close_round(r);

@@ -179,6 +179,44 @@ int cam_merge_accumulate_host(cam_round* rd, const void* const* ckpt, cam_dtype 
                               int64_t tokens);
 
 /*
+ * Folds one arriving worker into the round at once ("DiffuRefill-1B" model
+ * card, "How it is trained", Merging: each checkpoint is added to the running
+ * fp32 sum as it comes in). ckpt holds the worker's T_f tensors in fragment
+ * order, in device memory or in host memory the device can read (as for
+ * cam_merge_accumulate_host). The fold runs on `stream` (a cudaStream_t, NULL
+ * for the default stream):
+ *
+ * - MEAN_REPLACE: s <- s + x_k;
+ * - DELTA_NESTEROV: s <- s + w_k * (x_k - theta);
+ *
+ * with s an fp32 running sum that starts at +0 with the first fold. The
+ * buffers are borrowed only until this fold has run on `stream`, not until
+ * commit.
+ *
+ * A round is either folded or accumulated:
+ *
+ * - every fold of a round uses the same mode and dtype;
+ * - cam_merge_finalize must later name that mode;
+ * - per-worker drift (cam_worker_drift_norm) must be asked for before the
+ *   first fold;
+ * - orthogonalisation is not available.
+ *
+ * Successive folds of a round may use different streams; the library orders
+ * them, and the commit, after one another. cam_merge_commit then runs one
+ * pass over the sums instead of over the workers. Per element, every
+ * operation and its order are those of an accumulated round, so the results
+ * are the same bits.
+ *
+ * The first fold of a context allocates one fp32 buffer as large as the
+ * whole tensor list (CAM_E_NOMEM if it cannot).
+ *
+ * Errors: CAM_E_ARG, CAM_E_STATE (finalized, accumulated, or orthogonalised
+ * round), CAM_E_KMAX, CAM_E_NOMEM, CAM_E_CUDA.
+ */
+int cam_merge_fold(cam_round* rd, const void* const* ckpt, cam_dtype dtype, int64_t tokens,
+                   cam_mode mode, void* stream);
+
+/*
  * Chooses the outer step. MEAN_REPLACE ignores lr, mu and the token counts.
  * DELTA_NESTEROV needs momentum buffers. lr and mu must be finite.
  * Errors: CAM_E_ARG, CAM_E_STATE (finalized twice).

@@ -85,6 +85,7 @@ def test_null_handles_rejected():
     lib = B.lib()
     assert lib.cam_merge_begin(None, 0, 0, None) == B.E_ARG
     assert lib.cam_merge_accumulate(None, None, 0, 0) == B.E_ARG
+    assert lib.cam_merge_fold(None, None, 0, 0, 0, None) == B.E_ARG
     assert lib.cam_merge_finalize(None, 0, 1.0, 0.0) == B.E_ARG
     assert lib.cam_ema_update(None, 0.9) == B.E_ARG
     assert lib.cam_drift_norm(None, None, None) == B.E_ARG

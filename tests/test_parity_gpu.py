@@ -1081,3 +1081,173 @@ def test_short_side_flag_is_validated():
     rd.orthogonalize(0.1, B.ORTHO_SCALE_FIXED, B.ORTHO_FP32 | B.ORTHO_SHORT_SIDE, 10)
     rd.abort()
     mg.close()
+
+
+# ---- eagerly folded rounds (cam_merge_fold) ----------------------------------------
+
+def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=None):
+    rd = st.merger.begin(rnd, -1)
+    code = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
+    T = len(rd.tensors)
+    out = {}
+    if wnorms:
+        out["pwt"] = torch.full((len(draw.included) * T,), -1.0, dtype=torch.float64, device=DEV)
+        out["pw"] = torch.full((len(draw.included),), -1.0, dtype=torch.float64, device=DEV)
+        rd.worker_drift_norm(out["pwt"], out["pw"])
+    for i, k in enumerate(draw.included):
+        s = None if streams is None else streams[i % len(streams)]
+        if streams is None:
+            rd.accumulate(workers[k].views, draw.tokens[k])
+        else:
+            rd.fold(workers[k].views, draw.tokens[k], code, stream=s)
+    rd.finalize(code, wl.lr, wl.mu)
+    if wl.ema_beta is not None:
+        rd.ema_update(wl.ema_beta)
+    if wl.swa:
+        rd.swa_update()
+    if norms:
+        out["pt"] = torch.full((T,), -1.0, dtype=torch.float64, device=DEV)
+        out["pf"] = torch.full((1,), -1.0, dtype=torch.float64, device=DEV)
+        rd.drift_norm(out["pt"], out["pf"])
+    if publish:
+        out["th_pub"] = [torch.full_like(v, float("nan")) for v in st.theta.views]
+        out["e_pub"] = ([torch.full_like(v, float("nan")) for v in st.e.views]
+                        if st.e is not None else None)
+        rd.publish(out["th_pub"], out["e_pub"])
+    rd.commit()
+    return out
+
+
+@pytest.mark.parametrize("mode,dtype,ema,swa,norms,wnorms,publish,host", [
+    ("mean", "f32", True, False, False, False, False, False),
+    ("mean", "bf16", True, True, True, True, True, False),
+    ("delta", "bf16", False, False, True, True, False, False),
+    ("delta", "f32", True, False, True, False, True, True),   # pinned host workers
+    ("mean", "f32", False, True, True, False, False, True),
+])
+def test_folded_round_equals_accumulated_round_bitwise(mode, dtype, ema, swa, norms, wnorms,
+                                                       publish, host):
+    wl = dataclasses.replace(
+        _custom(STAGED_SIZES, K=4, mode=mode, dtype=dtype, ema=ema, norms=norms, n_masked=1,
+                rounds=((0, -1), (1, -1))), swa=swa)
+    g = W.make_global(wl, 4, DEV)
+    acc, fold = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    ost = oracle_state_from(g, wl)
+    for idx, (rnd, _) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, 4)
+        workers = [W.make_worker(wl, g, rnd, k, 4, DEV) for k in range(wl.K)]
+        if host:
+            workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
+        oa = _fold_round(acc, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish)
+        of = _fold_round(fold, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish,
+                         streams=[torch.cuda.current_stream()])
+        oracle_round(ost, wl, rnd, -1, workers, draw)
+        torch.cuda.synchronize()
+        for name in ("theta", "m", "e", "swa"):
+            x, y = getattr(acc, name), getattr(fold, name)
+            if x is not None:
+                assert torch.equal(x.flat.view(torch.int32), y.flat.view(torch.int32)), \
+                    f"round {rnd}: {name} differs between folded and accumulated"
+        compare_full(fold, ost, f"folded round {rnd}")
+        if publish:
+            for t, v in enumerate(fold.theta.views):
+                assert torch.equal(of["th_pub"][t].view(torch.int32), v.view(torch.int32))
+                if fold.e is not None:
+                    assert torch.equal(of["e_pub"][t].view(torch.int32), fold.e.views[t].view(torch.int32))
+        for key in ("pt", "pf", "pwt", "pw"):
+            if key in oa:
+                x, y = of[key].cpu().numpy(), oa[key].cpu().numpy()
+                assert (x >= 0).all(), f"{key}: norm not written"
+                assert np.all(np.abs(x - y) <= NORM_RTOL * np.abs(y) + 1e-300), f"{key}: {x} vs {y}"
+    for st in (acc, fold):
+        assert st.merger.status() == 0
+        st.merger.close()
+
+
+def test_folds_on_several_streams_are_ordered():
+    wl = _custom([1 << 20, 4097, 33], K=5, mode="delta", dtype="bf16", ema=True)
+    g = W.make_global(wl, 6, DEV)
+    draw = W.draw_round(wl, 0, 6)
+    workers = [W.make_worker(wl, g, 0, k, 6, DEV) for k in range(wl.K)]
+    seq, par = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    _fold_round(seq, wl, 0, workers, draw, norms=True, wnorms=False, publish=False,
+                streams=[torch.cuda.current_stream()])
+    _fold_round(par, wl, 0, workers, draw, norms=True, wnorms=False, publish=False, streams=streams)
+    torch.cuda.synchronize()
+    for name in ("theta", "m", "e"):
+        assert torch.equal(getattr(seq, name).flat.view(torch.int32), getattr(par, name).flat.view(torch.int32))
+    seq.merger.close()
+    par.merger.close()
+
+
+def test_worker_buffers_are_free_once_their_fold_has_run():
+    wl = _custom([100_003, 2048], K=3, mode="mean", dtype="f32", ema=True, norms=False)
+    g = W.make_global(wl, 8, DEV)
+    draw = W.draw_round(wl, 0, 8)
+    workers = [W.make_worker(wl, g, 0, k, 8, DEV) for k in range(wl.K)]
+    want = oracle_state_from(g, wl)
+    oracle_round(want, wl, 0, -1, workers, draw)
+    st = make_gpu_state(wl, g, DEV)
+    rd = st.merger.begin(0)
+    for k in draw.included:
+        rd.fold(workers[k].views, 0, B.MEAN_REPLACE)
+        torch.cuda.synchronize()
+        workers[k].flat.fill_(float("nan"))  # the fold has read it: the buffer may be reused
+    rd.finalize(B.MEAN_REPLACE)
+    rd.ema_update(0.9)
+    rd.commit()
+    compare_full(st, want, "folded round with reused worker buffers", bitwise=True)
+    st.merger.close()
+
+
+def test_fold_rules():
+    th = [torch.zeros(4096, device=DEV)]
+    m = [torch.zeros(4096, device=DEV)]
+    mg = B.Merger(th, momentum=m, quorum=1)
+    x = [torch.ones(4096, device=DEV)]
+    rd = mg.begin(0)
+    rd.accumulate(x, 1)
+    with pytest.raises(B.StateError):          # accumulated, then folded
+        rd.fold(x, 1, B.MEAN_REPLACE)
+    rd.abort()
+    rd = mg.begin(1)
+    rd.fold(x, 1, B.DELTA_NESTEROV)
+    with pytest.raises(B.StateError):          # folded, then accumulated
+        rd.accumulate(x, 1)
+    with pytest.raises(B.ArgError):            # another mode than the earlier folds
+        rd.fold(x, 1, B.MEAN_REPLACE)
+    with pytest.raises(B.StateError):          # per-worker drift after the first fold
+        rd.worker_drift_norm(torch.zeros(1, dtype=torch.float64, device=DEV), None)
+    with pytest.raises(B.StateError):          # orthogonalisation needs the workers at commit
+        rd.orthogonalize(0.1)
+    with pytest.raises(B.StateError):          # finalize with another mode
+        rd.finalize(B.MEAN_REPLACE)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    with pytest.raises(B.StateError):          # fold after finalize
+        rd.fold(x, 1, B.DELTA_NESTEROV)
+    rd.commit()
+    torch.cuda.synchronize()
+    assert mg.status() == 0
+    mg.close()
+
+
+def test_abort_after_folds_then_a_fresh_round():
+    wl = _custom([50_000, 7], K=3, mode="mean", dtype="bf16", ema=False, norms=True)
+    g = W.make_global(wl, 12, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    junk = [W.make_worker(wl, g, 9, k, 99, DEV) for k in range(2)]
+    rd = st.merger.begin(0)
+    for w in junk:
+        rd.fold(w.views, 0, B.MEAN_REPLACE)
+    rd.abort()
+    draw = W.draw_round(wl, 0, 12)
+    workers = [W.make_worker(wl, g, 1, k, 12, DEV) for k in range(wl.K)]
+    want = oracle_state_from(g, wl)
+    oracle_round(want, wl, 1, -1, workers, draw)
+    _fold_round(st, wl, 1, workers, draw, norms=False, wnorms=False, publish=False,
+                streams=[torch.cuda.current_stream()])
+    compare_full(st, want, "fresh folded round after an abort", bitwise=True)
+    st.merger.close()
