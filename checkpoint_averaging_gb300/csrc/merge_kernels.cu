@@ -29,6 +29,7 @@
 
 #include "cam_internal.h"
 #include "merge_device.cuh"
+#include "norm_device.cuh"
 
 namespace cam {
 namespace {
@@ -40,18 +41,15 @@ __global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
     const int warp = threadIdx.x >> 5;
     const int n_warps = blockDim.x >> 5;
     for (int t = warp; t < a.n_tensors; t += n_warps) {
-        double s = 0.0;
-        for (int c = a.first_chunk[t] + lane; c < a.first_chunk[t + 1]; c += 32)
-            s += a.partials[c];
+        double s = lane_sum(a.partials, 1, a.first_chunk[t], a.first_chunk[t + 1], lane);
         s = warp_sum(s);
         if (lane == 0) a.tsq[t] = s;
     }
     // per worker and tensor: one warp per (tensor, worker) pair
     for (int p = warp; p < a.n_tensors * a.K; p += n_warps) {
         const int t = p / a.K, k = p % a.K;
-        double s = 0.0;
-        for (int c = a.first_chunk[t] + lane; c < a.first_chunk[t + 1]; c += 32)
-            s += a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + k];
+        double s = lane_sum(a.worker_partials + k, CAM_KMAX, a.first_chunk[t], a.first_chunk[t + 1],
+                            lane);
         s = warp_sum(s);
         if (lane == 0) a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k] = s;
     }

@@ -18,6 +18,7 @@
 
 #include "cam_internal.h"
 #include "merge_device.cuh"
+#include "norm_device.cuh"
 
 #define CAM_API extern "C" __attribute__((visibility("default")))
 
@@ -120,8 +121,7 @@ __global__ void __launch_bounds__(1024) norm_finish_noalloc(const __grid_constan
     const int warp = threadIdx.x >> 5;
     const int n_warps = blockDim.x >> 5;
     for (int t = warp; t < a.n_tensors; t += n_warps) {
-        double s = 0.0;
-        for (int c = a.first_chunk[t] + lane; c < a.first_chunk[t + 1]; c += 32) s += a.partials[c];
+        double s = lane_sum(a.partials, 1, a.first_chunk[t], a.first_chunk[t + 1], lane);
         s = warp_sum(s);
         if (lane == 0) a.tsq[t] = s;
     }
