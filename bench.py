@@ -449,12 +449,14 @@ def run_ours(args, wl, ws, rank, local) -> int:
     per_round = [round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl)]
     big = max(range(len(per_round)), key=per_round.__getitem__)
     if n_streams > 1:
-        kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for a, b in group_pairs)
+        launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
+        kern_s = statistics.mean(launch_s)
         launch_bytes = step_bytes
         kernel_desc = f"{kernel} x{len(wl.rounds)} concurrent on {n_streams} streams"
     else:
-        kern_s = statistics.mean(a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
-                                 if i % len(wl.rounds) == big)
+        launch_s = [a.elapsed_time(b) / 1e3 for i, (a, b) in enumerate(ev_pairs)
+                    if i % len(wl.rounds) == big]
+        kern_s = statistics.mean(launch_s)
         launch_bytes = per_round[big]
         kernel_desc = kernel
     peaks = measured_peaks()
@@ -496,6 +498,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_src, "traffic": traffic,
                          "kernel": kernel_desc, "kernel_ms": round(kern_s * 1e3, 4),
+                         "kernel_ms_median": round(statistics.median(launch_s) * 1e3, 4),
+                         "kernel_ms_best": round(min(launch_s) * 1e3, 4),
                          "algorithmic_bytes_per_launch": launch_bytes},
             "clocks": ck,
             "e2e": e2e,
