@@ -23,6 +23,8 @@ F32, BF16 = 0, 1
 MEAN_REPLACE, DELTA_NESTEROV = 0, 1
 INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
 NO_STAGING = 8
+TIME_COMMITS = 16
+FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
 ORTHO_TF32, ORTHO_FP32 = 0, 1
@@ -91,6 +93,13 @@ class CtxDesc(ctypes.Structure):
 
 _lib = None
 
+class CommitRecord(ctypes.Structure):
+    """cam_commit_record: what the last commit did."""
+    _fields_ = [("round", ctypes.c_int64), ("fragment", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("form", ctypes.c_int32), ("elements", ctypes.c_int64),
+                ("bytes", ctypes.c_int64), ("launches", ctypes.c_int64), ("ms", ctypes.c_float)]
+
+
 EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_accumulate",
            "cam_merge_accumulate_host", "cam_merge_fold", "cam_merge_publish",
            "cam_swa_update", "cam_swa_reset", "cam_worker_drift_norm", "cam_adopt_keep_drift",
@@ -98,7 +107,7 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
-           "cam_ctx_staged_count", "cam_merge_round_noalloc", "cam_last_error", "cam_version")
+           "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_merge_round_noalloc", "cam_last_error", "cam_version")
 
 NOALLOC_MAX_TENSORS = 4096
 NOALLOC_MAX_CHUNKS = 131072
@@ -143,6 +152,7 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_ctx_status.argtypes = [vp, ctypes.POINTER(i32)]
     L.cam_ctx_staged_count.argtypes = [vp, ctypes.POINTER(i64)]
+    L.cam_ctx_last_commit.argtypes = [vp, ctypes.POINTER(CommitRecord)]
     L.cam_merge_round_noalloc.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, i32, vpp,
                                           ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, i32, ctypes.c_float,
@@ -303,6 +313,12 @@ def ctx_launch_count(ctx: int) -> int:
     return out.value
 
 
+def ctx_last_commit(ctx: int) -> dict:
+    rec = CommitRecord()
+    _check(lib().cam_ctx_last_commit(ctx, ctypes.byref(rec)))
+    return {name: getattr(rec, name) for name, _ in CommitRecord._fields_}
+
+
 def ctx_staged_count(ctx: int) -> int:
     out = ctypes.c_int64()
     _check(lib().cam_ctx_staged_count(ctx, ctypes.byref(out)))
@@ -417,11 +433,12 @@ class Merger:
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
                  zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
-                 staging=True):
+                 staging=True, time_commits=False):
         """rows: optional per-tensor matrix rows (default: the tensors' first
         dimension), used by orthogonalised rounds. staging=False keeps every
         merge pass on the register form (the staged form gives the same
-        results)."""
+        results). time_commits=True times each commit's device work
+        (last_commit()["ms"])."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -447,7 +464,7 @@ class Merger:
         self.n_fragments = n_fragments
         flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
                 (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
-                (0 if staging else NO_STAGING)
+                (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,
@@ -503,6 +520,11 @@ class Merger:
     @property
     def launch_count(self) -> int:
         return ctx_launch_count(self.ctx)
+
+    def last_commit(self) -> dict:
+        """The record of the last commit (round, fragment, K, mode, form,
+        elements, bytes, launches, ms); waits for its work when timed."""
+        return ctx_last_commit(self.ctx)
 
     @property
     def staged_count(self) -> int:

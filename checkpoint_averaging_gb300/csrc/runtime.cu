@@ -29,6 +29,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "cam_internal.h"
 
 #define CAM_API extern "C" __attribute__((visibility("default")))
@@ -71,6 +73,14 @@ struct DeviceScope {
 };
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// An NVTX range for profilers (a no-op unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* label) { nvtxRangePushA(label); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace
 
@@ -122,6 +132,10 @@ struct cam_ctx {
     }
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     bool staged = true;            // the staged form of the merge pass may be used
+    bool time_commits = false;     // CAM_TIME_COMMITS: events around each commit
+    cudaEvent_t commit_ev[2] = {nullptr, nullptr};
+    cam_commit_record last_commit{};
+    bool has_last_commit = false;
     // Running sums of eagerly folded rounds (cam_merge_fold): one fp32 buffer
     // over every tensor, made at the first fold. Open rounds cover disjoint
     // tensors, so they share it.
@@ -216,7 +230,7 @@ int validate_desc(const cam_ctx_desc* d) {
         return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
     if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
-                     CAM_NO_STAGING))
+                     CAM_NO_STAGING | CAM_TIME_COMMITS))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -375,6 +389,15 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
                                        dt, md, em != 0, nl, pb != 0, sw != 0}));
 
     c->staged = !(d->flags & CAM_NO_STAGING);
+    c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
+    for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
+        ce = cudaEventCreate(&c->commit_ev[i]);
+    if (ce != cudaSuccess) {
+        for (cudaEvent_t& ev : c->commit_ev)
+            if (ev) cudaEventDestroy(ev);
+        cudaFree(c->dev_block);
+        return cuda_fail(ce, "cam_ctx_create: commit events");
+    }
     if (c->staged) {
         ce = cam::staged_prepare();
         if (ce != cudaSuccess) {
@@ -417,6 +440,8 @@ CAM_API void cam_ctx_destroy(cam_ctx* c) {
         cam::ortho_destroy(c->ortho);
         if (c->d_sum) cudaFree(c->d_sum);
         for (cudaEvent_t ev : c->sum_ev) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : c->commit_ev)
+            if (ev) cudaEventDestroy(ev);
     }
     delete c;
 }
@@ -624,6 +649,10 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     }
     DeviceScope scope(c->device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_merge_fold: cudaSetDevice");
+    char label[80];
+    std::snprintf(label, sizeof label, "cam_merge_fold round %lld worker %d",
+                  static_cast<long long>(r->round), r->K);
+    NvtxRange nvtx(label);
     int rc = ensure_sum(c, fn);
     if (rc != CAM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -866,6 +895,12 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         }
     }
     cudaError_t ce = cudaSuccess;
+    char label[96];
+    std::snprintf(label, sizeof label, "cam_merge_commit round %lld fragment %d K %d",
+                  static_cast<long long>(r->round), r->fragment, K);
+    NvtxRange nvtx(label);
+    const int64_t launches0 = c->launches, staged0 = c->staged_launches;
+    if (c->time_commits) ce = cudaEventRecord(c->commit_ev[0], s);
     const int per_launch = cam::kXCap / stride;
     // The staged form: a ring of as many stages as fit (at least 2, at most
     // kStMaxStages), for launches whose workers are device memory.
@@ -1028,6 +1063,26 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ++c->launches;
     }
     if (ce == cudaSuccess && r->eager) ce = sum_mark(c, r->fragment, s);  // the sums were read
+    if (ce == cudaSuccess && c->time_commits) ce = cudaEventRecord(c->commit_ev[1], s);
+    if (ce == cudaSuccess) {
+        cam_commit_record& rec = c->last_commit;
+        rec.round = r->round;
+        rec.fragment = r->fragment;
+        rec.K = K;
+        rec.mode = r->mode;
+        rec.form = r->eager ? CAM_FORM_FOLDED
+                 : r->ortho ? CAM_FORM_ORTHO
+                            : (c->staged_launches > staged0 ? CAM_FORM_STAGED : CAM_FORM_REGISTER);
+        rec.elements = p.n_elems;
+        const int64_t xb = r->dtype == CAM_BF16 ? 2 : 4;
+        const int64_t per = (r->eager ? 4 : K * xb) + 4 + ((delta || norm_level >= 1) ? 4 : 0) +
+                            (delta ? 8 : 0) + (r->ema ? 8 : 0) + (r->swa ? 8 : 0) +
+                            (r->publish ? 4 : 0) + (r->publish_ema ? 4 : 0);
+        rec.bytes = r->ortho ? 0 : per * p.n_elems;
+        rec.launches = c->launches - launches0;
+        rec.ms = -1.0f;
+        c->has_last_commit = true;
+    }
     if (ce == cudaSuccess && r->swa)
         for (int32_t g : p.tensors) c->swa_count[g] = swa_prev + 1;
     close_round(r);
@@ -1101,6 +1156,22 @@ CAM_API int cam_ctx_status(cam_ctx* c, int32_t* out) {
     if (ce == cudaSuccess) ce = cudaMemcpy(&v, c->d_status, sizeof v, cudaMemcpyDeviceToHost);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_status");
     *out = v;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_last_commit(cam_ctx* c, cam_commit_record* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_last_commit: NULL argument");
+    if (!c->has_last_commit) return fail(CAM_E_ARG, "cam_ctx_last_commit: no commit yet");
+    *out = c->last_commit;
+    if (c->time_commits) {
+        DeviceScope scope(c->device);
+        float ms = 0.0f;
+        cudaError_t ce = scope.err;
+        if (ce == cudaSuccess) ce = cudaEventSynchronize(c->commit_ev[1]);
+        if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, c->commit_ev[0], c->commit_ev[1]);
+        if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_last_commit");
+        out->ms = ms;
+    }
     return CAM_OK;
 }
 

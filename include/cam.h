@@ -79,6 +79,7 @@ typedef enum {
 #define CAM_INIT_ZERO_MOMENTUM 2u   /* at create: m <- 0 */
 #define CAM_INIT_ZERO_SWA 4u        /* at create: running averages <- 0, no globals folded */
 #define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
+#define CAM_TIME_COMMITS 16u        /* time each commit's device work (cam_ctx_last_commit) */
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
@@ -374,6 +375,43 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * Errors: CAM_E_ARG, CAM_E_CUDA.
  */
 int cam_ctx_status(cam_ctx* ctx, int32_t* out);
+
+/* What the last successful cam_merge_commit of a context did. */
+typedef struct {
+    int64_t round;
+    int32_t fragment;   /* -1: every tensor */
+    int32_t K;          /* workers merged */
+    int32_t mode;       /* cam_mode */
+    int32_t form;       /* CAM_FORM_* of the merge pass */
+    int64_t elements;   /* elements of the round's tensors */
+    int64_t bytes;      /* algorithmic bytes of the merge pass (0 for orthogonalised rounds) */
+    int64_t launches;   /* kernels the commit launched */
+    float ms;           /* device time of the commit's work, or -1 without CAM_TIME_COMMITS */
+} cam_commit_record;
+
+#define CAM_FORM_REGISTER 0 /* the register form of the merge pass */
+#define CAM_FORM_STAGED 1   /* the staged (bulk-copy) form */
+#define CAM_FORM_FOLDED 2   /* the final pass of an eagerly folded round */
+#define CAM_FORM_ORTHO 3    /* an orthogonalised round */
+
+/*
+ * Copies the record of the context's last successful commit to *out. The
+ * algorithmic bytes count every byte the pass must move once:
+ *
+ * - per element, K worker elements (4 B fp32, 2 B bf16), or the 4-byte
+ *   running sum of a folded round;
+ * - theta written (4 B), and read (4 B) in delta mode or with drift norms;
+ * - m read and written (8 B) in delta mode;
+ * - e read and written (8 B) with an EMA update;
+ * - the running average read and written (8 B);
+ * - 4 B for each published copy.
+ *
+ * With CAM_TIME_COMMITS, ms is the device time between events recorded
+ * before the commit's first launch and after its last; the call then waits
+ * for that commit to finish. Errors: CAM_E_ARG (NULL, or no commit yet),
+ * CAM_E_CUDA.
+ */
+int cam_ctx_last_commit(cam_ctx* ctx, cam_commit_record* out);
 
 /* Merge passes this context has launched in the staged form (a subset of
  * cam_ctx_launch_count), so a caller can tell which form a round took. */

@@ -58,7 +58,7 @@ def test_version():
     (dict(n_fragments=0), "n_fragments"),
     (dict(fragment_of=[3], n_fragments=2), "fragment_of"),
     (dict(device=-1), "device"),
-    (dict(flags=16), "flags"),
+    (dict(flags=32), "flags"),
     (dict(flags=B.INIT_EMA_FROM_MASTER), "EMA"),
     (dict(flags=B.INIT_ZERO_MOMENTUM), "momentum"),
 ])
@@ -93,6 +93,7 @@ def test_null_handles_rejected():
     assert lib.cam_merge_abort(None) == B.E_ARG
     assert lib.cam_ctx_status(None, None) == B.E_ARG
     assert lib.cam_ctx_staged_count(None, None) == B.E_ARG
+    assert lib.cam_ctx_last_commit(None, None) == B.E_ARG
     assert "NULL" in B.last_error()
     lib.cam_ctx_destroy(None)  # no-op
 
@@ -101,7 +102,7 @@ def test_null_handles_rejected():
 def test_no_staging_flag_is_a_valid_description():
     # the description passes validation; only the missing device stops it
     with pytest.raises(B.CudaError):
-        B.ctx_create([16], [0x10000], flags=B.NO_STAGING)
+        B.ctx_create([16], [0x10000], flags=B.NO_STAGING | B.TIME_COMMITS)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the GPU-less failure")

@@ -1251,3 +1251,46 @@ def test_abort_after_folds_then_a_fresh_round():
                 streams=[torch.cuda.current_stream()])
     compare_full(st, want, "fresh folded round after an abort", bitwise=True)
     st.merger.close()
+
+
+def test_commit_record():
+    sizes = [70_001, 2048, 5]
+    n = sum(sizes)
+    th = [torch.randn(k, device=DEV) * 0.02 for k in sizes]
+    m = [torch.zeros(k, device=DEV) for k in sizes]
+    e = [t.clone() for t in th]
+    sw = [torch.zeros(k, device=DEV) for k in sizes]
+    mg = B.Merger(th, momentum=m, ema=e, swa=sw, quorum=1, time_commits=True)
+    xs = [[(t + 1e-3 * torch.randn_like(t)).to(torch.bfloat16) for t in th] for _ in range(3)]
+
+    rd = mg.begin(0)                    # Nesterov + norms: theta, m written -> staged
+    for x in xs:
+        rd.accumulate(x, 1000)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.drift_norm(torch.zeros(3, dtype=torch.float64, device=DEV), None)
+    rd.commit()
+    rec = mg.last_commit()
+    assert (rec["round"], rec["fragment"], rec["K"], rec["mode"]) == (0, -1, 3, B.DELTA_NESTEROV)
+    assert rec["form"] == B.FORM_STAGED and rec["elements"] == n
+    assert rec["bytes"] == (3 * 2 + 4 + 4 + 8) * n and rec["launches"] == 2 and rec["ms"] > 0
+
+    rd = mg.begin(1)                    # the same, folded
+    for x in xs:
+        rd.fold(x, 1000, B.DELTA_NESTEROV)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.commit()
+    rec = mg.last_commit()
+    assert rec["form"] == B.FORM_FOLDED and rec["bytes"] == (4 + 4 + 4 + 8) * n
+    assert rec["launches"] == 1 and rec["ms"] > 0
+
+    rd = mg.begin(2)                    # mean + EMA + running average: three arrays written
+    for x in xs:
+        rd.accumulate(x)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.ema_update(0.9)
+    rd.swa_update()
+    rd.commit()
+    rec = mg.last_commit()
+    assert rec["form"] == B.FORM_REGISTER and rec["bytes"] == (3 * 2 + 4 + 8 + 8) * n
+    assert mg.status() == 0
+    mg.close()
