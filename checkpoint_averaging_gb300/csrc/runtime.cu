@@ -219,6 +219,28 @@ void build_plan(Plan& p, const cam_ctx& c, int32_t fragment) {
     }
 }
 
+// The invariants every kernel's indexing rests on, checked once on the host
+// where the tables are made: each tensor's chunks lie inside it, in order,
+// without gaps or overlap; chunk starts are multiples of the chunk quantum
+// (so vectors stay aligned); first_chunk indexes them.
+bool check_plan(const Plan& p, const cam_ctx& c) {
+    if (p.first_chunk.size() != p.tensors.size() + 1 || p.first_chunk[0] != 0) return false;
+    if (p.chunk_elems <= 0 || p.chunk_elems % cam::kChunkQuantum != 0) return false;
+    for (int32_t l = 0; l < p.n_tensors(); ++l) {
+        const int64_t n = c.numel[p.tensors[l]];
+        int64_t next = 0;
+        for (int32_t q = p.first_chunk[l]; q < p.first_chunk[l + 1]; ++q) {
+            const ChunkDesc& ch = p.chunks[q];
+            if (ch.local != l || ch.start != next || ch.len <= 0 || ch.len > p.chunk_elems ||
+                ch.start % cam::kChunkQuantum != 0)
+                return false;
+            next = ch.start + ch.len;
+        }
+        if (next != n) return false;
+    }
+    return p.first_chunk.back() == p.n_chunks();
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int validate_desc(const cam_ctx_desc* d) {
@@ -329,6 +351,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     for (int32_t f = 0; f <= c->n_fragments; ++f) {
         Plan& p = c->plans[f];
         build_plan(p, *c, f < c->n_fragments ? f : -1);
+        if (!check_plan(p, *c))
+            return fail(CAM_E_ARG, "cam_ctx_create: internal error: inconsistent chunk plan");
         bytes += round_up(sizeof(ChunkDesc) * p.chunks.size(), 256);
         bytes += round_up(sizeof(TensorSlot) * p.tensors.size(), 256);
         bytes += round_up(sizeof(int32_t) * p.first_chunk.size(), 256);
