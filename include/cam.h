@@ -21,17 +21,19 @@
  *
  * Element arithmetic (fixed, so results are reproducible bit for bit): every
  * operation is one IEEE binary32 operation rounded to nearest-even, no fused
- * multiply-add, correctly rounded division. With x_k the k-th accumulated
- * worker's value widened to fp32 (bf16 widening is exact), in accumulate-call
- * order k = 1..K:
+ * multiply-add, correctly rounded division. With x_k the k-th worker's value
+ * widened to fp32 (bf16 widening is exact), in accumulate- or fold-call order
+ * k = 1..K:
  *   MEAN_REPLACE:    s = sum_k x_k;  theta' = s / K
  *   DELTA_NESTEROV:  s = sum_k w_k * (x_k - theta);  Delta = s / W,
  *                    w_k = (float)tokens_k, W = (float)(sum_k tokens_k);
  *                    g = -Delta;  m' = mu*m + g;  theta' = theta - lr*(g + mu*m')
  *   EMA:             e' = beta*e + (1 - beta)*theta'
  *   drift norm:      per tensor sqrt(sum_i delta_i^2), delta = Delta (DELTA mode)
- *                    or theta' - theta (MEAN mode), squares summed in fp64 in a
- *                    fixed order; per fragment sqrt(sum over its tensors).
+ *                    or theta' - theta (MEAN mode), squares summed in a fixed
+ *                    order (fp32 over runs of at most a few dozen squares,
+ *                    then fp64), so they are reproducible bit for bit; per
+ *                    fragment sqrt(sum over its tensors).
  *
  * Conventions:
  *   - Every call returns CAM_OK (0) or a negative cam_status. On any error the
@@ -39,8 +41,11 @@
  *     cam_last_error() returns a message for the calling thread.
  *   - "device pointer" means memory on the context's CUDA device; "host
  *     pointer" means ordinary CPU memory read during the call only.
- *   - All device work is stream-ordered on the stream passed to
- *     cam_merge_commit; nothing in this library synchronises the device.
+ *   - Device work is stream-ordered: a round's work on the stream passed to
+ *     cam_merge_commit, a fold's on the stream passed to cam_merge_fold.
+ *     Only cam_ctx_create, cam_ctx_status and a timed cam_ctx_last_commit
+ *     wait for the device, and the context's first fold or first
+ *     orthogonalised commit, which allocate (cudaMalloc).
  *   - Not thread-safe per context: calls on one context must not overlap.
  */
 #ifndef CAM_H
