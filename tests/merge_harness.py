@@ -82,12 +82,17 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True) -
 
 
 def gpu_round(st: GpuState, wl: W.Workload, rnd: int, frag: int, workers, draw,
-              stream=None, norms=None):
-    """Opens, fills and commits one round on the GPU. Returns (per_tensor,
-    per_fragment) device tensors when norms are requested."""
+              stream=None, norms=None, fold=False):
+    """Opens, fills and commits one round on the GPU, its workers accumulated
+    or (fold=True) folded as they arrive. Returns (per_tensor, per_fragment)
+    device tensors when norms are requested."""
     rd = st.merger.begin(rnd, frag)
+    code = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
     for k in draw.included:
-        rd.accumulate(workers[k].views, draw.tokens[k])
+        if fold:
+            rd.fold(workers[k].views, draw.tokens[k], code, stream=stream)
+        else:
+            rd.accumulate(workers[k].views, draw.tokens[k])
     rd.finalize(B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE, wl.lr, wl.mu)
     if wl.ema_beta is not None:
         rd.ema_update(wl.ema_beta)

@@ -61,7 +61,7 @@ def test_small_workloads_bitwise_equal_to_oracle():
                         workers_track_global=True), seed=4, bitwise=True)
 
 
-def _sampled_workload(wl, seed=0, per_tensor=4096, norm_tensors=()):
+def _sampled_workload(wl, seed=0, per_tensor=4096, norm_tensors=(), fold=False):
     g = W.make_global(wl, seed, DEV)
     st = make_gpu_state(wl, g, DEV)
     rng = np.random.default_rng(seed)
@@ -72,7 +72,7 @@ def _sampled_workload(wl, seed=0, per_tensor=4096, norm_tensors=()):
         idxs = [sample_indices(wl.specs[t].numel, per_tensor, rng) for t in tensors]
         before = gather_state(st, tensors, idxs)
         full_before = {t: to_np(st.theta.views[t]).copy() for t in norm_tensors if t in tensors}
-        gn = gpu_round(st, wl, rnd, frag, workers, draw)
+        gn = gpu_round(st, wl, rnd, frag, workers, draw, fold=fold)
         torch.cuda.synchronize()
         sampled_round_check(wl, st, frag, workers, draw, idxs, before, f"{wl.name} round {rnd}")
         if gn is not None:
@@ -90,6 +90,15 @@ def _sampled_workload(wl, seed=0, per_tensor=4096, norm_tensors=()):
 
 def test_diffurefill1b_f32_mean_ema_sampled():
     _sampled_workload(W.workload("diffurefill1b"))
+
+
+def test_diffurefill1b_f32_mean_ema_folded_sampled():
+    # the 1.08B round with its five workers folded as they arrive
+    _sampled_workload(W.workload("diffurefill1b"), seed=1, fold=True)
+
+
+def test_diffurefill1b_bf16_fragments_folded_sampled():
+    _sampled_workload(W.workload("diffurefill1b_bf16"), seed=2, norm_tensors=(0, 9), fold=True)
 
 
 def test_diffurefill1b_bf16_fragments_nesterov_norms_sampled():
