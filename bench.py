@@ -667,6 +667,117 @@ def run_adopt(args, wl, ws, rank, local) -> int:
     return 0
 
 
+def run_fold(args, wl, ws, rank, local) -> int:
+    """Times eagerly folded rounds with device-resident workers: per step,
+    every round of the workload folds its included workers as they "arrive"
+    (cam_merge_fold), then commits (the final pass from the running sums).
+    Bytes are the eager path's algorithmic traffic:
+
+    - per fold: the worker (4 or 2 B), the sum written (4 B) and, after the
+      first, read (4 B), and theta (4 B) in delta mode;
+    - the final pass: the sum (4 B) plus the state bytes of the round.
+
+    The roofline takes the fold kernel alone, from CUDA events around each
+    fold."""
+    import torch
+
+    import __graft_entry__
+    from checkpoint_averaging_gb300 import binding as B
+    from checkpoint_averaging_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = W.make_global(wl, args.seed, dev)
+    theta = W.empty_arena(g.numels, torch.float32, dev)
+    theta.flat.copy_(g.flat)
+    delta = wl.mode == "delta"
+    m = W.empty_arena(g.numels, torch.float32, dev) if delta else None
+    e = None
+    if wl.ema_beta is not None:
+        e = W.empty_arena(g.numels, torch.float32, dev)
+        e.flat.copy_(g.flat)
+    draws = [W.draw_round(wl, i, args.seed) for i in range(len(wl.rounds))]
+    workers = [[W.make_worker(wl, g, rnd, k, args.seed, dev) for k in range(wl.K)]
+               for rnd, _ in wl.rounds]
+    del g
+    mg = B.Merger(theta.views, momentum=None if m is None else m.views,
+                  ema=None if e is None else e.views, fragment_of=wl.fragment_of,
+                  n_fragments=wl.n_fragments, quorum=wl.quorum)
+    code = B.DELTA_NESTEROV if delta else B.MEAN_REPLACE
+    ck = [{k: mg.checkpoint(w[k].views, frag) for k in d.included}
+          for (_, frag), w, d in zip(wl.rounds, workers, draws)]
+    x_size = 2 if wl.ckpt_dtype == "bf16" else 4
+    fold_bytes, step_bytes = [], 0
+    for (_, frag), d in zip(wl.rounds, draws):
+        n = wl.fragment_numel(frag)
+        for j in range(len(d.included)):
+            b = n * (x_size + 4 + (4 if j > 0 else 0) + (4 if delta else 0))
+            fold_bytes.append(b)
+            step_bytes += b
+        step_bytes += n * (4 + 4 + (4 if delta or wl.norms else 0) + (8 if delta else 0)
+                           + (8 if e is not None else 0))
+    s = torch.cuda.current_stream(dev)
+    rnd_no = [0]
+    fold_ev = []
+
+    def step(timed):
+        i_fold = 0
+        for (_, frag), d, c in zip(wl.rounds, draws, ck):
+            rd = mg.begin(rnd_no[0], frag)
+            rnd_no[0] += 1
+            for k in d.included:
+                if timed:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                rd.fold(c[k], d.tokens[k], code, stream=s)
+                if timed:
+                    b.record(s)
+                    fold_ev.append((a, b, fold_bytes[i_fold]))
+                i_fold += 1
+            rd.finalize(code, wl.lr, wl.mu)
+            if e is not None:
+                rd.ema_update(wl.ema_beta)
+            rd.commit(s)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    l0 = mg.launch_count
+    with ClockSampler(local) as clocks:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(s)
+        torch.cuda.synchronize(dev)
+    t = t0.elapsed_time(t1) / 1e3 / args.steps
+    launches = mg.launch_count - l0
+    # the fold kernel: bytes over time of the largest folds (a full worker)
+    big = max(b for _, _, b in fold_ev)
+    fold_gbs = statistics.mean(b / (x.elapsed_time(y) / 1e3) / 1e9 for x, y, b in fold_ev
+                               if b == big)
+    peak = measured_peaks().get("hbm_gbs") or FALLBACK_HBM_GBS
+    gbs = step_bytes / t / 1e9
+    mg.close()
+    print(json.dumps({
+        "metric": "eagerly folded merge round HBM GB/s", "value": round(gbs, 2), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if wl.ckpt_dtype == "f32" else "bf16->f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "op": "fold", "n_params": wl.n_params, "K": wl.K,
+                   "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "roofline": {"bound": "hbm", "achieved": round(fold_gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(fold_gbs / peak, 4), "traffic": None,
+                     "kernel": "fold_worker (non-first folds)"},
+        "clocks": clocks.summary(), "gpu_launches": launches}), flush=True)
+    return 0
+
+
 def run_ortho(args, wl, ws, rank, local) -> int:
     """Times an orthogonalised plain-mean round (technical report, section 5.3)
     over the workload's tensor list: every matrix's averaged update replaced by
@@ -775,7 +886,7 @@ def parse(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="diffurefill1b")
-    p.add_argument("--op", choices=("merge", "adopt", "ortho"), default="merge")
+    p.add_argument("--op", choices=("merge", "adopt", "ortho", "fold"), default="merge")
     p.add_argument("--ortho-iterations", type=int, default=30)
     p.add_argument("--ortho-precision", choices=("tf32", "fp32"), default="tf32")
     p.add_argument("--ortho-short-side", action="store_true",
@@ -805,6 +916,8 @@ def main(argv=None) -> int:
         return run_adopt(args, wl, ws, rank, local)
     if args.op == "ortho":
         return run_ortho(args, wl, ws, rank, local)
+    if args.op == "fold":
+        return run_fold(args, wl, ws, rank, local)
     return run_ours(args, wl, ws, rank, local)
 
 
