@@ -478,8 +478,9 @@ def test_host_resident_checkpoints_match_oracle(where):
 
 
 @pytest.mark.parametrize("dest", ["pinned", "device"])
-def test_publish_writes_copies_of_theta_and_ema(dest):
-    wl = _custom(RAGGED, K=3, mode="delta", dtype="f32")
+@pytest.mark.parametrize("mode", ["delta", "mean"])  # mean + EMA takes the staged form
+def test_publish_writes_copies_of_theta_and_ema(dest, mode):
+    wl = _custom(RAGGED, K=3, mode=mode, dtype="f32")
     g = W.make_global(wl, 0, DEV)
     st = make_gpu_state(wl, g, DEV)
     draw = W.draw_round(wl, 0, 0)
@@ -495,7 +496,7 @@ def test_publish_writes_copies_of_theta_and_ema(dest):
     rd = st.merger.begin(0)
     for k in draw.included:
         rd.accumulate(workers[k].views, draw.tokens[k])
-    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.finalize(B.DELTA_NESTEROV if mode == "delta" else B.MEAN_REPLACE, wl.lr, wl.mu)
     rd.ema_update(0.9)
     rd.publish(pth.views, pe.views)
     rd.commit()
