@@ -945,9 +945,11 @@ def _ab_round(st, wl, rnd, workers, draw, *, worker_norms, publish):
         out["pw"] = torch.full((len(draw.included),), -1.0, dtype=torch.float64, device=DEV)
         rd.worker_drift_norm(out["pwt"], out["pw"])
     if publish:
-        out["th_pub"] = [torch.full_like(v, float("nan")) for v in st.theta.views]
-        out["e_pub"] = ([torch.full_like(v, float("nan")) for v in st.e.views]
-                        if st.e is not None else None)
+        def buf(v):
+            t = torch.full_like(v, float("nan"))
+            return t.cpu().pin_memory() if pub_host else t
+        out["th_pub"] = [buf(v) for v in st.theta.views]
+        out["e_pub"] = [buf(v) for v in st.e.views] if st.e is not None else None
         rd.publish(out["th_pub"], out["e_pub"])
     rd.commit()
     return out
@@ -1095,7 +1097,8 @@ def test_short_side_flag_is_validated():
 
 # ---- eagerly folded rounds (cam_merge_fold) ----------------------------------------
 
-def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=None):
+def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=None,
+                pub_host=False):
     rd = st.merger.begin(rnd, -1)
     code = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
     T = len(rd.tensors)
@@ -1120,9 +1123,11 @@ def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=N
         out["pf"] = torch.full((1,), -1.0, dtype=torch.float64, device=DEV)
         rd.drift_norm(out["pt"], out["pf"])
     if publish:
-        out["th_pub"] = [torch.full_like(v, float("nan")) for v in st.theta.views]
-        out["e_pub"] = ([torch.full_like(v, float("nan")) for v in st.e.views]
-                        if st.e is not None else None)
+        def buf(v):
+            t = torch.full_like(v, float("nan"))
+            return t.cpu().pin_memory() if pub_host else t
+        out["th_pub"] = [buf(v) for v in st.theta.views]
+        out["e_pub"] = [buf(v) for v in st.e.views] if st.e is not None else None
         rd.publish(out["th_pub"], out["e_pub"])
     rd.commit()
     return out
@@ -1150,7 +1155,7 @@ def test_folded_round_equals_accumulated_round_bitwise(mode, dtype, ema, swa, no
             workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
         oa = _fold_round(acc, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish)
         of = _fold_round(fold, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish,
-                         streams=[torch.cuda.current_stream()])
+                         streams=[torch.cuda.current_stream()], pub_host=host)
         oracle_round(ost, wl, rnd, -1, workers, draw)
         torch.cuda.synchronize()
         for name in ("theta", "m", "e", "swa"):
@@ -1161,9 +1166,10 @@ def test_folded_round_equals_accumulated_round_bitwise(mode, dtype, ema, swa, no
         compare_full(fold, ost, f"folded round {rnd}")
         if publish:
             for t, v in enumerate(fold.theta.views):
-                assert torch.equal(of["th_pub"][t].view(torch.int32), v.view(torch.int32))
+                assert torch.equal(of["th_pub"][t].cpu().view(torch.int32), v.cpu().view(torch.int32))
                 if fold.e is not None:
-                    assert torch.equal(of["e_pub"][t].view(torch.int32), fold.e.views[t].view(torch.int32))
+                    assert torch.equal(of["e_pub"][t].cpu().view(torch.int32),
+                                       fold.e.views[t].cpu().view(torch.int32))
         for key in ("pt", "pf", "pwt", "pw"):
             if key in oa:
                 x, y = of[key].cpu().numpy(), oa[key].cpu().numpy()
