@@ -945,11 +945,9 @@ def _ab_round(st, wl, rnd, workers, draw, *, worker_norms, publish):
         out["pw"] = torch.full((len(draw.included),), -1.0, dtype=torch.float64, device=DEV)
         rd.worker_drift_norm(out["pwt"], out["pw"])
     if publish:
-        def buf(v):
-            t = torch.full_like(v, float("nan"))
-            return t.cpu().pin_memory() if pub_host else t
-        out["th_pub"] = [buf(v) for v in st.theta.views]
-        out["e_pub"] = [buf(v) for v in st.e.views] if st.e is not None else None
+        out["th_pub"] = [torch.full_like(v, float("nan")) for v in st.theta.views]
+        out["e_pub"] = ([torch.full_like(v, float("nan")) for v in st.e.views]
+                        if st.e is not None else None)
         rd.publish(out["th_pub"], out["e_pub"])
     rd.commit()
     return out
