@@ -804,7 +804,7 @@ def run_ortho(args, wl, ws, rank, local) -> int:
     workers = [W.make_worker(wl, g, 0, k, args.seed, dev) for k in range(wl.K)]
     mg = B.Merger(th.views, ema=e.views, quorum=wl.K, rows=rows)
     ck = [mg.checkpoint(w.views) for w in workers]
-    prec = B.ORTHO_FP32 if args.ortho_precision == "fp32" else B.ORTHO_TF32
+    prec = {"fp32": B.ORTHO_FP32, "tf32": B.ORTHO_TF32, "bf16": B.ORTHO_BF16}[args.ortho_precision]
     its = args.ortho_iterations
 
     def short(shape):  # takes the short-side form of the iteration
@@ -856,7 +856,7 @@ def run_ortho(args, wl, ws, rank, local) -> int:
         gemm_calls += -(-cnt // per) * (2 + 3 * its if short(shape) else 2 * its)
     peaks = measured_peaks()
     bf16 = peaks.get("bf16_tflops_sustained") or 1700.0
-    peak = bf16 * (1.1 / 2.25) if prec == B.ORTHO_TF32 else None
+    peak = {B.ORTHO_TF32: bf16 * (1.1 / 2.25), B.ORTHO_BF16: bf16}.get(prec)
     tflops = flops / t / 1e12
     mg.close()
     print(json.dumps({
@@ -870,7 +870,8 @@ def run_ortho(args, wl, ws, rank, local) -> int:
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
                      "peak": None if peak is None else round(peak, 1), "unit": "TFLOP/s",
                      "frac": None if peak is None else round(tflops / peak, 4),
-                     "peak_source": "measured bf16 sustained x nominal tf32/bf16 (1.1/2.25)"
+                     "peak_source": ("measured bf16 sustained" if prec == B.ORTHO_BF16 else
+                                     "measured bf16 sustained x nominal tf32/bf16 (1.1/2.25)")
                      + ("; the short-side form runs its r x r products in fp32"
                         if args.ortho_short_side else ""),
                      "traffic": None, "kernel": "cuBLASLt GEMMs + ortho kernels"},
@@ -888,7 +889,7 @@ def parse(argv=None):
     p.add_argument("--workload", default="diffurefill1b")
     p.add_argument("--op", choices=("merge", "adopt", "ortho", "fold"), default="merge")
     p.add_argument("--ortho-iterations", type=int, default=30)
-    p.add_argument("--ortho-precision", choices=("tf32", "fp32"), default="tf32")
+    p.add_argument("--ortho-precision", choices=("tf32", "fp32", "bf16"), default="tf32")
     p.add_argument("--ortho-short-side", action="store_true",
                    help="iterate in the short side's space for matrices of aspect ratio >= 4")
     p.add_argument("--seed", type=int, default=0)

@@ -27,7 +27,7 @@ TIME_COMMITS = 16
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
-ORTHO_TF32, ORTHO_FP32 = 0, 1
+ORTHO_TF32, ORTHO_FP32, ORTHO_BF16 = 0, 1, 2
 ORTHO_SHORT_SIDE = 4  # OR into the precision: iterate in the short side's space
 
 OK, E_ARG, E_STATE, E_STALE, E_BUSY, E_QUORUM, E_KMAX, E_CUDA, E_NOMEM = \

@@ -18,6 +18,7 @@
 // the library never depends on it. The element-wise steps are this file's
 // kernels.
 #include <cublasLt.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <dlfcn.h>
 
@@ -246,6 +247,18 @@ __global__ void ortho_scale(float* X, int64_t n, const float* inv_norm) {
     for (int64_t i = done + tid; i < n; i += stride) Xj[i] = __fmul_rn(Xj[i], f);
 }
 
+// X_j / |Delta_j|_F (fp32 in X) into the bf16 iterate buffer Y, rounded to
+// nearest-even (CAM_ORTHO_BF16).
+__global__ void ortho_scale_bf16(const float* X, __nv_bfloat16* Y, int64_t n, const float* inv_norm) {
+    const int j = blockIdx.y;
+    const float f = inv_norm[j];
+    const float* Xj = X + int64_t(j) * n;
+    __nv_bfloat16* Yj = Y + int64_t(j) * n;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x)
+        Yj[i] = __float2bfloat16_rn(__fmul_rn(Xj[i], f));
+}
+
 // P_j <- I (r x r) for every slot j; total = slots x r x r.
 __global__ void ortho_identity(float* P, int64_t r, int64_t total) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
@@ -259,7 +272,7 @@ struct ApplyArgs {
     float* theta[kOrthoBatchMax];
     float* e[kOrthoBatchMax];  // EMA buffers, or null
     uint32_t vec[kOrthoBatchMax / 32];  // bit j: matrix j's buffers take 32-byte vectors
-    const float* O;            // the polar factors (converged iterates), slot j at O + j * n
+    const void* O;             // the polar factors (fp32, or bf16), slot j at O + j * n
     int64_t n;
     const double* scalars;     // [j] = |Delta_j|_F^2
     float lr;
@@ -268,12 +281,14 @@ struct ApplyArgs {
     float beta;
 };
 
-// theta' = theta + s O, then e' = beta e + (1 - beta) theta'.
+// theta' = theta + s O, then e' = beta e + (1 - beta) theta'. OT is the
+// polar factor's storage type (float, or bf16 bits widened exactly).
+template <typename OT>
 __global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
     const int j = blockIdx.y;
     float* theta = a.theta[j];
     float* e = a.e[j];
-    const float* O = a.O + int64_t(j) * a.n;
+    const OT* O = static_cast<const OT*>(a.O) + int64_t(j) * a.n;
     float s = a.lr;
     if (a.scale_mode == CAM_ORTHO_SCALE_MATCH_NORM)
         s = static_cast<float>(static_cast<double>(a.lr) * sqrt(a.scalars[j]) /
@@ -285,11 +300,12 @@ __global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
     if ((a.vec[j >> 5] >> (j & 31)) & 1u) {  // 8 elements per step
         const int64_t nv = a.n >> 3;
         for (int64_t v = tid; v < nv; v += stride) {
-            float th[8], o[8];
+            float th[8];
             dev::load_s8(theta + 8 * v, th);
-            dev::load_s8(O + 8 * v, o);
+            dev::XVec<OT> o;
+            o.load(O + 8 * v);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) th[q] = __fadd_rn(th[q], __fmul_rn(s, o[q]));
+            for (int q = 0; q < 8; ++q) th[q] = __fadd_rn(th[q], __fmul_rn(s, o.get(q)));
             dev::store_s8(theta + 8 * v, th);
             if (e) {
                 float ev[8];
@@ -303,7 +319,7 @@ __global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
         done = 8 * nv;
     }
     for (int64_t i = done + tid; i < a.n; i += stride) {
-        const float th = __fadd_rn(theta[i], __fmul_rn(s, O[i]));
+        const float th = __fadd_rn(theta[i], __fmul_rn(s, dev::load_x1(O + i)));
         theta[i] = th;
         if (e) e[i] = __fadd_rn(__fmul_rn(a.beta, e[i]), __fmul_rn(omb, th));
     }
@@ -333,16 +349,19 @@ int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
         }
     const LtApi& L = *w->lt;
     GemmPlan p{M, N, Kd, lda, ldb, ldc, ta, tb, precision, batch, sa, sb, sc};
+    // bf16 operands and results with fp32 accumulation, or fp32 ones in full
+    // fp32 or TF32 (inputs rounded to 10-bit mantissas inside the GEMM)
     const cublasComputeType_t ct =
-        precision == CAM_ORTHO_FP32 ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_FAST_TF32;
+        precision == CAM_ORTHO_TF32 ? CUBLAS_COMPUTE_32F_FAST_TF32 : CUBLAS_COMPUTE_32F;
+    const cudaDataType_t dt = precision == CAM_ORTHO_BF16 ? CUDA_R_16BF : CUDA_R_32F;
     int st = L.desc_create(&p.op, ct, CUDA_R_32F);
     if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matmul descriptor", st);
     const cublasOperation_t oa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, ob = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
     L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &oa, sizeof oa);
     L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &ob, sizeof ob);
-    st = L.layout_create(&p.la, CUDA_R_32F, ta ? Kd : M, ta ? M : Kd, lda);
-    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lb, CUDA_R_32F, tb ? N : Kd, tb ? Kd : N, ldb);
-    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lc, CUDA_R_32F, M, N, ldc);
+    st = L.layout_create(&p.la, dt, ta ? Kd : M, ta ? M : Kd, lda);
+    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lb, dt, tb ? N : Kd, tb ? Kd : N, ldb);
+    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lc, dt, M, N, ldc);
     if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matrix layout", st);
     if (batch > 1) {
         const cublasLtMatrixLayout_t lays[3] = {p.la, p.lb, p.lc};
@@ -374,8 +393,8 @@ int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
 // D = alpha op(A) op(B) + beta C for `batch` matrices at element strides
 // sa, sb, sc (column-major; C and D share a layout).
 int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
-         int64_t N, int64_t Kd, float alpha, const float* A, int64_t lda, const float* B,
-         int64_t ldb, float beta, const float* C, float* D, int64_t ldc, int32_t batch,
+         int64_t N, int64_t Kd, float alpha, const void* A, int64_t lda, const void* B,
+         int64_t ldb, float beta, const void* C, void* D, int64_t ldc, int32_t batch,
          int64_t sa, int64_t sb, int64_t sc, cudaStream_t s) {
     const GemmPlan* p = nullptr;
     int rc = gemm_plan(w, precision, ta, tb, M, N, Kd, lda, ldb, ldc, batch, sa, sb, sc, &p);
@@ -566,15 +585,20 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
         if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(da);
         else ortho_delta<float><<<bgrid, kOrthoThreads, 0, s>>>(da);
         ortho_norm<<<B, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
-        ortho_scale<<<bgrid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
+        const bool bf = p.precision == CAM_ORTHO_BF16;
+        if (bf)  // the bf16 iterate starts in Y; X's fp32 Delta is no longer needed
+            ortho_scale_bf16<<<bgrid, kOrthoThreads, 0, s>>>(
+                w->X, reinterpret_cast<__nv_bfloat16*>(w->Y), numel, w->inv_norm);
+        else
+            ortho_scale<<<bgrid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
         *launches += 3;
         cudaError_t ce = cudaGetLastError();
         if (ce != cudaSuccess)
             return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
         // Newton-Schulz on all B matrices at once. Row-major X (m x n) is the
         // column-major n x m matrix A = X^T (ld n).
-        float* cur = w->X;
-        float* nxt = w->Y;
+        void* cur = bf ? static_cast<void*>(w->Y) : static_cast<void*>(w->X);
+        void* nxt = bf ? static_cast<void*>(w->X) : static_cast<void*>(w->Y);
         const bool short_side = p.short_side && std::max(m, n) >= 4 * r;
         if (short_side) {
             const int rc = short_side_iteration(w, p, m, n, B, s, launches);
@@ -606,7 +630,10 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
         aa.scale_mode = p.scale_mode;
         aa.r = r;
         aa.beta = p.beta;
-        ortho_apply<<<bgrid, kOrthoThreads, 0, s>>>(aa);
+        if (bf)
+            ortho_apply<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(aa);
+        else
+            ortho_apply<float><<<bgrid, kOrthoThreads, 0, s>>>(aa);
         *launches += 1;
         ce = cudaGetLastError();
         if (ce != cudaSuccess)

@@ -776,7 +776,8 @@ CAM_API int cam_merge_orthogonalize(cam_round* r, float lr, int32_t scale_mode, 
     if (scale_mode != CAM_ORTHO_SCALE_FIXED && scale_mode != CAM_ORTHO_SCALE_MATCH_NORM)
         return fail(CAM_E_ARG, "%s: unknown scale mode %d", fn, scale_mode);
     const int32_t base = precision & ~int32_t(CAM_ORTHO_SHORT_SIDE);
-    if (base != CAM_ORTHO_TF32 && base != CAM_ORTHO_FP32)
+    const bool short_side = (precision & CAM_ORTHO_SHORT_SIDE) != 0;
+    if (base != CAM_ORTHO_TF32 && base != CAM_ORTHO_FP32 && !(base == CAM_ORTHO_BF16 && !short_side))
         return fail(CAM_E_ARG, "%s: unknown precision %d", fn, precision);
     if (iterations < 1 || iterations > 1000)
         return fail(CAM_E_ARG, "%s: iterations %d outside [1, 1000]", fn, iterations);

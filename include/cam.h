@@ -94,6 +94,7 @@ typedef enum {
 #define CAM_ORTHO_SCALE_MATCH_NORM 1 /* ... + lr * |Delta|_F / sqrt(min(m, n)) * polar(Delta) */
 #define CAM_ORTHO_TF32 0             /* GEMMs on the tensor cores, TF32 inputs, fp32 accumulation */
 #define CAM_ORTHO_FP32 1             /* GEMMs in full fp32 */
+#define CAM_ORTHO_BF16 2             /* iterate and GEMM inputs in bf16, fp32 accumulation */
 #define CAM_ORTHO_SHORT_SIDE 4       /* OR into precision: iterate in the short side's space */
 
 typedef struct cam_ctx cam_ctx;     /* opaque */
@@ -255,6 +256,11 @@ int cam_ema_update(cam_round* rd, float beta);
  * matrix, its Gram matrix and 32 MiB for cuBLASLt) and loads cuBLASLt
  * (CAM_E_CUDA if it cannot). Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
  *
+ * CAM_ORTHO_BF16 keeps the iterate and the Gram matrix in bf16 between
+ * steps (fp32 accumulation inside each GEMM, tensor cores at bf16 rate).
+ * Delta, its norm and the final step stay fp32. The polar factor carries
+ * bf16 rounding, a few units of 2^-8 relative.
+ *
  * CAM_ORTHO_SHORT_SIDE, OR-ed into precision, changes where the iteration
  * runs for matrices whose long side is at least 4 times the short side r.
  * Writing the iterate as X_k = X_0 P_k (tall) or P_k X_0 (wide), each step
@@ -266,7 +272,7 @@ int cam_ema_update(cam_round* rd, float beta);
  * G squares Delta's condition number, so rounding grows like
  * u * cond(Delta)^2: the option suits well-conditioned tall updates (token
  * embeddings), not ill-conditioned ones. Other shapes take the plain
- * iteration.
+ * iteration. It combines with CAM_ORTHO_TF32 or CAM_ORTHO_FP32 only.
  */
 int cam_merge_orthogonalize(cam_round* rd, float lr, int32_t scale_mode, int32_t precision,
                             int32_t iterations);

@@ -742,7 +742,9 @@ ORTHO_SHAPES = [(96, 40), (40, 96), (64, 64), (333, 0), (50, 7), (1, 0)]
 # Newton-Schulz fixed point absorbs each step's rounding, and the measured
 # error stays at 1.4-1.8 u (2048x2048 to 96x40 after 40 steps): the bound is
 # 8 u. With fp32 GEMMs the measured error is 0.6-2e-6; the bound is 1e-5.
-ORTHO_TOL = {B.ORTHO_FP32: 1e-5, B.ORTHO_TF32: 8 * 2.0 ** -11}
+# A bf16 iterate is rounded to 8 significant bits (u = 2^-8) on every step;
+# the same rule gives 8 u.
+ORTHO_TOL = {B.ORTHO_FP32: 1e-5, B.ORTHO_TF32: 8 * 2.0 ** -11, B.ORTHO_BF16: 8 * 2.0 ** -8}
 
 
 def _ortho_round(shapes, dtype, precision, mode, lr, iterations=40, seed=31, K=3):
@@ -780,7 +782,7 @@ def _ortho_round(shapes, dtype, precision, mode, lr, iterations=40, seed=31, K=3
     return out
 
 
-@pytest.mark.parametrize("precision", [B.ORTHO_FP32, B.ORTHO_TF32])
+@pytest.mark.parametrize("precision", [B.ORTHO_FP32, B.ORTHO_TF32, B.ORTHO_BF16])
 @pytest.mark.parametrize("mode", [B.ORTHO_SCALE_FIXED, B.ORTHO_SCALE_MATCH_NORM])
 def test_orthogonalised_round_matches_the_polar_factor(precision, mode):
     lr = 0.01 if mode == B.ORTHO_SCALE_FIXED else 0.7
@@ -799,7 +801,9 @@ def test_orthogonalised_round_matches_the_polar_factor(precision, mode):
         o = (got.astype(np.float64) - th0).reshape(r, c)
         o *= np.sqrt(min(r, c)) / np.linalg.norm(o)   # singular values ~1 if semi-orthogonal
         gram = o.T @ o if r >= c else o @ o.T
-        assert np.abs(gram - np.eye(min(r, c))).max() <= 30 * ORTHO_TOL[precision]
+        # to first order O^T O - I = Q^T E + E^T Q for O = Q + E: twice the
+        # step's error (measured 1e-6, 7e-4 and 2.7e-3 for fp32, tf32, bf16)
+        assert np.abs(gram - np.eye(min(r, c))).max() <= 4 * ORTHO_TOL[precision]
         # EMA of the new global, from the GPU's theta'
         e_want = 0.9 * th0.astype(np.float64) + np.float64(np.float32(1) - np.float32(0.9)) * got
         assert np.abs(e.astype(np.float64) - e_want).max() <= 4 * np.spacing(np.float32(np.abs(e_want).max()))
@@ -813,17 +817,18 @@ def test_orthogonalised_round_bf16_workers():
         assert np.abs(got - want).max() <= ORTHO_TOL[B.ORTHO_FP32] * scale + 1e-9
 
 
-def test_orthogonalised_round_on_1b_block_shapes_tf32():
+@pytest.mark.parametrize("precision", [B.ORTHO_TF32, B.ORTHO_BF16])
+def test_orthogonalised_round_on_1b_block_shapes(precision):
     shapes = [(2048, 2048), (5632, 2048), (2048, 5632), (2048, 0)]
-    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(shapes, "f32", B.ORTHO_TF32,
+    for kind, t, r, c, th0, got, want, delta, e in _ortho_round(shapes, "f32", precision,
                                                                  B.ORTHO_SCALE_MATCH_NORM, 0.7,
                                                                  iterations=40, seed=33):
         if kind == "vector":
             continue
         scale = np.abs(want - th0).max()
         err = np.abs(got.astype(np.float64) - want).max()
-        print(f"1b block {r}x{c}: max err / max step = {err / scale:.3e}")
-        assert err <= ORTHO_TOL[B.ORTHO_TF32] * scale + 2 * np.spacing(np.float32(np.abs(want).max()))
+        print(f"1b block precision={precision} {r}x{c}: max err / max step = {err / scale:.3e}")
+        assert err <= ORTHO_TOL[precision] * scale + 2 * np.spacing(np.float32(np.abs(want).max()))
 
 
 def test_orthogonalisation_of_a_zero_update_leaves_theta():
@@ -1085,7 +1090,7 @@ def test_short_side_flag_is_validated():
     e = [torch.zeros(64, device=DEV)]
     mg = B.Merger(th, ema=e, quorum=1, rows=[8])
     rd = mg.begin(0)
-    for bad in (2, 3, 6, 7, 8):
+    for bad in (3, B.ORTHO_BF16 | B.ORTHO_SHORT_SIDE, 7, 8, 11):
         with pytest.raises(B.ArgError):
             rd.orthogonalize(0.1, B.ORTHO_SCALE_FIXED, bad, 10)
     rd.orthogonalize(0.1, B.ORTHO_SCALE_FIXED, B.ORTHO_FP32 | B.ORTHO_SHORT_SIDE, 10)
