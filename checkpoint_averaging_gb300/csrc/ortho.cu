@@ -13,7 +13,8 @@
 //   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), then the
 //      EMA of the globals.
 // The two GEMMs of a step are plain dense contractions and run on the tensor
-// cores through cuBLASLt (TF32 inputs with fp32 accumulation, or full fp32),
+// cores through cuBLASLt (TF32 inputs with fp32 accumulation, full fp32, or a
+// bf16 iterate and Gram matrix with fp32 accumulation),
 // loaded with dlopen the first time a context orthogonalises, so the rest of
 // the library never depends on it. The element-wise steps are this file's
 // kernels.
@@ -254,9 +255,26 @@ __global__ void ortho_scale_bf16(const float* X, __nv_bfloat16* Y, int64_t n, co
     const float f = inv_norm[j];
     const float* Xj = X + int64_t(j) * n;
     __nv_bfloat16* Yj = Y + int64_t(j) * n;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
-         i += int64_t(gridDim.x) * blockDim.x)
-        Yj[i] = __float2bfloat16_rn(__fmul_rn(Xj[i], f));
+    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t done = 0;
+    if ((n & 7) == 0) {  // 32-byte reads, 16-byte writes (slot bases stay aligned)
+        for (int64_t v = tid; v < (n >> 3); v += stride) {
+            float x[8];
+            dev::load_s8(Xj + 8 * v, x);
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b =
+                    __floats2bfloat162_rn(__fmul_rn(x[2 * e], f), __fmul_rn(x[2 * e + 1], f));
+                ow[e] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(Yj + 8 * v) = o;
+        }
+        done = n;
+    }
+    for (int64_t i = done + tid; i < n; i += stride) Yj[i] = __float2bfloat16_rn(__fmul_rn(Xj[i], f));
 }
 
 // P_j <- I (r x r) for every slot j; total = slots x r x r.
