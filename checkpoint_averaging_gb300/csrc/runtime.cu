@@ -141,7 +141,12 @@ struct cam_ctx {
     // tensors, so they share it.
     float* d_sum = nullptr;
     std::vector<int64_t> sum_off;     // each tensor's offset in d_sum (8-element aligned)
-    std::vector<cudaEvent_t> sum_ev;  // per plan: the last fold or final pass on its tensors
+    // Per plan: the last device work (fold, commit, reset) on its tensors.
+    // Work on a plan waits for the events of every plan that shares tensors
+    // with it, so rounds on overlapping tensors run in call order whatever
+    // streams they are given, while rounds on disjoint fragments overlap.
+    std::vector<cudaEvent_t> plan_ev;
+    cudaEvent_t ortho_ev = nullptr;  // the last use of the orthogonalisation workspace
     int32_t* d_status = nullptr;   // device status word (CAM_STATUS_* bits), in dev_block
     std::vector<Plan> plans;  // [n_fragments] then "all"
     void* dev_block = nullptr;
@@ -416,16 +421,18 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
     for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
         ce = cudaEventCreate(&c->commit_ev[i]);
+    c->plan_ev.assign(c->n_fragments + 1, nullptr);
+    for (size_t i = 0; i < c->plan_ev.size() && ce == cudaSuccess; ++i)
+        ce = cudaEventCreateWithFlags(&c->plan_ev[i], cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&c->ortho_ev, cudaEventDisableTiming);
     if (ce != cudaSuccess) {
-        for (cudaEvent_t& ev : c->commit_ev)
-            if (ev) cudaEventDestroy(ev);
-        cudaFree(c->dev_block);
-        return cuda_fail(ce, "cam_ctx_create: commit events");
+        cam_ctx_destroy(c.release());
+        return cuda_fail(ce, "cam_ctx_create: events");
     }
     if (c->staged) {
         ce = cam::staged_prepare();
         if (ce != cudaSuccess) {
-            cudaFree(c->dev_block);
+            cam_ctx_destroy(c.release());
             return cuda_fail(ce, "cam_ctx_create: staged pass set-up");
         }
     }
@@ -447,7 +454,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         }
     }
     if (ce != cudaSuccess) {
-        cudaFree(c->dev_block);
+        cam_ctx_destroy(c.release());
         return cuda_fail(ce, "cam_ctx_create: init kernels");
     }
     *out = c.release();
@@ -458,12 +465,14 @@ CAM_API void cam_ctx_destroy(cam_ctx* c) {
     if (!c) return;
     for (cam_round* r : c->open) delete r;
     c->open.clear();
-    if (c->dev_block || c->ortho || c->d_sum) {
+    {
         DeviceScope scope(c->device);
         if (c->dev_block) cudaFree(c->dev_block);
         cam::ortho_destroy(c->ortho);
         if (c->d_sum) cudaFree(c->d_sum);
-        for (cudaEvent_t ev : c->sum_ev) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : c->plan_ev)
+            if (ev) cudaEventDestroy(ev);
+        if (c->ortho_ev) cudaEventDestroy(c->ortho_ev);
         for (cudaEvent_t ev : c->commit_ev)
             if (ev) cudaEventDestroy(ev);
     }
@@ -596,35 +605,24 @@ int ensure_sum(cam_ctx* c, const char* fn) {
         return fail(CAM_E_NOMEM, "%s: cudaMalloc of the running sums (%lld floats): %s", fn,
                     static_cast<long long>(total), cudaGetErrorString(ce));
     }
-    std::vector<cudaEvent_t> ev(c->n_fragments + 1, nullptr);
-    for (cudaEvent_t& e : ev) {
-        ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
-        if (ce != cudaSuccess) {
-            for (cudaEvent_t x : ev)
-                if (x) cudaEventDestroy(x);
-            cudaFree(buf);
-            return cuda_fail(ce, "cam_merge_fold: event");
-        }
-    }
     c->d_sum = buf;
     c->sum_off.swap(off);
-    c->sum_ev.swap(ev);
     return CAM_OK;
 }
 
-// Orders stream s after the last fold or final pass that touched any of the
-// round's tensors (its own plan, the whole-list plan, or every fragment's
-// plan for a whole-list round).
-cudaError_t sum_order(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+// Orders stream s after the last device work that touched any of a
+// fragment's tensors: its own plan and the whole-list plan, or every plan
+// for a whole-list round. An event not yet recorded is no wait.
+cudaError_t plan_order(cam_ctx* c, int32_t fragment, cudaStream_t s) {
     cudaError_t ce = cudaSuccess;
     for (int32_t f = 0; f <= c->n_fragments && ce == cudaSuccess; ++f)
         if (fragment < 0 || f == fragment || f == c->n_fragments)
-            ce = cudaStreamWaitEvent(s, c->sum_ev[f], 0);
+            ce = cudaStreamWaitEvent(s, c->plan_ev[f], 0);
     return ce;
 }
 
-cudaError_t sum_mark(cam_ctx* c, int32_t fragment, cudaStream_t s) {
-    return cudaEventRecord(c->sum_ev[fragment < 0 ? c->n_fragments : fragment], s);
+cudaError_t plan_mark(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+    return cudaEventRecord(c->plan_ev[fragment < 0 ? c->n_fragments : fragment], s);
 }
 
 // Bit l of vec[]: tensor l0 + l of the plan takes the vector path in a
@@ -680,7 +678,7 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     int rc = ensure_sum(c, fn);
     if (rc != CAM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t ce = sum_order(c, r->fragment, s);
+    cudaError_t ce = plan_order(c, r->fragment, s);
     const int k = r->K;
     const uintptr_t xa = dtype == CAM_F32 ? 32 : 16;
     const bool wd = r->worker_norms;
@@ -712,7 +710,7 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
         ce = cam::launch_fold(a, dtype, mode, wd, grid, s);
         ++launched;
     }
-    if (ce == cudaSuccess) ce = sum_mark(c, r->fragment, s);
+    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_fold: launch");
     c->launches += launched;
     r->eager = true;
@@ -925,7 +923,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                   static_cast<long long>(r->round), r->fragment, K);
     NvtxRange nvtx(label);
     const int64_t launches0 = c->launches, staged0 = c->staged_launches;
-    if (c->time_commits) ce = cudaEventRecord(c->commit_ev[0], s);
+    ce = plan_order(c, r->fragment, s);  // after earlier work on these tensors
+    if (ce == cudaSuccess && c->time_commits) ce = cudaEventRecord(c->commit_ev[0], s);
     const int per_launch = cam::kXCap / stride;
     // The staged form: a ring of as many stages as fit (at least 2, at most
     // kStMaxStages), for launches whose workers are device memory.
@@ -989,7 +988,6 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     };
     // Final pass of an eagerly folded round: from the running sums.
     auto launch_final = [&]() {
-        ce = sum_order(c, r->fragment, s);
         cam::FinalArgs fa;
         fa.slots = p.d_slots;
         fa.K = K;
@@ -1052,6 +1050,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                                   r->ema,
                                   r->beta,
                                   (r->ortho_precision & CAM_ORTHO_SHORT_SIDE) != 0};
+        // the workspace is the context's: after its last use on any stream
+        if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, c->ortho_ev, 0);
         std::vector<char> done(T, 0);
         std::vector<cam::OrthoMatrix> group;
         for (int l = 0; l < T && ce == cudaSuccess; ++l) {
@@ -1079,6 +1079,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                 return rc;
             }
         }
+        if (ce == cudaSuccess) ce = cudaEventRecord(c->ortho_ev, s);
     }
     if (ce == cudaSuccess && norm_level >= 1) {
         NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
@@ -1087,7 +1088,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }
-    if (ce == cudaSuccess && r->eager) ce = sum_mark(c, r->fragment, s);  // the sums were read
+    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s);
     if (ce == cudaSuccess && c->time_commits) ce = cudaEventRecord(c->commit_ev[1], s);
     if (ce == cudaSuccess) {
         cam_commit_record& rec = c->last_commit;
@@ -1128,12 +1129,15 @@ CAM_API int cam_swa_reset(cam_ctx* c, int32_t fragment, void* stream) {
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_swa_reset: cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Plan& p = c->plan_of(fragment);
+    cudaError_t ce = plan_order(c, fragment, s);
     for (int32_t g : p.tensors) {
+        if (ce != cudaSuccess) break;
         if (c->numel[g] == 0) continue;
-        cudaError_t ce = cam::launch_fill(c->swa[g], c->numel[g], 0.0f, s);
+        ce = cam::launch_fill(c->swa[g], c->numel[g], 0.0f, s);
         ++c->launches;
-        if (ce != cudaSuccess) return cuda_fail(ce, "cam_swa_reset: launch");
     }
+    if (ce == cudaSuccess) ce = plan_mark(c, fragment, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_swa_reset: launch");
     for (int32_t g : p.tensors) c->swa_count[g] = 0;
     return CAM_OK;
 }

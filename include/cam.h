@@ -43,6 +43,12 @@
  *     pointer" means ordinary CPU memory read during the call only.
  *   - Device work is stream-ordered: a round's work on the stream passed to
  *     cam_merge_commit, a fold's on the stream passed to cam_merge_fold.
+ *     Across streams the library orders, by CUDA events, work that shares
+ *     tensors (commits, folds and cam_swa_reset of overlapping fragments run
+ *     in call order) and orthogonalised commits (which share one workspace);
+ *     rounds on disjoint fragments may overlap. Work the caller issues on
+ *     the same buffers (reading theta, refilling a worker) is the caller's to
+ *     order against the stream it passed.
  *     Only cam_ctx_create, cam_ctx_status and a timed cam_ctx_last_commit
  *     wait for the device, and the context's first fold or first
  *     orthogonalised commit, which allocate (cudaMalloc).

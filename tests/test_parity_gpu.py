@@ -1202,6 +1202,86 @@ def test_folds_on_several_streams_are_ordered():
     par.merger.close()
 
 
+def test_rounds_on_shared_tensors_run_in_call_order_across_streams():
+    """Rounds that share tensors, each committed on another stream with no
+    synchronisation between them, give the bits of the same rounds on one
+    stream: the library orders work on shared tensors in call order (a
+    whole-list round before a fragment round and back), while the two
+    fragments' rounds may overlap."""
+    wl = _custom([3 << 20, 1 << 20, 4097], K=4, mode="delta", dtype="bf16", frags=[0, 1, 1],
+                 n_fragments=2, rounds=((0, -1), (1, 0), (2, 1), (3, -1), (4, 0)))
+    g = W.make_global(wl, 11, DEV)
+    draws = [W.draw_round(wl, i, 11) for i in range(len(wl.rounds))]
+    workers = [[W.make_worker(wl, g, rnd, k, 11, DEV) for k in range(wl.K)] for rnd, _ in wl.rounds]
+    seq, par = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    cur = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    for s in streams:
+        s.wait_stream(cur)
+    norms_par = []
+    for i, ((rnd, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
+        s = streams[i % len(streams)]
+        with torch.cuda.stream(s):
+            norms_par.append(gpu_round(par, wl, rnd, frag, w, d, stream=s))
+    for s in streams:
+        cur.wait_stream(s)
+    norms_seq = [gpu_round(seq, wl, rnd, frag, w, d)
+                 for (rnd, frag), w, d in zip(wl.rounds, workers, draws)]
+    torch.cuda.synchronize()
+    for name in ("theta", "m", "e"):
+        assert torch.equal(getattr(seq, name).flat.view(torch.int32),
+                           getattr(par, name).flat.view(torch.int32)), name
+    for a, b in zip(norms_par, norms_seq):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    seq.merger.close()
+    par.merger.close()
+
+
+def test_orthogonalised_rounds_on_two_streams_take_the_workspace_in_turn():
+    """Orthogonalised rounds on disjoint fragments, committed on two streams
+    at once, share the context's Newton-Schulz workspace one after the other
+    and give the bits of the same rounds on one stream."""
+    shapes = [(256, 192), (96, 40), (333, 0), (256, 192), (40, 96)]
+    sizes = [r * c if c else r for r, c in shapes]
+    rows = [r if c else 0 for r, c in shapes]
+    wl = _custom(sizes, K=3, mode="mean", dtype="f32", frags=[0, 0, 0, 1, 1], n_fragments=2,
+                 rounds=((0, 0), (1, 1)), norms=False)
+    g = W.make_global(wl, 12, DEV)
+    workers = [[W.make_worker(wl, g, rnd, k, 12, DEV) for k in range(wl.K)] for rnd, _ in wl.rounds]
+
+    def run(streams):
+        th = W.empty_arena(g.numels, torch.float32, DEV)
+        th.flat.copy_(g.flat)
+        e = W.empty_arena(g.numels, torch.float32, DEV)
+        e.flat.copy_(g.flat)
+        mg = B.Merger(th.views, ema=e.views, fragment_of=wl.fragment_of, n_fragments=2,
+                      quorum=wl.K, rows=rows)
+        cur = torch.cuda.current_stream()
+        for s in streams:
+            s.wait_stream(cur)
+        for i, (rnd, frag) in enumerate(wl.rounds):
+            s = streams[i % len(streams)]
+            with torch.cuda.stream(s):
+                rd = mg.begin(rnd, frag)
+                for k in range(wl.K):
+                    rd.accumulate(workers[i][k].views, 0)
+                rd.finalize(B.MEAN_REPLACE)
+                rd.ema_update(0.9)
+                rd.orthogonalize(0.05, B.ORTHO_SCALE_MATCH_NORM, B.ORTHO_FP32, 30)
+                rd.commit(s)
+        for s in streams:
+            cur.wait_stream(s)
+        torch.cuda.synchronize()
+        mg.close()
+        return th, e
+
+    th_par, e_par = run([torch.cuda.Stream(), torch.cuda.Stream()])
+    th_seq, e_seq = run([torch.cuda.current_stream()])
+    assert torch.equal(th_par.flat.view(torch.int32), th_seq.flat.view(torch.int32))
+    assert torch.equal(e_par.flat.view(torch.int32), e_seq.flat.view(torch.int32))
+    assert not torch.equal(th_seq.flat, g.flat)  # the rounds did move theta
+
+
 def test_worker_buffers_are_free_once_their_fold_has_run():
     wl = _custom([100_003, 2048], K=3, mode="mean", dtype="f32", ema=True, norms=False)
     g = W.make_global(wl, 8, DEV)
