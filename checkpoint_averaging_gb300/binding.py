@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import weakref
 from typing import Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -480,6 +481,9 @@ class Merger:
 
     def close(self):
         if getattr(self, "ctx", None):
+            # destroying the context frees its open rounds: their handles go too
+            for rd in list(getattr(self, "_rounds", ())):
+                rd.handle = None
             ctx_destroy(self.ctx)
             self.ctx = None
 
@@ -545,7 +549,11 @@ class Merger:
         ctx_set_last_round(self.ctx, r)
 
     def begin(self, round: int, fragment: int = -1) -> "Round":
-        return Round(self, merge_begin(self.ctx, round, fragment), fragment)
+        rd = Round(self, merge_begin(self.ctx, round, fragment), fragment)
+        if not hasattr(self, "_rounds"):
+            self._rounds = weakref.WeakSet()
+        self._rounds.add(rd)
+        return rd
 
     def checkpoint(self, ckpt, fragment: int = -1) -> "Checkpoint":
         """Validates a worker's tensors once for rounds on `fragment`."""
@@ -692,7 +700,11 @@ class Round:
     def commit(self, stream=None) -> None:
         torch = _torch()
         s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
-        merge_commit(self.handle, int(s.cuda_stream))
+        try:
+            merge_commit(self.handle, int(s.cuda_stream))
+        except CudaError:
+            self.handle = None  # the library freed the round
+            raise
         self.handle = None
         host = []
         for t in self._borrowed:  # freed memory is not reused before the merge ran
@@ -706,3 +718,12 @@ class Round:
     def abort(self) -> None:
         merge_abort(self.handle)
         self.handle = None
+
+    def __del__(self):
+        # a round dropped while open is aborted, so its fragment takes new rounds
+        try:
+            if getattr(self, "handle", None) is not None and self.merger.ctx:
+                merge_abort(self.handle)
+                self.handle = None
+        except Exception:
+            pass

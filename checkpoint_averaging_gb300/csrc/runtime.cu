@@ -912,10 +912,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     }
     if (r->ortho && !c->ortho) {  // workspace of the orthogonalisation, made once per context
         const int rc = cam::ortho_create(&c->ortho, c->ortho_cap_elems, c->ortho_cap_gram);
-        if (rc != CAM_OK) {
-            close_round(r);
-            return rc;
-        }
+        if (rc == CAM_E_CUDA) close_round(r);  // a CUDA failure frees the round, as below
+        if (rc != CAM_OK) return rc;            // CAM_E_NOMEM: nothing ran, the round stays open
     }
     cudaError_t ce = cudaSuccess;
     char label[96];

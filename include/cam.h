@@ -339,8 +339,10 @@ int cam_merge_publish(cam_round* rd, float* const* theta_out, float* const* ema_
  * launches the fused merge pass (and the norm pass if asked) on `stream`
  * (a cudaStream_t; NULL = legacy default stream) and frees the round handle.
  * Returns before the device work finishes. On CAM_E_STATE / CAM_E_QUORUM /
- * CAM_E_ARG nothing is launched and the round stays open. On CAM_E_CUDA the
- * round is freed and the fragment's buffers are undefined.
+ * CAM_E_ARG, and CAM_E_NOMEM (the workspace of a context's first
+ * orthogonalised round), nothing is launched and the round stays open. On
+ * CAM_E_CUDA the round is freed and the fragment's buffers are undefined.
+ * So the handle is gone exactly when the call returns CAM_OK or CAM_E_CUDA.
  */
 int cam_merge_commit(cam_round* rd, void* stream);
 

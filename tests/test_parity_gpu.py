@@ -1202,6 +1202,33 @@ def test_folds_on_several_streams_are_ordered():
     par.merger.close()
 
 
+def test_dropped_and_orphaned_round_handles():
+    """A round dropped while open is aborted (its fragment takes a new round);
+    closing the merger with a round open invalidates that round's handle, so
+    dropping it afterwards touches nothing."""
+    import gc
+    th = [torch.zeros(4096, device=DEV)]
+    mg = B.Merger(th, quorum=1)
+    rd = mg.begin(0)
+    rd.accumulate([torch.ones(4096, device=DEV)], 0)
+    del rd
+    gc.collect()
+    rd = mg.begin(1)  # no BusyError: the dropped round was aborted
+    rd.accumulate([torch.ones(4096, device=DEV)], 0)
+    mg.close()
+    assert rd.handle is None
+    del rd
+    gc.collect()
+    mg2 = B.Merger(th, quorum=1)
+    rd = mg2.begin(0)
+    rd.accumulate([torch.full((4096,), 2.0, device=DEV)], 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.commit()
+    torch.cuda.synchronize()
+    assert torch.equal(th[0], torch.full((4096,), 2.0, device=DEV))
+    mg2.close()
+
+
 def test_rounds_on_shared_tensors_run_in_call_order_across_streams():
     """Rounds that share tensors, each committed on another stream with no
     synchronisation between them, give the bits of the same rounds on one
