@@ -522,8 +522,11 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
       EMA into host buffers in the same pass (cam_merge_publish).
     copy: the workers are copied host->device with the copy engine, merged,
       and the new global and EMA copied device->host afterwards.
-    fold: as stream, but each worker is folded into the running sum as it
-      arrives (cam_merge_fold), so commit only finishes from the sum.
+    fold: as stream, but each worker except the last is folded into the
+      running sum as it arrives (cam_merge_fold); the last arrival is
+      accumulated, and the commit's final pass folds it, finishes and
+      publishes in one pass (its reads and the published writes share the
+      host link at once).
 
     In stream and fold mode, post_arrival_ms is the time from the last
     worker's arrival (its accumulate or fold call) to the new global in host
@@ -573,9 +576,10 @@ def run_e2e(args, wl, mg, workers, draws, theta, e, stream, mode, round_no) -> d
                     ev_a = torch.cuda.Event(enable_timing=True)
                     ev_b = torch.cuda.Event(enable_timing=True)
                 for j, k in enumerate(d.included):
-                    if ev_a is not None and j == len(d.included) - 1:
+                    last = j == len(d.included) - 1
+                    if ev_a is not None and last:
                         ev_a.record(stream)  # the last worker arrives
-                    if args.e2e_mode == "fold":
+                    if args.e2e_mode == "fold" and not last:
                         rd.fold(src[i][k], d.tokens[k], mode, stream=stream)
                     else:
                         rd.accumulate(src[i][k], d.tokens[k])
@@ -675,10 +679,13 @@ def run_fold(args, wl, ws, rank, local) -> int:
 
     - per fold: the worker (4 or 2 B), the sum written (4 B) and, after the
       first, read (4 B), and theta (4 B) in delta mode;
-    - the final pass: the sum (4 B) plus the state bytes of the round.
+    - the final pass: the sum (4 B) plus the state bytes of the round, plus
+      the last worker (4 or 2 B) with --fold-last, where the last arrival is
+      accumulated and the final pass folds it.
 
     The roofline takes the fold kernel alone, from CUDA events around each
-    fold."""
+    fold. post_arrival_ms is the device time from the last arrival (its fold,
+    or with --fold-last its accumulate) to the end of the commit."""
     import torch
 
     import __graft_entry__
@@ -711,24 +718,33 @@ def run_fold(args, wl, ws, rank, local) -> int:
           for (_, frag), w, d in zip(wl.rounds, workers, draws)]
     x_size = 2 if wl.ckpt_dtype == "bf16" else 4
     fold_bytes, step_bytes = [], 0
+    last_acc = args.fold_last
     for (_, frag), d in zip(wl.rounds, draws):
         n = wl.fragment_numel(frag)
-        for j in range(len(d.included)):
+        n_fold = len(d.included) - (1 if last_acc else 0)
+        for j in range(n_fold):
             b = n * (x_size + 4 + (4 if j > 0 else 0) + (4 if delta else 0))
             fold_bytes.append(b)
             step_bytes += b
         step_bytes += n * (4 + 4 + (4 if delta or wl.norms else 0) + (8 if delta else 0)
-                           + (8 if e is not None else 0))
+                           + (8 if e is not None else 0) + (x_size if last_acc else 0))
     s = torch.cuda.current_stream(dev)
     rnd_no = [0]
-    fold_ev = []
+    fold_ev, post_ev = [], []
 
     def step(timed):
         i_fold = 0
         for (_, frag), d, c in zip(wl.rounds, draws, ck):
             rd = mg.begin(rnd_no[0], frag)
             rnd_no[0] += 1
-            for k in d.included:
+            for j, k in enumerate(d.included):
+                last = j == len(d.included) - 1
+                if timed and last:
+                    p0 = torch.cuda.Event(enable_timing=True)
+                    p0.record(s)
+                if last and last_acc:
+                    rd.accumulate(c[k], d.tokens[k])
+                    continue
                 if timed:
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(s)
@@ -741,6 +757,10 @@ def run_fold(args, wl, ws, rank, local) -> int:
             if e is not None:
                 rd.ema_update(wl.ema_beta)
             rd.commit(s)
+            if timed:
+                p1 = torch.cuda.Event(enable_timing=True)
+                p1.record(s)
+                post_ev.append((p0, p1))
 
     for _ in range(args.warmup):
         step(False)
@@ -769,7 +789,8 @@ def run_fold(args, wl, ws, rank, local) -> int:
         "vs_baseline": None, "dtype": "f32" if wl.ckpt_dtype == "f32" else "bf16->f32",
         "data": "synthetic",
         "config": {"workload": wl.name, "op": "fold", "n_params": wl.n_params, "K": wl.K,
-                   "bytes_per_step": step_bytes,
+                   "bytes_per_step": step_bytes, "last_arrival_folded_at_commit": last_acc,
+                   "post_arrival_ms": round(statistics.mean(x.elapsed_time(y) for x, y in post_ev), 4),
                    "l2": "inputs larger than L2 (no flush needed)"},
         "roofline": {"bound": "hbm", "achieved": round(fold_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(fold_gbs / peak, 4), "traffic": None,
@@ -895,6 +916,8 @@ def parse(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy", "fold"), default="stream")
+    p.add_argument("--fold-last", action="store_true",
+                   help="--op fold: accumulate the last arrival; the commit's final pass folds it")
     p.add_argument("--cpu-seconds", type=float, default=8.0)
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="host threads for the CPU oracle legs (0: every core this process may use)")

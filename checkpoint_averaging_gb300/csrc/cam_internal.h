@@ -122,8 +122,11 @@ struct FoldArgs {
 };
 static_assert(sizeof(FoldArgs) <= 32000, "kernel parameter block too large");
 
-// The final pass of an eagerly folded round: finalize from the running sum,
-// outer step, EMA, running average, drift partials and published copies.
+// The final pass of an eagerly folded round: fold the workers accumulated
+// after the round's folds (P of them, arrival order; often just the last
+// arrival), then finalize from the running sum: outer step, EMA, running
+// average, drift partials and published copies.
+constexpr int kFinalPtrs = 3 * kEagerTensors;
 struct FinalArgs {
     const ChunkDesc* chunks;
     const TensorSlot* slots;
@@ -136,16 +139,20 @@ struct FinalArgs {
     float W;                   // (float)sum tokens
     float lr, mu, beta;
     float swa_n;               // globals in the running average after this round
+    int32_t stride;            // pointers per tensor in ptr[]: 3 + P
+    int32_t P;                 // workers folded by this pass
+    float wp[CAM_KMAX];        // (float)tokens of those workers
     uint32_t vec[kEagerTensors / 32];
-    const float* sum[kEagerTensors];
-    void* pub[2 * kEagerTensors];  // [2l]: copy of the new theta, [2l+1]: of the EMA (or null)
+    // per local tensor l, at ptr[l * stride]: the running sum, then the copy
+    // of the new theta and of the EMA (or null), then the P workers' copies
+    const void* ptr[kFinalPtrs];
 };
 static_assert(sizeof(FinalArgs) <= 32000, "kernel parameter block too large");
 
 cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drift, int grid,
                         cudaStream_t s);
-cudaError_t launch_final(const FinalArgs& a, int mode, bool ema, bool norm, bool pub, bool swa,
-                         int grid, cudaStream_t s);
+cudaError_t launch_final(const FinalArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
+                         bool swa, int grid, cudaStream_t s);
 
 // Outer orthogonalisation (ortho.cu): a per-context workspace, made at the
 // first orthogonalised commit, and the per-matrix pipeline.

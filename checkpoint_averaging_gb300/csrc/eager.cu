@@ -11,9 +11,13 @@
 //                 (x_k - theta)^2 per chunk. Reads the worker (device or
 //                 host memory) and s, writes s: the worker is no longer needed
 //                 once this launch has run.
-//   final_pass    at commit, from s: finalize, outer step, EMA, running
-//                 average, drift partials and published copies, through the
-//                 same merge_finish as the fused pass.
+//   final_pass    at commit: folds the workers accumulated after the folds
+//                 (typically the last arrival, read once, here), then from s:
+//                 finalize, outer step, EMA, running average, drift partials
+//                 and published copies, through the same merge_finish as the
+//                 fused pass. Folding the last arrival here overlaps its
+//                 host-to-device stream with the published copies'
+//                 device-to-host stream.
 //
 // Per element the operations are those of the fused pass in the same order,
 // so an eagerly folded round ends with the same bits as a round whose
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_worker(const __grid_constant
     }
 }
 
-template <int MODE, bool EMA, bool NORM, bool PUB, bool SWA>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB, bool SWA, bool PEND>
 __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant__ FinalArgs a) {
     constexpr int kWarps = kThreads / 32;
     __shared__ double part[2][kWarps];
@@ -102,14 +106,16 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
         const ChunkDesc ch = a.chunks[c];
         const int l = ch.local - a.local0;
         const TensorSlot ts = a.slots[ch.local];
-        const float* sum = a.sum[l] + ch.start;
+        const void* const* tp = a.ptr + static_cast<int64_t>(l) * a.stride;
+        const float* sum = static_cast<const float*>(tp[0]) + ch.start;
+        const void* const* xs = tp + 3;  // the workers folded here
         float* th_p = ts.theta + ch.start;
         float* m_p = ts.m + ch.start;
         float* e_p = ts.e + ch.start;
         float* sw_p = ts.swa + ch.start;
-        float* pt = PUB ? static_cast<float*>(a.pub[2 * l]) + ch.start : nullptr;
-        float* pe = (PUB && EMA && a.pub[2 * l + 1]) ? static_cast<float*>(a.pub[2 * l + 1]) + ch.start
-                                                     : nullptr;
+        float* pt = PUB ? static_cast<float*>(const_cast<void*>(tp[1])) + ch.start : nullptr;
+        float* pe = (PUB && EMA && tp[2]) ? static_cast<float*>(const_cast<void*>(tp[2])) + ch.start
+                                          : nullptr;
         float acc = 0.0f;
         int done = 0;
         if ((a.vec[l >> 5] >> (l & 31)) & 1u) {
@@ -121,6 +127,18 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
                 if (MODE == kDelta) load_s8(m_p + 8 * v, m);
                 if (EMA) load_s8(e_p + 8 * v, e);
                 if constexpr (SWA) load_s8(sw_p + 8 * v, sw);
+                if constexpr (PEND) {
+                    // worker by worker (one vector live), each element's
+                    // folds still in arrival order
+                    for (int p = 0; p < a.P; ++p) {
+                        XVec<XT> xv;
+                        xv.load(static_cast<const XT*>(xs[p]) + ch.start + 8 * v);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            sv[j] = fold_term<MODE>(sv[j], xv.get(j), a.wp[p],
+                                                    (MODE == kDelta) ? th[j] : 0.0f);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     merge_finish<MODE, EMA, NORM>(a, sv[j], th[j], m[j], e[j], acc);
@@ -141,7 +159,13 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
             float th = (MODE == kDelta || NORM) ? th_p[j] : 0.0f;
             float m = (MODE == kDelta) ? m_p[j] : 0.0f;
             float e = EMA ? e_p[j] : 0.0f;
-            merge_finish<MODE, EMA, NORM>(a, sum[j], th, m, e, acc);
+            float s = sum[j];
+            if constexpr (PEND) {
+                for (int p = 0; p < a.P; ++p)
+                    s = fold_term<MODE>(s, load_x1(static_cast<const XT*>(xs[p]) + ch.start + j),
+                                        a.wp[p], th);
+            }
+            merge_finish<MODE, EMA, NORM>(a, s, th, m, e, acc);
             th_p[j] = th;
             if (MODE == kDelta) m_p[j] = m;
             if (EMA) e_p[j] = e;
@@ -175,16 +199,28 @@ FoldFn pick_fold(int mode, bool wd) {
     return wd ? fold_worker<XT, kMean, true> : fold_worker<XT, kMean, false>;
 }
 
-template <int MODE, bool EMA, bool NORM>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PEND>
 FinalFn pick_final_ps(bool pub, bool swa) {
-    if (pub) return swa ? final_pass<MODE, EMA, NORM, true, true> : final_pass<MODE, EMA, NORM, true, false>;
-    return swa ? final_pass<MODE, EMA, NORM, false, true> : final_pass<MODE, EMA, NORM, false, false>;
+    if (pub)
+        return swa ? final_pass<XT, MODE, EMA, NORM, true, true, PEND>
+                   : final_pass<XT, MODE, EMA, NORM, true, false, PEND>;
+    return swa ? final_pass<XT, MODE, EMA, NORM, false, true, PEND>
+               : final_pass<XT, MODE, EMA, NORM, false, false, PEND>;
 }
 
-template <int MODE>
+template <typename XT, int MODE, bool PEND>
 FinalFn pick_final_mode(bool ema, bool norm, bool pub, bool swa) {
-    if (ema) return norm ? pick_final_ps<MODE, true, true>(pub, swa) : pick_final_ps<MODE, true, false>(pub, swa);
-    return norm ? pick_final_ps<MODE, false, true>(pub, swa) : pick_final_ps<MODE, false, false>(pub, swa);
+    if (ema)
+        return norm ? pick_final_ps<XT, MODE, true, true, PEND>(pub, swa)
+                    : pick_final_ps<XT, MODE, true, false, PEND>(pub, swa);
+    return norm ? pick_final_ps<XT, MODE, false, true, PEND>(pub, swa)
+                : pick_final_ps<XT, MODE, false, false, PEND>(pub, swa);
+}
+
+template <typename XT, bool PEND>
+FinalFn pick_final_xt(int mode, bool ema, bool norm, bool pub, bool swa) {
+    return mode == kDelta ? pick_final_mode<XT, kDelta, PEND>(ema, norm, pub, swa)
+                          : pick_final_mode<XT, kMean, PEND>(ema, norm, pub, swa);
 }
 
 }  // namespace
@@ -197,10 +233,12 @@ cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drif
     return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), args, 0, s);
 }
 
-cudaError_t launch_final(const FinalArgs& a, int mode, bool ema, bool norm, bool pub, bool swa,
-                         int grid, cudaStream_t s) {
-    const FinalFn fn = mode == kDelta ? pick_final_mode<kDelta>(ema, norm, pub, swa)
-                                      : pick_final_mode<kMean>(ema, norm, pub, swa);
+cudaError_t launch_final(const FinalArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
+                         bool swa, int grid, cudaStream_t s) {
+    // without workers to fold here the dtype plays no part: one instance
+    const FinalFn fn = a.P == 0 ? pick_final_xt<float, false>(mode, ema, norm, pub, swa)
+                     : dtype == kDtBF16 ? pick_final_xt<uint16_t, true>(mode, ema, norm, pub, swa)
+                                        : pick_final_xt<float, true>(mode, ema, norm, pub, swa);
     void* args[] = {const_cast<FinalArgs*>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), args, 0, s);
 }

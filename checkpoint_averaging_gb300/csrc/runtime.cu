@@ -174,6 +174,8 @@ struct cam_round {
     bool host_workers = false;   // some worker came through cam_merge_accumulate_host
     bool eager = false;          // workers are folded as they arrive (cam_merge_fold)
     int eager_mode = 0;          // the mode those folds used
+    int n_folded = 0;            // workers folded so far; later ones are accumulated and
+                                 // folded by the commit's final pass (x[(k - n_folded) * T_f + l])
     int64_t tokens[CAM_KMAX] = {};
     bool finalized = false;
     int mode = CAM_MODE_MEAN_REPLACE;
@@ -539,7 +541,8 @@ int accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t t
                bool host, const char* fn) {
     if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
     if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
-    if (r->eager) return fail(CAM_E_STATE, "%s: the round folds its workers eagerly", fn);
+    if (r->eager && r->worker_norms)
+        return fail(CAM_E_STATE, "%s: per-worker drift of a folded round comes from its folds", fn);
     if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
     if (dtype != CAM_F32 && dtype != CAM_BF16)
         return fail(CAM_E_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
@@ -641,8 +644,8 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     const char* fn = "cam_merge_fold";
     if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
     if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
-    if (!r->eager && r->K > 0)
-        return fail(CAM_E_STATE, "%s: the round already holds accumulated workers", fn);
+    if (r->K > r->n_folded)
+        return fail(CAM_E_STATE, "%s: the round already holds accumulated workers (folds come first)", fn);
     if (r->ortho) return fail(CAM_E_STATE, "%s: an orthogonalised round needs its workers at commit", fn);
     if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
     if (dtype != CAM_F32 && dtype != CAM_BF16)
@@ -718,6 +721,7 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     r->tokens[k] = tokens;
     r->dtype = dtype;
     ++r->K;
+    ++r->n_folded;
     return CAM_OK;
 }
 
@@ -995,21 +999,32 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         fa.mu = a.mu;
         fa.beta = a.beta;
         fa.swa_n = a.swa_n;
-        for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += cam::kEagerTensors) {
-            const int n = std::min(cam::kEagerTensors, T - l0);
+        const int P = K - r->n_folded;  // accumulated after the folds: folded here
+        fa.P = P;
+        fa.stride = 3 + P;
+        for (int q = 0; q < CAM_KMAX; ++q)
+            fa.wp[q] = q < P ? static_cast<float>(r->tokens[r->n_folded + q]) : 0.0f;
+        const int per = std::min(cam::kEagerTensors, cam::kFinalPtrs / fa.stride);
+        for (int l0 = 0; l0 < T && ce == cudaSuccess; l0 += per) {
+            const int n = std::min(per, T - l0);
             const int32_t c0 = p.first_chunk[l0], c1 = p.first_chunk[l0 + n];
             if (c1 == c0) continue;
             for (int l = 0; l < n; ++l) {
                 const int32_t g = p.tensors[l0 + l];
-                fa.sum[l] = c->d_sum + c->sum_off[g];
-                fa.pub[2 * l] = r->publish ? r->pub_theta[l0 + l] : nullptr;
-                fa.pub[2 * l + 1] = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
+                const void** tp = fa.ptr + static_cast<size_t>(l) * fa.stride;
+                tp[0] = c->d_sum + c->sum_off[g];
+                tp[1] = r->publish ? r->pub_theta[l0 + l] : nullptr;
+                tp[2] = r->publish_ema ? r->pub_ema[l0 + l] : nullptr;
+                for (int q = 0; q < P; ++q) tp[3 + q] = r->x[size_t(q) * T + l0 + l];
             }
             set_vec(fa.vec, n, [&](int l) {
                 const int32_t g = p.tensors[l0 + l];
-                return aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
-                       (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32)) &&
-                       aligned(fa.pub[2 * l], 32) && aligned(fa.pub[2 * l + 1], 32);
+                const void* const* tp = fa.ptr + static_cast<size_t>(l) * fa.stride;
+                bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
+                         (!r->ema || aligned(c->e[g], 32)) && (!r->swa || aligned(c->swa[g], 32)) &&
+                         aligned(tp[1], 32) && aligned(tp[2], 32);
+                for (int q = 0; q < P; ++q) v = v && aligned(tp[3 + q], xa);
+                return v;
             });
             fa.chunks = p.d_chunks + c0;
             fa.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
@@ -1017,7 +1032,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             fa.local0 = l0;
             fa.n_local = n;
             const int grid = static_cast<int>(std::min<int64_t>(fa.n_chunks, int64_t(c->sm_count) * 2));
-            ce = cam::launch_final(fa, r->mode, r->ema, norm_level >= 1, r->publish, r->swa, grid, s);
+            ce = cam::launch_final(fa, r->dtype, r->mode, r->ema, norm_level >= 1, r->publish, r->swa,
+                                   grid, s);
             ++c->launches;
         }
     };
@@ -1099,7 +1115,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                             : (c->staged_launches > staged0 ? CAM_FORM_STAGED : CAM_FORM_REGISTER);
         rec.elements = p.n_elems;
         const int64_t xb = r->dtype == CAM_BF16 ? 2 : 4;
-        const int64_t per = (r->eager ? 4 : K * xb) + 4 + ((delta || norm_level >= 1) ? 4 : 0) +
+        const int64_t per = (r->eager ? 4 + (K - r->n_folded) * xb : K * xb) + 4 +
+                            ((delta || norm_level >= 1) ? 4 : 0) +
                             (delta ? 8 : 0) + (r->ema ? 8 : 0) + (r->swa ? 8 : 0) +
                             (r->publish ? 4 : 0) + (r->publish_ema ? 4 : 0);
         rec.bytes = r->ortho ? 0 : per * p.n_elems;

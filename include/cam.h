@@ -168,8 +168,11 @@ int cam_merge_begin(cam_ctx* ctx, int64_t round, int32_t fragment, cam_round** o
  * the worker's token count (>= 0; used as its weight in DELTA_NESTEROV mode,
  * ignored in MEAN_REPLACE). The buffers are BORROWED: they must stay valid
  * and unmodified until the committed work has run on the commit stream.
- * Every accumulate of one round must use the same dtype.
- * Errors: CAM_E_ARG, CAM_E_STATE (already finalized), CAM_E_KMAX.
+ * Every accumulate of one round must use the same dtype. On a round that
+ * has folded workers (cam_merge_fold), accumulated workers come after the
+ * folds and are folded, in their order, by the commit's final pass.
+ * Errors: CAM_E_ARG, CAM_E_STATE (already finalized; a folded round that
+ * reports per-worker drift), CAM_E_KMAX.
  */
 int cam_merge_accumulate(cam_round* rd, const void* const* ckpt, cam_dtype dtype,
                          int64_t tokens);
@@ -206,19 +209,25 @@ int cam_merge_accumulate_host(cam_round* rd, const void* const* ckpt, cam_dtype 
  * buffers are borrowed only until this fold has run on `stream`, not until
  * commit.
  *
- * A round is either folded or accumulated:
+ * Rules of a folded round:
  *
  * - every fold of a round uses the same mode and dtype;
  * - cam_merge_finalize must later name that mode;
+ * - folds come first: once a worker has been accumulated, no more folds;
  * - per-worker drift (cam_worker_drift_norm) must be asked for before the
- *   first fold;
+ *   first fold, and then every worker is folded;
  * - orthogonalisation is not available.
  *
  * Successive folds of a round may use different streams; the library orders
  * them, and the commit, after one another. cam_merge_commit then runs one
- * pass over the sums instead of over the workers. Per element, every
- * operation and its order are those of an accumulated round, so the results
- * are the same bits.
+ * pass over the sums instead of over the workers, folding first any workers
+ * accumulated after the folds. Per element, every operation and its order
+ * are those of an accumulated round, so the results are the same bits.
+ *
+ * Folding all but the last arrival and accumulating the last one gives the
+ * shortest time from the last arrival to the new global: its fold, the
+ * finish and the published copies (cam_merge_publish) are one pass, whose
+ * host-to-device reads and device-to-host writes share the link at once.
  *
  * The first fold of a context allocates one fp32 buffer as large as the
  * whole tensor list (CAM_E_NOMEM if it cannot).

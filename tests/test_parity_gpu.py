@@ -1101,7 +1101,7 @@ def test_short_side_flag_is_validated():
 # ---- eagerly folded rounds (cam_merge_fold) ----------------------------------------
 
 def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=None,
-                pub_host=False):
+                pub_host=False, accumulate_last=0):
     rd = st.merger.begin(rnd, -1)
     code = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
     T = len(rd.tensors)
@@ -1110,9 +1110,10 @@ def _fold_round(st, wl, rnd, workers, draw, *, norms, wnorms, publish, streams=N
         out["pwt"] = torch.full((len(draw.included) * T,), -1.0, dtype=torch.float64, device=DEV)
         out["pw"] = torch.full((len(draw.included),), -1.0, dtype=torch.float64, device=DEV)
         rd.worker_drift_norm(out["pwt"], out["pw"])
+    n_inc = len(draw.included)
     for i, k in enumerate(draw.included):
         s = None if streams is None else streams[i % len(streams)]
-        if streams is None:
+        if streams is None or i >= n_inc - accumulate_last:  # the last ones: folded at commit
             rd.accumulate(workers[k].views, draw.tokens[k])
         else:
             rd.fold(workers[k].views, draw.tokens[k], code, stream=s)
@@ -1179,6 +1180,57 @@ def test_folded_round_equals_accumulated_round_bitwise(mode, dtype, ema, swa, no
                 assert (x >= 0).all(), f"{key}: norm not written"
                 assert np.all(np.abs(x - y) <= NORM_RTOL * np.abs(y) + 1e-300), f"{key}: {x} vs {y}"
     for st in (acc, fold):
+        assert st.merger.status() == 0
+        st.merger.close()
+
+
+@pytest.mark.parametrize("mode,dtype,ema,swa,norms,publish,host,last", [
+    ("mean", "f32", True, False, True, True, True, 1),     # the e2e pattern: pinned host in and out
+    ("delta", "bf16", True, False, True, True, False, 1),
+    ("delta", "f32", False, True, False, False, True, 2),
+    ("mean", "bf16", False, True, True, False, False, 3),  # every included worker accumulated
+])
+def test_folded_round_with_its_last_arrivals_accumulated(mode, dtype, ema, swa, norms, publish,
+                                                         host, last):
+    """Folding the first arrivals and accumulating the last ones (folded by the
+    commit's final pass) gives the bits of a round whose workers are all
+    accumulated, published copies included."""
+    wl = dataclasses.replace(
+        _custom(STAGED_SIZES, K=4, mode=mode, dtype=dtype, ema=ema, norms=norms, n_masked=1,
+                rounds=((0, -1), (1, -1))), swa=swa)
+    g = W.make_global(wl, 14, DEV)
+    acc, mixed = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    ost = oracle_state_from(g, wl)
+    for idx, (rnd, _) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, 14)
+        workers = [W.make_worker(wl, g, rnd, k, 14, DEV) for k in range(wl.K)]
+        if host:
+            workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
+        oa = _fold_round(acc, wl, rnd, workers, draw, norms=norms, wnorms=False, publish=publish)
+        om = _fold_round(mixed, wl, rnd, workers, draw, norms=norms, wnorms=False, publish=publish,
+                         streams=[torch.cuda.current_stream()], pub_host=host, accumulate_last=last)
+        oracle_round(ost, wl, rnd, -1, workers, draw)
+        torch.cuda.synchronize()
+        for name in ("theta", "m", "e", "swa"):
+            x, y = getattr(acc, name), getattr(mixed, name)
+            if x is not None:
+                assert torch.equal(x.flat.view(torch.int32), y.flat.view(torch.int32)), \
+                    f"round {rnd}: {name} differs from the accumulated round"
+        compare_full(mixed, ost, f"round {rnd} with its last {last} arrivals accumulated")
+        if publish:
+            for t, v in enumerate(mixed.theta.views):
+                assert torch.equal(om["th_pub"][t].cpu().view(torch.int32), v.cpu().view(torch.int32))
+                if mixed.e is not None:
+                    assert torch.equal(om["e_pub"][t].cpu().view(torch.int32),
+                                       mixed.e.views[t].cpu().view(torch.int32))
+        for key in ("pt", "pf"):
+            if key in oa:
+                x, y = om[key].cpu().numpy(), oa[key].cpu().numpy()
+                assert (x >= 0).all(), f"{key}: norm not written"
+                assert np.all(np.abs(x - y) <= NORM_RTOL * np.abs(y) + 1e-300), f"{key}: {x} vs {y}"
+        if last < len(draw.included):  # at least one fold: the commit takes the final pass
+            assert mixed.merger.last_commit()["form"] == B.FORM_FOLDED
+    for st in (acc, mixed):
         assert st.merger.status() == 0
         st.merger.close()
 
@@ -1341,14 +1393,15 @@ def test_fold_rules():
     rd.abort()
     rd = mg.begin(1)
     rd.fold(x, 1, B.DELTA_NESTEROV)
-    with pytest.raises(B.StateError):          # folded, then accumulated
-        rd.accumulate(x, 1)
     with pytest.raises(B.ArgError):            # another mode than the earlier folds
         rd.fold(x, 1, B.MEAN_REPLACE)
     with pytest.raises(B.StateError):          # per-worker drift after the first fold
         rd.worker_drift_norm(torch.zeros(1, dtype=torch.float64, device=DEV), None)
     with pytest.raises(B.StateError):          # orthogonalisation needs the workers at commit
         rd.orthogonalize(0.1)
+    rd.accumulate(x, 1)                        # folded, then accumulated: the commit folds it
+    with pytest.raises(B.StateError):          # a fold after an accumulated worker
+        rd.fold(x, 1, B.DELTA_NESTEROV)
     with pytest.raises(B.StateError):          # finalize with another mode
         rd.finalize(B.MEAN_REPLACE)
     rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
@@ -1356,6 +1409,15 @@ def test_fold_rules():
         rd.fold(x, 1, B.DELTA_NESTEROV)
     rd.commit()
     torch.cuda.synchronize()
+    # two workers at 1 from theta 0, equal weights: Delta 1, m' = -1, step -1.9, theta' = 1.33
+    want = np.float32(0) - np.float32(0.7) * (np.float32(-1) + np.float32(0.9) * np.float32(-1))
+    assert torch.equal(th[0], torch.full((4096,), float(want), device=DEV))
+    rd = mg.begin(2)
+    rd.worker_drift_norm(torch.zeros(2, dtype=torch.float64, device=DEV), None)
+    rd.fold(x, 1, B.DELTA_NESTEROV)
+    with pytest.raises(B.StateError):          # per-worker drift comes from folds only
+        rd.accumulate(x, 1)
+    rd.abort()
     assert mg.status() == 0
     mg.close()
 
