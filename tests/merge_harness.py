@@ -84,12 +84,13 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True) -
 def gpu_round(st: GpuState, wl: W.Workload, rnd: int, frag: int, workers, draw,
               stream=None, norms=None, fold=False):
     """Opens, fills and commits one round on the GPU, its workers accumulated
-    or (fold=True) folded as they arrive. Returns (per_tensor, per_fragment)
-    device tensors when norms are requested."""
+    or (fold=True) folded as they arrive, or (fold="last") folded except the
+    last arrival, which is accumulated and folded by the commit. Returns
+    (per_tensor, per_fragment) device tensors when norms are requested."""
     rd = st.merger.begin(rnd, frag)
     code = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
-    for k in draw.included:
-        if fold:
+    for i, k in enumerate(draw.included):
+        if fold and not (fold == "last" and i == len(draw.included) - 1):
             rd.fold(workers[k].views, draw.tokens[k], code, stream=stream)
         else:
             rd.accumulate(workers[k].views, draw.tokens[k])

@@ -101,6 +101,10 @@ def test_diffurefill1b_bf16_fragments_folded_sampled():
     _sampled_workload(W.workload("diffurefill1b_bf16"), seed=2, norm_tensors=(0, 9), fold=True)
 
 
+def test_diffurefill1b_bf16_fragments_last_arrival_folded_at_commit_sampled():
+    _sampled_workload(W.workload("diffurefill1b_bf16"), seed=3, norm_tensors=(0, 9), fold="last")
+
+
 def test_diffurefill1b_bf16_fragments_nesterov_norms_sampled():
     # last fragment includes the final norm; tensor 0 is the 151M embedding
     _sampled_workload(W.workload("diffurefill1b_bf16"), norm_tensors=(0, 8, 9, 10, 18))
