@@ -369,7 +369,11 @@ def run_ours(args, wl, ws, rank, local) -> int:
                   n_fragments=wl.n_fragments, quorum=wl.quorum,
                   swa=None if swa is None else swa.views, staging=not args.no_staging)
     n_streams = max(1, wl.in_flight)
-    streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
+    # with --graph the step is captured into a CUDA graph: it runs on a stream
+    # of its own, which the capture can take
+    main_stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
+    main_stream.wait_stream(torch.cuda.current_stream(dev))
+    streams = [main_stream] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
     norm_out = [(torch.zeros(len(mg.fragment_tensors(f)) or 1, dtype=torch.float64, device=dev),
                  torch.zeros(1, dtype=torch.float64, device=dev)) for _, f in wl.rounds]
     wnorm_out = [(torch.zeros(wl.K * max(1, len(mg.fragment_tensors(f))), dtype=torch.float64,
@@ -422,6 +426,16 @@ def run_ours(args, wl, ws, rank, local) -> int:
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize(dev)
+    graph = None
+    if args.graph:  # one step captured; the timed region replays it
+        l_cap, st_cap = mg.launch_count, mg.staged_count
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=streams[0]):
+            step(False)
+        per_replay, staged_per_replay = mg.launch_count - l_cap, mg.staged_count - st_cap
+        with torch.cuda.stream(streams[0]):
+            graph.replay()  # its first replay uploads it
+        torch.cuda.synchronize(dev)
     launches0, staged0 = mg.launch_count, mg.staged_count
     barrier(ws)
     torch.cuda.synchronize(dev)
@@ -430,7 +444,16 @@ def run_ours(args, wl, ws, rank, local) -> int:
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(streams[0])
         for _ in range(args.steps):
-            step(True)
+            if graph is None:
+                step(True)
+                continue
+            with torch.cuda.stream(streams[0]):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(streams[0])
+                graph.replay()
+                b.record(streams[0])
+                group_pairs.append((a, b))
         t1.record(streams[0])
         torch.cuda.synchronize(dev)
     elapsed = t0.elapsed_time(t1) / 1e3
@@ -438,6 +461,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
     launches = mg.launch_count - launches0
     # which form of the merge pass the library chose for these rounds
     staged_launches = mg.staged_count - staged0
+    if graph is not None:  # replays do not pass through the library's counters
+        launches, staged_launches = per_replay * args.steps, staged_per_replay * args.steps
     kernel = "merge_staged" if staged_launches > 0 else "merge_fused"
     k_incl = [len(d.included) for d in draws]
     step_bytes = sum(round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl))
@@ -448,7 +473,12 @@ def run_ours(args, wl, ws, rank, local) -> int:
     # launches are timed as one group from the fork to the join.
     per_round = [round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl)]
     big = max(range(len(per_round)), key=per_round.__getitem__)
-    if n_streams > 1:
+    if graph is not None:
+        launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
+        kern_s = statistics.mean(launch_s)
+        launch_bytes = step_bytes
+        kernel_desc = f"{kernel} x{len(wl.rounds)} rounds, one CUDA graph replay per step"
+    elif n_streams > 1:
         launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
         kern_s = statistics.mean(launch_s)
         launch_bytes = step_bytes
@@ -493,7 +523,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
                        "norms": wl.norms, "rounds_per_step": len(wl.rounds),
                        "streams": n_streams, "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
-                       "parallelism": f"replicas{ws}"},
+                       "parallelism": f"replicas{ws}", "cuda_graph": bool(args.graph)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_src, "traffic": traffic,
@@ -916,6 +946,8 @@ def parse(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy", "fold"), default="stream")
+    p.add_argument("--graph", action="store_true",
+                   help="capture one step of the merge op into a CUDA graph and time its replays")
     p.add_argument("--fold-last", action="store_true",
                    help="--op fold: accumulate the last arrival; the commit's final pass folds it")
     p.add_argument("--cpu-seconds", type=float, default=8.0)

@@ -108,7 +108,8 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
-           "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_merge_round_noalloc", "cam_last_error", "cam_version")
+           "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_stream_capturing",
+           "cam_merge_round_noalloc", "cam_last_error", "cam_version")
 
 NOALLOC_MAX_TENSORS = 4096
 NOALLOC_MAX_CHUNKS = 131072
@@ -154,6 +155,7 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_status.argtypes = [vp, ctypes.POINTER(i32)]
     L.cam_ctx_staged_count.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_ctx_last_commit.argtypes = [vp, ctypes.POINTER(CommitRecord)]
+    L.cam_stream_capturing.argtypes = [vp, ctypes.POINTER(i32)]
     L.cam_merge_round_noalloc.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, i32, vpp,
                                           ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, i32, ctypes.c_float,
@@ -419,6 +421,17 @@ def _torch():
     return torch
 
 
+def stream_capturing(stream: int) -> bool:
+    out = ctypes.c_int32()
+    _check(lib().cam_stream_capturing(stream or None, ctypes.byref(out)))
+    return out.value != 0
+
+
+def _capturing(stream) -> bool:
+    """True while the torch stream `stream` is being captured into a CUDA graph."""
+    return stream_capturing(int(stream.cuda_stream))
+
+
 def _stream_handle(stream) -> int:
     torch = _torch()
     if stream is None:
@@ -631,6 +644,8 @@ class Round:
         s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
         _check(lib().cam_merge_fold(self.handle, ckpt.ptr_array, ckpt.dtype_code, int(tokens),
                                     int(mode), int(s.cuda_stream)))
+        if _capturing(s):
+            return
         host = []
         for t in ckpt.keep:
             if t.device.type == "cuda":
@@ -706,13 +721,15 @@ class Round:
             self.handle = None  # the library freed the round
             raise
         self.handle = None
+        borrowed, self._borrowed = self._borrowed, []
+        if _capturing(s):
+            return  # a captured graph reads its buffers at every replay: they are the caller's
         host = []
-        for t in self._borrowed:  # freed memory is not reused before the merge ran
+        for t in borrowed:  # freed memory is not reused before the merge ran
             if t.device.type == "cuda":
                 t.record_stream(s)
             else:
                 host.append(t)
-        self._borrowed = []
         self.merger._hold_until_done(host, s)
 
     def abort(self) -> None:

@@ -136,6 +136,7 @@ struct cam_ctx {
     cudaEvent_t commit_ev[2] = {nullptr, nullptr};
     cam_commit_record last_commit{};
     bool has_last_commit = false;
+    bool last_commit_timed = false;  // its events were recorded (not inside a graph capture)
     // Running sums of eagerly folded rounds (cam_merge_fold): one fp32 buffer
     // over every tensor, made at the first fold. Open rounds cover disjoint
     // tensors, so they share it.
@@ -613,18 +614,31 @@ int ensure_sum(cam_ctx* c, const char* fn) {
     return CAM_OK;
 }
 
+// True while `s` is being captured into a CUDA graph. Captured work is
+// ordered by the capture alone: the per-plan events, recorded by work outside
+// any graph, are neither waited on nor recorded inside one.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
 // Orders stream s after the last device work that touched any of a
 // fragment's tensors: its own plan and the whole-list plan, or every plan
 // for a whole-list round. An event not yet recorded is no wait.
-cudaError_t plan_order(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+cudaError_t plan_order(cam_ctx* c, int32_t fragment, cudaStream_t s, bool cap) {
     cudaError_t ce = cudaSuccess;
-    for (int32_t f = 0; f <= c->n_fragments && ce == cudaSuccess; ++f)
+    for (int32_t f = 0; !cap && f <= c->n_fragments && ce == cudaSuccess; ++f)
         if (fragment < 0 || f == fragment || f == c->n_fragments)
             ce = cudaStreamWaitEvent(s, c->plan_ev[f], 0);
     return ce;
 }
 
-cudaError_t plan_mark(cam_ctx* c, int32_t fragment, cudaStream_t s) {
+cudaError_t plan_mark(cam_ctx* c, int32_t fragment, cudaStream_t s, bool cap) {
+    if (cap) return cudaSuccess;
     return cudaEventRecord(c->plan_ev[fragment < 0 ? c->n_fragments : fragment], s);
 }
 
@@ -678,10 +692,13 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     std::snprintf(label, sizeof label, "cam_merge_fold round %lld worker %d",
                   static_cast<long long>(r->round), r->K);
     NvtxRange nvtx(label);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool cap = capturing(s);
+    if (cap && !c->d_sum)
+        return fail(CAM_E_STATE, "%s: the context's first fold allocates; make it outside a graph capture", fn);
     int rc = ensure_sum(c, fn);
     if (rc != CAM_OK) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t ce = plan_order(c, r->fragment, s);
+    cudaError_t ce = plan_order(c, r->fragment, s, cap);
     const int k = r->K;
     const uintptr_t xa = dtype == CAM_F32 ? 32 : 16;
     const bool wd = r->worker_norms;
@@ -713,7 +730,7 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
         ce = cam::launch_fold(a, dtype, mode, wd, grid, s);
         ++launched;
     }
-    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s);
+    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s, cap);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_fold: launch");
     c->launches += launched;
     r->eager = true;
@@ -875,6 +892,17 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                         "cam_merge_commit: an orthogonalised round takes only an EMA update");
     }
 
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool cap = capturing(s);
+    if (cap && r->swa)
+        return fail(CAM_E_STATE,
+                    "cam_merge_commit: a running-average update cannot be captured (its count "
+                    "would not advance on replay)");
+    if (cap && r->ortho && !c->ortho)
+        return fail(CAM_E_STATE,
+                    "cam_merge_commit: the first orthogonalised commit allocates; make it outside a "
+                    "graph capture");
+
     const Plan& p = c->plan_of(r->fragment);
     const int K = r->K;
     const int T = p.n_tensors();
@@ -907,7 +935,6 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     const cam::MergeVariant variant{r->dtype, r->mode, r->ema, norm_level, r->publish, r->swa};
     const int stride = K + (r->publish ? 2 : 0);
     a.stride = stride;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     DeviceScope scope(c->device);
     if (scope.err != cudaSuccess) {
@@ -925,8 +952,9 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                   static_cast<long long>(r->round), r->fragment, K);
     NvtxRange nvtx(label);
     const int64_t launches0 = c->launches, staged0 = c->staged_launches;
-    ce = plan_order(c, r->fragment, s);  // after earlier work on these tensors
-    if (ce == cudaSuccess && c->time_commits) ce = cudaEventRecord(c->commit_ev[0], s);
+    ce = plan_order(c, r->fragment, s, cap);  // after earlier work on these tensors
+    const bool timed = c->time_commits && !cap;
+    if (ce == cudaSuccess && timed) ce = cudaEventRecord(c->commit_ev[0], s);
     const int per_launch = cam::kXCap / stride;
     // The staged form: a ring of as many stages as fit (at least 2, at most
     // kStMaxStages), for launches whose workers are device memory.
@@ -1065,7 +1093,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                                   r->beta,
                                   (r->ortho_precision & CAM_ORTHO_SHORT_SIDE) != 0};
         // the workspace is the context's: after its last use on any stream
-        if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, c->ortho_ev, 0);
+        if (ce == cudaSuccess && !cap) ce = cudaStreamWaitEvent(s, c->ortho_ev, 0);
         std::vector<char> done(T, 0);
         std::vector<cam::OrthoMatrix> group;
         for (int l = 0; l < T && ce == cudaSuccess; ++l) {
@@ -1093,7 +1121,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                 return rc;
             }
         }
-        if (ce == cudaSuccess) ce = cudaEventRecord(c->ortho_ev, s);
+        if (ce == cudaSuccess && !cap) ce = cudaEventRecord(c->ortho_ev, s);
     }
     if (ce == cudaSuccess && norm_level >= 1) {
         NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
@@ -1102,8 +1130,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }
-    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s);
-    if (ce == cudaSuccess && c->time_commits) ce = cudaEventRecord(c->commit_ev[1], s);
+    if (ce == cudaSuccess) ce = plan_mark(c, r->fragment, s, cap);
+    if (ce == cudaSuccess && timed) ce = cudaEventRecord(c->commit_ev[1], s);
     if (ce == cudaSuccess) {
         cam_commit_record& rec = c->last_commit;
         rec.round = r->round;
@@ -1123,6 +1151,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         rec.launches = c->launches - launches0;
         rec.ms = -1.0f;
         c->has_last_commit = true;
+        c->last_commit_timed = timed;
     }
     if (ce == cudaSuccess && r->swa)
         for (int32_t g : p.tensors) c->swa_count[g] = swa_prev + 1;
@@ -1143,15 +1172,18 @@ CAM_API int cam_swa_reset(cam_ctx* c, int32_t fragment, void* stream) {
     DeviceScope scope(c->device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cam_swa_reset: cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (capturing(s))
+        return fail(CAM_E_STATE, "cam_swa_reset: the counts it resets live on the host; not in a "
+                                 "graph capture");
     const Plan& p = c->plan_of(fragment);
-    cudaError_t ce = plan_order(c, fragment, s);
+    cudaError_t ce = plan_order(c, fragment, s, false);
     for (int32_t g : p.tensors) {
         if (ce != cudaSuccess) break;
         if (c->numel[g] == 0) continue;
         ce = cam::launch_fill(c->swa[g], c->numel[g], 0.0f, s);
         ++c->launches;
     }
-    if (ce == cudaSuccess) ce = plan_mark(c, fragment, s);
+    if (ce == cudaSuccess) ce = plan_mark(c, fragment, s, false);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_swa_reset: launch");
     for (int32_t g : p.tensors) c->swa_count[g] = 0;
     return CAM_OK;
@@ -1207,7 +1239,7 @@ CAM_API int cam_ctx_last_commit(cam_ctx* c, cam_commit_record* out) {
     if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_last_commit: NULL argument");
     if (!c->has_last_commit) return fail(CAM_E_ARG, "cam_ctx_last_commit: no commit yet");
     *out = c->last_commit;
-    if (c->time_commits) {
+    if (c->last_commit_timed) {
         DeviceScope scope(c->device);
         float ms = 0.0f;
         cudaError_t ce = scope.err;
@@ -1216,6 +1248,12 @@ CAM_API int cam_ctx_last_commit(cam_ctx* c, cam_commit_record* out) {
         if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_last_commit");
         out->ms = ms;
     }
+    return CAM_OK;
+}
+
+CAM_API int cam_stream_capturing(void* stream, int32_t* out) {
+    if (!out) return fail(CAM_E_ARG, "cam_stream_capturing: out is NULL");
+    *out = capturing(static_cast<cudaStream_t>(stream)) ? 1 : 0;
     return CAM_OK;
 }
 

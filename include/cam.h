@@ -52,6 +52,15 @@
  *     Only cam_ctx_create, cam_ctx_status and a timed cam_ctx_last_commit
  *     wait for the device, and the context's first fold or first
  *     orthogonalised commit, which allocate (cudaMalloc).
+ *   - CUDA graphs: commits and folds issued on a stream that is being
+ *     captured are recorded into the graph (kernel launches only, no event
+ *     of the library), and every replay repeats them with the arguments of
+ *     the capture, reading and writing the same buffers again. This removes
+ *     the host cost of small rounds issued in a loop. Refused inside a
+ *     capture (CAM_E_STATE), because a replay could not repeat them
+ *     faithfully or they allocate: a running-average update or reset (its
+ *     count lives on the host), a context's first fold and first
+ *     orthogonalised commit. A timed context does not time captured commits.
  *   - Not thread-safe per context: calls on one context must not overlap.
  */
 #ifndef CAM_H
@@ -444,6 +453,12 @@ int cam_ctx_last_commit(cam_ctx* ctx, cam_commit_record* out);
 /* Merge passes this context has launched in the staged form (a subset of
  * cam_ctx_launch_count), so a caller can tell which form a round took. */
 int cam_ctx_staged_count(const cam_ctx* ctx, int64_t* out);
+
+/* *out = 1 while `stream` (a cudaStream_t, NULL = legacy default stream) is
+ * being captured into a CUDA graph, else 0: what a binding needs to know to
+ * skip its own per-stream bookkeeping for captured work. Errors: CAM_E_ARG
+ * (out NULL). */
+int cam_stream_capturing(void* stream, int32_t* out);
 
 /*
  * cam_merge_round_noalloc -- a whole round (accumulate, finalize, optional

@@ -1258,6 +1258,71 @@ def test_folds_on_several_streams_are_ordered():
     par.merger.close()
 
 
+def test_rounds_captured_in_a_cuda_graph_replay_bit_for_bit():
+    """The Pythia-14M step (three fragment rounds, Nesterov + drift norms)
+    captured once into a CUDA graph and replayed gives, replay after replay,
+    the bits of the same rounds committed one by one; the graph reads the
+    workers' buffers afresh at every replay."""
+    wl = W.workload("pythia14m")
+    g = W.make_global(wl, 21, DEV)
+    draws = [W.draw_round(wl, i, 21) for i in range(len(wl.rounds))]
+    workers = [[W.make_worker(wl, g, rnd, k, 21, DEV) for k in range(wl.K)] for rnd, _ in wl.rounds]
+    eager, graphed = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    norms = {}
+
+    def step(st, rnd0, key):
+        for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
+            rd = st.merger.begin(rnd0 + i, frag)
+            for k in d.included:
+                rd.accumulate(w[k].views, d.tokens[k])
+            rd.finalize(B.DELTA_NESTEROV, wl.lr, wl.mu)
+            if (key, i) not in norms:
+                norms[key, i] = (torch.zeros(len(rd.tensors), dtype=torch.float64, device=DEV),
+                                 torch.zeros(1, dtype=torch.float64, device=DEV))
+            rd.drift_norm(*norms[key, i])
+            rd.commit()
+
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        step(graphed, 0, "graph")
+    torch.cuda.synchronize()
+    assert torch.equal(graphed.theta.flat, g.flat)  # capturing ran nothing
+    for rep in range(3):
+        if rep == 1:  # the replay reads the buffers as they are now
+            for w in workers:
+                for x in w:
+                    x.flat.mul_(1.001)
+        step(eager, 100 + 10 * rep, "eager")
+        graph.replay()
+        torch.cuda.synchronize()
+        for name in ("theta", "m"):
+            assert torch.equal(getattr(eager, name).flat.view(torch.int32),
+                               getattr(graphed, name).flat.view(torch.int32)), (rep, name)
+        for i in range(len(wl.rounds)):
+            a, b = norms["eager", i], norms["graph", i]
+            assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert graphed.merger.status() == 0
+    # what cannot be replayed faithfully is refused inside a capture
+    th = [torch.zeros(4096, device=DEV)]
+    sw = [torch.zeros(4096, device=DEV)]
+    mg = B.Merger(th, swa=sw, quorum=1)
+    x = [torch.ones(4096, device=DEV)]
+    g2 = torch.cuda.CUDAGraph()
+    with pytest.raises(B.StateError):
+        with torch.cuda.graph(g2, stream=side):
+            rd = mg.begin(0)
+            rd.accumulate(x, 1)
+            rd.finalize(B.MEAN_REPLACE)
+            rd.swa_update()
+            rd.commit()
+    rd.abort()
+    mg.close()
+    eager.merger.close()
+    graphed.merger.close()
+
+
 def test_dropped_and_orphaned_round_handles():
     """A round dropped while open is aborted (its fragment takes a new round);
     closing the merger with a round open invalidates that round's handle, so
