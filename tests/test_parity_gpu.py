@@ -1385,6 +1385,64 @@ def test_rounds_on_shared_tensors_run_in_call_order_across_streams():
     par.merger.close()
 
 
+def test_random_round_sequences_on_random_streams_equal_one_stream():
+    """Randomised: twelve rounds over three fragments and the whole list, each
+    accumulated, folded, or folded with its last arrival left to the commit,
+    each on one of three streams (folds on streams of their own), with no
+    synchronisation in between, end with the bits of the same calls issued on
+    one stream."""
+    rng = np.random.default_rng(77)
+    rounds = tuple((i, int(f)) for i, f in enumerate(rng.choice([-1, 0, 1, 2], size=12)))
+    wl = _custom([1 << 20, 300_001, 4097, 65_536, 9, 2_000_000], K=4, mode="delta", dtype="bf16",
+                 frags=[0, 0, 1, 1, 2, 2], n_fragments=3, rounds=rounds, n_masked=1)
+    g = W.make_global(wl, 15, DEV)
+    draws = [W.draw_round(wl, i, 15) for i in range(len(rounds))]
+    how = rng.choice(["accumulate", "fold", "fold_last"], size=len(rounds))
+    which = rng.integers(0, 3, size=(len(rounds), wl.K + 1))
+    workers = [[W.make_worker(wl, g, rnd, k, 15, DEV) for k in range(wl.K)] for rnd, _ in rounds]
+    code = B.DELTA_NESTEROV
+
+    def run(streams):
+        st = make_gpu_state(wl, g, DEV)
+        cur = torch.cuda.current_stream()
+        for s in streams:
+            s.wait_stream(cur)
+        outs = []
+        for i, ((rnd, frag), d) in enumerate(zip(rounds, draws)):
+            cs = streams[which[i, -1] % len(streams)]
+            with torch.cuda.stream(cs):
+                rd = st.merger.begin(rnd, frag)
+                for j, k in enumerate(d.included):
+                    fold = how[i] == "fold" or (how[i] == "fold_last" and j < len(d.included) - 1)
+                    if fold:
+                        rd.fold(workers[i][k].views, d.tokens[k], code,
+                                stream=streams[which[i, j] % len(streams)])
+                    else:
+                        rd.accumulate(workers[i][k].views, d.tokens[k])
+                rd.finalize(code, wl.lr, wl.mu)
+                rd.ema_update(0.9)
+                pt = torch.zeros(len(rd.tensors) or 1, dtype=torch.float64, device=DEV)
+                pf = torch.zeros(1, dtype=torch.float64, device=DEV)
+                rd.drift_norm(pt, pf)
+                rd.commit(cs)
+                outs.append((pt, pf))
+        for s in streams:
+            cur.wait_stream(s)
+        torch.cuda.synchronize()
+        return st, outs
+
+    par, norms_par = run([torch.cuda.Stream() for _ in range(3)])
+    seq, norms_seq = run([torch.cuda.current_stream()])
+    for name in ("theta", "m", "e"):
+        assert torch.equal(getattr(seq, name).flat.view(torch.int32),
+                           getattr(par, name).flat.view(torch.int32)), name
+    for a, b in zip(norms_par, norms_seq):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for st in (par, seq):
+        assert st.merger.status() == 0
+        st.merger.close()
+
+
 def test_orthogonalised_rounds_on_two_streams_take_the_workspace_in_turn():
     """Orthogonalised rounds on disjoint fragments, committed on two streams
     at once, share the context's Newton-Schulz workspace one after the other
