@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include "cam_internal.h"
+#include "side_internal.h"
 #include "merge_device.cuh"
 
 namespace cam {

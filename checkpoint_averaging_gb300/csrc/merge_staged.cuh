@@ -19,8 +19,10 @@
 //     stage's "full" mbarrier;
 //   * with each tile the producer leaves a small descriptor in shared memory
 //     (tensor, first element, length, last tile of its chunk), fetching the
-//     next chunk's descriptor one chunk ahead; the consumers never read the
-//     chunk tables, and a stage of length 0 tells them the work is done;
+//     next chunk's descriptor one chunk ahead; the consumers read no chunk
+//     table (except with per-worker drift, where they walk the block's chunks
+//     themselves, which measured faster there), and a stage of length 0 tells
+//     them the work is done;
 //   * consumers wait on "full", compute four elements each from shared
 //     memory, store the results straight to global memory, and release the
 //     stage on its "empty" mbarrier (one arrival per warp);

@@ -30,6 +30,7 @@
 #include <vector>
 
 #include "cam_internal.h"
+#include "side_internal.h"
 #include "merge_device.cuh"
 
 namespace cam {

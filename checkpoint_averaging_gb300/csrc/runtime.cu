@@ -32,6 +32,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "cam_internal.h"
+#include "side_internal.h"
 
 #define CAM_API extern "C" __attribute__((visibility("default")))
 
