@@ -1258,6 +1258,7 @@ def test_folds_on_several_streams_are_ordered():
     par.merger.close()
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # the refused capture records nothing
 def test_rounds_captured_in_a_cuda_graph_replay_bit_for_bit():
     """The Pythia-14M step (three fragment rounds, Nesterov + drift norms)
     captured once into a CUDA graph and replayed gives, replay after replay,
@@ -1321,6 +1322,63 @@ def test_rounds_captured_in_a_cuda_graph_replay_bit_for_bit():
     mg.close()
     eager.merger.close()
     graphed.merger.close()
+
+
+def test_folded_and_orthogonalised_rounds_captured_in_a_cuda_graph():
+    """Once a context has made its running-sum buffer and its Newton-Schulz
+    workspace (outside any capture), a folded round (last arrival folded by the
+    commit) and an orthogonalised round can be captured and replayed; each
+    replay equals the same round committed directly."""
+    shapes = [(256, 192), (333, 0), (96, 40)]
+    sizes = [r * c if c else r for r, c in shapes]
+    rows = [r if c else 0 for r, c in shapes]
+    wl = _custom(sizes, K=3, mode="mean", dtype="f32", norms=False)
+    g = W.make_global(wl, 16, DEV)
+    workers = [W.make_worker(wl, g, 0, k, 16, DEV) for k in range(wl.K)]
+    side = torch.cuda.Stream()
+
+    def state():
+        th = W.empty_arena(g.numels, torch.float32, DEV)
+        th.flat.copy_(g.flat)
+        e = W.empty_arena(g.numels, torch.float32, DEV)
+        e.flat.copy_(g.flat)
+        return th, e, B.Merger(th.views, ema=e.views, quorum=wl.K, rows=rows)
+
+    def folded(mg, rnd, stream=None):
+        rd = mg.begin(rnd)
+        for k in range(wl.K - 1):
+            rd.fold(workers[k].views, 0, B.MEAN_REPLACE, stream=stream)
+        rd.accumulate(workers[wl.K - 1].views, 0)
+        rd.finalize(B.MEAN_REPLACE)
+        rd.ema_update(0.9)
+        rd.commit(stream)
+
+    def ortho(mg, rnd, stream=None):
+        rd = mg.begin(rnd)
+        for k in range(wl.K):
+            rd.accumulate(workers[k].views, 0)
+        rd.finalize(B.MEAN_REPLACE)
+        rd.ema_update(0.9)
+        rd.orthogonalize(0.05, B.ORTHO_SCALE_MATCH_NORM, B.ORTHO_FP32, 20)
+        rd.commit(stream)
+
+    for body in (folded, ortho):
+        th_d, e_d, mg_d = state()
+        th_g, e_g, mg_g = state()
+        body(mg_g, 0)                  # allocates outside the capture
+        body(mg_d, 0)
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            body(mg_g, 1, side)
+        for rep in range(2):
+            body(mg_d, 2 + rep)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(th_d.flat.view(torch.int32), th_g.flat.view(torch.int32)), (body, rep)
+            assert torch.equal(e_d.flat.view(torch.int32), e_g.flat.view(torch.int32)), (body, rep)
+        mg_d.close()
+        mg_g.close()
 
 
 def test_dropped_and_orphaned_round_handles():
