@@ -98,10 +98,11 @@ __global__ void __launch_bounds__(kThreads, 2) fold_worker(const __grid_constant
     }
 }
 
-template <typename XT, int MODE, bool EMA, bool NORM, bool PUB, bool SWA, bool PEND>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PUB, bool SWA, bool PEND, bool WD>
 __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant__ FinalArgs a) {
     constexpr int kWarps = kThreads / 32;
     __shared__ double part[2][kWarps];
+    __shared__ double part_w[WD ? 2 : 1][WD ? CAM_KMAX : 1][kWarps];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
         const ChunkDesc ch = a.chunks[c];
@@ -118,26 +119,36 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
         float* pe = (PUB && EMA && tp[2]) ? static_cast<float*>(const_cast<void*>(tp[2])) + ch.start
                                           : nullptr;
         float acc = 0.0f;
+        float accw[WD ? CAM_KMAX : 1];  // each folded worker's squared drift, as fold_worker sums it
+#pragma unroll
+        for (int p = 0; p < (WD ? CAM_KMAX : 1); ++p) accw[p] = 0.0f;
         int done = 0;
         if ((a.vec[l >> 5] >> (l & 31)) & 1u) {
             const int nv = ch.len >> 3;
             for (int v = threadIdx.x; v < nv; v += kThreads) {
                 float sv[8], th[8], m[8], e[8], sw[8];
                 load_s8(sum + 8 * v, sv);
-                if (MODE == kDelta || NORM) load_s8(th_p + 8 * v, th);
+                if (MODE == kDelta || NORM || WD) load_s8(th_p + 8 * v, th);
                 if (MODE == kDelta) load_s8(m_p + 8 * v, m);
                 if (EMA) load_s8(e_p + 8 * v, e);
                 if constexpr (SWA) load_s8(sw_p + 8 * v, sw);
                 if constexpr (PEND) {
                     // worker by worker (one vector live), each element's
                     // folds still in arrival order
-                    for (int p = 0; p < a.P; ++p) {
+#pragma unroll
+                    for (int p = 0; p < CAM_KMAX; ++p) {
+                        if (p >= a.P) break;
                         XVec<XT> xv;
                         xv.load(static_cast<const XT*>(xs[p]) + ch.start + 8 * v);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
+                        for (int j = 0; j < 8; ++j) {
+                            if constexpr (WD) {
+                                const float d = __fsub_rn(xv.get(j), th[j]);
+                                accw[p] = __fmaf_rn(d, d, accw[p]);
+                            }
                             sv[j] = fold_term<MODE>(sv[j], xv.get(j), a.wp[p],
                                                     (MODE == kDelta) ? th[j] : 0.0f);
+                        }
                     }
                 }
 #pragma unroll
@@ -157,14 +168,21 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
             done = 8 * nv;
         }
         for (int j = done + threadIdx.x; j < ch.len; j += kThreads) {
-            float th = (MODE == kDelta || NORM) ? th_p[j] : 0.0f;
+            float th = (MODE == kDelta || NORM || WD) ? th_p[j] : 0.0f;
             float m = (MODE == kDelta) ? m_p[j] : 0.0f;
             float e = EMA ? e_p[j] : 0.0f;
             float s = sum[j];
             if constexpr (PEND) {
-                for (int p = 0; p < a.P; ++p)
-                    s = fold_term<MODE>(s, load_x1(static_cast<const XT*>(xs[p]) + ch.start + j),
-                                        a.wp[p], th);
+#pragma unroll
+                for (int p = 0; p < CAM_KMAX; ++p) {
+                    if (p >= a.P) break;
+                    const float x = load_x1(static_cast<const XT*>(xs[p]) + ch.start + j);
+                    if constexpr (WD) {
+                        const float d = __fsub_rn(x, th);
+                        accw[p] = __fmaf_rn(d, d, accw[p]);
+                    }
+                    s = fold_term<MODE>(s, x, a.wp[p], th);
+                }
             }
             merge_finish<MODE, EMA, NORM>(a, s, th, m, e, acc);
             th_p[j] = th;
@@ -180,12 +198,28 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
             const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
             const double d = warp_sum(static_cast<double>(acc));
             if (lane == 0) part[parity][warp] = d;
+            if constexpr (WD) {
+#pragma unroll
+                for (int p = 0; p < CAM_KMAX; ++p) {
+                    if (p >= a.P) break;
+                    const double dw = warp_sum(static_cast<double>(accw[p]));
+                    if (lane == 0) part_w[parity][p][warp] = dw;
+                }
+            }
             __syncthreads();
             if (threadIdx.x == 0) {
                 double s = 0.0;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) s += part[parity][w];
                 a.partials[c] = s;
+                if constexpr (WD) {
+                    for (int p = 0; p < a.P; ++p) {
+                        double sw = 0.0;
+#pragma unroll
+                        for (int w = 0; w < kWarps; ++w) sw += part_w[parity][p][w];
+                        a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + a.first_k + p] = sw;
+                    }
+                }
             }
         }
     }
@@ -200,26 +234,29 @@ FoldFn pick_fold(int mode, bool wd) {
     return wd ? fold_worker<XT, kMean, true> : fold_worker<XT, kMean, false>;
 }
 
-template <typename XT, int MODE, bool EMA, bool NORM, bool PEND>
+template <typename XT, int MODE, bool EMA, bool NORM, bool PEND, bool WD>
 FinalFn pick_final_ps(bool pub, bool swa) {
     if (pub)
-        return swa ? final_pass<XT, MODE, EMA, NORM, true, true, PEND>
-                   : final_pass<XT, MODE, EMA, NORM, true, false, PEND>;
-    return swa ? final_pass<XT, MODE, EMA, NORM, false, true, PEND>
-               : final_pass<XT, MODE, EMA, NORM, false, false, PEND>;
+        return swa ? final_pass<XT, MODE, EMA, NORM, true, true, PEND, WD>
+                   : final_pass<XT, MODE, EMA, NORM, true, false, PEND, WD>;
+    return swa ? final_pass<XT, MODE, EMA, NORM, false, true, PEND, WD>
+               : final_pass<XT, MODE, EMA, NORM, false, false, PEND, WD>;
 }
 
+// norm: 0 none, 1 round drift, 2 round drift and the folded workers' drift
 template <typename XT, int MODE, bool PEND>
-FinalFn pick_final_mode(bool ema, bool norm, bool pub, bool swa) {
+FinalFn pick_final_mode(bool ema, int norm, bool pub, bool swa) {
     if (ema)
-        return norm ? pick_final_ps<XT, MODE, true, true, PEND>(pub, swa)
-                    : pick_final_ps<XT, MODE, true, false, PEND>(pub, swa);
-    return norm ? pick_final_ps<XT, MODE, false, true, PEND>(pub, swa)
-                : pick_final_ps<XT, MODE, false, false, PEND>(pub, swa);
+        return norm == 2 ? pick_final_ps<XT, MODE, true, true, PEND, PEND>(pub, swa)
+             : norm == 1 ? pick_final_ps<XT, MODE, true, true, PEND, false>(pub, swa)
+                         : pick_final_ps<XT, MODE, true, false, PEND, false>(pub, swa);
+    return norm == 2 ? pick_final_ps<XT, MODE, false, true, PEND, PEND>(pub, swa)
+         : norm == 1 ? pick_final_ps<XT, MODE, false, true, PEND, false>(pub, swa)
+                     : pick_final_ps<XT, MODE, false, false, PEND, false>(pub, swa);
 }
 
 template <typename XT, bool PEND>
-FinalFn pick_final_xt(int mode, bool ema, bool norm, bool pub, bool swa) {
+FinalFn pick_final_xt(int mode, bool ema, int norm, bool pub, bool swa) {
     return mode == kDelta ? pick_final_mode<XT, kDelta, PEND>(ema, norm, pub, swa)
                           : pick_final_mode<XT, kMean, PEND>(ema, norm, pub, swa);
 }
@@ -235,11 +272,13 @@ cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drif
 }
 
 cudaError_t launch_final(const FinalArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
-                         bool swa, int grid, cudaStream_t s) {
-    // without workers to fold here the dtype plays no part: one instance
-    const FinalFn fn = a.P == 0 ? pick_final_xt<float, false>(mode, ema, norm, pub, swa)
-                     : dtype == kDtBF16 ? pick_final_xt<uint16_t, true>(mode, ema, norm, pub, swa)
-                                        : pick_final_xt<float, true>(mode, ema, norm, pub, swa);
+                         bool swa, bool worker_drift, int grid, cudaStream_t s) {
+    // without workers to fold here the dtype plays no part: one instance;
+    // the workers' drift is computed here only for the workers folded here
+    const int nl = !norm ? 0 : (worker_drift && a.P > 0) ? 2 : 1;
+    const FinalFn fn = a.P == 0 ? pick_final_xt<float, false>(mode, ema, nl, pub, swa)
+                     : dtype == kDtBF16 ? pick_final_xt<uint16_t, true>(mode, ema, nl, pub, swa)
+                                        : pick_final_xt<float, true>(mode, ema, nl, pub, swa);
     void* args[] = {const_cast<FinalArgs*>(&a)};
     return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads), args, 0, s);
 }

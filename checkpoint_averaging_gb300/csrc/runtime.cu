@@ -543,8 +543,6 @@ int accumulate(cam_round* r, const void* const* ckpt, cam_dtype dtype, int64_t t
                bool host, const char* fn) {
     if (!r) return fail(CAM_E_ARG, "%s: round is NULL", fn);
     if (r->finalized) return fail(CAM_E_STATE, "%s: round already finalized", fn);
-    if (r->eager && r->worker_norms)
-        return fail(CAM_E_STATE, "%s: per-worker drift of a folded round comes from its folds", fn);
     if (r->K >= CAM_KMAX) return fail(CAM_E_KMAX, "%s: more than %d workers", fn, CAM_KMAX);
     if (dtype != CAM_F32 && dtype != CAM_BF16)
         return fail(CAM_E_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
@@ -1030,6 +1028,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         fa.swa_n = a.swa_n;
         const int P = K - r->n_folded;  // accumulated after the folds: folded here
         fa.P = P;
+        fa.first_k = r->n_folded;
         fa.stride = 3 + P;
         for (int q = 0; q < CAM_KMAX; ++q)
             fa.wp[q] = q < P ? static_cast<float>(r->tokens[r->n_folded + q]) : 0.0f;
@@ -1057,12 +1056,14 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             });
             fa.chunks = p.d_chunks + c0;
             fa.partials = norm_level >= 1 ? p.d_partials + c0 : nullptr;
+            fa.worker_partials =
+                norm_level >= 2 ? p.d_worker_partials + static_cast<int64_t>(c0) * CAM_KMAX : nullptr;
             fa.n_chunks = c1 - c0;
             fa.local0 = l0;
             fa.n_local = n;
             const int grid = static_cast<int>(std::min<int64_t>(fa.n_chunks, int64_t(c->sm_count) * 2));
             ce = cam::launch_final(fa, r->dtype, r->mode, r->ema, norm_level >= 1, r->publish, r->swa,
-                                   grid, s);
+                                   norm_level >= 2, grid, s);
             ++c->launches;
         }
     };

@@ -48,7 +48,9 @@ struct FinalArgs {
     float swa_n;               // globals in the running average after this round
     int32_t stride;            // pointers per tensor in ptr[]: 3 + P
     int32_t P;                 // workers folded by this pass
+    int32_t first_k;           // arrival index of the first of them (the folds before)
     float wp[CAM_KMAX];        // (float)tokens of those workers
+    double* worker_partials;   // [chunk * CAM_KMAX + k]: their drift partials, or null
     uint32_t vec[kEagerTensors / 32];
     // per local tensor l, at ptr[l * stride]: the running sum, then the copy
     // of the new theta and of the EMA (or null), then the P workers' copies
@@ -59,7 +61,7 @@ static_assert(sizeof(FinalArgs) <= 32000, "kernel parameter block too large");
 cudaError_t launch_fold(const FoldArgs& a, int dtype, int mode, bool worker_drift, int grid,
                         cudaStream_t s);
 cudaError_t launch_final(const FinalArgs& a, int dtype, int mode, bool ema, bool norm, bool pub,
-                         bool swa, int grid, cudaStream_t s);
+                         bool swa, bool worker_drift, int grid, cudaStream_t s);
 
 // Outer orthogonalisation (ortho.cu): a per-context workspace, made at the
 // first orthogonalised commit, and the per-matrix pipeline.

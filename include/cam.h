@@ -180,8 +180,7 @@ int cam_merge_begin(cam_ctx* ctx, int64_t round, int32_t fragment, cam_round** o
  * Every accumulate of one round must use the same dtype. On a round that
  * has folded workers (cam_merge_fold), accumulated workers come after the
  * folds and are folded, in their order, by the commit's final pass.
- * Errors: CAM_E_ARG, CAM_E_STATE (already finalized; a folded round that
- * reports per-worker drift), CAM_E_KMAX.
+ * Errors: CAM_E_ARG, CAM_E_STATE (already finalized), CAM_E_KMAX.
  */
 int cam_merge_accumulate(cam_round* rd, const void* const* ckpt, cam_dtype dtype,
                          int64_t tokens);
@@ -224,7 +223,7 @@ int cam_merge_accumulate_host(cam_round* rd, const void* const* ckpt, cam_dtype 
  * - cam_merge_finalize must later name that mode;
  * - folds come first: once a worker has been accumulated, no more folds;
  * - per-worker drift (cam_worker_drift_norm) must be asked for before the
- *   first fold, and then every worker is folded;
+ *   first fold;
  * - orthogonalisation is not available.
  *
  * Successive folds of a round may use different streams; the library orders

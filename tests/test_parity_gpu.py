@@ -1188,31 +1188,36 @@ def test_folded_round_equals_accumulated_round_bitwise(mode, dtype, ema, swa, no
         st.merger.close()
 
 
-@pytest.mark.parametrize("mode,dtype,ema,swa,norms,publish,host,last", [
-    ("mean", "f32", True, False, True, True, True, 1),     # the e2e pattern: pinned host in and out
-    ("delta", "bf16", True, False, True, True, False, 1),
-    ("delta", "f32", False, True, False, False, True, 2),
-    ("mean", "bf16", False, True, True, False, False, 3),  # every included worker accumulated
+@pytest.mark.parametrize("mode,dtype,ema,swa,norms,wnorms,publish,host,last", [
+    ("mean", "f32", True, False, True, False, True, True, 1),   # the e2e pattern: pinned host in and out
+    ("delta", "bf16", True, False, True, True, True, False, 1),
+    ("delta", "f32", False, True, False, False, False, True, 2),
+    ("mean", "f32", True, False, True, True, False, True, 2),
+    ("mean", "bf16", False, True, True, True, False, False, 3),  # every included worker accumulated
 ])
-def test_folded_round_with_its_last_arrivals_accumulated(mode, dtype, ema, swa, norms, publish,
-                                                         host, last):
+def test_folded_round_with_its_last_arrivals_accumulated(mode, dtype, ema, swa, norms, wnorms,
+                                                         publish, host, last):
     """Folding the first arrivals and accumulating the last ones (folded by the
     commit's final pass) gives the bits of a round whose workers are all
-    accumulated, published copies included."""
+    accumulated, published copies included; each worker's drift equals, bit
+    for bit, what a fold of that worker reports."""
     wl = dataclasses.replace(
         _custom(STAGED_SIZES, K=4, mode=mode, dtype=dtype, ema=ema, norms=norms, n_masked=1,
                 rounds=((0, -1), (1, -1))), swa=swa)
     g = W.make_global(wl, 14, DEV)
-    acc, mixed = make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV)
+    acc, mixed, folded = (make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV),
+                          make_gpu_state(wl, g, DEV))
     ost = oracle_state_from(g, wl)
     for idx, (rnd, _) in enumerate(wl.rounds):
         draw = W.draw_round(wl, idx, 14)
         workers = [W.make_worker(wl, g, rnd, k, 14, DEV) for k in range(wl.K)]
         if host:
             workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
-        oa = _fold_round(acc, wl, rnd, workers, draw, norms=norms, wnorms=False, publish=publish)
-        om = _fold_round(mixed, wl, rnd, workers, draw, norms=norms, wnorms=False, publish=publish,
+        oa = _fold_round(acc, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish)
+        om = _fold_round(mixed, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=publish,
                          streams=[torch.cuda.current_stream()], pub_host=host, accumulate_last=last)
+        of = _fold_round(folded, wl, rnd, workers, draw, norms=norms, wnorms=wnorms, publish=False,
+                         streams=[torch.cuda.current_stream()])
         oracle_round(ost, wl, rnd, -1, workers, draw)
         torch.cuda.synchronize()
         for name in ("theta", "m", "e", "swa"):
@@ -1227,14 +1232,17 @@ def test_folded_round_with_its_last_arrivals_accumulated(mode, dtype, ema, swa, 
                 if mixed.e is not None:
                     assert torch.equal(om["e_pub"][t].cpu().view(torch.int32),
                                        mixed.e.views[t].cpu().view(torch.int32))
-        for key in ("pt", "pf"):
+        for key in ("pt", "pf", "pwt", "pw"):
             if key in oa:
                 x, y = om[key].cpu().numpy(), oa[key].cpu().numpy()
                 assert (x >= 0).all(), f"{key}: norm not written"
                 assert np.all(np.abs(x - y) <= NORM_RTOL * np.abs(y) + 1e-300), f"{key}: {x} vs {y}"
         if last < len(draw.included):  # at least one fold: the commit takes the final pass
             assert mixed.merger.last_commit()["form"] == B.FORM_FOLDED
-    for st in (acc, mixed):
+            for key in ("pwt", "pw"):   # the same per-worker sums as the folds compute
+                if key in of:
+                    assert torch.equal(om[key], of[key]), key
+    for st in (acc, mixed, folded):
         assert st.merger.status() == 0
         st.merger.close()
 
@@ -1598,11 +1606,16 @@ def test_fold_rules():
     want = np.float32(0) - np.float32(0.7) * (np.float32(-1) + np.float32(0.9) * np.float32(-1))
     assert torch.equal(th[0], torch.full((4096,), float(want), device=DEV))
     rd = mg.begin(2)
-    rd.worker_drift_norm(torch.zeros(2, dtype=torch.float64, device=DEV), None)
+    pw = torch.full((2,), -1.0, dtype=torch.float64, device=DEV)
+    rd.worker_drift_norm(None, pw)
     rd.fold(x, 1, B.DELTA_NESTEROV)
-    with pytest.raises(B.StateError):          # per-worker drift comes from folds only
-        rd.accumulate(x, 1)
-    rd.abort()
+    rd.accumulate(x, 1)                        # its drift comes from the commit's final pass
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.commit()
+    torch.cuda.synchronize()
+    d = abs(1.0 - float(want))                 # both workers sit at 1, theta was at `want`
+    assert torch.equal(pw[0], pw[1])
+    assert abs(pw[0].item() - 64.0 * d) <= 1e-6 * 64.0 * d
     assert mg.status() == 0
     mg.close()
 
