@@ -94,6 +94,7 @@ def test_null_handles_rejected():
     assert lib.cam_ctx_status(None, None) == B.E_ARG
     assert lib.cam_ctx_staged_count(None, None) == B.E_ARG
     assert lib.cam_ctx_last_commit(None, None) == B.E_ARG
+    assert lib.cam_stream_capturing(None, None) == B.E_ARG
     assert "NULL" in B.last_error()
     lib.cam_ctx_destroy(None)  # no-op
 
