@@ -109,6 +109,7 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
            "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_stream_capturing",
+           "cam_ctx_get_quorum", "cam_ctx_set_quorum",
            "cam_merge_round_noalloc", "cam_last_error", "cam_version")
 
 NOALLOC_MAX_TENSORS = 4096
@@ -156,6 +157,8 @@ def lib() -> ctypes.CDLL:
     L.cam_ctx_staged_count.argtypes = [vp, ctypes.POINTER(i64)]
     L.cam_ctx_last_commit.argtypes = [vp, ctypes.POINTER(CommitRecord)]
     L.cam_stream_capturing.argtypes = [vp, ctypes.POINTER(i32)]
+    L.cam_ctx_get_quorum.argtypes = [vp, ctypes.POINTER(i32)]
+    L.cam_ctx_set_quorum.argtypes = [vp, i32]
     L.cam_merge_round_noalloc.argtypes = [i32, ctypes.POINTER(i64), vpp, vpp, vpp, i32, vpp,
                                           ctypes.c_int, ctypes.POINTER(i64), ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, i32, ctypes.c_float,
@@ -552,6 +555,18 @@ class Merger:
         """Waits for the device, then returns its status word (0: no merge
         pass gave up waiting on a barrier)."""
         return ctx_status(self.ctx)
+
+    @property
+    def quorum(self) -> int:
+        """Participants a commit needs; lower it to merge the leftovers of a
+        shrunken fleet (down to 1)."""
+        out = ctypes.c_int32()
+        _check(lib().cam_ctx_get_quorum(self.ctx, ctypes.byref(out)))
+        return out.value
+
+    @quorum.setter
+    def quorum(self, q: int) -> None:
+        _check(lib().cam_ctx_set_quorum(self.ctx, int(q)))
 
     @property
     def last_round(self) -> int:

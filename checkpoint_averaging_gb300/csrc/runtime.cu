@@ -1271,6 +1271,20 @@ CAM_API int cam_ctx_get_last_round(const cam_ctx* c, int64_t* out) {
     return CAM_OK;
 }
 
+CAM_API int cam_ctx_get_quorum(const cam_ctx* c, int32_t* out) {
+    if (!c || !out) return fail(CAM_E_ARG, "cam_ctx_get_quorum: NULL argument");
+    *out = c->quorum;
+    return CAM_OK;
+}
+
+CAM_API int cam_ctx_set_quorum(cam_ctx* c, int32_t quorum) {
+    if (!c) return fail(CAM_E_ARG, "cam_ctx_set_quorum: ctx is NULL");
+    if (quorum < 1 || quorum > CAM_KMAX)
+        return fail(CAM_E_ARG, "cam_ctx_set_quorum: quorum %d outside [1, %d]", quorum, CAM_KMAX);
+    c->quorum = quorum;
+    return CAM_OK;
+}
+
 CAM_API int cam_ctx_set_last_round(cam_ctx* c, int64_t round) {
     if (!c) return fail(CAM_E_ARG, "cam_ctx_set_last_round: ctx is NULL");
     if (!c->open.empty()) return fail(CAM_E_STATE, "cam_ctx_set_last_round: a round is open");

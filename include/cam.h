@@ -378,6 +378,16 @@ int cam_fragment_info(const cam_ctx* ctx, int32_t fragment, int32_t* n_tensors,
 int cam_ctx_get_last_round(const cam_ctx* ctx, int64_t* out);
 int cam_ctx_set_last_round(cam_ctx* ctx, int64_t round);
 
+/* The quorum later commits require, changed without rebuilding the context:
+ * a merger left with fewer live workers merges the leftovers with a lower
+ * quorum, down to a single participant ("Pythia-14M on four rented GPUs and a
+ * bucket", the run's last round had one participant; "DiffuRefill-1B"
+ * technical report, section 3, "Failure handling": the merger can go on with
+ * N = 1). Applies to rounds committed afterwards, open ones included.
+ * Errors: CAM_E_ARG (NULL, or quorum outside [1, CAM_KMAX]). */
+int cam_ctx_get_quorum(const cam_ctx* ctx, int32_t* out);
+int cam_ctx_set_quorum(cam_ctx* ctx, int32_t quorum);
+
 /* Kernels this context has launched so far (merge passes, norm passes and
  * the CAM_INIT_* work), for accounting what a timed region ran. */
 int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);

@@ -95,6 +95,8 @@ def test_null_handles_rejected():
     assert lib.cam_ctx_staged_count(None, None) == B.E_ARG
     assert lib.cam_ctx_last_commit(None, None) == B.E_ARG
     assert lib.cam_stream_capturing(None, None) == B.E_ARG
+    assert lib.cam_ctx_get_quorum(None, None) == B.E_ARG
+    assert lib.cam_ctx_set_quorum(None, 1) == B.E_ARG
     assert "NULL" in B.last_error()
     lib.cam_ctx_destroy(None)  # no-op
 

@@ -1389,6 +1389,29 @@ def test_folded_and_orthogonalised_rounds_captured_in_a_cuda_graph():
         mg_g.close()
 
 
+def test_quorum_lowered_for_the_leftovers():
+    """A merger whose fleet shrank lowers the quorum without a new context and
+    merges the single remaining worker (plain replacement returns it)."""
+    th = [torch.zeros(5000, device=DEV)]
+    mg = B.Merger(th, quorum=3)
+    x = [torch.randn(5000, device=DEV)]
+    rd = mg.begin(0)
+    rd.accumulate(x, 1)
+    rd.finalize(B.MEAN_REPLACE)
+    with pytest.raises(B.QuorumError):
+        rd.commit()
+    assert mg.quorum == 3
+    mg.quorum = 1                       # applies to the open round too
+    rd.commit()
+    torch.cuda.synchronize()
+    assert torch.equal(th[0], x[0])
+    for bad in (0, 9):
+        with pytest.raises(B.ArgError):
+            mg.quorum = bad
+    assert mg.quorum == 1
+    mg.close()
+
+
 def test_dropped_and_orphaned_round_handles():
     """A round dropped while open is aborted (its fragment takes a new round);
     closing the merger with a round open invalidates that round's handle, so
