@@ -185,6 +185,58 @@ def test_ragged_and_empty_tensors(dtype, mode):
     run_full(_custom(RAGGED, K=3, mode=mode, dtype=dtype), seed=7)
 
 
+def _drift_norm_fp64(delta_of, n, step=1 << 27):
+    """sqrt(sum delta^2) in fp64 over [0, n), in slices; delta_of(a, b) gives
+    the fp32 drift of elements [a, b) as a device tensor."""
+    s = 0.0
+    for a in range(0, n, step):
+        d = delta_of(a, min(n, a + step)).double()
+        s += float(torch.dot(d, d))
+    return math.sqrt(s)
+
+
+@pytest.mark.parametrize("mode,fold", [("mean", False), ("mean", True), ("delta", False)])
+def test_tensor_of_more_than_2_pow_31_elements(mode, fold):
+    """One tensor of 2^31 + 13 elements (and a small one after it): 64-bit
+    element offsets in every form. Plain mean + EMA takes the staged form,
+    Nesterov + EMA the register form, fold=True the fold and final passes.
+    Sampled elements, 2^31 and 2^32 neighbourhoods included, match the
+    oracle; the big tensor's drift norm matches its definition summed in
+    fp64."""
+    n = (1 << 31) + 13
+    wl = _custom([n, 2049], K=2, mode=mode, dtype="bf16", ema=True, norms=True)
+    g = W.make_global(wl, 17, DEV)
+    st = make_gpu_state(wl, g, DEV)
+    draw = W.draw_round(wl, 0, 17)
+    workers = [W.make_worker(wl, g, 0, k, 17, DEV) for k in range(wl.K)]
+    rng = np.random.default_rng(17)
+    edge = [(1 << 31) + o for o in (-9, -8, -1, 0, 1, 7, 8, 12)]
+    idxs = [np.unique(np.concatenate([sample_indices(n, 2048, rng), np.array(edge, np.int64)])),
+            sample_indices(2049, 2048, rng)]
+    before = gather_state(st, [0, 1], idxs)
+    th0 = st.theta.views[0].clone()
+    pt, pf = gpu_round(st, wl, 0, -1, workers, draw, fold=fold)
+    torch.cuda.synchronize()
+    sampled_round_check(wl, st, -1, workers, draw, idxs, before, f"2^31+13 elements, {mode}")
+    xs = [workers[k].views[0] for k in draw.included]
+
+    def delta_of(a, b):
+        th = th0[a:b]
+        if mode == "mean":      # theta' - theta, theta' = (x_1 + x_2) / 2
+            return (xs[0][a:b].float() + xs[1][a:b].float()) / 2 - th
+        w = [float(draw.tokens[k]) for k in draw.included]   # Delta = sum w_k (x_k - theta) / W
+        s = torch.tensor(w[0], device=th.device) * (xs[0][a:b].float() - th)
+        s = s + torch.tensor(w[1], device=th.device) * (xs[1][a:b].float() - th)
+        return s / float(sum(draw.tokens[k] for k in draw.included))
+
+    want = _drift_norm_fp64(delta_of, n)
+    got = pt[0].item()
+    assert abs(got - want) <= NORM_RTOL * want, (got, want)
+    assert abs(pf.item() - math.sqrt(got ** 2 + pt[1].item() ** 2)) <= 1e-9 * pf.item()
+    assert st.merger.status() == 0
+    st.merger.close()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_k1_replacement_returns_input_bitwise(dtype):
     wl = _custom([4099, 65536], K=1, mode="mean", dtype=dtype, ema=False, norms=False)
