@@ -40,7 +40,7 @@ METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params
 KERNEL_SRCS = [os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", f)
                for f in ("merge_fused.cuh", "merge_fused_f32.cu", "merge_fused_bf16.cu",
                          "merge_staged.cuh", "merge_staged_f32.cu", "merge_staged_bf16.cu",
-                         "merge_device.cuh", "cam_internal.h")]
+                         "merge_device.cuh", "norm_device.cuh", "cam_internal.h")]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
 

@@ -25,6 +25,7 @@ MEAN_REPLACE, DELTA_NESTEROV = 0, 1
 INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
 NO_STAGING = 8
 TIME_COMMITS = 16
+NO_FUSED_FINISH = 32
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
@@ -450,12 +451,14 @@ class Merger:
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
                  zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
-                 staging=True, time_commits=False):
+                 staging=True, time_commits=False, fused_finish=True):
         """rows: optional per-tensor matrix rows (default: the tensors' first
         dimension), used by orthogonalised rounds. staging=False keeps every
         merge pass on the register form (the staged form gives the same
         results). time_commits=True times each commit's device work
-        (last_commit()["ms"])."""
+        (last_commit()["ms"]). fused_finish=False always launches the
+        separate norm pass (small rounds otherwise finish their norms in the
+        merge pass; the same bits)."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -481,7 +484,8 @@ class Merger:
         self.n_fragments = n_fragments
         flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
                 (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
-                (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0)
+                (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0) | \
+                (0 if fused_finish else NO_FUSED_FINISH)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,

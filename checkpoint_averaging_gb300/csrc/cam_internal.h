@@ -34,6 +34,10 @@ constexpr int kStRedSlots = 2;                 // drift hand-over buffers (doubl
 constexpr int kStSmemBytes = 224 * 1024;       // dynamic shared memory: ring + hand-over
 static_assert(kChunkQuantum % kStTile == 0, "tiles must not straddle chunks");
 
+// Fragments of at most this many chunks (with the round's drift norms asked
+// for) take the register form with the norm finish fused into its last block.
+constexpr int kFuseMaxChunks = 4096;
+
 // Bits of the context's device status word (cam_ctx_status).
 constexpr int32_t kStatusWaitTimeout = 1;  // a staged pass gave up waiting on a barrier
 
@@ -53,6 +57,22 @@ struct TensorSlot {
     float* e;
     float* swa;  // uniform running average of the globals, or null
     int64_t numel;
+};
+
+// Parameter block of the deterministic norm finish.
+struct NormArgs {
+    const double* partials;     // [n_chunks of the fragment]
+    const int32_t* first_chunk; // [n_tensors + 1]: tensor t owns chunks [first[t], first[t+1])
+    int32_t n_tensors;
+    double* tsq;                // scratch [n_tensors]: squared norms
+    double* per_tensor;         // output or null
+    double* per_fragment;       // output or null
+    // per-worker drift (K > 0 when asked for)
+    int32_t K;
+    const double* worker_partials;  // [n_chunks * CAM_KMAX]
+    double* worker_tsq;             // scratch [n_tensors * CAM_KMAX]
+    double* per_worker_tensor;      // output [K * n_tensors] or null
+    double* per_worker;             // output [K] or null
 };
 
 // Parameter block of one launch of the fused merge pass. The launch covers
@@ -75,6 +95,12 @@ struct MergeArgs {
     int32_t* status;          // device status word (kStatus* bits), staged pass only
     int32_t st_stages;        // staged pass: stages in the shared-memory ring
     int32_t st_stage_bytes;   // staged pass: bytes of one stage
+    // Register pass with the norm finish fused (MergeVariant::fin): the last
+    // block to finish its chunks (counted on *fin_counter, which it resets to
+    // 0) finishes the norms as the norm pass would, so that pass is not
+    // launched.
+    unsigned int* fin_counter;
+    NormArgs fin;
     uint32_t vec[(kXCap + 31) / 32];  // bit l: tensor local0+l takes the vector path
     // x[l*stride + k]: worker k's copy of tensor local0+l; when publishing,
     // x[l*stride + K] and x[l*stride + K + 1] take the new theta and EMA. The
@@ -83,21 +109,6 @@ struct MergeArgs {
 };
 static_assert(sizeof(MergeArgs) <= 32000, "kernel parameter block too large");
 
-// Parameter block of the deterministic norm finish.
-struct NormArgs {
-    const double* partials;     // [n_chunks of the fragment]
-    const int32_t* first_chunk; // [n_tensors + 1]: tensor t owns chunks [first[t], first[t+1])
-    int32_t n_tensors;
-    double* tsq;                // scratch [n_tensors]: squared norms
-    double* per_tensor;         // output or null
-    double* per_fragment;       // output or null
-    // per-worker drift (K > 0 when asked for)
-    int32_t K;
-    const double* worker_partials;  // [n_chunks * CAM_KMAX]
-    double* worker_tsq;             // scratch [n_tensors * CAM_KMAX]
-    double* per_worker_tensor;      // output [K * n_tensors] or null
-    double* per_worker;             // output [K] or null
-};
 
 enum Variant : int { kDtF32 = 0, kDtBF16 = 1 };
 
@@ -113,6 +124,7 @@ struct MergeVariant {
     bool ema;
     int norm_level;
     bool pub, swa;
+    bool fin = false;  // register form: finish the norms in the pass's last block
 };
 using MergeFn = void (*)(MergeArgs);
 MergeFn pick_merge_f32(const MergeVariant& v);

@@ -14,18 +14,21 @@
 //      per chunk.
 // Squares are summed in fp32 within a thread (at most 64 elements of one
 // chunk), then in fp64 across the warp and the block in a fixed order, so the
-// partials are reproducible bit for bit.
+// partials are reproducible bit for bit. With fuse_finish the launch also
+// finishes the norms from those partials in its last block (norm_device.cuh's
+// finish_norms, the same sums as the separate norm pass).
 #pragma once
 
 #include <cuda_runtime.h>
 
 #include "cam_internal.h"
 #include "merge_device.cuh"
+#include "norm_device.cuh"
 
 namespace cam {
 namespace dev {
 
-template <typename XT, int MODE, bool EMA, int NL, bool PUB, bool SWA>
+template <typename XT, int MODE, bool EMA, int NL, bool PUB, bool SWA, bool FIN = false>
 __global__ void __launch_bounds__(kThreads, 2)
     merge_fused(const __grid_constant__ MergeArgs a) {
     constexpr bool NORM = NL >= 1;
@@ -90,24 +93,44 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     }
+    if constexpr (NORM && FIN) {
+        // Every block passes here once, after its last chunk. The partial
+        // writes are fenced before the count; the block that brings the count
+        // to gridDim.x sees every block's partials (read through L2), finishes
+        // the norms and resets the count for the next launch.
+        __shared__ int last;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(a.fin_counter, 1u) == gridDim.x - 1;
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            finish_norms_tail(a.fin);
+            if (threadIdx.x == 0) *a.fin_counter = 0u;
+        }
+    }
+}
+
+// The fused finish exists for norm level 1 (the round's drift): with
+// per-worker drift as well, the finish's registers would push the fp32
+// variants' main loop into spilling.
+template <typename XT, int MODE, bool EMA, bool PUB, bool SWA>
+MergeFn pick_fin(int nl, bool fin) {
+    if (nl == 0) return merge_fused<XT, MODE, EMA, 0, PUB, SWA>;
+    if (nl == 1)
+        return fin ? merge_fused<XT, MODE, EMA, 1, PUB, SWA, true> : merge_fused<XT, MODE, EMA, 1, PUB, SWA>;
+    return merge_fused<XT, MODE, EMA, 2, PUB, SWA>;
 }
 
 template <typename XT, int MODE, bool PUB, bool SWA>
-MergeFn pick_level(bool ema, int nl) {
-    if (ema) {
-        if (nl == 0) return merge_fused<XT, MODE, true, 0, PUB, SWA>;
-        if (nl == 1) return merge_fused<XT, MODE, true, 1, PUB, SWA>;
-        return merge_fused<XT, MODE, true, 2, PUB, SWA>;
-    }
-    if (nl == 0) return merge_fused<XT, MODE, false, 0, PUB, SWA>;
-    if (nl == 1) return merge_fused<XT, MODE, false, 1, PUB, SWA>;
-    return merge_fused<XT, MODE, false, 2, PUB, SWA>;
+MergeFn pick_level(bool ema, int nl, bool fin) {
+    return ema ? pick_fin<XT, MODE, true, PUB, SWA>(nl, fin) : pick_fin<XT, MODE, false, PUB, SWA>(nl, fin);
 }
 
 template <typename XT, bool PUB, bool SWA>
 MergeFn pick_mode(const MergeVariant& v) {
-    return v.mode == kDelta ? pick_level<XT, kDelta, PUB, SWA>(v.ema, v.norm_level)
-                            : pick_level<XT, kMean, PUB, SWA>(v.ema, v.norm_level);
+    return v.mode == kDelta ? pick_level<XT, kDelta, PUB, SWA>(v.ema, v.norm_level, v.fin)
+                            : pick_level<XT, kMean, PUB, SWA>(v.ema, v.norm_level, v.fin);
 }
 
 template <typename XT>

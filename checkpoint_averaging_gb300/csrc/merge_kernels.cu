@@ -37,45 +37,7 @@ namespace {
 using namespace cam::dev;
 
 __global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int n_warps = blockDim.x >> 5;
-    for (int t = warp; t < a.n_tensors; t += n_warps) {
-        double s = lane_sum(a.partials, 1, a.first_chunk[t], a.first_chunk[t + 1], lane);
-        s = warp_sum(s);
-        if (lane == 0) a.tsq[t] = s;
-    }
-    // per worker and tensor: one warp per (tensor, worker) pair
-    for (int p = warp; p < a.n_tensors * a.K; p += n_warps) {
-        const int t = p / a.K, k = p % a.K;
-        double s = lane_sum(a.worker_partials + k, CAM_KMAX, a.first_chunk[t], a.first_chunk[t + 1],
-                            lane);
-        s = warp_sum(s);
-        if (lane == 0) a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k] = s;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        double s = 0.0;
-        for (int t = lane; t < a.n_tensors; t += 32) s += a.tsq[t];
-        s = warp_sum(s);
-        if (lane == 0 && a.per_fragment) *a.per_fragment = sqrt(s);
-    }
-    if (warp >= 1 && warp <= a.K) {  // warp 1 + k totals worker k
-        const int k = warp - 1;
-        double s = 0.0;
-        for (int t = lane; t < a.n_tensors; t += 32)
-            s += a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k];
-        s = warp_sum(s);
-        if (lane == 0 && a.per_worker) a.per_worker[k] = sqrt(s);
-    }
-    if (a.per_tensor)
-        for (int t = threadIdx.x; t < a.n_tensors; t += blockDim.x)
-            a.per_tensor[t] = sqrt(a.tsq[t]);
-    if (a.per_worker_tensor)
-        for (int p = threadIdx.x; p < a.n_tensors * a.K; p += blockDim.x) {
-            const int k = p / a.n_tensors, t = p % a.n_tensors;
-            a.per_worker_tensor[p] = sqrt(a.worker_tsq[static_cast<int64_t>(t) * CAM_KMAX + k]);
-        }
+    finish_norms<false>(a);
 }
 
 __global__ void fill_kernel(float* dst, int64_t n, float v) {

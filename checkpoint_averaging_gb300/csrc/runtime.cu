@@ -108,6 +108,7 @@ struct Plan {
     double* d_tsq = nullptr;
     double* d_worker_partials = nullptr;  // [n_chunks * CAM_KMAX]
     double* d_worker_tsq = nullptr;       // [n_tensors * CAM_KMAX]
+    unsigned int* d_fin_counter = nullptr;  // blocks done, for a pass that finishes its norms
     int32_t n_chunks() const { return static_cast<int32_t>(chunks.size()); }
     int32_t n_tensors() const { return static_cast<int32_t>(tensors.size()); }
 };
@@ -158,6 +159,8 @@ struct cam_ctx {
     std::vector<cam_round*> open;
     // resident blocks per SM: [dtype][mode][ema][norm level][publish][swa]
     int bps[2][2][2][3][2][2] = {};
+    int bps_fin[2][2][2][2][2] = {};  // the same for norm level 1 with the finish fused
+    bool fuse_finish = true;           // small rounds with norms finish them in the merge pass
     std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
 
     Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
@@ -261,7 +264,7 @@ int validate_desc(const cam_ctx_desc* d) {
         return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
     if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
-                     CAM_NO_STAGING | CAM_TIME_COMMITS))
+                     CAM_NO_STAGING | CAM_TIME_COMMITS | CAM_NO_FUSED_FINISH))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -369,6 +372,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         bytes += round_up(sizeof(double) * p.tensors.size(), 256);
         bytes += round_up(sizeof(double) * CAM_KMAX * p.chunks.size(), 256);
         bytes += round_up(sizeof(double) * CAM_KMAX * p.tensors.size(), 256);
+        bytes += 256;  // the fused finish's block counter
     }
     ce = cudaMalloc(&c->dev_block, std::max<size_t>(bytes, 256));
     if (ce != cudaSuccess) {
@@ -405,6 +409,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         p.d_worker_partials = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
         o = carve(sizeof(double) * CAM_KMAX * p.tensors.size());
         p.d_worker_tsq = reinterpret_cast<double*>(static_cast<unsigned char*>(c->dev_block) + o);
+        o = carve(sizeof(unsigned int));  // zero from the upload below
+        p.d_fin_counter = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(c->dev_block) + o);
     }
     ce = cudaMemcpy(c->dev_block, host.data(), bytes, cudaMemcpyHostToDevice);
     if (ce != cudaSuccess) {
@@ -421,6 +427,16 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
                                 1, cam::merge_blocks_per_sm(cam::MergeVariant{
                                        dt, md, em != 0, nl, pb != 0, sw != 0}));
 
+    for (int dt = 0; dt < 2; ++dt)
+        for (int md = 0; md < 2; ++md)
+            for (int em = 0; em < 2; ++em)
+                for (int pb = 0; pb < 2; ++pb)
+                    for (int sw = 0; sw < 2; ++sw) {
+                        cam::MergeVariant v{dt, md, em != 0, 1, pb != 0, sw != 0};
+                        v.fin = true;
+                        c->bps_fin[dt][md][em][pb][sw] = std::max(1, cam::merge_blocks_per_sm(v));
+                    }
+    c->fuse_finish = !(d->flags & CAM_NO_FUSED_FINISH);
     c->staged = !(d->flags & CAM_NO_STAGING);
     c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
     for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
@@ -966,6 +982,17 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     // register form is kept.
     const int state_writes = 1 + int(delta) + int(r->ema) + int(r->swa);
     const bool staged_ok = c->staged && !r->host_workers && st_stages >= 2 && state_writes <= 2;
+    // Small rounds with the round's drift norms finish them in the merge pass
+    // itself (register form, last block): one launch fewer, the same sums.
+    const NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
+                      norm_level >= 2 ? K : 0, p.d_worker_partials, p.d_worker_tsq,
+                      r->out_worker_tensor, r->out_worker};
+    const bool fuse = c->fuse_finish && norm_level == 1 && !r->eager && !r->ortho &&
+                      p.n_chunks() > 0 && p.n_chunks() <= cam::kFuseMaxChunks && T <= per_launch;
+    cam::MergeVariant variant_fin = variant;
+    variant_fin.fin = true;
+    a.fin = na;
+    a.fin_counter = p.d_fin_counter;
     a.status = c->d_status;
     a.st_stages = st_stages;
     a.st_stage_bytes = static_cast<int32_t>(st_bytes);
@@ -1003,7 +1030,12 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             a.n_chunks = c1 - c0;
             a.local0 = l0;
             a.n_local = n;
-            if (staged_ok && all_vec) {  // one block per SM
+            if (fuse) {  // a single launch covering the whole fragment
+                const int b = c->bps_fin[r->dtype][r->mode][r->ema][r->publish][r->swa];
+                const int grid =
+                    static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * b));
+                ce = cam::launch_merge(a, variant_fin, grid, s);
+            } else if (staged_ok && all_vec) {  // one block per SM
                 const int grid = static_cast<int>(std::min<int64_t>(a.n_chunks, c->sm_count));
                 ce = cam::launch_merge_staged(a, variant, grid, s);
                 ++c->staged_launches;
@@ -1125,10 +1157,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         }
         if (ce == cudaSuccess && !cap) ce = cudaEventRecord(c->ortho_ev, s);
     }
-    if (ce == cudaSuccess && norm_level >= 1) {
-        NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
-                    norm_level >= 2 ? K : 0, p.d_worker_partials, p.d_worker_tsq,
-                    r->out_worker_tensor, r->out_worker};
+    if (ce == cudaSuccess && norm_level >= 1 && !fuse) {
         ce = cam::launch_norm_finish(na, s);
         ++c->launches;
     }

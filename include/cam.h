@@ -100,6 +100,7 @@ typedef enum {
 #define CAM_INIT_ZERO_SWA 4u        /* at create: running averages <- 0, no globals folded */
 #define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
 #define CAM_TIME_COMMITS 16u        /* time each commit's device work (cam_ctx_last_commit) */
+#define CAM_NO_FUSED_FINISH 32u     /* always finish drift norms in a separate norm pass */
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
@@ -411,6 +412,13 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * form, so they keep it. Rounds with workers from cam_merge_accumulate_host
  * always use the register form, and so does a context created with
  * CAM_NO_STAGING.
+ *
+ * Small rounds that ask for the round's drift norms (not per-worker drift),
+ * whose fragment has at most 4,096 chunks (about 64M elements) and fits one
+ * launch, take the register form and finish the norms in that same pass: the
+ * pass's last block to finish sums the per-chunk partials exactly as the norm
+ * pass would, so the results are the same bits, one launch fewer. A context
+ * created with CAM_NO_FUSED_FINISH always launches the separate norm pass.
  *
  * Every wait of the staged form on one of its barriers gives up after a few
  * seconds. It then sets CAM_STATUS_WAIT_TIMEOUT in the context's device status

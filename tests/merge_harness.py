@@ -65,7 +65,8 @@ class GpuState:
     swa: W.Arena | None = None
 
 
-def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True) -> GpuState:
+def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
+                   fused_finish=True) -> GpuState:
     theta = W.empty_arena(g.numels, torch.float32, dev)
     theta.flat.copy_(g.flat)
     m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
@@ -77,7 +78,8 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True) -
     mg = B.Merger(theta.views, momentum=None if m is None else m.views,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
-                  swa=None if swa is None else swa.views, staging=staging)
+                  swa=None if swa is None else swa.views, staging=staging,
+                  fused_finish=fused_finish)
     return GpuState(theta, m, e, mg, swa)
 
 

@@ -1035,7 +1035,8 @@ def test_staged_and_register_forms_agree_bitwise(dtype, mode, ema, norms, swa, K
     wl = dataclasses.replace(_custom(STAGED_SIZES, K=K, mode=mode, dtype=dtype, ema=ema,
                                      norms=norms, rounds=((0, -1), (1, -1))), swa=swa)
     g = W.make_global(wl, 3, DEV)
-    states = [make_gpu_state(wl, g, DEV, staging=sg) for sg in (True, False)]
+    # the separate norm pass on both sides, so small rounds keep each form
+    states = [make_gpu_state(wl, g, DEV, staging=sg, fused_finish=False) for sg in (True, False)]
     ost = oracle_state_from(g, wl)
     for idx, (rnd, frag) in enumerate(wl.rounds):
         draw = W.draw_round(wl, idx, 3)
@@ -1067,25 +1068,87 @@ def test_staged_and_register_forms_agree_bitwise(dtype, mode, ema, norms, swa, K
         st.merger.close()
 
 
-def test_staged_form_is_used_and_reproducible():
-    """Two identical staged runs agree bit for bit, norms included, and a round
-    of device workers launches exactly one merge pass plus the norm finish."""
+@pytest.mark.parametrize("fused", [False, True])
+def test_staged_form_is_used_and_reproducible(fused):
+    """Two identical runs agree bit for bit, norms included, and a round of
+    device workers launches exactly one merge pass plus the norm finish, or
+    one pass alone when it finishes its norms itself (a small round)."""
     wl = _custom([1 << 20, 3, 2049, 5_000_000], K=4, mode="delta", dtype="bf16", ema=True)
     g = W.make_global(wl, 0, DEV)
     res = []
     for _ in range(2):
-        st = make_gpu_state(wl, g, DEV)
+        st = make_gpu_state(wl, g, DEV, fused_finish=fused)
         draw = W.draw_round(wl, 0, 0)
         workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
         n0 = st.merger.launch_count
         pt, pf = gpu_round(st, wl, 0, -1, workers, draw)
-        assert st.merger.launch_count - n0 == 2
+        assert st.merger.launch_count - n0 == (1 if fused else 2)
         torch.cuda.synchronize()
         res.append((st.theta.flat.clone(), st.m.flat.clone(), st.e.flat.clone(), pt.clone(), pf.clone()))
         assert st.merger.status() == 0
         st.merger.close()
     for x, y in zip(*res):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("mode,dtype,ema,publish,host", [
+    ("delta", "f32", False, False, False),   # the Pythia rounds' variant
+    ("mean", "bf16", True, False, False),    # a staged round without the fusion
+    ("delta", "bf16", True, True, False),
+    ("mean", "f32", False, False, True),     # pinned host workers
+])
+def test_fused_norm_finish_equals_the_norm_pass(mode, dtype, ema, publish, host):
+    """Small rounds whose merge pass finishes the drift norms itself give the
+    bits of the same rounds with the separate norm pass: theta, m, e, the
+    published copies and the norms, over several rounds and fragments (the
+    per-plan block counter is reset by every launch)."""
+    wl = _custom(RAGGED + [300_001], K=3, mode=mode, dtype=dtype, ema=ema, norms=True,
+                 frags=[i % 2 for i in range(len(RAGGED) + 1)], n_fragments=2,
+                 rounds=((0, 0), (1, 1), (2, -1), (3, 0)))
+    g = W.make_global(wl, 18, DEV)
+    # the fused pass is the register form: compare with that form's norm pass
+    states = [make_gpu_state(wl, g, DEV), make_gpu_state(wl, g, DEV, staging=False, fused_finish=False)]
+    for idx, (rnd, frag) in enumerate(wl.rounds):
+        draw = W.draw_round(wl, idx, 18)
+        workers = [W.make_worker(wl, g, rnd, k, 18, DEV) for k in range(wl.K)]
+        if host:
+            workers = [W.Arena(w.flat.cpu().pin_memory(), w.offsets, w.numels) for w in workers]
+        outs, launches = [], []
+        for st in states:
+            rd = st.merger.begin(rnd, frag)
+            for k in draw.included:
+                rd.accumulate(workers[k].views, draw.tokens[k])
+            code = B.DELTA_NESTEROV if mode == "delta" else B.MEAN_REPLACE
+            rd.finalize(code, wl.lr, wl.mu)
+            if ema:
+                rd.ema_update(0.9)
+            pt = torch.full((max(1, len(rd.tensors)),), -1.0, dtype=torch.float64, device=DEV)
+            pf = torch.full((1,), -1.0, dtype=torch.float64, device=DEV)
+            rd.drift_norm(pt, pf)
+            pub = None
+            if publish:
+                pub = [torch.full((st.merger.numel[t],), float("nan"), device=DEV)
+                       for t in rd.tensors]
+                rd.publish(pub)
+            n0 = st.merger.launch_count
+            rd.commit()
+            launches.append(st.merger.launch_count - n0)
+            outs.append((pt, pf, pub))
+        torch.cuda.synchronize()
+        fused, plain = states
+        for name in ("theta", "m", "e"):
+            x, y = getattr(fused, name), getattr(plain, name)
+            if x is not None:
+                assert torch.equal(x.flat.view(torch.int32), y.flat.view(torch.int32)), (rnd, name)
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]), rnd
+        assert (outs[0][0] >= 0).all() and outs[0][1].item() >= 0
+        if publish:
+            for a, b in zip(outs[0][2], outs[1][2]):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert launches[0] == launches[1] - 1, launches   # the norm pass is not launched
+    for st in states:
+        assert st.merger.status() == 0
+        st.merger.close()
 
 
 @pytest.mark.parametrize("mode,ema,swa,host,staging,want_staged", [
@@ -1724,16 +1787,16 @@ def test_commit_record():
     mg = B.Merger(th, momentum=m, ema=e, swa=sw, quorum=1, time_commits=True)
     xs = [[(t + 1e-3 * torch.randn_like(t)).to(torch.bfloat16) for t in th] for _ in range(3)]
 
-    rd = mg.begin(0)                    # Nesterov + norms: theta, m written -> staged
-    for x in xs:
+    rd = mg.begin(0)                    # Nesterov + norms, a small round: the register pass
+    for x in xs:                        # finishes the norms itself, one launch
         rd.accumulate(x, 1000)
     rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
     rd.drift_norm(torch.zeros(3, dtype=torch.float64, device=DEV), None)
     rd.commit()
     rec = mg.last_commit()
     assert (rec["round"], rec["fragment"], rec["K"], rec["mode"]) == (0, -1, 3, B.DELTA_NESTEROV)
-    assert rec["form"] == B.FORM_STAGED and rec["elements"] == n
-    assert rec["bytes"] == (3 * 2 + 4 + 4 + 8) * n and rec["launches"] == 2 and rec["ms"] > 0
+    assert rec["form"] == B.FORM_REGISTER and rec["elements"] == n
+    assert rec["bytes"] == (3 * 2 + 4 + 4 + 8) * n and rec["launches"] == 1 and rec["ms"] > 0
 
     rd = mg.begin(1)                    # the same, folded
     for x in xs:
@@ -1753,5 +1816,14 @@ def test_commit_record():
     rd.commit()
     rec = mg.last_commit()
     assert rec["form"] == B.FORM_REGISTER and rec["bytes"] == (3 * 2 + 4 + 8 + 8) * n
+
+    rd = mg.begin(3)                    # Nesterov, no norms: theta, m written -> staged
+    for x in xs:
+        rd.accumulate(x, 1000)
+    rd.finalize(B.DELTA_NESTEROV, 0.7, 0.9)
+    rd.commit()
+    rec = mg.last_commit()
+    assert rec["form"] == B.FORM_STAGED and rec["bytes"] == (3 * 2 + 4 + 4 + 8) * n
+    assert rec["launches"] == 1 and rec["ms"] > 0
     assert mg.status() == 0
     mg.close()
