@@ -354,7 +354,8 @@ int cam_merge_publish(cam_round* rd, float* const* theta_out, float* const* ema_
 
 /*
  * Closes the round: checks it (finalized, quorum met, weights valid), then
- * launches the fused merge pass (and the norm pass if asked) on `stream`
+ * launches the fused merge pass (and the norm pass if asked, unless the round
+ * is small enough for the merge pass to finish the norms itself) on `stream`
  * (a cudaStream_t; NULL = legacy default stream) and frees the round handle.
  * Returns before the device work finishes. On CAM_E_STATE / CAM_E_QUORUM /
  * CAM_E_ARG, and CAM_E_NOMEM (the workspace of a context's first
