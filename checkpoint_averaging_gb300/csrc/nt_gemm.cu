@@ -1,0 +1,832 @@
+// nt_gemm.cu -- batched NT GEMMs of the Newton-Schulz iteration (outer
+// orthogonalisation, "DiffuRefill-1B" technical report, section 5.3) on the
+// fifth-generation tensor cores of sm_103a, plus a CUDA-core fp32 form.
+//
+// Tensor-core kernel nt_gemm_tc<BF16, BN, EPI>: a persistent grid of one
+// block per SM; block b takes the output tiles b, b + grid, ... Each block is
+// six warps with fixed roles:
+//
+//   warp 0 (lane 0)  TMA producer: per K step, one 128-row box of A and BN/128
+//                    boxes of B (128-byte rows, 128-byte swizzle) into a ring
+//                    of shared-memory stages, counted on the stage's "full"
+//                    mbarrier;
+//   warp 1 (lane 0)  MMA issuer: four tcgen05.mma (M = 128, N = BN, K = 32
+//                    bytes each) per stage into one of two TMEM accumulators
+//                    (2 x BN fp32 columns), tcgen05.commit releasing the
+//                    stage and, after a tile's last stage, the accumulator;
+//                    warp 1 also allocates and frees the TMEM;
+//   warps 2..5       epilogue: each owns 32 TMEM lanes (rows of the tile),
+//                    reads 32 columns at a time with tcgen05.ld, hands the
+//                    accumulator back as soon as its last columns are in
+//                    registers, and writes the tile (and, where asked, its
+//                    transpose) to global memory.
+//
+// Two accumulators let the epilogue of one tile overlap the MMAs of the next.
+// Shared-memory operands use the canonical K-major 128-byte-swizzled layout
+// that TMA writes: 8-row groups of 1,024 bytes, so the matrix descriptors
+// carry a stride of 1,024 bytes, and the four MMAs of a stage start 32 bytes
+// apart inside each swizzled row.
+//
+// Every mbarrier wait is bounded (kTcWaitLimitNs of %globaltimer). A wait that
+// runs out sets CAM_STATUS_GEMM_TIMEOUT in the status word and a block-wide abort
+// flag; every role then leaves its loop, the producer waits (bounded) for the
+// copies it issued, the MMA issuer for its MMAs, and warp 1 frees the TMEM
+// before the block exits.
+//
+// CUDA-core kernel nt_gemm_simt: 128 x 128 tiles, 8 x 8 outputs per thread,
+// fp32 fused multiply-adds; used for CAM_ORTHO_FP32.
+#include "nt_gemm.h"
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "cam_internal.h"
+
+namespace cam {
+namespace tc {
+
+constexpr int kBM = 128;                 // tile rows (TMEM lanes)
+constexpr int kTcThreads = 192;          // six warps
+constexpr int kRowBytes = 128;           // one swizzled row of a stage: the K step
+constexpr int kBoxBytes = kBM * kRowBytes;  // one 128-row TMA box: 16 KB
+constexpr int kSmemBudget = 192 * 1024;  // the stage ring
+constexpr unsigned long long kTcWaitLimitNs = 4000000000ull;
+constexpr int kEpiPart = 2;              // Gram split: fp32 partial tiles
+
+// ---- PTX wrappers ---------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of the given parity; false if the block is aborting or
+// the wait ran out (which starts the abort).
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* status) {
+    if (bar_test(bar, parity)) return true;
+    const unsigned long long t0 = now_ns();
+    while (!bar_test(bar, parity)) {
+        if (*abort_flag) return false;
+        if (now_ns() - t0 > kTcWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, CAM_STATUS_GEMM_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Three-dimensional tiled TMA load {x = K element, y = row, z = matrix}.
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1,024 bytes apart (stride byte offset), leading byte offset unused (1),
+// descriptor version 1 (bits 46-48), swizzle mode 2 = 128 B (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) |
+           (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16 (bf16 A and B) or kind::tf32: fp32
+// accumulator (bits 4-5 = 1), A/B formats (bits 7-9, 10-12: bf16 = 1,
+// tf32 = 2), both K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4
+// (bits 24-28).
+template <bool BF16, int BN>
+__device__ __forceinline__ constexpr uint32_t instr_desc() {
+    return (1u << 4) | ((BF16 ? 1u : 2u) << 7) | ((BF16 ? 1u : 2u) << 10) |
+           (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                    uint32_t accumulate) {
+    if constexpr (BF16)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- kernel arguments -------------------------------------------------------------
+
+struct alignas(128) TcArgs {
+    CUtensorMap ta;          // A: dims {K, M, batch}, box {K step, 128, 1}
+    CUtensorMap tb;          // B: dims {K, N, batch}, box {K step, 128, 1}
+    int32_t batch;
+    int32_t m_blocks;        // M / 128
+    int32_t n_blocks;        // N / BN
+    int32_t k_blocks;        // K / K step
+    int32_t splits;          // Gram: K ranges per tile
+    int32_t k_per_split;     // Gram: K steps per range
+    int32_t n_tri;           // Gram: tiles per matrix reaching the upper triangle
+    int32_t n_units;         // tiles (x splits) over the whole batch
+    float alpha, beta;
+    const void* C; int64_t ldc, sC;
+    void* Y; int64_t ldy, sY;
+    void* Yt; int64_t ldyt, sYt;
+    float* P;                // Gram split: fp32 partial of range s, matrix b at P + (s*batch+b)*M*M
+    int32_t* status;
+};
+
+// One unit of work: the tile's first rows in A and B, its matrix, its K steps
+// and (Gram split) its range.
+struct Unit {
+    int b, rb, cb, split, k0, k1;
+};
+
+template <int BN, int EPI>
+__device__ __forceinline__ Unit decode(const TcArgs& a, int u) {
+    Unit t;
+    if constexpr (EPI == kNtAxpby) {
+        const int per = a.m_blocks * a.n_blocks;
+        t.b = u / per;
+        const int rem = u - t.b * per;
+        t.rb = rem / a.n_blocks;
+        t.cb = rem - t.rb * a.n_blocks;
+        t.split = 0;
+        t.k0 = 0;
+        t.k1 = a.k_blocks;
+    } else {
+        const int per = a.splits * a.n_tri;
+        t.b = u / per;
+        int rem = u - t.b * per;
+        t.split = rem / a.n_tri;
+        int q = rem - t.split * a.n_tri;
+        // column block cb holds row blocks 0 .. (BN cb + BN - 1) / 128
+        int cb = 0;
+        for (; cb < a.n_blocks - 1; ++cb) {
+            const int cnt = min(a.m_blocks, (BN * cb + BN - 1) / kBM + 1);
+            if (q < cnt) break;
+            q -= cnt;
+        }
+        t.rb = q;
+        t.cb = cb;
+        t.k0 = t.split * a.k_per_split;
+        t.k1 = min(a.k_blocks, t.k0 + a.k_per_split);
+    }
+    return t;
+}
+
+// ---- epilogue stores -------------------------------------------------------------
+
+template <bool BF16>
+struct Store;
+
+template <>
+struct Store<true> {  // bf16, rounded to nearest-even
+    using T = __nv_bfloat16;
+    __device__ static void row32(T* dst, const float* v) {  // 64 bytes, 16-byte aligned
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            reinterpret_cast<uint4*>(dst)[q] = o;
+        }
+    }
+    __device__ static void one(T* dst, float v) { *dst = __float2bfloat16_rn(v); }
+    __device__ static void load32(const T* src, float* v) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 i = reinterpret_cast<const uint4*>(src)[q];
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&i);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[8 * q + 2 * e] = __uint_as_float(w[e] << 16);
+                v[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        }
+    }
+};
+
+template <>
+struct Store<false> {  // fp32
+    using T = float;
+    __device__ static void row32(T* dst, const float* v) {  // 128 bytes, 16-byte aligned
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+    __device__ static void one(T* dst, float v) { *dst = v; }
+    __device__ static void load32(const T* src, float* v) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 f = reinterpret_cast<const float4*>(src)[q];
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+    }
+};
+
+// ---- the tensor-core kernel --------------------------------------------------------
+
+template <bool BF16, int BN>
+struct Geo {
+    static constexpr int kBBytes = BN * kRowBytes;
+    static constexpr int kStage = kBoxBytes + kBBytes;
+    static constexpr int kStages = kSmemBudget / kStage < 8 ? kSmemBudget / kStage : 8;
+    static constexpr int kBarOffset = kStages * kStage;
+    // ring + barriers (full, empty, tmem full, tmem empty, drain) + TMEM
+    // address + abort flag, plus 1 KB to align the ring to 1,024 bytes
+    static constexpr int kSmem = kBarOffset + 8 * (2 * kStages + 5) + 16 + 1024;
+    static constexpr int kKStep = kRowBytes / (BF16 ? 2 : 4);  // elements per K step
+    static constexpr int kUmmaK = 32 / (BF16 ? 2 : 4);           // elements per MMA
+};
+
+template <bool BF16, int BN, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constant__ TcArgs a) {
+    using G = Geo<BF16, BN>;
+    using S = Store<BF16>;
+    using T = typename S::T;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::kBarOffset);
+    const uint32_t full0 = su32(bars);
+    const uint32_t empty0 = full0 + 8 * G::kStages;
+    const uint32_t tfull0 = empty0 + 8 * G::kStages;
+    const uint32_t tempty0 = tfull0 + 16;
+    const uint32_t drain = tempty0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::kStages + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr uint32_t kCols = 2 * BN;  // two accumulators
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G::kStages; ++s) {
+            bar_init(full0 + 8 * s, 1);
+            bar_init(empty0 + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            bar_init(tfull0 + 8 * i, 1);
+            bar_init(tempty0 + 8 * i, 4);  // one arrival per epilogue warp
+        }
+        bar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.ta)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tb)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(tmem_slot)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer ----
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0;  // bit s: stage s has a fill whose phase is (filled_parity >> s) & 1
+        uint32_t filled_parity = 0;
+        for (int u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
+            const Unit t = decode<BN, EPI>(a, u);
+            const int arow = t.rb * kBM, brow = t.cb * BN;
+            for (int kb = t.k0; kb < t.k1; ++kb) {
+                if (!bar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) break;
+                const uint32_t sa = su32(smem + stage * G::kStage);
+                const uint32_t fb = full0 + 8 * stage;
+                bar_expect(fb, G::kStage);
+                const int x = kb * G::kKStep;
+                tma_load(sa, &a.ta, x, arow, t.b, fb);
+#pragma unroll
+                for (int h = 0; h < BN / kBM; ++h)
+                    tma_load(sa + kBoxBytes + h * kBoxBytes, &a.tb, x, brow + h * kBM, t.b, fb);
+                issued |= 1u << stage;
+                filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == G::kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (*abort_flag) {  // let the copies in flight land before the block exits
+            for (int s = 0; s < G::kStages; ++s)
+                if ((issued >> s) & 1) {
+                    const unsigned long long t0 = now_ns();
+                    while (!bar_test(full0 + 8 * s, (filled_parity >> s) & 1))
+                        if (now_ns() - t0 > kTcWaitLimitNs) break;
+                }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        constexpr uint32_t idesc = instr_desc<BF16, BN>();
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+            const Unit t = decode<BN, EPI>(a, u);
+            if (!bar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + uint32_t(acc * BN);
+            bool ok = true;
+            for (int kb = t.k0; kb < t.k1; ++kb) {
+                if (!bar_wait(full0 + 8 * stage, phase, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = su32(smem + stage * G::kStage);
+                const uint64_t da = smem_desc(sa), db = smem_desc(sa + kBoxBytes);
+#pragma unroll
+                for (int k = 0; k < kRowBytes / 32; ++k)  // 32 bytes of K per MMA
+                    mma<BF16>(d, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc,
+                              (kb > t.k0 || k > 0) ? 1u : 0u);
+                mma_commit(empty0 + 8 * stage);
+                if (++stage == G::kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            mma_commit(tfull0 + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        if (*abort_flag) {  // every MMA issued so far completes before TMEM is freed
+            mma_commit(drain);
+            const unsigned long long t0 = now_ns();
+            while (!bar_test(drain, 0))
+                if (now_ns() - t0 > kTcWaitLimitNs) break;
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue ----
+        const int quarter = warp & 3;          // TMEM lanes 32 quarter .. + 31
+        const int r_in = quarter * 32 + lane;  // row of the tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+            const Unit t = decode<BN, EPI>(a, u);
+            // the whole warp leaves together: tcgen05.ld is warp-collective
+            const bool ok = bar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int64_t row = int64_t(t.rb) * kBM + r_in;
+            const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tbase + uint32_t(cc * 32), v);
+                if (cc == BN / 32 - 1) {  // the accumulator is free for the next tile
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(tempty0 + 8 * acc);
+                }
+                const int64_t col0 = int64_t(t.cb) * BN + cc * 32;
+                if constexpr (EPI == kNtAxpby) {
+                    if (a.beta != 0.0f) {
+                        float c[32];
+                        S::load32(static_cast<const T*>(a.C) + t.b * a.sC + row * a.ldc + col0, c);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = fmaf(a.alpha, v[i], a.beta * c[i]);
+                    } else if (a.alpha != 1.0f) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= a.alpha;
+                    }
+                    if (a.Y) S::row32(static_cast<T*>(a.Y) + t.b * a.sY + row * a.ldy + col0, v);
+                    if (a.Yt) {
+                        T* yt = static_cast<T*>(a.Yt) + t.b * a.sYt + row;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) S::one(yt + (col0 + i) * a.ldyt, v[i]);
+                    }
+                } else if constexpr (EPI == kNtGram) {
+                    T* y = static_cast<T*>(a.Y) + t.b * a.sY;
+                    if (col0 > row) {  // the whole chunk lies above the diagonal
+                        S::row32(y + row * a.ldy + col0, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) S::one(y + (col0 + i) * a.ldy + row, v[i]);
+                    } else if (col0 + 31 >= row) {  // the chunk crosses it
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t col = col0 + i;
+                            if (col >= row) S::one(y + row * a.ldy + col, v[i]);
+                            if (col > row) S::one(y + col * a.ldy + row, v[i]);
+                        }
+                    }
+                } else {  // kEpiPart: the whole fp32 tile of this split
+                    const int64_t M = int64_t(a.m_blocks) * kBM;
+                    float* p = a.P + (int64_t(t.split) * a.batch + t.b) * M * M;
+                    Store<false>::row32(p + row * M + col0, v);
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
+                     : "memory");
+    }
+}
+
+// Sums the split partials of Gram matrices in range order and writes the whole
+// symmetric matrix: element (i, j) takes the partials of (min, max), so both
+// triangles carry the same bits. 32 x 32 tiles through shared memory, on and
+// above the diagonal; each writes itself and its mirror.
+template <typename T>
+__global__ void gram_reduce(const float* P, int splits, int batch, int64_t M, T* Y, int64_t ldy,
+                            int64_t sY) {
+    __shared__ float tile[32][33];
+    const int b = blockIdx.z;
+    const int64_t ti = blockIdx.y, tj = blockIdx.x;
+    if (tj < ti) return;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    for (int r = ty; r < 32; r += 8) {
+        const int64_t i = ti * 32 + r, j = tj * 32 + tx;
+        float s = 0.0f;
+        for (int q = 0; q < splits; ++q) {
+            const float* p = P + (int64_t(q) * batch + b) * M * M;
+            s += (j >= i) ? p[i * M + j] : p[j * M + i];  // diagonal tile: the upper element
+        }
+        tile[r][tx] = s;
+    }
+    __syncthreads();
+    using St = Store<sizeof(T) == 2>;
+    T* y = Y + b * sY;
+    for (int r = ty; r < 32; r += 8) {
+        const int64_t i = ti * 32 + r, j = tj * 32 + tx;
+        St::one(y + i * ldy + j, tile[r][tx]);
+        if (tj > ti) {  // the mirror (j, i): row tj*32 + r, column ti*32 + tx
+            const int64_t mi = tj * 32 + r, mj = ti * 32 + tx;
+            St::one(y + mi * ldy + mj, tile[tx][r]);
+        }
+    }
+}
+
+// ---- the CUDA-core fp32 kernel -------------------------------------------------------
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtBK = 8;
+
+struct SimtArgs {
+    const float* A; int64_t lda, sA;
+    const float* B; int64_t ldb, sB;
+    int64_t K;
+    int32_t n_blocks;   // N / 128
+    float alpha, beta;
+    const float* C; int64_t ldc, sC;
+    float* Y; int64_t ldy, sY;
+    float* Yt; int64_t ldyt, sYt;
+};
+
+// One 128 x 128 tile per block (blockIdx.x: tile, blockIdx.y: matrix); thread
+// (tx, ty) of a 16 x 16 grid owns rows ty*8 .. +7 and columns tx*4 .. +3 and
+// 64 + tx*4 .. +3. K steps of 8, staged in shared memory with K outermost.
+__global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_constant__ SimtArgs a) {
+    __shared__ __align__(16) float As[kSimtBK][128];
+    __shared__ __align__(16) float Bs[kSimtBK][128];
+    const int b = blockIdx.y;
+    const int mb = blockIdx.x / a.n_blocks, nb = blockIdx.x % a.n_blocks;
+    const float* A = a.A + b * a.sA + int64_t(mb) * 128 * a.lda;
+    const float* B = a.B + b * a.sB + int64_t(nb) * 128 * a.ldb;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    // loads: thread t reads row t/2, K elements 4 (t%2) .. +3 of A and of B
+    const int lr = tid >> 1, lk = (tid & 1) * 4;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int64_t k0 = 0; k0 < a.K; k0 += kSimtBK) {
+        const float4 av = *reinterpret_cast<const float4*>(A + lr * a.lda + k0 + lk);
+        const float4 bv = *reinterpret_cast<const float4*>(B + lr * a.ldb + k0 + lk);
+        __syncthreads();
+        As[lk][lr] = av.x;
+        As[lk + 1][lr] = av.y;
+        As[lk + 2][lr] = av.z;
+        As[lk + 3][lr] = av.w;
+        Bs[lk][lr] = bv.x;
+        Bs[lk + 1][lr] = bv.y;
+        Bs[lk + 2][lr] = bv.z;
+        Bs[lk + 3][lr] = bv.w;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kSimtBK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[k][ty * 8]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[k][ty * 8 + 4]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[k][64 + tx * 4]);
+            const float ar[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float br[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = int64_t(mb) * 128 + ty * 8 + i;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t col = int64_t(nb) * 128 + h * 64 + tx * 4;
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = acc[i][4 * h + j];
+            if (a.beta != 0.0f) {
+                const float4 c = *reinterpret_cast<const float4*>(a.C + b * a.sC + row * a.ldc + col);
+                const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = fmaf(a.alpha, v[j], a.beta * cv[j]);
+            } else if (a.alpha != 1.0f) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
+            }
+            if (a.Y)
+                *reinterpret_cast<float4*>(a.Y + b * a.sY + row * a.ldy + col) =
+                    make_float4(v[0], v[1], v[2], v[3]);
+            if (a.Yt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) a.Yt[b * a.sYt + (col + j) * a.ldyt + row] = v[j];
+        }
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// Tensor map over `batch` row-major matrices of `rows` x `k` elements (row
+// stride ld, matrix stride sm, in elements): boxes of one K step x 128 rows,
+// 128-byte swizzle, zero fill outside.
+int make_map(CUtensorMap* map, bool bf16, const void* base, int64_t k, int64_t rows, int64_t batch,
+             int64_t ld, int64_t sm) {
+    const auto enc = encoder();
+    if (!enc) return record_error(CAM_E_CUDA, "orthogonalisation: cuTensorMapEncodeTiled unavailable");
+    const int64_t eb = bf16 ? 2 : 4;
+    const cuuint64_t dims[3] = {cuuint64_t(k), cuuint64_t(rows), cuuint64_t(batch)};
+    const cuuint64_t strides[2] = {cuuint64_t(ld * eb), cuuint64_t(sm * eb)};
+    const cuuint32_t box[3] = {cuuint32_t(kRowBytes / eb), cuuint32_t(kBM), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r =
+        enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return record_error(CAM_E_CUDA, "orthogonalisation: cuTensorMapEncodeTiled failed (%d)",
+                            static_cast<int>(r));
+    return CAM_OK;
+}
+
+template <bool BF16, int BN, int EPI>
+cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
+    using G = Geo<BF16, BN>;
+    static cudaError_t attr = cudaFuncSetAttribute(
+        nt_gemm_tc<BF16, BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+    if (attr != cudaSuccess) return attr;
+    nt_gemm_tc<BF16, BN, EPI><<<grid, kTcThreads, G::kSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, int grid, cudaStream_t s) {
+    if (bn == 256) {
+        if (epi == kNtAxpby) return launch_tc<BF16, 256, kNtAxpby>(a, grid, s);
+        if (epi == kNtGram) return launch_tc<BF16, 256, kNtGram>(a, grid, s);
+        return launch_tc<BF16, 256, kEpiPart>(a, grid, s);
+    }
+    if (epi == kNtAxpby) return launch_tc<BF16, 128, kNtAxpby>(a, grid, s);
+    if (epi == kNtGram) return launch_tc<BF16, 128, kNtGram>(a, grid, s);
+    return launch_tc<BF16, 128, kEpiPart>(a, grid, s);
+}
+
+int launch_fail(cudaError_t e) {
+    return record_error(CAM_E_CUDA, "orthogonalisation: GEMM launch: %s", cudaGetErrorString(e));
+}
+
+int run_simt(const NtGemm& g, cudaStream_t s, int64_t* launches) {
+    SimtArgs a;
+    a.A = static_cast<const float*>(g.A);
+    a.lda = g.lda;
+    a.sA = g.sA;
+    a.B = static_cast<const float*>(g.B);
+    a.ldb = g.ldb;
+    a.sB = g.sB;
+    a.K = g.K;
+    a.n_blocks = static_cast<int32_t>(g.N / 128);
+    const bool gram = g.epilogue == kNtGram;
+    a.alpha = gram ? 1.0f : g.alpha;
+    a.beta = gram ? 0.0f : g.beta;
+    a.C = static_cast<const float*>(g.C);
+    a.ldc = g.ldc;
+    a.sC = g.sC;
+    a.Y = static_cast<float*>(g.Y);
+    a.ldy = g.ldy;
+    a.sY = g.sY;
+    a.Yt = gram ? nullptr : static_cast<float*>(g.Yt);
+    a.ldyt = g.ldyt;
+    a.sYt = g.sYt;
+    const dim3 grid(static_cast<unsigned>((g.M / 128) * (g.N / 128)), static_cast<unsigned>(g.batch));
+    nt_gemm_simt<<<grid, kSimtThreads, 0, s>>>(a);
+    ++*launches;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? CAM_OK : launch_fail(e);
+}
+
+}  // namespace tc
+
+int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int64_t* launches) {
+    using namespace tc;
+    if (g.M % 128 || g.N % 128 || g.K % 128 || g.batch < 1)
+        return record_error(CAM_E_ARG, "orthogonalisation: GEMM extents must be multiples of 128");
+    if (g.precision == CAM_ORTHO_FP32) return run_simt(g, s, launches);
+    const bool bf16 = g.precision == CAM_ORTHO_BF16;
+    const int bn = g.N % 256 == 0 ? 256 : 128;
+    const int64_t kstep = kRowBytes / (bf16 ? 2 : 4);
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    int rc = make_map(&a.ta, bf16, g.A, g.K, g.M, g.batch, g.lda, g.sA);
+    if (rc == CAM_OK) rc = make_map(&a.tb, bf16, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
+    if (rc != CAM_OK) return rc;
+    a.batch = g.batch;
+    a.m_blocks = static_cast<int32_t>(g.M / kBM);
+    a.n_blocks = static_cast<int32_t>(g.N / bn);
+    a.k_blocks = static_cast<int32_t>(g.K / kstep);
+    a.alpha = g.alpha;
+    a.beta = g.beta;
+    a.C = g.C;
+    a.ldc = g.ldc;
+    a.sC = g.sC;
+    a.Y = g.Y;
+    a.ldy = g.ldy;
+    a.sY = g.sY;
+    a.Yt = g.Yt;
+    a.ldyt = g.ldyt;
+    a.sYt = g.sYt;
+    a.status = status;
+    a.splits = 1;
+    a.k_per_split = a.k_blocks;
+    int epi = g.epilogue;
+    if (epi == kNtGram) {
+        if (g.M != g.N || g.A != g.B)
+            return record_error(CAM_E_ARG, "orthogonalisation: a Gram product takes one operand");
+        int tri = 0;
+        for (int cb = 0; cb < a.n_blocks; ++cb) tri += std::min(a.m_blocks, (bn * cb + bn - 1) / kBM + 1);
+        a.n_tri = tri;
+        // Split K when the tiles fill less than about one wave: ranges of at
+        // least 16 K steps, as many as bring the units near a whole number of
+        // waves, within the partial buffer.
+        const int64_t tiles = int64_t(tri) * g.batch;
+        int splits = 1;
+        if (tiles < sm_count && g.partials) {
+            const int64_t want = std::max<int64_t>(1, sm_count / tiles);
+            const int64_t by_k = std::max<int64_t>(1, a.k_blocks / 16);
+            const int64_t by_mem = g.partial_floats / (g.batch * g.M * g.M);
+            splits = static_cast<int>(std::min({want, by_k, by_mem}));
+            splits = std::max(splits, 1);
+        }
+        if (splits > 1) {
+            a.k_per_split = (a.k_blocks + splits - 1) / splits;
+            a.splits = (a.k_blocks + a.k_per_split - 1) / a.k_per_split;  // no empty range
+            a.P = g.partials;
+            epi = kEpiPart;
+        }
+        a.n_units = static_cast<int32_t>(tiles * a.splits);
+    } else {
+        a.n_tri = 0;
+        a.n_units = static_cast<int32_t>(int64_t(a.m_blocks) * a.n_blocks * g.batch);
+    }
+    const int grid = std::min(a.n_units, sm_count);
+    const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, grid, s)
+                               : launch_tc_any<false>(a, bn, epi, grid, s);
+    ++*launches;
+    if (e != cudaSuccess) return launch_fail(e);
+    if (epi == kEpiPart) {
+        const dim3 rgrid(static_cast<unsigned>(g.M / 32), static_cast<unsigned>(g.M / 32),
+                         static_cast<unsigned>(g.batch));
+        if (bf16)
+            gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 8), 0, s>>>(
+                g.partials, a.splits, g.batch, g.M, static_cast<__nv_bfloat16*>(g.Y), g.ldy, g.sY);
+        else
+            gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(g.partials, a.splits, g.batch, g.M,
+                                                             static_cast<float*>(g.Y), g.ldy, g.sY);
+        ++*launches;
+        const cudaError_t r = cudaGetLastError();
+        if (r != cudaSuccess) return launch_fail(r);
+    }
+    return CAM_OK;
+}
+
+}  // namespace cam

@@ -3,127 +3,65 @@
 // ("DiffuRefill-1B: Pretraining a Masked Diffusion Language Model on Free,
 // Preemptible Notebook GPUs", section 5.3).
 //
-// Per matrix tensor (row-major m x n):
+// Per matrix tensor (row-major m x n; r = min(m, n), L = max(m, n)):
 //   1. Delta = mean_k(x_k) - theta with the plain-mean arithmetic of the fused
 //      pass, into a workspace, with |Delta|_F^2 summed in a fixed order;
-//   2. X0 = Delta / |Delta|_F, so every singular value lies in (0, 1];
-//   3. `iterations` Newton-Schulz steps X <- 1.5 X - 0.5 X (X^T X) (with the
-//      smaller Gram matrix), which drive every singular value to 1 and so
-//      converge to the polar factor U V^T;
-//   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), then the
-//      EMA of the globals.
-// The two GEMMs of a step are plain dense contractions and run on the tensor
-// cores through cuBLASLt (TF32 inputs with fp32 accumulation, full fp32, or a
-// bf16 iterate and Gram matrix with fp32 accumulation),
-// loaded with dlopen the first time a context orthogonalises, so the rest of
-// the library never depends on it. The element-wise steps are this file's
-// kernels.
-#include <cublasLt.h>
+//   2. X0 = Delta / |Delta|_F, so every singular value lies in (0, 1], stored
+//      in the wide orientation W (r x L: Delta itself, or its transpose for a
+//      tall matrix) and, transposed, as V = W^T, both zero-padded to
+//      multiples of 128 (nt_gemm.h);
+//   3. `iterations` Newton-Schulz steps W <- 1.5 W - 0.5 (W W^T) W, which
+//      drive every singular value to 1 and so converge to the polar factor
+//      U V^T. Each step is two NT GEMMs (nt_gemm.cu): the Gram matrix
+//      G = W W^T (symmetric: only its upper triangle is computed and then
+//      mirrored), then V' = 1.5 V - 0.5 V G with the combination in the GEMM's
+//      epilogue, which also writes W' = V'^T;
+//   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), read
+//      from V (tall) or W (wide), then the EMA of the globals.
+// Equal-shape matrices run as one batch through every kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <dlfcn.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <mutex>
 #include <vector>
 
 #include "cam_internal.h"
-#include "side_internal.h"
 #include "merge_device.cuh"
+#include "nt_gemm.h"
+#include "side_internal.h"
 
 namespace cam {
 namespace {
 
-// ---- cuBLASLt, resolved at run time ------------------------------------------------
-
-struct LtApi {
-    bool ok = false;
-    decltype(&cublasLtCreate) create = nullptr;
-    decltype(&cublasLtDestroy) destroy = nullptr;
-    decltype(&cublasLtMatmulDescCreate) desc_create = nullptr;
-    decltype(&cublasLtMatmulDescDestroy) desc_destroy = nullptr;
-    decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
-    decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
-    decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
-    decltype(&cublasLtMatrixLayoutSetAttribute) layout_set = nullptr;
-    decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
-    decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
-    decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
-    decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
-    decltype(&cublasLtMatmul) matmul = nullptr;
-};
-
-LtApi g_lt;
-std::mutex g_lt_mutex;
-
-template <typename F>
-bool resolve(void* h, const char* name, F& out) {
-    out = reinterpret_cast<F>(dlsym(h, name));
-    return out != nullptr;
-}
-
-const LtApi* lt_api() {
-    std::lock_guard<std::mutex> lock(g_lt_mutex);
-    if (g_lt.ok) return &g_lt;
-    void* h = dlopen("libcublasLt.so.13", RTLD_NOW | RTLD_GLOBAL);
-    if (!h) h = dlopen("/usr/local/cuda/lib64/libcublasLt.so.13", RTLD_NOW | RTLD_GLOBAL);
-    if (!h) return nullptr;
-    LtApi a;
-    bool ok = resolve(h, "cublasLtCreate", a.create) && resolve(h, "cublasLtDestroy", a.destroy) &&
-              resolve(h, "cublasLtMatmulDescCreate", a.desc_create) &&
-              resolve(h, "cublasLtMatmulDescDestroy", a.desc_destroy) &&
-              resolve(h, "cublasLtMatmulDescSetAttribute", a.desc_set) &&
-              resolve(h, "cublasLtMatrixLayoutCreate", a.layout_create) &&
-              resolve(h, "cublasLtMatrixLayoutDestroy", a.layout_destroy) &&
-              resolve(h, "cublasLtMatrixLayoutSetAttribute", a.layout_set) &&
-              resolve(h, "cublasLtMatmulPreferenceCreate", a.pref_create) &&
-              resolve(h, "cublasLtMatmulPreferenceDestroy", a.pref_destroy) &&
-              resolve(h, "cublasLtMatmulPreferenceSetAttribute", a.pref_set) &&
-              resolve(h, "cublasLtMatmulAlgoGetHeuristic", a.heuristic) &&
-              resolve(h, "cublasLtMatmul", a.matmul);
-    if (!ok) return nullptr;
-    a.ok = true;
-    g_lt = a;
-    return &g_lt;
-}
-
-constexpr size_t kLtWorkspace = size_t(32) << 20;
 constexpr int kOrthoBatchMax = 256;  // matrices orthogonalised together
 constexpr int kOrthoBlocksMax = 4096;
+constexpr int64_t kSplitFloats = int64_t(1) << 25;  // Gram split-K partials (128 MB)
 
-// One cached GEMM configuration (column-major D = alpha op(A) op(B) + beta C).
-struct GemmPlan {
-    int64_t M, N, Kd, lda, ldb, ldc;
-    bool ta, tb;
-    int precision;
-    int32_t batch;                   // matrices per call (strided batch)
-    int64_t sa, sb, sc;              // element strides between them
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulAlgo_t algo;
-};
+int64_t pad128(int64_t v) { return (v + 127) / 128 * 128; }
 
 }  // namespace
 
 // Per-context workspace of the orthogonalisation, made at the first
-// orthogonalised commit: two fp32 matrix buffers sized for the context's
-// largest matrix, the Gram matrix, reduction partials and a cuBLASLt handle.
+// orthogonalised commit: Delta (dense fp32), two iterates W and two
+// transposes V in the padded layout (up to 4 bytes an element), the Gram
+// matrices, the short-side form's six r x r matrices per batch slot, the
+// Gram split partials and the norm reduction.
 struct OrthoWork {
-    const LtApi* lt = nullptr;
-    cublasLtHandle_t handle = nullptr;
-    float* X = nullptr;
-    float* Y = nullptr;
-    float* G = nullptr;
+    float* X = nullptr;          // Delta, matrix j dense at X + j m n
+    void* W[2] = {nullptr, nullptr};
+    void* V[2] = {nullptr, nullptr};
+    void* G = nullptr;
+    float* Sq = nullptr;         // short side: G0, P, Pt, P', Pt', T, M per slot
+    float* split = nullptr;      // Gram split-K partials
     double* partials = nullptr;  // [kOrthoBatchMax * kOrthoBlocksMax]
     double* scalars = nullptr;   // [j] = |Delta_j|_F^2
     float* inv_norm = nullptr;   // [j] = 1 / |Delta_j|_F (0 when Delta_j = 0)
-    void* lt_ws = nullptr;
     void* block = nullptr;       // one cudaMalloc holding all of the above
-    int64_t cap_elems = 0;       // floats in X and in Y
-    int64_t cap_gram = 0;        // floats in G
-    std::vector<GemmPlan> plans; // cuBLASLt configurations by GEMM shape
+    int64_t cap_pad = 0;         // elements in each W / V buffer and floats in X
+    int64_t cap_gram = 0;        // elements in G
+    int64_t cap_sq = 0;          // floats in Sq (7 squares of the largest matrix)
 };
 
 }  // namespace cam
@@ -228,62 +166,50 @@ __global__ void ortho_norm(const double* partials, int nb, double* scalars, floa
     }
 }
 
-// X_j <- X_j / |Delta_j|_F. Slot j is 32-byte aligned when n is a multiple of 8.
-__global__ void ortho_scale(float* X, int64_t n, const float* inv_norm) {
-    const int j = blockIdx.y;
+__device__ __forceinline__ void put(float* p, float v) { *p = v; }
+__device__ __forceinline__ void put(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// X0_j = Delta_j / |Delta_j|_F into W_j (rp x Lp, the wide orientation) and
+// V_j = W_j^T (Lp x rp), rounded once to the iterate's storage type, zero
+// outside the matrix. Blocks of 32 x 8 threads move 32 x 32 tiles of the
+// (L, r) index space through shared memory, so that reads of Delta and
+// writes of both copies are coalesced. grid: (Lp / 32, rp / 32, batch).
+template <typename T>
+__global__ void ortho_pack(const float* X, int64_t m, int64_t n, const float* inv_norm, T* W, T* V,
+                           int64_t rp, int64_t Lp) {
+    __shared__ float tile[32][33];  // [L index][r index]
+    const int j = blockIdx.z;
+    const int64_t i0 = int64_t(blockIdx.x) * 32, a0 = int64_t(blockIdx.y) * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+    const bool tall = m >= n;
+    const int64_t r = tall ? n : m, L = tall ? m : n;
     const float f = inv_norm[j];
-    float* Xj = X + int64_t(j) * n;
-    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    int64_t done = 0;
-    if ((n & 7) == 0) {
-        for (int64_t v = tid; v < (n >> 3); v += stride) {
-            float x[8];
-            dev::load_s8(Xj + 8 * v, x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __fmul_rn(x[e], f);
-            dev::store_s8(Xj + 8 * v, x);
+    const float* Xj = X + int64_t(j) * m * n;
+    for (int q = ty; q < 32; q += 8) {
+        if (tall) {  // Delta[i][a]: a along the row
+            const int64_t i = i0 + q, a = a0 + tx;
+            tile[q][tx] = (i < L && a < r) ? __fmul_rn(Xj[i * n + a], f) : 0.0f;
+        } else {     // Delta[a][i]: i along the row
+            const int64_t a = a0 + q, i = i0 + tx;
+            tile[tx][q] = (i < L && a < r) ? __fmul_rn(Xj[a * n + i], f) : 0.0f;
         }
-        done = n;
     }
-    for (int64_t i = done + tid; i < n; i += stride) Xj[i] = __fmul_rn(Xj[i], f);
+    __syncthreads();
+    T* Wj = W + int64_t(j) * rp * Lp;
+    T* Vj = V + int64_t(j) * Lp * rp;
+    for (int q = ty; q < 32; q += 8) {
+        put(Vj + (i0 + q) * rp + a0 + tx, tile[q][tx]);  // V[i][a]
+        put(Wj + (a0 + q) * Lp + i0 + tx, tile[tx][q]);  // W[a][i]
+    }
 }
 
-// X_j / |Delta_j|_F (fp32 in X) into the bf16 iterate buffer Y, rounded to
-// nearest-even (CAM_ORTHO_BF16).
-__global__ void ortho_scale_bf16(const float* X, __nv_bfloat16* Y, int64_t n, const float* inv_norm) {
-    const int j = blockIdx.y;
-    const float f = inv_norm[j];
-    const float* Xj = X + int64_t(j) * n;
-    __nv_bfloat16* Yj = Y + int64_t(j) * n;
-    const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    int64_t done = 0;
-    if ((n & 7) == 0) {  // 32-byte reads, 16-byte writes (slot bases stay aligned)
-        for (int64_t v = tid; v < (n >> 3); v += stride) {
-            float x[8];
-            dev::load_s8(Xj + 8 * v, x);
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 b =
-                    __floats2bfloat162_rn(__fmul_rn(x[2 * e], f), __fmul_rn(x[2 * e + 1], f));
-                ow[e] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            *reinterpret_cast<uint4*>(Yj + 8 * v) = o;
-        }
-        done = n;
-    }
-    for (int64_t i = done + tid; i < n; i += stride) Yj[i] = __float2bfloat16_rn(__fmul_rn(Xj[i], f));
-}
-
-// P_j <- I (r x r) for every slot j; total = slots x r x r.
-__global__ void ortho_identity(float* P, int64_t r, int64_t total) {
+// P_j <- the r x r identity inside its rp x rp square (zero elsewhere, so the
+// padding stays zero through the short-side steps); total = slots x rp x rp.
+__global__ void ortho_identity(float* P, int64_t r, int64_t rp, int64_t total) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t q = i % (r * r);
-        P[i] = (q / r == q % r) ? 1.0f : 0.0f;
+        const int64_t q = i % (rp * rp), row = q / rp, col = q % rp;
+        P[i] = (row == col && row < r) ? 1.0f : 0.0f;
     }
 }
 
@@ -291,8 +217,10 @@ struct ApplyArgs {
     float* theta[kOrthoBatchMax];
     float* e[kOrthoBatchMax];  // EMA buffers, or null
     uint32_t vec[kOrthoBatchMax / 32];  // bit j: matrix j's buffers take 32-byte vectors
-    const void* O;             // the polar factors (fp32, or bf16), slot j at O + j * n
-    int64_t n;
+    const void* O;             // the polar factors (fp32, or bf16) in the matrices' own
+                               // orientation: row i of slot j at O + j * so + i * ld
+    int64_t ld, so;
+    int64_t n, cols;           // elements and columns per matrix
     const double* scalars;     // [j] = |Delta_j|_F^2
     float lr;
     int32_t scale_mode;
@@ -307,7 +235,7 @@ __global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
     const int j = blockIdx.y;
     float* theta = a.theta[j];
     float* e = a.e[j];
-    const OT* O = static_cast<const OT*>(a.O) + int64_t(j) * a.n;
+    const OT* O = static_cast<const OT*>(a.O) + int64_t(j) * a.so;
     float s = a.lr;
     if (a.scale_mode == CAM_ORTHO_SCALE_MATCH_NORM)
         s = static_cast<float>(static_cast<double>(a.lr) * sqrt(a.scalars[j]) /
@@ -316,184 +244,139 @@ __global__ void ortho_apply(const __grid_constant__ ApplyArgs a) {
     const int64_t tid = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     int64_t done = 0;
-    if ((a.vec[j >> 5] >> (j & 31)) & 1u) {  // 8 elements per step
+    if ((a.vec[j >> 5] >> (j & 31)) & 1u) {  // 8 elements per step, never across a row
         const int64_t nv = a.n >> 3;
         for (int64_t v = tid; v < nv; v += stride) {
+            const int64_t i = 8 * v, row = i / a.cols, col = i - row * a.cols;
             float th[8];
-            dev::load_s8(theta + 8 * v, th);
+            dev::load_s8(theta + i, th);
             dev::XVec<OT> o;
-            o.load(O + 8 * v);
+            o.load(O + row * a.ld + col);
 #pragma unroll
             for (int q = 0; q < 8; ++q) th[q] = __fadd_rn(th[q], __fmul_rn(s, o.get(q)));
-            dev::store_s8(theta + 8 * v, th);
+            dev::store_s8(theta + i, th);
             if (e) {
                 float ev[8];
-                dev::load_s8(e + 8 * v, ev);
+                dev::load_s8(e + i, ev);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     ev[q] = __fadd_rn(__fmul_rn(a.beta, ev[q]), __fmul_rn(omb, th[q]));
-                dev::store_s8(e + 8 * v, ev);
+                dev::store_s8(e + i, ev);
             }
         }
         done = 8 * nv;
     }
     for (int64_t i = done + tid; i < a.n; i += stride) {
-        const float th = __fadd_rn(theta[i], __fmul_rn(s, dev::load_x1(O + i)));
+        const int64_t row = i / a.cols, col = i - row * a.cols;
+        const float th = __fadd_rn(theta[i], __fmul_rn(s, dev::load_x1(O + row * a.ld + col)));
         theta[i] = th;
         if (e) e[i] = __fadd_rn(__fmul_rn(a.beta, e[i]), __fmul_rn(omb, th));
     }
 }
 
-}  // namespace
-}  // namespace cam
-
-namespace cam {
-namespace {
-
-int lt_fail(const char* what, int st) {
-    return record_error(CAM_E_CUDA, "orthogonalisation: %s failed (cuBLASLt status %d)", what, st);
+int launch_error(const char* what) {
+    const cudaError_t ce = cudaGetLastError();
+    if (ce == cudaSuccess) return CAM_OK;
+    return record_error(CAM_E_CUDA, "orthogonalisation: %s: %s", what, cudaGetErrorString(ce));
 }
 
-// Finds or builds the plan for this GEMM shape.
-int gemm_plan(OrthoWork* w, int precision, bool ta, bool tb,
-              int64_t M, int64_t N, int64_t Kd, int64_t lda, int64_t ldb, int64_t ldc,
-              int32_t batch, int64_t sa, int64_t sb, int64_t sc, const GemmPlan** out) {
-    std::vector<GemmPlan>& cache = w->plans;
-    for (const GemmPlan& p : cache)
-        if (p.M == M && p.N == N && p.Kd == Kd && p.lda == lda && p.ldb == ldb && p.ldc == ldc &&
-            p.ta == ta && p.tb == tb && p.precision == precision && p.batch == batch &&
-            p.sa == sa && p.sb == sb && p.sc == sc) {
-            *out = &p;
-            return CAM_OK;
-        }
-    const LtApi& L = *w->lt;
-    GemmPlan p{M, N, Kd, lda, ldb, ldc, ta, tb, precision, batch, sa, sb, sc};
-    // bf16 operands and results with fp32 accumulation, or fp32 ones in full
-    // fp32 or TF32 (inputs rounded to 10-bit mantissas inside the GEMM)
-    const cublasComputeType_t ct =
-        precision == CAM_ORTHO_TF32 ? CUBLAS_COMPUTE_32F_FAST_TF32 : CUBLAS_COMPUTE_32F;
-    const cudaDataType_t dt = precision == CAM_ORTHO_BF16 ? CUDA_R_16BF : CUDA_R_32F;
-    int st = L.desc_create(&p.op, ct, CUDA_R_32F);
-    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matmul descriptor", st);
-    const cublasOperation_t oa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, ob = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-    L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &oa, sizeof oa);
-    L.desc_set(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &ob, sizeof ob);
-    st = L.layout_create(&p.la, dt, ta ? Kd : M, ta ? M : Kd, lda);
-    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lb, dt, tb ? N : Kd, tb ? Kd : N, ldb);
-    if (st == CUBLAS_STATUS_SUCCESS) st = L.layout_create(&p.lc, dt, M, N, ldc);
-    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matrix layout", st);
-    if (batch > 1) {
-        const cublasLtMatrixLayout_t lays[3] = {p.la, p.lb, p.lc};
-        const int64_t strides[3] = {sa, sb, sc};
-        for (int i = 0; i < 3 && st == CUBLAS_STATUS_SUCCESS; ++i) {
-            st = L.layout_set(lays[i], CUBLASLT_MATRIX_LAYOUT_BATCH_COUNT, &batch, sizeof batch);
-            if (st == CUBLAS_STATUS_SUCCESS)
-                st = L.layout_set(lays[i], CUBLASLT_MATRIX_LAYOUT_STRIDED_BATCH_OFFSET, &strides[i],
-                                  sizeof strides[i]);
-        }
-        if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("batched layout", st);
-    }
-    cublasLtMatmulPreference_t pref = nullptr;
-    st = L.pref_create(&pref);
-    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("preference", st);
-    const uint64_t ws = kLtWorkspace;
-    L.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws, sizeof ws);
-    cublasLtMatmulHeuristicResult_t res;
-    int found = 0;
-    st = L.heuristic(w->handle, p.op, p.la, p.lb, p.lc, p.lc, pref, 1, &res, &found);
-    L.pref_destroy(pref);
-    if (st != CUBLAS_STATUS_SUCCESS || found < 1) return lt_fail("algorithm heuristic", st);
-    p.algo = res.algo;
-    cache.push_back(p);
-    *out = &cache.back();
-    return CAM_OK;
+// Shape of one batch in the padded layout.
+struct Shape {
+    int64_t m, n, r, L, rp, Lp;
+    bool tall;
+};
+
+// One NT GEMM over `B` slots; strides in elements.
+NtGemm nt(int precision, int epi, int B, int64_t M, int64_t N, int64_t K, const void* A,
+          int64_t lda, int64_t sA, const void* Bm, int64_t ldb, int64_t sB) {
+    NtGemm g;
+    std::memset(&g, 0, sizeof g);
+    g.precision = precision;
+    g.epilogue = epi;
+    g.batch = B;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.A = A;
+    g.lda = lda;
+    g.sA = sA;
+    g.B = Bm;
+    g.ldb = ldb;
+    g.sB = sB;
+    g.alpha = 1.0f;
+    g.beta = 0.0f;
+    return g;
 }
 
-// D = alpha op(A) op(B) + beta C for `batch` matrices at element strides
-// sa, sb, sc (column-major; C and D share a layout).
-int gemm(OrthoWork* w, int precision, bool ta, bool tb, int64_t M,
-         int64_t N, int64_t Kd, float alpha, const void* A, int64_t lda, const void* B,
-         int64_t ldb, float beta, const void* C, void* D, int64_t ldc, int32_t batch,
-         int64_t sa, int64_t sb, int64_t sc, cudaStream_t s) {
-    const GemmPlan* p = nullptr;
-    int rc = gemm_plan(w, precision, ta, tb, M, N, Kd, lda, ldb, ldc, batch, sa, sb, sc, &p);
-    if (rc != CAM_OK) return rc;
-    const int st = w->lt->matmul(w->handle, p->op, &alpha, A, p->la, B, p->lb, &beta, C, p->lc, D,
-                                 p->lc, &p->algo, w->lt_ws, kLtWorkspace, s);
-    if (st != CUBLAS_STATUS_SUCCESS) return lt_fail("matmul", st);
-    return CAM_OK;
-}
-
-// The short-side form of the iteration (CAM_ORTHO_SHORT_SIDE) for B
-// matrices of m x n with max(m, n) >= 4 r, r = min(m, n). With the iterate
-// written X_k = X_0 P_k (tall) or P_k X_0 (wide), a Newton-Schulz step becomes
-// P <- 1.5 P - 0.5 P (P^T G P) (tall) or 1.5 P - 0.5 (P G P^T) P (wide) on
-// r x r matrices, G the Gram matrix of X_0 on its short side; the polar
-// factor is then one product with X_0. The normalised starts are in w->X,
-// the factors end in w->Y. Workspace: P in w->G, and G, T, M and P's second
-// buffer in w->Y (4 B r^2 <= B m n floats), which the final product then
-// overwrites. G and the r x r steps run in fp32; the final product in
-// p.precision.
-int short_side_iteration(OrthoWork* w, const OrthoParams& p, int64_t m, int64_t n, int B,
-                         cudaStream_t s, int64_t* launches) {
-    const int64_t r = std::min(m, n), numel = m * n, gram = r * r;
-    const bool tall = m >= n;
-    const float* A = w->X;  // each X_0 as the column-major n x m matrix X_0^T (ld n)
-    float* G = w->Y;
-    float* T = G + int64_t(B) * gram;
-    float* M = T + int64_t(B) * gram;
-    float* Pa = w->G;
-    float* Pb = M + int64_t(B) * gram;
+// The short-side form of the iteration (CAM_ORTHO_SHORT_SIDE), for matrices
+// with L >= 4 r: with W_k = P_k W_0, a Newton-Schulz step becomes
+// P <- 1.5 P - 0.5 (P G0 P^T) P on r x r matrices, G0 = W_0 W_0^T; the polar
+// factor is then one product with W_0. G0 and the r x r steps run in fp32 on
+// the CUDA cores; the final product in p.precision. Per slot, Sq holds G0, P,
+// P^T, their next values, T = P G0 and M = T P^T. The factor ends in
+// W[1] (and V[1] = its transpose).
+int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, int B, cudaStream_t s,
+                         int sm_count, int64_t* launches) {
+    const int64_t rp = sh.rp, Lp = sh.Lp, sq = rp * rp;
     const int fp = CAM_ORTHO_FP32;
-    int rc = tall ? gemm(w, fp, false, true, n, n, m, 1.0f, A, n, A, n, 0.0f, G, G, n, B, numel,
-                         numel, gram, s)   // G = X_0^T X_0 = A A^T
-                  : gemm(w, fp, true, false, m, m, n, 1.0f, A, n, A, n, 0.0f, G, G, m, B, numel,
-                         numel, gram, s);  // G = X_0 X_0^T = A^T A
+    float* G0 = w->Sq;
+    float* P = G0 + B * sq;
+    float* Pt = P + B * sq;
+    float* Pn = Pt + B * sq;
+    float* Ptn = Pn + B * sq;
+    float* T = Ptn + B * sq;
+    float* M = T + B * sq;
+    // G0 = W0 W0^T
+    NtGemm g = nt(fp, kNtAxpby, B, rp, rp, Lp, w->W[0], Lp, rp * Lp, w->W[0], Lp, rp * Lp);
+    g.Y = G0;
+    g.ldy = rp;
+    g.sY = sq;
+    int rc = nt_gemm(g, sm_count, p.status, s, launches);
     if (rc != CAM_OK) return rc;
-    const int64_t total = int64_t(B) * gram;
+    const int64_t total = int64_t(B) * sq;
     const int blocks =
         static_cast<int>(std::min<int64_t>(4096, (total + kOrthoThreads - 1) / kOrthoThreads));
-    ortho_identity<<<blocks, kOrthoThreads, 0, s>>>(Pa, r, total);
-    ++*launches;
-    cudaError_t ce = cudaGetLastError();
-    if (ce != cudaSuccess)
-        return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
-    float* P = Pa;
-    float* Pn = Pb;
-    for (int it = 0; it < p.iterations && rc == CAM_OK; ++it) {
-        if (tall) {  // T = P^T G; M = T P; P' = 1.5 P - 0.5 P M
-            rc = gemm(w, fp, true, false, r, r, r, 1.0f, P, r, G, r, 0.0f, T, T, r, B, gram, gram,
-                      gram, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, fp, false, false, r, r, r, 1.0f, T, r, P, r, 0.0f, M, M, r, B, gram,
-                          gram, gram, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, fp, false, false, r, r, r, -0.5f, P, r, M, r, 1.5f, P, Pn, r, B, gram,
-                          gram, gram, s);
-        } else {     // T = P G; M = T P^T; P' = 1.5 P - 0.5 M P
-            rc = gemm(w, fp, false, false, r, r, r, 1.0f, P, r, G, r, 0.0f, T, T, r, B, gram, gram,
-                      gram, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, fp, false, true, r, r, r, 1.0f, T, r, P, r, 0.0f, M, M, r, B, gram,
-                          gram, gram, s);
-            if (rc == CAM_OK)
-                rc = gemm(w, fp, false, false, r, r, r, -0.5f, M, r, P, r, 1.5f, P, Pn, r, B, gram,
-                          gram, gram, s);
-        }
+    ortho_identity<<<blocks, kOrthoThreads, 0, s>>>(P, sh.r, rp, total);
+    ortho_identity<<<blocks, kOrthoThreads, 0, s>>>(Pt, sh.r, rp, total);
+    *launches += 2;
+    if ((rc = launch_error("launch")) != CAM_OK) return rc;
+    for (int it = 0; it < p.iterations; ++it) {
+        g = nt(fp, kNtAxpby, B, rp, rp, rp, P, rp, sq, G0, rp, sq);  // T = P G0 (G0 symmetric)
+        g.Y = T;
+        g.ldy = rp;
+        g.sY = sq;
+        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+        g = nt(fp, kNtAxpby, B, rp, rp, rp, T, rp, sq, P, rp, sq);  // M = T P^T
+        g.Y = M;
+        g.ldy = rp;
+        g.sY = sq;
+        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+        // P'^T = 1.5 P^T - 0.5 P^T M (M symmetric), and P' beside it
+        g = nt(fp, kNtAxpby, B, rp, rp, rp, Pt, rp, sq, M, rp, sq);
+        g.alpha = -0.5f;
+        g.beta = 1.5f;
+        g.C = Pt;
+        g.ldc = rp;
+        g.sC = sq;
+        g.Y = Ptn;
+        g.ldy = rp;
+        g.sY = sq;
+        g.Yt = Pn;
+        g.ldyt = rp;
+        g.sYt = sq;
+        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         std::swap(P, Pn);
+        std::swap(Pt, Ptn);
     }
-    if (rc != CAM_OK) return rc;
-    if (P != Pa) {  // the final product writes over w->Y, where P_b lives
-        ce = cudaMemcpyAsync(Pa, P, sizeof(float) * total, cudaMemcpyDeviceToDevice, s);
-        if (ce != cudaSuccess)
-            return record_error(CAM_E_CUDA, "orthogonalisation: copy: %s", cudaGetErrorString(ce));
-        P = Pa;
-    }
-    // tall: X = X_0 P, column-major P^T A; wide: X = P X_0, column-major A P^T
-    return tall ? gemm(w, p.precision, true, false, n, m, n, 1.0f, P, n, A, n, 0.0f, w->Y, w->Y, n,
-                       B, gram, numel, numel, s)
-                : gemm(w, p.precision, false, true, n, m, m, 1.0f, A, n, P, m, 0.0f, w->Y, w->Y, n,
-                       B, numel, gram, numel, s);
+    // W = P W0 = NT(P, V0), V = W^T
+    g = nt(p.precision, kNtAxpby, B, rp, Lp, rp, P, rp, sq, w->V[0], rp, Lp * rp);
+    g.Y = w->W[1];
+    g.ldy = Lp;
+    g.sY = rp * Lp;
+    g.Yt = w->V[1];
+    g.ldyt = rp;
+    g.sYt = Lp * rp;
+    return nt_gemm(g, sm_count, p.status, s, launches);
 }
 
 }  // namespace
@@ -501,25 +384,22 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, int64_t m, int64_t 
 
 namespace cam {
 
-int ortho_create(OrthoWork** out, int64_t cap_elems, int64_t cap_gram) {
+int ortho_create(OrthoWork** out, int64_t cap_pad, int64_t cap_gram, int64_t big_gram) {
     *out = nullptr;
-    const LtApi* lt = lt_api();
-    if (!lt)
-        return record_error(CAM_E_CUDA,
-                            "orthogonalisation needs cuBLASLt (libcublasLt.so.13), which could not "
-                            "be loaded");
     OrthoWork* w = new (std::nothrow) OrthoWork;
     if (!w) return record_error(CAM_E_NOMEM, "orthogonalisation: out of host memory");
-    w->lt = lt;
-    w->cap_elems = std::max<int64_t>(cap_elems, 1);
-    w->cap_gram = std::max<int64_t>(cap_gram, 1);
+    w->cap_pad = std::max<int64_t>(cap_pad, 128 * 128);
+    w->cap_gram = std::max<int64_t>(cap_gram, 128 * 128);
+    w->cap_sq = 7 * std::max<int64_t>(big_gram, 128 * 128);
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
-    const size_t bx = up(sizeof(float) * size_t(w->cap_elems));
+    const size_t bx = up(sizeof(float) * size_t(w->cap_pad));
     const size_t bg = up(sizeof(float) * size_t(w->cap_gram));
+    const size_t bq = up(sizeof(float) * size_t(w->cap_sq));
+    const size_t bk = up(sizeof(float) * size_t(kSplitFloats));
     const size_t bp = up(sizeof(double) * size_t(kOrthoBatchMax) * kOrthoBlocksMax);
     const size_t bs = up(sizeof(double) * kOrthoBatchMax);
     const size_t bi = up(sizeof(float) * kOrthoBatchMax);
-    const size_t total = 2 * bx + bg + bp + bs + bi + kLtWorkspace;
+    const size_t total = 5 * bx + bg + bq + bk + bp + bs + bi;
     if (cudaMalloc(&w->block, total) != cudaSuccess) {
         cudaGetLastError();
         delete w;
@@ -527,31 +407,23 @@ int ortho_create(OrthoWork** out, int64_t cap_elems, int64_t cap_gram) {
     }
     char* b = static_cast<char*>(w->block);
     w->X = reinterpret_cast<float*>(b);
-    w->Y = reinterpret_cast<float*>(b + bx);
-    w->G = reinterpret_cast<float*>(b + 2 * bx);
-    w->partials = reinterpret_cast<double*>(b + 2 * bx + bg);
-    w->scalars = reinterpret_cast<double*>(b + 2 * bx + bg + bp);
-    w->inv_norm = reinterpret_cast<float*>(b + 2 * bx + bg + bp + bs);
-    w->lt_ws = b + 2 * bx + bg + bp + bs + bi;
-    const int st = lt->create(&w->handle);
-    if (st != CUBLAS_STATUS_SUCCESS) {
-        cudaFree(w->block);
-        delete w;
-        return lt_fail("handle", st);
-    }
+    w->W[0] = b + bx;
+    w->W[1] = b + 2 * bx;
+    w->V[0] = b + 3 * bx;
+    w->V[1] = b + 4 * bx;
+    b += 5 * bx;
+    w->G = b;
+    w->Sq = reinterpret_cast<float*>(b + bg);
+    w->split = reinterpret_cast<float*>(b + bg + bq);
+    w->partials = reinterpret_cast<double*>(b + bg + bq + bk);
+    w->scalars = reinterpret_cast<double*>(b + bg + bq + bk + bp);
+    w->inv_norm = reinterpret_cast<float*>(b + bg + bq + bk + bp + bs);
     *out = w;
     return CAM_OK;
 }
 
 void ortho_destroy(OrthoWork* w) {
     if (!w) return;
-    for (GemmPlan& p : w->plans) {
-        w->lt->layout_destroy(p.la);
-        w->lt->layout_destroy(p.lb);
-        w->lt->layout_destroy(p.lc);
-        w->lt->desc_destroy(p.op);
-    }
-    if (w->handle) w->lt->destroy(w->handle);
     cudaFree(w->block);
     delete w;
 }
@@ -559,10 +431,20 @@ void ortho_destroy(OrthoWork* w) {
 int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoParams& p,
                 cudaStream_t s, int sm_count, int64_t* launches) {
     if (count <= 0) return CAM_OK;
-    const int64_t m = mats[0].rows, n = mats[0].cols, numel = m * n;
-    const int64_t r = std::min(m, n), gram = r * r;
-    int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_elems / numel, w->cap_gram / gram));
+    Shape sh;
+    sh.m = mats[0].rows;
+    sh.n = mats[0].cols;
+    sh.tall = sh.m >= sh.n;
+    sh.r = std::min(sh.m, sh.n);
+    sh.L = std::max(sh.m, sh.n);
+    sh.rp = pad128(sh.r);
+    sh.Lp = pad128(sh.L);
+    const int64_t numel = sh.m * sh.n, padded = sh.rp * sh.Lp, sq = sh.rp * sh.rp;
+    const bool short_side = p.short_side && sh.L >= 4 * sh.r;
+    int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_pad / padded, w->cap_gram / sq));
+    if (short_side) per = std::min<int64_t>(per, w->cap_sq / (7 * sq));
     per = std::max<int64_t>(per, 1);
+    const bool bf = p.precision == CAM_ORTHO_BF16;
     for (int first = 0; first < count; first += static_cast<int>(per)) {
         const int B = static_cast<int>(std::min<int64_t>(per, count - first));
         // Blocks per matrix: about 8 per SM over the whole batch, and no more
@@ -573,7 +455,7 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
         const int grid = static_cast<int>(
             std::min<int64_t>(kOrthoBlocksMax, std::max<int64_t>(1, std::min(want, steps))));
         // Delta of each matrix into its slot, its norm, and the normalised
-        // start: one launch of each kernel for the whole batch.
+        // start in both orientations: one launch of each kernel for the batch.
         // a slot of the workspace is 32-byte aligned when numel is a multiple of 8
         const uintptr_t xa = p.dtype == kDtBF16 ? 16 : 32;
         auto al = [](const void* q, uintptr_t b) { return reinterpret_cast<uintptr_t>(q) % b == 0; };
@@ -592,7 +474,7 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
             if (v) da.vec[j >> 5] |= 1u << (j & 31);
             aa.theta[j] = t.theta;
             aa.e[j] = p.ema ? t.e : nullptr;
-            if (numel % 8 == 0 && al(t.theta, 32) && (!p.ema || al(t.e, 32)))
+            if (sh.n % 8 == 0 && al(t.theta, 32) && (!p.ema || al(t.e, 32)))
                 aa.vec[j >> 5] |= 1u << (j & 31);
         }
         da.K = p.K;
@@ -604,59 +486,68 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
         if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(da);
         else ortho_delta<float><<<bgrid, kOrthoThreads, 0, s>>>(da);
         ortho_norm<<<B, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
-        const bool bf = p.precision == CAM_ORTHO_BF16;
-        if (bf)  // the bf16 iterate starts in Y; X's fp32 Delta is no longer needed
-            ortho_scale_bf16<<<bgrid, kOrthoThreads, 0, s>>>(
-                w->X, reinterpret_cast<__nv_bfloat16*>(w->Y), numel, w->inv_norm);
+        const dim3 pgrid(static_cast<unsigned>(sh.Lp / 32), static_cast<unsigned>(sh.rp / 32), B);
+        if (bf)
+            ortho_pack<__nv_bfloat16><<<pgrid, dim3(32, 8), 0, s>>>(
+                w->X, sh.m, sh.n, w->inv_norm, static_cast<__nv_bfloat16*>(w->W[0]),
+                static_cast<__nv_bfloat16*>(w->V[0]), sh.rp, sh.Lp);
         else
-            ortho_scale<<<bgrid, kOrthoThreads, 0, s>>>(w->X, numel, w->inv_norm);
+            ortho_pack<float><<<pgrid, dim3(32, 8), 0, s>>>(w->X, sh.m, sh.n, w->inv_norm,
+                                                           static_cast<float*>(w->W[0]),
+                                                           static_cast<float*>(w->V[0]), sh.rp, sh.Lp);
         *launches += 3;
-        cudaError_t ce = cudaGetLastError();
-        if (ce != cudaSuccess)
-            return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
-        // Newton-Schulz on all B matrices at once. Row-major X (m x n) is the
-        // column-major n x m matrix A = X^T (ld n).
-        void* cur = bf ? static_cast<void*>(w->Y) : static_cast<void*>(w->X);
-        void* nxt = bf ? static_cast<void*>(w->X) : static_cast<void*>(w->Y);
-        const bool short_side = p.short_side && std::max(m, n) >= 4 * r;
+        int rc = launch_error("launch");
+        if (rc != CAM_OK) return rc;
+        int cur = 0;
         if (short_side) {
-            const int rc = short_side_iteration(w, p, m, n, B, s, launches);
+            rc = short_side_iteration(w, p, sh, B, s, sm_count, launches);
             if (rc != CAM_OK) return rc;
-            cur = w->Y;
+            cur = 1;
         }
         for (int it = 0; !short_side && it < p.iterations; ++it) {
-            int rc;
-            if (m >= n) {  // G = X^T X = A A^T (n x n); A' = 1.5 A - 0.5 G A
-                rc = gemm(w, p.precision, false, true, n, n, m, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G,
-                          n, B, numel, numel, gram, s);
-                if (rc == CAM_OK)
-                    rc = gemm(w, p.precision, false, false, n, m, n, -0.5f, w->G, n, cur, n, 1.5f, cur,
-                              nxt, n, B, gram, numel, numel, s);
-            } else {       // G = X X^T = A^T A (m x m); A' = 1.5 A - 0.5 A G
-                rc = gemm(w, p.precision, true, false, m, m, n, 1.0f, cur, n, cur, n, 0.0f, w->G, w->G,
-                          m, B, numel, numel, gram, s);
-                if (rc == CAM_OK)
-                    rc = gemm(w, p.precision, false, false, n, m, m, -0.5f, cur, n, w->G, m, 1.5f, cur,
-                              nxt, n, B, numel, gram, numel, s);
-            }
-            if (rc != CAM_OK) return rc;
-            std::swap(cur, nxt);
+            // G = W W^T (upper triangle, mirrored)
+            NtGemm g = nt(p.precision, kNtGram, B, sh.rp, sh.rp, sh.Lp, w->W[cur], sh.Lp, padded,
+                          w->W[cur], sh.Lp, padded);
+            g.Y = w->G;
+            g.ldy = sh.rp;
+            g.sY = sq;
+            g.partials = w->split;
+            g.partial_floats = kSplitFloats;
+            if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+            // V' = 1.5 V - 0.5 V G, W' = V'^T
+            g = nt(p.precision, kNtAxpby, B, sh.Lp, sh.rp, sh.rp, w->V[cur], sh.rp, padded, w->G,
+                   sh.rp, sq);
+            g.alpha = -0.5f;
+            g.beta = 1.5f;
+            g.C = w->V[cur];
+            g.ldc = sh.rp;
+            g.sC = padded;
+            g.Y = w->V[1 - cur];
+            g.ldy = sh.rp;
+            g.sY = padded;
+            g.Yt = w->W[1 - cur];
+            g.ldyt = sh.Lp;
+            g.sYt = padded;
+            if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+            cur ^= 1;
         }
-        aa.O = cur;
+        // the factor in the matrices' own orientation: V (tall) or W (wide)
+        aa.O = sh.tall ? w->V[cur] : w->W[cur];
+        aa.ld = sh.tall ? sh.rp : sh.Lp;
+        aa.so = padded;
         aa.n = numel;
+        aa.cols = sh.n;
         aa.scalars = w->scalars;
         aa.lr = p.lr;
         aa.scale_mode = p.scale_mode;
-        aa.r = r;
+        aa.r = sh.r;
         aa.beta = p.beta;
         if (bf)
             ortho_apply<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(aa);
         else
             ortho_apply<float><<<bgrid, kOrthoThreads, 0, s>>>(aa);
         *launches += 1;
-        ce = cudaGetLastError();
-        if (ce != cudaSuccess)
-            return record_error(CAM_E_CUDA, "orthogonalisation: launch: %s", cudaGetErrorString(ce));
+        if ((rc = launch_error("launch")) != CAM_OK) return rc;
     }
     return CAM_OK;
 }

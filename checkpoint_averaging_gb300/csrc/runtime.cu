@@ -128,7 +128,8 @@ struct cam_ctx {
     std::vector<int64_t> swa_count;  // globals folded into each tensor's running average
     std::vector<int64_t> rows;       // matrix rows of each tensor (0: not a matrix)
     cam::OrthoWork* ortho = nullptr; // made at the first orthogonalised commit
-    int64_t ortho_cap_elems = 0, ortho_cap_gram = 0;  // workspace sizing (floats)
+    int64_t ortho_cap_elems = 0, ortho_cap_gram = 0;  // workspace sizing (padded elements)
+    int64_t ortho_big_gram = 0;
     bool is_matrix(int32_t g) const {
         return rows[g] >= 2 && numel[g] % rows[g] == 0 && numel[g] / rows[g] >= 2;
     }
@@ -341,19 +342,23 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->swa_count.assign(d->n_tensors, 0);
     c->rows.assign(d->n_tensors, 0);
     if (d->rows) c->rows.assign(d->rows, d->rows + d->n_tensors);
-    {   // iterate buffers hold a batch of equal-shape matrices: at least the
-        // largest one, at most all of them, capped at 2 GiB (1 GiB for Gram)
+    {   // iterate buffers hold a batch of equal-shape matrices in the GEMMs'
+        // padded layout: at least the largest one, at most all of them,
+        // capped at 2^29 elements (2^28 for Gram)
         int64_t big = 0, big_gram = 0, all = 0, all_gram = 0;
+        auto pad = [](int64_t v) { return (v + 127) / 128 * 128; };
         for (int32_t t = 0; t < c->n_tensors; ++t)
             if (c->is_matrix(t)) {
-                const int64_t r = std::min(c->rows[t], c->numel[t] / c->rows[t]);
-                big = std::max(big, c->numel[t]);
-                big_gram = std::max(big_gram, r * r);
-                all += c->numel[t];
-                all_gram += r * r;
+                const int64_t rows = c->rows[t], cols = c->numel[t] / c->rows[t];
+                const int64_t rp = pad(std::min(rows, cols)), lp = pad(std::max(rows, cols));
+                big = std::max(big, rp * lp);
+                big_gram = std::max(big_gram, rp * rp);
+                all += rp * lp;
+                all_gram += rp * rp;
             }
         c->ortho_cap_elems = std::max(big, std::min(all, int64_t(1) << 29));
         c->ortho_cap_gram = std::max(big_gram, std::min(all_gram, int64_t(1) << 28));
+        c->ortho_big_gram = big_gram;
     }
 
     // Plans and one device block holding every plan's tables, after the
@@ -957,7 +962,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         return cuda_fail(scope.err, "cam_merge_commit: cudaSetDevice");
     }
     if (r->ortho && !c->ortho) {  // workspace of the orthogonalisation, made once per context
-        const int rc = cam::ortho_create(&c->ortho, c->ortho_cap_elems, c->ortho_cap_gram);
+        const int rc = cam::ortho_create(&c->ortho, c->ortho_cap_elems, c->ortho_cap_gram,
+                                         c->ortho_big_gram);
         if (rc == CAM_E_CUDA) close_round(r);  // a CUDA failure frees the round, as below
         if (rc != CAM_OK) return rc;            // CAM_E_NOMEM: nothing ran, the round stays open
     }
@@ -1125,7 +1131,8 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                                   r->ortho_iterations,
                                   r->ema,
                                   r->beta,
-                                  (r->ortho_precision & CAM_ORTHO_SHORT_SIDE) != 0};
+                                  (r->ortho_precision & CAM_ORTHO_SHORT_SIDE) != 0,
+                                  c->d_status};
         // the workspace is the context's: after its last use on any stream
         if (ce == cudaSuccess && !cap) ce = cudaStreamWaitEvent(s, c->ortho_ev, 0);
         std::vector<char> done(T, 0);

@@ -79,10 +79,13 @@ struct OrthoParams {
     bool ema;
     float beta;
     bool short_side;  // iterate in the short side's space (CAM_ORTHO_SHORT_SIDE)
+    int32_t* status;  // the context's device status word
 };
-// cap_elems / cap_gram: floats in each iterate buffer and in the Gram buffer
-// (at least one matrix's worth; batches of equal-shape matrices share them).
-int ortho_create(OrthoWork** out, int64_t cap_elems, int64_t cap_gram);
+// cap_pad / cap_gram: elements in each iterate buffer and in the Gram buffer,
+// in the GEMMs' layout (r x L and r x r, each side padded to a multiple of
+// 128; at least one matrix's worth, batches of equal-shape matrices share
+// them); big_gram: the largest padded r x r (the short-side form's squares).
+int ortho_create(OrthoWork** out, int64_t cap_pad, int64_t cap_gram, int64_t big_gram);
 void ortho_destroy(OrthoWork* w);
 // Orthogonalises `count` matrices of one shape, batching them into strided
 // GEMMs as far as the workspace allows.

@@ -104,12 +104,13 @@ typedef enum {
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
+#define CAM_STATUS_GEMM_TIMEOUT 2 /* a tensor-core GEMM of the orthogonalisation gave up waiting */
 
 /* cam_merge_orthogonalize */
 #define CAM_ORTHO_SCALE_FIXED 0      /* theta' = theta + lr * polar(Delta) */
 #define CAM_ORTHO_SCALE_MATCH_NORM 1 /* ... + lr * |Delta|_F / sqrt(min(m, n)) * polar(Delta) */
 #define CAM_ORTHO_TF32 0             /* GEMMs on the tensor cores, TF32 inputs, fp32 accumulation */
-#define CAM_ORTHO_FP32 1             /* GEMMs in full fp32 */
+#define CAM_ORTHO_FP32 1             /* GEMMs in full fp32 on the CUDA cores */
 #define CAM_ORTHO_BF16 2             /* iterate and GEMM inputs in bf16, fp32 accumulation */
 #define CAM_ORTHO_SHORT_SIDE 4       /* OR into precision: iterate in the short side's space */
 
@@ -172,7 +173,12 @@ void cam_ctx_destroy(cam_ctx* ctx);
 int cam_merge_begin(cam_ctx* ctx, int64_t round, int32_t fragment, cam_round** out);
 
 /*
- * Adds one worker to the round, in arrival order. ckpt is a host array of
+ * Adds one worker to the round, in arrival order: the merger sums the
+ * downloaded checkpoints in the order they come in ("DiffuRefill-1B" model
+ * card, "How it is trained", Merging), and in the token-weighted form each
+ * worker's delta counts by the tokens it trained on ("Pythia-14M on four
+ * rented GPUs and a bucket", "Getting updates through the bucket"). Nothing
+ * is read here; the commit's pass reads every worker once. ckpt is a host array of
  * T_f device pointers, the worker's copy of each tensor of the fragment in
  * fragment order (each numel[t] contiguous elements of `dtype`). tokens is
  * the worker's token count (>= 0; used as its weight in DELTA_NESTEROV mode,
@@ -248,15 +254,23 @@ int cam_merge_fold(cam_round* rd, const void* const* ckpt, cam_dtype dtype, int6
                    cam_mode mode, void* stream);
 
 /*
- * Chooses the outer step. MEAN_REPLACE ignores lr, mu and the token counts.
- * DELTA_NESTEROV needs momentum buffers. lr and mu must be finite.
+ * Chooses the outer step. MEAN_REPLACE is plain replacement by the mean
+ * ("DiffuRefill-1B" technical report, section 3, Table 2, "Outer step": outer
+ * learning rate 1, no momentum) and ignores lr, mu and the token counts.
+ * DELTA_NESTEROV is outer Nesterov on the token-weighted mean of the deltas
+ * ("Pythia-14M on four rented GPUs and a bucket", "Getting updates through
+ * the bucket": lr 0.7, momentum 0.9) and needs momentum buffers. lr and mu
+ * must be finite.
  * Errors: CAM_E_ARG, CAM_E_STATE (finalized twice).
  */
 int cam_merge_finalize(cam_round* rd, cam_mode mode, float lr, float mu);
 
 /*
  * Asks for the EMA update e' = beta*e + (1-beta)*theta' on the round's
- * tensors, fused into the same pass. beta must be finite. Needs EMA buffers.
+ * tensors, fused into the same pass: the EMA of the globals the merger keeps
+ * beside them ("DiffuRefill-1B" technical report, section 3, Table 2, "Side
+ * averages", beta 0.9; model card, "How it is trained", EMA). beta must be
+ * finite. Needs EMA buffers.
  * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
  */
 int cam_ema_update(cam_round* rd, float beta);
@@ -271,14 +285,17 @@ int cam_ema_update(cam_round* rd, float beta);
  * s = lr * |Delta|_F / sqrt(min(m, n)) (CAM_ORTHO_SCALE_MATCH_NORM: the
  * update keeps Delta's Frobenius norm). Other tensors are merged by plain
  * replacement. The polar factor is reached by `iterations` Newton-Schulz
- * steps from Delta / |Delta|_F (X <- 1.5 X - 0.5 X X^T X, on the tensor
- * cores via cuBLASLt in `precision`); singular values of Delta below about
- * 1.5^-(iterations - 8) of the largest have not converged by then. Only
- * plain-mean rounds, and only with an EMA update (no drift norms, publish or
- * running average: CAM_E_STATE at commit). The first orthogonalised commit
- * of a context allocates its workspace (two fp32 copies of the largest
- * matrix, its Gram matrix and 32 MiB for cuBLASLt) and loads cuBLASLt
- * (CAM_E_CUDA if it cannot). Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
+ * steps from Delta / |Delta|_F (X <- 1.5 X - 0.5 X X^T X in `precision`,
+ * this library's own GEMM kernels: the tensor cores for CAM_ORTHO_TF32 and
+ * CAM_ORTHO_BF16, the CUDA cores for CAM_ORTHO_FP32); singular values of
+ * Delta below about 1.5^-(iterations - 8) of the largest have not converged
+ * by then. Only plain-mean rounds, and only with an EMA update (no drift
+ * norms, publish or running average: CAM_E_STATE at commit). The first
+ * orthogonalised commit of a context allocates its workspace (Delta, two
+ * iterates and their transposes with each side padded to a multiple of 128,
+ * the Gram matrices, and 128 MiB of split partials; all equal-shape
+ * matrices of the round at once, up to 2^29 elements per buffer).
+ * Errors: CAM_E_ARG, CAM_E_STATE (asked twice).
  *
  * CAM_ORTHO_BF16 keeps the iterate and the Gram matrix in bf16 between
  * steps (fp32 accumulation inside each GEMM, tensor cores at bf16 rate).
@@ -353,7 +370,10 @@ int cam_drift_norm(cam_round* rd, double* per_tensor, double* per_fragment);
 int cam_merge_publish(cam_round* rd, float* const* theta_out, float* const* ema_out);
 
 /*
- * Closes the round: checks it (finalized, quorum met, weights valid), then
+ * Closes the round: the merger publishes only once enough fresh checkpoints
+ * are in ("DiffuRefill-1B" technical report, section 3, Table 2, "Merger";
+ * "Pythia-14M on four rented GPUs and a bucket", "Getting updates through the
+ * bucket": quorum_size). It checks the round (finalized, quorum met, weights valid), then
  * launches the fused merge pass (and the norm pass if asked, unless the round
  * is small enough for the merge pass to finish the norms itself) on `stream`
  * (a cudaStream_t; NULL = legacy default stream) and frees the round handle.
@@ -509,7 +529,10 @@ int cam_stream_capturing(void* stream, int32_t* out);
  * A round is cut into chunks of at most 16,384 elements, so one call covers
  * at most CAM_NOALLOC_MAX_CHUNKS chunks (about 2.1e9 elements). Larger rounds,
  * and more than CAM_NOALLOC_MAX_TENSORS tensors, are rejected with CAM_E_ARG
- * before anything runs. The array keeps the previous call's contents; every
+ * before any CUDA call. (Rounds under about 2e7 elements use shorter chunks,
+ * chosen from the device's SM count; their exact chunk count is checked after
+ * the device lookup, still before any launch, and stays far below the limit.)
+ * The array keeps the previous call's contents; every
  * entry a call reads is written by that call first, so nothing needs
  * clearing. All calls share the one array: calls whose device work overlaps
  * (different streams without ordering, or several host threads) race on it
@@ -517,7 +540,10 @@ int cam_stream_capturing(void* stream, int32_t* out);
  *
  * The first call on each device looks up the array's device address and the
  * device's properties, with that device current; make that first call before
- * any stream capture. Errors: CAM_E_ARG (checked before any CUDA call),
+ * any stream capture. The address is kept for the life of the process: after
+ * cudaDeviceReset on a device (a new context, where the array may sit
+ * elsewhere) the process must not call this entry point on that device again.
+ * Errors: CAM_E_ARG (argument and size checks, before any CUDA call),
  * CAM_E_CUDA.
  */
 #define CAM_NOALLOC_MAX_TENSORS 4096
