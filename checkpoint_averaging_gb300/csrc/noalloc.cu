@@ -248,7 +248,7 @@ CAM_API int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, flo
         }
         if (W <= 0) return record_error(CAM_E_ARG, "%s: total token count must be > 0", fn);
     }
-    int64_t n_elems = 0;
+    int64_t n_elems = 0, min_chunks = 0;
     for (int32_t t = 0; t < n_tensors; ++t) {
         if (numel[t] < 0 || numel[t] > (int64_t(1) << 40))
             return record_error(CAM_E_ARG, "%s: numel[%d] out of range", fn, t);
@@ -259,7 +259,15 @@ CAM_API int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, flo
             if (!ckpt[size_t(k) * n_tensors + t])
                 return record_error(CAM_E_ARG, "%s: ckpt[%d][%d] is NULL", fn, k, t);
         n_elems += numel[t];
+        min_chunks += (numel[t] + cam::kMaxChunkElems - 1) / cam::kMaxChunkElems;
     }
+    // Chunks are at most kMaxChunkElems long, so this many at least: a round
+    // beyond the scratch is refused here, before any CUDA call.
+    if (min_chunks > CAM_NOALLOC_MAX_CHUNKS)
+        return record_error(CAM_E_ARG,
+                            "%s: round too large for the fixed scratch: more than %d chunks of "
+                            "%d elements",
+                            fn, CAM_NOALLOC_MAX_CHUNKS, cam::kMaxChunkElems);
 
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);

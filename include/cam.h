@@ -101,6 +101,9 @@ typedef enum {
 #define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
 #define CAM_TIME_COMMITS 16u        /* time each commit's device work (cam_ctx_last_commit) */
 #define CAM_NO_FUSED_FINISH 32u     /* always finish drift norms in a separate norm pass */
+#define CAM_TEST_STALL_STAGED 64u   /* test hook, never for real rounds: every staged merge pass
+                                       withholds its first tile and gives up waiting after
+                                       about 1 ms (see cam_ctx_status) */
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
@@ -443,7 +446,13 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  *
  * Every wait of the staged form on one of its barriers gives up after a few
  * seconds. It then sets CAM_STATUS_WAIT_TIMEOUT in the context's device status
- * word, and the results of that commit are undefined.
+ * word, and the results of that commit are undefined. A context created with
+ * CAM_TEST_STALL_STAGED exercises that path on purpose: its staged passes
+ * never issue their first tile's copies, their waits give up after about
+ * 1 ms instead, every copy they did issue lands before the pass returns, and
+ * the status word reports the timeout. It exists to test this failure path
+ * without hanging or faulting the GPU; the buffers of such a round are
+ * left partly written.
  *
  * cam_ctx_status waits for all work on the context's device, then writes the
  * word (0: nothing went wrong) to *out. The word stays set once set.

@@ -58,7 +58,7 @@ def test_version():
     (dict(n_fragments=0), "n_fragments"),
     (dict(fragment_of=[3], n_fragments=2), "fragment_of"),
     (dict(device=-1), "device"),
-    (dict(flags=64), "flags"),
+    (dict(flags=128), "flags"),
     (dict(flags=B.INIT_EMA_FROM_MASTER), "EMA"),
     (dict(flags=B.INIT_ZERO_MOMENTUM), "momentum"),
 ])
@@ -113,6 +113,27 @@ def test_no_gpu_fails_loudly():
     with pytest.raises(B.CudaError) as ei:
         B.ctx_create([16], [0x10000])
     assert "CUDA" in str(ei.value) or "cuda" in str(ei.value)
+
+
+def test_noalloc_sizes_beyond_the_scratch_rejected_before_cuda():
+    """cam_merge_round_noalloc refuses rounds its fixed scratch cannot hold on
+    the host, before any CUDA call: the pointers below are never read, so
+    none of them needs to be real device memory."""
+    n_t = B.NOALLOC_MAX_TENSORS + 1
+    ptrs = [0x10000 + 64 * i for i in range(n_t)]
+    with pytest.raises(B.ArgError, match="n_tensors"):
+        B.merge_round_noalloc([8] * n_t, ptrs, [ptrs], B.F32, B.MEAN_REPLACE)
+    # one tensor cut into more chunks of at most 16,384 elements than the
+    # scratch has partials for
+    n = B.NOALLOC_MAX_CHUNKS * 16384 + 1
+    with pytest.raises(B.ArgError, match="too large"):
+        B.merge_round_noalloc([n], [0x10000], [[0x20000]], B.BF16, B.MEAN_REPLACE)
+    # the same limit summed over several tensors
+    k = 1 << 20
+    count = B.NOALLOC_MAX_CHUNKS // 64 + 1
+    with pytest.raises(B.ArgError, match="too large"):
+        B.merge_round_noalloc([k] * count, [0x10000 + 64 * i for i in range(count)],
+                              [[0x20000 + 64 * i for i in range(count)]], B.F32, B.MEAN_REPLACE)
 
 
 def test_missing_library_is_an_error(monkeypatch, tmp_path):
