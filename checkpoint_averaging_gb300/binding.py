@@ -26,8 +26,10 @@ INIT_EMA_FROM_MASTER, INIT_ZERO_MOMENTUM, INIT_ZERO_SWA = 1, 2, 4
 NO_STAGING = 8
 TIME_COMMITS = 16
 NO_FUSED_FINISH = 32
+TEST_STALL_STAGED = 64  # test hook: staged passes withhold their first tile and time out
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
+STATUS_GEMM_TIMEOUT = 2
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
 ORTHO_TF32, ORTHO_FP32, ORTHO_BF16 = 0, 1, 2
 ORTHO_SHORT_SIDE = 4  # OR into the precision: iterate in the short side's space
@@ -436,6 +438,27 @@ def _capturing(stream) -> bool:
     return stream_capturing(int(stream.cuda_stream))
 
 
+def _record_streams(tensors, stream, handle: int) -> list:
+    """record_stream for each CUDA tensor on `stream`, once per tensor object
+    and stream: the caching allocator fences every stream recorded on a block
+    when the block is freed, so one record covers every later use on that
+    stream while the tensor lives. Returns the CPU tensors, which need their
+    own hold."""
+    host = []
+    for t in tensors:
+        if t.device.type != "cuda":
+            host.append(t)
+            continue
+        seen = getattr(t, "_cam_recorded_streams", None)
+        if seen is None:
+            seen = set()
+            t._cam_recorded_streams = seen
+        if handle not in seen:
+            t.record_stream(stream)
+            seen.add(handle)
+    return host
+
+
 def _stream_handle(stream) -> int:
     torch = _torch()
     if stream is None:
@@ -451,14 +474,16 @@ class Merger:
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
                  zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
-                 staging=True, time_commits=False, fused_finish=True):
+                 staging=True, time_commits=False, fused_finish=True, test_stall_staged=False):
         """rows: optional per-tensor matrix rows (default: the tensors' first
         dimension), used by orthogonalised rounds. staging=False keeps every
         merge pass on the register form (the staged form gives the same
         results). time_commits=True times each commit's device work
         (last_commit()["ms"]). fused_finish=False always launches the
         separate norm pass (small rounds otherwise finish their norms in the
-        merge pass; the same bits)."""
+        merge pass; the same bits). test_stall_staged=True is a test hook
+        (CAM_TEST_STALL_STAGED): staged passes withhold their first tile, their
+        waits give up after about 1 ms and status() reports the timeout."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -485,7 +510,8 @@ class Merger:
         flags = (INIT_EMA_FROM_MASTER if init_ema_from_master else 0) | \
                 (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
                 (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0) | \
-                (0 if fused_finish else NO_FUSED_FINISH)
+                (0 if fused_finish else NO_FUSED_FINISH) | \
+                (TEST_STALL_STAGED if test_stall_staged else 0)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,
@@ -498,6 +524,7 @@ class Merger:
                 rows=list(rows) if rows is not None else
                 [t.shape[0] if t.dim() >= 2 else 0 for t in self.master])
         self._frag_cache = {}
+        self._inflight = []  # (event, host tensors) held until the work reading them ran
 
     def close(self):
         if getattr(self, "ctx", None):
@@ -517,7 +544,7 @@ class Merger:
         """Keeps host checkpoints referenced until the work that reads them
         has run (torch cannot record a stream on a CPU tensor)."""
         torch = _torch()
-        self._inflight = [(ev, ts) for ev, ts in getattr(self, "_inflight", []) if not ev.query()]
+        self._inflight = [(ev, ts) for ev, ts in self._inflight if not ev.query()]
         if host_tensors:
             ev = torch.cuda.Event()
             ev.record(stream)
@@ -661,17 +688,12 @@ class Round:
         elif ckpt.merger is not self.merger or ckpt.fragment != self.fragment:
             raise ValueError("checkpoint was prepared for another merger or fragment")
         s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
+        sh = int(s.cuda_stream)
         _check(lib().cam_merge_fold(self.handle, ckpt.ptr_array, ckpt.dtype_code, int(tokens),
-                                    int(mode), int(s.cuda_stream)))
-        if _capturing(s):
+                                    int(mode), sh))
+        if stream_capturing(sh):
             return
-        host = []
-        for t in ckpt.keep:
-            if t.device.type == "cuda":
-                t.record_stream(s)
-            else:
-                host.append(t)
-        self.merger._hold_until_done(host, s)
+        self.merger._hold_until_done(_record_streams(ckpt.keep, s, sh), s)
 
     def finalize(self, mode: int, lr: float = 1.0, mu: float = 0.0) -> None:
         merge_finalize(self.handle, mode, lr, mu)
@@ -734,22 +756,20 @@ class Round:
     def commit(self, stream=None) -> None:
         torch = _torch()
         s = torch.cuda.current_stream(self.merger.device) if stream is None else stream
+        sh = int(s.cuda_stream)
         try:
-            merge_commit(self.handle, int(s.cuda_stream))
+            merge_commit(self.handle, sh)
         except CudaError:
             self.handle = None  # the library freed the round
             raise
         self.handle = None
         borrowed, self._borrowed = self._borrowed, []
-        if _capturing(s):
+        if stream_capturing(sh):
             return  # a captured graph reads its buffers at every replay: they are the caller's
-        host = []
-        for t in borrowed:  # freed memory is not reused before the merge ran
-            if t.device.type == "cuda":
-                t.record_stream(s)
-            else:
-                host.append(t)
-        self.merger._hold_until_done(host, s)
+        # freed memory is not reused before the merge ran
+        host = _record_streams(borrowed, s, sh)
+        if host or self.merger._inflight:
+            self.merger._hold_until_done(host, s)
 
     def abort(self) -> None:
         merge_abort(self.handle)

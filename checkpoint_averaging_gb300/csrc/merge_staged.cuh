@@ -57,6 +57,7 @@ namespace cam {
 namespace dev {
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
+constexpr unsigned long long kTestWaitLimitNs = 1000000ull;  // 1 ms (CAM_TEST_STALL_STAGED)
 
 // ---- PTX: shared-memory addresses, mbarriers, bulk copies ---------------------
 
@@ -108,12 +109,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Waits until the phase with the given parity has completed; false when
-// kWaitLimitNs pass first.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// `limit` nanoseconds pass first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_test(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit) return false;
     return true;
 }
 
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring0 = smem_u32(ring);
     volatile int* abort_v = &abort_flag;
+    const unsigned long long lim = a.test_stall ? kTestWaitLimitNs : kWaitLimitNs;
 
     if (warp == kProducerWarp) {
         // ---- producer: lane 0 walks the block's chunks and issues every
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
                 const int s = it % P, n = it / P;
                 // the stage's previous tile must be released by every consumer warp
-                if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1)) {
+                if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) {
                     ok = false;
                     break;
                 }
@@ -333,7 +336,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 mt.l = l;
                 mt.last = t0 + kStTile >= ch.len;
                 const uint32_t bar = smem_u32(&full[s]);
-                if (len8 == 0) {  // a tensor of fewer than 8 elements: nothing to copy
+                if (a.test_stall && it == 0) {
+                    // test hook: the first tile is never issued, so its
+                    // consumers' waits run out
+                } else if (len8 == 0) {  // a tensor of fewer than 8 elements: nothing to copy
                     mbar_arrive(bar);
                 } else {
                     const uint32_t st = ring0 + s * stage_bytes;
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
         if (ok) {  // the end marker: a stage with len 0
             const int s = it % P, n = it / P;
-            if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1)) ok = false;
+            if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) ok = false;
             if (ok) {
                 meta[s].len = 0;
                 mbar_arrive(smem_u32(&full[s]));
@@ -365,11 +371,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
         // that no copy is in flight when the block exits.
         const int j0 = it > P ? it - P : 0;
         for (int j = j0; ok && j < it; ++j)
-            if (!mbar_wait(smem_u32(&empty[j % P]), (j / P) & 1)) ok = false;
+            if (!mbar_wait(smem_u32(&empty[j % P]), (j / P) & 1, lim)) ok = false;
         if (!ok) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
-            for (int j = j0; j < it; ++j) mbar_wait(smem_u32(&full[j % P]), (j / P) & 1);
+            for (int j = j0; j < it; ++j) mbar_wait(smem_u32(&full[j % P]), (j / P) & 1, lim);
         }
         return;
     }
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++ci) {
                 const int slot = ci % kStRedSlots, use = ci / kStRedSlots;
                 if (*abort_v) return;
-                if (!mbar_wait(smem_u32(&red_full[slot]), use & 1)) {
+                if (!mbar_wait(smem_u32(&red_full[slot]), use & 1, lim)) {
                     *abort_v = 1;
                     atomicOr(a.status, kStatusWaitTimeout);
                     return;
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     // the wait for a free slot gave up.
     auto hand_over = [&](int ci) -> bool {
         const int slot = ci % kStRedSlots, use = ci / kStRedSlots;
-        if (use > 0 && !mbar_wait(smem_u32(&red_empty[slot]), (use - 1) & 1)) {
+        if (use > 0 && !mbar_wait(smem_u32(&red_empty[slot]), (use - 1) & 1, lim)) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
             return false;
@@ -438,7 +444,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     // Waits for stage s's use n; false (with the abort flag set) on a timeout.
     auto wait_full = [&](int s, int n) -> bool {
         if (*abort_v) return false;
-        if (!mbar_wait(smem_u32(&full[s]), n & 1)) {
+        if (!mbar_wait(smem_u32(&full[s]), n & 1, lim)) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
             return false;

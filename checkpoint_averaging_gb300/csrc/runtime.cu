@@ -135,6 +135,7 @@ struct cam_ctx {
     }
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     bool staged = true;            // the staged form of the merge pass may be used
+    bool test_stall = false;       // CAM_TEST_STALL_STAGED
     bool time_commits = false;     // CAM_TIME_COMMITS: events around each commit
     cudaEvent_t commit_ev[2] = {nullptr, nullptr};
     cam_commit_record last_commit{};
@@ -265,7 +266,8 @@ int validate_desc(const cam_ctx_desc* d) {
         return fail(CAM_E_ARG, "cam_ctx_create: quorum must be in [1, %d]", CAM_KMAX);
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
     if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
-                     CAM_NO_STAGING | CAM_TIME_COMMITS | CAM_NO_FUSED_FINISH))
+                     CAM_NO_STAGING | CAM_TIME_COMMITS | CAM_NO_FUSED_FINISH |
+                     CAM_TEST_STALL_STAGED))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -443,6 +445,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
                     }
     c->fuse_finish = !(d->flags & CAM_NO_FUSED_FINISH);
     c->staged = !(d->flags & CAM_NO_STAGING);
+    c->test_stall = (d->flags & CAM_TEST_STALL_STAGED) != 0;
     c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
     for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
         ce = cudaEventCreate(&c->commit_ev[i]);
@@ -1002,6 +1005,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.status = c->d_status;
     a.st_stages = st_stages;
     a.st_stage_bytes = static_cast<int32_t>(st_bytes);
+    a.test_stall = c->test_stall ? 1 : 0;
     // Fused pass over the fragment's local tensors [lb, le).
     auto launch_range = [&](int lb, int le) {
         for (int l0 = lb; l0 < le && ce == cudaSuccess; l0 += per_launch) {

@@ -66,7 +66,7 @@ class GpuState:
 
 
 def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
-                   fused_finish=True) -> GpuState:
+                   fused_finish=True, test_stall_staged=False) -> GpuState:
     theta = W.empty_arena(g.numels, torch.float32, dev)
     theta.flat.copy_(g.flat)
     m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
@@ -79,7 +79,7 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
                   swa=None if swa is None else swa.views, staging=staging,
-                  fused_finish=fused_finish)
+                  fused_finish=fused_finish, test_stall_staged=test_stall_staged)
     return GpuState(theta, m, e, mg, swa)
 
 
@@ -233,6 +233,25 @@ def gather_state(st: GpuState, tensors, idxs):
     return (gather(st.theta, tensors, idxs),
             gather(st.m, tensors, idxs) if st.m is not None else None,
             gather(st.e, tensors, idxs) if st.e is not None else None)
+
+
+def sliced_tensor_norm(wl, workers, draw, theta_before, t: int, step: int = 1 << 27) -> float:
+    """Oracle drift norm of one tensor too large to copy to the host at once
+    (theta_before: its state before, on the device): the oracle's fp64 sum of
+    squared drift slice by slice, the slice sums added in fp64."""
+    xs = [workers[k].views[t] for k in draw.included]
+    n = theta_before.numel()
+    s = 0.0
+    for a in range(0, n, step):
+        b = min(n, a + step)
+        th = to_np(theta_before[a:b]).copy()
+        m = np.zeros_like(th) if wl.mode == "delta" else None
+        s += oracle.merge_tensor(
+            [to_np(x[a:b]) for x in xs], th,
+            mode=oracle.DELTA_NESTEROV if wl.mode == "delta" else oracle.MEAN_REPLACE,
+            tokens=[draw.tokens[k] for k in draw.included] if wl.mode == "delta" else None,
+            lr=wl.lr, mu=wl.mu, m=m)
+    return math.sqrt(s)
 
 
 def full_tensor_norm(wl, workers, draw, theta_before: np.ndarray, t: int) -> float:

@@ -24,7 +24,7 @@ from checkpoint_averaging_gb300 import workloads as W
 from merge_harness import (assert_close, bitwise_equal, compare_full, gather_state,
                            gpu_round, make_gpu_state, oracle_round, oracle_state_from,
                            run_full, sample_indices, sampled_round_check, to_np,
-                           full_tensor_norm, NORM_RTOL)
+                           full_tensor_norm, sliced_tensor_norm, NORM_RTOL)
 
 pytestmark = pytest.mark.gpu
 
@@ -185,24 +185,14 @@ def test_ragged_and_empty_tensors(dtype, mode):
     run_full(_custom(RAGGED, K=3, mode=mode, dtype=dtype), seed=7)
 
 
-def _drift_norm_fp64(delta_of, n, step=1 << 27):
-    """sqrt(sum delta^2) in fp64 over [0, n), in slices; delta_of(a, b) gives
-    the fp32 drift of elements [a, b) as a device tensor."""
-    s = 0.0
-    for a in range(0, n, step):
-        d = delta_of(a, min(n, a + step)).double()
-        s += float(torch.dot(d, d))
-    return math.sqrt(s)
-
-
 @pytest.mark.parametrize("mode,fold", [("mean", False), ("mean", True), ("delta", False)])
 def test_tensor_of_more_than_2_pow_31_elements(mode, fold):
     """One tensor of 2^31 + 13 elements (and a small one after it): 64-bit
     element offsets in every form. Plain mean + EMA takes the staged form,
     Nesterov + EMA the register form, fold=True the fold and final passes.
     Sampled elements, 2^31 and 2^32 neighbourhoods included, match the
-    oracle; the big tensor's drift norm matches its definition summed in
-    fp64."""
+    oracle; the big tensor's drift norm matches the oracle's, summed slice by
+    slice in fp64."""
     n = (1 << 31) + 13
     wl = _custom([n, 2049], K=2, mode=mode, dtype="bf16", ema=True, norms=True)
     g = W.make_global(wl, 17, DEV)
@@ -218,18 +208,7 @@ def test_tensor_of_more_than_2_pow_31_elements(mode, fold):
     pt, pf = gpu_round(st, wl, 0, -1, workers, draw, fold=fold)
     torch.cuda.synchronize()
     sampled_round_check(wl, st, -1, workers, draw, idxs, before, f"2^31+13 elements, {mode}")
-    xs = [workers[k].views[0] for k in draw.included]
-
-    def delta_of(a, b):
-        th = th0[a:b]
-        if mode == "mean":      # theta' - theta, theta' = (x_1 + x_2) / 2
-            return (xs[0][a:b].float() + xs[1][a:b].float()) / 2 - th
-        w = [float(draw.tokens[k]) for k in draw.included]   # Delta = sum w_k (x_k - theta) / W
-        s = torch.tensor(w[0], device=th.device) * (xs[0][a:b].float() - th)
-        s = s + torch.tensor(w[1], device=th.device) * (xs[1][a:b].float() - th)
-        return s / float(sum(draw.tokens[k] for k in draw.included))
-
-    want = _drift_norm_fp64(delta_of, n)
+    want = sliced_tensor_norm(wl, workers, draw, th0, 0)
     got = pt[0].item()
     assert abs(got - want) <= NORM_RTOL * want, (got, want)
     assert abs(pf.item() - math.sqrt(got ** 2 + pt[1].item() ** 2)) <= 1e-9 * pf.item()
@@ -1149,6 +1128,41 @@ def test_fused_norm_finish_equals_the_norm_pass(mode, dtype, ema, publish, host)
     for st in states:
         assert st.merger.status() == 0
         st.merger.close()
+
+
+@pytest.mark.parametrize("mode,norms", [("mean", False), ("delta", True)])
+def test_staged_wait_that_runs_out_is_reported_and_the_device_recovers(mode, norms):
+    """The staged pass's bounded waits, driven to their limit on purpose: with
+    CAM_TEST_STALL_STAGED every staged pass withholds its first tile, so its
+    consumers' waits (and, with norms, the reducer's) give up after about 1 ms.
+    The pass returns with CAM_STATUS_WAIT_TIMEOUT in the context's status word
+    and no copy in flight; nothing faults or hangs. A fresh context on the
+    same device then runs the round and matches the oracle."""
+    wl = _custom([300_000, 70_000, 2049], K=2, mode=mode, ema=mode == "mean", norms=norms)
+    g = W.make_global(wl, 0, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
+    # the norm pass stays separate, so a round with norms takes the staged form too
+    st = make_gpu_state(wl, g, DEV, fused_finish=False, test_stall_staged=True)
+    n0 = st.merger.staged_count
+    gpu_round(st, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    assert st.merger.staged_count - n0 > 0
+    assert st.merger.status() & B.STATUS_WAIT_TIMEOUT
+    st.merger.close()
+    fresh = make_gpu_state(wl, g, DEV, fused_finish=False)
+    gn = gpu_round(fresh, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    assert fresh.merger.staged_count > 0
+    ost = oracle_state_from(g, wl)
+    norms_want = oracle_round(ost, wl, 0, -1, workers, draw)
+    compare_full(fresh, ost, f"after a stalled pass: {mode}")
+    if norms:
+        pt, _ = norms_want
+        got = gn[0].cpu().numpy()[:len(pt)]
+        assert np.all(np.abs(got - np.asarray(pt)) <= NORM_RTOL * np.abs(np.asarray(pt)))
+    assert fresh.merger.status() == 0
+    fresh.merger.close()
 
 
 @pytest.mark.parametrize("mode,ema,swa,host,staging,want_staged", [
