@@ -15,11 +15,14 @@
 //                    (2 x BN fp32 columns), tcgen05.commit releasing the
 //                    stage and, after a tile's last stage, the accumulator;
 //                    warp 1 also allocates and frees the TMEM;
-//   warps 2..5       epilogue: each owns 32 TMEM lanes (rows of the tile),
-//                    reads 32 columns at a time with tcgen05.ld, hands the
-//                    accumulator back as soon as its last columns are in
-//                    registers, and writes the tile (and, where asked, its
-//                    transpose) to global memory.
+//   warps 2..5       epilogue: each owns 32 TMEM lanes (rows of the tile) and
+//                    works in 32 x 32 boxes: tcgen05.ld of 32 columns, the
+//                    scaling, the box (and, where asked, its transpose)
+//                    written to a per-warp shared-memory staging buffer, and
+//                    a TMA tensor store of each from lane 0. Two staging
+//                    buffers per warp let one box's store overlap the next
+//                    box's work; the accumulator is handed back as soon as
+//                    its last columns are in registers.
 //
 // Two accumulators let the epilogue of one tile overlap the MMAs of the next.
 // Shared-memory operands use the canonical K-major 128-byte-swizzled layout
@@ -28,10 +31,10 @@
 // apart inside each swizzled row.
 //
 // Every mbarrier wait is bounded (kTcWaitLimitNs of %globaltimer). A wait that
-// runs out sets CAM_STATUS_GEMM_TIMEOUT in the status word and a block-wide abort
-// flag; every role then leaves its loop, the producer waits (bounded) for the
-// copies it issued, the MMA issuer for its MMAs, and warp 1 frees the TMEM
-// before the block exits.
+// runs out sets CAM_STATUS_GEMM_TIMEOUT in the status word and a block-wide
+// abort flag; every role then leaves its loop, the producer waits (bounded)
+// for the copies it issued, the MMA issuer for its MMAs, the epilogue for its
+// stores, and warp 1 frees the TMEM before the block exits.
 //
 // CUDA-core kernel nt_gemm_simt: 128 x 128 tiles, 8 x 8 outputs per thread,
 // fp32 fused multiply-adds; used for CAM_ORTHO_FP32.
@@ -53,9 +56,12 @@ constexpr int kBM = 128;                 // tile rows (TMEM lanes)
 constexpr int kTcThreads = 192;          // six warps
 constexpr int kRowBytes = 128;           // one swizzled row of a stage: the K step
 constexpr int kBoxBytes = kBM * kRowBytes;  // one 128-row TMA box: 16 KB
-constexpr int kSmemBudget = 192 * 1024;  // the stage ring
+constexpr int kSmemBudget = 224 * 1024;  // the stage ring and the epilogue staging
 constexpr unsigned long long kTcWaitLimitNs = 4000000000ull;
 constexpr int kEpiPart = 2;              // Gram split: fp32 partial tiles
+constexpr int kEpiAxpbyC = 3;            // kNtAxpby reading C (prefetched by TMA)
+constexpr int kOutBox = 32;              // epilogue boxes: 32 x 32 elements
+constexpr int kEpiWarps = 4;
 
 // ---- PTX wrappers ---------------------------------------------------------------
 
@@ -193,11 +199,39 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Three-dimensional tiled TMA store of a shared-memory box, in this thread's
+// bulk async-group.
+__device__ __forceinline__ void tma_store(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Until at most one of this thread's groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Until every group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Makes this thread's shared-memory writes visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- kernel arguments -------------------------------------------------------------
 
 struct alignas(128) TcArgs {
     CUtensorMap ta;          // A: dims {K, M, batch}, box {K step, 128, 1}
     CUtensorMap tb;          // B: dims {K, N, batch}, box {K step, 128, 1}
+    CUtensorMap ty;          // Y (or the Gram split partials): boxes of 32 x 32
+    CUtensorMap tyt;         // Yt, or Y read transposed (Gram mirror): boxes of 32 x 32
+    CUtensorMap tcm;         // C (kEpiAxpbyC): boxes of 32 x 32, swizzled as box_row
     int32_t batch;
     int32_t m_blocks;        // M / 128
     int32_t n_blocks;        // N / BN
@@ -206,11 +240,8 @@ struct alignas(128) TcArgs {
     int32_t k_per_split;     // Gram: K steps per range
     int32_t n_tri;           // Gram: tiles per matrix reaching the upper triangle
     int32_t n_units;         // tiles (x splits) over the whole batch
-    float alpha, beta;
-    const void* C; int64_t ldc, sC;
-    void* Y; int64_t ldy, sY;
-    void* Yt; int64_t ldyt, sYt;
-    float* P;                // Gram split: fp32 partial of range s, matrix b at P + (s*batch+b)*M*M
+    int32_t has_y, has_yt;
+    float alpha, beta, diag;
     int32_t* status;
 };
 
@@ -223,7 +254,7 @@ struct Unit {
 template <int BN, int EPI>
 __device__ __forceinline__ Unit decode(const TcArgs& a, int u) {
     Unit t;
-    if constexpr (EPI == kNtAxpby) {
+    if constexpr (EPI == kNtAxpby || EPI == kEpiAxpbyC) {
         const int per = a.m_blocks * a.n_blocks;
         t.b = u / per;
         const int rem = u - t.b * per;
@@ -253,83 +284,120 @@ __device__ __forceinline__ Unit decode(const TcArgs& a, int u) {
     return t;
 }
 
-// ---- epilogue stores -------------------------------------------------------------
+// ---- epilogue boxes ----------------------------------------------------------------
 
-template <bool BF16>
-struct Store;
-
-template <>
-struct Store<true> {  // bf16, rounded to nearest-even
-    using T = __nv_bfloat16;
-    __device__ static void row32(T* dst, const float* v) {  // 64 bytes, 16-byte aligned
+// One 32 x 32 box of results in shared memory, as the TMA store reads it.
+// Row-major boxes (lane r writes its 32 values as row r): bf16 rows are 64
+// bytes under the 64-byte swizzle (16-byte chunk q of row r at chunk
+// q ^ ((r >> 1) & 3)), fp32 rows 128 bytes under the 128-byte swizzle (chunk
+// q ^ (r & 7)), so a warp's 16-byte writes spread over all banks.
+// Transposed boxes (value (r, c) at element c * 32 + r) are unswizzled: lane
+// r's writes for one c are consecutive across the warp.
+template <bool BF16OUT>
+__device__ __forceinline__ void box_row(uint32_t buf, int r, const float* v) {
+    if constexpr (BF16OUT) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+            uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
                 w[e] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            reinterpret_cast<uint4*>(dst)[q] = o;
+            const uint32_t addr = buf + r * 64 + 16 * (q ^ ((r >> 1) & 3));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                         "r"(w[2]), "r"(w[3])
+                         : "memory");
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t addr = buf + r * 128 + 16 * (q ^ (r & 7));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v[4 * q]),
+                         "f"(v[4 * q + 1]), "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                         : "memory");
         }
     }
-    __device__ static void one(T* dst, float v) { *dst = __float2bfloat16_rn(v); }
-    __device__ static void load32(const T* src, float* v) {
+}
+
+// Row r of a row-major box as box_row lays it out (and TMA loads it).
+template <bool BF16IN>
+__device__ __forceinline__ void box_row_read(uint32_t buf, int r, float* v) {
+    if constexpr (BF16IN) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 i = reinterpret_cast<const uint4*>(src)[q];
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(&i);
+            uint32_t w[4];
+            const uint32_t addr = buf + r * 64 + 16 * (q ^ ((r >> 1) & 3));
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(addr)
+                         : "memory");
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 v[8 * q + 2 * e] = __uint_as_float(w[e] << 16);
                 v[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
             }
         }
-    }
-};
-
-template <>
-struct Store<false> {  // fp32
-    using T = float;
-    __device__ static void row32(T* dst, const float* v) {  // 128 bytes, 16-byte aligned
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    }
-    __device__ static void one(T* dst, float v) { *dst = v; }
-    __device__ static void load32(const T* src, float* v) {
+    } else {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const float4 f = reinterpret_cast<const float4*>(src)[q];
-            v[4 * q] = f.x;
-            v[4 * q + 1] = f.y;
-            v[4 * q + 2] = f.z;
-            v[4 * q + 3] = f.w;
+            const uint32_t addr = buf + r * 128 + 16 * (q ^ (r & 7));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[4 * q]), "=f"(v[4 * q + 1]), "=f"(v[4 * q + 2]), "=f"(v[4 * q + 3])
+                         : "r"(addr)
+                         : "memory");
         }
     }
-};
+}
+
+template <bool BF16OUT>
+__device__ __forceinline__ void box_col(uint32_t buf, int r, const float* v) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        if constexpr (BF16OUT) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v[c]);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + (c * 32 + r) * 2),
+                         "h"(*reinterpret_cast<const unsigned short*>(&h))
+                         : "memory");
+        } else {
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(buf + (c * 32 + r) * 4), "f"(v[c]) : "memory");
+        }
+    }
+}
 
 // ---- the tensor-core kernel --------------------------------------------------------
 
-template <bool BF16, int BN>
+template <bool BF16, int BN, int EPI>
 struct Geo {
     static constexpr int kBBytes = BN * kRowBytes;
     static constexpr int kStage = kBoxBytes + kBBytes;
-    static constexpr int kStages = kSmemBudget / kStage < 8 ? kSmemBudget / kStage : 8;
-    static constexpr int kBarOffset = kStages * kStage;
-    // ring + barriers (full, empty, tmem full, tmem empty, drain) + TMEM
-    // address + abort flag, plus 1 KB to align the ring to 1,024 bytes
-    static constexpr int kSmem = kBarOffset + 8 * (2 * kStages + 5) + 16 + 1024;
+    // epilogue staging: per warp two buffers, each one box and its transpose
+    // (the Gram split: one fp32 box)
+    static constexpr int kOutBytes = (EPI == kEpiPart || !BF16) ? 4 : 2;
+    static constexpr int kBox = kOutBox * kOutBox * kOutBytes;
+    static constexpr int kStgBuf = (EPI == kEpiPart ? 1 : 2) * kBox;
+    // kEpiAxpbyC: one box of C per warp, prefetched a box ahead
+    static constexpr int kCBox = kOutBox * kOutBox * (BF16 ? 2 : 4);
+    static constexpr int kCRegion = EPI == kEpiAxpbyC ? kEpiWarps * kCBox : 0;
+    static constexpr int kStaging = kEpiWarps * 2 * kStgBuf + kCRegion;
+    static constexpr int kStagesFit = (kSmemBudget - kStaging) / kStage;
+    static constexpr int kStages = kStagesFit < 8 ? kStagesFit : 8;
+    static constexpr int kStgOffset = kStages * kStage;
+    static constexpr int kBarOffset = kStgOffset + kStaging;
+    // ring + staging + barriers (full, empty, tmem full, tmem empty, drain,
+    // one "C full" per epilogue warp) + TMEM address + abort flag, plus 1 KB
+    // to align the ring to 1,024 bytes
+    static constexpr int kBars = 2 * kStages + 5 + kEpiWarps;
+    static constexpr int kSmem = kBarOffset + 8 * kBars + 16 + 1024;
     static constexpr int kKStep = kRowBytes / (BF16 ? 2 : 4);  // elements per K step
-    static constexpr int kUmmaK = 32 / (BF16 ? 2 : 4);           // elements per MMA
+    static_assert(kStages >= 2, "shared memory too small for the ring");
+    static_assert(kSmem <= 232448, "over the per-block shared memory limit");
 };
 
 template <bool BF16, int BN, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constant__ TcArgs a) {
-    using G = Geo<BF16, BN>;
-    using S = Store<BF16>;
-    using T = typename S::T;
+    using G = Geo<BF16, BN, EPI>;
+    constexpr bool kOutBf16 = BF16 && EPI != kEpiPart;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -339,7 +407,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
     const uint32_t tfull0 = empty0 + 8 * G::kStages;
     const uint32_t tempty0 = tfull0 + 16;
     const uint32_t drain = tempty0 + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::kStages + 5);
+    const uint32_t cfull0 = drain + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + G::kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t kCols = 2 * BN;  // two accumulators
@@ -351,9 +420,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         }
         for (int i = 0; i < 2; ++i) {
             bar_init(tfull0 + 8 * i, 1);
-            bar_init(tempty0 + 8 * i, 4);  // one arrival per epilogue warp
+            bar_init(tempty0 + 8 * i, kEpiWarps);  // one arrival per epilogue warp
         }
         bar_init(drain, 1);
+        for (int w = 0; w < kEpiWarps; ++w) bar_init(cfull0 + 8 * w, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.ta)) : "memory");
@@ -452,9 +522,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         }
     } else if (warp >= 2) {
         // ---- epilogue ----
-        const int quarter = warp & 3;          // TMEM lanes 32 quarter .. + 31
-        const int r_in = quarter * 32 + lane;  // row of the tile
-        int acc = 0;
+        const int quarter = warp & 3;  // TMEM lanes 32 quarter .. + 31: rows of the tile
+        const uint32_t stg = su32(smem + G::kStgOffset + (warp - 2) * 2 * G::kStgBuf);
+        // kEpiAxpbyC: this warp's box of C, loaded by TMA one box ahead
+        const uint32_t cbuf = su32(smem + G::kStgOffset + kEpiWarps * 2 * G::kStgBuf +
+                                   (warp - 2) * G::kCBox);
+        const uint32_t cbar = cfull0 + 8 * (warp - 2);
+        uint32_t c_phase = 0;
+        bool c_pending = false;
+        auto load_c = [&](int u, int cc) {  // lane 0: the C box of unit u, column box cc
+            const Unit n = decode<BN, EPI>(a, u);
+            bar_expect(cbar, G::kCBox);
+            tma_load(cbuf, &a.tcm, n.cb * BN + cc * 32, n.rb * kBM + quarter * 32, n.b, cbar);
+        };
+        if (EPI == kEpiAxpbyC && lane == 0 && int(blockIdx.x) < a.n_units) {
+            load_c(blockIdx.x, 0);
+            c_pending = true;
+        }
+        int acc = 0, buf = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
             const Unit t = decode<BN, EPI>(a, u);
@@ -462,8 +547,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
             const bool ok = bar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int64_t row = int64_t(t.rb) * kBM + r_in;
+            const int row0 = t.rb * kBM + quarter * 32;  // first row of this warp's boxes
             const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
+            const int z = EPI == kEpiPart ? t.split * a.batch + t.b : t.b;
+            bool aborted = false;
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
                 float v[32];
@@ -473,48 +560,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                     __syncwarp();
                     if (lane == 0) bar_arrive(tempty0 + 8 * acc);
                 }
-                const int64_t col0 = int64_t(t.cb) * BN + cc * 32;
-                if constexpr (EPI == kNtAxpby) {
-                    if (a.beta != 0.0f) {
-                        float c[32];
-                        S::load32(static_cast<const T*>(a.C) + t.b * a.sC + row * a.ldc + col0, c);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = fmaf(a.alpha, v[i], a.beta * c[i]);
-                    } else if (a.alpha != 1.0f) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= a.alpha;
+                const int col0 = t.cb * BN + cc * 32;
+                bool direct, mirror;
+                if constexpr (EPI == kNtGram) {  // 32 x 32 boxes on / above the diagonal
+                    direct = col0 >= row0;
+                    mirror = col0 > row0;
+                } else if constexpr (EPI == kNtAxpby || EPI == kEpiAxpbyC) {
+                    direct = a.has_y != 0;
+                    mirror = a.has_yt != 0;
+                } else {
+                    direct = true;
+                    mirror = false;
+                }
+                if constexpr (EPI == kEpiAxpbyC) {
+                    const bool cok = bar_wait(cbar, c_phase, abort_flag, a.status);
+                    if (!__all_sync(0xffffffffu, cok)) {
+                        aborted = true;
+                        break;
                     }
-                    if (a.Y) S::row32(static_cast<T*>(a.Y) + t.b * a.sY + row * a.ldy + col0, v);
-                    if (a.Yt) {
-                        T* yt = static_cast<T*>(a.Yt) + t.b * a.sYt + row;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) S::one(yt + (col0 + i) * a.ldyt, v[i]);
-                    }
-                } else if constexpr (EPI == kNtGram) {
-                    T* y = static_cast<T*>(a.Y) + t.b * a.sY;
-                    if (col0 > row) {  // the whole chunk lies above the diagonal
-                        S::row32(y + row * a.ldy + col0, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) S::one(y + (col0 + i) * a.ldy + row, v[i]);
-                    } else if (col0 + 31 >= row) {  // the chunk crosses it
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int64_t col = col0 + i;
-                            if (col >= row) S::one(y + row * a.ldy + col, v[i]);
-                            if (col > row) S::one(y + col * a.ldy + row, v[i]);
+                    c_phase ^= 1;
+                    float c[32];
+                    box_row_read<BF16>(cbuf, lane, c);
+                    __syncwarp();  // every lane has read the box before it is refilled
+                    c_pending = false;
+                    if (lane == 0) {
+                        const int nu = cc + 1 < BN / 32 ? u : u + int(gridDim.x);
+                        if (nu < a.n_units) {
+                            load_c(nu, cc + 1 < BN / 32 ? cc + 1 : 0);
+                            c_pending = true;
                         }
                     }
-                } else {  // kEpiPart: the whole fp32 tile of this split
-                    const int64_t M = int64_t(a.m_blocks) * kBM;
-                    float* p = a.P + (int64_t(t.split) * a.batch + t.b) * M * M;
-                    Store<false>::row32(p + row * M + col0, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = fmaf(a.alpha, v[i], a.beta * c[i]);
+                } else if constexpr (EPI != kEpiPart) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= a.alpha;
                 }
+                if (!direct && !mirror) continue;
+                if constexpr (EPI != kEpiPart) {
+                    if (col0 == row0) {  // this lane's diagonal element is column `lane`
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i == lane) v[i] += a.diag;
+                    }
+                }
+                // the buffer's store from two boxes ago has finished reading it
+                if (lane == 0) bulk_wait_read1();
+                __syncwarp();
+                const uint32_t yb = stg + buf * G::kStgBuf;
+                const uint32_t ytb = yb + G::kBox;
+                if (direct) box_row<kOutBf16>(yb, lane, v);
+                if (mirror) box_col<kOutBf16>(ytb, lane, v);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (direct) tma_store(&a.ty, yb, col0, row0, z);
+                    if (mirror) tma_store(&a.tyt, ytb, row0, col0, t.b);
+                    bulk_commit();
+                }
+                buf ^= 1;
             }
+            if (aborted) break;
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) {
+            if (c_pending) {  // a C box still in flight lands before the block exits
+                const unsigned long long t0 = now_ns();
+                while (!bar_test(cbar, c_phase))
+                    if (now_ns() - t0 > kTcWaitLimitNs) break;
+            }
+            bulk_wait_all();  // stores done before the block (and its smem) goes
+        }
+        __syncwarp();
     }
     __syncthreads();
     if (warp == 1) {
@@ -525,36 +645,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
     }
 }
 
-// Sums the split partials of Gram matrices in range order and writes the whole
-// symmetric matrix: element (i, j) takes the partials of (min, max), so both
-// triangles carry the same bits. 32 x 32 tiles through shared memory, on and
-// above the diagonal; each writes itself and its mirror.
+// Sums the split partials of Gram products in range order and writes
+// Y = alpha sum + diag I, the whole symmetric matrix: element (i, j) takes the
+// partials of (min, max), so both triangles carry the same bits. 32 x 32 tiles
+// through shared memory, on and above the diagonal; each writes itself and
+// its mirror.
 template <typename T>
-__global__ void gram_reduce(const float* P, int splits, int batch, int64_t M, T* Y, int64_t ldy,
-                            int64_t sY) {
+__global__ void gram_reduce(const float* P, int splits, int batch, int64_t M, float alpha, float diag,
+                            T* Y, int64_t ldy, int64_t sY) {
     __shared__ float tile[32][33];
     const int b = blockIdx.z;
     const int64_t ti = blockIdx.y, tj = blockIdx.x;
     if (tj < ti) return;
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const int64_t split_stride = int64_t(batch) * M * M;
     for (int r = ty; r < 32; r += 8) {
         const int64_t i = ti * 32 + r, j = tj * 32 + tx;
+        // diagonal tile: the upper element of the pair
+        const float* p = P + int64_t(b) * M * M + (j >= i ? i * M + j : j * M + i);
         float s = 0.0f;
-        for (int q = 0; q < splits; ++q) {
-            const float* p = P + (int64_t(q) * batch + b) * M * M;
-            s += (j >= i) ? p[i * M + j] : p[j * M + i];  // diagonal tile: the upper element
-        }
-        tile[r][tx] = s;
+#pragma unroll 8
+        for (int q = 0; q < splits; ++q) s += p[q * split_stride];  // range order
+        tile[r][tx] = alpha * s + (i == j ? diag : 0.0f);
     }
     __syncthreads();
-    using St = Store<sizeof(T) == 2>;
     T* y = Y + b * sY;
     for (int r = ty; r < 32; r += 8) {
         const int64_t i = ti * 32 + r, j = tj * 32 + tx;
-        St::one(y + i * ldy + j, tile[r][tx]);
+        y[i * ldy + j] = T(tile[r][tx]);
         if (tj > ti) {  // the mirror (j, i): row tj*32 + r, column ti*32 + tx
             const int64_t mi = tj * 32 + r, mj = ti * 32 + tx;
-            St::one(y + mi * ldy + mj, tile[tx][r]);
+            y[mi * ldy + mj] = T(tile[tx][r]);
         }
     }
 }
@@ -569,7 +690,7 @@ struct SimtArgs {
     const float* B; int64_t ldb, sB;
     int64_t K;
     int32_t n_blocks;   // N / 128
-    float alpha, beta;
+    float alpha, beta, diag;
     const float* C; int64_t ldc, sC;
     float* Y; int64_t ldy, sY;
     float* Yt; int64_t ldyt, sYt;
@@ -638,6 +759,9 @@ __global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_consta
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (row == col + j) v[j] += a.diag;
             if (a.Y)
                 *reinterpret_cast<float4*>(a.Y + b * a.sY + row * a.ldy + col) =
                     make_float4(v[0], v[1], v[2], v[3]);
@@ -667,32 +791,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return g_encode;
 }
 
-// Tensor map over `batch` row-major matrices of `rows` x `k` elements (row
-// stride ld, matrix stride sm, in elements): boxes of one K step x 128 rows,
-// 128-byte swizzle, zero fill outside.
-int make_map(CUtensorMap* map, bool bf16, const void* base, int64_t k, int64_t rows, int64_t batch,
-             int64_t ld, int64_t sm) {
+// Tensor map over `batch` row-major matrices of `rows` x `cols` elements
+// (row stride ld, matrix stride sm, in elements), with boxes of
+// box_cols x box_rows elements; zero fill outside.
+int make_map(CUtensorMap* map, int64_t eb, const void* base, int64_t cols, int64_t rows,
+             int64_t batch, int64_t ld, int64_t sm, int box_cols, int box_rows,
+             CUtensorMapSwizzle swz) {
     const auto enc = encoder();
     if (!enc) return record_error(CAM_E_CUDA, "orthogonalisation: cuTensorMapEncodeTiled unavailable");
-    const int64_t eb = bf16 ? 2 : 4;
-    const cuuint64_t dims[3] = {cuuint64_t(k), cuuint64_t(rows), cuuint64_t(batch)};
+    const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(batch)};
     const cuuint64_t strides[2] = {cuuint64_t(ld * eb), cuuint64_t(sm * eb)};
-    const cuuint32_t box[3] = {cuuint32_t(kRowBytes / eb), cuuint32_t(kBM), 1};
+    const cuuint32_t box[3] = {cuuint32_t(box_cols), cuuint32_t(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
-        enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        enc(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return record_error(CAM_E_CUDA, "orthogonalisation: cuTensorMapEncodeTiled failed (%d)",
                             static_cast<int>(r));
     return CAM_OK;
 }
 
+// Operand map: boxes of one K step (128 bytes) x 128 rows, 128-byte swizzle.
+int operand_map(CUtensorMap* map, int64_t eb, const void* base, int64_t k, int64_t rows,
+                int64_t batch, int64_t ld, int64_t sm) {
+    return make_map(map, eb, base, k, rows, batch, ld, sm, static_cast<int>(kRowBytes / eb), kBM,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output maps: 32 x 32 boxes; row-major boxes swizzled as box_row writes
+// them, transposed boxes plain.
+int out_map(CUtensorMap* map, int64_t eb, void* base, int64_t cols, int64_t rows, int64_t batch,
+            int64_t ld, int64_t sm, bool row_box) {
+    const CUtensorMapSwizzle swz = !row_box ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                   : eb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_128B;
+    return make_map(map, eb, base, cols, rows, batch, ld, sm, kOutBox, kOutBox, swz);
+}
+
 template <bool BF16, int BN, int EPI>
 cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
-    using G = Geo<BF16, BN>;
+    using G = Geo<BF16, BN, EPI>;
     static cudaError_t attr = cudaFuncSetAttribute(
         nt_gemm_tc<BF16, BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (attr != cudaSuccess) return attr;
@@ -700,16 +840,20 @@ cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <bool BF16, int BN>
+cudaError_t launch_tc_epi(const TcArgs& a, int epi, int grid, cudaStream_t s) {
+    switch (epi) {
+        case kNtAxpby: return launch_tc<BF16, BN, kNtAxpby>(a, grid, s);
+        case kNtGram: return launch_tc<BF16, BN, kNtGram>(a, grid, s);
+        case kEpiAxpbyC: return launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
+        default: return launch_tc<BF16, BN, kEpiPart>(a, grid, s);
+    }
+}
+
 template <bool BF16>
 cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, int grid, cudaStream_t s) {
-    if (bn == 256) {
-        if (epi == kNtAxpby) return launch_tc<BF16, 256, kNtAxpby>(a, grid, s);
-        if (epi == kNtGram) return launch_tc<BF16, 256, kNtGram>(a, grid, s);
-        return launch_tc<BF16, 256, kEpiPart>(a, grid, s);
-    }
-    if (epi == kNtAxpby) return launch_tc<BF16, 128, kNtAxpby>(a, grid, s);
-    if (epi == kNtGram) return launch_tc<BF16, 128, kNtGram>(a, grid, s);
-    return launch_tc<BF16, 128, kEpiPart>(a, grid, s);
+    return bn == 256 ? launch_tc_epi<BF16, 256>(a, epi, grid, s)
+                     : launch_tc_epi<BF16, 128>(a, epi, grid, s);
 }
 
 int launch_fail(cudaError_t e) {
@@ -727,8 +871,9 @@ int run_simt(const NtGemm& g, cudaStream_t s, int64_t* launches) {
     a.K = g.K;
     a.n_blocks = static_cast<int32_t>(g.N / 128);
     const bool gram = g.epilogue == kNtGram;
-    a.alpha = gram ? 1.0f : g.alpha;
+    a.alpha = g.alpha;
     a.beta = gram ? 0.0f : g.beta;
+    a.diag = g.diag;
     a.C = static_cast<const float*>(g.C);
     a.ldc = g.ldc;
     a.sC = g.sC;
@@ -753,12 +898,13 @@ int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int6
         return record_error(CAM_E_ARG, "orthogonalisation: GEMM extents must be multiples of 128");
     if (g.precision == CAM_ORTHO_FP32) return run_simt(g, s, launches);
     const bool bf16 = g.precision == CAM_ORTHO_BF16;
+    const int64_t eb = bf16 ? 2 : 4;
     const int bn = g.N % 256 == 0 ? 256 : 128;
-    const int64_t kstep = kRowBytes / (bf16 ? 2 : 4);
+    const int64_t kstep = kRowBytes / eb;
     TcArgs a;
     std::memset(&a, 0, sizeof a);
-    int rc = make_map(&a.ta, bf16, g.A, g.K, g.M, g.batch, g.lda, g.sA);
-    if (rc == CAM_OK) rc = make_map(&a.tb, bf16, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
+    int rc = operand_map(&a.ta, eb, g.A, g.K, g.M, g.batch, g.lda, g.sA);
+    if (rc == CAM_OK) rc = operand_map(&a.tb, eb, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
     if (rc != CAM_OK) return rc;
     a.batch = g.batch;
     a.m_blocks = static_cast<int32_t>(g.M / kBM);
@@ -766,15 +912,7 @@ int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int6
     a.k_blocks = static_cast<int32_t>(g.K / kstep);
     a.alpha = g.alpha;
     a.beta = g.beta;
-    a.C = g.C;
-    a.ldc = g.ldc;
-    a.sC = g.sC;
-    a.Y = g.Y;
-    a.ldy = g.ldy;
-    a.sY = g.sY;
-    a.Yt = g.Yt;
-    a.ldyt = g.ldyt;
-    a.sYt = g.sYt;
+    a.diag = g.diag;
     a.status = status;
     a.splits = 1;
     a.k_per_split = a.k_blocks;
@@ -800,14 +938,30 @@ int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int6
         if (splits > 1) {
             a.k_per_split = (a.k_blocks + splits - 1) / splits;
             a.splits = (a.k_blocks + a.k_per_split - 1) / a.k_per_split;  // no empty range
-            a.P = g.partials;
             epi = kEpiPart;
+            rc = out_map(&a.ty, 4, g.partials, g.M, g.M, int64_t(a.splits) * g.batch, g.M,
+                         g.M * g.M, true);
+        } else {
+            rc = out_map(&a.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
+            if (rc == CAM_OK)  // the mirror: the same matrix, boxes written transposed
+                rc = out_map(&a.tyt, eb, g.Y, g.M, g.N, g.batch, g.ldy, g.sY, false);
         }
         a.n_units = static_cast<int32_t>(tiles * a.splits);
     } else {
         a.n_tri = 0;
         a.n_units = static_cast<int32_t>(int64_t(a.m_blocks) * a.n_blocks * g.batch);
+        a.has_y = g.Y != nullptr;
+        a.has_yt = g.Yt != nullptr;
+        if (a.has_y) rc = out_map(&a.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
+        if (rc == CAM_OK && a.has_yt)
+            rc = out_map(&a.tyt, eb, g.Yt, g.M, g.N, g.batch, g.ldyt, g.sYt, false);
+        if (rc == CAM_OK && g.beta != 0.0f) {  // C, read in boxes like the row-major output
+            if (!g.C) return record_error(CAM_E_ARG, "orthogonalisation: beta needs C");
+            epi = kEpiAxpbyC;
+            rc = out_map(&a.tcm, eb, const_cast<void*>(g.C), g.N, g.M, g.batch, g.ldc, g.sC, true);
+        }
     }
+    if (rc != CAM_OK) return rc;
     const int grid = std::min(a.n_units, sm_count);
     const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, grid, s)
                                : launch_tc_any<false>(a, bn, epi, grid, s);
@@ -818,9 +972,11 @@ int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int6
                          static_cast<unsigned>(g.batch));
         if (bf16)
             gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 8), 0, s>>>(
-                g.partials, a.splits, g.batch, g.M, static_cast<__nv_bfloat16*>(g.Y), g.ldy, g.sY);
+                g.partials, a.splits, g.batch, g.M, g.alpha, g.diag,
+                static_cast<__nv_bfloat16*>(g.Y), g.ldy, g.sY);
         else
             gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(g.partials, a.splits, g.batch, g.M,
+                                                             g.alpha, g.diag,
                                                              static_cast<float*>(g.Y), g.ldy, g.sY);
         ++*launches;
         const cudaError_t r = cudaGetLastError();

@@ -6,10 +6,11 @@
 //     D[b][i][j] = sum_k A[b][i][k] * B[b][j][k]      (A: M x K, B: N x K)
 //
 // Both operands are row-major with K contiguous ("K-major" for the tensor
-// cores), so every product the iteration needs is one of these: the Gram
-// matrix G = W W^T of an iterate W (A = B = W), and the update
-// V' = 1.5 V - 0.5 V G of its transpose V = W^T (A = V, B = G, which is
-// symmetric), whose epilogue also writes W' = V'^T for the next Gram matrix.
+// cores), so every product the iteration needs is one of these: the matrix
+// H = 1.5 I - 0.5 W W^T of an iterate W (a Gram product, A = B = W, with the
+// step's combination in its epilogue), and the update V' = V H of its
+// transpose V = W^T (A = V, B = H, which is symmetric), whose epilogue also
+// writes W' = V'^T for the next Gram product.
 //
 // M, N and K are multiples of 128, with zero padding outside the matrices'
 // own extent (zero rows and columns stay zero through the iteration), so no
@@ -17,8 +18,8 @@
 //
 // Precisions: CAM_ORTHO_BF16 (bf16 operands and results, fp32 accumulation)
 // and CAM_ORTHO_TF32 (fp32 storage read as TF32, fp32 accumulation) run on the
-// tensor cores (tcgen05.mma with TMEM accumulators, operands staged by TMA);
-// CAM_ORTHO_FP32 runs a CUDA-core fp32 kernel.
+// tensor cores (tcgen05.mma with TMEM accumulators, operands staged by TMA,
+// results written back by TMA); CAM_ORTHO_FP32 runs a CUDA-core fp32 kernel.
 #pragma once
 
 #include <cuda.h>
@@ -30,12 +31,13 @@ namespace cam {
 
 // What the epilogue does with the accumulated tile D.
 enum NtEpilogue : int {
-    // Y = alpha D + beta C (C optional), stored to Y (optional) and, transposed,
-    // to Yt (optional).
+    // Y = alpha D + beta C + diag I (C optional: CUDA-core kernel only),
+    // stored to Y (optional) and, transposed, to Yt (optional).
     kNtAxpby = 0,
-    // The Gram matrix of A (B must be A, M = N): only tiles that reach the
-    // upper triangle are computed; each stores its elements on and above the
-    // diagonal and mirrors those above it, so Y is the whole symmetric matrix.
+    // Y = alpha D + diag I with D the Gram matrix of A (B must be A, M = N):
+    // only tiles that reach the upper triangle are computed; each stores its
+    // 32 x 32 boxes on and above the diagonal and mirrors those above it, so
+    // Y is the whole symmetric matrix, every element written once.
     kNtGram = 1,
 };
 
@@ -46,8 +48,8 @@ struct NtGemm {
     int64_t M, N, K;        // multiples of 128
     const void* A; int64_t lda, sA;   // row stride and batch stride, in elements
     const void* B; int64_t ldb, sB;
-    float alpha, beta;
-    const void* C; int64_t ldc, sC;   // read by kNtAxpby when beta != 0
+    float alpha, beta, diag;
+    const void* C; int64_t ldc, sC;   // CAM_ORTHO_FP32 only: read when beta != 0
     void* Y; int64_t ldy, sY;
     void* Yt; int64_t ldyt, sYt;      // kNtAxpby: transposed copy, or null
     // Gram matrices of long operands split their K range over several blocks

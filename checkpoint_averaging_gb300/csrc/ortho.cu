@@ -12,10 +12,12 @@
 //      multiples of 128 (nt_gemm.h);
 //   3. `iterations` Newton-Schulz steps W <- 1.5 W - 0.5 (W W^T) W, which
 //      drive every singular value to 1 and so converge to the polar factor
-//      U V^T. Each step is two NT GEMMs (nt_gemm.cu): the Gram matrix
-//      G = W W^T (symmetric: only its upper triangle is computed and then
-//      mirrored), then V' = 1.5 V - 0.5 V G with the combination in the GEMM's
-//      epilogue, which also writes W' = V'^T;
+//      U V^T. Each step is two NT GEMMs (nt_gemm.cu): H = 1.5 I - 0.5 W W^T
+//      (a Gram product with the combination in its epilogue; symmetric, so
+//      only its upper triangle is computed and then mirrored), then
+//      V' = V H, whose epilogue also writes W' = V'^T. H is stored in the
+//      iterate's type. With TF32 inputs the step stays in the form
+//      V' = 1.5 V - 0.5 V G, V read in fp32 by the epilogue;
 //   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), read
 //      from V (tall) or W (wide), then the EMA of the globals.
 // Equal-shape matrices run as one batch through every kernel.
@@ -305,6 +307,7 @@ NtGemm nt(int precision, int epi, int B, int64_t M, int64_t N, int64_t K, const 
     g.sB = sB;
     g.alpha = 1.0f;
     g.beta = 0.0f;
+    g.diag = 0.0f;
     return g;
 }
 
@@ -505,23 +508,32 @@ int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoPar
             cur = 1;
         }
         for (int it = 0; !short_side && it < p.iterations; ++it) {
-            // G = W W^T (upper triangle, mirrored)
+            // bf16 and fp32: H = 1.5 I - 0.5 W W^T (upper triangle, mirrored),
+            // then V' = V H. TF32: G = W W^T, then V' = 1.5 V - 0.5 V G with V
+            // read in fp32 in the epilogue, so that only the correction passes
+            // through TF32 inputs (V H would round the whole iterate to TF32
+            // on every step).
+            const bool cform = p.precision == CAM_ORTHO_TF32;
             NtGemm g = nt(p.precision, kNtGram, B, sh.rp, sh.rp, sh.Lp, w->W[cur], sh.Lp, padded,
                           w->W[cur], sh.Lp, padded);
+            g.alpha = cform ? 1.0f : -0.5f;
+            g.diag = cform ? 0.0f : 1.5f;
             g.Y = w->G;
             g.ldy = sh.rp;
             g.sY = sq;
             g.partials = w->split;
             g.partial_floats = kSplitFloats;
             if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
-            // V' = 1.5 V - 0.5 V G, W' = V'^T
+            // V' = V H (or 1.5 V - 0.5 V G), W' = V'^T
             g = nt(p.precision, kNtAxpby, B, sh.Lp, sh.rp, sh.rp, w->V[cur], sh.rp, padded, w->G,
                    sh.rp, sq);
-            g.alpha = -0.5f;
-            g.beta = 1.5f;
-            g.C = w->V[cur];
-            g.ldc = sh.rp;
-            g.sC = padded;
+            if (cform) {
+                g.alpha = -0.5f;
+                g.beta = 1.5f;
+                g.C = w->V[cur];
+                g.ldc = sh.rp;
+                g.sC = padded;
+            }
             g.Y = w->V[1 - cur];
             g.ldy = sh.rp;
             g.sY = padded;

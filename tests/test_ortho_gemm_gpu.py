@@ -3,13 +3,15 @@ technical report, section 5.3), one step at a time, through the C ABI.
 
 With `iterations = 1` an orthogonalised round applies
 theta' = theta + lr X1 with X1 = 1.5 X0 - 0.5 (X0 X0^T) X0 (Gram matrix on the
-short side) and X0 = Delta / |Delta|_F. The reference here restates that one
+short side) and X0 = Delta / |Delta|_F; the library forms it as X1 = H X0 (wide
+orientation) with H = 1.5 I - 0.5 X0 X0^T, or, with TF32 inputs, as
+1.5 X0 - 0.5 G X0 with X0 read in fp32. The reference here restates that one
 step in fp64 from the round's Delta (the oracle's plain mean minus theta) and
 reproduces the roundings the library's storage makes: X0 rounded once to the
-iterate's type, the Gram matrix stored in it. What remains between the two is
-fp32 accumulation against fp64 and the final rounding of X1, so the bound is a
-few units of the storage type's rounding, far below what a wrong index, a
-dropped term or a transposed operand would leave.
+iterate's type, H (or G) stored in it. What remains between the two is fp32
+accumulation against fp64, TF32 inputs, and the final rounding of X1, so the
+bound is a few units of the storage type's rounding, far below what a wrong
+index, a dropped term or a transposed operand would leave.
 
 The shapes cover every path of the GEMM kernels: tiles 128 and 256 wide, more
 than one tile each way, sides that are not multiples of 128 (zero padding),
@@ -59,7 +61,7 @@ def _to_bf16(a):
 def newton_schulz_step(delta, precision):
     """One Newton-Schulz step from Delta, in fp64, with the library's storage
     roundings: X0 = fp32(Delta * fp32(1/|Delta|_F)), rounded to bf16 for a bf16
-    iterate; the Gram matrix rounded to bf16 for a bf16 iterate."""
+    iterate; H = 1.5 I - 0.5 W W^T rounded to the iterate's type."""
     m, n = delta.shape
     d64 = delta.astype(np.float64)
     inv = np.float32(1.0 / np.sqrt(np.sum(d64 * d64)))
@@ -67,10 +69,14 @@ def newton_schulz_step(delta, precision):
     if precision == B.ORTHO_BF16:
         x0 = _to_bf16(x0)
     w = x0.T.astype(np.float64) if m >= n else x0.astype(np.float64)  # r x L
-    g = w @ w.T
-    if precision == B.ORTHO_BF16:
-        g = _to_bf16(g.astype(np.float32)).astype(np.float64)
-    x1 = 1.5 * w - 0.5 * (g @ w)
+    if precision == B.ORTHO_TF32:  # X1 = 1.5 X0 - 0.5 G X0, X0 exact in the epilogue
+        g = (w @ w.T).astype(np.float32).astype(np.float64)
+        x1 = 1.5 * w - 0.5 * (g @ w)
+    else:                          # X1 = H X0, H stored in the iterate's type
+        h = (1.5 * np.eye(w.shape[0]) - 0.5 * (w @ w.T)).astype(np.float32)
+        if precision == B.ORTHO_BF16:
+            h = _to_bf16(h)
+        x1 = h.astype(np.float64) @ w
     return x1.T if m >= n else x1
 
 
