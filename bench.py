@@ -402,6 +402,14 @@ def run_ours(args, wl, ws, rank, local) -> int:
                 for (_, frag), w, d in zip(wl.rounds, workers, draws)]
 
     group_pairs = []
+    # Rounds on disjoint fragments go to the stream with the fewest bytes so far
+    # (largest round first), so a long round runs beside the short ones.
+    rb = [round_bytes(wl, f, len(d.included)) for (_, f), d in zip(wl.rounds, draws)]
+    load = [0] * n_streams
+    stream_of = [0] * len(wl.rounds)
+    for i in sorted(range(len(wl.rounds)), key=lambda i: -rb[i]):
+        stream_of[i] = min(range(n_streams), key=lambda j: load[j])
+        load[stream_of[i]] += rb[i]
 
     def step(timed: bool) -> None:
         main = streams[0]
@@ -411,7 +419,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
         for s in streams[1:]:
             s.wait_stream(main)
         for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
-            s = streams[i % n_streams]
+            s = streams[stream_of[i]]
             rd = mg.begin(round_no[0], frag)
             round_no[0] += 1
             for k in d.included:
@@ -963,6 +971,140 @@ def run_ortho(args, wl, ws, rank, local) -> int:
     return 0
 
 
+def run_hostcost(args, wl, ws, rank, local) -> int:
+    """Host time the C ABI spends per round: the workload's rounds (begin,
+    accumulate for each included worker, finalize, optional EMA and drift
+    norms, commit) issued in a loop through ctypes with every argument made
+    ahead of time, each call timed with perf_counter_ns. ctypes' own cost per
+    call, taken from a call that does nothing (cam_ctx_launch_count), is
+    reported beside it and subtracted in `library_us_per_round`. The same
+    rounds through the binding's Merger/Round give `binding_us_per_round`.
+    The device is synchronised between batches of rounds, outside the timed
+    calls, so no call waits for a full launch queue."""
+    import ctypes
+    import time
+
+    import torch
+
+    import __graft_entry__
+    from checkpoint_averaging_gb300 import binding as B
+    from checkpoint_averaging_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    seed = args.seed
+    g = W.make_global(wl, seed, dev)
+    theta = W.empty_arena(g.numels, torch.float32, dev)
+    theta.flat.copy_(g.flat)
+    m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
+    e = None
+    if wl.ema_beta is not None:
+        e = W.empty_arena(g.numels, torch.float32, dev)
+        e.flat.copy_(g.flat)
+    draws = [W.draw_round(wl, i, seed) for i in range(len(wl.rounds))]
+    workers = [[W.make_worker(wl, g, rnd, k, seed, dev) for k in range(wl.K)]
+               for rnd, _ in wl.rounds]
+    mg = B.Merger(theta.views, momentum=None if m is None else m.views,
+                  ema=None if e is None else e.views, fragment_of=wl.fragment_of,
+                  n_fragments=wl.n_fragments, quorum=wl.quorum)
+    mode = B.DELTA_NESTEROV if wl.mode == "delta" else B.MEAN_REPLACE
+    L = B.lib()
+    s = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(int(s.cuda_stream))
+    prepared = [{k: mg.checkpoint(w[k].views, frag) for k in d.included}
+                for (_, frag), w, d in zip(wl.rounds, workers, draws)]
+    norm_out = [(torch.zeros(max(1, len(mg.fragment_tensors(f))), dtype=torch.float64, device=dev),
+                 torch.zeros(1, dtype=torch.float64, device=dev)) for _, f in wl.rounds]
+    calls = ["begin", "accumulate", "finalize", "ema_update", "drift_norm", "commit"]
+    tot = dict.fromkeys(calls, 0)
+    cnt = dict.fromkeys(calls, 0)
+    rnd = [0]
+    ns = time.perf_counter_ns
+
+    def raw_round(i):
+        (_, frag), d = wl.rounds[i], draws[i]
+        h = ctypes.c_void_p()
+        t = ns(); rc = L.cam_merge_begin(mg.ctx, rnd[0], frag, ctypes.byref(h)); tot["begin"] += ns() - t
+        cnt["begin"] += 1
+        rnd[0] += 1
+        if rc != 0:
+            raise RuntimeError(B.last_error())
+        for k in d.included:
+            c = prepared[i][k]
+            t = ns(); L.cam_merge_accumulate(h, c.ptr_array, c.dtype_code, d.tokens[k])
+            tot["accumulate"] += ns() - t
+            cnt["accumulate"] += 1
+        t = ns(); L.cam_merge_finalize(h, mode, wl.lr, wl.mu); tot["finalize"] += ns() - t
+        cnt["finalize"] += 1
+        if wl.ema_beta is not None:
+            t = ns(); L.cam_ema_update(h, wl.ema_beta); tot["ema_update"] += ns() - t
+            cnt["ema_update"] += 1
+        if wl.norms:
+            pt, pf = norm_out[i]
+            a, b = ctypes.c_void_p(pt.data_ptr()), ctypes.c_void_p(pf.data_ptr())
+            t = ns(); L.cam_drift_norm(h, a, b); tot["drift_norm"] += ns() - t
+            cnt["drift_norm"] += 1
+        t = ns(); rc = L.cam_merge_commit(h, sp); tot["commit"] += ns() - t
+        cnt["commit"] += 1
+        if rc != 0:
+            raise RuntimeError(B.last_error())
+
+    def binding_round(i):
+        (_, frag), d = wl.rounds[i], draws[i]
+        rd = mg.begin(rnd[0], frag)
+        rnd[0] += 1
+        for k in d.included:
+            rd.accumulate(prepared[i][k], d.tokens[k])
+        rd.finalize(mode, wl.lr, wl.mu)
+        if wl.ema_beta is not None:
+            rd.ema_update(wl.ema_beta)
+        if wl.norms:
+            rd.drift_norm(*norm_out[i])
+        rd.commit(s)
+
+    n_rounds, batch = 600, 30
+    for i in range(len(wl.rounds) * 3):  # warm-up
+        raw_round(i % len(wl.rounds))
+    torch.cuda.synchronize(dev)
+    tot = dict.fromkeys(calls, 0)
+    cnt = dict.fromkeys(calls, 0)
+    for j in range(n_rounds):
+        raw_round(j % len(wl.rounds))
+        if (j + 1) % batch == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    out = ctypes.c_int64()
+    t = ns()
+    for _ in range(20000):
+        L.cam_ctx_launch_count(mg.ctx, ctypes.byref(out))
+    noop_us = (ns() - t) / 20000 / 1e3
+    per_call = {c: tot[c] / cnt[c] / 1e3 for c in calls if cnt[c]}
+    calls_per_round = sum(cnt.values()) / n_rounds
+    raw_us = sum(tot.values()) / n_rounds / 1e3
+    bind_ns = 0
+    for j in range(n_rounds):
+        t = ns()
+        binding_round(j % len(wl.rounds))
+        bind_ns += ns() - t
+        if (j + 1) % batch == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    mg.close()
+    print(json.dumps({
+        "metric": "host us per round (C ABI)", "value": round(raw_us - calls_per_round * noop_us, 2),
+        "unit": "us", "n_gpus": 1, "steps": n_rounds, "warmup": 3 * len(wl.rounds),
+        "higher_is_better": False, "data": "synthetic",
+        "config": {"workload": wl.name, "op": "hostcost", "calls_per_round": calls_per_round},
+        "library_us_per_round": round(raw_us - calls_per_round * noop_us, 2),
+        "ctypes_us_per_round": round(raw_us, 2), "ctypes_noop_us_per_call": round(noop_us, 3),
+        "per_call_us_with_ctypes": {c: round(v, 2) for c, v in per_call.items()},
+        "binding_us_per_round": round(bind_ns / n_rounds / 1e3, 2)}), flush=True)
+    return 0
+
+
 def parse(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -970,7 +1112,7 @@ def parse(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="diffurefill1b")
-    p.add_argument("--op", choices=("merge", "adopt", "ortho", "fold"), default="merge")
+    p.add_argument("--op", choices=("merge", "adopt", "ortho", "fold", "hostcost"), default="merge")
     p.add_argument("--ortho-iterations", type=int, default=30)
     p.add_argument("--ortho-precision", choices=("tf32", "fp32", "bf16"), default="tf32")
     p.add_argument("--ortho-short-side", action="store_true",
@@ -1004,6 +1146,8 @@ def main(argv=None) -> int:
         return run_adopt(args, wl, ws, rank, local)
     if args.op == "ortho":
         return run_ortho(args, wl, ws, rank, local)
+    if args.op == "hostcost":
+        return run_hostcost(args, wl, ws, rank, local)
     if args.op == "fold":
         return run_fold(args, wl, ws, rank, local)
     return run_ours(args, wl, ws, rank, local)

@@ -202,9 +202,11 @@ class Workload:
 
 
 def _wl_pythia() -> Workload:
+    # three fragment rounds per step; as in the Pythia page's run ("Getting
+    # updates through the bucket"), two rounds may be in flight at once
     return Workload("pythia14m_f4_q3_delta_nesterov", tuple(pythia14m_specs()), 4,
                     K=4, n_masked=1, quorum=3, ckpt_dtype="f32", mode="delta",
-                    lr=0.7, mu=0.9, rounds=((0, 0), (1, 1), (2, 2)),
+                    lr=0.7, mu=0.9, rounds=((0, 0), (1, 1), (2, 2)), in_flight=2,
                     noise_std=1e-3, tokens=(200_000, 600_000), norms=True)
 
 
