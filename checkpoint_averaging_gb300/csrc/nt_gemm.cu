@@ -58,8 +58,8 @@ constexpr int kRowBytes = 128;           // one swizzled row of a stage: the K s
 constexpr int kBoxBytes = kBM * kRowBytes;  // one 128-row TMA box: 16 KB
 constexpr int kSmemBudget = 224 * 1024;  // the stage ring and the epilogue staging
 constexpr unsigned long long kTcWaitLimitNs = 4000000000ull;
-constexpr int kEpiPart = 2;              // Gram split: fp32 partial tiles
-constexpr int kEpiAxpbyC = 3;            // kNtAxpby reading C (prefetched by TMA)
+constexpr int kEpiAxpbyC = 2;            // kNtAxpby reading C (prefetched by TMA)
+constexpr int kMaxProblems = 8;          // problems per launch
 constexpr int kOutBox = 32;              // epilogue boxes: 32 x 32 elements
 constexpr int kEpiWarps = 4;
 
@@ -226,7 +226,10 @@ __device__ __forceinline__ void fence_async_smem() {
 
 // ---- kernel arguments -------------------------------------------------------------
 
-struct alignas(128) TcArgs {
+// One problem of a launch: a batch of equal-shape products with its own
+// tensor maps. A launch runs up to kMaxProblems problems of one precision, one
+// tile width and one epilogue kind, their units numbered one after another.
+struct alignas(128) TcProblem {
     CUtensorMap ta;          // A: dims {K, M, batch}, box {K step, 128, 1}
     CUtensorMap tb;          // B: dims {K, N, batch}, box {K step, 128, 1}
     CUtensorMap ty;          // Y (or the Gram split partials): boxes of 32 x 32
@@ -236,50 +239,62 @@ struct alignas(128) TcArgs {
     int32_t m_blocks;        // M / 128
     int32_t n_blocks;        // N / BN
     int32_t k_blocks;        // K / K step
-    int32_t splits;          // Gram: K ranges per tile
+    int32_t splits;          // Gram: K ranges per tile (> 1: fp32 partials)
     int32_t k_per_split;     // Gram: K steps per range
     int32_t n_tri;           // Gram: tiles per matrix reaching the upper triangle
-    int32_t n_units;         // tiles (x splits) over the whole batch
+    int32_t unit0;           // first unit of this problem in the launch
     int32_t has_y, has_yt;
+};
+
+struct alignas(128) TcArgs {
+    TcProblem prob[kMaxProblems];
+    int32_t n_problems;
+    int32_t n_units;         // units of every problem
     float alpha, beta, diag;
     int32_t* status;
 };
 
-// One unit of work: the tile's first rows in A and B, its matrix, its K steps
-// and (Gram split) its range.
+// One unit of work: its problem, the tile's first rows in A and B, its
+// matrix, its K steps and (Gram split) its range.
 struct Unit {
-    int b, rb, cb, split, k0, k1;
+    int p, b, rb, cb, split, k0, k1;
 };
 
 template <int BN, int EPI>
 __device__ __forceinline__ Unit decode(const TcArgs& a, int u) {
     Unit t;
+    int p = a.n_problems - 1;
+    while (p > 0 && u < a.prob[p].unit0) --p;
+    const TcProblem& P = a.prob[p];
+    u -= P.unit0;
+    t.p = p;
     if constexpr (EPI == kNtAxpby || EPI == kEpiAxpbyC) {
-        const int per = a.m_blocks * a.n_blocks;
+        const int per = P.m_blocks * P.n_blocks;
         t.b = u / per;
         const int rem = u - t.b * per;
-        t.rb = rem / a.n_blocks;
-        t.cb = rem - t.rb * a.n_blocks;
+        t.rb = rem / P.n_blocks;
+        t.cb = rem - t.rb * P.n_blocks;
         t.split = 0;
         t.k0 = 0;
-        t.k1 = a.k_blocks;
+        t.k1 = P.k_blocks;
     } else {
-        const int per = a.splits * a.n_tri;
-        t.b = u / per;
-        int rem = u - t.b * per;
-        t.split = rem / a.n_tri;
-        int q = rem - t.split * a.n_tri;
+        // ranges outermost: the units running at once share their K range
+        const int per_split = P.n_tri * P.batch;
+        t.split = u / per_split;
+        int rem = u - t.split * per_split;
+        t.b = rem / P.n_tri;
+        int q = rem - t.b * P.n_tri;
         // column block cb holds row blocks 0 .. (BN cb + BN - 1) / 128
         int cb = 0;
-        for (; cb < a.n_blocks - 1; ++cb) {
-            const int cnt = min(a.m_blocks, (BN * cb + BN - 1) / kBM + 1);
+        for (; cb < P.n_blocks - 1; ++cb) {
+            const int cnt = min(P.m_blocks, (BN * cb + BN - 1) / kBM + 1);
             if (q < cnt) break;
             q -= cnt;
         }
         t.rb = q;
         t.cb = cb;
-        t.k0 = t.split * a.k_per_split;
-        t.k1 = min(a.k_blocks, t.k0 + a.k_per_split);
+        t.k0 = t.split * P.k_per_split;
+        t.k1 = min(P.k_blocks, t.k0 + P.k_per_split);
     }
     return t;
 }
@@ -372,10 +387,11 @@ struct Geo {
     static constexpr int kBBytes = BN * kRowBytes;
     static constexpr int kStage = kBoxBytes + kBBytes;
     // epilogue staging: per warp two buffers, each one box and its transpose
-    // (the Gram split: one fp32 box)
-    static constexpr int kOutBytes = (EPI == kEpiPart || !BF16) ? 4 : 2;
+    // (a Gram split's fp32 partial box fits one buffer)
+    static constexpr int kOutBytes = BF16 ? 2 : 4;
     static constexpr int kBox = kOutBox * kOutBox * kOutBytes;
-    static constexpr int kStgBuf = (EPI == kEpiPart ? 1 : 2) * kBox;
+    static constexpr int kStgBuf = 2 * kBox;
+    static_assert(kStgBuf >= kOutBox * kOutBox * 4, "a partial box must fit a buffer");
     // kEpiAxpbyC: one box of C per warp, prefetched a box ahead
     static constexpr int kCBox = kOutBox * kOutBox * (BF16 ? 2 : 4);
     static constexpr int kCRegion = EPI == kEpiAxpbyC ? kEpiWarps * kCBox : 0;
@@ -397,7 +413,6 @@ struct Geo {
 template <bool BF16, int BN, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constant__ TcArgs a) {
     using G = Geo<BF16, BN, EPI>;
-    constexpr bool kOutBf16 = BF16 && EPI != kEpiPart;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -426,8 +441,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         for (int w = 0; w < kEpiWarps; ++w) bar_init(cfull0 + 8 * w, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.ta)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tb)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -440,6 +453,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: everything above overlapped its tail; no global memory is
+    // touched before it has completed. The next kernel may then start its
+    // own set-up as soon as SMs free up.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 && lane == 0) {
         // ---- producer ----
@@ -449,6 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         uint32_t filled_parity = 0;
         for (int u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
             const Unit t = decode<BN, EPI>(a, u);
+            const TcProblem& P = a.prob[t.p];
             const int arow = t.rb * kBM, brow = t.cb * BN;
             for (int kb = t.k0; kb < t.k1; ++kb) {
                 if (!bar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, a.status)) break;
@@ -456,10 +476,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                 const uint32_t fb = full0 + 8 * stage;
                 bar_expect(fb, G::kStage);
                 const int x = kb * G::kKStep;
-                tma_load(sa, &a.ta, x, arow, t.b, fb);
+                tma_load(sa, &P.ta, x, arow, t.b, fb);
 #pragma unroll
                 for (int h = 0; h < BN / kBM; ++h)
-                    tma_load(sa + kBoxBytes + h * kBoxBytes, &a.tb, x, brow + h * kBM, t.b, fb);
+                    tma_load(sa + kBoxBytes + h * kBoxBytes, &P.tb, x, brow + h * kBM, t.b, fb);
                 issued |= 1u << stage;
                 filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == G::kStages) {
@@ -533,7 +553,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         auto load_c = [&](int u, int cc) {  // lane 0: the C box of unit u, column box cc
             const Unit n = decode<BN, EPI>(a, u);
             bar_expect(cbar, G::kCBox);
-            tma_load(cbuf, &a.tcm, n.cb * BN + cc * 32, n.rb * kBM + quarter * 32, n.b, cbar);
+            tma_load(cbuf, &a.prob[n.p].tcm, n.cb * BN + cc * 32, n.rb * kBM + quarter * 32, n.b,
+                     cbar);
         };
         if (EPI == kEpiAxpbyC && lane == 0 && int(blockIdx.x) < a.n_units) {
             load_c(blockIdx.x, 0);
@@ -543,13 +564,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
             const Unit t = decode<BN, EPI>(a, u);
+            const TcProblem& P = a.prob[t.p];
             // the whole warp leaves together: tcgen05.ld is warp-collective
             const bool ok = bar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, a.status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const int row0 = t.rb * kBM + quarter * 32;  // first row of this warp's boxes
             const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(acc * BN);
-            const int z = EPI == kEpiPart ? t.split * a.batch + t.b : t.b;
+            // a Gram product split over K ranges writes fp32 partial boxes
+            const bool part = EPI == kNtGram && P.splits > 1;
+            const int z = part ? t.split * P.batch + t.b : t.b;
             bool aborted = false;
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
@@ -563,14 +587,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                 const int col0 = t.cb * BN + cc * 32;
                 bool direct, mirror;
                 if constexpr (EPI == kNtGram) {  // 32 x 32 boxes on / above the diagonal
-                    direct = col0 >= row0;
-                    mirror = col0 > row0;
-                } else if constexpr (EPI == kNtAxpby || EPI == kEpiAxpbyC) {
-                    direct = a.has_y != 0;
-                    mirror = a.has_yt != 0;
+                    direct = part || col0 >= row0;
+                    mirror = !part && col0 > row0;
                 } else {
-                    direct = true;
-                    mirror = false;
+                    direct = P.has_y != 0;
+                    mirror = P.has_yt != 0;
                 }
                 if constexpr (EPI == kEpiAxpbyC) {
                     const bool cok = bar_wait(cbar, c_phase, abort_flag, a.status);
@@ -592,30 +613,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = fmaf(a.alpha, v[i], a.beta * c[i]);
-                } else if constexpr (EPI != kEpiPart) {
+                } else {
+                    if (!part) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= a.alpha;
+                        for (int i = 0; i < 32; ++i) v[i] *= a.alpha;
+                    }
                 }
                 if (!direct && !mirror) continue;
-                if constexpr (EPI != kEpiPart) {
-                    if (col0 == row0) {  // this lane's diagonal element is column `lane`
+                if (!part && col0 == row0) {  // this lane's diagonal element is column `lane`
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i == lane) v[i] += a.diag;
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i == lane) v[i] += a.diag;
                 }
                 // the buffer's store from two boxes ago has finished reading it
                 if (lane == 0) bulk_wait_read1();
                 __syncwarp();
                 const uint32_t yb = stg + buf * G::kStgBuf;
                 const uint32_t ytb = yb + G::kBox;
-                if (direct) box_row<kOutBf16>(yb, lane, v);
-                if (mirror) box_col<kOutBf16>(ytb, lane, v);
+                if (part) {
+                    box_row<false>(yb, lane, v);
+                } else {
+                    if (direct) box_row<BF16>(yb, lane, v);
+                    if (mirror) box_col<BF16>(ytb, lane, v);
+                }
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (direct) tma_store(&a.ty, yb, col0, row0, z);
-                    if (mirror) tma_store(&a.tyt, ytb, row0, col0, t.b);
+                    if (direct) tma_store(&P.ty, yb, col0, row0, z);
+                    if (mirror) tma_store(&P.tyt, ytb, row0, col0, t.b);
                     bulk_commit();
                 }
                 buf ^= 1;
@@ -822,22 +847,34 @@ int operand_map(CUtensorMap* map, int64_t eb, const void* base, int64_t k, int64
 
 // Output maps: 32 x 32 boxes; row-major boxes swizzled as box_row writes
 // them, transposed boxes plain.
-int out_map(CUtensorMap* map, int64_t eb, void* base, int64_t cols, int64_t rows, int64_t batch,
-            int64_t ld, int64_t sm, bool row_box) {
+int out_map(CUtensorMap* map, int64_t eb, const void* base, int64_t cols, int64_t rows,
+            int64_t batch, int64_t ld, int64_t sm, bool row_box) {
     const CUtensorMapSwizzle swz = !row_box ? CU_TENSOR_MAP_SWIZZLE_NONE
                                    : eb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
                                              : CU_TENSOR_MAP_SWIZZLE_128B;
     return make_map(map, eb, base, cols, rows, batch, ld, sm, kOutBox, kOutBox, swz);
 }
 
+// Launched as a programmatic dependent of the previous kernel on the stream
+// (the kernel waits in griddepcontrol.wait before touching global memory).
 template <bool BF16, int BN, int EPI>
 cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
     using G = Geo<BF16, BN, EPI>;
     static cudaError_t attr = cudaFuncSetAttribute(
         nt_gemm_tc<BF16, BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (attr != cudaSuccess) return attr;
-    nt_gemm_tc<BF16, BN, EPI><<<grid, kTcThreads, G::kSmem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = G::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, nt_gemm_tc<BF16, BN, EPI>, a);
 }
 
 template <bool BF16, int BN>
@@ -845,8 +882,7 @@ cudaError_t launch_tc_epi(const TcArgs& a, int epi, int grid, cudaStream_t s) {
     switch (epi) {
         case kNtAxpby: return launch_tc<BF16, BN, kNtAxpby>(a, grid, s);
         case kNtGram: return launch_tc<BF16, BN, kNtGram>(a, grid, s);
-        case kEpiAxpbyC: return launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
-        default: return launch_tc<BF16, BN, kEpiPart>(a, grid, s);
+        default: return launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
     }
 }
 
@@ -892,92 +928,135 @@ int run_simt(const NtGemm& g, cudaStream_t s, int64_t* launches) {
 
 }  // namespace tc
 
-int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int64_t* launches) {
+int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t s,
+            int64_t* launches) {
     using namespace tc;
-    if (g.M % 128 || g.N % 128 || g.K % 128 || g.batch < 1)
-        return record_error(CAM_E_ARG, "orthogonalisation: GEMM extents must be multiples of 128");
-    if (g.precision == CAM_ORTHO_FP32) return run_simt(g, s, launches);
-    const bool bf16 = g.precision == CAM_ORTHO_BF16;
+    if (n < 1 || n > kMaxProblems)
+        return record_error(CAM_E_ARG, "orthogonalisation: 1 to %d problems per GEMM launch",
+                            kMaxProblems);
+    const NtGemm& g0 = gs[0];
+    bool all256 = true;
+    for (int i = 0; i < n; ++i) {
+        const NtGemm& g = gs[i];
+        if (g.M % 128 || g.N % 128 || g.K % 128 || g.batch < 1)
+            return record_error(CAM_E_ARG, "orthogonalisation: GEMM extents must be multiples of 128");
+        if (g.precision != g0.precision || g.epilogue != g0.epilogue || g.alpha != g0.alpha ||
+            g.beta != g0.beta || g.diag != g0.diag || (g.beta != 0.0f && !g.C))
+            return record_error(CAM_E_ARG, "orthogonalisation: problems of one launch must agree");
+        if (g.epilogue == kNtGram && (g.M != g.N || g.A != g.B))
+            return record_error(CAM_E_ARG, "orthogonalisation: a Gram product takes one operand");
+        all256 = all256 && g.N % 256 == 0;
+    }
+    if (g0.precision == CAM_ORTHO_FP32) {
+        for (int i = 0; i < n; ++i) {
+            const int rc = run_simt(gs[i], s, launches);
+            if (rc != CAM_OK) return rc;
+        }
+        return CAM_OK;
+    }
+    const bool bf16 = g0.precision == CAM_ORTHO_BF16;
     const int64_t eb = bf16 ? 2 : 4;
-    const int bn = g.N % 256 == 0 ? 256 : 128;
+    const int bn = all256 ? 256 : 128;
     const int64_t kstep = kRowBytes / eb;
+    const bool gram = g0.epilogue == kNtGram;
+    const int epi = gram ? kNtGram : (g0.beta != 0.0f ? kEpiAxpbyC : kNtAxpby);
     TcArgs a;
     std::memset(&a, 0, sizeof a);
-    int rc = operand_map(&a.ta, eb, g.A, g.K, g.M, g.batch, g.lda, g.sA);
-    if (rc == CAM_OK) rc = operand_map(&a.tb, eb, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
-    if (rc != CAM_OK) return rc;
-    a.batch = g.batch;
-    a.m_blocks = static_cast<int32_t>(g.M / kBM);
-    a.n_blocks = static_cast<int32_t>(g.N / bn);
-    a.k_blocks = static_cast<int32_t>(g.K / kstep);
-    a.alpha = g.alpha;
-    a.beta = g.beta;
-    a.diag = g.diag;
+    a.n_problems = n;
+    a.alpha = g0.alpha;
+    a.beta = g0.beta;
+    a.diag = g0.diag;
     a.status = status;
-    a.splits = 1;
-    a.k_per_split = a.k_blocks;
-    int epi = g.epilogue;
-    if (epi == kNtGram) {
-        if (g.M != g.N || g.A != g.B)
-            return record_error(CAM_E_ARG, "orthogonalisation: a Gram product takes one operand");
-        int tri = 0;
-        for (int cb = 0; cb < a.n_blocks; ++cb) tri += std::min(a.m_blocks, (bn * cb + bn - 1) / kBM + 1);
-        a.n_tri = tri;
-        // Split K when the tiles fill less than about one wave: ranges of at
-        // least 16 K steps, as many as bring the units near a whole number of
-        // waves, within the partial buffer.
-        const int64_t tiles = int64_t(tri) * g.batch;
-        int splits = 1;
-        if (tiles < sm_count && g.partials) {
-            const int64_t want = std::max<int64_t>(1, sm_count / tiles);
-            const int64_t by_k = std::max<int64_t>(1, a.k_blocks / 16);
-            const int64_t by_mem = g.partial_floats / (g.batch * g.M * g.M);
-            splits = static_cast<int>(std::min({want, by_k, by_mem}));
-            splits = std::max(splits, 1);
-        }
-        if (splits > 1) {
-            a.k_per_split = (a.k_blocks + splits - 1) / splits;
-            a.splits = (a.k_blocks + a.k_per_split - 1) / a.k_per_split;  // no empty range
-            epi = kEpiPart;
-            rc = out_map(&a.ty, 4, g.partials, g.M, g.M, int64_t(a.splits) * g.batch, g.M,
-                         g.M * g.M, true);
+    // Gram products: tiles reaching the upper triangle, and a K split for
+    // products whose tiles are long, so that no unit is much longer than a
+    // third of one block's share of the launch (ranges of at least 16 K
+    // steps, within the partial buffer).
+    int64_t work = 0;
+    for (int i = 0; i < n; ++i) {
+        TcProblem& P = a.prob[i];
+        const NtGemm& g = gs[i];
+        P.batch = g.batch;
+        P.m_blocks = static_cast<int32_t>(g.M / kBM);
+        P.n_blocks = static_cast<int32_t>(g.N / bn);
+        P.k_blocks = static_cast<int32_t>(g.K / kstep);
+        P.splits = 1;
+        P.k_per_split = P.k_blocks;
+        if (gram) {
+            int tri = 0;
+            for (int cb = 0; cb < P.n_blocks; ++cb)
+                tri += std::min(P.m_blocks, (bn * cb + bn - 1) / kBM + 1);
+            P.n_tri = tri;
+            work += int64_t(tri) * g.batch * P.k_blocks;
         } else {
-            rc = out_map(&a.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
-            if (rc == CAM_OK)  // the mirror: the same matrix, boxes written transposed
-                rc = out_map(&a.tyt, eb, g.Y, g.M, g.N, g.batch, g.ldy, g.sY, false);
-        }
-        a.n_units = static_cast<int32_t>(tiles * a.splits);
-    } else {
-        a.n_tri = 0;
-        a.n_units = static_cast<int32_t>(int64_t(a.m_blocks) * a.n_blocks * g.batch);
-        a.has_y = g.Y != nullptr;
-        a.has_yt = g.Yt != nullptr;
-        if (a.has_y) rc = out_map(&a.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
-        if (rc == CAM_OK && a.has_yt)
-            rc = out_map(&a.tyt, eb, g.Yt, g.M, g.N, g.batch, g.ldyt, g.sYt, false);
-        if (rc == CAM_OK && g.beta != 0.0f) {  // C, read in boxes like the row-major output
-            if (!g.C) return record_error(CAM_E_ARG, "orthogonalisation: beta needs C");
-            epi = kEpiAxpbyC;
-            rc = out_map(&a.tcm, eb, const_cast<void*>(g.C), g.N, g.M, g.batch, g.ldc, g.sC, true);
+            work += int64_t(P.m_blocks) * P.n_blocks * g.batch * P.k_blocks;
         }
     }
-    if (rc != CAM_OK) return rc;
-    const int grid = std::min(a.n_units, sm_count);
+    const int64_t longest = std::max<int64_t>(16, work / (3 * int64_t(sm_count)));
+    int64_t part_used = 0;
+    int32_t units = 0;
+    for (int i = 0; i < n; ++i) {
+        TcProblem& P = a.prob[i];
+        const NtGemm& g = gs[i];
+        int rc = operand_map(&P.ta, eb, g.A, g.K, g.M, g.batch, g.lda, g.sA);
+        if (rc == CAM_OK) rc = operand_map(&P.tb, eb, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
+        if (rc != CAM_OK) return rc;
+        P.unit0 = units;
+        if (gram) {
+            int splits = 1;
+            if (P.k_blocks > longest && g.partials) {
+                const int64_t want = (P.k_blocks + longest - 1) / longest;
+                const int64_t by_mem = (g.partial_floats - part_used) / (int64_t(g.batch) * g.M * g.M);
+                splits = static_cast<int>(std::max<int64_t>(1, std::min(want, by_mem)));
+            }
+            if (splits > 1) {
+                P.k_per_split = (P.k_blocks + splits - 1) / splits;
+                P.splits = (P.k_blocks + P.k_per_split - 1) / P.k_per_split;  // no empty range
+                float* part = g.partials + part_used;
+                part_used += int64_t(P.splits) * g.batch * g.M * g.M;
+                rc = out_map(&P.ty, 4, part, g.M, g.M, int64_t(P.splits) * g.batch, g.M, g.M * g.M,
+                             true);
+            } else {
+                rc = out_map(&P.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
+                if (rc == CAM_OK)  // the mirror: the same matrix, boxes written transposed
+                    rc = out_map(&P.tyt, eb, g.Y, g.M, g.N, g.batch, g.ldy, g.sY, false);
+            }
+            units += P.n_tri * g.batch * P.splits;
+        } else {
+            P.has_y = g.Y != nullptr;
+            P.has_yt = g.Yt != nullptr;
+            if (P.has_y) rc = out_map(&P.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
+            if (rc == CAM_OK && P.has_yt)
+                rc = out_map(&P.tyt, eb, g.Yt, g.M, g.N, g.batch, g.ldyt, g.sYt, false);
+            if (rc == CAM_OK && epi == kEpiAxpbyC)  // C, read in boxes like the row-major output
+                rc = out_map(&P.tcm, eb, g.C, g.N, g.M, g.batch, g.ldc, g.sC, true);
+            units += P.m_blocks * P.n_blocks * g.batch;
+        }
+        if (rc != CAM_OK) return rc;
+    }
+    a.n_units = units;
+    const int grid = std::min(units, sm_count);
     const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, grid, s)
                                : launch_tc_any<false>(a, bn, epi, grid, s);
     ++*launches;
     if (e != cudaSuccess) return launch_fail(e);
-    if (epi == kEpiPart) {
+    // the split Gram products' partials, summed in range order
+    int64_t part_off = 0;
+    for (int i = 0; gram && i < n; ++i) {
+        const TcProblem& P = a.prob[i];
+        const NtGemm& g = gs[i];
+        if (P.splits <= 1) continue;
+        const float* part = g.partials + part_off;
+        part_off += int64_t(P.splits) * g.batch * g.M * g.M;
         const dim3 rgrid(static_cast<unsigned>(g.M / 32), static_cast<unsigned>(g.M / 32),
                          static_cast<unsigned>(g.batch));
         if (bf16)
             gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 8), 0, s>>>(
-                g.partials, a.splits, g.batch, g.M, g.alpha, g.diag,
-                static_cast<__nv_bfloat16*>(g.Y), g.ldy, g.sY);
+                part, P.splits, g.batch, g.M, g.alpha, g.diag, static_cast<__nv_bfloat16*>(g.Y),
+                g.ldy, g.sY);
         else
-            gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(g.partials, a.splits, g.batch, g.M,
-                                                             g.alpha, g.diag,
-                                                             static_cast<float*>(g.Y), g.ldy, g.sY);
+            gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(part, P.splits, g.batch, g.M, g.alpha,
+                                                             g.diag, static_cast<float*>(g.Y), g.ldy,
+                                                             g.sY);
         ++*launches;
         const cudaError_t r = cudaGetLastError();
         if (r != cudaSuccess) return launch_fail(r);

@@ -58,11 +58,21 @@ struct NtGemm {
     float* partials; int64_t partial_floats;
 };
 
-// Enqueues the product on `s`. `status` is the context's device status word:
-// a tensor-core kernel whose barrier wait runs out (a fault of this library,
-// never expected) sets CAM_STATUS_GEMM_TIMEOUT there and returns. Counts the
-// kernels launched in *launches.
-int nt_gemm(const NtGemm& g, int sm_count, int32_t* status, cudaStream_t s, int64_t* launches);
+// Enqueues n products (1 <= n <= 8) on `s` as one launch of the tensor-core
+// kernel: every problem of a launch has the same precision, epilogue, alpha,
+// beta and diag; their tiles are numbered one problem after another and the
+// persistent grid takes them in turn, so small products share the GPU
+// instead of each leaving most of it idle. Gram products whose tiles are long
+// split their K range (partials summed afterwards, one launch per such
+// problem). The launch is a programmatic dependent of the previous kernel on
+// the stream: its set-up overlaps that kernel's tail, and it reads and writes
+// global memory only once that kernel has completed. (CAM_ORTHO_FP32: one
+// CUDA-core launch per problem.) `status` is the context's device status
+// word: a tensor-core kernel whose barrier wait runs out (a fault of this
+// library, never expected) sets CAM_STATUS_GEMM_TIMEOUT there and returns.
+// Counts the kernels launched in *launches.
+int nt_gemm(const NtGemm* g, int n, int sm_count, int32_t* status, cudaStream_t s,
+            int64_t* launches);
 
 // Bytes of one stored element: bf16 for CAM_ORTHO_BF16, fp32 otherwise.
 inline int64_t nt_elem_bytes(int precision) { return precision == 2 /* CAM_ORTHO_BF16 */ ? 2 : 4; }

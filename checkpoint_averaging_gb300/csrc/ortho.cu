@@ -40,6 +40,7 @@ namespace {
 constexpr int kOrthoBatchMax = 256;  // matrices orthogonalised together
 constexpr int kOrthoBlocksMax = 4096;
 constexpr int64_t kSplitFloats = int64_t(1) << 25;  // Gram split-K partials (128 MB)
+constexpr int kOrthoPassChunks = 8;  // chunks iterated together (problems of one GEMM launch)
 
 int64_t pad128(int64_t v) { return (v + 127) / 128 * 128; }
 
@@ -311,13 +312,29 @@ NtGemm nt(int precision, int epi, int B, int64_t M, int64_t N, int64_t K, const 
     return g;
 }
 
+// One batch of equal-shape matrices inside a pass: its slots in the scalar
+// arrays and its offsets (in elements) in the workspace buffers.
+struct Chunk {
+    const OrthoMatrix* mats;
+    int count;
+    Shape sh;
+    int slot0;          // first slot: partials, scalars and inv_norm
+    int64_t off_x;      // Delta (floats)
+    int64_t off_pad;    // W and V (elements of the iterate's type)
+    int64_t off_gram;   // G (elements of the iterate's type)
+    int64_t padded() const { return sh.rp * sh.Lp; }
+    int64_t sq() const { return sh.rp * sh.rp; }
+};
+
+void* at(void* base, int64_t elems, int64_t eb) { return static_cast<char*>(base) + elems * eb; }
+
 // The short-side form of the iteration (CAM_ORTHO_SHORT_SIDE), for matrices
 // with L >= 4 r: with W_k = P_k W_0, a Newton-Schulz step becomes
 // P <- 1.5 P - 0.5 (P G0 P^T) P on r x r matrices, G0 = W_0 W_0^T; the polar
 // factor is then one product with W_0. G0 and the r x r steps run in fp32 on
 // the CUDA cores; the final product in p.precision. Per slot, Sq holds G0, P,
-// P^T, their next values, T = P G0 and M = T P^T. The factor ends in
-// W[1] (and V[1] = its transpose).
+// P^T, their next values, T = P G0 and M = T P^T. The chunk runs alone in its
+// pass (offsets 0); the factor ends in W[1] (and V[1] = its transpose).
 int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, int B, cudaStream_t s,
                          int sm_count, int64_t* launches) {
     const int64_t rp = sh.rp, Lp = sh.Lp, sq = rp * rp;
@@ -334,7 +351,7 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
     g.Y = G0;
     g.ldy = rp;
     g.sY = sq;
-    int rc = nt_gemm(g, sm_count, p.status, s, launches);
+    int rc = nt_gemm(&g, 1, sm_count, p.status, s, launches);
     if (rc != CAM_OK) return rc;
     const int64_t total = int64_t(B) * sq;
     const int blocks =
@@ -348,12 +365,12 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
         g.Y = T;
         g.ldy = rp;
         g.sY = sq;
-        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+        if ((rc = nt_gemm(&g, 1, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         g = nt(fp, kNtAxpby, B, rp, rp, rp, T, rp, sq, P, rp, sq);  // M = T P^T
         g.Y = M;
         g.ldy = rp;
         g.sY = sq;
-        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+        if ((rc = nt_gemm(&g, 1, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         // P'^T = 1.5 P^T - 0.5 P^T M (M symmetric), and P' beside it
         g = nt(fp, kNtAxpby, B, rp, rp, rp, Pt, rp, sq, M, rp, sq);
         g.alpha = -0.5f;
@@ -367,7 +384,7 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
         g.Yt = Pn;
         g.ldyt = rp;
         g.sYt = sq;
-        if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
+        if ((rc = nt_gemm(&g, 1, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         std::swap(P, Pn);
         std::swap(Pt, Ptn);
     }
@@ -379,7 +396,170 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
     g.Yt = w->V[1];
     g.ldyt = rp;
     g.sYt = Lp * rp;
-    return nt_gemm(g, sm_count, p.status, s, launches);
+    return nt_gemm(&g, 1, sm_count, p.status, s, launches);
+}
+
+// Delta, its norm and the normalised start (both orientations) of one chunk:
+// one launch of each kernel for its matrices.
+int prepare_chunk(OrthoWork* w, const Chunk& ch, const OrthoParams& p, cudaStream_t s,
+                  int sm_count, int64_t* launches, int* grid_out) {
+    const Shape& sh = ch.sh;
+    const int B = ch.count;
+    const int64_t numel = sh.m * sh.n;
+    const int64_t eb = nt_elem_bytes(p.precision);
+    // Blocks per matrix: about 8 per SM over the whole chunk, and no more than
+    // the matrix has 8-element steps for (small matrices in a big batch would
+    // otherwise leave most threads idle).
+    const int64_t steps = (numel + 8 * kOrthoThreads - 1) / (8 * kOrthoThreads);
+    const int64_t want = (int64_t(sm_count) * 8 + B - 1) / B;
+    const int grid = static_cast<int>(
+        std::min<int64_t>(kOrthoBlocksMax, std::max<int64_t>(1, std::min(want, steps))));
+    *grid_out = grid;
+    // a slot of Delta is 32-byte aligned when numel is a multiple of 8
+    const uintptr_t xa = p.dtype == kDtBF16 ? 16 : 32;
+    auto al = [](const void* q, uintptr_t b) { return reinterpret_cast<uintptr_t>(q) % b == 0; };
+    DeltaArgs da;
+    std::fill(da.vec, da.vec + kOrthoBatchMax / 32, 0u);
+    for (int j = 0; j < B; ++j) {
+        const OrthoMatrix& t = ch.mats[j];
+        bool v = numel % 8 == 0 && ch.off_x % 8 == 0 && al(t.theta, 32);
+        for (int k = 0; k < CAM_KMAX; ++k) {
+            da.x[j][k] = k < p.K ? t.x[k] : nullptr;
+            if (k < p.K) v = v && al(t.x[k], xa);
+        }
+        da.theta[j] = t.theta;
+        if (v) da.vec[j >> 5] |= 1u << (j & 31);
+    }
+    da.K = p.K;
+    da.Kf = static_cast<float>(p.K);
+    da.X = w->X + ch.off_x;
+    da.n = numel;
+    da.partials = w->partials + int64_t(ch.slot0) * kOrthoBlocksMax;
+    const dim3 bgrid(grid, B);
+    if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(da);
+    else ortho_delta<float><<<bgrid, kOrthoThreads, 0, s>>>(da);
+    ortho_norm<<<B, 32, 0, s>>>(da.partials, grid, w->scalars + ch.slot0, w->inv_norm + ch.slot0);
+    const dim3 pgrid(static_cast<unsigned>(sh.Lp / 32), static_cast<unsigned>(sh.rp / 32), B);
+    if (p.precision == CAM_ORTHO_BF16)
+        ortho_pack<__nv_bfloat16><<<pgrid, dim3(32, 8), 0, s>>>(
+            da.X, sh.m, sh.n, w->inv_norm + ch.slot0,
+            static_cast<__nv_bfloat16*>(at(w->W[0], ch.off_pad, eb)),
+            static_cast<__nv_bfloat16*>(at(w->V[0], ch.off_pad, eb)), sh.rp, sh.Lp);
+    else
+        ortho_pack<float><<<pgrid, dim3(32, 8), 0, s>>>(
+            da.X, sh.m, sh.n, w->inv_norm + ch.slot0, static_cast<float*>(at(w->W[0], ch.off_pad, eb)),
+            static_cast<float*>(at(w->V[0], ch.off_pad, eb)), sh.rp, sh.Lp);
+    *launches += 3;
+    return launch_error("launch");
+}
+
+// theta' = theta + s X and the EMA for one chunk, X read from V (tall) or W
+// (wide) of iterate buffer `cur`.
+int apply_chunk(OrthoWork* w, const Chunk& ch, const OrthoParams& p, int cur, int grid,
+                cudaStream_t s, int64_t* launches) {
+    const Shape& sh = ch.sh;
+    const int B = ch.count;
+    const int64_t eb = nt_elem_bytes(p.precision);
+    auto al = [](const void* q, uintptr_t b) { return reinterpret_cast<uintptr_t>(q) % b == 0; };
+    ApplyArgs aa;
+    std::fill(aa.vec, aa.vec + kOrthoBatchMax / 32, 0u);
+    for (int j = 0; j < B; ++j) {
+        const OrthoMatrix& t = ch.mats[j];
+        aa.theta[j] = t.theta;
+        aa.e[j] = p.ema ? t.e : nullptr;
+        if (sh.n % 8 == 0 && al(t.theta, 32) && (!p.ema || al(t.e, 32)))
+            aa.vec[j >> 5] |= 1u << (j & 31);
+    }
+    aa.O = at(sh.tall ? w->V[cur] : w->W[cur], ch.off_pad, eb);
+    aa.ld = sh.tall ? sh.rp : sh.Lp;
+    aa.so = ch.padded();
+    aa.n = sh.m * sh.n;
+    aa.cols = sh.n;
+    aa.scalars = w->scalars + ch.slot0;
+    aa.lr = p.lr;
+    aa.scale_mode = p.scale_mode;
+    aa.r = sh.r;
+    aa.beta = p.beta;
+    const dim3 bgrid(grid, B);
+    if (p.precision == CAM_ORTHO_BF16)
+        ortho_apply<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(aa);
+    else
+        ortho_apply<float><<<bgrid, kOrthoThreads, 0, s>>>(aa);
+    *launches += 1;
+    return launch_error("launch");
+}
+
+// One pass: chunks that share the workspace, iterated together: each
+// Newton-Schulz step is one Gram launch and one update launch over all of
+// them (nt_gemm's problems).
+int run_pass(OrthoWork* w, const std::vector<Chunk>& pass, const OrthoParams& p, cudaStream_t s,
+             int sm_count, int64_t* launches) {
+    std::vector<int> grids(pass.size());
+    for (size_t i = 0; i < pass.size(); ++i) {
+        const int rc = prepare_chunk(w, pass[i], p, s, sm_count, launches, &grids[i]);
+        if (rc != CAM_OK) return rc;
+    }
+    const int64_t eb = nt_elem_bytes(p.precision);
+    int cur = 0;
+    const bool short_side = pass.size() == 1 && p.short_side && pass[0].sh.L >= 4 * pass[0].sh.r;
+    if (short_side) {
+        const int rc = short_side_iteration(w, p, pass[0].sh, pass[0].count, s, sm_count, launches);
+        if (rc != CAM_OK) return rc;
+        cur = 1;
+    }
+    // bf16 and fp32: H = 1.5 I - 0.5 W W^T (upper triangle, mirrored), then
+    // V' = V H. TF32: G = W W^T, then V' = 1.5 V - 0.5 V G with V read in
+    // fp32 in the epilogue, so that only the correction passes through TF32
+    // inputs (V H would round the whole iterate to TF32 on every step).
+    const bool cform = p.precision == CAM_ORTHO_TF32;
+    NtGemm gram[kOrthoPassChunks], upd[kOrthoPassChunks];
+    const int n = static_cast<int>(pass.size());
+    for (int it = 0; !short_side && it < p.iterations; ++it) {
+        for (int i = 0; i < n; ++i) {
+            const Chunk& ch = pass[i];
+            const Shape& sh = ch.sh;
+            const int64_t padded = ch.padded(), sq = ch.sq();
+            void* Wc = at(w->W[cur], ch.off_pad, eb);
+            void* Vc = at(w->V[cur], ch.off_pad, eb);
+            void* G = at(w->G, ch.off_gram, eb);
+            NtGemm& g = gram[i];
+            g = nt(p.precision, kNtGram, ch.count, sh.rp, sh.rp, sh.Lp, Wc, sh.Lp, padded, Wc,
+                   sh.Lp, padded);
+            g.alpha = cform ? 1.0f : -0.5f;
+            g.diag = cform ? 0.0f : 1.5f;
+            g.Y = G;
+            g.ldy = sh.rp;
+            g.sY = sq;
+            g.partials = w->split;
+            g.partial_floats = kSplitFloats;
+            // V' = V H (or 1.5 V - 0.5 V G), W' = V'^T
+            NtGemm& u = upd[i];
+            u = nt(p.precision, kNtAxpby, ch.count, sh.Lp, sh.rp, sh.rp, Vc, sh.rp, padded, G, sh.rp,
+                   sq);
+            if (cform) {
+                u.alpha = -0.5f;
+                u.beta = 1.5f;
+                u.C = Vc;
+                u.ldc = sh.rp;
+                u.sC = padded;
+            }
+            u.Y = at(w->V[1 - cur], ch.off_pad, eb);
+            u.ldy = sh.rp;
+            u.sY = padded;
+            u.Yt = at(w->W[1 - cur], ch.off_pad, eb);
+            u.ldyt = sh.Lp;
+            u.sYt = padded;
+        }
+        int rc = nt_gemm(gram, n, sm_count, p.status, s, launches);
+        if (rc == CAM_OK) rc = nt_gemm(upd, n, sm_count, p.status, s, launches);
+        if (rc != CAM_OK) return rc;
+        cur ^= 1;
+    }
+    for (size_t i = 0; i < pass.size(); ++i) {
+        const int rc = apply_chunk(w, pass[i], p, cur, grids[i], s, launches);
+        if (rc != CAM_OK) return rc;
+    }
+    return CAM_OK;
 }
 
 }  // namespace
@@ -431,135 +611,63 @@ void ortho_destroy(OrthoWork* w) {
     delete w;
 }
 
-int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoParams& p,
-                cudaStream_t s, int sm_count, int64_t* launches) {
-    if (count <= 0) return CAM_OK;
-    Shape sh;
-    sh.m = mats[0].rows;
-    sh.n = mats[0].cols;
-    sh.tall = sh.m >= sh.n;
-    sh.r = std::min(sh.m, sh.n);
-    sh.L = std::max(sh.m, sh.n);
-    sh.rp = pad128(sh.r);
-    sh.Lp = pad128(sh.L);
-    const int64_t numel = sh.m * sh.n, padded = sh.rp * sh.Lp, sq = sh.rp * sh.rp;
-    const bool short_side = p.short_side && sh.L >= 4 * sh.r;
-    int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_pad / padded, w->cap_gram / sq));
-    if (short_side) per = std::min<int64_t>(per, w->cap_sq / (7 * sq));
-    per = std::max<int64_t>(per, 1);
-    const bool bf = p.precision == CAM_ORTHO_BF16;
-    for (int first = 0; first < count; first += static_cast<int>(per)) {
-        const int B = static_cast<int>(std::min<int64_t>(per, count - first));
-        // Blocks per matrix: about 8 per SM over the whole batch, and no more
-        // than the matrix has 8-element steps for (small matrices in a big
-        // batch would otherwise leave most threads idle).
-        const int64_t steps = (numel + 8 * kOrthoThreads - 1) / (8 * kOrthoThreads);
-        const int64_t want = (int64_t(sm_count) * 8 + B - 1) / B;
-        const int grid = static_cast<int>(
-            std::min<int64_t>(kOrthoBlocksMax, std::max<int64_t>(1, std::min(want, steps))));
-        // Delta of each matrix into its slot, its norm, and the normalised
-        // start in both orientations: one launch of each kernel for the batch.
-        // a slot of the workspace is 32-byte aligned when numel is a multiple of 8
-        const uintptr_t xa = p.dtype == kDtBF16 ? 16 : 32;
-        auto al = [](const void* q, uintptr_t b) { return reinterpret_cast<uintptr_t>(q) % b == 0; };
-        DeltaArgs da;
-        ApplyArgs aa;
-        std::fill(da.vec, da.vec + kOrthoBatchMax / 32, 0u);
-        std::fill(aa.vec, aa.vec + kOrthoBatchMax / 32, 0u);
-        for (int j = 0; j < B; ++j) {
-            const OrthoMatrix& t = mats[first + j];
-            bool v = numel % 8 == 0 && al(t.theta, 32);
-            for (int k = 0; k < CAM_KMAX; ++k) {
-                da.x[j][k] = k < p.K ? t.x[k] : nullptr;
-                if (k < p.K) v = v && al(t.x[k], xa);
-            }
-            da.theta[j] = t.theta;
-            if (v) da.vec[j >> 5] |= 1u << (j & 31);
-            aa.theta[j] = t.theta;
-            aa.e[j] = p.ema ? t.e : nullptr;
-            if (sh.n % 8 == 0 && al(t.theta, 32) && (!p.ema || al(t.e, 32)))
-                aa.vec[j >> 5] |= 1u << (j & 31);
+int ortho_round(OrthoWork* w, const std::vector<std::vector<OrthoMatrix>>& groups,
+                const OrthoParams& p, cudaStream_t s, int sm_count, int64_t* launches) {
+    // Chunks: each shape group cut into batches the workspace holds.
+    std::vector<Chunk> chunks;
+    for (const auto& grp : groups) {
+        if (grp.empty()) continue;
+        Shape sh;
+        sh.m = grp[0].rows;
+        sh.n = grp[0].cols;
+        sh.tall = sh.m >= sh.n;
+        sh.r = std::min(sh.m, sh.n);
+        sh.L = std::max(sh.m, sh.n);
+        sh.rp = pad128(sh.r);
+        sh.Lp = pad128(sh.L);
+        const int64_t padded = sh.rp * sh.Lp, sq = sh.rp * sh.rp;
+        const bool short_side = p.short_side && sh.L >= 4 * sh.r;
+        int64_t per = std::min<int64_t>(kOrthoBatchMax, std::min(w->cap_pad / padded, w->cap_gram / sq));
+        if (short_side) per = std::min<int64_t>(per, w->cap_sq / (7 * sq));
+        per = std::max<int64_t>(per, 1);
+        for (size_t first = 0; first < grp.size(); first += per) {
+            Chunk ch{};
+            ch.mats = grp.data() + first;
+            ch.count = static_cast<int>(std::min<int64_t>(per, int64_t(grp.size() - first)));
+            ch.sh = sh;
+            chunks.push_back(ch);
         }
-        da.K = p.K;
-        da.Kf = static_cast<float>(p.K);
-        da.X = w->X;
-        da.n = numel;
-        da.partials = w->partials;
-        const dim3 bgrid(grid, B);
-        if (p.dtype == kDtBF16) ortho_delta<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(da);
-        else ortho_delta<float><<<bgrid, kOrthoThreads, 0, s>>>(da);
-        ortho_norm<<<B, 32, 0, s>>>(w->partials, grid, w->scalars, w->inv_norm);
-        const dim3 pgrid(static_cast<unsigned>(sh.Lp / 32), static_cast<unsigned>(sh.rp / 32), B);
-        if (bf)
-            ortho_pack<__nv_bfloat16><<<pgrid, dim3(32, 8), 0, s>>>(
-                w->X, sh.m, sh.n, w->inv_norm, static_cast<__nv_bfloat16*>(w->W[0]),
-                static_cast<__nv_bfloat16*>(w->V[0]), sh.rp, sh.Lp);
-        else
-            ortho_pack<float><<<pgrid, dim3(32, 8), 0, s>>>(w->X, sh.m, sh.n, w->inv_norm,
-                                                           static_cast<float*>(w->W[0]),
-                                                           static_cast<float*>(w->V[0]), sh.rp, sh.Lp);
-        *launches += 3;
-        int rc = launch_error("launch");
+    }
+    // Passes: consecutive chunks of one tile width that fit the workspace
+    // together; a short-side chunk runs alone.
+    size_t i = 0;
+    while (i < chunks.size()) {
+        std::vector<Chunk> pass;
+        int64_t pad = 0, gram = 0;
+        int slots = 0;
+        const bool wide256 = chunks[i].sh.rp % 256 == 0;
+        while (i < chunks.size()) {
+            Chunk ch = chunks[i];
+            const bool ss = p.short_side && ch.sh.L >= 4 * ch.sh.r;
+            const int64_t need_pad = ch.padded() * ch.count, need_gram = ch.sq() * ch.count;
+            const bool fits = pad + need_pad <= w->cap_pad && gram + need_gram <= w->cap_gram &&
+                              slots + ch.count <= kOrthoBatchMax &&
+                              int(pass.size()) < kOrthoPassChunks &&
+                              (ch.sh.rp % 256 == 0) == wide256;
+            if (!pass.empty() && (ss || !fits)) break;
+            ch.slot0 = slots;
+            ch.off_x = pad;  // Delta holds m n <= padded floats per matrix
+            ch.off_pad = pad;
+            ch.off_gram = gram;
+            pass.push_back(ch);
+            pad += need_pad;
+            gram += need_gram;
+            slots += ch.count;
+            ++i;
+            if (ss) break;
+        }
+        const int rc = run_pass(w, pass, p, s, sm_count, launches);
         if (rc != CAM_OK) return rc;
-        int cur = 0;
-        if (short_side) {
-            rc = short_side_iteration(w, p, sh, B, s, sm_count, launches);
-            if (rc != CAM_OK) return rc;
-            cur = 1;
-        }
-        for (int it = 0; !short_side && it < p.iterations; ++it) {
-            // bf16 and fp32: H = 1.5 I - 0.5 W W^T (upper triangle, mirrored),
-            // then V' = V H. TF32: G = W W^T, then V' = 1.5 V - 0.5 V G with V
-            // read in fp32 in the epilogue, so that only the correction passes
-            // through TF32 inputs (V H would round the whole iterate to TF32
-            // on every step).
-            const bool cform = p.precision == CAM_ORTHO_TF32;
-            NtGemm g = nt(p.precision, kNtGram, B, sh.rp, sh.rp, sh.Lp, w->W[cur], sh.Lp, padded,
-                          w->W[cur], sh.Lp, padded);
-            g.alpha = cform ? 1.0f : -0.5f;
-            g.diag = cform ? 0.0f : 1.5f;
-            g.Y = w->G;
-            g.ldy = sh.rp;
-            g.sY = sq;
-            g.partials = w->split;
-            g.partial_floats = kSplitFloats;
-            if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
-            // V' = V H (or 1.5 V - 0.5 V G), W' = V'^T
-            g = nt(p.precision, kNtAxpby, B, sh.Lp, sh.rp, sh.rp, w->V[cur], sh.rp, padded, w->G,
-                   sh.rp, sq);
-            if (cform) {
-                g.alpha = -0.5f;
-                g.beta = 1.5f;
-                g.C = w->V[cur];
-                g.ldc = sh.rp;
-                g.sC = padded;
-            }
-            g.Y = w->V[1 - cur];
-            g.ldy = sh.rp;
-            g.sY = padded;
-            g.Yt = w->W[1 - cur];
-            g.ldyt = sh.Lp;
-            g.sYt = padded;
-            if ((rc = nt_gemm(g, sm_count, p.status, s, launches)) != CAM_OK) return rc;
-            cur ^= 1;
-        }
-        // the factor in the matrices' own orientation: V (tall) or W (wide)
-        aa.O = sh.tall ? w->V[cur] : w->W[cur];
-        aa.ld = sh.tall ? sh.rp : sh.Lp;
-        aa.so = padded;
-        aa.n = numel;
-        aa.cols = sh.n;
-        aa.scalars = w->scalars;
-        aa.lr = p.lr;
-        aa.scale_mode = p.scale_mode;
-        aa.r = sh.r;
-        aa.beta = p.beta;
-        if (bf)
-            ortho_apply<uint16_t><<<bgrid, kOrthoThreads, 0, s>>>(aa);
-        else
-            ortho_apply<float><<<bgrid, kOrthoThreads, 0, s>>>(aa);
-        *launches += 1;
-        if ((rc = launch_error("launch")) != CAM_OK) return rc;
     }
     return CAM_OK;
 }

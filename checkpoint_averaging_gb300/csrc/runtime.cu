@@ -1140,11 +1140,11 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         // the workspace is the context's: after its last use on any stream
         if (ce == cudaSuccess && !cap) ce = cudaStreamWaitEvent(s, c->ortho_ev, 0);
         std::vector<char> done(T, 0);
-        std::vector<cam::OrthoMatrix> group;
+        std::vector<std::vector<cam::OrthoMatrix>> groups;
         for (int l = 0; l < T && ce == cudaSuccess; ++l) {
             const int32_t g0 = p.tensors[l];
             if (done[l] || !c->is_matrix(g0)) continue;
-            group.clear();
+            groups.emplace_back();
             for (int q = l; q < T; ++q) {
                 const int32_t g = p.tensors[q];
                 if (done[q] || !c->is_matrix(g) || c->rows[g] != c->rows[g0] ||
@@ -1157,10 +1157,11 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                 om.rows = c->rows[g];
                 om.cols = c->numel[g] / c->rows[g];
                 for (int k = 0; k < CAM_KMAX; ++k) om.x[k] = k < K ? r->x[size_t(k) * T + q] : nullptr;
-                group.push_back(om);
+                groups.back().push_back(om);
             }
-            const int rc = cam::ortho_group(c->ortho, group.data(), static_cast<int>(group.size()), op,
-                                            s, c->sm_count, &c->launches);
+        }
+        if (ce == cudaSuccess) {
+            const int rc = cam::ortho_round(c->ortho, groups, op, s, c->sm_count, &c->launches);
             if (rc != CAM_OK) {
                 close_round(r);
                 return rc;

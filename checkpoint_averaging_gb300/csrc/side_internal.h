@@ -4,6 +4,8 @@
 // from, so that these paths change without touching it.
 #pragma once
 
+#include <vector>
+
 #include "cam_internal.h"
 
 namespace cam {
@@ -87,9 +89,11 @@ struct OrthoParams {
 // them); big_gram: the largest padded r x r (the short-side form's squares).
 int ortho_create(OrthoWork** out, int64_t cap_pad, int64_t cap_gram, int64_t big_gram);
 void ortho_destroy(OrthoWork* w);
-// Orthogonalises `count` matrices of one shape, batching them into strided
-// GEMMs as far as the workspace allows.
-int ortho_group(OrthoWork* w, const OrthoMatrix* mats, int count, const OrthoParams& p,
-                cudaStream_t s, int sm_count, int64_t* launches);
+// Orthogonalises a round's matrices, given as groups of equal shape: each
+// group in batches the workspace holds, and batches of one tile width that
+// fit the workspace together iterated in step (one Gram and one update GEMM
+// launch per Newton-Schulz step for all of them).
+int ortho_round(OrthoWork* w, const std::vector<std::vector<OrthoMatrix>>& groups,
+                const OrthoParams& p, cudaStream_t s, int sm_count, int64_t* launches);
 
 }  // namespace cam
