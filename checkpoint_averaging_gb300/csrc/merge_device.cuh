@@ -77,6 +77,44 @@ __device__ __forceinline__ void load_s8(const float* p, float (&v)[8]) {
         : "l"(p));
 }
 
+// N = 2 or 4 consecutive floats: state (read once, written back by the same
+// thread) and fp32 worker elements, for the narrow steps below.
+template <int N>
+__device__ __forceinline__ void load_sn(const float* p, float (&v)[N]) {
+    if constexpr (N == 4)
+        asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.L1::no_allocate.v2.f32 {%0,%1}, [%2];"
+                     : "=f"(v[0]), "=f"(v[1])
+                     : "l"(p));
+}
+
+template <int N>
+__device__ __forceinline__ void store_sn(float* p, const float (&v)[N]) {
+    if constexpr (N == 4)
+        asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v[0]),
+                     "f"(v[1]), "f"(v[2]), "f"(v[3])
+                     : "memory");
+    else
+        asm volatile("st.global.L1::no_allocate.v2.f32 [%0], {%1,%2};" ::"l"(p), "f"(v[0]),
+                     "f"(v[1])
+                     : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void load_xn(const float* p, float (&v)[N]) {
+    if constexpr (N == 4)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0,%1}, [%2];"
+                     : "=f"(v[0]), "=f"(v[1])
+                     : "l"(p));
+}
+
 __device__ __forceinline__ void store_s8(float* p, const float (&v)[8]) {
     asm volatile(
         "st.global.L1::no_allocate.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
@@ -160,11 +198,56 @@ __device__ __forceinline__ void worker_drift(const A& a, const float (&xk)[CAM_K
 // copy of the new theta and xs[K+1] (when not null) a copy of the new EMA.
 // With SWA the uniform running average ts.swa is updated from the new theta.
 // With WD, accw[0..K) collect each worker's squared drift.
+// N (2 or 4) consecutive elements from fp32 workers with narrower accesses:
+// the register-heavy variants (a running average with norms, per-worker
+// drift or published copies) take an 8-element step as 8 / N of these, which
+// keeps them from spilling. Same operations in the same order per element
+// as merge_vec8.
+template <int N, int MODE, bool EMA, bool NORM, bool PUB, bool SWA, bool WD, class A>
+__device__ __forceinline__ void merge_vecn_f32(const A& a, const void* const* xs,
+                                               const TensorSlot& ts, int64_t i, float& acc,
+                                               float* accw) {
+    float x[CAM_KMAX][N];
+#pragma unroll
+    for (int k = 0; k < CAM_KMAX; ++k)
+        if (k < a.K) load_xn<N>(static_cast<const float*>(xs[k]) + i, x[k]);
+    float th[N], m[N], e[N], sw[N];
+    if (MODE == kDelta || NORM || WD) load_sn<N>(ts.theta + i, th);
+    if (MODE == kDelta) load_sn<N>(ts.m + i, m);
+    if (EMA) load_sn<N>(ts.e + i, e);
+    if constexpr (SWA) load_sn<N>(ts.swa + i, sw);
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        float xk[CAM_KMAX];
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k][j];
+        if constexpr (WD) worker_drift(a, xk, th[j], accw);
+        merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
+        if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
+    }
+    store_sn<N>(ts.theta + i, th);
+    if constexpr (SWA) store_sn<N>(ts.swa + i, sw);
+    if (MODE == kDelta) store_sn<N>(ts.m + i, m);
+    if (EMA) store_sn<N>(ts.e + i, e);
+    if (PUB) {
+        store_sn<N>(static_cast<float*>(const_cast<void*>(xs[a.K])) + i, th);
+        if (EMA && xs[a.K + 1]) store_sn<N>(static_cast<float*>(const_cast<void*>(xs[a.K + 1])) + i, e);
+    }
+}
+
 template <typename XT, int MODE, bool EMA, bool NORM, bool PUB = false, bool SWA = false,
           bool WD = false, class A>
 __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
                                            const TensorSlot& ts, int64_t i, float& acc,
                                            float* accw = nullptr) {
+    if constexpr (sizeof(XT) == 4 && SWA && (NORM || WD)) {
+        // published copies or per-worker drift on top: 2 elements a step
+        constexpr int N = (PUB || (WD && MODE == kMean && !EMA)) ? 2 : 4;
+#pragma unroll
+        for (int h = 0; h < 8; h += N)
+            merge_vecn_f32<N, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i + h, acc, accw);
+        return;
+    }
     XVec<XT> x[CAM_KMAX];
 #pragma unroll
     for (int k = 0; k < CAM_KMAX; ++k)
