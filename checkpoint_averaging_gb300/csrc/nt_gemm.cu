@@ -145,13 +145,23 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
            (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// MN-major operand (M or N contiguous in memory, as TMA writes boxes of 128
+// bytes of M (or N) by K rows under the 128-byte swizzle): 8-row groups along
+// K 1,024 bytes apart (stride byte offset), and the next 128 bytes of M (or
+// N) `lbo` bytes further (leading byte offset: one TMA box).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t addr, uint32_t lbo) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (uint64_t(lbo >> 4) << 16) |
+           (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
 // Instruction descriptor of kind::f16 (bf16 A and B) or kind::tf32: fp32
 // accumulator (bits 4-5 = 1), A/B formats (bits 7-9, 10-12: bf16 = 1,
-// tf32 = 2), both K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4
-// (bits 24-28).
-template <bool BF16, int BN>
+// tf32 = 2), K-major (bits 15, 16 = 0) or MN-major (1) operands, N >> 3
+// (bits 17-22), M >> 4 (bits 24-28).
+template <bool BF16, int BN, bool MNM>
 __device__ __forceinline__ constexpr uint32_t instr_desc() {
     return (1u << 4) | ((BF16 ? 1u : 2u) << 7) | ((BF16 ? 1u : 2u) << 10) |
+           (uint32_t(MNM ? 1 : 0) << 15) | (uint32_t(MNM ? 1 : 0) << 16) |
            (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
 }
 
@@ -410,9 +420,13 @@ struct Geo {
     static_assert(kSmem <= 232448, "over the per-block shared memory limit");
 };
 
-template <bool BF16, int BN, int EPI>
+template <bool BF16, int BN, int EPI, bool MNM>
 __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constant__ TcArgs a) {
     using G = Geo<BF16, BN, EPI>;
+    // MN-major operands: TMA boxes of 128 bytes of M (or N) by one K step of
+    // rows; kMnBox bytes each, kMnCols elements of M (or N)
+    constexpr int kMnCols = kRowBytes / (BF16 ? 2 : 4);
+    constexpr int kMnBox = G::kKStep * kRowBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -476,10 +490,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                 const uint32_t fb = full0 + 8 * stage;
                 bar_expect(fb, G::kStage);
                 const int x = kb * G::kKStep;
-                tma_load(sa, &P.ta, x, arow, t.b, fb);
+                if constexpr (MNM) {  // boxes of kMnCols M (N) by one K step
 #pragma unroll
-                for (int h = 0; h < BN / kBM; ++h)
-                    tma_load(sa + kBoxBytes + h * kBoxBytes, &P.tb, x, brow + h * kBM, t.b, fb);
+                    for (int h = 0; h < kBM / kMnCols; ++h)
+                        tma_load(sa + h * kMnBox, &P.ta, arow + h * kMnCols, x, t.b, fb);
+#pragma unroll
+                    for (int h = 0; h < BN / kMnCols; ++h)
+                        tma_load(sa + kBoxBytes + h * kMnBox, &P.tb, brow + h * kMnCols, x, t.b, fb);
+                } else {
+                    tma_load(sa, &P.ta, x, arow, t.b, fb);
+#pragma unroll
+                    for (int h = 0; h < BN / kBM; ++h)
+                        tma_load(sa + kBoxBytes + h * kBoxBytes, &P.tb, x, brow + h * kBM, t.b, fb);
+                }
                 issued |= 1u << stage;
                 filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == G::kStages) {
@@ -498,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
-        constexpr uint32_t idesc = instr_desc<BF16, BN>();
+        constexpr uint32_t idesc = instr_desc<BF16, BN, MNM>();
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -516,10 +539,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                 }
                 tc_fence_after();
                 const uint32_t sa = su32(smem + stage * G::kStage);
-                const uint64_t da = smem_desc(sa), db = smem_desc(sa + kBoxBytes);
+                // four MMAs of 32 bytes of K each: 32 bytes further along a
+                // K-major row, or 32 bytes / element rows further down an
+                // MN-major box
+                constexpr uint32_t kAdv = MNM ? (32 / (BF16 ? 2 : 4)) * kRowBytes / 16 : 2;
+                const uint64_t da = MNM ? smem_desc_mn(sa, kMnBox) : smem_desc(sa);
+                const uint64_t db = MNM ? smem_desc_mn(sa + kBoxBytes, kMnBox) : smem_desc(sa + kBoxBytes);
 #pragma unroll
-                for (int k = 0; k < kRowBytes / 32; ++k)  // 32 bytes of K per MMA
-                    mma<BF16>(d, da + uint64_t(2 * k), db + uint64_t(2 * k), idesc,
+                for (int k = 0; k < kRowBytes / 32; ++k)
+                    mma<BF16>(d, da + uint64_t(kAdv * k), db + uint64_t(kAdv * k), idesc,
                               (kb > t.k0 || k > 0) ? 1u : 0u);
                 mma_commit(empty0 + 8 * stage);
                 if (++stage == G::kStages) {
@@ -672,37 +700,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
 
 // Sums the split partials of Gram products in range order and writes
 // Y = alpha sum + diag I, the whole symmetric matrix: element (i, j) takes the
-// partials of (min, max), so both triangles carry the same bits. 32 x 32 tiles
-// through shared memory, on and above the diagonal; each writes itself and
-// its mirror.
+// partials of (min, max), so both triangles carry the same bits. One block of
+// 32 x 32 threads per 32 x 32 tile on or above the diagonal (blockIdx.x walks
+// those tiles row by row), one element per thread with its loads for several
+// ranges in flight; the tile is written, and mirrored, through shared memory.
 template <typename T>
-__global__ void gram_reduce(const float* P, int splits, int batch, int64_t M, float alpha, float diag,
-                            T* Y, int64_t ldy, int64_t sY) {
+__global__ void __launch_bounds__(1024) gram_reduce(const float* P, int splits, int batch,
+                                                    int64_t M, float alpha, float diag, T* Y,
+                                                    int64_t ldy, int64_t sY) {
     __shared__ float tile[32][33];
-    const int b = blockIdx.z;
-    const int64_t ti = blockIdx.y, tj = blockIdx.x;
-    if (tj < ti) return;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    const int64_t split_stride = int64_t(batch) * M * M;
-    for (int r = ty; r < 32; r += 8) {
-        const int64_t i = ti * 32 + r, j = tj * 32 + tx;
-        // diagonal tile: the upper element of the pair
-        const float* p = P + int64_t(b) * M * M + (j >= i ? i * M + j : j * M + i);
-        float s = 0.0f;
-#pragma unroll 8
-        for (int q = 0; q < splits; ++q) s += p[q * split_stride];  // range order
-        tile[r][tx] = alpha * s + (i == j ? diag : 0.0f);
+    const int b = blockIdx.y;
+    // tile index -> (ti, tj), tj >= ti, over a (M/32) x (M/32) grid
+    const int64_t nt = M / 32;
+    int64_t q = blockIdx.x, ti = 0;
+    while (q >= nt - ti) {
+        q -= nt - ti;
+        ++ti;
     }
+    const int64_t tj = ti + q;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 32
+    const int64_t i = ti * 32 + ty, j = tj * 32 + tx;
+    const int64_t split_stride = int64_t(batch) * M * M;
+    // diagonal tile: the upper element of the pair
+    const float* p = P + int64_t(b) * M * M + (j >= i ? i * M + j : j * M + i);
+    float acc = 0.0f;
+#pragma unroll 8
+    for (int r = 0; r < splits; ++r) acc += p[r * split_stride];  // range order
+    tile[ty][tx] = alpha * acc + (i == j ? diag : 0.0f);
     __syncthreads();
     T* y = Y + b * sY;
-    for (int r = ty; r < 32; r += 8) {
-        const int64_t i = ti * 32 + r, j = tj * 32 + tx;
-        y[i * ldy + j] = T(tile[r][tx]);
-        if (tj > ti) {  // the mirror (j, i): row tj*32 + r, column ti*32 + tx
-            const int64_t mi = tj * 32 + r, mj = ti * 32 + tx;
-            y[mi * ldy + mj] = T(tile[tx][r]);
-        }
-    }
+    y[i * ldy + j] = T(tile[ty][tx]);
+    if (tj > ti) y[(tj * 32 + ty) * ldy + ti * 32 + tx] = T(tile[tx][ty]);  // the mirror (j, i)
 }
 
 // ---- the CUDA-core fp32 kernel -------------------------------------------------------
@@ -857,11 +885,11 @@ int out_map(CUtensorMap* map, int64_t eb, const void* base, int64_t cols, int64_
 
 // Launched as a programmatic dependent of the previous kernel on the stream
 // (the kernel waits in griddepcontrol.wait before touching global memory).
-template <bool BF16, int BN, int EPI>
+template <bool BF16, int BN, int EPI, bool MNM = false>
 cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
     using G = Geo<BF16, BN, EPI>;
     static cudaError_t attr = cudaFuncSetAttribute(
-        nt_gemm_tc<BF16, BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+        nt_gemm_tc<BF16, BN, EPI, MNM>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -874,22 +902,24 @@ cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, nt_gemm_tc<BF16, BN, EPI>, a);
+    return cudaLaunchKernelEx(&cfg, nt_gemm_tc<BF16, BN, EPI, MNM>, a);
 }
 
 template <bool BF16, int BN>
-cudaError_t launch_tc_epi(const TcArgs& a, int epi, int grid, cudaStream_t s) {
+cudaError_t launch_tc_epi(const TcArgs& a, int epi, bool mn, int grid, cudaStream_t s) {
     switch (epi) {
         case kNtAxpby: return launch_tc<BF16, BN, kNtAxpby>(a, grid, s);
-        case kNtGram: return launch_tc<BF16, BN, kNtGram>(a, grid, s);
+        case kNtGram:
+            return mn ? launch_tc<BF16, BN, kNtGram, true>(a, grid, s)
+                      : launch_tc<BF16, BN, kNtGram>(a, grid, s);
         default: return launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
     }
 }
 
 template <bool BF16>
-cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, int grid, cudaStream_t s) {
-    return bn == 256 ? launch_tc_epi<BF16, 256>(a, epi, grid, s)
-                     : launch_tc_epi<BF16, 128>(a, epi, grid, s);
+cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, bool mn, int grid, cudaStream_t s) {
+    return bn == 256 ? launch_tc_epi<BF16, 256>(a, epi, mn, grid, s)
+                     : launch_tc_epi<BF16, 128>(a, epi, mn, grid, s);
 }
 
 int launch_fail(cudaError_t e) {
@@ -945,6 +975,10 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
             return record_error(CAM_E_ARG, "orthogonalisation: problems of one launch must agree");
         if (g.epilogue == kNtGram && (g.M != g.N || g.A != g.B))
             return record_error(CAM_E_ARG, "orthogonalisation: a Gram product takes one operand");
+        if (g.mn_major != g0.mn_major ||
+            (g.mn_major && (g.epilogue != kNtGram || g.precision != CAM_ORTHO_BF16)))
+            return record_error(CAM_E_ARG,
+                                "orthogonalisation: MN-major operands serve bf16 Gram products");
         all256 = all256 && g.N % 256 == 0;
     }
     if (g0.precision == CAM_ORTHO_FP32) {
@@ -959,6 +993,7 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     const int bn = all256 ? 256 : 128;
     const int64_t kstep = kRowBytes / eb;
     const bool gram = g0.epilogue == kNtGram;
+    const bool mn = g0.mn_major;
     const int epi = gram ? kNtGram : (g0.beta != 0.0f ? kEpiAxpbyC : kNtAxpby);
     TcArgs a;
     std::memset(&a, 0, sizeof a);
@@ -968,9 +1003,9 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     a.diag = g0.diag;
     a.status = status;
     // Gram products: tiles reaching the upper triangle, and a K split for
-    // products whose tiles are long, so that no unit is much longer than a
-    // third of one block's share of the launch (ranges of at least 16 K
-    // steps, within the partial buffer).
+    // products whose tiles are long, so that no unit is longer than one
+    // block's share of the launch (ranges of at least 16 K steps, within the
+    // partial buffer; each range costs a pass over the matrix in partials).
     int64_t work = 0;
     for (int i = 0; i < n; ++i) {
         TcProblem& P = a.prob[i];
@@ -991,14 +1026,25 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
             work += int64_t(P.m_blocks) * P.n_blocks * g.batch * P.k_blocks;
         }
     }
-    const int64_t longest = std::max<int64_t>(16, work / (3 * int64_t(sm_count)));
+    const int64_t longest = std::max<int64_t>(16, work / int64_t(sm_count));
     int64_t part_used = 0;
     int32_t units = 0;
     for (int i = 0; i < n; ++i) {
         TcProblem& P = a.prob[i];
         const NtGemm& g = gs[i];
-        int rc = operand_map(&P.ta, eb, g.A, g.K, g.M, g.batch, g.lda, g.sA);
-        if (rc == CAM_OK) rc = operand_map(&P.tb, eb, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
+        int rc;
+        if (mn) {  // A stored K x M, B stored K x N: boxes of 128 bytes of M (N) by one K step
+            rc = make_map(&P.ta, eb, g.A, g.M, g.K, g.batch, g.lda, g.sA,
+                          static_cast<int>(kRowBytes / eb), static_cast<int>(kstep),
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+            if (rc == CAM_OK)
+                rc = make_map(&P.tb, eb, g.B, g.N, g.K, g.batch, g.ldb, g.sB,
+                              static_cast<int>(kRowBytes / eb), static_cast<int>(kstep),
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            rc = operand_map(&P.ta, eb, g.A, g.K, g.M, g.batch, g.lda, g.sA);
+            if (rc == CAM_OK) rc = operand_map(&P.tb, eb, g.B, g.K, g.N, g.batch, g.ldb, g.sB);
+        }
         if (rc != CAM_OK) return rc;
         P.unit0 = units;
         if (gram) {
@@ -1035,8 +1081,8 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     }
     a.n_units = units;
     const int grid = std::min(units, sm_count);
-    const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, grid, s)
-                               : launch_tc_any<false>(a, bn, epi, grid, s);
+    const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, mn, grid, s)
+                               : launch_tc_any<false>(a, bn, epi, mn, grid, s);
     ++*launches;
     if (e != cudaSuccess) return launch_fail(e);
     // the split Gram products' partials, summed in range order
@@ -1047,14 +1093,14 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
         if (P.splits <= 1) continue;
         const float* part = g.partials + part_off;
         part_off += int64_t(P.splits) * g.batch * g.M * g.M;
-        const dim3 rgrid(static_cast<unsigned>(g.M / 32), static_cast<unsigned>(g.M / 32),
-                         static_cast<unsigned>(g.batch));
+        const int64_t nt = g.M / 32;  // tiles on or above the diagonal, per matrix
+        const dim3 rgrid(static_cast<unsigned>(nt * (nt + 1) / 2), static_cast<unsigned>(g.batch));
         if (bf16)
-            gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 8), 0, s>>>(
+            gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 32), 0, s>>>(
                 part, P.splits, g.batch, g.M, g.alpha, g.diag, static_cast<__nv_bfloat16*>(g.Y),
                 g.ldy, g.sY);
         else
-            gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(part, P.splits, g.batch, g.M, g.alpha,
+            gram_reduce<float><<<rgrid, dim3(32, 32), 0, s>>>(part, P.splits, g.batch, g.M, g.alpha,
                                                              g.diag, static_cast<float*>(g.Y), g.ldy,
                                                              g.sY);
         ++*launches;

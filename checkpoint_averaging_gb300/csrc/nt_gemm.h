@@ -48,6 +48,10 @@ struct NtGemm {
     int64_t M, N, K;        // multiples of 128
     const void* A; int64_t lda, sA;   // row stride and batch stride, in elements
     const void* B; int64_t ldb, sB;
+    // A stored transposed (K x M, row stride lda) and B likewise (K x N):
+    // "MN-major" operands, for the Gram product V^T V of a tall iterate V
+    // without its transpose (bf16 Gram products only)
+    bool mn_major;
     float alpha, beta, diag;
     const void* C; int64_t ldc, sC;   // CAM_ORTHO_FP32 only: read when beta != 0
     void* Y; int64_t ldy, sY;

@@ -13,11 +13,12 @@
 //   3. `iterations` Newton-Schulz steps W <- 1.5 W - 0.5 (W W^T) W, which
 //      drive every singular value to 1 and so converge to the polar factor
 //      U V^T. Each step is two NT GEMMs (nt_gemm.cu): H = 1.5 I - 0.5 W W^T
-//      (a Gram product with the combination in its epilogue; symmetric, so
-//      only its upper triangle is computed and then mirrored), then
-//      V' = V H, whose epilogue also writes W' = V'^T. H is stored in the
+//      (a Gram product with the combination in its epilogue, read with bf16
+//      operands from V as V^T V; symmetric, so only its upper triangle is
+//      computed and then mirrored), then V' = V H. H is stored in the
 //      iterate's type. With TF32 inputs the step stays in the form
-//      V' = 1.5 V - 0.5 V G, V read in fp32 by the epilogue;
+//      V' = 1.5 V - 0.5 V G, V read in fp32 by the epilogue. TF32 and the
+//      CUDA-core form write W' = V'^T beside V' for their next Gram product;
 //   4. theta' = theta + s X, s = lr or lr |Delta|_F / sqrt(min(m, n)), read
 //      from V (tall) or W (wide), then the EMA of the globals.
 // Equal-shape matrices run as one batch through every kernel.
@@ -512,9 +513,15 @@ int run_pass(OrthoWork* w, const std::vector<Chunk>& pass, const OrthoParams& p,
     // fp32 in the epilogue, so that only the correction passes through TF32
     // inputs (V H would round the whole iterate to TF32 on every step).
     const bool cform = p.precision == CAM_ORTHO_TF32;
+    // With bf16 operands the Gram product reads V itself (MN-major operands:
+    // G = V^T V), so W = V^T is written only where the applied step reads it,
+    // on the last step of a wide matrix. TF32 (whose MMA is given K-major
+    // operands only) and the CUDA-core form keep both orientations.
+    const bool mn = p.precision == CAM_ORTHO_BF16;
     NtGemm gram[kOrthoPassChunks], upd[kOrthoPassChunks];
     const int n = static_cast<int>(pass.size());
     for (int it = 0; !short_side && it < p.iterations; ++it) {
+        const bool last = it + 1 == p.iterations;
         for (int i = 0; i < n; ++i) {
             const Chunk& ch = pass[i];
             const Shape& sh = ch.sh;
@@ -523,8 +530,14 @@ int run_pass(OrthoWork* w, const std::vector<Chunk>& pass, const OrthoParams& p,
             void* Vc = at(w->V[cur], ch.off_pad, eb);
             void* G = at(w->G, ch.off_gram, eb);
             NtGemm& g = gram[i];
-            g = nt(p.precision, kNtGram, ch.count, sh.rp, sh.rp, sh.Lp, Wc, sh.Lp, padded, Wc,
-                   sh.Lp, padded);
+            if (mn) {
+                g = nt(p.precision, kNtGram, ch.count, sh.rp, sh.rp, sh.Lp, Vc, sh.rp, padded, Vc,
+                       sh.rp, padded);
+                g.mn_major = true;
+            } else {
+                g = nt(p.precision, kNtGram, ch.count, sh.rp, sh.rp, sh.Lp, Wc, sh.Lp, padded, Wc,
+                       sh.Lp, padded);
+            }
             g.alpha = cform ? 1.0f : -0.5f;
             g.diag = cform ? 0.0f : 1.5f;
             g.Y = G;
@@ -546,9 +559,11 @@ int run_pass(OrthoWork* w, const std::vector<Chunk>& pass, const OrthoParams& p,
             u.Y = at(w->V[1 - cur], ch.off_pad, eb);
             u.ldy = sh.rp;
             u.sY = padded;
-            u.Yt = at(w->W[1 - cur], ch.off_pad, eb);
-            u.ldyt = sh.Lp;
-            u.sYt = padded;
+            if (!mn || (last && !sh.tall)) {
+                u.Yt = at(w->W[1 - cur], ch.off_pad, eb);
+                u.ldyt = sh.Lp;
+                u.sYt = padded;
+            }
         }
         int rc = nt_gemm(gram, n, sm_count, p.status, s, launches);
         if (rc == CAM_OK) rc = nt_gemm(upd, n, sm_count, p.status, s, launches);

@@ -135,6 +135,53 @@ def test_one_short_side_step(precision):
         assert err <= STEP_TOL[precision] * scale, (r, c)
 
 
+# The polar factor after 40 steps, relative to the largest element of the step
+# (the bounds the other orthogonalisation tests use: 8 units of the storage's
+# rounding).
+POLAR_TOL = {B.ORTHO_BF16: 8 * 2.0 ** -8, B.ORTHO_TF32: 8 * 2.0 ** -11}
+
+
+@pytest.mark.parametrize("precision", [B.ORTHO_BF16, B.ORTHO_TF32])
+def test_polar_factor_on_full_operand_boxes(precision):
+    """After one step the Gram product's share of the step is small (X0 has
+    unit Frobenius norm, so its singular values are about 1/sqrt(r)); after 40
+    it decides the result. These shapes fill every 128-byte operand box along
+    the short side (r = 256, 384, 512: no zero padding there), tall and wide,
+    with 256- and 128-wide tiles, so a wrong operand layout in any box shows
+    here against the oracle's polar factor (fp64 SVD)."""
+    shapes = [(640, 256), (256, 1000), (384, 1152), (1536, 512)]
+    sizes = [r * c for r, c in shapes]
+    specs = tuple(W.TensorSpec(f"t{i}", (n,), 0) for i, n in enumerate(sizes))
+    wl = W.Workload("ns_polar", specs, 1, K=2, n_masked=0, quorum=2, ckpt_dtype="f32",
+                    mode="mean", ema_beta=0.9, rounds=((0, -1),))
+    g = W.make_global(wl, 47, DEV)
+    th = W.empty_arena(g.numels, torch.float32, DEV)
+    th.flat.copy_(g.flat)
+    e = W.empty_arena(g.numels, torch.float32, DEV)
+    e.flat.copy_(g.flat)
+    mg = B.Merger(th.views, ema=e.views, quorum=2, rows=[r for r, _ in shapes])
+    workers = [W.make_worker(wl, g, 0, k, 47, DEV) for k in range(2)]
+    rd = mg.begin(0)
+    for k in range(2):
+        rd.accumulate(workers[k].views, 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.ema_update(0.9)
+    rd.orthogonalize(0.7, B.ORTHO_SCALE_MATCH_NORM, precision, 40)
+    rd.commit()
+    torch.cuda.synchronize()
+    for t, (r, c) in enumerate(shapes):
+        xs = [w.views[t].cpu().numpy() for w in workers]
+        th0 = g.views[t].cpu().numpy().copy()
+        want, _ = oracle.orthogonal_update(xs, th0, r, lr=0.7, scale_mode=oracle.ORTHO_SCALE_MATCH_NORM)
+        got = th.views[t].cpu().numpy().astype(np.float64)
+        scale = np.abs(want - th0.astype(np.float64)).max()
+        err = np.abs(got - want).max()
+        print(f"polar precision={precision} {r}x{c}: max err / max step = {err / scale:.3e}")
+        assert err <= POLAR_TOL[precision] * scale + 2 * np.spacing(np.float32(np.abs(want).max())), (r, c)
+    assert mg.status() == 0
+    mg.close()
+
+
 @pytest.mark.parametrize("precision", [B.ORTHO_BF16, B.ORTHO_TF32])
 def test_orthogonalised_rounds_repeat_bit_for_bit(precision):
     """The GEMMs sum in a fixed order (no atomics; split partials summed in
