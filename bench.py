@@ -384,7 +384,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum,
                   swa=None if swa is None else swa.views, staging=not args.no_staging,
-                  fused_finish=not args.no_fused_finish)
+                  fused_finish=not args.no_fused_finish, share_sms=args.share_sms or wl.share_sms)
     n_streams = max(1, wl.in_flight)
     # with --graph the step is captured into a CUDA graph: it runs on a stream
     # of its own, which the capture can take
@@ -549,7 +549,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
                        "streams": n_streams, "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replicas{ws}", "cuda_graph": bool(args.graph),
-                       "fused_finish": not args.no_fused_finish},
+                       "fused_finish": not args.no_fused_finish,
+                       "share_sms": args.share_sms or wl.share_sms},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": peak_src, "traffic": traffic,
@@ -1132,6 +1133,9 @@ def parse(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-staging", action="store_true",
                    help="merge passes in the register form instead of the staged (bulk-copy) form")
+    p.add_argument("--share-sms", action="store_true",
+                   help="merge passes keep to one register-form block per SM, so rounds in "
+                        "flight on other streams run beside them (CAM_SHARE_SMS)")
     p.add_argument("--no-fused-finish", action="store_true",
                    help="drift norms always finished by the separate norm pass (small rounds "
                         "otherwise finish them in a register-form merge pass)")

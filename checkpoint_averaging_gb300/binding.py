@@ -27,6 +27,7 @@ NO_STAGING = 8
 TIME_COMMITS = 16
 NO_FUSED_FINISH = 32
 TEST_STALL_STAGED = 64  # test hook: staged passes withhold their first tile and time out
+SHARE_SMS = 128  # merge passes leave room on every SM for a round in flight beside them
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 STATUS_GEMM_TIMEOUT = 2
@@ -474,14 +475,17 @@ class Merger:
     def __init__(self, master, *, momentum=None, ema=None, fragment_of=None,
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
                  zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
-                 staging=True, time_commits=False, fused_finish=True, test_stall_staged=False):
+                 staging=True, time_commits=False, fused_finish=True, test_stall_staged=False,
+                 share_sms=False):
         """rows: optional per-tensor matrix rows (default: the tensors' first
         dimension), used by orthogonalised rounds. staging=False keeps every
         merge pass on the register form (the staged form gives the same
         results). time_commits=True times each commit's device work
         (last_commit()["ms"]). fused_finish=False always launches the
         separate norm pass (small rounds otherwise finish their norms in the
-        merge pass; the same bits). test_stall_staged=True is a test hook
+        merge pass; the same bits). share_sms=True (CAM_SHARE_SMS) keeps every
+        merge pass to one register-form block per SM, so that rounds in flight
+        on other streams run beside it (the same bits). test_stall_staged=True is a test hook
         (CAM_TEST_STALL_STAGED): staged passes withhold their first tile, their
         waits give up after about 1 ms and status() reports the timeout."""
         torch = _torch()
@@ -511,7 +515,7 @@ class Merger:
                 (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
                 (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0) | \
                 (0 if fused_finish else NO_FUSED_FINISH) | \
-                (TEST_STALL_STAGED if test_stall_staged else 0)
+                (TEST_STALL_STAGED if test_stall_staged else 0) | (SHARE_SMS if share_sms else 0)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,

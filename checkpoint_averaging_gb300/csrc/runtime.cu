@@ -136,6 +136,7 @@ struct cam_ctx {
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     bool staged = true;            // the staged form of the merge pass may be used
     bool test_stall = false;       // CAM_TEST_STALL_STAGED
+    bool share_sms = false;        // CAM_SHARE_SMS: one register-form block per SM at most
     bool time_commits = false;     // CAM_TIME_COMMITS: events around each commit
     cudaEvent_t commit_ev[2] = {nullptr, nullptr};
     cam_commit_record last_commit{};
@@ -267,7 +268,7 @@ int validate_desc(const cam_ctx_desc* d) {
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
     if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
                      CAM_NO_STAGING | CAM_TIME_COMMITS | CAM_NO_FUSED_FINISH |
-                     CAM_TEST_STALL_STAGED))
+                     CAM_TEST_STALL_STAGED | CAM_SHARE_SMS))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -446,6 +447,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->fuse_finish = !(d->flags & CAM_NO_FUSED_FINISH);
     c->staged = !(d->flags & CAM_NO_STAGING);
     c->test_stall = (d->flags & CAM_TEST_STALL_STAGED) != 0;
+    c->share_sms = (d->flags & CAM_SHARE_SMS) != 0;
     c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
     for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
         ce = cudaEventCreate(&c->commit_ev[i]);
@@ -954,7 +956,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.beta = r->beta;
     a.swa_n = static_cast<float>(swa_prev + 1);
     const int norm_level = r->worker_norms ? 2 : (r->norms ? 1 : 0);
-    const int bps = c->bps[r->dtype][r->mode][r->ema][norm_level][r->publish][r->swa];
+    const int bps = c->share_sms ? 1 : c->bps[r->dtype][r->mode][r->ema][norm_level][r->publish][r->swa];
     const cam::MergeVariant variant{r->dtype, r->mode, r->ema, norm_level, r->publish, r->swa};
     const int stride = K + (r->publish ? 2 : 0);
     a.stride = stride;
@@ -990,7 +992,10 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     // behind when it writes three (theta, m, e or theta, e, swa), where the
     // register form is kept.
     const int state_writes = 1 + int(delta) + int(r->ema) + int(r->swa);
-    const bool staged_ok = c->staged && !r->host_workers && st_stages >= 2 && state_writes <= 2;
+    // (a staged block takes its SM's shared memory: with CAM_SHARE_SMS the
+    // register form leaves room for another round's blocks)
+    const bool staged_ok = c->staged && !c->share_sms && !r->host_workers && st_stages >= 2 &&
+                           state_writes <= 2;
     // Small rounds with the round's drift norms finish them in the merge pass
     // itself (register form, last block): one launch fewer, the same sums.
     const NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
@@ -1041,7 +1046,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
             a.local0 = l0;
             a.n_local = n;
             if (fuse) {  // a single launch covering the whole fragment
-                const int b = c->bps_fin[r->dtype][r->mode][r->ema][r->publish][r->swa];
+                const int b = c->share_sms ? 1 : c->bps_fin[r->dtype][r->mode][r->ema][r->publish][r->swa];
                 const int grid =
                     static_cast<int>(std::min<int64_t>(a.n_chunks, int64_t(c->sm_count) * b));
                 ce = cam::launch_merge(a, variant_fin, grid, s);

@@ -188,6 +188,7 @@ class Workload:
     workers_track_global: bool = False  # workers start from the current global
     swa: bool = False                   # also fold each global into the uniform average
     worker_norms: bool = False          # also report each worker's own drift
+    share_sms: bool = False             # merge passes leave room for rounds in flight beside them
 
     @property
     def n_params(self) -> int:
@@ -203,11 +204,12 @@ class Workload:
 
 def _wl_pythia() -> Workload:
     # three fragment rounds per step; as in the Pythia page's run ("Getting
-    # updates through the bucket"), two rounds may be in flight at once
+    # updates through the bucket"), two rounds may be in flight at once, and
+    # their merge passes share the SMs (the long round beside the short ones)
     return Workload("pythia14m_f4_q3_delta_nesterov", tuple(pythia14m_specs()), 4,
                     K=4, n_masked=1, quorum=3, ckpt_dtype="f32", mode="delta",
                     lr=0.7, mu=0.9, rounds=((0, 0), (1, 1), (2, 2)), in_flight=2,
-                    noise_std=1e-3, tokens=(200_000, 600_000), norms=True)
+                    noise_std=1e-3, tokens=(200_000, 600_000), norms=True, share_sms=True)
 
 
 def _wl_stand() -> Workload:

@@ -101,6 +101,9 @@ typedef enum {
 #define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
 #define CAM_TIME_COMMITS 16u        /* time each commit's device work (cam_ctx_last_commit) */
 #define CAM_NO_FUSED_FINISH 32u     /* always finish drift norms in a separate norm pass */
+#define CAM_SHARE_SMS 128u          /* merge passes take at most one register-form block per SM,
+                                       leaving room beside them for a round in flight on another
+                                       stream (small fragment rounds run alongside) */
 #define CAM_TEST_STALL_STAGED 64u   /* test hook, never for real rounds: every staged merge pass
                                        withholds its first tile and gives up waiting after
                                        about 1 ms (see cam_ctx_status) */
@@ -443,6 +446,12 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * pass's last block to finish sums the per-chunk partials exactly as the norm
  * pass would, so the results are the same bits, one launch fewer. A context
  * created with CAM_NO_FUSED_FINISH always launches the separate norm pass.
+ *
+ * A context created with CAM_SHARE_SMS keeps every merge pass in the
+ * register form with at most one block per SM. A pass then holds half of
+ * each SM's registers and little shared memory, so the pass of a round in
+ * flight on another stream runs beside it instead of after it: a long round
+ * and short rounds of other fragments overlap. The results are the same bits.
  *
  * Every wait of the staged form on one of its barriers gives up after a few
  * seconds. It then sets CAM_STATUS_WAIT_TIMEOUT in the context's device status

@@ -66,7 +66,7 @@ class GpuState:
 
 
 def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
-                   fused_finish=True, test_stall_staged=False) -> GpuState:
+                   fused_finish=True, test_stall_staged=False, share_sms=False) -> GpuState:
     theta = W.empty_arena(g.numels, torch.float32, dev)
     theta.flat.copy_(g.flat)
     m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
@@ -79,7 +79,8 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
                   ema=None if e is None else e.views, fragment_of=wl.fragment_of,
                   n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
                   swa=None if swa is None else swa.views, staging=staging,
-                  fused_finish=fused_finish, test_stall_staged=test_stall_staged)
+                  fused_finish=fused_finish, test_stall_staged=test_stall_staged,
+                  share_sms=share_sms)
     return GpuState(theta, m, e, mg, swa)
 
 
@@ -163,10 +164,10 @@ def compare_norms(gpu_norms, ora_norms, what: str) -> None:
         f"{what}: fragment drift norm {pf.item()} vs {frag}"
 
 
-def run_full(wl: W.Workload, seed: int = 0, dev="cuda", bitwise=False):
+def run_full(wl: W.Workload, seed: int = 0, dev="cuda", bitwise=False, share_sms=False):
     """Every round of the workload, full element-by-element comparison."""
     g = W.make_global(wl, seed, dev)
-    st = make_gpu_state(wl, g, dev)
+    st = make_gpu_state(wl, g, dev, share_sms=share_sms)
     ost = oracle_state_from(g, wl)
     for idx, (rnd, frag) in enumerate(wl.rounds):
         draw = W.draw_round(wl, idx, seed)
