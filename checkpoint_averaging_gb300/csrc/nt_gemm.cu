@@ -60,6 +60,7 @@ constexpr int kSmemBudget = 224 * 1024;  // the stage ring and the epilogue stag
 constexpr unsigned long long kTcWaitLimitNs = 4000000000ull;
 constexpr int kEpiAxpbyC = 2;            // kNtAxpby reading C (prefetched by TMA)
 constexpr int kMaxProblems = 8;          // problems per launch
+constexpr int kQueue = 4;                // unit queue of a Gram launch (slots)
 constexpr int kOutBox = 32;              // epilogue boxes: 32 x 32 elements
 constexpr int kEpiWarps = 4;
 
@@ -262,6 +263,9 @@ struct alignas(128) TcArgs {
     int32_t n_units;         // units of every problem
     float alpha, beta, diag;
     int32_t* status;
+    // Gram launches: [0] the next unit to hand out, [1] blocks finished; both
+    // 0 between launches (the last block to finish resets them)
+    int32_t* sched;
 };
 
 // One unit of work: its problem, the tile's first rows in A and B, its
@@ -413,8 +417,8 @@ struct Geo {
     // ring + staging + barriers (full, empty, tmem full, tmem empty, drain,
     // one "C full" per epilogue warp) + TMEM address + abort flag, plus 1 KB
     // to align the ring to 1,024 bytes
-    static constexpr int kBars = 2 * kStages + 5 + kEpiWarps;
-    static constexpr int kSmem = kBarOffset + 8 * kBars + 16 + 1024;
+    static constexpr int kBars = 2 * kStages + 5 + kEpiWarps + 2 * kQueue;
+    static constexpr int kSmem = kBarOffset + 8 * kBars + 16 + 4 * kQueue + 1024;
     static constexpr int kKStep = kRowBytes / (BF16 ? 2 : 4);  // elements per K step
     static_assert(kStages >= 2, "shared memory too small for the ring");
     static_assert(kSmem <= 232448, "over the per-block shared memory limit");
@@ -437,8 +441,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
     const uint32_t tempty0 = tfull0 + 16;
     const uint32_t drain = tempty0 + 16;
     const uint32_t cfull0 = drain + 8;
+    const uint32_t qfull0 = cfull0 + 8 * kEpiWarps;  // unit queue (Gram launches)
+    const uint32_t qempty0 = qfull0 + 8 * kQueue;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + G::kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* qval = reinterpret_cast<volatile int*>(tmem_slot + 4);
+    // Gram launches hand units out dynamically (their tiles' K ranges differ
+    // from problem to problem); the others take u = block, block + grid, ...
+    constexpr bool kDyn = EPI == kNtGram;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t kCols = 2 * BN;  // two accumulators
 
@@ -453,6 +463,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         }
         bar_init(drain, 1);
         for (int w = 0; w < kEpiWarps; ++w) bar_init(cfull0 + 8 * w, 1);
+        for (int q = 0; q < kQueue; ++q) {
+            bar_init(qfull0 + 8 * q, 1);
+            bar_init(qempty0 + 8 * q, 1 + kEpiWarps);  // the MMA issuer and each epilogue warp
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -480,7 +494,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         uint32_t phase = 0;
         uint32_t issued = 0;  // bit s: stage s has a fill whose phase is (filled_parity >> s) & 1
         uint32_t filled_parity = 0;
-        for (int u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
+        int qslot = 0, iter = 0;
+        uint32_t qphase = 0;
+        for (;;) {
+            int u;
+            if constexpr (kDyn) {  // the next unit, published to the other roles
+                if (*abort_flag) break;
+                u = atomicAdd(a.sched, 1);
+                if (u >= a.n_units) u = -1;
+                if (!bar_wait(qempty0 + 8 * qslot, qphase ^ 1, abort_flag, a.status)) break;
+                qval[qslot] = u;
+                bar_arrive(qfull0 + 8 * qslot);
+                if (++qslot == kQueue) {
+                    qslot = 0;
+                    qphase ^= 1;
+                }
+                if (u < 0) break;
+            } else {
+                u = blockIdx.x + iter++ * gridDim.x;
+                if (u >= a.n_units || *abort_flag) break;
+            }
             const Unit t = decode<BN, EPI>(a, u);
             const TcProblem& P = a.prob[t.p];
             const int arow = t.rb * kBM, brow = t.cb * BN;
@@ -511,6 +544,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                 }
             }
         }
+        if constexpr (kDyn) {  // the last block out leaves the counters at 0
+            if (!*abort_flag) {
+                __threadfence();
+                if (atomicAdd(a.sched + 1, 1) == int(gridDim.x) - 1) {
+                    a.sched[0] = 0;
+                    a.sched[1] = 0;
+                    __threadfence();
+                }
+            }
+        }
         if (*abort_flag) {  // let the copies in flight land before the block exits
             for (int s = 0; s < G::kStages; ++s)
                 if ((issued >> s) & 1) {
@@ -526,7 +569,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        int qslot = 0, iter = 0;
+        uint32_t qphase = 0;
+        for (;;) {
+            int u;
+            if constexpr (kDyn) {
+                if (!bar_wait(qfull0 + 8 * qslot, qphase, abort_flag, a.status)) break;
+                u = qval[qslot];
+                bar_arrive(qempty0 + 8 * qslot);
+                if (++qslot == kQueue) {
+                    qslot = 0;
+                    qphase ^= 1;
+                }
+                if (u < 0) break;
+            } else {
+                u = blockIdx.x + iter++ * gridDim.x;
+                if (u >= a.n_units) break;
+            }
             const Unit t = decode<BN, EPI>(a, u);
             if (!bar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, a.status)) break;
             tc_fence_after();
@@ -590,7 +649,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
         }
         int acc = 0, buf = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        int qslot = 0, iter = 0;
+        uint32_t qphase = 0;
+        for (;;) {
+            int u;
+            if constexpr (kDyn) {
+                const bool okq = bar_wait(qfull0 + 8 * qslot, qphase, abort_flag, a.status);
+                if (!__all_sync(0xffffffffu, okq)) break;
+                u = qval[qslot];
+                __syncwarp();
+                if (lane == 0) bar_arrive(qempty0 + 8 * qslot);
+                if (++qslot == kQueue) {
+                    qslot = 0;
+                    qphase ^= 1;
+                }
+                if (u < 0) break;
+            } else {
+                u = blockIdx.x + iter++ * gridDim.x;
+                if (u >= a.n_units) break;
+            }
             const Unit t = decode<BN, EPI>(a, u);
             const TcProblem& P = a.prob[t.p];
             // the whole warp leaves together: tcgen05.ld is warp-collective
@@ -701,25 +778,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
 // Sums the split partials of Gram products in range order and writes
 // Y = alpha sum + diag I, the whole symmetric matrix: element (i, j) takes the
 // partials of (min, max), so both triangles carry the same bits. One block of
-// 32 x 32 threads per 32 x 32 tile on or above the diagonal (blockIdx.x walks
-// those tiles row by row), one element per thread with its loads for several
-// ranges in flight; the tile is written, and mirrored, through shared memory.
+// 32 x 8 threads per 8-row quarter of a 32 x 32 tile on or above the diagonal
+// (blockIdx.x: the tile, row by row, times four), one element per thread with
+// its loads for several ranges in flight; the quarter is written, and
+// mirrored, through shared memory.
 template <typename T>
-__global__ void __launch_bounds__(1024) gram_reduce(const float* P, int splits, int batch,
-                                                    int64_t M, float alpha, float diag, T* Y,
-                                                    int64_t ldy, int64_t sY) {
-    __shared__ float tile[32][33];
+__global__ void __launch_bounds__(256) gram_reduce(const float* P, int splits, int batch,
+                                                   int64_t M, float alpha, float diag, T* Y,
+                                                   int64_t ldy, int64_t sY) {
+    __shared__ float tile[8][33];
     const int b = blockIdx.y;
-    // tile index -> (ti, tj), tj >= ti, over a (M/32) x (M/32) grid
+    // (tile, quarter) -> (ti, tj, rows 8 quarter .. + 7), tj >= ti
     const int64_t nt = M / 32;
-    int64_t q = blockIdx.x, ti = 0;
+    const int quarter = blockIdx.x & 3;
+    int64_t q = blockIdx.x >> 2, ti = 0;
     while (q >= nt - ti) {
         q -= nt - ti;
         ++ti;
     }
     const int64_t tj = ti + q;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 32
-    const int64_t i = ti * 32 + ty, j = tj * 32 + tx;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    const int64_t i = ti * 32 + quarter * 8 + ty, j = tj * 32 + tx;
     const int64_t split_stride = int64_t(batch) * M * M;
     // diagonal tile: the upper element of the pair
     const float* p = P + int64_t(b) * M * M + (j >= i ? i * M + j : j * M + i);
@@ -730,7 +809,10 @@ __global__ void __launch_bounds__(1024) gram_reduce(const float* P, int splits, 
     __syncthreads();
     T* y = Y + b * sY;
     y[i * ldy + j] = T(tile[ty][tx]);
-    if (tj > ti) y[(tj * 32 + ty) * ldy + ti * 32 + tx] = T(tile[tx][ty]);  // the mirror (j, i)
+    if (tj > ti) {  // the mirror: rows tj*32 + c, columns ti*32 + 8 quarter + r
+        const int lin = ty * 32 + tx, c = lin >> 3, r = lin & 7;
+        y[(tj * 32 + c) * ldy + ti * 32 + quarter * 8 + r] = T(tile[r][c]);
+    }
 }
 
 // ---- the CUDA-core fp32 kernel -------------------------------------------------------
@@ -1002,36 +1084,62 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     a.beta = g0.beta;
     a.diag = g0.diag;
     a.status = status;
-    // Gram products: tiles reaching the upper triangle, and a K split for
-    // products whose tiles are long, so that no unit is longer than one
-    // block's share of the launch (ranges of at least 16 K steps, within the
-    // partial buffer; each range costs a pass over the matrix in partials).
+    // Per problem (caller's order): tile counts and K steps; for Gram
+    // products the tiles reaching the upper triangle and a K split for long
+    // tiles, so that no unit is longer than one block's share of the launch
+    // (ranges of at least 16 K steps, within the partial buffer; each range
+    // costs a pass over the matrix in partials).
     int64_t work = 0;
+    int n_blk[kMaxProblems], m_blk[kMaxProblems], k_blk[kMaxProblems], tri[kMaxProblems];
     for (int i = 0; i < n; ++i) {
-        TcProblem& P = a.prob[i];
         const NtGemm& g = gs[i];
-        P.batch = g.batch;
-        P.m_blocks = static_cast<int32_t>(g.M / kBM);
-        P.n_blocks = static_cast<int32_t>(g.N / bn);
-        P.k_blocks = static_cast<int32_t>(g.K / kstep);
-        P.splits = 1;
-        P.k_per_split = P.k_blocks;
+        m_blk[i] = static_cast<int>(g.M / kBM);
+        n_blk[i] = static_cast<int>(g.N / bn);
+        k_blk[i] = static_cast<int>(g.K / kstep);
+        tri[i] = 0;
         if (gram) {
-            int tri = 0;
-            for (int cb = 0; cb < P.n_blocks; ++cb)
-                tri += std::min(P.m_blocks, (bn * cb + bn - 1) / kBM + 1);
-            P.n_tri = tri;
-            work += int64_t(tri) * g.batch * P.k_blocks;
+            for (int cb = 0; cb < n_blk[i]; ++cb) tri[i] += std::min(m_blk[i], (bn * cb + bn - 1) / kBM + 1);
+            work += int64_t(tri[i]) * g.batch * k_blk[i];
         } else {
-            work += int64_t(P.m_blocks) * P.n_blocks * g.batch * P.k_blocks;
+            work += int64_t(m_blk[i]) * n_blk[i] * g.batch * k_blk[i];
         }
     }
     const int64_t longest = std::max<int64_t>(16, work / int64_t(sm_count));
+    int splits[kMaxProblems], kps[kMaxProblems], ord[kMaxProblems];
+    int64_t part_need = 0;
+    for (int i = 0; i < n; ++i) {
+        const NtGemm& g = gs[i];
+        int sp = 1;
+        if (gram && k_blk[i] > longest && g.partials) {
+            const int64_t want = (k_blk[i] + longest - 1) / longest;
+            const int64_t by_mem = (g.partial_floats - part_need) / (int64_t(g.batch) * g.M * g.M);
+            sp = static_cast<int>(std::max<int64_t>(1, std::min(want, by_mem)));
+        }
+        kps[i] = (k_blk[i] + sp - 1) / sp;
+        splits[i] = (k_blk[i] + kps[i] - 1) / kps[i];  // no empty range
+        if (splits[i] > 1) part_need += int64_t(splits[i]) * g.batch * g.M * g.M;
+        ord[i] = i;
+    }
+    // Gram launches hand their units out longest first: problems ordered by
+    // the K steps of one unit
+    if (gram)
+        std::stable_sort(ord, ord + n, [&](int x, int y) { return kps[x] > kps[y]; });
+    if (gram && !g0.sched)
+        return record_error(CAM_E_ARG, "orthogonalisation: a Gram launch needs its unit counter");
+    a.sched = g0.sched;
     int64_t part_used = 0;
     int32_t units = 0;
-    for (int i = 0; i < n; ++i) {
-        TcProblem& P = a.prob[i];
+    for (int j = 0; j < n; ++j) {
+        const int i = ord[j];
+        TcProblem& P = a.prob[j];
         const NtGemm& g = gs[i];
+        P.batch = g.batch;
+        P.m_blocks = m_blk[i];
+        P.n_blocks = n_blk[i];
+        P.k_blocks = k_blk[i];
+        P.n_tri = tri[i];
+        P.splits = splits[i];
+        P.k_per_split = kps[i];
         int rc;
         if (mn) {  // A stored K x M, B stored K x N: boxes of 128 bytes of M (N) by one K step
             rc = make_map(&P.ta, eb, g.A, g.M, g.K, g.batch, g.lda, g.sA,
@@ -1048,15 +1156,7 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
         if (rc != CAM_OK) return rc;
         P.unit0 = units;
         if (gram) {
-            int splits = 1;
-            if (P.k_blocks > longest && g.partials) {
-                const int64_t want = (P.k_blocks + longest - 1) / longest;
-                const int64_t by_mem = (g.partial_floats - part_used) / (int64_t(g.batch) * g.M * g.M);
-                splits = static_cast<int>(std::max<int64_t>(1, std::min(want, by_mem)));
-            }
-            if (splits > 1) {
-                P.k_per_split = (P.k_blocks + splits - 1) / splits;
-                P.splits = (P.k_blocks + P.k_per_split - 1) / P.k_per_split;  // no empty range
+            if (P.splits > 1) {
                 float* part = g.partials + part_used;
                 part_used += int64_t(P.splits) * g.batch * g.M * g.M;
                 rc = out_map(&P.ty, 4, part, g.M, g.M, int64_t(P.splits) * g.batch, g.M, g.M * g.M,
@@ -1087,20 +1187,20 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     if (e != cudaSuccess) return launch_fail(e);
     // the split Gram products' partials, summed in range order
     int64_t part_off = 0;
-    for (int i = 0; gram && i < n; ++i) {
-        const TcProblem& P = a.prob[i];
-        const NtGemm& g = gs[i];
+    for (int j = 0; gram && j < n; ++j) {
+        const TcProblem& P = a.prob[j];
+        const NtGemm& g = gs[ord[j]];
         if (P.splits <= 1) continue;
         const float* part = g.partials + part_off;
         part_off += int64_t(P.splits) * g.batch * g.M * g.M;
         const int64_t nt = g.M / 32;  // tiles on or above the diagonal, per matrix
-        const dim3 rgrid(static_cast<unsigned>(nt * (nt + 1) / 2), static_cast<unsigned>(g.batch));
+        const dim3 rgrid(static_cast<unsigned>(4 * nt * (nt + 1) / 2), static_cast<unsigned>(g.batch));
         if (bf16)
-            gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 32), 0, s>>>(
+            gram_reduce<__nv_bfloat16><<<rgrid, dim3(32, 8), 0, s>>>(
                 part, P.splits, g.batch, g.M, g.alpha, g.diag, static_cast<__nv_bfloat16*>(g.Y),
                 g.ldy, g.sY);
         else
-            gram_reduce<float><<<rgrid, dim3(32, 32), 0, s>>>(part, P.splits, g.batch, g.M, g.alpha,
+            gram_reduce<float><<<rgrid, dim3(32, 8), 0, s>>>(part, P.splits, g.batch, g.M, g.alpha,
                                                              g.diag, static_cast<float*>(g.Y), g.ldy,
                                                              g.sY);
         ++*launches;

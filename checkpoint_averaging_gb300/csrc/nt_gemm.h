@@ -60,6 +60,10 @@ struct NtGemm {
     // into fp32 partial tiles here (summed in a fixed order by a second
     // kernel); null or too small: no split.
     float* partials; int64_t partial_floats;
+    // Gram products on the tensor cores: two int32 counters in device memory,
+    // 0 before the first launch, through which the launch hands out its tiles
+    // (and which it leaves at 0); launches that share them run one at a time
+    int32_t* sched;
 };
 
 // Enqueues n products (1 <= n <= 8) on `s` as one launch of the tensor-core

@@ -62,6 +62,7 @@ struct OrthoWork {
     double* partials = nullptr;  // [kOrthoBatchMax * kOrthoBlocksMax]
     double* scalars = nullptr;   // [j] = |Delta_j|_F^2
     float* inv_norm = nullptr;   // [j] = 1 / |Delta_j|_F (0 when Delta_j = 0)
+    int32_t* sched = nullptr;    // the Gram launches' unit counters (0 between launches)
     void* block = nullptr;       // one cudaMalloc holding all of the above
     int64_t cap_pad = 0;         // elements in each W / V buffer and floats in X
     int64_t cap_gram = 0;        // elements in G
@@ -545,6 +546,7 @@ int run_pass(OrthoWork* w, const std::vector<Chunk>& pass, const OrthoParams& p,
             g.sY = sq;
             g.partials = w->split;
             g.partial_floats = kSplitFloats;
+            g.sched = w->sched;
             // V' = V H (or 1.5 V - 0.5 V G), W' = V'^T
             NtGemm& u = upd[i];
             u = nt(p.precision, kNtAxpby, ch.count, sh.Lp, sh.rp, sh.rp, Vc, sh.rp, padded, G, sh.rp,
@@ -597,7 +599,8 @@ int ortho_create(OrthoWork** out, int64_t cap_pad, int64_t cap_gram, int64_t big
     const size_t bp = up(sizeof(double) * size_t(kOrthoBatchMax) * kOrthoBlocksMax);
     const size_t bs = up(sizeof(double) * kOrthoBatchMax);
     const size_t bi = up(sizeof(float) * kOrthoBatchMax);
-    const size_t total = 5 * bx + bg + bq + bk + bp + bs + bi;
+    const size_t bc = 256;  // the unit counters
+    const size_t total = 5 * bx + bg + bq + bk + bp + bs + bi + bc;
     if (cudaMalloc(&w->block, total) != cudaSuccess) {
         cudaGetLastError();
         delete w;
@@ -616,6 +619,14 @@ int ortho_create(OrthoWork** out, int64_t cap_pad, int64_t cap_gram, int64_t big
     w->partials = reinterpret_cast<double*>(b + bg + bq + bk);
     w->scalars = reinterpret_cast<double*>(b + bg + bq + bk + bp);
     w->inv_norm = reinterpret_cast<float*>(b + bg + bq + bk + bp + bs);
+    w->sched = reinterpret_cast<int32_t*>(b + bg + bq + bk + bp + bs + bi);
+    // (once per context: finished before any stream's GEMM can read them)
+    if (cudaMemset(w->sched, 0, bc) != cudaSuccess || cudaStreamSynchronize(nullptr) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(w->block);
+        delete w;
+        return record_error(CAM_E_CUDA, "orthogonalisation: clearing the unit counters failed");
+    }
     *out = w;
     return CAM_OK;
 }

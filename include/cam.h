@@ -101,12 +101,12 @@ typedef enum {
 #define CAM_NO_STAGING 8u           /* never use the staged (bulk-copy) form of the merge pass */
 #define CAM_TIME_COMMITS 16u        /* time each commit's device work (cam_ctx_last_commit) */
 #define CAM_NO_FUSED_FINISH 32u     /* always finish drift norms in a separate norm pass */
-#define CAM_SHARE_SMS 128u          /* merge passes take at most one register-form block per SM,
-                                       leaving room beside them for a round in flight on another
-                                       stream (small fragment rounds run alongside) */
 #define CAM_TEST_STALL_STAGED 64u   /* test hook, never for real rounds: every staged merge pass
                                        withholds its first tile and gives up waiting after
                                        about 1 ms (see cam_ctx_status) */
+#define CAM_SHARE_SMS 128u          /* merge passes take at most one register-form block per SM,
+                                       leaving room beside them for a round in flight on another
+                                       stream (small fragment rounds run alongside) */
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */

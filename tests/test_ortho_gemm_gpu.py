@@ -183,6 +183,45 @@ def test_polar_factor_on_full_operand_boxes(precision):
 
 
 @pytest.mark.parametrize("precision", [B.ORTHO_BF16, B.ORTHO_TF32])
+def test_polar_factor_of_a_tied_embedding(precision):
+    """The width-512 stand's tied embedding (73,760 x 512) with a q/k/v/o-sized
+    matrix beside it, 30 steps, against the oracle's polar factor: the Gram
+    product of the long matrix is split over many K ranges (fp32 partials
+    summed by the reduce kernel) and shares its launches with the small one."""
+    shapes = [(73760, 512), (512, 512)]
+    sizes = [r * c for r, c in shapes]
+    specs = tuple(W.TensorSpec(f"t{i}", (n,), 0) for i, n in enumerate(sizes))
+    wl = W.Workload("ns_embed", specs, 1, K=2, n_masked=0, quorum=2, ckpt_dtype="f32",
+                    mode="mean", ema_beta=0.9, rounds=((0, -1),))
+    g = W.make_global(wl, 53, DEV)
+    th = W.empty_arena(g.numels, torch.float32, DEV)
+    th.flat.copy_(g.flat)
+    e = W.empty_arena(g.numels, torch.float32, DEV)
+    e.flat.copy_(g.flat)
+    mg = B.Merger(th.views, ema=e.views, quorum=2, rows=[r for r, _ in shapes])
+    workers = [W.make_worker(wl, g, 0, k, 53, DEV) for k in range(2)]
+    rd = mg.begin(0)
+    for k in range(2):
+        rd.accumulate(workers[k].views, 0)
+    rd.finalize(B.MEAN_REPLACE)
+    rd.ema_update(0.9)
+    rd.orthogonalize(0.7, B.ORTHO_SCALE_MATCH_NORM, precision, 30)
+    rd.commit()
+    torch.cuda.synchronize()
+    for t, (r, c) in enumerate(shapes):
+        xs = [w.views[t].cpu().numpy() for w in workers]
+        th0 = g.views[t].cpu().numpy().copy()
+        want, _ = oracle.orthogonal_update(xs, th0, r, lr=0.7, scale_mode=oracle.ORTHO_SCALE_MATCH_NORM)
+        got = th.views[t].cpu().numpy().astype(np.float64)
+        scale = np.abs(want - th0.astype(np.float64)).max()
+        err = np.abs(got - want).max()
+        print(f"embedding polar precision={precision} {r}x{c}: max err / max step = {err / scale:.3e}")
+        assert err <= POLAR_TOL[precision] * scale + 2 * np.spacing(np.float32(np.abs(want).max())), (r, c)
+    assert mg.status() == 0
+    mg.close()
+
+
+@pytest.mark.parametrize("precision", [B.ORTHO_BF16, B.ORTHO_TF32])
 def test_orthogonalised_rounds_repeat_bit_for_bit(precision):
     """The GEMMs sum in a fixed order (no atomics; split partials summed in
     range order), so the same round gives the same bits."""
