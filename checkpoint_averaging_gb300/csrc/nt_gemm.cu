@@ -824,16 +824,20 @@ struct SimtArgs {
     const float* A; int64_t lda, sA;
     const float* B; int64_t ldb, sB;
     int64_t K;
+    int64_t k_len;      // K elements per range (blockIdx.z), a multiple of 8
     int32_t n_blocks;   // N / 128
     float alpha, beta, diag;
     const float* C; int64_t ldc, sC;
     float* Y; int64_t ldy, sY;
     float* Yt; int64_t ldyt, sYt;
+    // split K: each range's raw sums, [range][matrix][M][N]; null: no split
+    float* part; int64_t M, N;
 };
 
-// One 128 x 128 tile per block (blockIdx.x: tile, blockIdx.y: matrix); thread
-// (tx, ty) of a 16 x 16 grid owns rows ty*8 .. +7 and columns tx*4 .. +3 and
-// 64 + tx*4 .. +3. K steps of 8, staged in shared memory with K outermost.
+// One 128 x 128 tile per block (blockIdx.x: tile, blockIdx.y: matrix,
+// blockIdx.z: K range); thread (tx, ty) of a 16 x 16 grid owns rows
+// ty*8 .. +7 and columns tx*4 .. +3 and 64 + tx*4 .. +3. K steps of 8, staged
+// in shared memory with K outermost.
 __global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_constant__ SimtArgs a) {
     __shared__ __align__(16) float As[kSimtBK][128];
     __shared__ __align__(16) float Bs[kSimtBK][128];
@@ -849,7 +853,9 @@ __global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_consta
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-    for (int64_t k0 = 0; k0 < a.K; k0 += kSimtBK) {
+    const int64_t k_begin = int64_t(blockIdx.z) * a.k_len;
+    const int64_t k_end = k_begin + a.k_len < a.K ? k_begin + a.k_len : a.K;
+    for (int64_t k0 = k_begin; k0 < k_end; k0 += kSimtBK) {
         const float4 av = *reinterpret_cast<const float4*>(A + lr * a.lda + k0 + lk);
         const float4 bv = *reinterpret_cast<const float4*>(B + lr * a.ldb + k0 + lk);
         __syncthreads();
@@ -875,6 +881,18 @@ __global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_consta
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
         }
+    }
+    if (a.part) {  // a range's raw sums
+        float* part = a.part + (int64_t(blockIdx.z) * gridDim.y + b) * a.M * a.N;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t row = int64_t(mb) * 128 + ty * 8 + i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<float4*>(part + row * a.N + int64_t(nb) * 128 + h * 64 + tx * 4) =
+                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+        }
+        return;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -904,6 +922,41 @@ __global__ void __launch_bounds__(kSimtThreads) nt_gemm_simt(const __grid_consta
 #pragma unroll
                 for (int j = 0; j < 4; ++j) a.Yt[b * a.sYt + (col + j) * a.ldyt + row] = v[j];
         }
+    }
+}
+
+// The split CUDA-core product's epilogue: Y = alpha (sum of the ranges, in
+// range order) + beta C + diag I, four elements per thread.
+__global__ void simt_reduce(const __grid_constant__ SimtArgs a, int splits) {
+    const int64_t quads = a.M * a.N / 4, per = int64_t(gridDim.y) * a.M * a.N;
+    const int b = blockIdx.y;
+    for (int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; q < quads;
+         q += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t row = 4 * q / a.N, col = 4 * q % a.N;
+        const float* p = a.part + int64_t(b) * a.M * a.N + 4 * q;
+        float4 t = *reinterpret_cast<const float4*>(p);
+        for (int r = 1; r < splits; ++r) {
+            const float4 u = *reinterpret_cast<const float4*>(p + r * per);
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
+        }
+        float v[4] = {t.x, t.y, t.z, t.w};
+        if (a.beta != 0.0f) {
+            const float4 c = *reinterpret_cast<const float4*>(a.C + b * a.sC + row * a.ldc + col);
+            const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = fmaf(a.alpha, v[j], a.beta * cv[j]);
+        } else if (a.alpha != 1.0f) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (row == col + j) v[j] += a.diag;
+        *reinterpret_cast<float4*>(a.Y + b * a.sY + row * a.ldy + col) =
+            make_float4(v[0], v[1], v[2], v[3]);
     }
 }
 
@@ -1008,7 +1061,10 @@ int launch_fail(cudaError_t e) {
     return record_error(CAM_E_CUDA, "orthogonalisation: GEMM launch: %s", cudaGetErrorString(e));
 }
 
-int run_simt(const NtGemm& g, cudaStream_t s, int64_t* launches) {
+// CUDA-core product; K split into ranges (summed by simt_reduce) when the
+// tiles alone would leave most SMs idle, each range at least 128 long, within
+// the partial buffer, and only for a row-major result.
+int run_simt(const NtGemm& g, int sm_count, cudaStream_t s, int64_t* launches) {
     SimtArgs a;
     a.A = static_cast<const float*>(g.A);
     a.lda = g.lda;
@@ -1031,10 +1087,33 @@ int run_simt(const NtGemm& g, cudaStream_t s, int64_t* launches) {
     a.Yt = gram ? nullptr : static_cast<float*>(g.Yt);
     a.ldyt = g.ldyt;
     a.sYt = g.sYt;
-    const dim3 grid(static_cast<unsigned>((g.M / 128) * (g.N / 128)), static_cast<unsigned>(g.batch));
+    a.M = g.M;
+    a.N = g.N;
+    a.part = nullptr;
+    const int64_t tiles = (g.M / 128) * (g.N / 128) * g.batch;
+    int64_t splits = 1;
+    if (g.partials && g.Y && !a.Yt) {
+        const int64_t want = (2 * int64_t(sm_count) + tiles - 1) / tiles;
+        const int64_t by_k = g.K / 128;
+        const int64_t by_mem = g.partial_floats / (int64_t(g.batch) * g.M * g.N);
+        splits = std::max<int64_t>(1, std::min(std::min(want, by_k), std::min<int64_t>(by_mem, 65535)));
+    }
+    // ranges of whole 128-element steps; no empty range
+    a.k_len = ((g.K / 128 + splits - 1) / splits) * 128;
+    splits = (g.K + a.k_len - 1) / a.k_len;
+    if (splits > 1) a.part = g.partials;
+    const dim3 grid(static_cast<unsigned>((g.M / 128) * (g.N / 128)), static_cast<unsigned>(g.batch),
+                    static_cast<unsigned>(splits));
     nt_gemm_simt<<<grid, kSimtThreads, 0, s>>>(a);
     ++*launches;
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && splits > 1) {
+        const int64_t quads = g.M * g.N / 4;
+        const unsigned rb = static_cast<unsigned>(std::min<int64_t>((quads + 255) / 256, 1024));
+        simt_reduce<<<dim3(rb, static_cast<unsigned>(g.batch)), 256, 0, s>>>(a, static_cast<int>(splits));
+        ++*launches;
+        e = cudaGetLastError();
+    }
     return e == cudaSuccess ? CAM_OK : launch_fail(e);
 }
 
@@ -1065,7 +1144,7 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
     }
     if (g0.precision == CAM_ORTHO_FP32) {
         for (int i = 0; i < n; ++i) {
-            const int rc = run_simt(gs[i], s, launches);
+            const int rc = run_simt(gs[i], sm_count, s, launches);
             if (rc != CAM_OK) return rc;
         }
         return CAM_OK;

@@ -353,6 +353,8 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
     g.Y = G0;
     g.ldy = rp;
     g.sY = sq;
+    g.partials = w->split;  // the CUDA-core kernel splits long K ranges
+    g.partial_floats = kSplitFloats;
     int rc = nt_gemm(&g, 1, sm_count, p.status, s, launches);
     if (rc != CAM_OK) return rc;
     const int64_t total = int64_t(B) * sq;
@@ -367,11 +369,15 @@ int short_side_iteration(OrthoWork* w, const OrthoParams& p, const Shape& sh, in
         g.Y = T;
         g.ldy = rp;
         g.sY = sq;
+        g.partials = w->split;
+        g.partial_floats = kSplitFloats;
         if ((rc = nt_gemm(&g, 1, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         g = nt(fp, kNtAxpby, B, rp, rp, rp, T, rp, sq, P, rp, sq);  // M = T P^T
         g.Y = M;
         g.ldy = rp;
         g.sY = sq;
+        g.partials = w->split;
+        g.partial_floats = kSplitFloats;
         if ((rc = nt_gemm(&g, 1, sm_count, p.status, s, launches)) != CAM_OK) return rc;
         // P'^T = 1.5 P^T - 0.5 P^T M (M symmetric), and P' beside it
         g = nt(fp, kNtAxpby, B, rp, rp, rp, Pt, rp, sq, M, rp, sq);
