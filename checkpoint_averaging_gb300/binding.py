@@ -28,9 +28,13 @@ TIME_COMMITS = 16
 NO_FUSED_FINISH = 32
 TEST_STALL_STAGED = 64  # test hook: staged passes withhold their first tile and time out
 SHARE_SMS = 128  # merge passes leave room on every SM for a round in flight beside them
+TEST_BAD_CHUNK = 256  # test hook: the first tensor's last chunk runs past its end on the device
+TEST_BAD_TAG = 512  # test hook: staged passes mislabel their first stage and stop
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 STATUS_GEMM_TIMEOUT = 2
+STATUS_BAD_CHUNK = 4
+STATUS_PROTOCOL = 8
 ORTHO_SCALE_FIXED, ORTHO_SCALE_MATCH_NORM = 0, 1
 ORTHO_TF32, ORTHO_FP32, ORTHO_BF16 = 0, 1, 2
 ORTHO_SHORT_SIDE = 4  # OR into the precision: iterate in the short side's space
@@ -476,7 +480,7 @@ class Merger:
                  n_fragments: int = 1, quorum: int = 1, init_ema_from_master=False,
                  zero_momentum=False, stream=None, swa=None, zero_swa=False, rows=None,
                  staging=True, time_commits=False, fused_finish=True, test_stall_staged=False,
-                 share_sms=False):
+                 share_sms=False, test_bad_chunk=False, test_bad_tag=False):
         """rows: optional per-tensor matrix rows (default: the tensors' first
         dimension), used by orthogonalised rounds. staging=False keeps every
         merge pass on the register form (the staged form gives the same
@@ -487,7 +491,12 @@ class Merger:
         merge pass to one register-form block per SM, so that rounds in flight
         on other streams run beside it (the same bits). test_stall_staged=True is a test hook
         (CAM_TEST_STALL_STAGED): staged passes withhold their first tile, their
-        waits give up after about 1 ms and status() reports the timeout."""
+        waits give up after about 1 ms and status() reports the timeout.
+        test_bad_chunk=True (CAM_TEST_BAD_CHUNK) and test_bad_tag=True
+        (CAM_TEST_BAD_TAG) are test hooks for the passes' own checks: a chunk
+        table whose first tensor's last chunk runs 2,048 elements past its end
+        (the caller's buffers of that tensor must have that room), and staged
+        passes whose first stage carries a wrong fill number."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)
@@ -515,7 +524,8 @@ class Merger:
                 (INIT_ZERO_MOMENTUM if zero_momentum else 0) | (INIT_ZERO_SWA if zero_swa else 0) | \
                 (0 if staging else NO_STAGING) | (TIME_COMMITS if time_commits else 0) | \
                 (0 if fused_finish else NO_FUSED_FINISH) | \
-                (TEST_STALL_STAGED if test_stall_staged else 0) | (SHARE_SMS if share_sms else 0)
+                (TEST_STALL_STAGED if test_stall_staged else 0) | (SHARE_SMS if share_sms else 0) | \
+                (TEST_BAD_CHUNK if test_bad_chunk else 0) | (TEST_BAD_TAG if test_bad_tag else 0)
         with torch.cuda.device(dev):
             self.ctx = ctx_create(
                 self.numel, [t.data_ptr() for t in self.master], fragment_of=self.fragment_of,

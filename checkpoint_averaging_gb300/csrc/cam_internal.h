@@ -40,6 +40,8 @@ constexpr int kFuseMaxChunks = 4096;
 
 // Bits of the context's device status word (cam_ctx_status).
 constexpr int32_t kStatusWaitTimeout = 1;  // a staged pass gave up waiting on a barrier
+constexpr int32_t kStatusBadChunk = 4;     // a merge pass met a chunk outside its tensor
+constexpr int32_t kStatusProtocol = 8;     // a staged pass found a stage out of sequence
 
 // One chunk of the fragment's element space: elements [start, start+len) of
 // the fragment's local tensor `local`. Chunks never straddle tensors.
@@ -92,11 +94,13 @@ struct MergeArgs {
     float W;                  // (float)sum tokens
     float lr, mu, beta;
     float swa_n;              // globals in the running average after this round
-    int32_t* status;          // device status word (kStatus* bits), staged pass only
+    int32_t* status;          // device status word (kStatus* bits)
     int32_t st_stages;        // staged pass: stages in the shared-memory ring
     int32_t st_stage_bytes;   // staged pass: bytes of one stage
     int32_t test_stall;       // staged pass, CAM_TEST_STALL_STAGED: withhold the first tile,
                               // give up waiting after kTestWaitLimitNs
+    int32_t test_tag;         // staged pass, CAM_TEST_BAD_TAG: tag the first tile with a
+                              // wrong sequence number, give up waiting after kTestWaitLimitNs
     // Register pass with the norm finish fused (MergeVariant::fin): the last
     // block to finish its chunks (counted on *fin_counter, which it resets to
     // 0) finishes the norms as the norm pass would, so that pass is not

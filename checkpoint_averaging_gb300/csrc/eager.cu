@@ -41,11 +41,12 @@ __global__ void __launch_bounds__(kThreads, 2) fold_worker(const __grid_constant
     __shared__ double part[2][kWarps];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
-        const ChunkDesc ch = a.chunks[c];
+        TensorSlot ts;
+        const ChunkDesc ch = checked_chunk(a, c, ts);
         const int l = ch.local - a.local0;
         const XT* x = static_cast<const XT*>(a.x[l]) + ch.start;
         float* s = a.sum[l] + ch.start;
-        const float* th = a.slots[ch.local].theta + ch.start;
+        const float* th = ts.theta + ch.start;
         float accw = 0.0f;
         int done = 0;
         if ((a.vec[l >> 5] >> (l & 31)) & 1u) {
@@ -105,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
     __shared__ double part_w[WD ? 2 : 1][WD ? CAM_KMAX : 1][kWarps];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
-        const ChunkDesc ch = a.chunks[c];
+        TensorSlot ts;
+        const ChunkDesc ch = checked_chunk(a, c, ts);
         const int l = ch.local - a.local0;
-        const TensorSlot ts = a.slots[ch.local];
         const void* const* tp = a.ptr + static_cast<int64_t>(l) * a.stride;
         const float* sum = static_cast<const float*>(tp[0]) + ch.start;
         const void* const* xs = tp + 3;  // the workers folded here

@@ -41,9 +41,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ double worker_part[2][WD ? kWarps * CAM_KMAX : 1];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
-        const ChunkDesc ch = a.chunks[c];
+        TensorSlot ts;
+        const ChunkDesc ch = checked_chunk(a, c, ts);
         const int l = ch.local - a.local0;
-        const TensorSlot ts = a.slots[ch.local];
         const void* const* xs = a.x + static_cast<int64_t>(l) * a.stride;
         const bool vec = (a.vec[l >> 5] >> (l & 31)) & 1u;
         float acc = 0.0f;

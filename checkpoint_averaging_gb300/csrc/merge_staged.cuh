@@ -46,6 +46,13 @@
 // mbarrier gives up after kWaitLimitNs: it then sets kStatusWaitTimeout in the
 // status word, and the producer waits (again with a limit) for the copies it
 // has issued before the block exits.
+//
+// Checks of the protocol itself: the producer checks each chunk against the
+// launch's tensors and a chunk that fails takes one stage marked kSkipTile
+// (kStatusBadChunk); every stage carries its fill number, which the consumers
+// compare with their own count, and every drift hand-over the count of
+// chunks handed over, which the reducer compares with its own. A mismatch
+// sets kStatusProtocol and stops the block as a timeout does.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -238,11 +245,17 @@ __device__ __forceinline__ void staged_vec4(const MergeArgs& a, const void* cons
 struct TileMeta {
     TensorSlot ts;
     int64_t i0;    // first element of the tile, within its tensor
-    int32_t len;   // elements in the tile; 0 marks the end of the block's work
+    int32_t len;   // elements in the tile; 0 marks the end of the block's work,
+                   // kSkipTile a chunk that failed the device-side checks
     int32_t l;     // launch-local tensor index
     int32_t last;  // 1 on the last tile of a chunk
-    int32_t pad;
+    int32_t seq;   // the stage's fill number (tiles, skips and the end marker in order)
 };
+
+// A chunk outside its launch or its tensor takes one stage of this length in
+// place of its tiles: nothing is copied or computed for it, and its drift
+// partials come out as 0.
+constexpr int32_t kSkipTile = -1;
 
 template <typename XT, int MODE, bool EMA, int NL, bool PUB, bool SWA>
 __global__ void __launch_bounds__(kStThreads, 1)
@@ -258,6 +271,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     __shared__ __align__(8) uint64_t red_full[kStRedSlots];
     __shared__ __align__(8) uint64_t red_empty[kStRedSlots];
     __shared__ TileMeta meta[kStMaxStages];
+    __shared__ int red_tag[kStRedSlots];  // the hand-over's chunk count, checked by the reducer
     __shared__ int abort_flag;
 
     const int P = a.st_stages;
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring0 = smem_u32(ring);
     volatile int* abort_v = &abort_flag;
-    const unsigned long long lim = a.test_stall ? kTestWaitLimitNs : kWaitLimitNs;
+    const unsigned long long lim = (a.test_stall || a.test_tag) ? kTestWaitLimitNs : kWaitLimitNs;
 
     if (warp == kProducerWarp) {
         // ---- producer: lane 0 walks the block's chunks and issues every
@@ -301,21 +315,26 @@ __global__ void __launch_bounds__(kStThreads, 1)
         // ahead so that its latency hides behind the current chunk's tiles.
         if (lane != 0) return;
         const uint64_t once = policy_evict_first();
-        int it = 0;  // stages filled so far (tiles and the end marker)
+        int it = 0;  // stages filled so far (tiles, skips and the end marker)
         bool ok = true;
         int c = blockIdx.x;
         ChunkDesc ch{}, chn{};
         TensorSlot ts{}, tsn{};
         if (c < a.n_chunks) {
             ch = a.chunks[c];
-            ts = a.slots[ch.local];
+            if (chunk_in_launch(ch, a.local0, a.n_local)) ts = a.slots[ch.local];
         }
         for (; ok && c < a.n_chunks; c += gridDim.x) {
             const bool has_next = c + static_cast<int>(gridDim.x) < a.n_chunks;
             if (has_next) chn = a.chunks[c + gridDim.x];
-            const int l = ch.local - a.local0;
+            const bool good = chunk_in_launch(ch, a.local0, a.n_local) && chunk_in_tensor(ch, ts);
+            if (!good) atomicOr(a.status, kStatusBadChunk);
+            const int l = good ? ch.local - a.local0 : 0;
             const void* const* xs = a.x + static_cast<int64_t>(l) * a.stride;
-            for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
+            const int tiles =
+                good ? static_cast<int>((static_cast<int64_t>(ch.len) + kStTile - 1) / kStTile) : 1;
+            for (int t = 0; t < tiles; ++t, ++it) {
+                const int t0 = t * kStTile;
                 const int s = it % P, n = it / P;
                 // the stage's previous tile must be released by every consumer warp
                 if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) {
@@ -326,20 +345,22 @@ __global__ void __launch_bounds__(kStThreads, 1)
                     ok = false;
                     break;
                 }
-                const int len = min(kStTile, ch.len - t0);
-                const int len8 = len & ~7;
+                const int len = good ? min(kStTile, ch.len - t0) : kSkipTile;
+                const int len8 = good ? len & ~7 : 0;
                 const int64_t i0 = ch.start + t0;
                 TileMeta& mt = meta[s];
                 mt.ts = ts;
                 mt.i0 = i0;
                 mt.len = len;
                 mt.l = l;
-                mt.last = t0 + kStTile >= ch.len;
+                mt.last = t + 1 == tiles;
+                // (test hook: the first stage carries a wrong fill number)
+                mt.seq = (a.test_tag && it == 0) ? -1 : it;
                 const uint32_t bar = smem_u32(&full[s]);
                 if (a.test_stall && it == 0) {
                     // test hook: the first tile is never issued, so its
                     // consumers' waits run out
-                } else if (len8 == 0) {  // a tensor of fewer than 8 elements: nothing to copy
+                } else if (len8 == 0) {  // skipped, or fewer than 8 elements: nothing to copy
                     mbar_arrive(bar);
                 } else {
                     const uint32_t st = ring0 + s * stage_bytes;
@@ -353,7 +374,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
                     if (EMA) bulk_load(st + L.e, ts.e + i0, sb, bar);
                     if constexpr (SWA) bulk_load(st + L.sw, ts.swa + i0, sb, bar);
                 }
-                if (t0 == 0 && has_next) tsn = a.slots[chn.local];
+                if (t == 0 && has_next)
+                    tsn = chunk_in_launch(chn, a.local0, a.n_local) ? a.slots[chn.local] : TensorSlot{};
             }
             ch = chn;
             ts = tsn;
@@ -363,6 +385,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
             if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) ok = false;
             if (ok) {
                 meta[s].len = 0;
+                meta[s].seq = it;
                 mbar_arrive(smem_u32(&full[s]));
                 ++it;
             }
@@ -393,6 +416,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
                 if (!mbar_wait(smem_u32(&red_full[slot]), use & 1, lim)) {
                     *abort_v = 1;
                     atomicOr(a.status, kStatusWaitTimeout);
+                    return;
+                }
+                if (red_tag[slot] != ci) {  // the consumers handed over another chunk
+                    *abort_v = 1;
+                    if (lane == 0) atomicOr(a.status, kStatusProtocol);
                     return;
                 }
                 const float* rb = red + slot * nq * kStConsumers;
@@ -437,16 +465,24 @@ __global__ void __launch_bounds__(kStThreads, 1)
             if (WD && k < a.K) rb[(1 + k) * kStConsumers + g] = accw[k];
             accw[k] = 0.0f;
         }
+        if (g == 0) red_tag[slot] = ci;  // before warp 0's arrival
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&red_full[slot]));
         return true;
     };
     // Waits for stage s's use n; false (with the abort flag set) on a timeout.
-    auto wait_full = [&](int s, int n) -> bool {
+    // Then checks that the stage holds fill number it (= n P + s): a stage
+    // out of sequence sets kStatusProtocol and stops the block like a timeout.
+    auto wait_full = [&](int s, int n, int it) -> bool {
         if (*abort_v) return false;
         if (!mbar_wait(smem_u32(&full[s]), n & 1, lim)) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
+            return false;
+        }
+        if (meta[s].seq != it) {
+            *abort_v = 1;
+            if (lane == 0) atomicOr(a.status, kStatusProtocol);
             return false;
         }
         return true;
@@ -458,29 +494,40 @@ __global__ void __launch_bounds__(kStThreads, 1)
         // chunks themselves and keep each chunk's pointers in registers, which
         // measured faster than reading the per-tile descriptor; they only
         // release the producer's end marker at the end.
+        // They check each chunk as the producer does: one stage, nothing
+        // computed, for a chunk that fails.
         int it = 0, ci = 0;
         for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++ci) {
             const ChunkDesc ch = a.chunks[c];
-            const TensorSlot ts = a.slots[ch.local];
-            const void* const* xs = a.x + static_cast<int64_t>(ch.local - a.local0) * a.stride;
-            for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
+            const bool in_launch = chunk_in_launch(ch, a.local0, a.n_local);
+            const TensorSlot ts = in_launch ? a.slots[ch.local] : TensorSlot{};
+            const bool good = in_launch && chunk_in_tensor(ch, ts);
+            const void* const* xs =
+                a.x + static_cast<int64_t>(good ? ch.local - a.local0 : 0) * a.stride;
+            const int tiles =
+                good ? static_cast<int>((static_cast<int64_t>(ch.len) + kStTile - 1) / kStTile) : 1;
+            for (int t = 0; t < tiles; ++t, ++it) {
                 const int s = it % P;
-                if (!wait_full(s, it / P)) return;
-                const int len = min(kStTile, ch.len - t0);
-                const int len8 = len & ~7;
-                const int64_t i0 = ch.start + t0;
-                if (4 * g < len8)
-                    staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(
-                        a, xs, ts, ring0 + s * stage_bytes, L, i0 + 4 * g, 4 * g, acc, accw);
-                if (g < len - len8)  // the ragged end, straight from global memory
-                    merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc, accw);
+                if (!wait_full(s, it / P, it)) return;
+                if (good) {
+                    const int t0 = t * kStTile;
+                    const int len = min(kStTile, ch.len - t0);
+                    const int len8 = len & ~7;
+                    const int64_t i0 = ch.start + t0;
+                    if (4 * g < len8)
+                        staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(
+                            a, xs, ts, ring0 + s * stage_bytes, L, i0 + 4 * g, 4 * g, acc, accw);
+                    if (g < len - len8)  // the ragged end, straight from global memory
+                        merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc,
+                                                                     accw);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
             if (!hand_over(ci)) return;
         }
         const int s = it % P;  // the end marker
-        if (!wait_full(s, it / P)) return;
+        if (!wait_full(s, it / P, it)) return;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     } else {
@@ -488,12 +535,18 @@ __global__ void __launch_bounds__(kStThreads, 1)
         // stages, reading each tile's descriptor, until the end marker.
         for (int it = 0, ci = 0;; ++it) {
             const int s = it % P;
-            if (!wait_full(s, it / P)) return;
+            if (!wait_full(s, it / P, it)) return;
             const int len = meta[s].len;
             if (len == 0) {  // end marker: release it and stop
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
                 return;
+            }
+            if (len == kSkipTile) {  // a chunk that failed the checks: its partials are 0
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                if (NORM && !hand_over(ci++)) return;
+                continue;
             }
             const TensorSlot ts = meta[s].ts;
             const int64_t i0 = meta[s].i0;

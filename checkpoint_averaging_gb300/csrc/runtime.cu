@@ -136,6 +136,7 @@ struct cam_ctx {
     bool pageable_access = false;  // the GPU reads pageable host memory directly
     bool staged = true;            // the staged form of the merge pass may be used
     bool test_stall = false;       // CAM_TEST_STALL_STAGED
+    bool test_tag = false;         // CAM_TEST_BAD_TAG
     bool share_sms = false;        // CAM_SHARE_SMS: one register-form block per SM at most
     bool time_commits = false;     // CAM_TIME_COMMITS: events around each commit
     cudaEvent_t commit_ev[2] = {nullptr, nullptr};
@@ -258,6 +259,14 @@ bool check_plan(const Plan& p, const cam_ctx& c) {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Elements of the running-sum buffer (tensors in order, each rounded up to 8
+// elements) after the end of tensor g's own.
+int64_t sum_room_after(const cam_ctx& c, int32_t g) {
+    int64_t room = (c.numel[g] + 7) / 8 * 8 - c.numel[g];
+    for (int32_t t = g + 1; t < c.n_tensors; ++t) room += (c.numel[t] + 7) / 8 * 8;
+    return room;
+}
+
 int validate_desc(const cam_ctx_desc* d) {
     if (!d) return fail(CAM_E_ARG, "cam_ctx_create: desc is NULL");
     if (d->n_tensors < 1) return fail(CAM_E_ARG, "cam_ctx_create: n_tensors must be >= 1");
@@ -268,7 +277,8 @@ int validate_desc(const cam_ctx_desc* d) {
     if (d->device < 0) return fail(CAM_E_ARG, "cam_ctx_create: device must be >= 0");
     if (d->flags & ~(CAM_INIT_EMA_FROM_MASTER | CAM_INIT_ZERO_MOMENTUM | CAM_INIT_ZERO_SWA |
                      CAM_NO_STAGING | CAM_TIME_COMMITS | CAM_NO_FUSED_FINISH |
-                     CAM_TEST_STALL_STAGED | CAM_SHARE_SMS))
+                     CAM_TEST_STALL_STAGED | CAM_SHARE_SMS | CAM_TEST_BAD_CHUNK |
+                     CAM_TEST_BAD_TAG))
         return fail(CAM_E_ARG, "cam_ctx_create: unknown flags 0x%x", d->flags);
     if ((d->flags & CAM_INIT_EMA_FROM_MASTER) && !d->ema)
         return fail(CAM_E_ARG, "cam_ctx_create: CAM_INIT_EMA_FROM_MASTER without EMA buffers");
@@ -402,6 +412,15 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
         size_t o;
         o = carve(sizeof(ChunkDesc) * p.chunks.size());
         if (!p.chunks.empty()) std::memcpy(&host[o], p.chunks.data(), sizeof(ChunkDesc) * p.chunks.size());
+        if ((d->flags & CAM_TEST_BAD_CHUNK) && p.tensors.size() >= 2 && p.first_chunk[1] > 0 &&
+            sum_room_after(*c, p.tensors[0]) >= cam::kChunkQuantum) {
+            // test hook: the device copy of the first tensor's last chunk runs
+            // one chunk quantum past the tensor's end (inside the running-sum
+            // buffer too, which holds the tensors in order)
+            ChunkDesc bad = p.chunks[p.first_chunk[1] - 1];
+            bad.len += cam::kChunkQuantum;
+            std::memcpy(&host[o + sizeof(ChunkDesc) * (p.first_chunk[1] - 1)], &bad, sizeof bad);
+        }
         p.d_chunks = reinterpret_cast<ChunkDesc*>(static_cast<unsigned char*>(c->dev_block) + o);
         o = carve(sizeof(TensorSlot) * slots.size());
         if (!slots.empty()) std::memcpy(&host[o], slots.data(), sizeof(TensorSlot) * slots.size());
@@ -447,6 +466,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     c->fuse_finish = !(d->flags & CAM_NO_FUSED_FINISH);
     c->staged = !(d->flags & CAM_NO_STAGING);
     c->test_stall = (d->flags & CAM_TEST_STALL_STAGED) != 0;
+    c->test_tag = (d->flags & CAM_TEST_BAD_TAG) != 0;
     c->share_sms = (d->flags & CAM_SHARE_SMS) != 0;
     c->time_commits = (d->flags & CAM_TIME_COMMITS) != 0;
     for (int i = 0; c->time_commits && i < 2 && ce == cudaSuccess; ++i)
@@ -729,6 +749,7 @@ CAM_API int cam_merge_fold(cam_round* r, const void* const* ckpt, cam_dtype dtyp
     const bool wd = r->worker_norms;
     cam::FoldArgs a;
     a.slots = p.d_slots;
+    a.status = c->d_status;
     a.k = k;
     a.first = k == 0;
     a.w = static_cast<float>(tokens);
@@ -1011,6 +1032,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.st_stages = st_stages;
     a.st_stage_bytes = static_cast<int32_t>(st_bytes);
     a.test_stall = c->test_stall ? 1 : 0;
+    a.test_tag = c->test_tag ? 1 : 0;
     // Fused pass over the fragment's local tensors [lb, le).
     auto launch_range = [&](int lb, int le) {
         for (int l0 = lb; l0 < le && ce == cudaSuccess; l0 += per_launch) {
@@ -1066,6 +1088,7 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     auto launch_final = [&]() {
         cam::FinalArgs fa;
         fa.slots = p.d_slots;
+        fa.status = c->d_status;
         fa.K = K;
         fa.Kf = a.Kf;
         fa.W = a.W;

@@ -19,6 +19,7 @@ struct FoldArgs {
     const ChunkDesc* chunks;   // first chunk of this launch (device)
     const TensorSlot* slots;   // the fragment's tensors, by local index (device)
     double* worker_partials;   // [chunk * CAM_KMAX + k]: this worker's drift partials, or null
+    int32_t* status;           // device status word (kStatus* bits)
     int32_t n_chunks;
     int32_t local0;
     int32_t n_local;
@@ -40,6 +41,7 @@ struct FinalArgs {
     const ChunkDesc* chunks;
     const TensorSlot* slots;
     double* partials;          // drift partial per chunk of this launch, or null
+    int32_t* status;           // device status word (kStatus* bits)
     int32_t n_chunks;
     int32_t local0;
     int32_t n_local;

@@ -107,10 +107,20 @@ typedef enum {
 #define CAM_SHARE_SMS 128u          /* merge passes take at most one register-form block per SM,
                                        leaving room beside them for a round in flight on another
                                        stream (small fragment rounds run alongside) */
+#define CAM_TEST_BAD_CHUNK 256u     /* test hook, never for real rounds: the device copy of the
+                                       chunk table runs the first tensor's last chunk 2,048
+                                       elements past that tensor's end (see cam_ctx_status) */
+#define CAM_TEST_BAD_TAG 512u       /* test hook, never for real rounds: every staged merge pass
+                                       tags its first stage with a wrong fill number and gives up
+                                       waiting after about 1 ms (see cam_ctx_status) */
 
 /* Bits of the device status word (cam_ctx_status) */
 #define CAM_STATUS_WAIT_TIMEOUT 1 /* a staged merge pass gave up waiting for its copies */
 #define CAM_STATUS_GEMM_TIMEOUT 2 /* a tensor-core GEMM of the orthogonalisation gave up waiting */
+#define CAM_STATUS_BAD_CHUNK 4    /* a merge or fold pass met a chunk outside its tensor and
+                                     skipped it */
+#define CAM_STATUS_PROTOCOL 8     /* a staged merge pass found a stage or a drift hand-over out
+                                     of sequence and stopped */
 
 /* cam_merge_orthogonalize */
 #define CAM_ORTHO_SCALE_FIXED 0      /* theta' = theta + lr * polar(Delta) */
@@ -462,6 +472,24 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * the status word reports the timeout. It exists to test this failure path
  * without hanging or faulting the GPU; the buffers of such a round are
  * left partly written.
+ *
+ * The merge and fold passes also check every chunk of the context's tables
+ * as they take it: its tensor among the launch's, at least one element, all
+ * of them inside the tensor. The tables are built and checked on the host at
+ * cam_ctx_create, so a chunk fails only if its table was corrupted in device
+ * memory; the pass then reads and writes nothing for that chunk, counts its
+ * drift as 0, and sets CAM_STATUS_BAD_CHUNK. A context created with
+ * CAM_TEST_BAD_CHUNK plants such a chunk (in every table of two or more
+ * tensors, the first tensor's last chunk reaches 2,048 elements past its
+ * end) to test this; the caller gives that tensor's buffers (state, workers
+ * and published copies) 2,048 spare elements past its end, so that even an
+ * unchecked pass would stay inside them. The staged form further checks its
+ * own protocol: each stage of its ring carries its fill number and each
+ * drift hand-over its chunk count, compared by the warps that take them; a
+ * mismatch sets CAM_STATUS_PROTOCOL and stops the pass as a timeout does. A
+ * context created with CAM_TEST_BAD_TAG has every staged pass mislabel its
+ * first stage to test this (its waits give up after about 1 ms, as with
+ * CAM_TEST_STALL_STAGED).
  *
  * cam_ctx_status waits for all work on the context's device, then writes the
  * word (0: nothing went wrong) to *out. The word stays set once set.

@@ -66,7 +66,8 @@ class GpuState:
 
 
 def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
-                   fused_finish=True, test_stall_staged=False, share_sms=False) -> GpuState:
+                   fused_finish=True, test_stall_staged=False, share_sms=False,
+                   test_bad_chunk=False, test_bad_tag=False) -> GpuState:
     theta = W.empty_arena(g.numels, torch.float32, dev)
     theta.flat.copy_(g.flat)
     m = W.empty_arena(g.numels, torch.float32, dev) if wl.mode == "delta" else None
@@ -80,7 +81,7 @@ def make_gpu_state(wl: W.Workload, g: W.Arena, dev, quorum=None, staging=True,
                   n_fragments=wl.n_fragments, quorum=wl.quorum if quorum is None else quorum,
                   swa=None if swa is None else swa.views, staging=staging,
                   fused_finish=fused_finish, test_stall_staged=test_stall_staged,
-                  share_sms=share_sms)
+                  share_sms=share_sms, test_bad_chunk=test_bad_chunk, test_bad_tag=test_bad_tag)
     return GpuState(theta, m, e, mg, swa)
 
 

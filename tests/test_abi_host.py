@@ -58,7 +58,7 @@ def test_version():
     (dict(n_fragments=0), "n_fragments"),
     (dict(fragment_of=[3], n_fragments=2), "fragment_of"),
     (dict(device=-1), "device"),
-    (dict(flags=256), "flags"),
+    (dict(flags=1024), "flags"),
     (dict(flags=B.INIT_EMA_FROM_MASTER), "EMA"),
     (dict(flags=B.INIT_ZERO_MOMENTUM), "momentum"),
 ])

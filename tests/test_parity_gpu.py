@@ -1172,6 +1172,91 @@ def test_staged_wait_that_runs_out_is_reported_and_the_device_recovers(mode, nor
     fresh.merger.close()
 
 
+@pytest.mark.parametrize("form", ["register_fin", "register", "staged", "fold"])
+def test_corrupted_chunk_is_skipped_and_reported(form):
+    """The passes' own chunk checks, met on purpose: with CAM_TEST_BAD_CHUNK
+    the device copy of the chunk table has the first tensor's last chunk reach
+    2,048 elements past that tensor's end. The arena puts the next tensor
+    there, so even an unchecked pass would stay inside the allocations (and
+    show up as wrong values in that tensor). Every form -- the register pass
+    with and without its fused norm finish, the staged pass and the eager
+    folds with their final pass -- must skip the chunk: its elements keep
+    their values, its drift counts as 0, CAM_STATUS_BAD_CHUNK is set, and
+    everything else equals the oracle run on the list without that chunk."""
+    wl = _custom([300_000, 70_000, 2049], K=2, mode="delta", ema=False, norms=True)
+    g = W.make_global(wl, 0, DEV)
+    assert g.offsets[1] + g.numels[1] >= g.numels[0] + 2048  # room for the overrun
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
+    st = make_gpu_state(wl, g, DEV, staging=form == "staged",
+                        fused_finish=form == "register_fin", test_bad_chunk=True)
+    n0 = st.merger.staged_count
+    pt, pf = gpu_round(st, wl, 0, -1, workers, draw, fold=form == "fold")
+    torch.cuda.synchronize()
+    assert (st.merger.staged_count - n0 > 0) == (form == "staged")
+    assert st.merger.status() == B.STATUS_BAD_CHUNK
+    # the skipped chunk: the trailing run of tensor 0 that kept its bits
+    g0 = to_np(g.views[0])
+    th0 = to_np(st.theta.views[0])
+    same = th0.view(np.uint32) == g0.view(np.uint32)
+    s = len(same) - int(np.argmin(same[::-1])) if not same.all() else 0
+    assert 0 < s < len(g0) and s % 2048 == 0, s
+    assert not same[:s].any()
+    assert (to_np(st.m.views[0])[s:] == 0).all()
+    # what lies between tensor 0's end and tensor 1 kept its bits
+    gap = slice(g.numels[0], g.offsets[1])
+    assert torch.equal(st.theta.flat[gap].view(torch.int32), g.flat[gap].view(torch.int32))
+    assert (st.m.flat[gap] == 0).all()
+    # the oracle on the list without the skipped chunk
+    ost = oracle.OracleState(
+        theta=[g0[:s].copy()] + [to_np(v).copy() for v in g.views[1:]],
+        m=[np.zeros(s, np.float32)] + [np.zeros(n, np.float32) for n in g.numels[1:]],
+        fragment_of=wl.fragment_of)
+    ck = [[to_np(w.views[0])[:s]] + [to_np(v) for v in w.views[1:]] for w in workers]
+    pt_want, pf_want = oracle.merge_round(
+        ost, round=0, fragment=-1, ckpts=ck, included=draw.included, tokens=draw.tokens,
+        mode=oracle.DELTA_NESTEROV, lr=wl.lr, mu=wl.mu, quorum=wl.quorum, ema_beta=None,
+        swa_update=False)
+    assert_close(th0[:s], ost.theta[0], "theta, tensor 0 before the skipped chunk")
+    assert_close(to_np(st.m.views[0])[:s], ost.m[0], "m, tensor 0 before the skipped chunk")
+    for t in (1, 2):
+        assert_close(to_np(st.theta.views[t]), ost.theta[t], f"theta, tensor {t}")
+        assert_close(to_np(st.m.views[t]), ost.m[t], f"m, tensor {t}")
+    got = pt.cpu().numpy()
+    want = np.asarray(pt_want)
+    assert np.all(np.abs(got - want) <= NORM_RTOL * np.abs(want)), (got, want)
+    assert abs(pf.item() - pf_want) <= NORM_RTOL * abs(pf_want)
+    st.merger.close()
+
+
+@pytest.mark.parametrize("mode,norms", [("mean", False), ("delta", True)])
+def test_staged_stage_out_of_sequence_is_reported(mode, norms):
+    """The staged pass's protocol check, met on purpose: with CAM_TEST_BAD_TAG
+    every staged pass labels its first stage with a wrong fill number. The
+    consumers find it, set CAM_STATUS_PROTOCOL and stop before touching the
+    stage; the producer's and the reducer's waits then give up after about
+    1 ms with every copy landed. Nothing faults or hangs, and a fresh context
+    on the same device runs the round like the oracle."""
+    wl = _custom([300_000, 70_000, 2049], K=2, mode=mode, ema=mode == "mean", norms=norms)
+    g = W.make_global(wl, 0, DEV)
+    draw = W.draw_round(wl, 0, 0)
+    workers = [W.make_worker(wl, g, 0, k, 0, DEV) for k in range(wl.K)]
+    st = make_gpu_state(wl, g, DEV, fused_finish=False, test_bad_tag=True)
+    n0 = st.merger.staged_count
+    gpu_round(st, wl, 0, -1, workers, draw)
+    torch.cuda.synchronize()
+    assert st.merger.staged_count - n0 > 0
+    assert st.merger.status() & B.STATUS_PROTOCOL
+    st.merger.close()
+    fresh = make_gpu_state(wl, g, DEV, fused_finish=False)
+    gpu_round(fresh, wl, 0, -1, workers, draw)
+    ost = oracle_state_from(g, wl)
+    oracle_round(ost, wl, 0, -1, workers, draw)
+    compare_full(fresh, ost, f"after a pass stopped on its protocol check: {mode}")
+    assert fresh.merger.status() == 0
+    fresh.merger.close()
+
+
 @pytest.mark.parametrize("mode,ema,swa,host,staging,want_staged", [
     ("mean", True, False, False, True, True),     # theta, e written
     ("delta", False, False, False, True, True),   # theta, m written
