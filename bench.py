@@ -945,7 +945,11 @@ def run_ortho(args, wl, ws, rank, local) -> int:
     n_mat = sum(1 for sp in wl.specs if len(sp.shape) == 2)
     peaks = measured_peaks()
     bf16 = peaks.get("bf16_tflops_sustained") or 1700.0
-    peak = {B.ORTHO_TF32: bf16 * (1.1 / 2.25), B.ORTHO_BF16: bf16}.get(prec)
+    # fp32 on the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops (an FMA) x
+    # the 2,070 MHz maximum SM clock
+    fp32_alu = 152 * 128 * 2 * 2.07e9 / 1e12
+    peak = {B.ORTHO_TF32: bf16 * (1.1 / 2.25), B.ORTHO_BF16: bf16,
+            B.ORTHO_FP32: fp32_alu}[prec]
     tflops = flops / t / 1e12
     exec_tflops = executed / t / 1e12
     mg.close()
@@ -958,12 +962,15 @@ def run_ortho(args, wl, ws, rank, local) -> int:
                    "n_params": wl.n_params, "K": wl.K, "flops_per_step": flops,
                    "executed_flops_per_step": executed,
                    "matrices": n_mat, "short_side": bool(args.ortho_short_side)},
-        "roofline": {"bound": "tensor", "achieved": round(exec_tflops, 2),
-                     "peak": None if peak is None else round(peak, 1), "unit": "TFLOP/s",
-                     "frac": None if peak is None else round(exec_tflops / peak, 4),
+        "roofline": {"bound": "alu" if prec == B.ORTHO_FP32 else "tensor",
+                     "achieved": round(exec_tflops, 2),
+                     "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(exec_tflops / peak, 4),
                      "achieved_from": "executed flops (padded, Gram upper-triangle tiles) over "
                                       "the whole round's time, streaming kernels included",
                      "peak_source": ("measured bf16 sustained" if prec == B.ORTHO_BF16 else
+                                     "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (nominal)"
+                                     if prec == B.ORTHO_FP32 else
                                      "measured bf16 sustained x nominal tf32/bf16 (1.1/2.25)")
                      + ("; the short-side form runs its r x r products in fp32"
                         if args.ortho_short_side else ""),

@@ -29,7 +29,7 @@ NO_FUSED_FINISH = 32
 TEST_STALL_STAGED = 64  # test hook: staged passes withhold their first tile and time out
 SHARE_SMS = 128  # merge passes leave room on every SM for a round in flight beside them
 TEST_BAD_CHUNK = 256  # test hook: the first tensor's last chunk runs past its end on the device
-TEST_BAD_TAG = 512  # test hook: staged passes mislabel their first stage and stop
+TEST_BAD_TAG = 512  # test hook: staged passes mislabel their end marker and stop
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
 STATUS_WAIT_TIMEOUT = 1
 STATUS_GEMM_TIMEOUT = 2
@@ -496,7 +496,7 @@ class Merger:
         (CAM_TEST_BAD_TAG) are test hooks for the passes' own checks: a chunk
         table whose first tensor's last chunk runs 2,048 elements past its end
         (the caller's buffers of that tensor must have that room), and staged
-        passes whose first stage carries a wrong fill number."""
+        passes whose end marker carries a wrong fill number."""
         torch = _torch()
         self.master = list(master)
         self.momentum = None if momentum is None else list(momentum)

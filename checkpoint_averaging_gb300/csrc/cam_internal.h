@@ -99,8 +99,8 @@ struct MergeArgs {
     int32_t st_stage_bytes;   // staged pass: bytes of one stage
     int32_t test_stall;       // staged pass, CAM_TEST_STALL_STAGED: withhold the first tile,
                               // give up waiting after kTestWaitLimitNs
-    int32_t test_tag;         // staged pass, CAM_TEST_BAD_TAG: tag the first tile with a
-                              // wrong sequence number, give up waiting after kTestWaitLimitNs
+    int32_t test_tag;         // staged pass, CAM_TEST_BAD_TAG: give the end marker a wrong
+                              // fill number, give up waiting after kTestWaitLimitNs
     // Register pass with the norm finish fused (MergeVariant::fin): the last
     // block to finish its chunks (counted on *fin_counter, which it resets to
     // 0) finishes the norms as the norm pass would, so that pass is not

@@ -41,8 +41,17 @@ __global__ void __launch_bounds__(kThreads, 2) fold_worker(const __grid_constant
     __shared__ double part[2][kWarps];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
-        TensorSlot ts;
-        const ChunkDesc ch = checked_chunk(a, c, ts);
+        const ChunkDesc ch = a.chunks[c];
+        const bool in_launch = chunk_in_launch(ch, a.local0, a.n_local);
+        const TensorSlot ts = a.slots[in_launch ? ch.local : a.local0];
+        if (!in_launch || !chunk_in_tensor(ch, ts)) {  // skipped, its partial 0
+            if (threadIdx.x == 0) {
+                atomicOr(a.status, kStatusBadChunk);
+                if (WD) a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + a.k] = 0.0;
+            }
+            parity ^= 1;  // the slots stay as they were: no barrier for this chunk
+            continue;
+        }
         const int l = ch.local - a.local0;
         const XT* x = static_cast<const XT*>(a.x[l]) + ch.start;
         float* s = a.sum[l] + ch.start;
@@ -106,8 +115,19 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
     __shared__ double part_w[WD ? 2 : 1][WD ? CAM_KMAX : 1][kWarps];
     int parity = 0;
     for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, parity ^= 1) {
-        TensorSlot ts;
-        const ChunkDesc ch = checked_chunk(a, c, ts);
+        const ChunkDesc ch = a.chunks[c];
+        const bool in_launch = chunk_in_launch(ch, a.local0, a.n_local);
+        const TensorSlot ts = a.slots[in_launch ? ch.local : a.local0];
+        if (!in_launch || !chunk_in_tensor(ch, ts)) {  // skipped, its partials 0
+            if (threadIdx.x == 0) {
+                atomicOr(a.status, kStatusBadChunk);
+                if (NORM) a.partials[c] = 0.0;
+                for (int p = 0; WD && p < a.P; ++p)
+                    a.worker_partials[static_cast<int64_t>(c) * CAM_KMAX + a.first_k + p] = 0.0;
+            }
+            parity ^= 1;  // the slots stay as they were: no barrier for this chunk
+            continue;
+        }
         const int l = ch.local - a.local0;
         const void* const* tp = a.ptr + static_cast<int64_t>(l) * a.stride;
         const float* sum = static_cast<const float*>(tp[0]) + ch.start;

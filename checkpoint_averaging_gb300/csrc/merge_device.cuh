@@ -24,7 +24,9 @@ constexpr int kDelta = CAM_MODE_DELTA_NESTEROV;
 // The host builds every chunk table and checks it once (each tensor's chunks
 // inside it, in order, without gaps); the passes check each chunk again as
 // they take it, at the cost of a compare per chunk, so that a corrupted table
-// is reported instead of read or written through.
+// is reported (kStatusBadChunk) and the chunk skipped instead of read or
+// written through. A pass loads the chunk's slot once, from the launch's
+// first tensor when the chunk names another, before checking it.
 
 // Chunk ch's tensor is one of the launch's, [local0, local0 + n_local): only
 // then may its slot be read.
@@ -36,27 +38,6 @@ __device__ __forceinline__ bool chunk_in_launch(const ChunkDesc& ch, int32_t loc
 // At least one element, all of them inside the tensor of slot ts.
 __device__ __forceinline__ bool chunk_in_tensor(const ChunkDesc& ch, const TensorSlot& ts) {
     return ch.start >= 0 && ch.len > 0 && ch.start <= ts.numel - ch.len;
-}
-
-// Chunk c of a register-form launch and its tensor's slot. A chunk that fails
-// either check sets kStatusBadChunk and comes back empty (length 0, the
-// launch's first tensor, a zero slot): the pass reads and writes nothing for
-// it, and its drift partials come out as 0. Every thread of the block takes
-// the same decision. The argument block A provides chunks, slots, local0,
-// n_local and status.
-template <typename A>
-__device__ __forceinline__ ChunkDesc checked_chunk(const A& a, int c, TensorSlot& ts) {
-    ChunkDesc ch = a.chunks[c];
-    const bool in_launch = chunk_in_launch(ch, a.local0, a.n_local);
-    ts = in_launch ? a.slots[ch.local] : TensorSlot{};
-    if (!in_launch || !chunk_in_tensor(ch, ts)) {
-        if (threadIdx.x == 0) atomicOr(a.status, kStatusBadChunk);
-        ch.start = 0;
-        ch.local = a.local0;
-        ch.len = 0;
-        ts = TensorSlot{};
-    }
-    return ch;
 }
 
 // ---- memory access -----------------------------------------------------------

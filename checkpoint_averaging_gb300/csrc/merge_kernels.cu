@@ -36,7 +36,7 @@ namespace {
 
 using namespace cam::dev;
 
-__global__ void __launch_bounds__(1024) norm_finish(const NormArgs a) {
+__global__ void __launch_bounds__(512) norm_finish(const NormArgs a) {
     finish_norms<false>(a);
 }
 
@@ -127,7 +127,7 @@ int merge_blocks_per_sm(const MergeVariant& v) {
 }
 
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s) {
-    norm_finish<<<1, 1024, 0, s>>>(a);
+    norm_finish<<<1, 512, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -48,11 +48,14 @@
 // has issued before the block exits.
 //
 // Checks of the protocol itself: the producer checks each chunk against the
-// launch's tensors and a chunk that fails takes one stage marked kSkipTile
-// (kStatusBadChunk); every stage carries its fill number, which the consumers
-// compare with their own count, and every drift hand-over the count of
-// chunks handed over, which the reducer compares with its own. A mismatch
-// sets kStatusProtocol and stops the block as a timeout does.
+// launch's tensors and a chunk that fails takes one empty stage marked as the
+// last of its chunk instead of its tiles (kStatusBadChunk); the end marker
+// carries the number of stages filled before it, which the consumers compare
+// with their own count of stages taken; every drift hand-over carries the
+// count of chunks handed over, which the reducer compares with its own. A
+// mismatch sets kStatusProtocol and stops the block as a timeout does. (The
+// consumers check the end marker only: they are issue-bound on some variants,
+// where a compare per tile measured 1 %.)
 #pragma once
 
 #include <cuda_runtime.h>
@@ -245,17 +248,13 @@ __device__ __forceinline__ void staged_vec4(const MergeArgs& a, const void* cons
 struct TileMeta {
     TensorSlot ts;
     int64_t i0;    // first element of the tile, within its tensor
-    int32_t len;   // elements in the tile; 0 marks the end of the block's work,
-                   // kSkipTile a chunk that failed the device-side checks
+    int32_t len;   // elements in the tile; 0 with last = 0 marks the end of the
+                   // block's work, 0 with last = 1 a chunk that failed the
+                   // device-side checks (nothing to compute, a zero partial)
     int32_t l;     // launch-local tensor index
     int32_t last;  // 1 on the last tile of a chunk
-    int32_t seq;   // the stage's fill number (tiles, skips and the end marker in order)
+    int32_t seq;   // end marker only: the stages filled before it
 };
-
-// A chunk outside its launch or its tensor takes one stage of this length in
-// place of its tiles: nothing is copied or computed for it, and its drift
-// partials come out as 0.
-constexpr int32_t kSkipTile = -1;
 
 template <typename XT, int MODE, bool EMA, int NL, bool PUB, bool SWA>
 __global__ void __launch_bounds__(kStThreads, 1)
@@ -327,14 +326,28 @@ __global__ void __launch_bounds__(kStThreads, 1)
         for (; ok && c < a.n_chunks; c += gridDim.x) {
             const bool has_next = c + static_cast<int>(gridDim.x) < a.n_chunks;
             if (has_next) chn = a.chunks[c + gridDim.x];
-            const bool good = chunk_in_launch(ch, a.local0, a.n_local) && chunk_in_tensor(ch, ts);
-            if (!good) atomicOr(a.status, kStatusBadChunk);
-            const int l = good ? ch.local - a.local0 : 0;
+            if (!chunk_in_launch(ch, a.local0, a.n_local) || !chunk_in_tensor(ch, ts)) {
+                // a chunk that fails the checks: one empty stage, marked as
+                // the last of its chunk, in place of its tiles
+                atomicOr(a.status, kStatusBadChunk);
+                const int s = it % P, n = it / P;
+                if ((n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) || *abort_v) {
+                    ok = false;
+                    break;
+                }
+                meta[s].len = 0;
+                meta[s].last = 1;
+                mbar_arrive(smem_u32(&full[s]));
+                ++it;
+                if (has_next)
+                    tsn = chunk_in_launch(chn, a.local0, a.n_local) ? a.slots[chn.local] : TensorSlot{};
+                ch = chn;
+                ts = tsn;
+                continue;
+            }
+            const int l = ch.local - a.local0;
             const void* const* xs = a.x + static_cast<int64_t>(l) * a.stride;
-            const int tiles =
-                good ? static_cast<int>((static_cast<int64_t>(ch.len) + kStTile - 1) / kStTile) : 1;
-            for (int t = 0; t < tiles; ++t, ++it) {
-                const int t0 = t * kStTile;
+            for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
                 const int s = it % P, n = it / P;
                 // the stage's previous tile must be released by every consumer warp
                 if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) {
@@ -345,22 +358,20 @@ __global__ void __launch_bounds__(kStThreads, 1)
                     ok = false;
                     break;
                 }
-                const int len = good ? min(kStTile, ch.len - t0) : kSkipTile;
-                const int len8 = good ? len & ~7 : 0;
+                const int len = min(kStTile, ch.len - t0);
+                const int len8 = len & ~7;
                 const int64_t i0 = ch.start + t0;
                 TileMeta& mt = meta[s];
                 mt.ts = ts;
                 mt.i0 = i0;
                 mt.len = len;
                 mt.l = l;
-                mt.last = t + 1 == tiles;
-                // (test hook: the first stage carries a wrong fill number)
-                mt.seq = (a.test_tag && it == 0) ? -1 : it;
+                mt.last = t0 + kStTile >= ch.len;
                 const uint32_t bar = smem_u32(&full[s]);
                 if (a.test_stall && it == 0) {
                     // test hook: the first tile is never issued, so its
                     // consumers' waits run out
-                } else if (len8 == 0) {  // skipped, or fewer than 8 elements: nothing to copy
+                } else if (len8 == 0) {  // a tensor of fewer than 8 elements: nothing to copy
                     mbar_arrive(bar);
                 } else {
                     const uint32_t st = ring0 + s * stage_bytes;
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
                     if (EMA) bulk_load(st + L.e, ts.e + i0, sb, bar);
                     if constexpr (SWA) bulk_load(st + L.sw, ts.swa + i0, sb, bar);
                 }
-                if (t == 0 && has_next)
+                if (t0 == 0 && has_next)
                     tsn = chunk_in_launch(chn, a.local0, a.n_local) ? a.slots[chn.local] : TensorSlot{};
             }
             ch = chn;
@@ -385,7 +396,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
             if (n > 0 && !mbar_wait(smem_u32(&empty[s]), (n - 1) & 1, lim)) ok = false;
             if (ok) {
                 meta[s].len = 0;
-                meta[s].seq = it;
+                meta[s].last = 0;
+                meta[s].seq = a.test_tag ? -1 : it;  // (test hook: a wrong fill number)
                 mbar_arrive(smem_u32(&full[s]));
                 ++it;
             }
@@ -471,21 +483,23 @@ __global__ void __launch_bounds__(kStThreads, 1)
         return true;
     };
     // Waits for stage s's use n; false (with the abort flag set) on a timeout.
-    // Then checks that the stage holds fill number it (= n P + s): a stage
-    // out of sequence sets kStatusProtocol and stops the block like a timeout.
-    auto wait_full = [&](int s, int n, int it) -> bool {
+    auto wait_full = [&](int s, int n) -> bool {
         if (*abort_v) return false;
         if (!mbar_wait(smem_u32(&full[s]), n & 1, lim)) {
             *abort_v = 1;
             atomicOr(a.status, kStatusWaitTimeout);
             return false;
         }
-        if (meta[s].seq != it) {
-            *abort_v = 1;
-            if (lane == 0) atomicOr(a.status, kStatusProtocol);
-            return false;
-        }
         return true;
+    };
+    // The end marker must carry the consumers' own count of stages taken
+    // (it = n P + s): otherwise they took a stage too many or too few, which
+    // sets kStatusProtocol and stops the block like a timeout.
+    auto end_in_sequence = [&](int s, int it) -> bool {
+        if (meta[s].seq == it) return true;
+        *abort_v = 1;
+        if (lane == 0) atomicOr(a.status, kStatusProtocol);
+        return false;
     };
 
     if constexpr (WD) {
@@ -500,34 +514,35 @@ __global__ void __launch_bounds__(kStThreads, 1)
         for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x, ++ci) {
             const ChunkDesc ch = a.chunks[c];
             const bool in_launch = chunk_in_launch(ch, a.local0, a.n_local);
-            const TensorSlot ts = in_launch ? a.slots[ch.local] : TensorSlot{};
-            const bool good = in_launch && chunk_in_tensor(ch, ts);
-            const void* const* xs =
-                a.x + static_cast<int64_t>(good ? ch.local - a.local0 : 0) * a.stride;
-            const int tiles =
-                good ? static_cast<int>((static_cast<int64_t>(ch.len) + kStTile - 1) / kStTile) : 1;
-            for (int t = 0; t < tiles; ++t, ++it) {
+            const TensorSlot ts = a.slots[in_launch ? ch.local : a.local0];
+            if (!in_launch || !chunk_in_tensor(ch, ts)) {  // the producer's one empty stage
                 const int s = it % P;
-                if (!wait_full(s, it / P, it)) return;
-                if (good) {
-                    const int t0 = t * kStTile;
-                    const int len = min(kStTile, ch.len - t0);
-                    const int len8 = len & ~7;
-                    const int64_t i0 = ch.start + t0;
-                    if (4 * g < len8)
-                        staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(
-                            a, xs, ts, ring0 + s * stage_bytes, L, i0 + 4 * g, 4 * g, acc, accw);
-                    if (g < len - len8)  // the ragged end, straight from global memory
-                        merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc,
-                                                                     accw);
-                }
+                if (!wait_full(s, it / P)) return;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+                ++it;
+                if (!hand_over(ci)) return;
+                continue;
+            }
+            const void* const* xs = a.x + static_cast<int64_t>(ch.local - a.local0) * a.stride;
+            for (int t0 = 0; t0 < ch.len; t0 += kStTile, ++it) {
+                const int s = it % P;
+                if (!wait_full(s, it / P)) return;
+                const int len = min(kStTile, ch.len - t0);
+                const int len8 = len & ~7;
+                const int64_t i0 = ch.start + t0;
+                if (4 * g < len8)
+                    staged_vec4<XT, MODE, EMA, NORM, PUB, SWA, WD>(
+                        a, xs, ts, ring0 + s * stage_bytes, L, i0 + 4 * g, 4 * g, acc, accw);
+                if (g < len - len8)  // the ragged end, straight from global memory
+                    merge_one<XT, MODE, EMA, NORM, PUB, SWA, WD>(a, xs, ts, i0 + len8 + g, acc, accw);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
             if (!hand_over(ci)) return;
         }
         const int s = it % P;  // the end marker
-        if (!wait_full(s, it / P, it)) return;
+        if (!wait_full(s, it / P) || !end_in_sequence(s, it)) return;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     } else {
@@ -535,19 +550,16 @@ __global__ void __launch_bounds__(kStThreads, 1)
         // stages, reading each tile's descriptor, until the end marker.
         for (int it = 0, ci = 0;; ++it) {
             const int s = it % P;
-            if (!wait_full(s, it / P, it)) return;
+            if (!wait_full(s, it / P)) return;
             const int len = meta[s].len;
-            if (len == 0) {  // end marker: release it and stop
+            if (len == 0 && !meta[s].last) {  // end marker: release it and stop
+                if (!end_in_sequence(s, it)) return;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
                 return;
             }
-            if (len == kSkipTile) {  // a chunk that failed the checks: its partials are 0
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-                if (NORM && !hand_over(ci++)) return;
-                continue;
-            }
+            // (len 0 with last set: a chunk that failed the checks; nothing
+            // below computes, and its partial is handed over as 0)
             const TensorSlot ts = meta[s].ts;
             const int64_t i0 = meta[s].i0;
             const int last = meta[s].last;

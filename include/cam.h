@@ -111,7 +111,7 @@ typedef enum {
                                        chunk table runs the first tensor's last chunk 2,048
                                        elements past that tensor's end (see cam_ctx_status) */
 #define CAM_TEST_BAD_TAG 512u       /* test hook, never for real rounds: every staged merge pass
-                                       tags its first stage with a wrong fill number and gives up
+                                       gives its end marker a wrong fill number and gives up
                                        waiting after about 1 ms (see cam_ctx_status) */
 
 /* Bits of the device status word (cam_ctx_status) */
@@ -484,12 +484,13 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * end) to test this; the caller gives that tensor's buffers (state, workers
  * and published copies) 2,048 spare elements past its end, so that even an
  * unchecked pass would stay inside them. The staged form further checks its
- * own protocol: each stage of its ring carries its fill number and each
- * drift hand-over its chunk count, compared by the warps that take them; a
- * mismatch sets CAM_STATUS_PROTOCOL and stops the pass as a timeout does. A
- * context created with CAM_TEST_BAD_TAG has every staged pass mislabel its
- * first stage to test this (its waits give up after about 1 ms, as with
- * CAM_TEST_STALL_STAGED).
+ * own protocol: the marker that ends a block's stages carries the number of
+ * stages filled, which its consumers compare with the number they took, and
+ * each drift hand-over carries its chunk count, which the reducer compares
+ * with its own; a mismatch sets CAM_STATUS_PROTOCOL and stops the pass as a
+ * timeout does. A context created with CAM_TEST_BAD_TAG has every staged pass
+ * mislabel its end marker to test this (its waits give up after about 1 ms,
+ * as with CAM_TEST_STALL_STAGED).
  *
  * cam_ctx_status waits for all work on the context's device, then writes the
  * word (0: nothing went wrong) to *out. The word stays set once set.

@@ -1232,11 +1232,12 @@ def test_corrupted_chunk_is_skipped_and_reported(form):
 @pytest.mark.parametrize("mode,norms", [("mean", False), ("delta", True)])
 def test_staged_stage_out_of_sequence_is_reported(mode, norms):
     """The staged pass's protocol check, met on purpose: with CAM_TEST_BAD_TAG
-    every staged pass labels its first stage with a wrong fill number. The
-    consumers find it, set CAM_STATUS_PROTOCOL and stop before touching the
-    stage; the producer's and the reducer's waits then give up after about
-    1 ms with every copy landed. Nothing faults or hangs, and a fresh context
-    on the same device runs the round like the oracle."""
+    every staged pass labels its end marker with a wrong fill number. The
+    consumers find that it does not match the number of stages they took, set
+    CAM_STATUS_PROTOCOL and stop without releasing it; the producer's wait for
+    that release then gives up after about 1 ms, with every copy landed.
+    Nothing faults or hangs, and a fresh context on the same device runs the
+    round like the oracle."""
     wl = _custom([300_000, 70_000, 2049], K=2, mode=mode, ema=mode == "mean", norms=norms)
     g = W.make_global(wl, 0, DEV)
     draw = W.draw_round(wl, 0, 0)
