@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libcam.so")
 
 SOURCES = ["merge_fused_f32.cu", "merge_fused_bf16.cu", "merge_staged_f32.cu",
            "merge_staged_bf16.cu", "merge_kernels.cu", "runtime.cu", "noalloc.cu", "adopt.cu",
-           "ortho.cu", "nt_gemm.cu", "eager.cu"]
+           "ortho.cu", "nt_gemm.cu", "eager.cu", "merge_multi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -75,7 +75,20 @@ struct NormArgs {
     double* worker_tsq;             // scratch [n_tensors * CAM_KMAX]
     double* per_worker_tensor;      // output [K * n_tensors] or null
     double* per_worker;             // output [K] or null
+    // the fused finish (K = 0 only): the fragment's chunk count, and 1 when
+    // the launch gives every block finish_smem_bytes() of dynamic shared
+    // memory, into which the finishing block copies the partials first
+    int32_t n_chunks;
+    int32_t shared;
 };
+
+// Dynamic shared memory of a fused finish that stages the partials, the
+// squared norms and the chunk index of a fragment of n_tensors tensors and
+// n_chunks chunks; launches give it when it is at most kFinishSmemMax.
+inline size_t finish_smem_bytes(int64_t n_tensors, int64_t n_chunks) {
+    return size_t(8 * n_chunks + 8 * n_tensors + 4 * (n_tensors + 1));
+}
+constexpr size_t kFinishSmemMax = 48 * 1024;
 
 // Parameter block of one launch of the fused merge pass. The launch covers
 // the fragment's local tensors [local0, local0 + n_local) and their chunks.
@@ -151,6 +164,51 @@ cudaError_t launch_merge_staged(const MergeArgs& a, const MergeVariant& v, int g
                                 cudaStream_t s);
 // Resident blocks per SM of that variant (0 on error).
 int merge_blocks_per_sm(const MergeVariant& v);
+
+// ---- several rounds in one register-form pass (cam_merge_commit_many) -------
+
+constexpr int kMultiMax = CAM_MAX_OPEN_ROUNDS;  // rounds per pass
+constexpr int kMultiXCap = 3584;                // worker and copy pointers per pass
+
+// One round of a multi-round pass: its fragment's tables, its finish, the
+// place of its chunks among the pass's and of its pointers in x[], and the
+// scalars the per-element arithmetic reads (merge_elem's K, Kf, w, W, lr, mu,
+// beta).
+struct MultiRound {
+    const ChunkDesc* chunks;   // the fragment's chunk table (device)
+    const TensorSlot* slots;   // the fragment's tensors, by local index (device)
+    double* partials;          // the fragment's drift partials (norms only)
+    unsigned int* fin_counter; // blocks done with this round's chunks (norms only)
+    NormArgs fin;              // the finish of this round's norms (norms only)
+    int32_t c_begin;           // the round's chunks are the pass's [c_begin, c_begin + n_chunks)
+    int32_t n_chunks;
+    int32_t x0;                // x[x0 + l * stride + k]: worker k's copy of local tensor l
+    int32_t vec0;              // bit vec0 + l of vec[]: tensor l takes the vector path
+    int32_t n_local;           // the fragment's tensors
+    int32_t stride;            // K, or K + 2 when publishing
+    int32_t K;
+    float Kf;
+    float w[CAM_KMAX];
+    float W, lr, mu, beta;
+};
+
+struct MultiArgs {
+    int32_t n_rounds;
+    int32_t n_chunks;          // all rounds' chunks
+    int32_t* status;           // device status word (kStatus* bits)
+    int32_t pad;
+    MultiRound r[kMultiMax];
+    uint32_t vec[kMultiXCap / 32];
+    const void* x[kMultiXCap + CAM_KMAX + 2];
+};
+static_assert(sizeof(MultiArgs) <= 32000, "kernel parameter block too large");
+
+// The multi-round pass of a variant (no running average, norm level 0 or 1,
+// the norms finished in the pass), with `smem` bytes of dynamic shared
+// memory for the finishes.
+cudaError_t launch_merge_multi(const MultiArgs& a, const MergeVariant& v, int grid, size_t smem,
+                               cudaStream_t s);
+int multi_blocks_per_sm(const MergeVariant& v);
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s);
 cudaError_t launch_fill(float* dst, int64_t n, float v, cudaStream_t s);
 cudaError_t launch_copy(float* dst, const float* src, int64_t n, cudaStream_t s);

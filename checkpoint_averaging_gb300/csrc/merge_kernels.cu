@@ -36,7 +36,7 @@ namespace {
 
 using namespace cam::dev;
 
-__global__ void __launch_bounds__(512) norm_finish(const NormArgs a) {
+__global__ void __launch_bounds__(256, 1) norm_finish(const NormArgs a) {
     finish_norms<false>(a);
 }
 
@@ -61,8 +61,11 @@ MergeFn pick(const MergeVariant& v) {
 cudaError_t launch_merge(const MergeArgs& a, const MergeVariant& v, int grid, cudaStream_t s) {
     MergeFn fn = pick(v);
     void* args[] = {const_cast<MergeArgs*>(&a)};
+    // a fused finish that stages its partials in shared memory gets it here
+    const size_t smem = v.fin && a.fin.shared ? finish_smem_bytes(a.fin.n_tensors, a.fin.n_chunks) : 0;
+    if (smem > kFinishSmemMax) return cudaErrorInvalidValue;
     return cudaLaunchKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kThreads),
-                            args, 0, s);
+                            args, smem, s);
 }
 
 int staged_state_arrays(const MergeVariant& v) {
@@ -127,7 +130,7 @@ int merge_blocks_per_sm(const MergeVariant& v) {
 }
 
 cudaError_t launch_norm_finish(const NormArgs& a, cudaStream_t s) {
-    norm_finish<<<1, 512, 0, s>>>(a);
+    norm_finish<<<1, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

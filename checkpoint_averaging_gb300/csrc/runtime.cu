@@ -166,6 +166,8 @@ struct cam_ctx {
     int bps_fin[2][2][2][2][2] = {};  // the same for norm level 1 with the finish fused
     bool fuse_finish = true;           // small rounds with norms finish them in the merge pass
     std::unique_ptr<MergeArgs> args;  // parameter block staging (copied at launch)
+    std::unique_ptr<cam::MultiArgs> multi_args;  // the same for cam_merge_commit_many
+    int bps_multi[2][2][2][2][2] = {};  // multi-round pass: [dtype][mode][ema][norms][publish]
 
     Plan& plan_of(int32_t fragment) { return plans[fragment < 0 ? n_fragments : fragment]; }
     const Plan& plan_of(int32_t fragment) const {
@@ -328,7 +330,8 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
     std::unique_ptr<cam_ctx> c(new (std::nothrow) cam_ctx);
     if (!c) return fail(CAM_E_NOMEM, "cam_ctx_create: out of host memory");
     c->args.reset(new (std::nothrow) MergeArgs);
-    if (!c->args) return fail(CAM_E_NOMEM, "cam_ctx_create: out of host memory");
+    c->multi_args.reset(new (std::nothrow) cam::MultiArgs);
+    if (!c->args || !c->multi_args) return fail(CAM_E_NOMEM, "cam_ctx_create: out of host memory");
     c->device = d->device;
     ce = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, d->device);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_ctx_create: SM count");
@@ -463,6 +466,14 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
                         v.fin = true;
                         c->bps_fin[dt][md][em][pb][sw] = std::max(1, cam::merge_blocks_per_sm(v));
                     }
+    for (int dt = 0; dt < 2; ++dt)
+        for (int md = 0; md < 2; ++md)
+            for (int em = 0; em < 2; ++em)
+                for (int nl = 0; nl < 2; ++nl)
+                    for (int pb = 0; pb < 2; ++pb)
+                        c->bps_multi[dt][md][em][nl][pb] = std::max(
+                            1, cam::multi_blocks_per_sm(cam::MergeVariant{
+                                   dt, md, em != 0, nl, pb != 0, false}));
     c->fuse_finish = !(d->flags & CAM_NO_FUSED_FINISH);
     c->staged = !(d->flags & CAM_NO_STAGING);
     c->test_stall = (d->flags & CAM_TEST_STALL_STAGED) != 0;
@@ -1019,9 +1030,11 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
                            state_writes <= 2;
     // Small rounds with the round's drift norms finish them in the merge pass
     // itself (register form, last block): one launch fewer, the same sums.
+    const int32_t fin_shared =
+        cam::finish_smem_bytes(T, p.n_chunks()) <= cam::kFinishSmemMax ? 1 : 0;
     const NormArgs na{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
                       norm_level >= 2 ? K : 0, p.d_worker_partials, p.d_worker_tsq,
-                      r->out_worker_tensor, r->out_worker};
+                      r->out_worker_tensor, r->out_worker, p.n_chunks(), fin_shared};
     const bool fuse = c->fuse_finish && norm_level == 1 && !r->eager && !r->ortho &&
                       p.n_chunks() > 0 && p.n_chunks() <= cam::kFuseMaxChunks && T <= per_launch;
     cam::MergeVariant variant_fin = variant;
