@@ -412,7 +412,42 @@ def run_ours(args, wl, ws, rank, local) -> int:
         stream_of[i] = min(range(n_streams), key=lambda j: load[j])
         load[stream_of[i]] += rb[i]
 
+    many = max(0, args.many if args.many is not None else wl.commit_many)
+
+    def step_many(timed: bool) -> None:
+        # the step's rounds opened, then committed in groups of `many` rounds
+        # by one call each (cam_merge_commit_many), all on the main stream
+        main = streams[0]
+        if timed:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+        for g0 in range(0, len(wl.rounds), many):
+            opened = []
+            for i in range(g0, min(len(wl.rounds), g0 + many)):
+                (_, frag), d = wl.rounds[i], draws[i]
+                rd = mg.begin(round_no[0], frag)
+                round_no[0] += 1
+                for k in d.included:
+                    rd.accumulate(prepared[i][k], d.tokens[k])
+                rd.finalize(mode, wl.lr, wl.mu)
+                if wl.ema_beta is not None:
+                    rd.ema_update(wl.ema_beta)
+                if wl.swa:
+                    rd.swa_update()
+                if wl.norms:
+                    rd.drift_norm(*norm_out[i])
+                if wl.worker_norms:
+                    rd.worker_drift_norm(*wnorm_out[i])
+                opened.append(rd)
+            mg.commit_many(opened, main)
+        if timed:
+            b.record(main)
+            group_pairs.append((a, b))
+
     def step(timed: bool) -> None:
+        if many >= 2:
+            step_many(timed)
+            return
         main = streams[0]
         if timed and n_streams > 1:
             ga = torch.cuda.Event(enable_timing=True)
@@ -498,11 +533,18 @@ def run_ours(args, wl, ws, rank, local) -> int:
     # launches are timed as one group from the fork to the join.
     per_round = [round_bytes(wl, f, k) for (_, f), k in zip(wl.rounds, k_incl)]
     big = max(range(len(per_round)), key=per_round.__getitem__)
+    if many >= 2 and launches > 0 and launches <= (len(wl.rounds) + many - 1) // many * args.steps:
+        kernel = "merge_multi"
     if graph is not None:
         launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
         kern_s = statistics.mean(launch_s)
         launch_bytes = step_bytes
         kernel_desc = f"{kernel} x{len(wl.rounds)} rounds, one CUDA graph replay per step"
+    elif many >= 2:
+        launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
+        kern_s = statistics.mean(launch_s)
+        launch_bytes = step_bytes
+        kernel_desc = f"{kernel}: {len(wl.rounds)} rounds, {many} per call"
     elif n_streams > 1:
         launch_s = [a.elapsed_time(b) / 1e3 for a, b in group_pairs]
         kern_s = statistics.mean(launch_s)
@@ -546,7 +588,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
                        "included": k_incl, "mode": wl.mode, "ema": wl.ema_beta is not None,
                        "swa": wl.swa, "worker_norms": wl.worker_norms,
                        "norms": wl.norms, "rounds_per_step": len(wl.rounds),
-                       "streams": n_streams, "bytes_per_step": step_bytes,
+                       "streams": 1 if many >= 2 else n_streams, "commit_many": many,
+                       "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
                        "parallelism": f"replicas{ws}", "cuda_graph": bool(args.graph),
                        "fused_finish": not args.no_fused_finish,
@@ -1130,6 +1173,9 @@ def parse(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--e2e-mode", choices=("stream", "copy", "fold"), default="stream")
+    p.add_argument("--many", type=int, default=None,
+                   help="commit the step's rounds in groups of this many by one call "
+                        "(cam_merge_commit_many); 0: one commit per round (default: the workload's)")
     p.add_argument("--graph", action="store_true",
                    help="capture one step of the merge op into a CUDA graph and time its replays")
     p.add_argument("--fold-last", action="store_true",

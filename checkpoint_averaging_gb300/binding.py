@@ -114,7 +114,7 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_swa_update", "cam_swa_reset", "cam_worker_drift_norm", "cam_adopt_keep_drift",
            "cam_merge_orthogonalize", "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
-           "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
+           "cam_merge_commit_many", "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
            "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_stream_capturing",
            "cam_ctx_get_quorum", "cam_ctx_set_quorum",
@@ -155,6 +155,7 @@ def lib() -> ctypes.CDLL:
     L.cam_ema_update.argtypes = [vp, ctypes.c_float]
     L.cam_drift_norm.argtypes = [vp, vp, vp]
     L.cam_merge_commit.argtypes = [vp, vp]
+    L.cam_merge_commit_many.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32, vp]
     L.cam_merge_abort.argtypes = [vp]
     L.cam_fragment_info.argtypes = [vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                     ctypes.POINTER(i32)]
@@ -297,6 +298,11 @@ def merge_publish(rd: int, theta_out: Sequence[int], ema_out: Sequence[int] | No
 
 def merge_commit(rd: int, stream: int = 0) -> None:
     _check(lib().cam_merge_commit(rd, stream or None))
+
+
+def merge_commit_many(rds: Sequence[int], stream: int = 0) -> None:
+    arr = (ctypes.c_void_p * len(rds))(*rds)
+    _check(lib().cam_merge_commit_many(arr, len(rds), stream or None))
 
 
 def merge_abort(rd: int) -> None:
@@ -631,6 +637,31 @@ class Merger:
     def checkpoint(self, ckpt, fragment: int = -1) -> "Checkpoint":
         """Validates a worker's tensors once for rounds on `fragment`."""
         return Checkpoint(self, ckpt, fragment)
+
+    def commit_many(self, rounds, stream=None) -> None:
+        """Commits open rounds of this merger as one call (cam_merge_commit_many):
+        the same results as committing each in order on `stream`; rounds of
+        one register-form variant share one merge pass."""
+        torch = _torch()
+        rounds = list(rounds)
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        sh = int(s.cuda_stream)
+        try:
+            merge_commit_many([rd.handle for rd in rounds], sh)
+        except CudaError:
+            for rd in rounds:
+                rd.handle = None  # the library freed the rounds of a shared pass
+            raise
+        borrowed = []
+        for rd in rounds:
+            rd.handle = None
+            borrowed.extend(rd._borrowed)
+            rd._borrowed = []
+        if stream_capturing(sh):
+            return  # a captured graph reads its buffers at every replay: they are the caller's
+        host = _record_streams(borrowed, s, sh)
+        if host or self._inflight:
+            self._hold_until_done(host, s)
 
 
 class Checkpoint:

@@ -88,7 +88,7 @@ struct NormArgs {
 inline size_t finish_smem_bytes(int64_t n_tensors, int64_t n_chunks) {
     return size_t(8 * n_chunks + 8 * n_tensors + 4 * (n_tensors + 1));
 }
-constexpr size_t kFinishSmemMax = 48 * 1024;
+constexpr size_t kFinishSmemMax = 40 * 1024;  // (with the static shared memory, within the default 48 KB)
 
 // Parameter block of one launch of the fused merge pass. The launch covers
 // the fragment's local tensors [local0, local0 + n_local) and their chunks.

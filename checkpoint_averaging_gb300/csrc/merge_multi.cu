@@ -58,10 +58,11 @@ __global__ void __launch_bounds__(kThreads, 2) merge_multi(const __grid_constant
             for (int v = threadIdx.x; v < nv; v += kThreads) {
                 const int64_t i = ch.start + 8 * int64_t(v);
                 if constexpr (sizeof(XT) == 4) {
-                    // fp32 workers in narrower steps: the round's scalars, held
-                    // in registers here, leave no room for eight elements of
-                    // every worker (four, or two with norms or EMA and copies)
-                    constexpr int N = (NORM || (EMA && PUB)) ? 2 : 4;
+                    // fp32 workers in two steps of four: the round's scalars,
+                    // held in registers here, leave no room for eight elements
+                    // of every worker (eight measured 9 % slower with spills,
+                    // two 27 % slower)
+                    constexpr int N = 4;
 #pragma unroll
                     for (int h = 0; h < 8; h += N)
                         merge_vecn_f32<N, MODE, EMA, NORM, PUB, false, false>(R, xs, ts, i + h, acc,

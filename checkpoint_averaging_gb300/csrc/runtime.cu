@@ -927,38 +927,61 @@ CAM_API int cam_merge_abort(cam_round* r) {
     return CAM_OK;
 }
 
-CAM_API int cam_merge_commit(cam_round* r, void* stream) {
-    if (!r) return fail(CAM_E_ARG, "cam_merge_commit: round is NULL");
-    cam_ctx* c = r->ctx;
-    if (!r->finalized) return fail(CAM_E_STATE, "cam_merge_commit: round not finalized");
+namespace {
+
+// Whether round r can be committed (on a stream that is or is not being
+// captured): the checks cam_merge_commit makes before anything runs.
+// Records the message for `fn` and returns the error, else CAM_OK.
+int commit_checks(const cam_round* r, bool cap, const char* fn) {
+    const cam_ctx* c = r->ctx;
+    if (!r->finalized) return fail(CAM_E_STATE, "%s: round not finalized", fn);
     if (r->K < c->quorum)
-        return fail(CAM_E_QUORUM, "cam_merge_commit: %d participants < quorum %d", r->K, c->quorum);
-    if (r->K < 1) return fail(CAM_E_QUORUM, "cam_merge_commit: no participants");
+        return fail(CAM_E_QUORUM, "%s: %d participants < quorum %d", fn, r->K, c->quorum);
+    if (r->K < 1) return fail(CAM_E_QUORUM, "%s: no participants", fn);
     if (r->publish_ema && !r->ema)
-        return fail(CAM_E_STATE, "cam_merge_commit: an EMA copy was asked for without an EMA update");
+        return fail(CAM_E_STATE, "%s: an EMA copy was asked for without an EMA update", fn);
     int64_t W = 0;
     for (int k = 0; k < r->K; ++k) W += r->tokens[k];
     if (r->mode == CAM_MODE_DELTA_NESTEROV && W <= 0)
-        return fail(CAM_E_ARG, "cam_merge_commit: total token count must be > 0");
-
+        return fail(CAM_E_ARG, "%s: total token count must be > 0", fn);
     if (r->ortho) {
         if (r->mode != CAM_MODE_MEAN_REPLACE)
-            return fail(CAM_E_STATE, "cam_merge_commit: orthogonalisation applies to plain-mean rounds");
+            return fail(CAM_E_STATE, "%s: orthogonalisation applies to plain-mean rounds", fn);
         if (r->norms || r->worker_norms || r->publish || r->swa)
-            return fail(CAM_E_STATE,
-                        "cam_merge_commit: an orthogonalised round takes only an EMA update");
+            return fail(CAM_E_STATE, "%s: an orthogonalised round takes only an EMA update", fn);
     }
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool cap = capturing(s);
     if (cap && r->swa)
         return fail(CAM_E_STATE,
-                    "cam_merge_commit: a running-average update cannot be captured (its count "
-                    "would not advance on replay)");
+                    "%s: a running-average update cannot be captured (its count would not "
+                    "advance on replay)", fn);
     if (cap && r->ortho && !c->ortho)
         return fail(CAM_E_STATE,
-                    "cam_merge_commit: the first orthogonalised commit allocates; make it outside a "
-                    "graph capture");
+                    "%s: the first orthogonalised commit allocates; make it outside a graph capture",
+                    fn);
+    if (r->swa) {
+        int64_t prev = -1;
+        for (int32_t g : c->plan_of(r->fragment).tensors) {
+            if (c->numel[g] == 0) continue;
+            if (prev >= 0 && c->swa_count[g] != prev)
+                return fail(CAM_E_STATE,
+                            "%s: the fragment's running averages hold different numbers of "
+                            "globals (reset them together)", fn);
+            prev = c->swa_count[g];
+        }
+    }
+    return CAM_OK;
+}
+
+}  // namespace
+
+CAM_API int cam_merge_commit(cam_round* r, void* stream) {
+    if (!r) return fail(CAM_E_ARG, "cam_merge_commit: round is NULL");
+    cam_ctx* c = r->ctx;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool cap = capturing(s);
+    if (const int rc = commit_checks(r, cap, "cam_merge_commit"); rc != CAM_OK) return rc;
+    int64_t W = 0;
+    for (int k = 0; k < r->K; ++k) W += r->tokens[k];
 
     const Plan& p = c->plan_of(r->fragment);
     const int K = r->K;
@@ -1241,6 +1264,171 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         for (int32_t g : p.tensors) c->swa_count[g] = swa_prev + 1;
     close_round(r);
     if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_commit: launch");
+    return CAM_OK;
+}
+
+CAM_API int cam_merge_commit_many(cam_round* const* rounds, int32_t n, void* stream) {
+    const char* fn = "cam_merge_commit_many";
+    if (!rounds || n < 1) return fail(CAM_E_ARG, "%s: no rounds", fn);
+    if (n > cam::kMultiMax) return fail(CAM_E_ARG, "%s: at most %d rounds", fn, cam::kMultiMax);
+    for (int i = 0; i < n; ++i) {
+        if (!rounds[i]) return fail(CAM_E_ARG, "%s: round %d is NULL", fn, i);
+        if (rounds[i]->ctx != rounds[0]->ctx)
+            return fail(CAM_E_ARG, "%s: the rounds belong to different contexts", fn);
+        for (int j = 0; j < i; ++j)
+            if (rounds[j] == rounds[i]) return fail(CAM_E_ARG, "%s: round %d given twice", fn, i);
+    }
+    cam_ctx* c = rounds[0]->ctx;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool cap = capturing(s);
+    // every round's checks before anything runs (open rounds never overlap:
+    // cam_merge_begin refuses a fragment that shares tensors with one)
+    for (int i = 0; i < n; ++i)
+        if (const int rc = commit_checks(rounds[i], cap, fn); rc != CAM_OK) return rc;
+
+    // One register-form pass for all of them when they are the same variant,
+    // their norms (if any) finished in the pass, and their pointers fit;
+    // otherwise one commit after another, in the given order.
+    const cam_round* r0 = rounds[0];
+    bool one_pass = n > 1 && c->fuse_finish;
+    int64_t ptrs = 0;
+    for (int i = 0; i < n && one_pass; ++i) {
+        const cam_round* r = rounds[i];
+        const Plan& p = c->plan_of(r->fragment);
+        one_pass = !r->eager && !r->ortho && !r->swa && !r->worker_norms && r->dtype == r0->dtype &&
+                   r->mode == r0->mode && r->ema == r0->ema && r->norms == r0->norms &&
+                   r->publish == r0->publish &&
+                   (!r->norms || (p.n_chunks() > 0 && p.n_chunks() <= cam::kFuseMaxChunks));
+        ptrs += int64_t(p.n_tensors()) * (r->K + (r->publish ? 2 : 0));
+    }
+    if (!one_pass || ptrs > cam::kMultiXCap) {
+        for (int i = 0; i < n; ++i)
+            if (const int rc = cam_merge_commit(rounds[i], stream); rc != CAM_OK) return rc;
+        return CAM_OK;
+    }
+
+    DeviceScope scope(c->device);
+    if (scope.err != cudaSuccess) {
+        for (int i = 0; i < n; ++i) close_round(rounds[i]);
+        return cuda_fail(scope.err, "cam_merge_commit_many: cudaSetDevice");
+    }
+    const bool delta = r0->mode == CAM_MODE_DELTA_NESTEROV;
+    const int norm_level = r0->norms ? 1 : 0;
+    const uintptr_t xa = r0->dtype == CAM_F32 ? 32 : 16;
+    cam::MultiArgs& a = *c->multi_args;
+    a.n_rounds = n;
+    a.status = c->d_status;
+    std::memset(a.vec, 0, sizeof a.vec);
+    // the rounds with fewest chunks first: their finishes then run while the
+    // blocks still stream the longer rounds
+    std::vector<int> ord(n);
+    for (int i = 0; i < n; ++i) ord[i] = i;
+    std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) {
+        return c->plan_of(rounds[x]->fragment).n_chunks() < c->plan_of(rounds[y]->fragment).n_chunks();
+    });
+    int32_t chunks = 0, xp = 0;
+    size_t smem = 0;
+    int64_t elems = 0, bytes = 0;
+    for (int j = 0; j < n; ++j) {
+        const cam_round* r = rounds[ord[j]];
+        const Plan& p = c->plan_of(r->fragment);
+        const int K = r->K, T = p.n_tensors(), stride = K + (r->publish ? 2 : 0);
+        int64_t W = 0;
+        for (int k = 0; k < K; ++k) W += r->tokens[k];
+        cam::MultiRound& R = a.r[j];
+        R.chunks = p.d_chunks;
+        R.slots = p.d_slots;
+        R.partials = norm_level ? p.d_partials : nullptr;
+        R.fin_counter = p.d_fin_counter;
+        const int32_t shared = cam::finish_smem_bytes(T, p.n_chunks()) <= cam::kFinishSmemMax ? 1 : 0;
+        R.fin = NormArgs{p.d_partials, p.d_first, T, p.d_tsq, r->out_tensor, r->out_fragment,
+                         0, nullptr, nullptr, nullptr, nullptr, p.n_chunks(), shared};
+        if (norm_level && shared) smem = std::max(smem, cam::finish_smem_bytes(T, p.n_chunks()));
+        R.c_begin = chunks;
+        R.n_chunks = p.n_chunks();
+        R.x0 = xp;
+        R.vec0 = 0;  // (set below: one bit per tensor)
+        R.n_local = T;
+        R.stride = stride;
+        R.K = K;
+        R.Kf = static_cast<float>(K);
+        for (int k = 0; k < CAM_KMAX; ++k) R.w[k] = k < K ? static_cast<float>(r->tokens[k]) : 0.0f;
+        R.W = static_cast<float>(W);
+        R.lr = r->lr;
+        R.mu = r->mu;
+        R.beta = r->beta;
+        chunks += p.n_chunks();
+        xp += T * stride;
+        elems += p.n_elems;
+        const int64_t xb = r->dtype == CAM_BF16 ? 2 : 4;
+        bytes += (K * xb + 4 + ((delta || norm_level >= 1) ? 4 : 0) + (delta ? 8 : 0) +
+                  (r->ema ? 8 : 0) + (r->publish ? 4 : 0) + (r->publish_ema ? 4 : 0)) *
+                 p.n_elems;
+    }
+    // pointers and the vector-path bits, one bit per tensor over the rounds
+    int32_t vb = 0;
+    for (int j = 0; j < n; ++j) {
+        const cam_round* r = rounds[ord[j]];
+        const Plan& p = c->plan_of(r->fragment);
+        cam::MultiRound& R = a.r[j];
+        const int K = r->K, T = p.n_tensors();
+        R.vec0 = vb;
+        for (int l = 0; l < T; ++l) {
+            const int32_t g = p.tensors[l];
+            const void** xs = a.x + R.x0 + static_cast<size_t>(l) * R.stride;
+            bool v = aligned(c->theta[g], 32) && (!delta || aligned(c->m[g], 32)) &&
+                     (!r->ema || aligned(c->e[g], 32));
+            for (int k = 0; k < K; ++k) {
+                xs[k] = r->x[size_t(k) * T + l];
+                v = v && aligned(xs[k], xa);
+            }
+            if (r->publish) {
+                xs[K] = r->pub_theta[l];
+                xs[K + 1] = r->publish_ema ? r->pub_ema[l] : nullptr;
+                v = v && aligned(xs[K], 32) && aligned(xs[K + 1], 32);
+            }
+            if (v) a.vec[(vb + l) >> 5] |= 1u << ((vb + l) & 31);
+        }
+        vb += T;
+    }
+    a.n_chunks = chunks;  // (vb <= ptrs <= kMultiXCap: every tensor has a pointer)
+
+    char label[96];
+    std::snprintf(label, sizeof label, "cam_merge_commit_many %d rounds", n);
+    NvtxRange nvtx(label);
+    const int64_t launches0 = c->launches;
+    cudaError_t ce = cudaSuccess;
+    for (int i = 0; i < n && ce == cudaSuccess; ++i)
+        ce = plan_order(c, rounds[i]->fragment, s, cap);  // after earlier work on these tensors
+    const bool timed = c->time_commits && !cap;
+    if (ce == cudaSuccess && timed) ce = cudaEventRecord(c->commit_ev[0], s);
+    if (ce == cudaSuccess && chunks > 0) {
+        const cam::MergeVariant v{r0->dtype, r0->mode, r0->ema, norm_level, r0->publish, false};
+        // (all the rounds are in this launch: CAM_SHARE_SMS has nothing to leave room for)
+        const int b = c->bps_multi[r0->dtype][r0->mode][r0->ema][norm_level][r0->publish];
+        const int grid = static_cast<int>(std::min<int64_t>(chunks, int64_t(c->sm_count) * b));
+        ce = cam::launch_merge_multi(a, v, grid, smem, s);
+        ++c->launches;
+    }
+    for (int i = 0; i < n && ce == cudaSuccess; ++i) ce = plan_mark(c, rounds[i]->fragment, s, cap);
+    if (ce == cudaSuccess && timed) ce = cudaEventRecord(c->commit_ev[1], s);
+    if (ce == cudaSuccess) {
+        const cam_round* rl = rounds[n - 1];
+        cam_commit_record& rec = c->last_commit;
+        rec.round = rl->round;
+        rec.fragment = rl->fragment;
+        rec.K = rl->K;
+        rec.mode = rl->mode;
+        rec.form = CAM_FORM_REGISTER;
+        rec.elements = elems;
+        rec.bytes = bytes;
+        rec.launches = c->launches - launches0;
+        rec.ms = -1.0f;
+        c->has_last_commit = true;
+        c->last_commit_timed = timed;
+    }
+    for (int i = 0; i < n; ++i) close_round(rounds[i]);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cam_merge_commit_many: launch");
     return CAM_OK;
 }
 

@@ -189,6 +189,7 @@ class Workload:
     swa: bool = False                   # also fold each global into the uniform average
     worker_norms: bool = False          # also report each worker's own drift
     share_sms: bool = False             # merge passes leave room for rounds in flight beside them
+    commit_many: int = 0                # rounds committed together by one call (0: one per call)
 
     @property
     def n_params(self) -> int:

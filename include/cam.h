@@ -401,6 +401,34 @@ int cam_merge_publish(cam_round* rd, float* const* theta_out, float* const* ema_
  */
 int cam_merge_commit(cam_round* rd, void* stream);
 
+/*
+ * Commits n open rounds of one context (n <= CAM_MAX_OPEN_ROUNDS; open rounds
+ * never share tensors) as if cam_merge_commit were called for each in array
+ * order on `stream`, with the same results bit for bit. "Pythia-14M on four
+ * rented GPUs and a bucket", "Getting updates through the bucket": fragments
+ * have rounds of their own and two may be in flight at once, so rounds can
+ * close together; their merges then share one pass. When the rounds are the
+ * same variant of the register form -- the same worker dtype, mode, EMA
+ * update, drift norms or none (no per-worker drift), published copies or
+ * none, no running-average update, eager folds or orthogonalisation, norms
+ * finished in the pass (at most 4,096 chunks per fragment, the context not
+ * created with CAM_NO_FUSED_FINISH) -- and their worker and copy pointers
+ * number at most 3,584 together, one launch merges all of them: its blocks
+ * take every round's chunks, a round's norms are finished by the block that
+ * completes its last chunk, and short rounds end while long ones still
+ * stream. Otherwise the rounds are committed one after another.
+ *
+ * Every round is checked as cam_merge_commit checks it before anything runs:
+ * on CAM_E_ARG (NULL or repeated handles, rounds of different contexts, more
+ * than CAM_MAX_OPEN_ROUNDS), CAM_E_STATE or CAM_E_QUORUM nothing is launched
+ * and every round stays open. On CAM_E_CUDA the rounds of a shared pass are
+ * freed and their buffers undefined; rounds committed one after another
+ * behave as cam_merge_commit, in order, and a failure leaves the later ones
+ * open. cam_ctx_last_commit then describes the last round of the array, with
+ * the elements, bytes, launches and time of the whole call.
+ */
+int cam_merge_commit_many(cam_round* const* rounds, int32_t n, void* stream);
+
 /* Drops an open round without touching any buffer. The round number stays
  * used. */
 int cam_merge_abort(cam_round* rd);
