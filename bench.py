@@ -1187,8 +1187,9 @@ def parse(argv=None):
     p.add_argument("--no-staging", action="store_true",
                    help="merge passes in the register form instead of the staged (bulk-copy) form")
     p.add_argument("--share-sms", action="store_true",
-                   help="merge passes keep to one register-form block per SM, so rounds in "
-                        "flight on other streams run beside them (CAM_SHARE_SMS)")
+                   help="merge passes take at most three quarters of the register form's block "
+                        "slots, so rounds in flight on other streams start beside them "
+                        "(CAM_SHARE_SMS)")
     p.add_argument("--no-fused-finish", action="store_true",
                    help="drift norms always finished by the separate norm pass (small rounds "
                         "otherwise finish them in a register-form merge pass)")

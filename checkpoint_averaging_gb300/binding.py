@@ -27,7 +27,7 @@ NO_STAGING = 8
 TIME_COMMITS = 16
 NO_FUSED_FINISH = 32
 TEST_STALL_STAGED = 64  # test hook: staged passes withhold their first tile and time out
-SHARE_SMS = 128  # merge passes leave room on every SM for a round in flight beside them
+SHARE_SMS = 128  # merge passes leave block slots for rounds in flight beside them
 TEST_BAD_CHUNK = 256  # test hook: the first tensor's last chunk runs past its end on the device
 TEST_BAD_TAG = 512  # test hook: staged passes mislabel their end marker and stop
 FORM_REGISTER, FORM_STAGED, FORM_FOLDED, FORM_ORTHO = 0, 1, 2, 3
@@ -493,9 +493,10 @@ class Merger:
         results). time_commits=True times each commit's device work
         (last_commit()["ms"]). fused_finish=False always launches the
         separate norm pass (small rounds otherwise finish their norms in the
-        merge pass; the same bits). share_sms=True (CAM_SHARE_SMS) keeps every
-        merge pass to one register-form block per SM, so that rounds in flight
-        on other streams run beside it (the same bits). test_stall_staged=True is a test hook
+        merge pass; the same bits). share_sms=True (CAM_SHARE_SMS) gives every
+        merge pass at most three quarters of the register form's block slots,
+        so that rounds in flight on other streams start beside it (the same
+        bits). test_stall_staged=True is a test hook
         (CAM_TEST_STALL_STAGED): staged passes withhold their first tile, their
         waits give up after about 1 ms and status() reports the timeout.
         test_bad_chunk=True (CAM_TEST_BAD_CHUNK) and test_bad_tag=True

@@ -104,9 +104,9 @@ typedef enum {
 #define CAM_TEST_STALL_STAGED 64u   /* test hook, never for real rounds: every staged merge pass
                                        withholds its first tile and gives up waiting after
                                        about 1 ms (see cam_ctx_status) */
-#define CAM_SHARE_SMS 128u          /* merge passes take at most one register-form block per SM,
-                                       leaving room beside them for a round in flight on another
-                                       stream (small fragment rounds run alongside) */
+#define CAM_SHARE_SMS 128u          /* merge passes take at most three quarters of the register
+                                       form's block slots, so rounds in flight on other streams
+                                       start alongside */
 #define CAM_TEST_BAD_CHUNK 256u     /* test hook, never for real rounds: the device copy of the
                                        chunk table runs the first tensor's last chunk 2,048
                                        elements past that tensor's end (see cam_ctx_status) */
@@ -486,10 +486,10 @@ int cam_ctx_launch_count(const cam_ctx* ctx, int64_t* out);
  * created with CAM_NO_FUSED_FINISH always launches the separate norm pass.
  *
  * A context created with CAM_SHARE_SMS keeps every merge pass in the
- * register form with at most one block per SM. A pass then holds half of
- * each SM's registers and little shared memory, so the pass of a round in
- * flight on another stream runs beside it instead of after it: a long round
- * and short rounds of other fragments overlap. The results are the same bits.
+ * register form with at most three quarters of the form's block slots (the
+ * blocks the device holds at once). The pass of a round in flight on another
+ * stream then starts beside it instead of after it: a long round and short
+ * rounds of other fragments overlap. The results are the same bits.
  *
  * Every wait of the staged form on one of its barriers gives up after a few
  * seconds. It then sets CAM_STATUS_WAIT_TIMEOUT in the context's device status

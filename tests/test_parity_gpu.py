@@ -52,8 +52,8 @@ def test_stand_mean_ema_ten_rounds_full():
 
 
 def test_rounds_sharing_the_sms_equal_the_oracle_bitwise():
-    """CAM_SHARE_SMS (one register-form block per SM, so rounds in flight run
-    side by side) changes only the launch shape: the Pythia-14M rounds still
+    """CAM_SHARE_SMS (each pass takes at most three quarters of the register
+    form's block slots, so rounds in flight run side by side) changes only the launch shape: the Pythia-14M rounds still
     equal the oracle bit for bit, norms within their tolerance."""
     run_full(W.workload("pythia14m"), seed=9, bitwise=True, share_sms=True)
 
