@@ -266,8 +266,12 @@ SWEEP_K = (2, 4, 8)
 
 def workload(name: str) -> Workload:
     """A workload by name; a "+swa" suffix also folds each global into the
-    uniform running average, a "-ema" suffix drops the EMA update."""
+    uniform running average, a "-ema" suffix drops the EMA update, a "+wnorms"
+    suffix asks for the round's and each worker's drift norms."""
     import dataclasses
+    if name.endswith("+wnorms"):
+        wl = workload(name[:-len("+wnorms")])
+        return dataclasses.replace(wl, name=wl.name + "_wnorms", norms=True, worker_norms=True)
     if name.endswith("+swa"):
         wl = workload(name[:-len("+swa")])
         return dataclasses.replace(wl, name=wl.name + "_swa", swa=True)
