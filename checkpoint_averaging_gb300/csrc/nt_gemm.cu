@@ -226,6 +226,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// Until every group of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Until every group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -246,6 +250,8 @@ struct alignas(128) TcProblem {
     CUtensorMap ty;          // Y (or the Gram split partials): boxes of 32 x 32
     CUtensorMap tyt;         // Yt, or Y read transposed (Gram mirror): boxes of 32 x 32
     CUtensorMap tcm;         // C (kEpiAxpbyC): boxes of 32 x 32, swizzled as box_row
+    const float* c;          // C (kEpiAxpbyC read directly, fp32): row stride ldc, matrix stride sc
+    int64_t ldc, sc;
     int32_t batch;
     int32_t m_blocks;        // M / 128
     int32_t n_blocks;        // N / BN
@@ -396,20 +402,25 @@ __device__ __forceinline__ void box_col(uint32_t buf, int r, const float* v) {
 
 // ---- the tensor-core kernel --------------------------------------------------------
 
-template <bool BF16, int BN, int EPI>
+template <bool BF16, int BN, int EPI, bool DC = false>
 struct Geo {
     static constexpr int kBBytes = BN * kRowBytes;
     static constexpr int kStage = kBoxBytes + kBBytes;
-    // epilogue staging: per warp two buffers, each one box and its transpose
-    // (a Gram split's fp32 partial box fits one buffer)
+    // epilogue staging: per warp kStgBufs buffers, each one box and its
+    // transpose (a Gram split's fp32 partial box fits one buffer). bf16 boxes
+    // are double-buffered; fp32 boxes, twice the bytes, single-buffered, which
+    // leaves the TF32 ring four stages instead of three -- except for the
+    // kEpiAxpbyC form that reads C through TMA (!DC, short K), which keeps
+    // double buffers and one box of C per warp, prefetched a box ahead.
+    static constexpr bool kTmaC = EPI == kEpiAxpbyC && !DC;
     static constexpr int kOutBytes = BF16 ? 2 : 4;
     static constexpr int kBox = kOutBox * kOutBox * kOutBytes;
     static constexpr int kStgBuf = 2 * kBox;
+    static constexpr int kStgBufs = (BF16 || kTmaC) ? 2 : 1;
     static_assert(kStgBuf >= kOutBox * kOutBox * 4, "a partial box must fit a buffer");
-    // kEpiAxpbyC: one box of C per warp, prefetched a box ahead
     static constexpr int kCBox = kOutBox * kOutBox * (BF16 ? 2 : 4);
-    static constexpr int kCRegion = EPI == kEpiAxpbyC ? kEpiWarps * kCBox : 0;
-    static constexpr int kStaging = kEpiWarps * 2 * kStgBuf + kCRegion;
+    static constexpr int kCRegion = kTmaC ? kEpiWarps * kCBox : 0;
+    static constexpr int kStaging = kEpiWarps * kStgBufs * kStgBuf + kCRegion;
     static constexpr int kStagesFit = (kSmemBudget - kStaging) / kStage;
     static constexpr int kStages = kStagesFit < 8 ? kStagesFit : 8;
     static constexpr int kStgOffset = kStages * kStage;
@@ -424,9 +435,9 @@ struct Geo {
     static_assert(kSmem <= 232448, "over the per-block shared memory limit");
 };
 
-template <bool BF16, int BN, int EPI, bool MNM>
+template <bool BF16, int BN, int EPI, bool MNM, bool DC = false>
 __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constant__ TcArgs a) {
-    using G = Geo<BF16, BN, EPI>;
+    using G = Geo<BF16, BN, EPI, DC>;
     // MN-major operands: TMA boxes of 128 bytes of M (or N) by one K step of
     // rows; kMnBox bytes each, kMnCols elements of M (or N)
     constexpr int kMnCols = kRowBytes / (BF16 ? 2 : 4);
@@ -630,23 +641,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
     } else if (warp >= 2) {
         // ---- epilogue ----
         const int quarter = warp & 3;  // TMEM lanes 32 quarter .. + 31: rows of the tile
-        const uint32_t stg = su32(smem + G::kStgOffset + (warp - 2) * 2 * G::kStgBuf);
-        // kEpiAxpbyC: this warp's box of C, loaded by TMA one box ahead
-        const uint32_t cbuf = su32(smem + G::kStgOffset + kEpiWarps * 2 * G::kStgBuf +
+        const uint32_t stg = su32(smem + G::kStgOffset + (warp - 2) * G::kStgBufs * G::kStgBuf);
+        // kEpiAxpbyC through TMA (!DC): this warp's box of C, loaded one box ahead
+        const uint32_t cbuf = su32(smem + G::kStgOffset + kEpiWarps * G::kStgBufs * G::kStgBuf +
                                    (warp - 2) * G::kCBox);
         const uint32_t cbar = cfull0 + 8 * (warp - 2);
         uint32_t c_phase = 0;
         bool c_pending = false;
-        auto load_c = [&](int u, int cc) {  // lane 0: the C box of unit u, column box cc
+        auto tma_c = [&](int u, int cc) {  // lane 0: the C box of unit u, column box cc
             const Unit n = decode<BN, EPI>(a, u);
             bar_expect(cbar, G::kCBox);
             tma_load(cbuf, &a.prob[n.p].tcm, n.cb * BN + cc * 32, n.rb * kBM + quarter * 32, n.b,
                      cbar);
         };
-        if (EPI == kEpiAxpbyC && lane == 0 && int(blockIdx.x) < a.n_units) {
-            load_c(blockIdx.x, 0);
+        if (G::kTmaC && lane == 0 && int(blockIdx.x) < a.n_units) {
+            tma_c(blockIdx.x, 0);
             c_pending = true;
         }
+        // kEpiAxpbyC read directly (DC, fp32 C, long K): this lane's row of the
+        // next C box, 32 floats (one 128-byte line) from global memory a box
+        // ahead, which frees the C boxes' shared memory for a fourth stage
+        float cn[EPI == kEpiAxpbyC && DC ? 32 : 1];
+        auto load_c = [&](int u, int cc) {
+            if constexpr (EPI == kEpiAxpbyC && DC) {
+                const Unit n = decode<BN, EPI>(a, u);
+                const TcProblem& Q = a.prob[n.p];
+                const float4* src = reinterpret_cast<const float4*>(
+                    Q.c + n.b * Q.sc + int64_t(n.rb * kBM + quarter * 32 + lane) * Q.ldc +
+                    n.cb * BN + cc * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 x = __ldg(src + j);
+                    cn[4 * j] = x.x;
+                    cn[4 * j + 1] = x.y;
+                    cn[4 * j + 2] = x.z;
+                    cn[4 * j + 3] = x.w;
+                }
+            }
+        };
+        if (EPI == kEpiAxpbyC && DC && int(blockIdx.x) < a.n_units) load_c(blockIdx.x, 0);
         int acc = 0, buf = 0;
         uint32_t acc_phase = 0;
         int qslot = 0, iter = 0;
@@ -699,20 +732,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                     mirror = P.has_yt != 0;
                 }
                 if constexpr (EPI == kEpiAxpbyC) {
-                    const bool cok = bar_wait(cbar, c_phase, abort_flag, a.status);
-                    if (!__all_sync(0xffffffffu, cok)) {
-                        aborted = true;
-                        break;
-                    }
-                    c_phase ^= 1;
                     float c[32];
-                    box_row_read<BF16>(cbuf, lane, c);
-                    __syncwarp();  // every lane has read the box before it is refilled
-                    c_pending = false;
-                    if (lane == 0) {
-                        const int nu = cc + 1 < BN / 32 ? u : u + int(gridDim.x);
-                        if (nu < a.n_units) {
-                            load_c(nu, cc + 1 < BN / 32 ? cc + 1 : 0);
+                    // the next box's C: this unit's next column box, or the
+                    // first of the next unit this block takes (a static stride)
+                    const int nu = cc + 1 < BN / 32 ? u : u + int(gridDim.x);
+                    if constexpr (DC) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) c[i] = cn[i];
+                        if (nu < a.n_units) load_c(nu, cc + 1 < BN / 32 ? cc + 1 : 0);
+                    } else {
+                        const bool cok = bar_wait(cbar, c_phase, abort_flag, a.status);
+                        if (!__all_sync(0xffffffffu, cok)) {
+                            aborted = true;
+                            break;
+                        }
+                        c_phase ^= 1;
+                        box_row_read<BF16>(cbuf, lane, c);
+                        __syncwarp();  // every lane has read the box before it is refilled
+                        c_pending = false;
+                        if (lane == 0 && nu < a.n_units) {
+                            tma_c(nu, cc + 1 < BN / 32 ? cc + 1 : 0);
                             c_pending = true;
                         }
                     }
@@ -730,8 +769,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                     for (int i = 0; i < 32; ++i)
                         if (i == lane) v[i] += a.diag;
                 }
-                // the buffer's store from two boxes ago has finished reading it
-                if (lane == 0) bulk_wait_read1();
+                // the buffer's store from kStgBufs boxes ago has finished reading it
+                if (lane == 0) {
+                    if constexpr (G::kStgBufs == 2) bulk_wait_read1();
+                    else bulk_wait_read0();
+                }
                 __syncwarp();
                 const uint32_t yb = stg + buf * G::kStgBuf;
                 const uint32_t ytb = yb + G::kBox;
@@ -748,7 +790,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) nt_gemm_tc(const __grid_constan
                     if (mirror) tma_store(&P.tyt, ytb, row0, col0, t.b);
                     bulk_commit();
                 }
-                buf ^= 1;
+                if constexpr (G::kStgBufs == 2) buf ^= 1;
             }
             if (aborted) break;
             if (++acc == 2) {
@@ -1020,11 +1062,11 @@ int out_map(CUtensorMap* map, int64_t eb, const void* base, int64_t cols, int64_
 
 // Launched as a programmatic dependent of the previous kernel on the stream
 // (the kernel waits in griddepcontrol.wait before touching global memory).
-template <bool BF16, int BN, int EPI, bool MNM = false>
+template <bool BF16, int BN, int EPI, bool MNM = false, bool DC = false>
 cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
-    using G = Geo<BF16, BN, EPI>;
+    using G = Geo<BF16, BN, EPI, DC>;
     static cudaError_t attr = cudaFuncSetAttribute(
-        nt_gemm_tc<BF16, BN, EPI, MNM>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+        nt_gemm_tc<BF16, BN, EPI, MNM, DC>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -1037,24 +1079,28 @@ cudaError_t launch_tc(const TcArgs& a, int grid, cudaStream_t s) {
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, nt_gemm_tc<BF16, BN, EPI, MNM>, a);
+    return cudaLaunchKernelEx(&cfg, nt_gemm_tc<BF16, BN, EPI, MNM, DC>, a);
 }
 
 template <bool BF16, int BN>
-cudaError_t launch_tc_epi(const TcArgs& a, int epi, bool mn, int grid, cudaStream_t s) {
+cudaError_t launch_tc_epi(const TcArgs& a, int epi, bool mn, bool dc, int grid, cudaStream_t s) {
     switch (epi) {
         case kNtAxpby: return launch_tc<BF16, BN, kNtAxpby>(a, grid, s);
         case kNtGram:
             return mn ? launch_tc<BF16, BN, kNtGram, true>(a, grid, s)
                       : launch_tc<BF16, BN, kNtGram>(a, grid, s);
-        default: return launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
+        default:  // (C is fp32: TF32 products only, checked on the host)
+            if constexpr (BF16) return cudaErrorInvalidValue;
+            else return dc ? launch_tc<BF16, BN, kEpiAxpbyC, false, true>(a, grid, s)
+                           : launch_tc<BF16, BN, kEpiAxpbyC>(a, grid, s);
     }
 }
 
 template <bool BF16>
-cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, bool mn, int grid, cudaStream_t s) {
-    return bn == 256 ? launch_tc_epi<BF16, 256>(a, epi, mn, grid, s)
-                     : launch_tc_epi<BF16, 128>(a, epi, mn, grid, s);
+cudaError_t launch_tc_any(const TcArgs& a, int bn, int epi, bool mn, bool dc, int grid,
+                          cudaStream_t s) {
+    return bn == 256 ? launch_tc_epi<BF16, 256>(a, epi, mn, dc, grid, s)
+                     : launch_tc_epi<BF16, 128>(a, epi, mn, dc, grid, s);
 }
 
 int launch_fail(cudaError_t e) {
@@ -1142,6 +1188,8 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
                                 "orthogonalisation: MN-major operands serve bf16 Gram products");
         all256 = all256 && g.N % 256 == 0;
     }
+    if (g0.precision == CAM_ORTHO_BF16 && g0.beta != 0.0f)
+        return record_error(CAM_E_ARG, "orthogonalisation: a bf16 product takes no C term");
     if (g0.precision == CAM_ORTHO_FP32) {
         for (int i = 0; i < n; ++i) {
             const int rc = run_simt(gs[i], sm_count, s, launches);
@@ -1252,16 +1300,26 @@ int nt_gemm(const NtGemm* gs, int n, int sm_count, int32_t* status, cudaStream_t
             if (P.has_y) rc = out_map(&P.ty, eb, g.Y, g.N, g.M, g.batch, g.ldy, g.sY, true);
             if (rc == CAM_OK && P.has_yt)
                 rc = out_map(&P.tyt, eb, g.Yt, g.M, g.N, g.batch, g.ldyt, g.sYt, false);
-            if (rc == CAM_OK && epi == kEpiAxpbyC)  // C, read in boxes like the row-major output
+            if (rc == CAM_OK && epi == kEpiAxpbyC) {  // C: in boxes like the row-major output, or directly
                 rc = out_map(&P.tcm, eb, g.C, g.N, g.M, g.batch, g.ldc, g.sC, true);
+                P.c = static_cast<const float*>(g.C);
+                P.ldc = g.ldc;
+                P.sc = g.sC;
+            }
             units += P.m_blocks * P.n_blocks * g.batch;
         }
         if (rc != CAM_OK) return rc;
     }
     a.n_units = units;
     const int grid = std::min(units, sm_count);
-    const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, mn, grid, s)
-                               : launch_tc_any<false>(a, bn, epi, mn, grid, s);
+    // the C term read directly, with a fourth ring stage, when every
+    // product's K loop is long enough (1,024 or more) to hide the epilogue's
+    // slower C reads; TMA boxes of C otherwise (measured: the 2,048-wide list
+    // 6 % faster direct, the 512-wide stand 8 % slower)
+    bool dc = true;
+    for (int i = 0; i < n; ++i) dc = dc && gs[i].K >= 1024;
+    const cudaError_t e = bf16 ? launch_tc_any<true>(a, bn, epi, mn, dc, grid, s)
+                               : launch_tc_any<false>(a, bn, epi, mn, dc, grid, s);
     ++*launches;
     if (e != cudaSuccess) return launch_fail(e);
     // the split Gram products' partials, summed in range order
