@@ -2,6 +2,7 @@
 // of libcam. Not part of the C ABI (include/cam.h is).
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -82,6 +83,47 @@ struct NormArgs {
     int32_t shared;
 };
 
+// The divisor of a round's division (the worker count in plain-mean mode,
+// the token total in delta mode) and what its reciprocal form needs: the
+// reciprocal as two terms, y = RN(1/d) and y_lo = RN(1/d - y), and the
+// dividends s that take that form, |s| in [2^lo_e, 2^hi_e) -- as floats lo_f
+// and hi_f, and as the bit patterns [lo, lo + span) of |s|. For those no
+// intermediate of the form leaves the normal range (the derivation is at
+// div_fast in merge_device.cuh). A zero dividend gives itself; every other
+// dividend, and every dividend of a divisor outside [2^-100, 2^100]
+// (active 0: span 0, lo_f = inf, hi_f = 0), takes the division instruction
+// sequence.
+struct DivPlan {
+    float d;
+    float y;
+    float y_lo;
+    float lo_f;
+    float hi_f;
+    uint32_t lo;
+    uint32_t span;
+    uint32_t active;
+};
+
+inline DivPlan div_plan(float d) {
+    // (host binary32 division: correctly rounded; 1/d - y is exact in binary64
+    // up to the binary64 quotient's rounding, 2^-53 of 1/d)
+    const float y = 1.0f / d;
+    DivPlan p{d, y, static_cast<float>(1.0 / static_cast<double>(d) - static_cast<double>(y)),
+              HUGE_VALF, 0.0f, 0u, 0u, 0u};
+    if (d >= 0x1p-100f && d <= 0x1p100f) {
+        int e = 0;
+        std::frexp(d, &e);  // d in [2^(e-1), 2^e)
+        const int lo_e = e - 124 > -100 ? e - 124 : -100;
+        const int hi_e = e + 124 < 126 ? e + 124 : 126;
+        p.lo_f = std::ldexp(1.0f, lo_e);
+        p.hi_f = std::ldexp(1.0f, hi_e);
+        p.lo = static_cast<uint32_t>(lo_e + 127) << 23;
+        p.span = (static_cast<uint32_t>(hi_e + 127) << 23) - p.lo;
+        p.active = 1u;
+    }
+    return p;
+}
+
 // Dynamic shared memory of a fused finish that stages the partials, the
 // squared norms and the chunk index of a fragment of n_tensors tensors and
 // n_chunks chunks; launches give it when it is at most kFinishSmemMax.
@@ -107,6 +149,8 @@ struct MergeArgs {
     float W;                  // (float)sum tokens
     float lr, mu, beta;
     float swa_n;              // globals in the running average after this round
+    DivPlan div;              // the division: by Kf (plain mean) or W (delta)
+    DivPlan swa_div;          // the running average's division, by swa_n
     int32_t* status;          // device status word (kStatus* bits)
     int32_t st_stages;        // staged pass: stages in the shared-memory ring
     int32_t st_stage_bytes;   // staged pass: bytes of one stage
@@ -173,7 +217,7 @@ constexpr int kMultiXCap = 3584;                // worker and copy pointers per 
 // One round of a multi-round pass: its fragment's tables, its finish, the
 // place of its chunks among the pass's and of its pointers in x[], and the
 // scalars the per-element arithmetic reads (merge_elem's K, Kf, w, W, lr, mu,
-// beta).
+// beta, div).
 struct MultiRound {
     const ChunkDesc* chunks;   // the fragment's chunk table (device)
     const TensorSlot* slots;   // the fragment's tensors, by local index (device)
@@ -190,6 +234,7 @@ struct MultiRound {
     float Kf;
     float w[CAM_KMAX];
     float W, lr, mu, beta;
+    DivPlan div;               // the division: by Kf (plain mean) or W (delta)
 };
 
 struct MultiArgs {

@@ -172,11 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2) final_pass(const __grid_constant_
                         }
                     }
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    merge_finish<MODE, EMA, NORM>(a, sv[j], th[j], m[j], e[j], acc);
-                    if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
-                }
+                merge_finish_n<8, MODE, EMA, NORM, SWA>(a, sv, th, m, e, sw, acc);
                 store_s8(th_p + 8 * v, th);
                 if (MODE == kDelta) store_s8(m_p + 8 * v, m);
                 if (EMA) store_s8(e_p + 8 * v, e);

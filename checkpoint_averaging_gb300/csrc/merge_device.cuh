@@ -6,7 +6,7 @@
 // delta mean, plain replacement or outer Nesterov, EMA of the globals, squared
 // drift. Explicit round-to-nearest intrinsics keep every multiply and add
 // separately rounded. The argument block type A provides K, Kf, w[], W, lr,
-// mu and beta.
+// mu, beta and div (the division's DivPlan: by Kf or by W).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -144,25 +144,96 @@ __device__ __forceinline__ void store_s8(float* p, const float (&v)[8]) {
         : "memory");
 }
 
+// ---- division --------------------------------------------------------------
+
+// s / d correctly rounded -- the bits __fdiv_rn(s, d) gives -- for the round's
+// divisor d = p.d, from its reciprocal held as two binary32 terms, y = p.y =
+// RN(1/d) and y_lo = p.y_lo = RN(1/d - y), and one of Markstein's
+// corrections (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990; also Muller
+// et al., "Handbook of Floating-Point Arithmetic", division with a fused
+// multiply-add):
+//   q0 = RN(s*y + RN(s*y_lo))   within one unit in the last place of s/d:
+//                               the two terms carry 1/d to about 2^-47 of
+//                               itself, so the sum is s/d to within
+//                               |s/d| * 2^-46 before its one rounding
+//   r  = s - d*q0               exact, q0 being faithful (one fused multiply-add)
+//   q  = RN(q0 + r*y)           = RN(s/d) by Markstein's theorem (y within
+//                               half a unit of 1/d, q0 faithful, r exact)
+// All of it holds while nothing leaves the normal range. div_plan admits
+// d in [2^(e-1), 2^e) inside [2^-100, 2^100] and |s| in
+// [2^max(-100, e-124), 2^min(126, e+124)): then |s/d| lies in
+// [2^-124, 2^125), so q0 and q are normal and d*q0 finite, s*y_lo loses at
+// most 2^-150 to underflow (far below a unit of q0), and r is an integer
+// multiple of ulp(d)*ulp(q0) >= 2^-148, fewer than 2^24 of them, so
+// representable. A zero dividend gives itself (+-0 / d is +-0 for the plan's
+// positive d). Every other s outside the range (smaller, larger, infinite,
+// NaN), and every s of a divisor out of range (p.active 0), takes __fdiv_rn,
+// out of line.
+
+// |s| inside the plan's range (zeros are not).
+__device__ __forceinline__ bool div_in_range(float s, const DivPlan& p) {
+    return (__float_as_uint(s) & 0x7FFFFFFFu) - p.lo < p.span;
+}
+
+__device__ __forceinline__ float div_fast(float s, const DivPlan& p) {
+    const float q0 = __fmaf_rn(s, p.y, __fmul_rn(s, p.y_lo));
+    return __fmaf_rn(__fmaf_rn(-p.d, q0, s), p.y, q0);
+}
+
+static __device__ __noinline__ float div_rn_slow(float s, float d) { return __fdiv_rn(s, d); }
+
+// A dividend outside the range.
+__device__ __forceinline__ float div_outside(float s, const DivPlan& p) {
+    return (s == 0.0f && p.active) ? s : div_rn_slow(s, p.d);
+}
+
+// One quotient (the passes' scalar tails).
+__device__ __forceinline__ float div_rn(float s, const DivPlan& p) {
+    return div_in_range(s, p) ? div_fast(s, p) : div_outside(s, p);
+}
+
+// N quotients: the reciprocal form for all of them, then one test of the N
+// dividends against the range: t = 2|s| - 2^(lo_e + 1) as bit patterns
+// (the sign shifted out) lies below 2*span for every |s| in range and at or
+// above it for every other s (a zero wraps around to a large t), so the
+// largest t decides for all N, at a shift-add and a maximum per element.
+// Only when that test fails -- a zero, a dividend out of range, a divisor
+// out of range -- are the N checked one by one and those outside the range
+// taken again by div_outside. The merge loops so take one branch per N
+// elements, and the N elements' arithmetic stays one straight run of code.
+template <int N>
+__device__ __forceinline__ void div_rn_n(const float (&s)[N], float (&q)[N], const DivPlan& p) {
+    uint32_t tmax = 0u;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        q[j] = div_fast(s[j], p);
+        tmax = max(tmax, (__float_as_uint(s[j]) << 1) - (p.lo << 1));
+    }
+    if (tmax >= (p.span << 1)) {
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if (!div_in_range(s[j], p)) q[j] = div_outside(s[j], p);
+    }
+}
+
 // ---- per-element arithmetic ----------------------------------------------------
 
-// What follows the fold for one element: s is the arrival-order sum (the
-// plain sum of the workers, or the token-weighted sum of their deltas);
-// finalize, outer step and EMA update th, m, e in place, and acc collects the
-// squared drift. Shared by the fused pass and the final pass of eagerly folded
-// rounds, so both produce the same bits.
+// What follows the fold and the division for one element: q is the quotient
+// (the mean s / K, or the token-weighted delta mean s / W); outer step and
+// EMA update th, m, e in place, and acc collects the squared drift. Shared by
+// every pass, so all produce the same bits.
 template <int MODE, bool EMA, bool NORM, class A>
-__device__ __forceinline__ void merge_finish(const A& a, float s, float& th, float& m, float& e,
+__device__ __forceinline__ void merge_update(const A& a, float q, float& th, float& m, float& e,
                                              float& acc) {
     if (MODE == kMean) {
-        const float mean = __fdiv_rn(s, a.Kf);
         if (NORM) {
-            const float d = __fsub_rn(mean, th);
+            const float d = __fsub_rn(q, th);
             acc = __fmaf_rn(d, d, acc);
         }
-        th = mean;  // plain replacement
+        th = q;  // plain replacement
     } else {
-        const float delta = __fdiv_rn(s, a.W);
+        const float delta = q;
         if (NORM) acc = __fmaf_rn(delta, delta, acc);
         const float g = -delta;  // pseudo-gradient theta - (theta + delta)
         const float m_new = __fadd_rn(__fmul_rn(a.mu, m), g);
@@ -176,6 +247,14 @@ __device__ __forceinline__ void merge_finish(const A& a, float s, float& th, flo
     }
 }
 
+// The division and merge_update for one element: s is the arrival-order sum
+// (the plain sum of the workers, or the token-weighted sum of their deltas).
+template <int MODE, bool EMA, bool NORM, class A>
+__device__ __forceinline__ void merge_finish(const A& a, float s, float& th, float& m, float& e,
+                                             float& acc) {
+    merge_update<MODE, EMA, NORM>(a, div_rn(s, a.div), th, m, e, acc);
+}
+
 // One worker's term of the arrival-order fold: s + x (plain mean) or
 // s + w * (x - theta) (token-weighted delta mean), one rounding per operation.
 template <int MODE>
@@ -183,23 +262,30 @@ __device__ __forceinline__ float fold_term(float s, float x, float w, float th) 
     return MODE == kMean ? __fadd_rn(s, x) : __fadd_rn(s, __fmul_rn(w, __fsub_rn(x, th)));
 }
 
-// One element of one round. xk[k] (k < K) are the workers' values in arrival
-// order; th, m, e are updated in place; acc collects the squared drift.
-template <int MODE, bool EMA, bool NORM, class A>
-__device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMAX],
-                                           float& th, float& m, float& e, float& acc) {
+// The arrival-order sum of one element: xk[k] (k < K) are the workers'
+// values in arrival order.
+template <int MODE, class A>
+__device__ __forceinline__ float merge_fold(const A& a, const float (&xk)[CAM_KMAX], float th) {
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < CAM_KMAX; ++k)
         if (k < a.K) s = fold_term<MODE>(s, xk[k], MODE == kMean ? 1.0f : a.w[k], th);
-    merge_finish<MODE, EMA, NORM>(a, s, th, m, e, acc);
+    return s;
+}
+
+// One element of one round: th, m, e are updated in place; acc collects the
+// squared drift.
+template <int MODE, bool EMA, bool NORM, class A>
+__device__ __forceinline__ void merge_elem(const A& a, const float (&xk)[CAM_KMAX],
+                                           float& th, float& m, float& e, float& acc) {
+    merge_finish<MODE, EMA, NORM>(a, merge_fold<MODE>(a, xk, th), th, m, e, acc);
 }
 
 // Folds the new global into the uniform running average: mu + (theta' - mu)/n,
 // n = the number of globals in the average after this one.
 template <class A>
 __device__ __forceinline__ float swa_fold(const A& a, float mu, float th) {
-    return __fadd_rn(mu, __fdiv_rn(__fsub_rn(th, mu), a.swa_n));
+    return __fadd_rn(mu, div_rn(__fsub_rn(th, mu), a.swa_div));
 }
 
 // Per-worker drift: accw[k] += (x_k - theta_old)^2 for k < K, before the
@@ -213,6 +299,46 @@ __device__ __forceinline__ void worker_drift(const A& a, const float (&xk)[CAM_K
             const float d = __fsub_rn(xk[k], th);
             accw[k] = __fmaf_rn(d, d, accw[k]);
         }
+}
+
+// N elements whose sums s[] are formed: their quotients (div_rn_n), then
+// merge_update element by element and, with SWA, the running average.
+template <int N, int MODE, bool EMA, bool NORM, bool SWA, class A>
+__device__ __forceinline__ void merge_finish_n(const A& a, const float (&s)[N], float (&th)[N],
+                                               float (&m)[N], float (&e)[N], float (&sw)[N],
+                                               float& acc) {
+    float q[N];
+    div_rn_n<N>(s, q, a.div);
+#pragma unroll
+    for (int j = 0; j < N; ++j) merge_update<MODE, EMA, NORM>(a, q[j], th[j], m[j], e[j], acc);
+    if constexpr (SWA) {  // swa_fold's operations, the N divisions together
+        float dv[N], qv[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) dv[j] = __fsub_rn(th[j], sw[j]);
+        div_rn_n<N>(dv, qv, a.swa_div);
+#pragma unroll
+        for (int j = 0; j < N; ++j) sw[j] = __fadd_rn(sw[j], qv[j]);
+    }
+}
+
+// N elements of one step, worker k's value of element j given by xv(k, j):
+// in element order each worker's squared drift (WD) and the fold, then
+// merge_finish_n. Per element the operations and their order are
+// merge_elem's, and acc and accw collect in element order.
+template <int N, int MODE, bool EMA, bool NORM, bool SWA, bool WD, class A, class XV>
+__device__ __forceinline__ void merge_group(const A& a, const XV& xv, float (&th)[N],
+                                            float (&m)[N], float (&e)[N], float (&sw)[N],
+                                            float& acc, float* accw) {
+    float s[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        float xk[CAM_KMAX];
+#pragma unroll
+        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = xv(k, j);
+        if constexpr (WD) worker_drift(a, xk, th[j], accw);
+        s[j] = merge_fold<MODE>(a, xk, th[j]);
+    }
+    merge_finish_n<N, MODE, EMA, NORM, SWA>(a, s, th, m, e, sw, acc);
 }
 
 // xs[0..K) are the workers' copies of the tensor; with PUB, xs[K] receives a
@@ -237,15 +363,8 @@ __device__ __forceinline__ void merge_vecn_f32(const A& a, const void* const* xs
     if (MODE == kDelta) load_sn<N>(ts.m + i, m);
     if (EMA) load_sn<N>(ts.e + i, e);
     if constexpr (SWA) load_sn<N>(ts.swa + i, sw);
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-        float xk[CAM_KMAX];
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k][j];
-        if constexpr (WD) worker_drift(a, xk, th[j], accw);
-        merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
-        if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
-    }
+    merge_group<N, MODE, EMA, NORM, SWA, WD>(a, [&](int k, int j) { return x[k][j]; }, th, m, e, sw,
+                                             acc, accw);
     store_sn<N>(ts.theta + i, th);
     if constexpr (SWA) store_sn<N>(ts.swa + i, sw);
     if (MODE == kDelta) store_sn<N>(ts.m + i, m);
@@ -279,15 +398,8 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
     if (EMA) load_s8(ts.e + i, e);
     float sw[8];
     if constexpr (SWA) load_s8(ts.swa + i, sw);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float xk[CAM_KMAX];
-#pragma unroll
-        for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
-        if constexpr (WD) worker_drift(a, xk, th[j], accw);
-        merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
-        if constexpr (SWA) sw[j] = swa_fold(a, sw[j], th[j]);
-    }
+    merge_group<8, MODE, EMA, NORM, SWA, WD>(a, [&](int k, int j) { return x[k].get(j); }, th, m, e,
+                                             sw, acc, accw);
     store_s8(ts.theta + i, th);
     if constexpr (SWA) store_s8(ts.swa + i, sw);
     if (MODE == kDelta) store_s8(ts.m + i, m);

@@ -48,6 +48,7 @@ struct NoAllocArgs {
     float w[CAM_KMAX];
     float W;
     float lr, mu, beta;
+    DivPlan div;       // the division: by Kf (plain mean) or W (delta)
     double* partials;  // scratch entry of this launch's first chunk
     int32_t n_chunks;
     int32_t n_local;
@@ -301,6 +302,7 @@ CAM_API int cam_merge_round_noalloc(int32_t n_tensors, const int64_t* numel, flo
     for (int k = 0; k < CAM_KMAX; ++k)
         a.w[k] = (delta && k < n_workers) ? static_cast<float>(tokens[k]) : 0.0f;
     a.W = static_cast<float>(W);
+    a.div = cam::div_plan(delta ? a.W : a.Kf);
     a.lr = lr;
     a.mu = mu;
     a.beta = beta;

@@ -1006,10 +1006,12 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
     a.Kf = static_cast<float>(K);
     for (int k = 0; k < CAM_KMAX; ++k) a.w[k] = k < K ? static_cast<float>(r->tokens[k]) : 0.0f;
     a.W = static_cast<float>(W);
+    a.div = cam::div_plan(delta ? a.W : a.Kf);
     a.lr = r->lr;
     a.mu = r->mu;
     a.beta = r->beta;
     a.swa_n = static_cast<float>(swa_prev + 1);
+    a.swa_div = cam::div_plan(a.swa_n);
     const int norm_level = r->worker_norms ? 2 : (r->norms ? 1 : 0);
     const int bps = c->bps[r->dtype][r->mode][r->ema][norm_level][r->publish][r->swa];
     // CAM_SHARE_SMS: a pass takes at most three quarters of the register
@@ -1134,10 +1136,12 @@ CAM_API int cam_merge_commit(cam_round* r, void* stream) {
         fa.K = K;
         fa.Kf = a.Kf;
         fa.W = a.W;
+        fa.div = a.div;
         fa.lr = a.lr;
         fa.mu = a.mu;
         fa.beta = a.beta;
         fa.swa_n = a.swa_n;
+        fa.swa_div = a.swa_div;
         const int P = K - r->n_folded;  // accumulated after the folds: folded here
         fa.P = P;
         fa.first_k = r->n_folded;
@@ -1360,6 +1364,7 @@ CAM_API int cam_merge_commit_many(cam_round* const* rounds, int32_t n, void* str
         R.Kf = static_cast<float>(K);
         for (int k = 0; k < CAM_KMAX; ++k) R.w[k] = k < K ? static_cast<float>(r->tokens[k]) : 0.0f;
         R.W = static_cast<float>(W);
+        R.div = cam::div_plan(r->mode == CAM_MODE_DELTA_NESTEROV ? R.W : R.Kf);
         R.lr = r->lr;
         R.mu = r->mu;
         R.beta = r->beta;

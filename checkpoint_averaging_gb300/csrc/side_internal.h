@@ -50,6 +50,8 @@ struct FinalArgs {
     float W;                   // (float)sum tokens
     float lr, mu, beta;
     float swa_n;               // globals in the running average after this round
+    DivPlan div;               // the division: by Kf (plain mean) or W (delta)
+    DivPlan swa_div;           // the running average's division, by swa_n
     int32_t stride;            // pointers per tensor in ptr[]: 3 + P
     int32_t P;                 // workers folded by this pass
     int32_t first_k;           // arrival index of the first of them (the folds before)
