@@ -413,13 +413,26 @@ def run_ours(args, wl, ws, rank, local) -> int:
         load[stream_of[i]] += rb[i]
 
     many = max(0, args.many if args.many is not None else wl.commit_many)
+    one_call = args.api == "round"
+    if one_call and (many >= 2 or wl.swa or wl.worker_norms):
+        raise SystemExit("bench.py: --api round takes rounds without SWA, per-worker drift or "
+                         "--many")
+    round_ckpts = [[prepared[i][k] for k in d.included] for i, d in enumerate(draws)]
+    round_tokens = [[d.tokens[k] for k in d.included] if wl.mode == "delta" else None
+                    for d in draws]
+    # CUDA events for the timed region, made (and their CUDA events created by
+    # a first record) before it, so that making them is not timed
+    ev_pool = []
+
+    def new_event():
+        return ev_pool.pop() if ev_pool else torch.cuda.Event(enable_timing=True)
 
     def step_many(timed: bool) -> None:
         # the step's rounds opened, then committed in groups of `many` rounds
         # by one call each (cam_merge_commit_many), all on the main stream
         main = streams[0]
         if timed:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a, b = new_event(), new_event()
             a.record(main)
         for g0 in range(0, len(wl.rounds), many):
             opened = []
@@ -450,12 +463,24 @@ def run_ours(args, wl, ws, rank, local) -> int:
             return
         main = streams[0]
         if timed and n_streams > 1:
-            ga = torch.cuda.Event(enable_timing=True)
+            ga = new_event()
             ga.record(main)
         for s in streams[1:]:
             s.wait_stream(main)
         for i, ((_, frag), w, d) in enumerate(zip(wl.rounds, workers, draws)):
             s = streams[stream_of[i]]
+            if one_call:  # the whole round through cam_merge_round
+                if timed:
+                    a, b = new_event(), new_event()
+                    a.record(s)
+                mg.merge(round_no[0], round_ckpts[i], round_tokens[i], fragment=frag, mode=mode,
+                         lr=wl.lr, mu=wl.mu, ema_beta=wl.ema_beta,
+                         norms=norm_out[i] if wl.norms else None, stream=s)
+                round_no[0] += 1
+                if timed:
+                    b.record(s)
+                    ev_pairs.append((a, b))
+                continue
             rd = mg.begin(round_no[0], frag)
             round_no[0] += 1
             for k in d.included:
@@ -470,7 +495,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
             if wl.worker_norms:
                 rd.worker_drift_norm(*wnorm_out[i])
             if timed:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a, b = new_event(), new_event()
                 a.record(s)
             rd.commit(s)
             if timed:
@@ -479,7 +504,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
         for s in streams[1:]:
             main.wait_stream(s)
         if timed and n_streams > 1:
-            gb = torch.cuda.Event(enable_timing=True)
+            gb = new_event()
             gb.record(main)
             group_pairs.append((ga, gb))
 
@@ -497,6 +522,10 @@ def run_ours(args, wl, ws, rank, local) -> int:
             graph.replay()  # its first replay uploads it
         torch.cuda.synchronize(dev)
     launches0, staged0 = mg.launch_count, mg.staged_count
+    ev_pool.extend(torch.cuda.Event(enable_timing=True)
+                   for _ in range(args.steps * (2 * len(wl.rounds) + 2)))
+    for e in ev_pool:
+        e.record(streams[0])
     barrier(ws)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
@@ -508,8 +537,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
                 step(True)
                 continue
             with torch.cuda.stream(streams[0]):
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
+                a, b = new_event(), new_event()
                 a.record(streams[0])
                 graph.replay()
                 b.record(streams[0])
@@ -591,7 +619,7 @@ def run_ours(args, wl, ws, rank, local) -> int:
                        "streams": 1 if many >= 2 else n_streams, "commit_many": many,
                        "bytes_per_step": step_bytes,
                        "l2": "inputs larger than L2 (no flush needed)",
-                       "parallelism": f"replicas{ws}", "cuda_graph": bool(args.graph),
+                       "parallelism": f"replicas{ws}", "cuda_graph": bool(args.graph), "api": args.api,
                        "fused_finish": not args.no_fused_finish,
                        "share_sms": args.share_sms or wl.share_sms},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -1031,7 +1059,9 @@ def run_hostcost(args, wl, ws, rank, local) -> int:
     ahead of time, each call timed with perf_counter_ns. ctypes' own cost per
     call, taken from a call that does nothing (cam_ctx_launch_count), is
     reported beside it and subtracted in `library_us_per_round`. The same
-    rounds through the binding's Merger/Round give `binding_us_per_round`.
+    rounds through the binding's Merger/Round give `binding_us_per_round`,
+    and through Merger.merge and a bare cam_merge_round call (one host call
+    per round) `one_call`.
     The device is synchronised between batches of rounds, outside the timed
     calls, so no call waits for a full launch queue."""
     import ctypes
@@ -1118,6 +1148,37 @@ def run_hostcost(args, wl, ws, rank, local) -> int:
             rd.drift_norm(*norm_out[i])
         rd.commit(s)
 
+    round_ck = [[prepared[i][k] for k in d.included] for i, d in enumerate(draws)]
+    round_tok = [[d.tokens[k] for k in d.included] if wl.mode == "delta" else None for d in draws]
+
+    def one_call_round(i):
+        mg.merge(rnd[0], round_ck[i], round_tok[i], fragment=wl.rounds[i][1], mode=mode,
+                 lr=wl.lr, mu=wl.mu, ema_beta=wl.ema_beta,
+                 norms=norm_out[i] if wl.norms else None, stream=s)
+        rnd[0] += 1
+
+    # the same call through ctypes alone, its arguments made ahead of time
+    raw_args = []
+    for i, ((_, frag), d) in enumerate(zip(wl.rounds, draws)):
+        arr = (ctypes.POINTER(ctypes.c_void_p) * len(round_ck[i]))(*[c.ptr_array for c in round_ck[i]])
+        tok = None if round_tok[i] is None else (ctypes.c_int64 * len(round_tok[i]))(*round_tok[i])
+        pt, pf = norm_out[i]
+        raw_args.append((frag, len(round_ck[i]), arr, round_ck[i][0].dtype_code, tok,
+                         ctypes.c_void_p(pt.data_ptr()) if wl.norms else None,
+                         ctypes.c_void_p(pf.data_ptr()) if wl.norms else None))
+    raw_one_ns = [0]
+
+    def raw_one_call(i):
+        frag, n, arr, dt, tok, pt, pf = raw_args[i]
+        t = ns()
+        rc = L.cam_merge_round(mg.ctx, rnd[0], frag, n, arr, dt, tok, mode, wl.lr, wl.mu,
+                               0 if wl.ema_beta is None else 1,
+                               0.0 if wl.ema_beta is None else wl.ema_beta, pt, pf, sp)
+        raw_one_ns[0] += ns() - t
+        rnd[0] += 1
+        if rc != 0:
+            raise RuntimeError(B.last_error())
+
     n_rounds, batch = 600, 30
     for i in range(len(wl.rounds) * 3):  # warm-up
         raw_round(i % len(wl.rounds))
@@ -1145,6 +1206,19 @@ def run_hostcost(args, wl, ws, rank, local) -> int:
         if (j + 1) % batch == 0:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
+    one_ns = 0
+    for j in range(n_rounds):
+        t = ns()
+        one_call_round(j % len(wl.rounds))
+        one_ns += ns() - t
+        if (j + 1) % batch == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    for j in range(n_rounds):
+        raw_one_call(j % len(wl.rounds))
+        if (j + 1) % batch == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
     mg.close()
     print(json.dumps({
         "metric": "host us per round (C ABI)", "value": round(raw_us - calls_per_round * noop_us, 2),
@@ -1154,7 +1228,11 @@ def run_hostcost(args, wl, ws, rank, local) -> int:
         "library_us_per_round": round(raw_us - calls_per_round * noop_us, 2),
         "ctypes_us_per_round": round(raw_us, 2), "ctypes_noop_us_per_call": round(noop_us, 3),
         "per_call_us_with_ctypes": {c: round(v, 2) for c, v in per_call.items()},
-        "binding_us_per_round": round(bind_ns / n_rounds / 1e3, 2)}), flush=True)
+        "binding_us_per_round": round(bind_ns / n_rounds / 1e3, 2),
+        "one_call": {"binding_us_per_round": round(one_ns / n_rounds / 1e3, 2),
+                     "library_us_per_round": round(raw_one_ns[0] / n_rounds / 1e3 - noop_us, 2),
+                     "note": "Merger.merge / cam_merge_round: the same round in one call"}}),
+          flush=True)
     return 0
 
 
@@ -1176,6 +1254,9 @@ def parse(argv=None):
     p.add_argument("--many", type=int, default=None,
                    help="commit the step's rounds in groups of this many by one call "
                         "(cam_merge_commit_many); 0: one commit per round (default: the workload's)")
+    p.add_argument("--api", choices=("steps", "round"), default="steps",
+                   help="merge op: each round through begin/accumulate/finalize/.../commit "
+                        "(steps) or through one cam_merge_round call (round)")
     p.add_argument("--graph", action="store_true",
                    help="capture one step of the merge op into a CUDA graph and time its replays")
     p.add_argument("--fold-last", action="store_true",

@@ -114,7 +114,8 @@ EXPORTS = ("cam_ctx_create", "cam_ctx_destroy", "cam_merge_begin", "cam_merge_ac
            "cam_swa_update", "cam_swa_reset", "cam_worker_drift_norm", "cam_adopt_keep_drift",
            "cam_merge_orthogonalize", "cam_swa_counts", "cam_swa_set_counts",
            "cam_merge_finalize", "cam_ema_update", "cam_drift_norm", "cam_merge_commit",
-           "cam_merge_commit_many", "cam_merge_abort", "cam_fragment_info", "cam_ctx_get_last_round",
+           "cam_merge_commit_many", "cam_merge_abort", "cam_merge_round", "cam_fragment_info",
+           "cam_ctx_get_last_round",
            "cam_ctx_set_last_round", "cam_ctx_launch_count", "cam_ctx_status",
            "cam_ctx_staged_count", "cam_ctx_last_commit", "cam_stream_capturing",
            "cam_ctx_get_quorum", "cam_ctx_set_quorum",
@@ -157,6 +158,9 @@ def lib() -> ctypes.CDLL:
     L.cam_merge_commit.argtypes = [vp, vp]
     L.cam_merge_commit_many.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32, vp]
     L.cam_merge_abort.argtypes = [vp]
+    L.cam_merge_round.argtypes = [vp, i64, i32, i32, ctypes.POINTER(vpp), ctypes.c_int,
+                                  ctypes.POINTER(i64), ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_float, i32, ctypes.c_float, vp, vp, vp]
     L.cam_fragment_info.argtypes = [vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                     ctypes.POINTER(i32)]
     L.cam_ctx_get_last_round.argtypes = [vp, ctypes.POINTER(i64)]
@@ -457,7 +461,7 @@ def _record_streams(tensors, stream, handle: int) -> list:
     own hold."""
     host = []
     for t in tensors:
-        if t.device.type != "cuda":
+        if not t.is_cuda:
             host.append(t)
             continue
         seen = getattr(t, "_cam_recorded_streams", None)
@@ -545,6 +549,7 @@ class Merger:
                 rows=list(rows) if rows is not None else
                 [t.shape[0] if t.dim() >= 2 else 0 for t in self.master])
         self._frag_cache = {}
+        self._round_args = {}  # merge(): marshalled arguments by (fragment, checkpoints, tokens)
         self._inflight = []  # (event, host tensors) held until the work reading them ran
 
     def close(self):
@@ -634,6 +639,64 @@ class Merger:
             self._rounds = weakref.WeakSet()
         self._rounds.add(rd)
         return rd
+
+    def merge(self, round: int, ckpts, tokens=None, *, fragment: int = -1,
+              mode: int = MEAN_REPLACE, lr: float = 1.0, mu: float = 0.0, ema_beta=None,
+              norms=None, stream=None) -> None:
+        """One whole round in one host call (cam_merge_round): the same as
+        begin(round, fragment), accumulate of each worker of `ckpts` in
+        arrival order with its `tokens`, finalize(mode, lr, mu),
+        ema_update(ema_beta) when it is given, drift_norm(*norms) when norms
+        = (per_tensor, per_fragment) is given, and commit(stream), with the
+        same results. ckpts are device-resident Checkpoints made for
+        `fragment`, or tensor lists (made into Checkpoints at each call).
+        Host-resident workers are not taken here: open the round with begin
+        and accumulate them. The marshalled arguments of Checkpoint lists are
+        kept for the next call with the same Checkpoints and tokens."""
+        torch = _torch()
+        key = None
+        if all(isinstance(c, Checkpoint) for c in ckpts):
+            key = (fragment, tuple(map(id, ckpts)), None if tokens is None else tuple(tokens))
+        hit = None if key is None else self._round_args.get(key)
+        if hit is None:
+            cks = [c if isinstance(c, Checkpoint) and c.merger is self and c.fragment == fragment
+                   else Checkpoint(self, c, fragment) for c in ckpts]
+            if not cks or len(cks) > KMAX:
+                raise ValueError(f"a round takes 1 to {KMAX} workers")
+            if any(c.host for c in cks):
+                raise ValueError("host-resident checkpoints go through Round.accumulate")
+            if any(c.dtype_code != cks[0].dtype_code for c in cks):
+                raise ValueError("every worker of a round must have the same dtype")
+            arr = (ctypes.POINTER(ctypes.c_void_p) * len(cks))(*[c.ptr_array for c in cks])
+            tok = None if tokens is None else (ctypes.c_int64 * len(cks))(*map(int, tokens))
+            keep = [t for c in cks for t in c.keep]
+            hit = (arr, tok, cks[0].dtype_code, keep, list(ckpts))
+            if key is not None:
+                if len(self._round_args) >= 64:
+                    self._round_args.clear()
+                self._round_args[key] = hit  # (it holds the Checkpoints: their ids stay theirs)
+        arr, tok, dtype, keep, _ = hit
+        pt = pf = None
+        if norms is not None:
+            pt, pf = norms
+            for t, n in ((pt, len(self.fragment_tensors(fragment))), (pf, 1)):
+                if t is not None and (t.device != self.device or t.dtype != torch.float64
+                                      or not t.is_contiguous() or t.numel() < n):
+                    raise ValueError("norm outputs must be contiguous fp64 device tensors")
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        sh = int(s.cuda_stream)
+        _check(lib().cam_merge_round(
+            self.ctx, int(round), int(fragment), len(arr), arr, dtype, tok, int(mode),
+            float(lr), float(mu), 0 if ema_beta is None else 1,
+            0.0 if ema_beta is None else float(ema_beta),
+            None if pt is None else pt.data_ptr(), None if pf is None else pf.data_ptr(),
+            sh or None))
+        if stream_capturing(sh):
+            return  # a captured graph reads its buffers at every replay: they are the caller's
+        outs = [t for t in (pt, pf) if t is not None]
+        _record_streams(keep + outs if outs else keep, s, sh)
+        if self._inflight:
+            self._hold_until_done([], s)
 
     def checkpoint(self, ckpt, fragment: int = -1) -> "Checkpoint":
         """Validates a worker's tensors once for rounds on `fragment`."""

@@ -1575,3 +1575,32 @@ CAM_API int cam_ctx_set_last_round(cam_ctx* c, int64_t round) {
     c->last_round = round;
     return CAM_OK;
 }
+
+CAM_API int cam_merge_round(cam_ctx* c, int64_t round, int32_t fragment, int32_t n_workers,
+                            const void* const* const* ckpt, cam_dtype dtype,
+                            const int64_t* tokens, cam_mode mode, float lr, float mu,
+                            int32_t do_ema, float beta, double* per_tensor, double* per_fragment,
+                            void* stream) {
+    const char* fn = "cam_merge_round";
+    if (!c) return fail(CAM_E_ARG, "%s: ctx is NULL", fn);
+    if (!ckpt || n_workers < 1 || n_workers > CAM_KMAX)
+        return fail(CAM_E_ARG, "%s: %d workers (1 to %d, with their pointer arrays)", fn,
+                    static_cast<int>(n_workers), CAM_KMAX);
+    cam_round* r = nullptr;
+    if (const int rc = cam_merge_begin(c, round, fragment, &r); rc != CAM_OK) return rc;
+    int rc = CAM_OK;
+    for (int32_t k = 0; rc == CAM_OK && k < n_workers; ++k)
+        rc = cam_merge_accumulate(r, ckpt[k], dtype, tokens ? tokens[k] : 0);
+    if (rc == CAM_OK) rc = cam_merge_finalize(r, mode, lr, mu);
+    if (rc == CAM_OK && do_ema) rc = cam_ema_update(r, beta);
+    if (rc == CAM_OK && (per_tensor || per_fragment))
+        rc = cam_drift_norm(r, per_tensor, per_fragment);
+    // the commit's own checks first, so that a round that fails them is dropped
+    // here (cam_merge_commit leaves such a round open for its caller)
+    if (rc == CAM_OK) rc = commit_checks(r, capturing(static_cast<cudaStream_t>(stream)), fn);
+    if (rc != CAM_OK) {
+        close_round(r);  // nothing launched; the failing step's message stays
+        return rc;
+    }
+    return cam_merge_commit(r, stream);  // closes the round, launched or not
+}

@@ -433,6 +433,35 @@ int cam_merge_commit_many(cam_round* const* rounds, int32_t n, void* stream);
  * used. */
 int cam_merge_abort(cam_round* rd);
 
+/*
+ * One whole round in one call, for callers whose host time per round counts
+ * (small fragment rounds committed back to back, as in the Pythia-14M run:
+ * "Pythia-14M on four rented GPUs and a bucket", "Getting updates through
+ * the bucket"). It is cam_merge_begin(round, fragment); cam_merge_accumulate
+ * of workers 0 .. n_workers-1, in that (arrival) order; cam_merge_finalize
+ * (mode, lr, mu); cam_ema_update(beta) when do_ema is nonzero;
+ * cam_drift_norm(per_tensor, per_fragment) when either is non-NULL; and
+ * cam_merge_commit(stream): the same checks, launches and results, in one
+ * host call.
+ *
+ * ckpt is a host array of n_workers (1 .. CAM_KMAX) pointers, ckpt[k] worker
+ * k's host array of T_f device pointers in fragment order (as for
+ * cam_merge_accumulate), every worker of `dtype`. tokens is a host array of
+ * n_workers token counts, or NULL for none (then only MEAN_REPLACE can
+ * commit). per_tensor and per_fragment are device arrays as for
+ * cam_drift_norm, or NULL. The workers' buffers and the norm outputs are
+ * borrowed as for those calls, until the work has run on `stream`.
+ *
+ * On an error before the commit's launches nothing is launched, the round
+ * is dropped as by cam_merge_abort (its number counts as used) and the
+ * failing step's error is returned; an error in the launches is returned as
+ * cam_merge_commit returns it. Errors: those of the calls above.
+ */
+int cam_merge_round(cam_ctx* ctx, int64_t round, int32_t fragment, int32_t n_workers,
+                    const void* const* const* ckpt, cam_dtype dtype, const int64_t* tokens,
+                    cam_mode mode, float lr, float mu, int32_t do_ema, float beta,
+                    double* per_tensor, double* per_fragment, void* stream);
+
 /* Number of tensors and elements of `fragment` (-1: all), and its tensor
  * indices in fragment order when `tensor_ids` (host, [T_f]) is not NULL. */
 int cam_fragment_info(const cam_ctx* ctx, int32_t fragment, int32_t* n_tensors,
