@@ -524,8 +524,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
     launches0, staged0 = mg.launch_count, mg.staged_count
     ev_pool.extend(torch.cuda.Event(enable_timing=True)
                    for _ in range(args.steps * (2 * len(wl.rounds) + 2)))
-    for e in ev_pool:
-        e.record(streams[0])
+    for ev in ev_pool:
+        ev.record(streams[0])
     barrier(ws)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:

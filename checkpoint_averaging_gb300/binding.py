@@ -550,6 +550,7 @@ class Merger:
                 [t.shape[0] if t.dim() >= 2 else 0 for t in self.master])
         self._frag_cache = {}
         self._round_args = {}  # merge(): marshalled arguments by (fragment, checkpoints, tokens)
+        self._norm_args = {}  # merge(): validated norm outputs by (their ids, fragment)
         self._inflight = []  # (event, host tensors) held until the work reading them ran
 
     def close(self):
@@ -670,31 +671,55 @@ class Merger:
             arr = (ctypes.POINTER(ctypes.c_void_p) * len(cks))(*[c.ptr_array for c in cks])
             tok = None if tokens is None else (ctypes.c_int64 * len(cks))(*map(int, tokens))
             keep = [t for c in cks for t in c.keep]
-            hit = (arr, tok, cks[0].dtype_code, keep, list(ckpts))
+            # (the entry holds the Checkpoints, so the ids in its key stay
+            # theirs; the set names the streams their tensors are recorded on)
+            hit = (arr, tok, cks[0].dtype_code, keep, list(ckpts), set())
             if key is not None:
                 if len(self._round_args) >= 64:
                     self._round_args.clear()
-                self._round_args[key] = hit  # (it holds the Checkpoints: their ids stay theirs)
-        arr, tok, dtype, keep, _ = hit
-        pt = pf = None
+                self._round_args[key] = hit
+        arr, tok, dtype, keep, _, recorded = hit
+        pt_p = pf_p = None
+        nhit = None
         if norms is not None:
-            pt, pf = norms
-            for t, n in ((pt, len(self.fragment_tensors(fragment))), (pf, 1)):
-                if t is not None and (t.device != self.device or t.dtype != torch.float64
-                                      or not t.is_contiguous() or t.numel() < n):
-                    raise ValueError("norm outputs must be contiguous fp64 device tensors")
-        s = torch.cuda.current_stream(self.device) if stream is None else stream
-        sh = int(s.cuda_stream)
+            nkey = (id(norms[0]), id(norms[1]), fragment)
+            nhit = self._norm_args.get(nkey)
+            if nhit is None:
+                pt, pf = norms
+                for t, n in ((pt, len(self.fragment_tensors(fragment))), (pf, 1)):
+                    if t is not None and (t.device != self.device or t.dtype != torch.float64
+                                          or not t.is_contiguous() or t.numel() < n):
+                        raise ValueError("norm outputs must be contiguous fp64 device tensors")
+                outs = [t for t in (pt, pf) if t is not None]
+                nhit = (None if pt is None else pt.data_ptr(), None if pf is None else pf.data_ptr(),
+                        outs, set())
+                if len(self._norm_args) >= 64:
+                    self._norm_args.clear()
+                self._norm_args[nkey] = nhit  # (it holds the tensors: their ids stay theirs)
+            pt_p, pf_p = nhit[0], nhit[1]
+        if stream is None:
+            s = torch.cuda.current_stream(self.device)
+            sh = int(s.cuda_stream)
+            capturing = torch.cuda.is_current_stream_capturing()
+        else:
+            s = stream
+            sh = int(s.cuda_stream)
+            capturing = None
         _check(lib().cam_merge_round(
             self.ctx, int(round), int(fragment), len(arr), arr, dtype, tok, int(mode),
             float(lr), float(mu), 0 if ema_beta is None else 1,
-            0.0 if ema_beta is None else float(ema_beta),
-            None if pt is None else pt.data_ptr(), None if pf is None else pf.data_ptr(),
-            sh or None))
-        if stream_capturing(sh):
+            0.0 if ema_beta is None else float(ema_beta), pt_p, pf_p, sh or None))
+        if capturing is None:
+            capturing = stream_capturing(sh)
+        if capturing:
             return  # a captured graph reads its buffers at every replay: they are the caller's
-        outs = [t for t in (pt, pf) if t is not None]
-        _record_streams(keep + outs if outs else keep, s, sh)
+        # record_stream once per tensor and stream covers every later use on it
+        if sh not in recorded:
+            _record_streams(keep, s, sh)
+            recorded.add(sh)
+        if nhit is not None and sh not in nhit[3]:
+            _record_streams(nhit[2], s, sh)
+            nhit[3].add(sh)
         if self._inflight:
             self._hold_until_done([], s)
 

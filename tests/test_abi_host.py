@@ -90,6 +90,8 @@ def test_null_handles_rejected():
     assert lib.cam_ema_update(None, 0.9) == B.E_ARG
     assert lib.cam_drift_norm(None, None, None) == B.E_ARG
     assert lib.cam_merge_commit(None, None) == B.E_ARG
+    assert lib.cam_merge_round(None, 0, 0, 1, None, 0, None, 0, 1.0, 0.0, 0, 0.0, None, None,
+                               None) == B.E_ARG
     assert lib.cam_merge_abort(None) == B.E_ARG
     assert lib.cam_ctx_status(None, None) == B.E_ARG
     assert lib.cam_ctx_staged_count(None, None) == B.E_ARG
