@@ -398,8 +398,23 @@ __device__ __forceinline__ void merge_vec8(const A& a, const void* const* xs,
     if (EMA) load_s8(ts.e + i, e);
     float sw[8];
     if constexpr (SWA) load_s8(ts.swa + i, sw);
-    merge_group<8, MODE, EMA, NORM, SWA, WD>(a, [&](int k, int j) { return x[k].get(j); }, th, m, e,
-                                             sw, acc, accw);
+    if constexpr (EMA && !SWA) {
+        // an EMA without a running average: element by element, each division
+        // with its own range test (measured on GB300: the bf16 Nesterov + EMA
+        // sweeps 1.5-2 % faster than with the eight divisions grouped; the
+        // other variants as fast or faster grouped)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float xk[CAM_KMAX];
+#pragma unroll
+            for (int k = 0; k < CAM_KMAX; ++k) xk[k] = x[k].get(j);
+            if constexpr (WD) worker_drift(a, xk, th[j], accw);
+            merge_elem<MODE, EMA, NORM>(a, xk, th[j], m[j], e[j], acc);
+        }
+    } else {
+        merge_group<8, MODE, EMA, NORM, SWA, WD>(a, [&](int k, int j) { return x[k].get(j); }, th,
+                                                 m, e, sw, acc, accw);
+    }
     store_s8(ts.theta + i, th);
     if constexpr (SWA) store_s8(ts.swa + i, sw);
     if (MODE == kDelta) store_s8(ts.m + i, m);
