@@ -11,7 +11,10 @@ Prints one JSON line: whole-job algorithmic HBM GB/s (value), ms per round,
 the roofline of the fused merge kernel against the measured HBM copy
 bandwidth, SM clocks sampled during the timed region, an end-to-end figure
 through the public API with inputs in pinned host memory, and the CPU oracle
-timed on a bounded sample of the same workload.
+timed on a bounded sample of the same workload. A default run (one GPU, the
+default workload) then measures the other configurations of the metric, each
+in a short child run, and adds their figures to the line (other_configs;
+--no-configs skips them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload diffurefill1b|diffurefill1b_bf16|stand|pythia14m|sweep:T,N,K]
@@ -37,6 +40,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "merge round ms and achieved HBM GB/s (% of GB300 peak) at 1.08B params"
+DEFAULT_WORKLOAD = "diffurefill1b"
 KERNEL_SRCS = [os.path.join(ROOT, "checkpoint_averaging_gb300", "csrc", f)
                for f in ("merge_fused.cuh", "merge_fused_f32.cu", "merge_fused_bf16.cu",
                          "merge_staged.cuh", "merge_staged_f32.cu", "merge_staged_bf16.cu",
@@ -346,6 +350,48 @@ def run_reference(args, wl, ws, rank) -> int:
     return 0
 
 
+# The other configurations of the same metric, run after the headline one:
+# (workload, extra arguments). Each is one short run of this script in a
+# child process, the parent idle meanwhile, so their lines are recorded with
+# the headline's.
+OTHER_CONFIGS = [
+    ("pythia14m", ["--graph", "--steps", "200", "--warmup", "5"]),
+    ("pythia14m", ["--api", "round", "--steps", "100", "--warmup", "5"]),
+    ("stand", ["--steps", "10", "--warmup", "3"]),
+    ("diffurefill1b_bf16", ["--steps", "10", "--warmup", "3"]),
+    ("diffurefill1b_bf16_wnorms", ["--steps", "10", "--warmup", "3"]),
+    ("sweep:64,16000000,4", ["--steps", "10", "--warmup", "3"]),
+    ("sweep:128,256000000,4", ["--steps", "10", "--warmup", "3"]),
+    ("sweep:256,1000000000,4", ["--steps", "10", "--warmup", "3"]),
+]
+
+
+def other_configs(args) -> list:
+    out = []
+    for name, extra in OTHER_CONFIGS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, *extra,
+               "--no-cpu-baseline", "--e2e-steps", "0", "--no-configs"]
+        rec = {"workload": name, "args": " ".join(extra)}
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+            lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+            if r.returncode != 0 or len(lines) != 1:
+                rec["error"] = (r.stderr.strip().splitlines() or ["no output"])[-1][:300]
+            else:
+                d = json.loads(lines[0])
+                rec.update({"name": d["config"]["workload"], "value": d["value"],
+                            "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+                            "frac": d["roofline"]["frac"], "kernel": d["roofline"]["kernel"],
+                            "traffic": d["roofline"]["traffic"],
+                            "gpu_launches": d["gpu_launches"],
+                            "sm_mhz": d["clocks"].get("sm_mhz"),
+                            "clock_reasons": d["clocks"].get("reasons")})
+        except (subprocess.TimeoutExpired, OSError, ValueError, KeyError) as exc:
+            rec["error"] = f"{type(exc).__name__}: {exc}"[:300]
+        out.append(rec)
+    return out
+
+
 def run_ours(args, wl, ws, rank, local) -> int:
     import torch
 
@@ -604,6 +650,10 @@ def run_ours(args, wl, ws, rank, local) -> int:
 
     ck = clocks.summary()
     mg.close()
+    others = None
+    if rank == 0 and ws == 1 and args.op == "merge" and not args.no_configs and \
+            args.workload == DEFAULT_WORKLOAD and not args.graph and args.many is None:
+        others = other_configs(args)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s", "n_gpus": ws,
@@ -634,6 +684,8 @@ def run_ours(args, wl, ws, rank, local) -> int:
             "gpu_launches": launches,
             "cpu_baseline": cpu,
         }
+        if others is not None:
+            line["other_configs"] = others
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -1242,7 +1294,7 @@ def parse(argv=None):
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="diffurefill1b")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--op", choices=("merge", "adopt", "ortho", "fold", "hostcost"), default="merge")
     p.add_argument("--ortho-iterations", type=int, default=30)
     p.add_argument("--ortho-precision", choices=("tf32", "fp32", "bf16"), default="tf32")
@@ -1254,6 +1306,9 @@ def parse(argv=None):
     p.add_argument("--many", type=int, default=None,
                    help="commit the step's rounds in groups of this many by one call "
                         "(cam_merge_commit_many); 0: one commit per round (default: the workload's)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other configurations that a default run measures after the "
+                        "headline one (other_configs in its line)")
     p.add_argument("--api", choices=("steps", "round"), default="steps",
                    help="merge op: each round through begin/accumulate/finalize/.../commit "
                         "(steps) or through one cam_merge_round call (round)")
