@@ -363,6 +363,11 @@ OTHER_CONFIGS = [
     ("sweep:64,16000000,4", ["--steps", "10", "--warmup", "3"]),
     ("sweep:128,256000000,4", ["--steps", "10", "--warmup", "3"]),
     ("sweep:256,1000000000,4", ["--steps", "10", "--warmup", "3"]),
+    (DEFAULT_WORKLOAD, ["--op", "fold", "--fold-last", "--steps", "3", "--warmup", "3"]),
+    (DEFAULT_WORKLOAD, ["--op", "adopt", "--steps", "5", "--warmup", "3"]),
+    (DEFAULT_WORKLOAD, ["--op", "ortho", "--ortho-precision", "bf16", "--steps", "3",
+                        "--warmup", "3"]),
+    (DEFAULT_WORKLOAD, ["--op", "ortho", "--steps", "3", "--warmup", "3"]),
 ]
 
 
@@ -379,14 +384,15 @@ def other_configs(args) -> list:
                 rec["error"] = (r.stderr.strip().splitlines() or ["no output"])[-1][:300]
             else:
                 d = json.loads(lines[0])
-                rec.update({"name": d["config"]["workload"], "value": d["value"],
-                            "unit": d["unit"], "ms_per_step": d["ms_per_step"],
-                            "frac": d["roofline"]["frac"], "kernel": d["roofline"]["kernel"],
-                            "traffic": d["roofline"]["traffic"],
-                            "gpu_launches": d["gpu_launches"],
-                            "sm_mhz": d["clocks"].get("sm_mhz"),
-                            "clock_reasons": d["clocks"].get("reasons")})
-        except (subprocess.TimeoutExpired, OSError, ValueError, KeyError) as exc:
+                roof, clk = d.get("roofline") or {}, d.get("clocks") or {}
+                rec.update({"name": (d.get("config") or {}).get("workload"),
+                            "metric": d.get("metric"), "value": d.get("value"),
+                            "unit": d.get("unit"), "ms_per_step": d.get("ms_per_step"),
+                            "frac": roof.get("frac"), "bound": roof.get("bound"),
+                            "kernel": roof.get("kernel"), "traffic": roof.get("traffic"),
+                            "gpu_launches": d.get("gpu_launches"),
+                            "sm_mhz": clk.get("sm_mhz"), "clock_reasons": clk.get("reasons")})
+        except (subprocess.TimeoutExpired, OSError, ValueError, KeyError, TypeError) as exc:
             rec["error"] = f"{type(exc).__name__}: {exc}"[:300]
         out.append(rec)
     return out
