@@ -220,13 +220,41 @@ int32_t choose_chunk(int64_t n, int sm_count) {
     return static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(c, q), cam::kMaxChunkElems));
 }
 
+// Per-chunk cost of a register-form pass in element-equivalents (the chunk's
+// table reads, its block barrier and drift-partial sum), for chunk_for_blocks.
+constexpr int64_t kChunkCostElems = 1024;
+
+// A fragment below kMaxChunkElems-sized chunks is spread over few waves of
+// the register form's blocks, where the last wave's fill decides the time:
+// among the whole numbers of block-steps, the chunk size with the smallest
+// (waves x (chunk + kChunkCostElems)) for G blocks, tensors chunked one by
+// one. Measured on the Pythia-14M step (6.4M-element fragment, G = 228):
+// 14,336-element chunks (two per block) instead of 6,144 (four or five)
+// took the graphed step from 0.0472 to 0.0448 ms.
+int32_t chunk_for_blocks(const cam_ctx& c, const std::vector<int32_t>& tensors, int32_t chunk) {
+    if (chunk >= cam::kMaxChunkElems) return chunk;
+    const int64_t G = c.share_sms ? (2 * int64_t(c.sm_count) * 3) / 4 : 2 * int64_t(c.sm_count);
+    auto cost = [&](int64_t ch) {
+        int64_t n = 0;
+        for (int32_t g : tensors) n += (c.numel[g] + ch - 1) / ch;
+        return ((n + G - 1) / G) * (ch + kChunkCostElems);
+    };
+    int64_t best = chunk, best_cost = cost(chunk);
+    for (int64_t ch = cam::kChunkQuantum; ch <= cam::kMaxChunkElems; ch += cam::kChunkQuantum)
+        if (const int64_t k = cost(ch); k < best_cost) {
+            best = ch;
+            best_cost = k;
+        }
+    return static_cast<int32_t>(best);
+}
+
 void build_plan(Plan& p, const cam_ctx& c, int32_t fragment) {
     p.tensors.clear();
     for (int32_t t = 0; t < c.n_tensors; ++t)
         if (fragment < 0 || c.fragment_of[t] == fragment) p.tensors.push_back(t);
     p.n_elems = 0;
     for (int32_t g : p.tensors) p.n_elems += c.numel[g];
-    p.chunk_elems = choose_chunk(p.n_elems, c.sm_count);
+    p.chunk_elems = chunk_for_blocks(c, p.tensors, choose_chunk(p.n_elems, c.sm_count));
     p.chunks.clear();
     p.first_chunk.assign(1, 0);
     for (int32_t l = 0; l < p.n_tensors(); ++l) {
@@ -379,6 +407,7 @@ CAM_API int cam_ctx_create(const cam_ctx_desc* d, cam_ctx** out) {
 
     // Plans and one device block holding every plan's tables, after the
     // status word.
+    c->share_sms = (d->flags & CAM_SHARE_SMS) != 0;  // (the plans' chunk sizes depend on it)
     c->plans.resize(c->n_fragments + 1);
     size_t bytes = 256;
     for (int32_t f = 0; f <= c->n_fragments; ++f) {
