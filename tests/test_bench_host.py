@@ -53,3 +53,32 @@ def test_threaded_sample_rate_runs_on_a_small_workload():
                                                   pool_elems=1 << 16, threads=2)
     assert gbs > 0 and secs > 0 and n == 1 << 18
     assert "2 host threads" in desc
+
+
+def test_other_configs_records_each_child_line_or_its_error(monkeypatch):
+    """A default run's other_configs: one record per configuration, with the
+    child's figures, or the child's last error line when it failed."""
+    import json
+    import subprocess
+    import types
+
+    good = {"metric": "m", "value": 123.4, "unit": "GB/s", "ms_per_step": 1.5,
+            "config": {"workload": "w"}, "gpu_launches": 3,
+            "roofline": {"frac": 0.9, "bound": "hbm", "kernel": "k", "traffic": None},
+            "clocks": {"sm_mhz": 2070.0, "reasons": []}}
+    calls = []
+
+    def fake_run(cmd, capture_output, text, timeout):
+        calls.append(cmd)
+        if len(calls) == 2:
+            return types.SimpleNamespace(returncode=1, stdout="", stderr="a\nboom\n")
+        return types.SimpleNamespace(returncode=0, stdout="noise\n" + json.dumps(good) + "\n",
+                                     stderr="")
+
+    monkeypatch.setattr(subprocess, "run", fake_run)
+    out = bench.other_configs(bench.parse([]))
+    assert len(out) == len(bench.OTHER_CONFIGS) == len(calls)
+    assert all("--no-configs" in c and "--no-cpu-baseline" in c for c in calls)
+    assert out[0]["value"] == 123.4 and out[0]["frac"] == 0.9 and out[0]["unit"] == "GB/s"
+    assert out[1]["error"] == "boom" and "value" not in out[1]
+    assert out[0]["workload"] == bench.OTHER_CONFIGS[0][0]
