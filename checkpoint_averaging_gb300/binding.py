@@ -655,6 +655,7 @@ class Merger:
         and accumulate them. The marshalled arguments of Checkpoint lists are
         kept for the next call with the same Checkpoints and tokens."""
         torch = _torch()
+        ckpts = list(ckpts)
         key = None
         if all(isinstance(c, Checkpoint) for c in ckpts):
             key = (fragment, tuple(map(id, ckpts)), None if tokens is None else tuple(tokens))
